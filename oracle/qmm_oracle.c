@@ -1,0 +1,396 @@
+/*
+ * qmm_oracle.c -- plain, slow CPU reference for matrix multiplication against
+ * block-quantized weights (q6_K, Q4_0, Q8_0).
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load or call this file. The CUDA library never does:
+ * the two share no code, header, table or constant. The numbering of formats
+ * and activation kinds below is written out again here on purpose.
+ *
+ * Everything follows the plain definition of each quantity, with no blocking,
+ * fusion or reordering beyond what the definition states:
+ *   - each weight is decoded from its block exactly (the decoded value is an
+ *     exact fp32 number, see orc_weight),
+ *   - dot products accumulate in double precision in increasing k,
+ *   - the activation quantizer takes its rounding decisions in fp32, the
+ *     precision the quantized format itself is defined in (fp32 scale).
+ *
+ * Sources (page title, then section):
+ *   [MINFER]  "57 - r54 MINFER_MMQ_Q6K_EXP: an exit valve for the 1.52 GB
+ *             W_exp plane", section 2.1 (the q6_K element expansion
+ *             v = ((ql>>qsh)&0xF) | (((qh>>qh_shift)&3)<<4) - 32 done per
+ *             16-element group) and section 2.2 (the W_exp plane: one
+ *             centered int8 byte per weight, od x id bytes).
+ *   [LAWS]    quantprobe "LAWS.md", Law 4 amendment L-15 (matvec with dp4a
+ *             on quantized activations).
+ *   [X100]    "Chasing x100", "Where the wall actually fell: inversion"
+ *             (routed experts kept resident and decoded in place; top-k
+ *             routed expert FFN per token).
+ *
+ * Readings where the pages are silent (they print no byte order for the
+ * nibbles): q6_K element i of a 256-weight super-block takes its low four
+ * bits from ql[i mod 128] (low nibble for i < 128, high nibble otherwise),
+ * its high two bits from qh[i mod 64] at bit 2*(i div 64), and its scale from
+ * scales[i div 16]; every 16-element group therefore reads 16 consecutive ql
+ * bytes and 16 consecutive qh bytes with one shift pair, as [MINFER] 2.1
+ * describes the in-kernel expansion.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* formats, numbered as the library's C interface numbers them */
+#define ORC_Q4_0 1
+#define ORC_Q8_0 2
+#define ORC_Q6_K 3
+
+/* activation element kinds */
+#define ORC_X_F32 0
+#define ORC_X_BF16 1
+
+/* ------------------------------------------------------------------ */
+/* scalar decoders                                                     */
+/* ------------------------------------------------------------------ */
+
+/* IEEE 754 binary16 -> double, exact for every finite input (subnormals
+ * included: many q6_K scales d = fp16(|N(0,1)| * 2e-4) are subnormal). */
+double orc_half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24); /* 0.m * 2^-14 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25); /* 1.m * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32 */
+double orc_bf16_to_double(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double load_x(const void* x, int xkind, int64_t i) {
+    if (xkind == ORC_X_BF16)
+        return orc_bf16_to_double(((const uint16_t*)x)[i]);
+    return (double)((const float*)x)[i];
+}
+
+/* ------------------------------------------------------------------ */
+/* block formats                                                       */
+/* ------------------------------------------------------------------ */
+
+int orc_block_elems(int fmt) {
+    switch (fmt) {
+    case ORC_Q4_0: return 32;
+    case ORC_Q8_0: return 32;
+    case ORC_Q6_K: return 256;
+    }
+    return 0;
+}
+
+int orc_block_bytes(int fmt) {
+    switch (fmt) {
+    case ORC_Q4_0: return 2 + 16;              /* d fp16, 16 bytes of nibbles  */
+    case ORC_Q8_0: return 2 + 32;              /* d fp16, 32 int8 values       */
+    case ORC_Q6_K: return 128 + 64 + 16 + 2;   /* ql, qh, scales, d = 210 B    */
+    }
+    return 0;
+}
+
+/* size of the integer group that carries one weight-side scale factor */
+int orc_group_elems(int fmt) { return fmt == ORC_Q6_K ? 16 : 32; }
+
+/* q6_K: the unsigned 6-bit code of element i (0..255) of a super-block,
+ * [MINFER] 2.1: low four bits from ql, high two bits from qh. */
+int orc_q6k_code(const uint8_t* blk, int i) {
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    int lo = (ql[i % 128] >> (4 * (i / 128))) & 0xF;
+    int hi = (qh[i % 64] >> (2 * (i / 64))) & 0x3;
+    return lo | (hi << 4);
+}
+
+/* integer value of element i before the weight-side scale: q6_K gives
+ * sc[i/16] * (q - 32), Q4_0 gives q - 8, Q8_0 gives q. */
+static int int_value(int fmt, const uint8_t* blk, int i) {
+    if (fmt == ORC_Q6_K) {
+        int sc = (int8_t)blk[192 + i / 16];
+        return sc * (orc_q6k_code(blk, i) - 32);
+    }
+    if (fmt == ORC_Q4_0) {
+        const uint8_t* qs = blk + 2;
+        int q = (qs[i % 16] >> (4 * (i / 16))) & 0xF;
+        return q - 8;
+    }
+    /* Q8_0 */
+    return (int8_t)blk[2 + i];
+}
+
+/* the centered code without the sub-block scale (what the integer dot
+ * products multiply): q6_K q-32, Q4_0 q-8, Q8_0 q */
+int orc_centered_code(int fmt, const uint8_t* blk, int i) {
+    if (fmt == ORC_Q6_K) return orc_q6k_code(blk, i) - 32;
+    return int_value(fmt, blk, i);
+}
+
+/* the per-block fp16 scale d */
+double orc_block_d(int fmt, const uint8_t* blk) {
+    int off = (fmt == ORC_Q6_K) ? 208 : 0;
+    uint16_t h = (uint16_t)(blk[off] | (blk[off + 1] << 8));
+    return orc_half_to_double(h);
+}
+
+/* the sub-block scale that multiplies group g: q6_K scales[g], else 1 */
+int orc_group_scale(int fmt, const uint8_t* blk, int g) {
+    if (fmt == ORC_Q6_K) return (int8_t)blk[192 + g];
+    return 1;
+}
+
+/* Dequantized weight k of a row: d * (integer value). d has an 11-bit
+ * significand and |integer value| <= 1024 needs at most 11 bits, so the
+ * product is exact in fp32 as well as in double. */
+double orc_weight(int fmt, const uint8_t* row, int64_t k) {
+    int be = orc_block_elems(fmt);
+    const uint8_t* blk = row + (k / be) * orc_block_bytes(fmt);
+    return orc_block_d(fmt, blk) * (double)int_value(fmt, blk, (int)(k % be));
+}
+
+/* dequantize a whole row of K weights */
+void orc_dequant_row(int fmt, const uint8_t* row, int64_t K, double* out) {
+    for (int64_t k = 0; k < K; ++k) out[k] = orc_weight(fmt, row, k);
+}
+
+static const uint8_t* row_ptr(int fmt, const uint8_t* W, int64_t K, int64_t n) {
+    return W + n * (K / orc_block_elems(fmt)) * orc_block_bytes(fmt);
+}
+
+/* ------------------------------------------------------------------ */
+/* float-activation matvec: y[b][n] = sum_k w[n][k] * x[b][k]          */
+/* ------------------------------------------------------------------ */
+
+/* one dot product in double; *absum receives sum_k |w*x| (the scale the
+ * float tolerance is stated against) */
+double orc_dot_float(int fmt, const uint8_t* row, int64_t K, const void* x,
+                     int xkind, int64_t xoff, double* absum) {
+    double s = 0.0, a = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double p = orc_weight(fmt, row, k) * load_x(x, xkind, xoff + k);
+        s += p;
+        a += fabs(p);
+    }
+    if (absum) *absum = a;
+    return s;
+}
+
+void orc_gemv_float(int fmt, const uint8_t* W, int64_t N, int64_t K,
+                    const void* x, int xkind, int B, double* y, double* absum) {
+    for (int b = 0; b < B; ++b)
+        for (int64_t n = 0; n < N; ++n)
+            y[b * N + n] = orc_dot_float(fmt, row_ptr(fmt, W, K, n), K, x, xkind,
+                                         (int64_t)b * K, absum ? &absum[b * N + n] : NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* activation quantizer: per 32-element block, s = amax/127 (fp32),     */
+/* x_q = round-half-even(x / s) clamped to [-127, 127]; amax == 0 gives */
+/* s = 0 and x_q = 0. Decisions taken in fp32.                          */
+/* ------------------------------------------------------------------ */
+
+void orc_quantize_q8(const void* x, int xkind, int64_t rows, int64_t K,
+                     int8_t* xq, float* s) {
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b0 = 0; b0 < K; b0 += 32) {
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float v = (float)load_x(x, xkind, r * K + b0 + i);
+                float av = fabsf(v);
+                if (av > amax) amax = av;
+            }
+            float sc = amax / 127.0f;
+            s[r * (K / 32) + b0 / 32] = sc;
+            for (int i = 0; i < 32; ++i) {
+                int q = 0;
+                if (amax != 0.0f) {
+                    float v = (float)load_x(x, xkind, r * K + b0 + i);
+                    float t = v / sc;
+                    float rq = nearbyintf(t); /* default mode: to nearest, ties to even */
+                    if (rq > 127.0f) rq = 127.0f;
+                    if (rq < -127.0f) rq = -127.0f;
+                    q = (int)rq;
+                }
+                xq[r * K + b0 + i] = (int8_t)q;
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* quantized-activation matvec ([LAWS] L-15: integer dot products)      */
+/* I_g = sum_{k in g} x_q[k] * c[k]   (c the centered code, exact int)  */
+/* y   = sum_g s_x[block(g)] * d * sc_g * I_g                            */
+/* ------------------------------------------------------------------ */
+
+/* integer partial of group g (global group index along the row) */
+int64_t orc_group_int(int fmt, const uint8_t* row, const int8_t* xq, int64_t g) {
+    int be = orc_block_elems(fmt), ge = orc_group_elems(fmt);
+    int64_t k0 = g * ge;
+    const uint8_t* blk = row + (k0 / be) * orc_block_bytes(fmt);
+    int64_t acc = 0;
+    for (int i = 0; i < ge; ++i) {
+        int e = (int)((k0 + i) % be);
+        acc += (int64_t)xq[k0 + i] * orc_centered_code(fmt, blk, e);
+    }
+    return acc;
+}
+
+double orc_dot_q8(int fmt, const uint8_t* row, int64_t K, const int8_t* xq,
+                  const float* s, double* absum) {
+    int be = orc_block_elems(fmt), ge = orc_group_elems(fmt);
+    double y = 0.0, a = 0.0;
+    for (int64_t g = 0; g < K / ge; ++g) {
+        int64_t k0 = g * ge;
+        const uint8_t* blk = row + (k0 / be) * orc_block_bytes(fmt);
+        double d = orc_block_d(fmt, blk);
+        int sc = orc_group_scale(fmt, blk, (int)((k0 % be) / ge));
+        double sx = (double)s[k0 / 32];
+        int64_t I = orc_group_int(fmt, row, xq, g);
+        y += sx * d * (double)sc * (double)I;
+        if (absum)
+            for (int i = 0; i < ge; ++i)
+                a += fabs(orc_weight(fmt, row, k0 + i) * sx * (double)xq[k0 + i]);
+    }
+    if (absum) *absum = a;
+    return y;
+}
+
+void orc_gemv_q8(int fmt, const uint8_t* W, int64_t N, int64_t K, const int8_t* xq,
+                 const float* s, int B, double* y, double* absum) {
+    for (int b = 0; b < B; ++b)
+        for (int64_t n = 0; n < N; ++n)
+            y[b * N + n] = orc_dot_q8(fmt, row_ptr(fmt, W, K, n), K, xq + (int64_t)b * K,
+                                      s + (int64_t)b * (K / 32),
+                                      absum ? &absum[b * N + n] : NULL);
+}
+
+/* Prefill GEMM, Y[m][n] = quantized-activation dot of X[m] with W[n], for a
+ * list of (m, n) pairs (so that full-size matrices can be spot-checked).
+ * xq/s are the quantized activations of all M rows. */
+void orc_gemm_q8_pairs(int fmt, const uint8_t* W, int64_t K, const int8_t* xq,
+                       const float* s, const int64_t* ms, const int64_t* ns,
+                       int64_t count, double* y, double* absum) {
+    for (int64_t i = 0; i < count; ++i)
+        y[i] = orc_dot_q8(fmt, row_ptr(fmt, W, K, ns[i]), K, xq + ms[i] * K,
+                          s + ms[i] * (K / 32), absum ? &absum[i] : NULL);
+}
+
+/* float-mode matvec for a list of (b, n) pairs */
+void orc_gemv_float_pairs(int fmt, const uint8_t* W, int64_t K, const void* x,
+                          int xkind, const int64_t* bs, const int64_t* ns,
+                          int64_t count, double* y, double* absum) {
+    for (int64_t i = 0; i < count; ++i)
+        y[i] = orc_dot_float(fmt, row_ptr(fmt, W, K, ns[i]), K, x, xkind, bs[i] * K,
+                             absum ? &absum[i] : NULL);
+}
+
+/* ------------------------------------------------------------------ */
+/* W_exp plane ([MINFER] 2.2): one centered int8 per weight, row-major  */
+/* N x K, plane[n][k] = q(n,k) - 32                                      */
+/* ------------------------------------------------------------------ */
+
+void orc_plane_q6k(const uint8_t* W, int64_t N, int64_t K, int8_t* plane) {
+    for (int64_t n = 0; n < N; ++n) {
+        const uint8_t* row = row_ptr(ORC_Q6_K, W, K, n);
+        for (int64_t k = 0; k < K; ++k)
+            plane[n * K + k] =
+                (int8_t)(orc_q6k_code(row + (k / 256) * 210, (int)(k % 256)) - 32);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* routed MoE ([X100] inversion section; top-k with softmax gates)      */
+/* ------------------------------------------------------------------ */
+
+/* top-k by logit value, ties to the lower expert index, then a softmax over
+ * the k selected logits (renormalized over the selection), in double. */
+void orc_route_topk_softmax(const float* logits, int T, int E, int k,
+                            int32_t* idx, double* gate) {
+    char* taken = (char*)malloc((size_t)E);
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (int64_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!taken[e] && (best < 0 || l[e] > l[best])) best = e;
+            taken[best] = 1;
+            idx[t * k + j] = best;
+        }
+        double mx = (double)l[idx[t * k]];
+        double z = 0.0;
+        for (int j = 0; j < k; ++j) z += exp((double)l[idx[t * k + j]] - mx);
+        for (int j = 0; j < k; ++j) gate[t * k + j] = exp((double)l[idx[t * k + j]] - mx) / z;
+    }
+    free(taken);
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Routed expert FFN for T tokens, float activations:
+ *   g = Wg_e x_t, u = Wu_e x_t, h = silu(g) * u, o = Wd_e h,
+ *   y_t = sum_j gate[t][j] * o_{idx[t][j]}.
+ * wg/wu hold I x H matrices, wd holds H x I matrices, one pointer per expert.
+ * bound (optional, [T][H]) receives the float tolerance the GPU result is
+ * held to: the per-matvec bound 1e-4 * sum|w x| + 1e-6 carried through
+ * silu (|silu'| <= 1.1) and the down projection. h_out (optional,
+ * [T][k][I]) receives h. */
+void orc_moe_float(int fmt, int H, int I, const uint8_t* const* wg,
+                   const uint8_t* const* wu, const uint8_t* const* wd, int T, int k,
+                   const int32_t* idx, const double* gate, const void* x, int xkind,
+                   double* y, double* bound, double* h_out) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    double* dh = (double*)malloc(sizeof(double) * (size_t)I);
+    for (int t = 0; t < T; ++t) {
+        for (int n = 0; n < H; ++n) {
+            y[(int64_t)t * H + n] = 0.0;
+            if (bound) bound[(int64_t)t * H + n] = 1e-6;
+        }
+        for (int j = 0; j < k; ++j) {
+            int e = idx[t * k + j];
+            double gw = gate[t * k + j];
+            for (int i = 0; i < I; ++i) {
+                double ag, au;
+                double g = orc_dot_float(fmt, row_ptr(fmt, wg[e], H, i), H, x, xkind,
+                                         (int64_t)t * H, &ag);
+                double u = orc_dot_float(fmt, row_ptr(fmt, wu[e], H, i), H, x, xkind,
+                                         (int64_t)t * H, &au);
+                double sg = silu(g);
+                h[i] = sg * u;
+                double eg = 1e-4 * ag + 1e-6, eu = 1e-4 * au + 1e-6;
+                dh[i] = fabs(u) * 1.1 * eg + (fabs(sg) + 1.1 * eg) * eu + 1e-6 * fabs(h[i]);
+                if (h_out) h_out[((int64_t)t * k + j) * I + i] = h[i];
+            }
+            for (int n = 0; n < H; ++n) {
+                const uint8_t* row = row_ptr(fmt, wd[e], I, n);
+                double o = 0.0, a = 0.0, p = 0.0;
+                for (int i = 0; i < I; ++i) {
+                    double w = orc_weight(fmt, row, i);
+                    o += w * h[i];
+                    a += fabs(w * h[i]);
+                    p += fabs(w) * dh[i];
+                }
+                y[(int64_t)t * H + n] += gw * o;
+                if (bound) bound[(int64_t)t * H + n] += gw * (1e-4 * a + p);
+            }
+        }
+    }
+    free(h);
+    free(dh);
+}

@@ -1,0 +1,157 @@
+"""Seeded synthetic inputs for block-quantized weight matmul.
+
+This module only draws random numbers and places them in the byte fields of
+the block formats; it holds none of the matmul arithmetic (no decoding, no
+dot products, no quantization). Both the CUDA tests/bench and the CPU oracle
+consume what it produces.
+
+Generator: splitmix64 on a counter (z = seed + (i+1) * 0x9E3779B97F4A7C15,
+then the published splitmix64 finalizer), one independent stream per tensor
+and field. Normals: Box-Muller in float64 from two uniforms of 53 bits.
+
+Value distributions (per block of each format):
+  q6_K (210 B): ql[128] and qh[64] uniform random bytes, so every 6-bit code
+      q is uniform on 0..63; scales[16] uniform on -32..31; d =
+      fp16(|N(0,1)| * 2e-4) little-endian.
+  Q4_0 (18 B):  d as above, then 16 uniform bytes (every nibble q uniform on
+      0..15).
+  Q8_0 (34 B):  d as above, then 32 int8 uniform on -127..127.
+  activations:  N(0,1) as float32, or rounded to bfloat16 (ties to even).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+Q4_0, Q8_0, Q6_K = 1, 2, 3
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210}
+
+_CHUNK = 1 << 22  # draws per numpy pass (bounded temporaries)
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def substream(seed: int, tag: int) -> int:
+    """A seed for an independent stream, derived from (seed, tag)."""
+    with np.errstate(over="ignore"):
+        z = _mix(np.array([np.uint64(seed & 0xFFFFFFFFFFFFFFFF) ^ np.uint64(tag * 0x100000001B3)],
+                          dtype=np.uint64))
+    return int(z[0])
+
+
+def splitmix64(seed: int, n: int) -> np.ndarray:
+    """n uint64 draws of the counter-based splitmix64 stream `seed`."""
+    out = np.empty(n, np.uint64)
+    s = np.uint64(seed & 0xFFFFFFFFFFFFFFFF)
+    with np.errstate(over="ignore"):
+        for i0 in range(0, n, _CHUNK):
+            i = np.arange(i0 + 1, min(n, i0 + _CHUNK) + 1, dtype=np.uint64)
+            out[i0:i0 + len(i)] = _mix(s + i * _GOLDEN)
+    return out
+
+
+def uniform_bytes(seed: int, nbytes: int) -> np.ndarray:
+    words = splitmix64(seed, (nbytes + 7) // 8)
+    return words.view(np.uint8)[:nbytes].copy()
+
+
+def uniform_ints(seed: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """n integers uniform on [lo, hi] (multiply-shift range reduction)."""
+    u = splitmix64(seed, n) >> np.uint64(32)
+    span = np.uint64(hi - lo + 1)
+    with np.errstate(over="ignore"):
+        v = (u * span) >> np.uint64(32)
+    return v.astype(np.int64) + lo
+
+
+def normals(seed: int, n: int) -> np.ndarray:
+    """n standard normals (float64), Box-Muller."""
+    m = (n + 1) // 2
+    u = splitmix64(seed, 2 * m)
+    u1 = ((u[0::2] >> np.uint64(11)).astype(np.float64) + 0.5) * 2.0 ** -53
+    u2 = ((u[1::2] >> np.uint64(11)).astype(np.float64) + 0.5) * 2.0 ** -53
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(2 * m, np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return z[:n]
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    b = (b + np.uint64(0x7FFF) + ((b >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return b.astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _scale_d(seed: int, nblocks: int) -> np.ndarray:
+    """d = fp16(|N(0,1)| * 2e-4) as little-endian byte pairs [nblocks][2]."""
+    d = (np.abs(normals(seed, nblocks)) * 2e-4).astype(np.float16)
+    return d.view(np.uint8).reshape(nblocks, 2)
+
+
+def q6k_matrix(seed: int, N: int, K: int) -> np.ndarray:
+    """N x K q6_K weights, rows of K/256 consecutive 210-byte super-blocks."""
+    assert K % 256 == 0
+    nb = N * (K // 256)
+    out = np.empty((nb, 210), np.uint8)
+    out[:, 0:192] = uniform_bytes(substream(seed, 1), nb * 192).reshape(nb, 192)
+    out[:, 192:208] = uniform_ints(substream(seed, 2), nb * 16, -32, 31).astype(
+        np.int8).view(np.uint8).reshape(nb, 16)
+    out[:, 208:210] = _scale_d(substream(seed, 3), nb)
+    return out.reshape(-1)
+
+
+def q4_0_matrix(seed: int, N: int, K: int) -> np.ndarray:
+    """N x K Q4_0 weights, rows of K/32 consecutive 18-byte blocks."""
+    assert K % 32 == 0
+    nb = N * (K // 32)
+    out = np.empty((nb, 18), np.uint8)
+    out[:, 0:2] = _scale_d(substream(seed, 3), nb)
+    out[:, 2:18] = uniform_bytes(substream(seed, 1), nb * 16).reshape(nb, 16)
+    return out.reshape(-1)
+
+
+def q8_0_matrix(seed: int, N: int, K: int) -> np.ndarray:
+    """N x K Q8_0 weights, rows of K/32 consecutive 34-byte blocks."""
+    assert K % 32 == 0
+    nb = N * (K // 32)
+    out = np.empty((nb, 34), np.uint8)
+    out[:, 0:2] = _scale_d(substream(seed, 3), nb)
+    out[:, 2:34] = uniform_ints(substream(seed, 1), nb * 32, -127, 127).astype(
+        np.int8).view(np.uint8).reshape(nb, 32)
+    return out.reshape(-1)
+
+
+def matrix(fmt: int, seed: int, N: int, K: int) -> np.ndarray:
+    return {Q4_0: q4_0_matrix, Q8_0: q8_0_matrix, Q6_K: q6k_matrix}[fmt](seed, N, K)
+
+
+def matrix_bytes(fmt: int, N: int, K: int) -> int:
+    return N * (K // BLOCK_ELEMS[fmt]) * BLOCK_BYTES[fmt]
+
+
+def normal_f32(seed: int, shape) -> np.ndarray:
+    n = int(np.prod(shape))
+    return normals(substream(seed, 7), n).astype(np.float32).reshape(shape)
+
+
+def normal_bf16(seed: int, shape) -> np.ndarray:
+    """N(0,1) activations as bfloat16 bit patterns (uint16)."""
+    return to_bf16_bits(normal_f32(seed, shape)).reshape(shape)
+
+
+def workload_seed(config_id: int, matrix_id: int) -> int:
+    return 0x5EED0000 + config_id * 16 + matrix_id

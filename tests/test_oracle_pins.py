@@ -1,0 +1,392 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle against something independent: hand-built blocks
+with hand-derived values (tests/golden), closed forms over every code and
+scale, textbook facts (IEEE binary16/bfloat16 via numpy), library routines
+(numpy matmul / integer matmul, stable argsort, scipy softmax), identity and
+one-hot matrices, and brute force on small inputs.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import pack
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_fixture(name):
+    hexs, rows = None, []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("hex "):
+                hexs = bytes.fromhex(line[4:])
+            else:
+                rows.append(line.split())
+    return np.frombuffer(hexs, np.uint8).copy(), rows
+
+
+# --------------------------------------------------------------- scalars
+
+def test_fp16_decode_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    # textbook values: 1.0, smallest subnormal, largest normal
+    assert oracle.half_to_double(0x3C00) == 1.0
+    assert oracle.half_to_double(0x0001) == 2.0 ** -24
+    assert oracle.half_to_double(0x7BFF) == 65504.0
+
+
+def test_bf16_decode():
+    rng = np.random.default_rng(1)
+    bits = rng.integers(0, 65536, 4000).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert oracle.bf16_to_double(0x3F80) == 1.0
+
+
+# --------------------------------------------------------------- block layouts
+
+def test_q6k_hand_block():
+    blk, rows = _read_fixture("q6k_block_hand.txt")
+    assert blk.size == 210
+    codes = oracle.q6k_codes(blk)
+    w = oracle.dequant(oracle.Q6_K, blk, 1, 256)[0]
+    for i, q, sc, wt in rows:
+        i = int(i)
+        assert codes[i] == int(q), i
+        assert w[i] == float(wt), i
+    # same bytes with d = smallest fp16 subnormal: every weight scales by 2^-24
+    blk2 = blk.copy()
+    blk2[208], blk2[209] = 0x01, 0x00
+    w2 = oracle.dequant(oracle.Q6_K, blk2, 1, 256)[0]
+    assert np.array_equal(w2, w * 2.0 ** -24)
+
+
+def test_q4_0_hand_block():
+    blk, rows = _read_fixture("q4_0_block_hand.txt")
+    w = oracle.dequant(oracle.Q4_0, blk, 1, 32)[0]
+    for i, q, wt in rows:
+        assert w[int(i)] == float(wt)
+
+
+def test_q8_0_hand_block():
+    blk, rows = _read_fixture("q8_0_block_hand.txt")
+    w = oracle.dequant(oracle.Q8_0, blk, 1, 32)[0]
+    for i, q, wt in rows:
+        assert w[int(i)] == float(wt)
+
+
+@pytest.mark.parametrize("d", [1.0, 3.0517578125e-05, 1.7881393432617188e-07, -0.000244140625])
+def test_q6k_closed_form_all_codes_and_scales(d):
+    """w = d * sc * (q - 32) for all 64 codes x 64 scales (normal, subnormal d)."""
+    d_bits = pack.f16_bits(d)
+    dval = float(np.array([d_bits], np.uint16).view(np.float16)[0])
+    codes = np.arange(256) % 64
+    for sc in range(-32, 32):
+        blk = pack.pack_q6k_block(codes, np.full(16, sc), d_bits)
+        w = oracle.dequant(oracle.Q6_K, blk, 1, 256)[0]
+        ref = dval * sc * (codes - 32).astype(np.float64)
+        assert np.array_equal(w, ref)
+        assert np.array_equal(w.astype(np.float32).astype(np.float64), w)  # exact in fp32
+
+
+def test_q6k_codes_permuted():
+    """every element position decodes its own code (no index mix-up)"""
+    rng = np.random.default_rng(7)
+    for _ in range(8):
+        codes = rng.integers(0, 64, 256)
+        scales = rng.integers(-32, 32, 16)
+        blk = pack.pack_q6k_block(codes, scales, pack.f16_bits(1.0))
+        assert np.array_equal(oracle.q6k_codes(blk), codes)
+        w = oracle.dequant(oracle.Q6_K, blk, 1, 256)[0]
+        assert np.array_equal(w, scales[np.arange(256) // 16] * (codes - 32.0))
+
+
+def test_q4_0_and_q8_0_closed_form():
+    for d in [0.5, 6.103515625e-05, 5.960464477539063e-08]:
+        db = pack.f16_bits(d)
+        dv = float(np.array([db], np.uint16).view(np.float16)[0])
+        codes = np.arange(32) % 16
+        w = oracle.dequant(oracle.Q4_0, pack.pack_q4_0_block(codes, db), 1, 32)[0]
+        assert np.array_equal(w, dv * (codes - 8.0))
+        vals = np.concatenate([np.arange(-127, -111), np.arange(112, 128)])
+        w = oracle.dequant(oracle.Q8_0, pack.pack_q8_0_block(vals, db), 1, 32)[0]
+        assert np.array_equal(w, dv * vals)
+
+
+def test_synth_fields_land_where_the_layout_says():
+    """generator draws: q6_K codes cover 0..63, scales -32..31, d >= 0 fp16"""
+    W = synth.q6k_matrix(5, 64, 512)
+    blocks = W.reshape(-1, 210)
+    sc = blocks[:, 192:208].view(np.int8)
+    assert sc.min() == -32 and sc.max() == 31
+    d = blocks[:, 208:210].copy().view(np.float16).astype(np.float64)
+    assert (d >= 0).all() and d.max() < 2e-3
+    codes = np.concatenate([oracle.q6k_codes(b) for b in blocks[:16]])
+    assert codes.min() == 0 and codes.max() == 63
+
+
+# --------------------------------------------------------------- float matvec
+
+def _identity_q6k(n):
+    codes = np.full((n, n), 32)
+    np.fill_diagonal(codes, 33)
+    return pack.pack_q6k_matrix(codes, np.ones((n, n // 16), int),
+                                np.full((n, n // 256), pack.f16_bits(1.0)))
+
+
+def test_gemv_identity_returns_x_bitwise():
+    n = 256
+    W = _identity_q6k(n)
+    x = synth.normal_f32(3, (2, n))
+    y, _ = oracle.gemv_float(oracle.Q6_K, W, x, n, n)
+    assert np.array_equal(y, x.astype(np.float64))
+    xb = synth.normal_bf16(4, (1, n))
+    y, _ = oracle.gemv_float(oracle.Q6_K, W, xb, n, n)
+    assert np.array_equal(y[0], synth.bf16_bits_to_f32(xb[0]).astype(np.float64))
+
+
+def test_gemv_one_hot_rows():
+    N, K = 4, 512
+    rng = np.random.default_rng(3)
+    codes = np.full((N, K), 32)
+    ks = rng.integers(0, K, N)
+    qs = rng.integers(0, 64, N)
+    for n in range(N):
+        codes[n, ks[n]] = qs[n]
+    scales = rng.integers(-32, 32, (N, K // 16))
+    d = np.full((N, K // 256), pack.f16_bits(0.0078125))
+    W = pack.pack_q6k_matrix(codes, scales, d)
+    x = synth.normal_f32(9, (1, K))
+    y, _ = oracle.gemv_float(oracle.Q6_K, W, x, N, K)
+    for n in range(N):
+        w = 0.0078125 * scales[n, ks[n] // 16] * (qs[n] - 32)
+        assert y[0, n] == w * float(x[0, ks[n]])
+
+
+@pytest.mark.parametrize("fmt", [oracle.Q6_K, oracle.Q4_0, oracle.Q8_0])
+def test_gemv_brute_force_4x256(fmt):
+    """blocked oracle vs numpy matmul of the dense matrix built from logical values"""
+    N, K = 4, 256
+    rng = np.random.default_rng(fmt)
+    if fmt == oracle.Q6_K:
+        codes = rng.integers(0, 64, (N, K))
+        scales = rng.integers(-32, 32, (N, K // 16))
+        dv = np.abs(rng.normal(size=(N, K // 256))) * 2e-4
+        db = dv.astype(np.float16).view(np.uint16)
+        W = pack.pack_q6k_matrix(codes, scales, db)
+        dense = (db.view(np.float16).astype(np.float64).repeat(256, 1)
+                 * scales.repeat(16, 1) * (codes - 32))
+    elif fmt == oracle.Q4_0:
+        codes = rng.integers(0, 16, (N, K))
+        db = (np.abs(rng.normal(size=(N, K // 32))) * 2e-4).astype(np.float16).view(np.uint16)
+        W = pack.pack_q4_0_matrix(codes, db)
+        dense = db.view(np.float16).astype(np.float64).repeat(32, 1) * (codes - 8)
+    else:
+        vals = rng.integers(-127, 128, (N, K))
+        db = (np.abs(rng.normal(size=(N, K // 32))) * 2e-4).astype(np.float16).view(np.uint16)
+        W = pack.pack_q8_0_matrix(vals, db)
+        dense = db.view(np.float16).astype(np.float64).repeat(32, 1) * vals
+    assert np.array_equal(oracle.dequant(fmt, W, N, K), dense)
+    x = rng.normal(size=(3, K)).astype(np.float32)
+    y, a = oracle.gemv_float(fmt, W, x, N, K)
+    ref = x.astype(np.float64) @ dense.T
+    assert np.allclose(y, ref, rtol=1e-13, atol=1e-18)
+    assert np.allclose(a, np.abs(x.astype(np.float64)) @ np.abs(dense).T, rtol=1e-13)
+    # integer-valued activations: every partial sum is exact, so equality is exact
+    xi = rng.integers(-8, 9, (2, K)).astype(np.float32)
+    yi, _ = oracle.gemv_float(fmt, W, xi, N, K)
+    assert np.array_equal(yi, xi.astype(np.float64) @ dense.T)
+
+
+# --------------------------------------------------------------- q8 quantizer
+
+def test_quantizer_hand_vectors():
+    with open(os.path.join(GOLDEN, "q8_quantizer_hand.txt")) as f:
+        lines = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    xs = [np.array(l[1:], np.float32) for l in lines if l[0] == "x"]
+    qs = [np.array(l[1:], np.int64) for l in lines if l[0] == "q"]
+    x = np.concatenate(xs)[None, :]
+    xq, s = oracle.quantize_q8(x)
+    assert np.array_equal(xq[0], np.concatenate(qs))
+    assert s[0, 0] == np.float32(1.0)
+    assert s[0, 1] == np.float32(0.0)
+    assert s[0, 2] == np.float32(3.0) / np.float32(127.0)
+
+
+def test_quantizer_amax_maps_to_127_and_range():
+    x = synth.normal_f32(11, (8, 1024))
+    xq, s = oracle.quantize_q8(x)
+    blocks = x.reshape(8, 32, 32)
+    qb = xq.reshape(8, 32, 32).astype(np.int64)
+    amax_pos = np.abs(blocks).argmax(axis=2)
+    got = np.take_along_axis(qb, amax_pos[..., None], 2)[..., 0]
+    sign = np.sign(np.take_along_axis(blocks, amax_pos[..., None], 2)[..., 0])
+    assert np.array_equal(got, (127 * sign).astype(np.int64))
+    assert xq.min() >= -127
+    # reconstruction error within half a quantization step
+    rec = qb * s.reshape(8, 32, 1).astype(np.float64)
+    assert (np.abs(rec - blocks) <= 0.5 * s.reshape(8, 32, 1) * (1 + 1e-6)).all()
+
+
+def test_quantizer_bf16_equals_f32_of_same_values():
+    xb = synth.normal_bf16(12, (4, 256))
+    xf = synth.bf16_bits_to_f32(xb).reshape(4, 256)
+    a = oracle.quantize_q8(xb)
+    b = oracle.quantize_q8(xf)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# --------------------------------------------------------------- integer matvec
+
+@pytest.mark.parametrize("fmt", [oracle.Q6_K, oracle.Q4_0, oracle.Q8_0])
+def test_q8_gemv_unit_scale_is_exact_integer(fmt):
+    """d = 1, sub-block scales 1 and activation scale 1 (x integer, amax 127):
+    the quantized path reduces to an integer matmul, exactly."""
+    N, K = 5, 512
+    rng = np.random.default_rng(20 + fmt)
+    one = pack.f16_bits(1.0)
+    if fmt == oracle.Q6_K:
+        codes = rng.integers(0, 64, (N, K))
+        W = pack.pack_q6k_matrix(codes, np.ones((N, K // 16), int), np.full((N, K // 256), one))
+        wint = codes - 32
+    elif fmt == oracle.Q4_0:
+        codes = rng.integers(0, 16, (N, K))
+        W = pack.pack_q4_0_matrix(codes, np.full((N, K // 32), one))
+        wint = codes - 8
+    else:
+        wint = rng.integers(-127, 128, (N, K))
+        W = pack.pack_q8_0_matrix(wint, np.full((N, K // 32), one))
+    x = rng.integers(-127, 128, (3, K))
+    x[:, ::32] = 127  # every 32-block has amax 127 -> s = 1
+    xq, s = oracle.quantize_q8(x.astype(np.float32))
+    assert np.array_equal(xq, x) and (s == 1.0).all()
+    y, _ = oracle.gemv_q8(fmt, W, xq, s, N, K)
+    assert np.array_equal(y, (x @ wint.T).astype(np.float64))
+
+
+def test_q6k_group_int_brute_force():
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 64, (1, 512))
+    W = pack.pack_q6k_matrix(codes, rng.integers(-32, 32, (1, 32)),
+                             np.full((1, 2), pack.f16_bits(1.0)))
+    xq = rng.integers(-127, 128, 512).astype(np.int8)
+    for g in range(32):
+        ref = int(np.dot(xq[16 * g:16 * g + 16].astype(np.int64), codes[0, 16 * g:16 * g + 16] - 32))
+        assert oracle.group_int(oracle.Q6_K, W, xq, g) == ref
+
+
+@pytest.mark.parametrize("fmt", [oracle.Q6_K, oracle.Q4_0, oracle.Q8_0])
+def test_q8_gemv_equals_float_definition_on_dequantized_x(fmt):
+    """y_q8 = W_dense @ (s * x_q): the integer path is a regrouping of the
+    float definition applied to the quantized activations"""
+    N, K = 6, 512
+    W = synth.matrix(fmt, 31, N, K)
+    x = synth.normal_f32(32, (2, K))
+    xq, s = oracle.quantize_q8(x)
+    y, a = oracle.gemv_q8(fmt, W, xq, s, N, K)
+    xhat = xq.astype(np.float64) * np.repeat(s.astype(np.float64), 32, axis=1)
+    dense = oracle.dequant(fmt, W, N, K)
+    ref = xhat @ dense.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-20)
+    assert np.allclose(a, np.abs(xhat) @ np.abs(dense).T, rtol=1e-12)
+
+
+def test_gemm_pairs_match_gemv_rows():
+    N, K, M = 16, 512, 4
+    W = synth.q6k_matrix(40, N, K)
+    X = synth.normal_bf16(41, (M, K))
+    xq, s = oracle.quantize_q8(X)
+    y, _ = oracle.gemv_q8(oracle.Q6_K, W, xq, s, N, K)
+    ms, ns = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    yp, _ = oracle.gemm_q8_pairs(oracle.Q6_K, W, K, xq, s, ms.ravel(), ns.ravel())
+    assert np.array_equal(yp.reshape(M, N), y)
+
+
+def test_gemv_float_pairs_match_full():
+    N, K = 8, 512
+    W = synth.q4_0_matrix(42, N, K)
+    x = synth.normal_f32(43, (3, K))
+    y, a = oracle.gemv_float(oracle.Q4_0, W, x, N, K)
+    bs, ns = np.meshgrid(np.arange(3), np.arange(N), indexing="ij")
+    yp, ap = oracle.gemv_float_pairs(oracle.Q4_0, W, K, x, bs.ravel(), ns.ravel())
+    assert np.array_equal(yp.reshape(3, N), y) and np.array_equal(ap.reshape(3, N), a)
+
+
+# --------------------------------------------------------------- plane
+
+def test_plane_is_centered_codes():
+    rng = np.random.default_rng(8)
+    N, K = 3, 768
+    codes = rng.integers(0, 64, (N, K))
+    W = pack.pack_q6k_matrix(codes, rng.integers(-32, 32, (N, K // 16)),
+                             np.full((N, K // 256), pack.f16_bits(0.5)))
+    assert np.array_equal(oracle.plane_q6k(W, N, K), (codes - 32).astype(np.int8))
+
+
+# --------------------------------------------------------------- routing / MoE
+
+def test_route_topk_matches_stable_sort_and_scipy_softmax():
+    from scipy.special import softmax
+    logits = synth.normal_f32(50, (16, 256))
+    logits[3, 10] = logits[3, 200] = 9.0  # a tie: the lower index must come first
+    idx, gate = oracle.route_topk_softmax(logits, 8)
+    for t in range(16):
+        ref = np.argsort(-logits[t].astype(np.float64), kind="stable")[:8]
+        assert np.array_equal(idx[t], ref)
+        assert np.allclose(gate[t], softmax(logits[t, ref].astype(np.float64)), rtol=1e-14)
+    assert list(idx[3, :2]) == [10, 200]
+    assert np.allclose(gate.sum(1), 1.0, rtol=1e-15)
+
+
+def _dense_ffn(fmt, wg, wu, wd, H, I, x):
+    g = oracle.dequant(fmt, wg, I, H) @ x
+    u = oracle.dequant(fmt, wu, I, H) @ x
+    h = g / (1.0 + np.exp(-g)) * u
+    return oracle.dequant(fmt, wd, H, I) @ h
+
+
+def test_moe_single_expert_is_plain_swiglu_ffn():
+    H, I, E = 64, 96, 4
+    fmt = oracle.Q4_0
+    wg = [synth.q4_0_matrix(60 + e, I, H) for e in range(E)]
+    wu = [synth.q4_0_matrix(70 + e, I, H) for e in range(E)]
+    wd = [synth.q4_0_matrix(80 + e, H, I) for e in range(E)]
+    x = synth.normal_f32(61, (2, H))
+    idx = np.array([[2], [0]], np.int32)
+    gate = np.ones((2, 1))
+    y, bound = oracle.moe_float(fmt, H, I, wg, wu, wd, idx, gate, x)
+    for t in range(2):
+        ref = _dense_ffn(fmt, wg[idx[t, 0]], wu[idx[t, 0]], wd[idx[t, 0]], H, I,
+                         x[t].astype(np.float64))
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-15)
+    assert (bound > 0).all()
+
+
+def test_moe_identical_experts_sum_of_gates_is_one():
+    H, I, E, k = 64, 32, 8, 4
+    fmt = oracle.Q4_0
+    g0 = synth.q4_0_matrix(90, I, H)
+    u0 = synth.q4_0_matrix(91, I, H)
+    d0 = synth.q4_0_matrix(92, H, I)
+    x = synth.normal_bf16(93, (3, H))
+    logits = synth.normal_f32(94, (3, E))
+    idx, gate = oracle.route_topk_softmax(logits, k)
+    y, _ = oracle.moe_float(fmt, H, I, [g0] * E, [u0] * E, [d0] * E, idx, gate, x)
+    for t in range(3):
+        ref = _dense_ffn(fmt, g0, u0, d0, H, I, synth.bf16_bits_to_f32(x[t]).astype(np.float64))
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-15)
