@@ -201,7 +201,9 @@ void orc_gemv_float(int fmt, const uint8_t* W, int64_t N, int64_t K,
 /* ------------------------------------------------------------------ */
 /* activation quantizer: per 32-element block, s = amax/127 (fp32),     */
 /* x_q = round-half-even(x / s) clamped to [-127, 127]; amax == 0 gives */
-/* s = 0 and x_q = 0. Decisions taken in fp32.                          */
+/* s = 0 and x_q = 0. Decisions taken in fp32. Reading: a block whose   */
+/* scale amax/127 rounds to zero in fp32 (amax below about 9e-44) is     */
+/* treated like the all-zero block, since x/s is undefined there.        */
 /* ------------------------------------------------------------------ */
 
 void orc_quantize_q8(const void* x, int xkind, int64_t rows, int64_t K,
@@ -218,7 +220,7 @@ void orc_quantize_q8(const void* x, int xkind, int64_t rows, int64_t K,
             s[r * (K / 32) + b0 / 32] = sc;
             for (int i = 0; i < 32; ++i) {
                 int q = 0;
-                if (amax != 0.0f) {
+                if (sc != 0.0f) {
                     float v = (float)load_x(x, xkind, r * K + b0 + i);
                     float t = v / sc;
                     float rq = nearbyintf(t); /* default mode: to nearest, ties to even */

@@ -228,6 +228,18 @@ def test_quantizer_hand_vectors():
     assert s[0, 2] == np.float32(3.0) / np.float32(127.0)
 
 
+def test_quantizer_scale_underflow_gives_zeros():
+    """amax so small that amax/127 rounds to 0 in fp32: the block is all zeros"""
+    x = np.zeros((1, 32), np.float32)
+    x[0, 5] = np.float32(1e-45)  # smallest fp32 subnormal
+    x[0, 6] = -np.float32(1e-45)
+    xq, s = oracle.quantize_q8(x)
+    assert s[0, 0] == 0.0 and not xq.any()
+    x[0, 5] = np.float32(2e-38)  # normal tiny amax: scale stays non-zero
+    xq, s = oracle.quantize_q8(x)
+    assert s[0, 0] == np.float32(2e-38) / np.float32(127.0) and xq[0, 5] == 127
+
+
 def test_quantizer_amax_maps_to_127_and_range():
     x = synth.normal_f32(11, (8, 1024))
     xq, s = oracle.quantize_q8(x)
