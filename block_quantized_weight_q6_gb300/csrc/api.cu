@@ -1,0 +1,431 @@
+// api.cu -- the C interface of libqmm (include/qmm.h): argument checks,
+// launch planning, the W_exp plane registry and gate, liveness counters and
+// error reporting. All compute runs in the kernels of the other files.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "kernels.h"
+#include "qmm.h"
+
+using namespace qmm;
+
+// Library state that lives in device memory (one copy per device).
+__device__ unsigned long long g_live[QMM_LIVE_COUNT];
+__device__ unsigned int g_err;
+
+namespace {
+
+thread_local cudaStream_t t_stream = nullptr;
+thread_local void* t_ws = nullptr;
+thread_local size_t t_ws_bytes = 0;
+thread_local char t_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_err, sizeof t_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(QMM_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- env gate
+// Read once ("57 - r54 MINFER_MMQ_Q6K_EXP" section 3.1: the env is read
+// exactly once, at load; unset means on, only an explicit "0" opts out).
+struct Env {
+    bool exp_on = true;
+    bool debug_label = false;
+    bool fault_plane_alloc = false;
+};
+Env g_env;
+std::once_flag g_env_once;
+
+void read_env() {
+    const char* e = std::getenv("QMM_Q6K_EXP");
+    g_env.exp_on = !(e && std::strcmp(e, "0") == 0);
+    const char* d = std::getenv("QMM_DEBUG_LABEL");
+    g_env.debug_label = d && std::strcmp(d, "1") == 0;
+    const char* f = std::getenv("QMM_FAULT");
+    g_env.fault_plane_alloc = f && std::strcmp(f, "plane_alloc") == 0;
+}
+
+// ---------------------------------------------------------------- devices
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+    DevState st{};
+};
+constexpr int kMaxDev = 64;
+DevInfo g_dev[kMaxDev];
+std::mutex g_dev_mu;
+
+int dev_info(DevInfo** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDev) return fail(QMM_EUNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ready) {
+        e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_live);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(live)");
+        d.st.live = static_cast<unsigned long long*>(p);
+        e = cudaGetSymbolAddress(&p, g_err);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(err)");
+        d.st.err = static_cast<unsigned int*>(p);
+        d.ready = true;
+    }
+    *out = &d;
+    return QMM_OK;
+}
+
+// ---------------------------------------------------------------- plane registry
+// Keyed by the weight pointer the GEMM receives (the key the page's engine
+// had to get right, section 3.3), remembering the geometry the plane was
+// built for so that a plane of another shape is never used silently.
+struct PlaneEntry {
+    const int8_t* plane;
+    int64_t N, K;
+};
+std::unordered_map<const void*, PlaneEntry> g_planes;
+std::mutex g_planes_mu;
+
+// ---------------------------------------------------------------- formats
+int block_elems(int f) { return f == FMT_Q6_K ? 256 : 32; }
+int block_bytes(int f) { return f == FMT_Q6_K ? 210 : (f == FMT_Q4_0 ? 18 : 34); }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int check_fmt(uint32_t fmt, int* wf, bool* bf16, bool* q8) {
+    if (fmt & ~static_cast<uint32_t>(QMM_FMT_MASK | QMM_X_MASK | QMM_ACT_MASK))
+        return fail(QMM_EINVAL, "fmt 0x%x has unknown bits", fmt);
+    *wf = static_cast<int>(fmt & QMM_FMT_MASK);
+    if (*wf != QMM_Q4_0 && *wf != QMM_Q8_0 && *wf != QMM_Q6_K)
+        return fail(QMM_EINVAL, "unknown weight format 0x%x", fmt & QMM_FMT_MASK);
+    const uint32_t xk = fmt & QMM_X_MASK, am = fmt & QMM_ACT_MASK;
+    if (xk != QMM_X_F32 && xk != QMM_X_BF16)
+        return fail(QMM_EINVAL, "unknown activation type 0x%x", xk);
+    if (am != QMM_ACT_FLOAT && am != QMM_ACT_Q8)
+        return fail(QMM_EINVAL, "unknown activation mode 0x%x", am);
+    *bf16 = xk == QMM_X_BF16;
+    *q8 = am == QMM_ACT_Q8;
+    return QMM_OK;
+}
+
+// ---------------------------------------------------------------- GEMV plan
+struct GemvPlan {
+    int NB, R, splits, cps, nchunks, grid;
+    int64_t n_items;
+    size_t ws_xq, ws_xs, ws_part, ws_total;  // workspace byte offsets / total
+};
+
+int occupancy_cached(int fmt, bool q8, int NB, int R) {
+    // [fmt][q8][NB index][R index]
+    static int cache[4][2][5][3];
+    static std::mutex mu;
+    const int nbi = NB == 1 ? 0 : NB == 2 ? 1 : NB == 4 ? 2 : NB == 8 ? 3 : 4;
+    const int ri = R == 1 ? 0 : R == 2 ? 1 : 2;
+    std::lock_guard<std::mutex> lk(mu);
+    int& c = cache[fmt][q8][nbi][ri];
+    if (c == 0) c = gemv_occupancy(fmt, q8, NB, R);
+    return c;
+}
+
+int plan_gemv(int fmt, bool q8, int B, int64_t N, int64_t K, int sms, GemvPlan* p) {
+    p->NB = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+    const int64_t nb = K / block_elems(fmt);
+    p->nchunks = static_cast<int>((nb + gemv_chunk_blocks(fmt) - 1) / gemv_chunk_blocks(fmt));
+    int R = p->NB == 1 ? 4 : (p->NB == 2 ? 2 : 1);
+    int occ = occupancy_cached(fmt, q8, p->NB, R);
+    if (R == 4) {
+        // rows grouped by 4 only when that alone fills every warp slot
+        const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
+        if ((N + 3) / 4 < cap) {
+            R = 1;
+            occ = occupancy_cached(fmt, q8, p->NB, R);
+        }
+    }
+    if (occ <= 0) return fail(QMM_ECUDA, "gemv kernel (fmt %d, NB %d, R %d) cannot launch", fmt,
+                              p->NB, R);
+    p->R = R;
+    const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
+    const int64_t groups = (N + R - 1) / R;
+    int splits = 1;
+    if (groups < cap) {
+        int64_t s = (cap + groups - 1) / groups;
+        splits = static_cast<int>(s < p->nchunks ? s : p->nchunks);
+    }
+    p->cps = (p->nchunks + splits - 1) / splits;
+    p->splits = (p->nchunks + p->cps - 1) / p->cps;
+    p->n_items = groups * p->splits;
+    int64_t grid = (p->n_items + kGemvWarps - 1) / kGemvWarps;
+    const int64_t maxg = static_cast<int64_t>(sms) * occ;
+    p->grid = static_cast<int>(grid < maxg ? grid : maxg);
+    size_t off = 0;
+    p->ws_xq = p->ws_xs = p->ws_part = 0;
+    if (q8) {
+        p->ws_xq = off;
+        off = round_up(off + static_cast<size_t>(B) * K, 256);
+        p->ws_xs = off;
+        off = round_up(off + static_cast<size_t>(B) * (K / 32) * 4, 256);
+    }
+    if (p->splits > 1) {
+        p->ws_part = off;
+        off = round_up(off + static_cast<size_t>(p->splits) * B * N * 4, 256);
+    }
+    p->ws_total = off;
+    return QMM_OK;
+}
+
+int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, int64_t N,
+                    int64_t K, int B, int* wf, bool* bf16, bool* q8) {
+    int rc = check_fmt(fmt, wf, bf16, q8);
+    if (rc) return rc;
+    if (!W || !x || !y) return fail(QMM_EINVAL, "null pointer (W %p, x %p, y %p)", W, x, (const void*)y);
+    if (N <= 0 || K <= 0) return fail(QMM_EINVAL, "N %lld and K %lld must be positive",
+                                      (long long)N, (long long)K);
+    if (B < 1 || B > 16) return fail(QMM_EINVAL, "B = %d outside 1..16", B);
+    if (K % block_elems(*wf)) return fail(QMM_EALIGN, "K = %lld is not a multiple of %d",
+                                          (long long)K, block_elems(*wf));
+    if (!aligned16(W) || !aligned16(x)) return fail(QMM_EALIGN, "W and x must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(y) & 3u) return fail(QMM_EALIGN, "y must be 4-byte aligned");
+    return QMM_OK;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+int qmm_init(void) {
+    std::call_once(g_env_once, read_env);
+    return QMM_OK;
+}
+
+int qmm_set_stream(void* cuda_stream) {
+    qmm_init();
+    t_stream = static_cast<cudaStream_t>(cuda_stream);
+    return QMM_OK;
+}
+
+int qmm_set_workspace(void* dev, size_t bytes) {
+    qmm_init();
+    if (!dev && bytes) return fail(QMM_EINVAL, "null workspace with %zu bytes", bytes);
+    if (reinterpret_cast<uintptr_t>(dev) & 255u)
+        return fail(QMM_EALIGN, "workspace must be 256-byte aligned");
+    t_ws = dev;
+    t_ws_bytes = dev ? bytes : 0;
+    return QMM_OK;
+}
+
+size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
+
+int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, int64_t K, int B) {
+    qmm_init();
+    int wf;
+    bool bf16, q8;
+    int rc = check_gemv_args(fmt, W, x, y, N, K, B, &wf, &bf16, &q8);
+    if (rc) return rc;
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    GemvPlan p;
+    if ((rc = plan_gemv(wf, q8, B, N, K, d->sms, &p))) return rc;
+    if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
+        return fail(QMM_ENOWORKSPACE, "qmm_gemv needs %zu bytes of workspace, %zu set", p.ws_total,
+                    t_ws_bytes);
+    uint8_t* ws = static_cast<uint8_t*>(t_ws);
+    GemvArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.N = N;
+    a.K = K;
+    a.nb = K / block_elems(wf);
+    a.total_bytes = N * a.nb * block_bytes(wf);
+    a.x = x;
+    a.x_bf16 = bf16;
+    a.B = B;
+    a.y = y;
+    a.splits = p.splits;
+    a.cps = p.cps;
+    a.nchunks = p.nchunks;
+    a.n_items = p.n_items;
+    a.st = d->st;
+    a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
+    cudaError_t e;
+    if (q8) {
+        a.xq = reinterpret_cast<int8_t*>(ws + p.ws_xq);
+        a.xs = reinterpret_cast<float*>(ws + p.ws_xs);
+        e = quantize_q8_launch(x, bf16, B, K, const_cast<int8_t*>(a.xq), const_cast<float*>(a.xs),
+                               nullptr, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    }
+    if (p.splits > 1) a.part = reinterpret_cast<float*>(ws + p.ws_part);
+    e = gemv_launch(wf, q8, p.NB, p.R, p.grid, t_stream, a);
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    if (p.splits > 1) {
+        e = splitk_reduce_launch(a.part, y, p.splits, static_cast<int64_t>(B) * N, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+    }
+    return QMM_OK;
+}
+
+int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int8_t* xq,
+                    float* s) {
+    qmm_init();
+    if (x_type != QMM_X_F32 && x_type != QMM_X_BF16)
+        return fail(QMM_EINVAL, "x_type 0x%x is not QMM_X_F32 or QMM_X_BF16", x_type);
+    if (!x || !xq || !s) return fail(QMM_EINVAL, "null pointer");
+    if (rows <= 0 || K <= 0) return fail(QMM_EINVAL, "rows and K must be positive");
+    if (K % 32) return fail(QMM_EALIGN, "K = %lld is not a multiple of 32", (long long)K);
+    if (!aligned16(x) || !aligned16(xq)) return fail(QMM_EALIGN, "x and xq must be 16-byte aligned");
+    if (reinterpret_cast<uintptr_t>(s) & 3u) return fail(QMM_EALIGN, "s must be 4-byte aligned");
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = quantize_q8_launch(x, x_type == QMM_X_BF16, rows, K, xq, s, nullptr, t_stream,
+                                       d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    return QMM_OK;
+}
+
+size_t qmm_plane_bytes(int64_t N, int64_t K) {
+    if (N <= 0 || K <= 0) return 0;
+    return static_cast<size_t>(N) * static_cast<size_t>(K);
+}
+
+int qmm_plane_wanted(int64_t N, int64_t K) {
+    qmm_init();
+    return (g_env.exp_on && N > 0 && K > 0 && K % 256 == 0) ? 1 : 0;
+}
+
+int qmm_plane_build(const void* W_q6k, int64_t N, int64_t K, int8_t* plane_dst) {
+    qmm_init();
+    if (!W_q6k) return fail(QMM_EINVAL, "null W");
+    if (N <= 0 || K <= 0) return fail(QMM_EINVAL, "N and K must be positive");
+    if (K % 256) return fail(QMM_EALIGN, "K = %lld is not a multiple of 256", (long long)K);
+    if (!aligned16(W_q6k)) return fail(QMM_EALIGN, "W must be 16-byte aligned");
+    if (plane_dst && !aligned16(plane_dst)) return fail(QMM_EALIGN, "plane must be 16-byte aligned");
+    if (!plane_dst || g_env.fault_plane_alloc) {
+        // a plane was wanted but none could be allocated: remember it so that
+        // the in-kernel path taken later is labelled as a fallback
+        std::lock_guard<std::mutex> lk(g_planes_mu);
+        g_planes[W_q6k] = PlaneEntry{nullptr, N, K};
+        std::fprintf(stderr, "qmm: W_exp plane for %p (%lld x %lld) not available; "
+                             "q6_K GEMM falls back to in-kernel expansion\n",
+                     W_q6k, (long long)N, (long long)K);
+        return QMM_OK;
+    }
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = plane_build_launch(static_cast<const uint8_t*>(W_q6k), N, K, plane_dst,
+                                       t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "plane build launch");
+    std::lock_guard<std::mutex> lk(g_planes_mu);
+    g_planes[W_q6k] = PlaneEntry{plane_dst, N, K};
+    return QMM_OK;
+}
+
+int qmm_plane_release(const void* W_q6k) {
+    qmm_init();
+    std::lock_guard<std::mutex> lk(g_planes_mu);
+    g_planes.erase(W_q6k);
+    return QMM_OK;
+}
+
+int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
+             const int8_t* exp_plane) {
+    qmm_init();
+    (void)fmt; (void)W; (void)X; (void)Y; (void)M; (void)N; (void)K; (void)exp_plane;
+    return fail(QMM_EUNSUPPORTED, "qmm_gemm is not built yet");
+}
+
+int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const float* gate_w,
+             const void* x, float* y) {
+    qmm_init();
+    (void)fmt; (void)experts; (void)idx; (void)gate_w; (void)x; (void)y;
+    return fail(QMM_EUNSUPPORTED, "moe_gemv is not built yet");
+}
+
+size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts) {
+    (void)experts;
+    return 0;
+}
+
+int qmm_route_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate_w) {
+    qmm_init();
+    (void)logits; (void)T; (void)E; (void)k; (void)idx; (void)gate_w;
+    return fail(QMM_EUNSUPPORTED, "routing is not built yet");
+}
+
+size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
+    qmm_init();
+    int wf;
+    bool bf16, q8;
+    if (check_fmt(fmt, &wf, &bf16, &q8)) return 0;
+    if (M_or_B < 1 || M_or_B > 16 || N <= 0 || K <= 0 || K % block_elems(wf)) return 0;
+    DevInfo* d;
+    if (dev_info(&d)) return 0;
+    GemvPlan p;
+    if (plan_gemv(wf, q8, static_cast<int>(M_or_B), N, K, d->sms, &p)) return 0;
+    return p.ws_total;
+}
+
+int qmm_liveness_read(int64_t* counts, int n) {
+    qmm_init();
+    if (!counts || n < 0 || n > QMM_LIVE_COUNT)
+        return fail(QMM_EINVAL, "counts must hold n <= %d values", QMM_LIVE_COUNT);
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    unsigned long long tmp[QMM_LIVE_COUNT];
+    cudaError_t e = cudaMemcpy(tmp, d->st.live, sizeof tmp, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "liveness read");
+    for (int i = 0; i < n; ++i) counts[i] = static_cast<int64_t>(tmp[i]);
+    return QMM_OK;
+}
+
+int qmm_liveness_reset(void) {
+    qmm_init();
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = cudaMemsetAsync(d->st.live, 0, sizeof(unsigned long long) * QMM_LIVE_COUNT,
+                                    t_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "liveness reset");
+    return QMM_OK;
+}
+
+int qmm_sync_check(void) {
+    qmm_init();
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = cudaStreamSynchronize(t_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    unsigned int err = 0;
+    e = cudaMemcpy(&err, d->st.err, sizeof err, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "error word read");
+    if (err) {
+        unsigned int zero = 0;
+        cudaMemcpy(d->st.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        return fail(QMM_EDEVICE_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", err);
+    }
+    return QMM_OK;
+}
+
+const char* qmm_last_error(void) { return t_err; }
+
+}  // extern "C"

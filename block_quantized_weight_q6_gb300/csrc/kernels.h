@@ -1,0 +1,63 @@
+// kernels.h -- internal interface between the host dispatch (api.cu) and the
+// kernel translation units. Not part of the public C interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace qmm {
+
+// ---------------------------------------------------------------- GEMV
+// One warp owns a run of (row group, K split) items; each item is R
+// consecutive rows over a range of K chunks. A chunk is CB consecutive
+// blocks of a row (q6_K: 8 super-blocks, Q4_0 / Q8_0: 32 blocks). The warp
+// streams its chunks into a private ring of shared-memory slots with 1-D
+// bulk TMA copies and decodes them from there.
+constexpr int kGemvWarps = 8;
+constexpr int kGemvThreads = kGemvWarps * 32;
+constexpr int kGemvSlots = 4;
+
+struct GemvArgs {
+    const uint8_t* W;
+    int64_t N, K, nb;      // rows, columns, blocks per row
+    int64_t total_bytes;   // bytes of W (N * nb * block bytes)
+    const void* x;         // float mode: [B][K] fp32 or bf16
+    int x_bf16;
+    const int8_t* xq;      // q8 mode: [B][K] int8
+    const float* xs;       // q8 mode: [B][K/32] fp32
+    int B;
+    float* y;              // [B][N] when splits == 1
+    float* part;           // [splits][B][N] when splits > 1
+    int splits, cps, nchunks;
+    int64_t n_items;       // ceil(N / R) * splits
+    DevState st;
+    int live_slot;
+};
+
+// shared memory bytes of one CTA of the (fmt, R) kernel
+size_t gemv_smem_bytes(int fmt, int R);
+int gemv_chunk_blocks(int fmt);
+// launches the kernel instantiation for (fmt, q8, NB, R); returns
+// cudaErrorInvalidValue if that instantiation is not built.
+cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t s,
+                        const GemvArgs& a);
+// max resident CTAs per SM for (fmt, q8, NB, R) (0 if not built)
+int gemv_occupancy(int fmt, bool q8, int NB, int R);
+
+cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
+                                 cudaStream_t s, DevState st);
+
+// ---------------------------------------------------------------- quantizer
+// x [rows][K] (fp32 or bf16) -> xq [rows][K] int8, xs [rows][K/32] fp32.
+// If a16 != nullptr, also writes the quantized values as fp16 in the GEMM's
+// A-operand tile layout (see gemm.cu), for rows rounded up to 128.
+cudaError_t quantize_q8_launch(const void* x, int x_bf16, int64_t rows, int64_t K, int8_t* xq,
+                               float* xs, uint16_t* a16, cudaStream_t s, DevState st);
+
+// ---------------------------------------------------------------- plane
+cudaError_t plane_build_launch(const uint8_t* W, int64_t N, int64_t K, int8_t* plane,
+                               cudaStream_t s, DevState st);
+
+}  // namespace qmm

@@ -1,0 +1,228 @@
+/*
+ * qmm.h -- C interface of libqmm, matrix multiplication against
+ * block-quantized LLM weights with the dequantization fused into the kernels,
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions that hold for every call below unless its comment says
+ * otherwise:
+ *  - Pointers named W, x, X, y, Y, plane, idx, gate_w, logits are DEVICE
+ *    pointers. The caller allocates and owns them (typically torch tensors);
+ *    the library never frees them and keeps no reference after the call
+ *    returns, except the plane registry described at qmm_plane_build.
+ *  - Calls are asynchronous on the calling thread's current stream
+ *    (qmm_set_stream); none synchronizes the device except
+ *    qmm_liveness_read and qmm_sync_check.
+ *  - Every call returns QMM_OK (0) or a negative QMM_E* code. Argument errors
+ *    are detected on the host before anything is launched; qmm_last_error()
+ *    then gives a one-line reason (thread-local, valid until the next call).
+ *  - Weight matrices are row-major by output row n: row n is K/E consecutive
+ *    blocks (E = 256 for q6_K, 32 for Q4_0 and Q8_0), with no padding between
+ *    rows. W must be 16-byte aligned.
+ *
+ * Block formats (weight w of element i of a block; d is fp16 little-endian):
+ *  q6_K, 210 B per 256 weights: ql[128] | qh[64] | scales[16] int8 | d.
+ *      q = ((ql[i%128] >> 4*(i/128)) & 0xF) | ((qh[i%64] >> 2*(i/64)) & 3) << 4,
+ *      w = d * scales[i/16] * (q - 32).  The element expansion is the one of
+ *      "57 - r54 MINFER_MMQ_Q6K_EXP" section 2.1 (per 16-element group); the
+ *      nibble order within ql/qh is this library's reading, stated here.
+ *  Q4_0, 18 B per 32 weights: d | qs[16]; q = (qs[i%16] >> 4*(i/16)) & 0xF,
+ *      w = d * (q - 8).
+ *  Q8_0, 34 B per 32 weights: d | qs[32] int8; w = d * qs[i].
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* fmt = weight format | activation element type | activation mode */
+enum {
+    QMM_Q4_0 = 0x01,
+    QMM_Q8_0 = 0x02,
+    QMM_Q6_K = 0x03,
+    QMM_FMT_MASK = 0xFF,
+
+    QMM_X_F32 = 0x000,  /* activations are fp32                              */
+    QMM_X_BF16 = 0x100, /* activations are bfloat16                          */
+    QMM_X_MASK = 0xF00,
+
+    QMM_ACT_FLOAT = 0x0000, /* fp32 arithmetic on the activations as given    */
+    QMM_ACT_Q8 = 0x1000,    /* activations quantized per 32 to int8 + fp32
+                               scale (s = amax/127, x_q = round-half-even(x/s)),
+                               then exact integer dot products per weight
+                               group, as in quantprobe "LAWS.md" Law 4
+                               amendment L-15 (dp4a matvec)                   */
+    QMM_ACT_MASK = 0xF000
+};
+
+enum {
+    QMM_OK = 0,
+    QMM_EINVAL = -1,           /* null pointer, non-positive size, bad B/fmt  */
+    QMM_EUNSUPPORTED = -2,     /* format/mode combination not built            */
+    QMM_EALIGN = -3,           /* K not a multiple of the block, or a pointer
+                                  not 16-byte aligned                          */
+    QMM_ECUDA = -4,            /* a CUDA runtime call failed                   */
+    QMM_EPLANE = -5,           /* exp_plane was not built for this W / N / K   */
+    QMM_EDEVICE_TIMEOUT = -6,  /* a kernel gave up a bounded wait (see
+                                  qmm_sync_check)                              */
+    QMM_ENOWORKSPACE = -7      /* the call needs more workspace than is set    */
+};
+
+/* Liveness counters: one slot per kernel path, incremented once per launch by
+ * the launched kernel itself (so a launch that silently never ran is not
+ * counted). The four q6_K GEMM slots are the four labels of
+ * "57 - r54 MINFER_MMQ_Q6K_EXP" section 3.2: plane path, raw weights that
+ * never had a plane, plane deliberately switched off, plane expected but
+ * missing (an accidental fallback). */
+enum {
+    QMM_LIVE_GEMV_FLOAT = 0,
+    QMM_LIVE_GEMV_Q8 = 1,
+    QMM_LIVE_GEMV_SPLITK_REDUCE = 2,
+    QMM_LIVE_QUANTIZE = 3,
+    QMM_LIVE_PLANE_BUILD = 4,
+    QMM_LIVE_GEMM_EXP_PLANE = 5,      /* "W_exp-cp.async"                    */
+    QMM_LIVE_GEMM_IN_KERNEL = 6,      /* "in-kernel-expand" (never eligible) */
+    QMM_LIVE_GEMM_EXP_OFF = 7,        /* "in-kernel-expand(exp=off)"         */
+    QMM_LIVE_GEMM_FALLBACK = 8,       /* "in-kernel-expand(fallback!)"       */
+    QMM_LIVE_GEMM_Q4_0 = 9,
+    QMM_LIVE_ROUTE = 10,
+    QMM_LIVE_MOE_GATE_UP = 11,
+    QMM_LIVE_MOE_DOWN = 12,
+    QMM_LIVE_MOE_COMBINE = 13,
+    QMM_LIVE_COUNT = 16
+};
+
+/* Reads the environment once: QMM_Q6K_EXP ("0" opts out of building W_exp
+ * planes; unset or anything else keeps them on, the default-on / "0" opt-out
+ * gate of "57 - r54 MINFER_MMQ_Q6K_EXP" section 3.1), QMM_DEBUG_LABEL ("1"
+ * prints one stderr line per q6_K GEMM launch naming its path, section 2.4),
+ * QMM_FAULT ("plane_alloc" makes qmm_plane_wanted's caller-side allocation be
+ * treated as failed; host-side fault injection only). Called implicitly by
+ * every entry point; calling it again is a no-op. */
+int qmm_init(void);
+
+/* Sets the CUDA stream (a cudaStream_t, e.g. torch's current stream) that the
+ * calling thread's subsequent calls launch on. NULL selects the legacy
+ * default stream. */
+int qmm_set_stream(void* cuda_stream);
+
+/* Sets the calling thread's workspace: a device buffer of `bytes` bytes,
+ * 256-byte aligned, owned by the caller, that calls may use as scratch
+ * (split-K partial sums, quantized activations, MoE intermediates). Calls on
+ * the same stream may reuse it back to back; the caller must not use it
+ * concurrently on two streams. */
+int qmm_set_workspace(void* dev, size_t bytes);
+
+/* Workspace that qmm_gemv (M_or_B = B) or qmm_gemm (M_or_B = M) needs for
+ * these sizes; 0 if none. */
+size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
+
+/* Batched decode matvec, y[b][n] = sum_k w[n][k] * x[b][k], b < B <= 16.
+ * x: [B][K] fp32 or bf16 (fmt bits), y: [B][N] fp32 (overwritten).
+ * QMM_ACT_FLOAT: fp32 products and sums of the activations as given.
+ * QMM_ACT_Q8: x is first quantized per 32 (needs workspace), then
+ *   y = sum_g s_x * d * sc_g * I_g with exact int32 group partials I_g.
+ * Short N is split along K; the partial sums are then added in a fixed order
+ * by a second launch, so results are bitwise reproducible. */
+int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
+             int64_t K, int B);
+
+/* The per-32 activation quantizer on its own (the first step of QMM_ACT_Q8
+ * and of qmm_gemm): x [rows][K] of type x_type (QMM_X_F32 or QMM_X_BF16),
+ * K % 32 == 0 -> xq [rows][K] int8 and s [rows][K/32] fp32 with
+ * s = amax/127 and xq = round-half-even(x/s) clamped to [-127, 127], both
+ * divisions IEEE fp32; a block whose s is 0 gives zeros. x, xq 16-byte
+ * aligned. */
+int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int8_t* xq,
+                    float* s);
+
+/* Prefill GEMM, Y[m][n] = sum_b s_x[m][b] * sum_{g in b} d[n] * sc[n][g] *
+ * sum_{k in g} x_q[m][k] * c[n][k], with X quantized per 32 as in
+ * QMM_ACT_Q8 and c the centered weight code. X: [M][K] bf16, Y: [M][N] fp32.
+ * The integer partials run on the tensor cores (tcgen05, fp16 operands that
+ * hold the integers exactly, fp32 accumulation that stays exact per 32-wide
+ * block).
+ * q6_K: exp_plane != NULL selects the W_exp-plane variant (the B tile is a
+ *   plain copy of the centered-int8 plane, "57 - r54 MINFER_MMQ_Q6K_EXP"
+ *   section 2.1, first bullet); NULL selects in-kernel ql/qh expansion
+ *   (second bullet). The two give bitwise-identical Y (section 2.3). The
+ *   plane must come from qmm_plane_build for this same W, N and K, else
+ *   QMM_EPLANE.
+ * Q4_0: in-kernel expansion only; exp_plane must be NULL.
+ * Needs workspace (quantized X). */
+int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M,
+             int64_t N, int64_t K, const int8_t* exp_plane);
+
+/* Bytes of the W_exp plane of an N x K q6_K matrix: N*K (one centered int8
+ * per weight, "57 - r54 MINFER_MMQ_Q6K_EXP" section 2.2). */
+size_t qmm_plane_bytes(int64_t N, int64_t K);
+
+/* Whether the registration gate builds a plane for an N x K q6_K matrix:
+ * QMM_Q6K_EXP != "0" AND K % 256 == 0 (section 3.1, "AND semantics").
+ * Returns 1 or 0. With QMM_FAULT=plane_alloc it still returns 1, and
+ * qmm_plane_build(W, N, K, NULL) then records the failure. */
+int qmm_plane_wanted(int64_t N, int64_t K);
+
+/* Builds the plane of W into plane_dst (qmm_plane_bytes(N, K) bytes, device,
+ * caller-owned) and registers it as W's plane: plane[n][k] = q(n,k) - 32.
+ * plane_dst == NULL records that a plane was wanted for W but could not be
+ * allocated; later qmm_gemm calls on W with a NULL plane are then counted as
+ * QMM_LIVE_GEMM_FALLBACK, and "fallback!" is printed once to stderr
+ * (section 1, failure semantics). */
+int qmm_plane_build(const void* W_q6k, int64_t N, int64_t K, int8_t* plane_dst);
+
+/* Forgets the registration of W's plane (call before freeing either). */
+int qmm_plane_release(const void* W_q6k);
+
+/* Routed experts of one MoE layer, all in format fmt, all resident in device
+ * memory: w_gate[e], w_up[e] are inter x hidden, w_down[e] is hidden x inter.
+ * The three pointer arrays are HOST arrays of n_experts DEVICE pointers. */
+typedef struct {
+    int n_experts, hidden, inter, top_k, n_tokens;
+    const void* const* w_gate;
+    const void* const* w_up;
+    const void* const* w_down;
+} qmm_moe_t;
+
+/* Routed expert FFN for n_tokens tokens ("Chasing x100", section "Where the
+ * wall actually fell: inversion": experts stay resident and are decoded in
+ * place): for each token t and each of its top_k experts e = idx[t][j],
+ * h = silu(Wg_e x_t) * (Wu_e x_t), o = Wd_e h, and
+ * y[t] = sum_j gate_w[t][j] * o_j, summed in j order.
+ * idx: [T][top_k] int32, gate_w: [T][top_k] fp32, x: [T][hidden] (fmt's
+ * activation type), y: [T][hidden] fp32. Float activation mode only. Each
+ * selected expert's matrices are read once per call however many of the
+ * tokens chose it. Needs workspace. */
+int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
+             const float* gate_w, const void* x, float* y);
+
+/* Workspace moe_gemv needs. */
+size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts);
+
+/* Router helper: per token, the k largest of E fp32 logits (ties go to the
+ * lower expert index) and their softmax over those k. logits: [T][E],
+ * idx: [T][k] int32, gate_w: [T][k] fp32. E <= 1024, k <= 32. */
+int qmm_route_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx,
+                           float* gate_w);
+
+/* Copies the first n liveness counters to the HOST array counts (synchronizes
+ * the current device). */
+int qmm_liveness_read(int64_t* counts, int n);
+int qmm_liveness_reset(void);
+
+/* Synchronizes the current stream and reports QMM_EDEVICE_TIMEOUT if any
+ * kernel gave up a bounded wait since the last check (the flag is cleared). */
+int qmm_sync_check(void);
+
+/* Reason for the calling thread's last non-OK return. */
+const char* qmm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,220 @@
+"""Decode matvec on the GPU (through the C interface) against the CPU oracle.
+
+Float paths: |y - y_ref| <= 1e-4 * sum_k |w_k x_k| + 1e-6 per element.
+Integer paths (unit scales, integer activations): bitwise equal.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import pack
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU-only containers
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import block_quantized_weight_q6_gb300 as qmm  # noqa: E402
+
+FMTS = {"q6_K": qmm.Q6_K, "Q4_0": qmm.Q4_0, "Q8_0": qmm.Q8_0}
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def x_tensor(x):
+    """numpy fp32 or bf16-bits -> torch cuda tensor of the same values"""
+    if x.dtype == np.uint16:
+        return dev(x.view(np.int16)).view(torch.bfloat16)
+    return dev(x)
+
+
+def run_gemv(fmt, W, x, N, K, act=qmm.ACT_FLOAT):
+    B = x.shape[0]
+    y = torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.gemv(fmt, dev(W), x_tensor(x), y, N, K, act)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    return y.cpu().numpy()
+
+
+def assert_within(y, ref, absum, what=""):
+    err = np.abs(y.astype(np.float64) - ref)
+    bound = 1e-4 * absum + 1e-6
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} elements out of bound; first {tuple(i)}: "
+                             f"got {y[tuple(i)]}, ref {ref[tuple(i)]}, bound {bound[tuple(i)]}")
+
+
+SMALL = [("q6_K", 37, 256 * 19), ("Q4_0", 53, 32 * 71), ("Q8_0", 29, 32 * 45),
+         ("q6_K", 5, 256), ("Q4_0", 3, 32)]
+
+
+@pytest.mark.parametrize("name,N,K", SMALL)
+@pytest.mark.parametrize("B", [1, 2, 3, 8, 16])
+@pytest.mark.parametrize("xdt", ["f32", "bf16"])
+def test_gemv_float_small(name, N, K, B, xdt):
+    fmt = FMTS[name]
+    W = synth.matrix(fmt, 100 + N, N, K)
+    x = synth.normal_f32(7 + B, (B, K)) if xdt == "f32" else synth.normal_bf16(7 + B, (B, K))
+    y = run_gemv(fmt, W, x, N, K)
+    ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+    assert_within(y, ref, absum, f"{name} {N}x{K} B={B} {xdt}")
+
+
+@pytest.mark.parametrize("name,N,K", SMALL)
+@pytest.mark.parametrize("B", [1, 2, 8, 16])
+def test_gemv_q8_small(name, N, K, B):
+    fmt = FMTS[name]
+    W = synth.matrix(fmt, 200 + N, N, K)
+    x = synth.normal_bf16(17 + B, (B, K))
+    y = run_gemv(fmt, W, x, N, K, qmm.ACT_Q8)
+    xq, s = oracle.quantize_q8(x)
+    ref, absum = oracle.gemv_q8(fmt, W, xq, s, N, K)
+    assert_within(y, ref, absum, f"q8 {name} {N}x{K} B={B}")
+
+
+@pytest.mark.parametrize("xdt", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,K", [(1, 32), (3, 4096), (16, 11008), (7, 7168)])
+def test_quantizer_bitwise(xdt, rows, K):
+    x = synth.normal_f32(31, (rows, K)) if xdt == "f32" else synth.normal_bf16(31, (rows, K))
+    if xdt == "f32":
+        x[0, :32] = np.float32([127, 2.5, -2.5, 3.5, 0.5, 1.5, -0.5, -1.5] * 4)  # exact ties
+        if K >= 64:
+            x[0, 32:64] = 0.0
+    xt = x_tensor(x)
+    xq = torch.empty((rows, K), dtype=torch.int8, device="cuda")
+    s = torch.empty((rows, K // 32), dtype=torch.float32, device="cuda")
+    qmm.quantize_q8(xt, xq, s)
+    torch.cuda.synchronize()
+    rq, rs = oracle.quantize_q8(x)
+    assert np.array_equal(xq.cpu().numpy(), rq)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+def _unit_scale(fmt, N, K, rng):
+    one = pack.f16_bits(1.0)
+    if fmt == qmm.Q6_K:
+        codes = rng.integers(0, 64, (N, K))
+        return pack.pack_q6k_matrix(codes, np.ones((N, K // 16), int),
+                                    np.full((N, K // 256), one)), codes - 32
+    if fmt == qmm.Q4_0:
+        codes = rng.integers(0, 16, (N, K))
+        return pack.pack_q4_0_matrix(codes, np.full((N, K // 32), one)), codes - 8
+    vals = rng.integers(-127, 128, (N, K))
+    return pack.pack_q8_0_matrix(vals, np.full((N, K // 32), one)), vals
+
+
+@pytest.mark.parametrize("name", ["q6_K", "Q4_0", "Q8_0"])
+@pytest.mark.parametrize("B", [1, 8])
+def test_gemv_integer_paths_bitwise(name, B):
+    """d = 1, sub-scales 1, integer activations with amax 127 per 32: the q8
+    path is an exact integer matmul; so is the float path (all partial sums
+    are integers below 2^24). Both must equal the oracle bitwise."""
+    fmt = FMTS[name]
+    N, K = 24, 512
+    rng = np.random.default_rng(fmt * 10 + B)
+    W, wint = _unit_scale(fmt, N, K, rng)
+    xi = rng.integers(-127, 128, (B, K))
+    xi[:, ::32] = 127
+    x = xi.astype(np.float32)
+    exact = (xi @ wint.T).astype(np.float64)
+    y8 = run_gemv(fmt, W, x, N, K, qmm.ACT_Q8)
+    yf = run_gemv(fmt, W, x, N, K, qmm.ACT_FLOAT)
+    xq, s = oracle.quantize_q8(x)
+    r8, _ = oracle.gemv_q8(fmt, W, xq, s, N, K)
+    assert np.array_equal(r8, exact)
+    assert np.array_equal(y8.astype(np.float64), exact)
+    assert np.array_equal(yf.astype(np.float64), exact)
+
+
+def test_gemv_identity_returns_x():
+    n = 512
+    codes = np.full((n, n), 32)
+    np.fill_diagonal(codes, 33)
+    W = pack.pack_q6k_matrix(codes, np.ones((n, n // 16), int),
+                             np.full((n, n // 256), pack.f16_bits(1.0)))
+    x = synth.normal_f32(5, (2, n))
+    y = run_gemv(qmm.Q6_K, W, x, n, n)
+    assert np.array_equal(y, x)
+
+
+def test_q6k_full_size_1024x4096_b1_fp32_all_outputs():
+    """the single-matvec workload: q6_K 1024 x 4096, batch 1, fp32 activations"""
+    N, K = 1024, 4096
+    W = synth.q6k_matrix(synth.workload_seed(0, 0), N, K)
+    x = synth.normal_f32(synth.workload_seed(0, 1), (1, K))
+    y = run_gemv(qmm.Q6_K, W, x, N, K)
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+    assert_within(y, ref, absum, "q6_K 1024x4096")
+    # split-K reduction is deterministic: a second run is bitwise identical
+    y2 = run_gemv(qmm.Q6_K, W, x, N, K)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+DECODE_SET = [("wq", "Q4_0", 4096, 4096), ("w1", "Q4_0", 11008, 4096),
+              ("attn_v", "q6_K", 4096, 4096), ("ffn_down", "q6_K", 4096, 11008),
+              ("output", "q6_K", 32000, 4096), ("wq_q8_0", "Q8_0", 4096, 4096)]
+
+
+@pytest.mark.parametrize("mid", range(len(DECODE_SET)))
+@pytest.mark.parametrize("B", [1, 8])
+@pytest.mark.parametrize("act", ["float", "q8"])
+def test_decode_set_full_size_sampled(mid, B, act):
+    """7B-shaped decode matrices at full size, batch 1 and 8, bf16 activations:
+    512 sampled outputs against the oracle, computed one by one."""
+    name, fmt_name, N, K = DECODE_SET[mid]
+    fmt = FMTS[fmt_name]
+    W = synth.matrix(fmt, synth.workload_seed(1, mid), N, K)
+    x = synth.normal_bf16(synth.workload_seed(1, 8 + B), (B, K))
+    y = run_gemv(fmt, W, x, N, K, qmm.ACT_Q8 if act == "q8" else qmm.ACT_FLOAT)
+    rng = np.random.default_rng(mid)
+    bs = rng.integers(0, B, 512)
+    ns = np.concatenate([rng.integers(0, N, 508), [0, N - 1, N // 2, N - 2]])
+    if act == "float":
+        ref, absum = oracle.gemv_float_pairs(fmt, W, K, x, bs, ns)
+    else:
+        xq, s = oracle.quantize_q8(x)
+        ref, absum = oracle.gemm_q8_pairs(fmt, W, K, xq, s, bs, ns)
+    assert_within(y[bs, ns], ref, absum, f"{name} B={B} {act}")
+    assert np.isfinite(y).all()
+
+
+def test_tail_bytes_and_tiny_shapes():
+    """matrices whose byte size is not a multiple of 16 (tail copied by plain
+    loads) and single-block rows"""
+    for fmt, N, K in [(qmm.Q4_0, 1, 32), (qmm.Q4_0, 3, 64), (qmm.Q8_0, 1, 32),
+                      (qmm.Q8_0, 5, 96), (qmm.Q6_K, 1, 256), (qmm.Q6_K, 3, 512)]:
+        W = synth.matrix(fmt, 7, N, K)
+        for B in (1, 16):
+            x = synth.normal_f32(3, (B, K))
+            y = run_gemv(fmt, W, x, N, K)
+            ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+            assert_within(y, ref, absum, f"tiny fmt={fmt} {N}x{K} B={B}")
+
+
+def test_liveness_counts_each_launch():
+    qmm.liveness_reset()
+    N, K = 64, 4096
+    W = synth.q6k_matrix(1, N, K)
+    x = synth.normal_f32(2, (1, K))
+    run_gemv(qmm.Q6_K, W, x, N, K)
+    run_gemv(qmm.Q6_K, W, x, N, K, qmm.ACT_Q8)
+    live = qmm.liveness()
+    assert live["gemv_float"] == 1 and live["gemv_q8"] == 1 and live["quantize"] == 1
+    assert live["gemv_splitk_reduce"] == 2  # short N is split along K
+
+
+def test_missing_workspace_is_an_error():
+    N, K = 64, 1024
+    Wt = dev(synth.q6k_matrix(1, N, K))
+    xt = x_tensor(synth.normal_f32(2, (1, K)))
+    y = torch.empty((1, N), dtype=torch.float32, device="cuda")
+    qmm.lib.qmm_set_workspace(None, 0)
+    rc = qmm.lib.qmm_gemv(qmm.Q6_K | qmm.ACT_Q8, qmm._ptr(Wt), qmm._ptr(xt), qmm._ptr(y), N, K, 1)
+    assert rc == qmm.ENOWORKSPACE
