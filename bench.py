@@ -145,10 +145,10 @@ def max_over_ranks(world, v: float, device) -> float:
 # ------------------------------------------------------------------ workload
 
 class DecodeSet:
-    def __init__(self, torch, device):
+    def __init__(self, torch, device, act=0):
         import synth
         import block_quantized_weight_q6_gb300 as qmm
-        self.torch, self.qmm, self.device = torch, qmm, device
+        self.torch, self.qmm, self.device, self.act = torch, qmm, device, act
         self.items = []  # (name, fmt, N, K, B, W, x, y)
         self.weight_bytes = 0
         self.algo_bytes = 0
@@ -170,7 +170,7 @@ class DecodeSet:
 
     def run(self):
         for (name, fmt, N, K, B, W, x, y) in self.items:
-            self.qmm.gemv(FMT_CODE[fmt], W, x, y, N, K)
+            self.qmm.gemv(FMT_CODE[fmt], W, x, y, N, K, self.act)
 
 
 def capture(torch, fn, device):
@@ -311,6 +311,14 @@ def main():
     gbs = dec.weight_bytes / (ms_dec * 1e-3) / 1e9
     value = gbs * world
 
+    # the same decode set with per-32 quantized activations (integer dot products)
+    dec8 = DecodeSet(torch, device, act=qmm.ACT_Q8)
+    g_dec8 = capture(torch, dec8.run, device)
+    for _ in range(args.warmup):
+        g_dec8.replay()
+    ms_dec8 = max_over_ranks(world, time_graph(torch, g_dec8, args.steps, device), device)
+    del dec8, g_dec8
+
     # end to end: pinned host activations in, results out, every step
     host_x = [it[6].cpu().pin_memory() for it in dec.items]
     host_y = [torch.empty(it[7].shape, dtype=torch.float32).pin_memory() for it in dec.items]
@@ -361,6 +369,9 @@ def main():
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "hbm_frac_of_measured": gbs / pk["hbm_gbs"],
+            "q8_mode": {"value": dec.weight_bytes / (ms_dec8 * 1e-3) / 1e9 * world, "unit": "GB/s",
+                        "ms_per_step": ms_dec8,
+                        "note": "same decode set, activations quantized per 32 (int8 dot products)"},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

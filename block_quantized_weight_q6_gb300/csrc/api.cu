@@ -128,38 +128,28 @@ int check_fmt(uint32_t fmt, int* wf, bool* bf16, bool* q8) {
 struct GemvPlan {
     int NB, R, splits, cps, nchunks, grid;
     int64_t n_items;
-    size_t ws_xq, ws_xs, ws_part, ws_total;  // workspace byte offsets / total
+    bool xf;                                         // needs the fp32 activation copy
+    size_t ws_xq, ws_xs, ws_xf, ws_part, ws_total;   // workspace byte offsets / total
 };
 
-int occupancy_cached(int fmt, bool q8, int NB, int R) {
-    // [fmt][q8][NB index][R index]
-    static int cache[4][2][5][3];
-    static std::mutex mu;
-    const int nbi = NB == 1 ? 0 : NB == 2 ? 1 : NB == 4 ? 2 : NB == 8 ? 3 : 4;
-    const int ri = R == 1 ? 0 : R == 2 ? 1 : 2;
-    std::lock_guard<std::mutex> lk(mu);
-    int& c = cache[fmt][q8][nbi][ri];
-    if (c == 0) c = gemv_occupancy(fmt, q8, NB, R);
-    return c;
-}
-
-int plan_gemv(int fmt, bool q8, int B, int64_t N, int64_t K, int sms, GemvPlan* p) {
+int plan_gemv(int fmt, bool q8, bool bf16, int B, int64_t N, int64_t K, int sms, GemvPlan* p) {
     p->NB = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
     const int64_t nb = K / block_elems(fmt);
     p->nchunks = static_cast<int>((nb + gemv_chunk_blocks(fmt) - 1) / gemv_chunk_blocks(fmt));
-    int R = p->NB == 1 ? 4 : (p->NB == 2 ? 2 : 1);
-    int occ = occupancy_cached(fmt, q8, p->NB, R);
-    if (R == 4) {
-        // rows grouped by 4 only when that alone fills every warp slot
+    int R = gemv_preferred_rows(q8, p->NB);
+    int occ = gemv_occupancy(fmt, q8, p->NB, R);
+    if (R > 1) {
+        // group rows only while the items still cover most warp slots
         const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
-        if ((N + 3) / 4 < cap) {
+        if ((N + R - 1) / R * p->nchunks * 2 < cap) {
             R = 1;
-            occ = occupancy_cached(fmt, q8, p->NB, R);
+            occ = gemv_occupancy(fmt, q8, p->NB, R);
         }
     }
     if (occ <= 0) return fail(QMM_ECUDA, "gemv kernel (fmt %d, NB %d, R %d) cannot launch", fmt,
                               p->NB, R);
     p->R = R;
+    p->xf = gemv_needs_xf(q8, p->NB, R);
     const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
     const int64_t groups = (N + R - 1) / R;
     int splits = 1;
@@ -174,12 +164,16 @@ int plan_gemv(int fmt, bool q8, int B, int64_t N, int64_t K, int sms, GemvPlan* 
     const int64_t maxg = static_cast<int64_t>(sms) * occ;
     p->grid = static_cast<int>(grid < maxg ? grid : maxg);
     size_t off = 0;
-    p->ws_xq = p->ws_xs = p->ws_part = 0;
+    p->ws_xq = p->ws_xs = p->ws_xf = p->ws_part = 0;
     if (q8) {
         p->ws_xq = off;
         off = round_up(off + static_cast<size_t>(B) * K, 256);
         p->ws_xs = off;
         off = round_up(off + static_cast<size_t>(B) * (K / 32) * 4, 256);
+    }
+    if (p->xf && bf16) {
+        p->ws_xf = off;
+        off = round_up(off + static_cast<size_t>(B) * K * 4, 256);
     }
     if (p->splits > 1) {
         p->ws_part = off;
@@ -242,7 +236,7 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
     GemvPlan p;
-    if ((rc = plan_gemv(wf, q8, B, N, K, d->sms, &p))) return rc;
+    if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
     if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
         return fail(QMM_ENOWORKSPACE, "qmm_gemv needs %zu bytes of workspace, %zu set", p.ws_total,
                     t_ws_bytes);
@@ -270,6 +264,15 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
         e = quantize_q8_launch(x, bf16, B, K, const_cast<int8_t*>(a.xq), const_cast<float*>(a.xs),
                                nullptr, t_stream, d->st);
         if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    }
+    if (p.xf) {
+        if (bf16) {
+            a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
+            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream);
+            if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
+        } else {
+            a.xf = static_cast<const float*>(x);
+        }
     }
     if (p.splits > 1) a.part = reinterpret_cast<float*>(ws + p.ws_part);
     e = gemv_launch(wf, q8, p.NB, p.R, p.grid, t_stream, a);
@@ -379,7 +382,7 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
     DevInfo* d;
     if (dev_info(&d)) return 0;
     GemvPlan p;
-    if (plan_gemv(wf, q8, static_cast<int>(M_or_B), N, K, d->sms, &p)) return 0;
+    if (plan_gemv(wf, q8, bf16, static_cast<int>(M_or_B), N, K, d->sms, &p)) return 0;
     return p.ws_total;
 }
 

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace qmm {
 
 // Weight formats (same numbering as the C interface).
@@ -24,6 +26,24 @@ struct DevState {
     unsigned long long* live;  // liveness counters, one per path label
     unsigned int* err;         // error word
 };
+
+// Launches `kernel` with the programmatic-stream-serialization attribute, so
+// that it may begin while the previous kernel on the stream finishes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
@@ -119,13 +139,27 @@ __device__ __forceinline__ void sts_u8(uint32_t a, uint32_t v) {
 
 // NW consecutive 32-bit words starting at a 2-byte-aligned shared address:
 // NW+1 aligned loads and a funnel shift each.
+template <int OFF>
+__device__ __forceinline__ uint32_t lds_u32_off(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+    return v;
+}
+
+template <int NW, int I = 0>
+__device__ __forceinline__ void lds_words_from(uint32_t base, uint32_t (&t)[NW + 1]) {
+    if constexpr (I <= NW) {
+        t[I] = lds_u32_off<4 * I>(base);
+        lds_words_from<NW, I + 1>(base, t);
+    }
+}
+
 template <int NW>
 __device__ __forceinline__ void lds_words_unaligned(uint32_t a, uint32_t (&w)[NW]) {
     const uint32_t base = a & ~3u;
     const uint32_t sh = (a & 3u) * 8u;
     uint32_t t[NW + 1];
-#pragma unroll
-    for (int i = 0; i <= NW; ++i) t[i] = lds_u32(base + 4u * i);
+    lds_words_from<NW>(base, t);
 #pragma unroll
     for (int i = 0; i < NW; ++i) w[i] = __funnelshift_r(t[i], t[i + 1], sh);
 }
@@ -141,10 +175,51 @@ __device__ __forceinline__ float byte_as_magic_float(uint32_t codes) {
     return __uint_as_float(__byte_perm(codes, 0x4B000000u, 0x7540u + J));
 }
 
+// Packed fp32 pair arithmetic (sm_100 family): one instruction, two lanes.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching, and wait until the kernel this one depends on has completed
+// and its writes are visible (both are no-ops without the launch attribute).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void live_bump(const DevState& st, int slot) {

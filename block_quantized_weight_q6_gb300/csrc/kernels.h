@@ -15,9 +15,8 @@ namespace qmm {
 // blocks of a row (q6_K: 8 super-blocks, Q4_0 / Q8_0: 32 blocks). The warp
 // streams its chunks into a private ring of shared-memory slots with 1-D
 // bulk TMA copies and decodes them from there.
-constexpr int kGemvWarps = 8;
+constexpr int kGemvWarps = 12;
 constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kGemvSlots = 4;
 
 struct GemvArgs {
     const uint8_t* W;
@@ -25,6 +24,7 @@ struct GemvArgs {
     int64_t total_bytes;   // bytes of W (N * nb * block bytes)
     const void* x;         // float mode: [B][K] fp32 or bf16
     int x_bf16;
+    const float* xf;       // float mode, many batch rows: the same activations as fp32
     const int8_t* xq;      // q8 mode: [B][K] int8
     const float* xs;       // q8 mode: [B][K/32] fp32
     int B;
@@ -36,6 +36,24 @@ struct GemvArgs {
     int live_slot;
 };
 
+using GemvKernel = void (*)(const GemvArgs);
+GemvKernel gemv_pick_q6k(bool q8, int NB, int R);
+GemvKernel gemv_pick_q4_0(bool q8, int NB, int R);
+GemvKernel gemv_pick_q8_0(bool q8, int NB, int R);
+
+// rows per item the variants prefer when N is large enough
+inline int gemv_preferred_rows(bool q8, int NB) {
+    (void)q8;
+    (void)NB;
+    return 4;
+}
+// whether the (mode, NB) variant reads its activations from the fp32 copy
+// a.xf (the narrow, many-batch-row float variants)
+inline bool gemv_needs_xf(bool q8, int NB, int R) {
+    (void)R;
+    return !q8 && NB >= 4;
+}
+
 // shared memory bytes of one CTA of the (fmt, R) kernel
 size_t gemv_smem_bytes(int fmt, int R);
 int gemv_chunk_blocks(int fmt);
@@ -45,6 +63,9 @@ cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t 
                         const GemvArgs& a);
 // max resident CTAs per SM for (fmt, q8, NB, R) (0 if not built)
 int gemv_occupancy(int fmt, bool q8, int NB, int R);
+
+// bf16 [n] -> fp32 [n]
+cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s);
 
 cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
                                  cudaStream_t s, DevState st);
