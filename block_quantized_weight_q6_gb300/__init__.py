@@ -157,8 +157,8 @@ def gemv_workspace_bytes(fmt: int, B: int, N: int, K: int, x_bits: int = X_F32,
 
 
 def gemm(fmt: int, W, X, Y, M: int, N: int, K: int, plane=None):
-    """Y[M][N] = quantized-activation GEMM of X[M][K] (bf16) with W."""
-    code = fmt | X_BF16 | ACT_Q8
+    """Y[M][N] = quantized-activation GEMM of X[M][K] (bf16 or fp32) with W."""
+    code = fmt | _act_bits(X) | ACT_Q8
     _prepare(X.device, lib.qmm_workspace_bytes(code, M, N, K))
     with _torch().cuda.device(X.device):
         _check(lib.qmm_gemm(code, _ptr(W), _ptr(X), _ptr(Y), M, N, K, _ptr(plane)))

@@ -15,6 +15,10 @@
 
 using namespace qmm;
 
+namespace qmm {
+bool g_pdl_enabled = true;
+}
+
 // Library state that lives in device memory (one copy per device).
 __device__ unsigned long long g_live[QMM_LIVE_COUNT];
 __device__ unsigned int g_err;
@@ -56,6 +60,8 @@ void read_env() {
     g_env.debug_label = d && std::strcmp(d, "1") == 0;
     const char* f = std::getenv("QMM_FAULT");
     g_env.fault_plane_alloc = f && std::strcmp(f, "plane_alloc") == 0;
+    const char* pdl = std::getenv("QMM_PDL");
+    qmm::g_pdl_enabled = !(pdl && std::strcmp(pdl, "0") == 0);
 }
 
 // ---------------------------------------------------------------- devices
@@ -351,8 +357,64 @@ int qmm_plane_release(const void* W_q6k) {
 int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, int64_t N, int64_t K,
              const int8_t* exp_plane) {
     qmm_init();
-    (void)fmt; (void)W; (void)X; (void)Y; (void)M; (void)N; (void)K; (void)exp_plane;
-    return fail(QMM_EUNSUPPORTED, "qmm_gemm is not built yet");
+    int wf;
+    bool bf16, q8;
+    int rc = check_fmt(fmt, &wf, &bf16, &q8);
+    if (rc) return rc;
+    if (wf == QMM_Q8_0) return fail(QMM_EUNSUPPORTED, "qmm_gemm supports q6_K and Q4_0 weights");
+    if (!W || !X || !Y) return fail(QMM_EINVAL, "null pointer (W %p, X %p, Y %p)", W, X, (void*)Y);
+    if (M <= 0 || N <= 0 || K <= 0) return fail(QMM_EINVAL, "M, N, K must be positive");
+    if (K % block_elems(wf))
+        return fail(QMM_EALIGN, "K = %lld is not a multiple of %d", (long long)K, block_elems(wf));
+    if (!aligned16(W) || !aligned16(X) || !aligned16(Y))
+        return fail(QMM_EALIGN, "W, X and Y must be 16-byte aligned");
+    if (wf == QMM_Q4_0 && exp_plane) return fail(QMM_EINVAL, "Q4_0 has no W_exp plane");
+    // which B path this launch takes ("57 - r54 MINFER_MMQ_Q6K_EXP" section 3.2 labels)
+    int label = QMM_LIVE_GEMM_Q4_0;
+    const char* label_name = "Q4_0 in-kernel-expand";
+    if (wf == QMM_Q6_K) {
+        std::lock_guard<std::mutex> lk(g_planes_mu);
+        auto it = g_planes.find(W);
+        if (exp_plane) {
+            if (it == g_planes.end() || it->second.plane != exp_plane || it->second.N != N ||
+                it->second.K != K)
+                return fail(QMM_EPLANE, "exp_plane %p was not built for W %p (%lld x %lld)",
+                            (const void*)exp_plane, W, (long long)N, (long long)K);
+            label = QMM_LIVE_GEMM_EXP_PLANE;
+            label_name = "W_exp-cp.async";
+        } else if (it != g_planes.end()) {
+            // a plane was wanted for this weight but is not here: failed
+            // allocation, or a caller that lost it -- an accidental fallback
+            label = QMM_LIVE_GEMM_FALLBACK;
+            label_name = "in-kernel-expand(fallback!)";
+        } else if (!g_env.exp_on) {
+            label = QMM_LIVE_GEMM_EXP_OFF;
+            label_name = "in-kernel-expand(exp=off)";
+        } else {
+            label = QMM_LIVE_GEMM_IN_KERNEL;
+            label_name = "in-kernel-expand";
+        }
+    }
+    if (g_env.debug_label)
+        std::fprintf(stderr, "qmm: gemm %s M=%lld N=%lld K=%lld B path: %s\n",
+                     wf == QMM_Q6_K ? "q6_K" : "Q4_0", (long long)M, (long long)N, (long long)K,
+                     label_name);
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    const size_t a16b = round_up(gemm_a16_bytes(M, K), 256);
+    const size_t need = a16b + round_up(static_cast<size_t>(M) * (K / 32) * 4, 256);
+    if (need > t_ws_bytes || !t_ws)
+        return fail(QMM_ENOWORKSPACE, "qmm_gemm needs %zu bytes of workspace, %zu set", need,
+                    t_ws_bytes);
+    uint8_t* ws = static_cast<uint8_t*>(t_ws);
+    uint16_t* a16 = reinterpret_cast<uint16_t*>(ws);
+    float* xs = reinterpret_cast<float*>(ws + a16b);
+    cudaError_t e = quantize_q8_launch(X, bf16, M, K, nullptr, xs, a16, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    e = gemm_launch(wf, exp_plane != nullptr, static_cast<const uint8_t*>(W), exp_plane, a16, xs, Y,
+                    M, N, K, t_stream, d->st, label);
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return QMM_OK;
 }
 
 int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const float* gate_w,
@@ -378,12 +440,18 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
     int wf;
     bool bf16, q8;
     if (check_fmt(fmt, &wf, &bf16, &q8)) return 0;
-    if (M_or_B < 1 || M_or_B > 16 || N <= 0 || K <= 0 || K % block_elems(wf)) return 0;
+    if (M_or_B < 1 || N <= 0 || K <= 0 || K % block_elems(wf)) return 0;
+    // the GEMM's quantized activations (fp16 tiles + scales)
+    size_t gemm = 0;
+    if (wf != QMM_Q8_0)
+        gemm = round_up(gemm_a16_bytes(M_or_B, K), 256) +
+               round_up(static_cast<size_t>(M_or_B) * (K / 32) * 4, 256);
+    if (M_or_B > 16) return gemm;
     DevInfo* d;
-    if (dev_info(&d)) return 0;
+    if (dev_info(&d)) return gemm;
     GemvPlan p;
-    if (plan_gemv(wf, q8, bf16, static_cast<int>(M_or_B), N, K, d->sms, &p)) return 0;
-    return p.ws_total;
+    if (plan_gemv(wf, q8, bf16, static_cast<int>(M_or_B), N, K, d->sms, &p)) return gemm;
+    return p.ws_total > gemm ? p.ws_total : gemm;
 }
 
 int qmm_liveness_read(int64_t* counts, int n) {

@@ -27,6 +27,10 @@ struct DevState {
     unsigned int* err;         // error word
 };
 
+// Whether launches carry the programmatic-dependent-launch attribute
+// (environment QMM_PDL=0 turns it off; read once by qmm_init).
+extern bool g_pdl_enabled;
+
 // Launches `kernel` with the programmatic-stream-serialization attribute, so
 // that it may begin while the previous kernel on the stream finishes.
 template <typename... KArgs, typename... Args>
@@ -41,7 +45,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = g_pdl_enabled ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

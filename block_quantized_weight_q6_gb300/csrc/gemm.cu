@@ -1,0 +1,724 @@
+// gemm.cu -- prefill GEMM against q6_K / Q4_0 weights on the sm_103a tensor
+// cores (tcgen05, accumulators in tensor memory).
+//
+// Y[m][n] = sum_b s_x[m][b] * D[n][b] * I[m][n][b], b = 32-wide K blocks:
+//   q6_K: I = sum_k x_q[m][k] * sc[n][k/16] * (q[n][k] - 32), D = d[n][k/256]
+//   Q4_0: I = sum_k x_q[m][k] * (q[n][k] - 8),               D = d[n][b]
+// The integer partials run on the tensor cores as an fp16 MMA: x_q (|.| <=
+// 127) and sc*(q-32) (|.| <= 1024) are exact fp16 values, every product is an
+// integer below 2^17 and a 32-wide block sums to below 2^22, so the fp32
+// accumulator holds I exactly. The accumulator is drained once per K block
+// and the scales are applied on the CUDA cores.
+//
+// The two q6_K variants of "57 - r54 MINFER_MMQ_Q6K_EXP" section 2.1:
+//   EXP  : the B tile comes from the centered-int8 W_exp plane (one byte per
+//          weight, a plain copy; only the sub-block scale is applied);
+//   !EXP : the B tile is expanded in the kernel from the raw ql / qh bytes.
+// Both write exactly the same fp16 values into the B tile, and everything
+// after that is shared code, so their outputs are bitwise identical (section
+// 2.3: identity by construction).
+//
+// CTA roles (448 threads):
+//   warp 0      producer: 1-D bulk TMA copies of the A tiles (quantized
+//               activations, pre-tiled by the quantizer) and of the raw
+//               weight rows (or plane rows and scales)
+//   warp 1      owns the tensor memory; one lane issues tcgen05.mma
+//   warps 2-5   converters: weights -> fp16 B tile (core-matrix layout)
+//   warps 6-13  epilogue: tcgen05.ld of the accumulator, scaling, output
+#include <cuda_fp16.h>
+
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "kernels.h"
+
+namespace qmm {
+
+namespace {
+
+constexpr int BM = 128;           // tokens per tile (tensor-memory lanes)
+constexpr int BN = 128;           // weight rows per tile (accumulator columns)
+constexpr int NS = 4;             // A / B stages (one 32-wide K block each)
+constexpr int NR = 2;             // raw weight stages (256 columns each)
+constexpr int NBUF = 3;           // accumulator buffers in tensor memory
+constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
+constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
+constexpr int kThreads = 448;
+constexpr int kTmemCols = 512;    // NBUF * BN accumulators + BN for y
+constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
+constexpr int kBTile = BN * 32 * 2;   // bytes of one B stage
+
+// raw stage row strides (16-byte multiples with room for the lead-in)
+constexpr int kRawQ6K = 240;      // one 210-byte super-block
+constexpr int kRawQ40 = 176;      // up to 8 18-byte blocks
+constexpr int kRawPlane = 304;    // 256 plane bytes + 48 for scales and d
+
+struct SmemLayout {
+    uint32_t a, b, raw, dv, bars, tslot, abort_flag;
+    uint32_t total;
+};
+
+__host__ __device__ constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
+    SmemLayout L{};
+    const uint32_t rs = exp ? kRawPlane : (fmt == FMT_Q6_K ? kRawQ6K : kRawQ40);
+    const uint32_t dr = fmt == FMT_Q6_K ? DR_Q6K : DR_Q40;
+    uint32_t o = 0;
+    L.a = o;
+    o += NS * kATile;
+    L.b = o;
+    o += NS * kBTile;
+    L.raw = o;
+    o += NR * BN * rs;
+    L.dv = o;
+    o += dr * BN * 4;
+    o = align_up(o, 8);
+    L.bars = o;
+    o += 8 * (4 * NS + 2 * NR + 2 * NBUF + dr);
+    L.tslot = o;
+    o += 4;
+    L.abort_flag = o;
+    o += 4;
+    L.total = align_up(o, 128);
+    return L;
+}
+
+// barrier indices
+__device__ __forceinline__ uint32_t bar_a_full(uint32_t B, int s) { return B + 8 * s; }
+__device__ __forceinline__ uint32_t bar_b_full(uint32_t B, int s) { return B + 8 * (NS + s); }
+__device__ __forceinline__ uint32_t bar_stage_empty(uint32_t B, int s) { return B + 8 * (2 * NS + s); }
+__device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (3 * NS + r); }
+__device__ __forceinline__ uint32_t bar_raw_empty(uint32_t B, int r) { return B + 8 * (3 * NS + NR + r); }
+__device__ __forceinline__ uint32_t bar_acc_full(uint32_t B, int i) { return B + 8 * (3 * NS + 2 * NR + i); }
+__device__ __forceinline__ uint32_t bar_acc_empty(uint32_t B, int i) {
+    return B + 8 * (3 * NS + 2 * NR + NBUF + i);
+}
+__device__ __forceinline__ uint32_t bar_dv_full(uint32_t B, int i) {
+    return B + 8 * (3 * NS + 2 * NR + 2 * NBUF + i);
+}
+
+// ---------------------------------------------------------------- tcgen05
+
+// Shared-memory matrix descriptor, K-major operand without swizzle: core
+// matrices of 8 rows x 16 bytes, adjacent along K 128 bytes apart (leading
+// byte offset), adjacent 8-row groups 512 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((128u >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version of the sm_100 family
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4)                                 // D format fp32
+           | (0u << 7) | (0u << 10)                  // A, B format fp16
+           | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------- trace
+// Diagnostic builds define QMM_GEMM_TRACE and point qmm_gemm_trace at mapped
+// host memory: each warp records where it is, so a stall can be located from
+// the host while the kernel is still running. Product builds compile it out.
+#ifdef QMM_GEMM_TRACE
+__device__ unsigned* qmm_gemm_trace;
+#define QMM_TRACE(code, kb)                                                                   \
+    do {                                                                                      \
+        if (qmm_gemm_trace && (threadIdx.x & 31) == 0) {                                       \
+            unsigned* t_ = qmm_gemm_trace + (blockIdx.y * gridDim.x + blockIdx.x) * 64 + 4 * (threadIdx.x >> 5); \
+            asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(t_), "r"((unsigned)(code)) : "memory"); \
+            asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(t_ + 1), "r"((unsigned)(kb)) : "memory"); \
+        }                                                                                     \
+    } while (0)
+#else
+#define QMM_TRACE(code, kb) \
+    do {                    \
+    } while (0)
+#endif
+
+// ---------------------------------------------------------------- waits
+
+__device__ __forceinline__ bool aborted(uint32_t flag) { return lds_u32(flag) != 0; }
+
+// Bounded wait that also gives up once another role of the CTA has given up.
+// Warp-collective: every lane of the calling warp polls, and all lanes leave
+// together with the same result, so the warp is converged afterwards (the
+// tensor-memory loads and stores that follow are .sync.aligned).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t flag,
+                                              unsigned int* err) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((it & 63u) == 0) {
+            int give_up = aborted(flag) ? 1 : 0;
+            if (!give_up && globaltimer_ns() - t0 > kWaitLimitNs) give_up = 2;
+            give_up = __shfl_sync(0xffffffffu, give_up, 0);
+            if (give_up) {
+                if (give_up == 2 && (threadIdx.x & 31) == 0) {
+                    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(flag), "r"(1u) : "memory");
+                    atomicOr(err, DERR_GEMM_TIMEOUT);
+                }
+                __syncwarp();
+                return false;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- B tile
+// Converter lane (kc = lane / 8, rw = lane % 8) writes 8 fp16 values: row
+// n = 8 * rg + rw, columns 8 * kc .. + 7 of the 32-wide block, at
+// rg * 512 + kc * 128 + rw * 16 (core-matrix layout; one warp store covers
+// 512 contiguous bytes).
+
+// code bytes (0..63, or 0..15) -> fp16 pairs (1024 + code)
+__device__ __forceinline__ uint32_t half_pair_lo(uint32_t w) { return __byte_perm(w, 0x64646464u, 0x5140); }
+__device__ __forceinline__ uint32_t half_pair_hi(uint32_t w) { return __byte_perm(w, 0x64646464u, 0x7362); }
+
+// fma on fp16 pairs: a * b + c, rounded once
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t half2_bits(float x) {
+    const uint32_t h = __half_as_ushort(__float2half_rn(x));
+    return h | (h << 16);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- kernel
+
+struct GemmArgs {
+    const uint8_t* W;      // q6_K or Q4_0 rows
+    const int8_t* plane;   // W_exp plane (EXP variant)
+    const uint16_t* a16;   // quantized activations as fp16, tiled
+    const float* xs;       // [M][K/32] activation scales
+    float* Y;              // [M][N]
+    int64_t M, N, K, nb;   // nb: blocks per row
+    int64_t total_bytes;   // bytes of W
+    DevState st;
+    int live_slot;
+    float* dbg;            // optional [M][N]: the raw accumulator of the first K block
+};
+
+template <int FMT, bool EXP>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
+    constexpr bool Q6 = (FMT == FMT_Q6_K);
+    constexpr int DR = Q6 ? DR_Q6K : DR_Q40;
+    constexpr int RS = EXP ? kRawPlane : (Q6 ? kRawQ6K : kRawQ40);
+    const SmemLayout L = smem_layout(FMT, EXP);
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t S = smem_u32(smem);
+    const uint32_t BARS = S + L.bars;
+    const uint32_t FLAG = S + L.abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nkb = a.K / 32;
+    const int64_t nsc = (a.K + 255) / 256;  // 256-column super-chunks
+    const int64_t mt = blockIdx.y, nt = blockIdx.x;
+    const int64_t n0 = nt * BN;
+
+    grid_launch_dependents();
+    live_bump(a.st, a.live_slot);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_a_full(BARS, s), 1);
+            mbar_init(bar_b_full(BARS, s), 4);
+            mbar_init(bar_stage_empty(BARS, s), 1);
+        }
+        for (int r = 0; r < NR; ++r) {
+            mbar_init(bar_raw_full(BARS, r), 1);
+            mbar_init(bar_raw_empty(BARS, r), 4);
+        }
+        for (int i = 0; i < NBUF; ++i) {
+            mbar_init(bar_acc_full(BARS, i), 1);
+            mbar_init(bar_acc_empty(BARS, i), 8);
+        }
+        for (int i = 0; i < DR; ++i) mbar_init(bar_dv_full(BARS, i), 4);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(FLAG), "r"(0u) : "memory");
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(S + L.tslot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = lds_u32(S + L.tslot);
+    // the quantized activations come from the previous kernel on the stream
+    grid_dependency_wait();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const int s = static_cast<int>(kb % NS);
+            if ((kb & 7) == 0) {
+                const int64_t sc = kb >> 3;
+                const int r = static_cast<int>(sc % NR);
+                QMM_TRACE(1, kb);
+                if (sc >= NR &&
+                    !wait_or_abort(bar_raw_empty(BARS, r), ((sc / NR) - 1) & 1, FLAG, a.st.err))
+                    break;
+                const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * BN * RS;
+                // this lane's rows: byte ranges and manual tails
+                uint32_t bytes = 0;
+                for (int n = lane; n < BN; n += 32) {
+                    const int64_t ng = n0 + n;
+                    if (ng >= a.N) break;
+                    int64_t st, len;
+                    if (EXP) {
+                        st = (ng * a.nb + sc) * 210 + 192;  // the scales and d of the block
+                        len = 18;
+                        bytes += 256;                       // plane row chunk
+                    } else if (Q6) {
+                        st = (ng * a.nb + sc) * 210;
+                        len = 210;
+                    } else {
+                        const int64_t b0 = sc * 8;
+                        st = (ng * a.nb + b0) * 18;
+                        len = min(static_cast<int64_t>(8), a.nb - b0) * 18;
+                    }
+                    const int64_t s16 = st & ~static_cast<int64_t>(15);
+                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                    if (e16 > s16) bytes += static_cast<uint32_t>(e16 - s16);
+                    const uint32_t rdst = dst0 + n * RS + (EXP ? 256 : 0);
+                    for (int64_t q = max(e16, s16); q < st + len; ++q)
+                        sts_u8(rdst + static_cast<uint32_t>(q - s16), a.W[q]);
+                }
+                fence_proxy_async_smem();
+                bytes = __reduce_add_sync(0xffffffffu, bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar_raw_full(BARS, r), bytes);
+                __syncwarp();
+                for (int n = lane; n < BN; n += 32) {
+                    const int64_t ng = n0 + n;
+                    if (ng >= a.N) break;
+                    int64_t st, len;
+                    if (EXP) {
+                        bulk_g2s(dst0 + n * RS, a.plane + ng * a.K + sc * 256, 256,
+                                 bar_raw_full(BARS, r));
+                        st = (ng * a.nb + sc) * 210 + 192;
+                        len = 18;
+                    } else if (Q6) {
+                        st = (ng * a.nb + sc) * 210;
+                        len = 210;
+                    } else {
+                        const int64_t b0 = sc * 8;
+                        st = (ng * a.nb + b0) * 18;
+                        len = min(static_cast<int64_t>(8), a.nb - b0) * 18;
+                    }
+                    const int64_t s16 = st & ~static_cast<int64_t>(15);
+                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                    if (e16 > s16)
+                        bulk_g2s(dst0 + n * RS + (EXP ? 256 : 0), a.W + s16,
+                                 static_cast<uint32_t>(e16 - s16), bar_raw_full(BARS, r));
+                }
+            }
+            QMM_TRACE(2, kb);
+            if (kb >= NS &&
+                !wait_or_abort(bar_stage_empty(BARS, s), ((kb / NS) - 1) & 1, FLAG, a.st.err))
+                break;
+            QMM_TRACE(3, kb);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar_a_full(BARS, s), kATile);
+                bulk_g2s(S + L.a + s * kATile, a.a16 + (mt * nkb + kb) * (BM * 32), kATile,
+                         bar_a_full(BARS, s));
+            }
+            __syncwarp();
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        constexpr uint32_t idesc = idesc_f16(BM, BN);
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const int s = static_cast<int>(kb % NS);
+            const int ab = static_cast<int>(kb % NBUF);
+            const uint32_t ph = (kb / NS) & 1;
+            QMM_TRACE(10, kb);
+            if (!wait_or_abort(bar_a_full(BARS, s), ph, FLAG, a.st.err)) break;
+            QMM_TRACE(11, kb);
+            if (!wait_or_abort(bar_b_full(BARS, s), ph, FLAG, a.st.err)) break;
+            QMM_TRACE(12, kb);
+            if (kb >= NBUF &&
+                !wait_or_abort(bar_acc_empty(BARS, ab), ((kb / NBUF) - 1) & 1, FLAG, a.st.err))
+                break;
+            QMM_TRACE(13, kb);
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t ad = smem_desc(S + L.a + s * kATile);
+                const uint64_t bd = smem_desc(S + L.b + s * kBTile);
+                const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
+                tc_mma(d, ad, bd, idesc, 0u);
+                tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
+                tc_commit(bar_stage_empty(BARS, s));
+                tc_commit(bar_acc_full(BARS, ab));
+            }
+            __syncwarp();
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ converters
+        const int cw = warp - 2;              // 0..3
+        const int tid = threadIdx.x - 64;     // 0..127: this thread's row for d
+        const int kc = lane >> 3, rw = lane & 7;
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const int s = static_cast<int>(kb % NS);
+            const int64_t sc = kb >> 3;
+            const int j = static_cast<int>(kb & 7);
+            const int r = static_cast<int>(sc % NR);
+            const uint32_t raw0 = S + L.raw + static_cast<uint32_t>(r) * BN * RS;
+            QMM_TRACE(20, kb);
+            if (j == 0 && !wait_or_abort(bar_raw_full(BARS, r), (sc / NR) & 1, FLAG, a.st.err)) break;
+            QMM_TRACE(21, kb);
+            // lead-in of row n's data inside its raw stage row
+            auto lead = [&](int64_t ng) -> uint32_t {
+                if (EXP) return static_cast<uint32_t>(((ng * a.nb + sc) * 210 + 192) & 15);
+                if (Q6) return static_cast<uint32_t>(((ng * a.nb + sc) * 210) & 15);
+                return static_cast<uint32_t>(((ng * a.nb + sc * 8) * 18) & 15);
+            };
+            // d of this thread's row (q6_K: once per super-block, Q4_0: per block)
+            if (Q6 ? (j == 0) : true) {
+                const int di = static_cast<int>(Q6 ? (sc % DR) : (kb % DR));
+                float dval = 0.0f;
+                const int64_t ng = n0 + tid;
+                if (ng < a.N) {
+                    const uint32_t rowb = raw0 + tid * RS + (EXP ? 256 : 0) + lead(ng);
+                    const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * j);
+                    dval = half_bits_to_float(lds_u16(rowb + doff));
+                }
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(S + L.dv + (di * BN + tid) * 4), "f"(dval)
+                             : "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_dv_full(BARS, di));
+            }
+            if (kb >= NS &&
+                !wait_or_abort(bar_stage_empty(BARS, s), ((kb / NS) - 1) & 1, FLAG, a.st.err))
+                break;
+            QMM_TRACE(22, kb);
+            const uint32_t bt = S + L.b + s * kBTile;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int rg = cw + 4 * t;
+                const int n = rg * 8 + rw;
+                const int64_t ng = n0 + n;
+                uint32_t h[4] = {0u, 0u, 0u, 0u};
+                if (ng < a.N) {
+                    const uint32_t rowb = raw0 + n * RS;
+                    const int e = 32 * j + 8 * kc;  // first column of the 8 within the chunk
+                    if (Q6) {
+                        uint32_t c[2];
+                        float scf;
+                        if (EXP) {
+                            // centered int8 plane bytes -> 1152 + v as fp16 pairs
+                            const uint32_t p0 = lds_u32(rowb + e) ^ 0x80808080u;
+                            const uint32_t p1 = lds_u32(rowb + e + 4) ^ 0x80808080u;
+                            c[0] = p0;
+                            c[1] = p1;
+                            scf = static_cast<float>(lds_s8(rowb + 256 + lead(ng) + (e >> 4)));
+                        } else {
+                            const uint32_t rb = rowb + lead(ng);
+                            uint32_t lw[2], hw[2];
+                            lds_words_unaligned<2>(rb + (e & 127), lw);
+                            lds_words_unaligned<2>(rb + 128 + (e & 63), hw);
+                            const uint32_t ns = 4u * static_cast<uint32_t>(e >> 7);
+                            const uint32_t hs = 2u * static_cast<uint32_t>(e >> 6);
+                            c[0] = ((lw[0] >> ns) & 0x0F0F0F0Fu) | (((hw[0] >> hs) & 0x03030303u) << 4);
+                            c[1] = ((lw[1] >> ns) & 0x0F0F0F0Fu) | (((hw[1] >> hs) & 0x03030303u) << 4);
+                            scf = static_cast<float>(lds_s8(rb + 192 + (e >> 4)));
+                        }
+                        // sc * (v - off) exactly: (off + v) * sc - off * sc, one rounding
+                        const float off = EXP ? 1152.0f : 1056.0f;
+                        const uint32_t sc2 = half2_bits(scf);
+                        const uint32_t bias = half2_bits(-off * scf);
+                        h[0] = hfma2_u(half_pair_lo(c[0]), sc2, bias);
+                        h[1] = hfma2_u(half_pair_hi(c[0]), sc2, bias);
+                        h[2] = hfma2_u(half_pair_lo(c[1]), sc2, bias);
+                        h[3] = hfma2_u(half_pair_hi(c[1]), sc2, bias);
+                    } else {
+                        // Q4_0 block j of the chunk: nibbles of qs bytes 8*(kc%2).., nibble kc/2
+                        const uint32_t rb = rowb + lead(ng) + 18 * j;
+                        uint32_t qw[2];
+                        lds_words_unaligned<2>(rb + 2 + 8 * (kc & 1), qw);
+                        const uint32_t ns = 4u * static_cast<uint32_t>(kc >> 1);
+                        const uint32_t c0 = (qw[0] >> ns) & 0x0F0F0F0Fu;
+                        const uint32_t c1 = (qw[1] >> ns) & 0x0F0F0F0Fu;
+                        const uint32_t one = 0x3C003C00u, bias = half2_bits(-1032.0f);
+                        h[0] = hfma2_u(half_pair_lo(c0), one, bias);
+                        h[1] = hfma2_u(half_pair_hi(c0), one, bias);
+                        h[2] = hfma2_u(half_pair_lo(c1), one, bias);
+                        h[3] = hfma2_u(half_pair_hi(c1), one, bias);
+                    }
+                }
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 bt + rg * 512 + kc * 128 + rw * 16),
+                             "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_b_full(BARS, s));
+            if (j == 7 || kb == nkb - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;      // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
+        const int h = (warp - 6) >> 2;  // columns 64*h .. +63 of the tile
+        const int64_t m = mt * BM + 32 * quad + lane;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
+        // q6_K: z (this super-block's s_x-weighted sums) in registers, the
+        // running output y in tensor memory after the accumulator buffers;
+        // Q4_0: y in registers (d changes every block)
+        const uint32_t ty = tl + NBUF * BN + 64 * h;
+        float z[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) z[c] = 0.0f;
+        bool ok = true;
+        for (int64_t kb = 0; kb < nkb; ++kb) {
+            const int ab = static_cast<int>(kb % NBUF);
+            QMM_TRACE(30, kb);
+            if (!wait_or_abort(bar_acc_full(BARS, ab), (kb / NBUF) & 1, FLAG, a.st.err)) {
+                ok = false;
+                break;
+            }
+            QMM_TRACE(31, kb);
+            tc_fence_after();
+            float v[64];
+            tc_ld32(tl + ab * BN + 64 * h, *reinterpret_cast<float(*)[32]>(v));
+            tc_ld32(tl + ab * BN + 64 * h + 32, *reinterpret_cast<float(*)[32]>(v + 32));
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
+            QMM_TRACE(32, kb);
+            if (a.dbg != nullptr && kb == 0 && m < a.M) {
+                for (int c = 0; c < 64; ++c)
+                    if (n0 + 64 * h + c < a.N) a.dbg[m * a.N + n0 + 64 * h + c] = v[c];
+            }
+            const float sx = (m < a.M) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
+            const float2 s2 = make_float2(sx, sx);
+            if (Q6) {
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2, make_float2(z[c], z[c + 1]));
+                    z[c] = t.x;
+                    z[c + 1] = t.y;
+                }
+                if ((kb & 7) == 7 || kb == nkb - 1) {
+                    const int64_t sb = kb >> 3;
+                    const int di = static_cast<int>(sb % DR);
+                    QMM_TRACE(33, kb);
+                    if (!wait_or_abort(bar_dv_full(BARS, di), (sb / DR) & 1, FLAG, a.st.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dv = S + L.dv + (di * BN + 64 * h) * 4;
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float yv[32];
+                        if (sb > 0) {
+                            tc_ld32(ty + 32 * half, yv);
+                            tc_wait_ld();
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) yv[c] = 0.0f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            float2 d2;
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                                         : "=f"(d2.x), "=f"(d2.y)
+                                         : "r"(dv + 4 * (32 * half + c)));
+                            const float2 t = ffma2(d2, make_float2(z[32 * half + c], z[32 * half + c + 1]),
+                                                   make_float2(yv[c], yv[c + 1]));
+                            yv[c] = t.x;
+                            yv[c + 1] = t.y;
+                            z[32 * half + c] = 0.0f;
+                            z[32 * half + c + 1] = 0.0f;
+                        }
+                        tc_st32(ty + 32 * half, yv);
+                    }
+                    tc_wait_st();
+                    QMM_TRACE(34, kb);
+                }
+            } else {
+                const int di = static_cast<int>(kb % DR);
+                if (!wait_or_abort(bar_dv_full(BARS, di), (kb / DR) & 1, FLAG, a.st.err)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dv = S + L.dv + (di * BN + 64 * h) * 4;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float2 d2;
+                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
+                    const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
+                                           make_float2(z[c], z[c + 1]));
+                    z[c] = t.x;  // Q4_0: z holds y
+                    z[c + 1] = t.y;
+                }
+            }
+        }
+        // ok is warp-uniform, so the whole warp takes this branch: the tensor
+        // memory loads are warp-collective and run for every lane; only the
+        // stores depend on the lane's row
+        if (ok) {
+            const int64_t nb0 = n0 + 64 * h;
+            float* out = a.Y + m * a.N + nb0;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float yv[32];
+                if (Q6) {
+                    tc_ld32(ty + 32 * half, yv);
+                    tc_wait_ld();
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) yv[c] = z[32 * half + c];
+                }
+                if (m >= a.M) continue;
+                const int64_t c0 = nb0 + 32 * half;
+                if (c0 + 32 <= a.N && (a.N & 3) == 0) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(out + 32 * half + c) =
+                            make_float4(yv[c], yv[c + 1], yv[c + 2], yv[c + 3]);
+                } else {
+                    for (int c = 0; c < 32; ++c)
+                        if (c0 + c < a.N) out[32 * half + c] = yv[c];
+                }
+            }
+        }
+    }
+    QMM_TRACE(90, nkb);
+    tc_fence_before();
+    __syncthreads();
+    QMM_TRACE(91, nkb);
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- launch
+
+using GemmKernel = void (*)(const GemmArgs);
+
+static GemmKernel pick_gemm(int fmt, bool exp) {
+    if (fmt == FMT_Q6_K) return exp ? gemm_kernel<FMT_Q6_K, true> : gemm_kernel<FMT_Q6_K, false>;
+    if (fmt == FMT_Q4_0 && !exp) return gemm_kernel<FMT_Q4_0, false>;
+    return nullptr;
+}
+
+size_t gemm_a16_bytes(int64_t M, int64_t K) {
+    return static_cast<size_t>((M + BM - 1) / BM * BM) * static_cast<size_t>(K) * 2;
+}
+
+cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
+                        const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t s, DevState st, int live_slot, float* dbg) {
+    GemmKernel k = pick_gemm(fmt, exp);
+    if (!k) return cudaErrorInvalidValue;
+    const SmemLayout L = smem_layout(fmt, exp);
+    static std::mutex mu;
+    static std::map<std::pair<int, GemmKernel>, bool> ready;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!ready[{dev, k}]) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(L.total));
+            if (e != cudaSuccess) return e;
+            ready[{dev, k}] = true;
+        }
+    }
+    GemmArgs a{};
+    a.W = W;
+    a.plane = plane;
+    a.a16 = a16;
+    a.xs = xs;
+    a.Y = Y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.nb = K / (fmt == FMT_Q6_K ? 256 : 32);
+    a.total_bytes = N * a.nb * (fmt == FMT_Q6_K ? 210 : 18);
+    a.st = st;
+    a.live_slot = live_slot;
+    a.dbg = dbg;
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
+    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace qmm

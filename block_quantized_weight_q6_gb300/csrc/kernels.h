@@ -77,6 +77,15 @@ cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_
 cudaError_t quantize_q8_launch(const void* x, int x_bf16, int64_t rows, int64_t K, int8_t* xq,
                                float* xs, uint16_t* a16, cudaStream_t s, DevState st);
 
+// ---------------------------------------------------------------- GEMM
+// bytes of the fp16 A-operand tiles for M x K activations (M rounded up to 128)
+size_t gemm_a16_bytes(int64_t M, int64_t K);
+// fmt FMT_Q6_K (exp: plane variant) or FMT_Q4_0 (exp false)
+cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
+                        const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
+                        int64_t K, cudaStream_t s, DevState st, int live_slot,
+                        float* dbg = nullptr);
+
 // ---------------------------------------------------------------- plane
 cudaError_t plane_build_launch(const uint8_t* W, int64_t N, int64_t K, int8_t* plane,
                                cudaStream_t s, DevState st);

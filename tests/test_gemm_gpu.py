@@ -1,0 +1,229 @@
+"""Prefill GEMM on the GPU (tcgen05) against the CPU oracle, the W_exp plane
+variant against the in-kernel expansion (bitwise), and the path labels.
+
+Float outputs: |Y - Y_ref| <= 1e-4 * sum_k |w_k x^_k| + 1e-6 (x^ = s * x_q).
+Integer cases (unit scales, integer activations with amax 127): bitwise.
+"""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import pack
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import block_quantized_weight_q6_gb300 as qmm  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def x_tensor(x):
+    if x.dtype == np.uint16:
+        return dev(x.view(np.int16)).view(torch.bfloat16)
+    return dev(x)
+
+
+def run_gemm(fmt, W, X, N, K, plane=None, Wt=None):
+    M = X.shape[0]
+    Y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    qmm.gemm(fmt, Wt if Wt is not None else dev(W), x_tensor(X), Y, M, N, K, plane)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    return Y.cpu().numpy()
+
+
+def assert_within(y, ref, absum, what=""):
+    err = np.abs(y.astype(np.float64) - ref)
+    bound = 1e-4 * absum + 1e-6
+    bad = ~(err <= bound)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} out of bound; first {tuple(i)}: "
+                             f"got {y[tuple(i)]}, ref {ref[tuple(i)]}, bound {bound[tuple(i)]}")
+
+
+def unit_q6k(N, K, rng):
+    codes = rng.integers(0, 64, (N, K))
+    W = pack.pack_q6k_matrix(codes, np.ones((N, K // 16), int),
+                             np.full((N, K // 256), pack.f16_bits(1.0)))
+    return W, codes - 32
+
+
+def int_acts(M, K, rng):
+    xi = rng.integers(-127, 128, (M, K))
+    xi[:, ::32] = 127
+    return xi, xi.astype(np.float32)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (200, 136, 512), (1, 8, 256), (300, 260, 768)])
+def test_q6k_gemm_unit_scale_bitwise(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    W, wint = unit_q6k(N, K, rng)
+    xi, X = int_acts(M, K, rng)
+    exact = (xi @ wint.T).astype(np.float64)
+    Y2 = run_gemm(qmm.Q6_K, W, X, N, K)
+    assert np.array_equal(Y2.astype(np.float64), exact)
+    Wt = dev(W)
+    plane = qmm.plane_build(Wt, N, K)
+    Y1 = run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)
+    qmm.plane_release(Wt)
+    assert np.array_equal(Y1.astype(np.float64), exact)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (130, 96, 512), (257, 300, 1024)])
+def test_q4_0_gemm_unit_scale_bitwise(M, N, K):
+    rng = np.random.default_rng(7 * M + N)
+    codes = rng.integers(0, 16, (N, K))
+    W = pack.pack_q4_0_matrix(codes, np.full((N, K // 32), pack.f16_bits(1.0)))
+    xi, X = int_acts(M, K, rng)
+    Y = run_gemm(qmm.Q4_0, W, X, N, K)
+    assert np.array_equal(Y.astype(np.float64), (xi @ (codes - 8).T).astype(np.float64))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 1024), (77, 130, 2048)])
+def test_q6k_gemm_random_plane_equals_in_kernel_and_oracle(M, N, K):
+    W = synth.q6k_matrix(11 + M, N, K)
+    X = synth.normal_bf16(12 + M, (M, K))
+    Wt = dev(W)
+    Y2 = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    plane = qmm.plane_build(Wt, N, K)
+    Y1 = run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)
+    qmm.plane_release(Wt)
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32)), "W_exp and in-kernel differ"
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemv_q8(qmm.Q6_K, W, xq, s, N, K)
+    assert_within(Y2, ref, absum, f"q6_K gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 512), (200, 72, 4096)])
+def test_q4_0_gemm_random(M, N, K):
+    W = synth.q4_0_matrix(21 + M, N, K)
+    X = synth.normal_bf16(22 + M, (M, K))
+    Y = run_gemm(qmm.Q4_0, W, X, N, K)
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemv_q8(qmm.Q4_0, W, xq, s, N, K)
+    assert_within(Y, ref, absum, f"Q4_0 gemm {M}x{N}x{K}")
+
+
+def test_gemm_rows_match_q8_gemv():
+    """a GEMM row is the q8-activation matvec of that row (same definition)"""
+    N, K = 256, 1024
+    W = synth.q6k_matrix(31, N, K)
+    X = synth.normal_bf16(32, (16, K))
+    Wt = dev(W)
+    Y = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    y = torch.empty((16, N), dtype=torch.float32, device="cuda")
+    qmm.gemv(qmm.Q6_K, Wt, x_tensor(X), y, N, K, qmm.ACT_Q8)
+    torch.cuda.synchronize()
+    xq, s = oracle.quantize_q8(X)
+    _, absum = oracle.gemv_q8(qmm.Q6_K, W, xq, s, N, K)
+    assert (np.abs(Y.astype(np.float64) - y.cpu().numpy()) <= 2e-4 * absum + 2e-6).all()
+
+
+def test_plane_build_bitwise():
+    N, K = 96, 768
+    W = synth.q6k_matrix(41, N, K)
+    Wt = dev(W)
+    plane = qmm.plane_build(Wt, N, K)
+    torch.cuda.synchronize()
+    qmm.plane_release(Wt)
+    assert np.array_equal(plane.cpu().numpy(), oracle.plane_q6k(W, N, K))
+
+
+def test_full_size_ffn_down_prefill_sampled():
+    """q6_K ffn_down 4096 x 11008, 512 bf16 tokens: both variants bitwise
+    identical; 1024 sampled outputs against the oracle."""
+    M, N, K = 512, 4096, 11008
+    W = synth.q6k_matrix(synth.workload_seed(2, 0), N, K)
+    X = synth.normal_bf16(synth.workload_seed(2, 1), (M, K))
+    Wt = dev(W)
+    Y2 = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    plane = qmm.plane_build(Wt, N, K)
+    Y1 = run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)
+    qmm.plane_release(Wt)
+    del plane
+    assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32))
+    rng = np.random.default_rng(5)
+    ms = np.concatenate([rng.integers(0, M, 1020), [0, M - 1, 0, M - 1]])
+    ns = np.concatenate([rng.integers(0, N, 1020), [0, N - 1, N - 1, 0]])
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemm_q8_pairs(qmm.Q6_K, W, K, xq, s, ms, ns)
+    assert_within(Y2[ms, ns], ref, absum, "ffn_down prefill")
+    assert np.isfinite(Y2).all()
+
+
+def test_labels_and_plane_errors():
+    N, K, M = 64, 512, 16
+    W = synth.q6k_matrix(51, N, K)
+    X = synth.normal_bf16(52, (M, K))
+    Wt = dev(W)
+    qmm.liveness_reset()
+    run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)                 # never registered: in-kernel
+    plane = qmm.plane_build(Wt, N, K)
+    run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)    # the plane path
+    run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)                 # plane exists but not passed
+    live = qmm.liveness()
+    assert live["gemm_in_kernel"] == 1 and live["gemm_exp_plane"] == 1
+    assert live["gemm_fallback"] == 1 and live["plane_build"] == 1
+    # a plane of other geometry is refused, never used silently
+    Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.gemm(qmm.Q6_K, Wt, x_tensor(X), Y, M, N // 2, K, plane)
+    assert ei.value.code == qmm.EPLANE
+    other = torch.zeros_like(plane)
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.gemm(qmm.Q6_K, Wt, x_tensor(X), Y, M, N, K, other)
+    assert ei.value.code == qmm.EPLANE
+    qmm.plane_release(Wt)
+    # registration that could not allocate: later launches count as fallback
+    qmm.liveness_reset()
+    qmm.plane_register_failed(Wt, N, K)
+    run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    assert qmm.liveness()["gemm_fallback"] == 1
+    qmm.plane_release(Wt)
+
+
+def _fresh(code, env_extra):
+    env = dict(os.environ)
+    env.update(env_extra)
+    return subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                          text=True, timeout=300)
+
+
+def test_exp_off_label_and_fault_injection_in_fresh_processes():
+    code = r"""
+import numpy as np, torch, synth, block_quantized_weight_q6_gb300 as qmm
+N, K, M = 64, 512, 8
+W = torch.from_numpy(synth.q6k_matrix(1, N, K)).cuda()
+X = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+Y = torch.empty(M, N, device="cuda")
+qmm.liveness_reset()
+wanted = qmm.plane_wanted(N, K)
+if wanted:
+    qmm.plane_build(W, N, K)      # QMM_FAULT=plane_alloc: recorded as a failed allocation
+qmm.gemm(qmm.Q6_K, W, X, Y, M, N, K, None)
+torch.cuda.synchronize()
+l = qmm.liveness()
+print(int(wanted), l["gemm_exp_off"], l["gemm_fallback"], l["gemm_in_kernel"], l["gemm_exp_plane"])
+"""
+    r = _fresh(code, {"QMM_Q6K_EXP": "0", "QMM_DEBUG_LABEL": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == ["0", "1", "0", "0", "0"]
+    assert "in-kernel-expand(exp=off)" in r.stderr
+    r = _fresh(code, {"QMM_FAULT": "plane_alloc", "QMM_DEBUG_LABEL": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split() == ["1", "0", "1", "0", "0"]
+    assert "fallback!" in r.stderr
