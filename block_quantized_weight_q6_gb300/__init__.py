@@ -56,6 +56,7 @@ def _load():
         "qmm_workspace_bytes": (SZ, [U32, I64, I64, I64]),
         "qmm_gemv": (I, [U32, P, P, P, I64, I64, I]),
         "qmm_quantize_q8": (I, [U32, P, I64, I64, P, P]),
+        "qmm_gemv_noalloc": (I, [U32, P, P, P, I64, I64, I]),
         "qmm_gemm": (I, [U32, P, P, P, I64, I64, I64, P]),
         "qmm_plane_bytes": (SZ, [I64, I64]),
         "qmm_plane_wanted": (I, [I64, I64]),

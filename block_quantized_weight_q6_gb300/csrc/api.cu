@@ -23,6 +23,10 @@ bool g_pdl_enabled = true;
 __device__ unsigned long long g_live[QMM_LIVE_COUNT];
 __device__ unsigned int g_err;
 
+// Scratch of qmm_gemv_noalloc: a fixed array in device memory (one copy per
+// device that loads the library), so that entry point never allocates.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QMM_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 thread_local cudaStream_t t_stream = nullptr;
@@ -493,6 +497,88 @@ int qmm_sync_check(void) {
         unsigned int zero = 0;
         cudaMemcpy(d->st.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
         return fail(QMM_EDEVICE_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", err);
+    }
+    return QMM_OK;
+}
+
+// The device address of g_noalloc_scratch on the current device, looked up
+// once per device (host code cannot use the symbol itself as an address).
+static int noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[kMaxDev] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDev) return fail(QMM_EUNSUPPORTED, "device ordinal %d", dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return QMM_OK;
+}
+
+int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, int64_t K,
+                     int B) {
+    qmm_init();
+    int wf;
+    bool bf16, q8;
+    int rc = check_gemv_args(fmt, W, x, y, N, K, B, &wf, &bf16, &q8);
+    if (rc) return rc;
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    GemvPlan p;
+    if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
+    if (p.ws_total > QMM_NOALLOC_SCRATCH_BYTES)
+        return fail(QMM_ENOWORKSPACE,
+                    "qmm_gemv_noalloc: this shape needs %zu bytes of scratch, the fixed array "
+                    "holds %u",
+                    p.ws_total, QMM_NOALLOC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch))) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(scratch);
+    GemvArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.N = N;
+    a.K = K;
+    a.nb = K / block_elems(wf);
+    a.total_bytes = N * a.nb * block_bytes(wf);
+    a.x = x;
+    a.x_bf16 = bf16;
+    a.B = B;
+    a.y = y;
+    a.splits = p.splits;
+    a.cps = p.cps;
+    a.nchunks = p.nchunks;
+    a.n_items = p.n_items;
+    a.st = d->st;
+    a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
+    cudaError_t e;
+    if (q8) {
+        a.xq = reinterpret_cast<int8_t*>(ws + p.ws_xq);
+        a.xs = reinterpret_cast<float*>(ws + p.ws_xs);
+        e = quantize_q8_launch(x, bf16, B, K, const_cast<int8_t*>(a.xq), const_cast<float*>(a.xs),
+                               nullptr, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    }
+    if (p.xf) {
+        if (bf16) {
+            a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
+            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream);
+            if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
+        } else {
+            a.xf = static_cast<const float*>(x);
+        }
+    }
+    if (p.splits > 1) a.part = reinterpret_cast<float*>(ws + p.ws_part);
+    e = gemv_launch(wf, q8, p.NB, p.R, p.grid, t_stream, a);
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    if (p.splits > 1) {
+        e = splitk_reduce_launch(a.part, y, p.splits, static_cast<int64_t>(B) * N, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }
     return QMM_OK;
 }

@@ -131,6 +131,30 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
 int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
              int64_t K, int B);
 
+/* Size of the fixed scratch array that qmm_gemv_noalloc uses (4 MiB). */
+#define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* The same batched matvec as qmm_gemv (same arguments, same kernels, same
+ * results), for callers that cannot allocate device memory when they call:
+ * code hosted by an engine or framework that owns all device memory and
+ * hands out only the input and output buffers, and latency-critical loops
+ * that must not call into an allocator after start-up (cudaMalloc can block
+ * on locks and synchronize the device). It needs no workspace: its scratch
+ * (split-K partial sums, quantized or fp32 activation copies) lives in a
+ * fixed array of QMM_NOALLOC_SCRATCH_BYTES that the library keeps in device
+ * memory on every GPU that loads it, until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ * The first call on each device looks up that array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Shapes whose scratch would exceed the array are refused with
+ * QMM_ENOWORKSPACE before anything is launched. Every call uses the same
+ * array and leaves its contents behind (each call overwrites what it reads),
+ * so two calls that run at the same time on the GPU (e.g. on two streams)
+ * race: keep them ordered on one stream. The pages have no counterpart to
+ * this entry point. */
+int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
+                     int64_t K, int B);
+
 /* The per-32 activation quantizer on its own (the first step of QMM_ACT_Q8
  * and of qmm_gemm): x [rows][K] of type x_type (QMM_X_F32 or QMM_X_BF16),
  * K % 32 == 0 -> xq [rows][K] int8 and s [rows][K/32] fp32 with
