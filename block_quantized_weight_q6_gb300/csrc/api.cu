@@ -424,19 +424,64 @@ int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, in
 int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const float* gate_w,
              const void* x, float* y) {
     qmm_init();
-    (void)fmt; (void)experts; (void)idx; (void)gate_w; (void)x; (void)y;
-    return fail(QMM_EUNSUPPORTED, "moe_gemv is not built yet");
+    int wf;
+    bool bf16, q8;
+    int rc = check_fmt(fmt, &wf, &bf16, &q8);
+    if (rc) return rc;
+    if (q8) return fail(QMM_EUNSUPPORTED, "moe_gemv runs in float activation mode");
+    if (!experts || !experts->w_gate || !experts->w_up || !experts->w_down)
+        return fail(QMM_EINVAL, "null expert table");
+    const qmm_moe_t& m = *experts;
+    if (m.n_experts < 1 || m.n_experts > kMoeMaxExperts)
+        return fail(QMM_EINVAL, "n_experts = %d outside 1..%d", m.n_experts, kMoeMaxExperts);
+    if (m.hidden <= 0 || m.inter <= 0 || m.n_tokens <= 0)
+        return fail(QMM_EINVAL, "hidden, inter and n_tokens must be positive");
+    if (m.top_k < 1 || m.top_k > 32 || m.top_k > m.n_experts)
+        return fail(QMM_EINVAL, "top_k = %d outside 1..min(32, n_experts)", m.top_k);
+    if (static_cast<int64_t>(m.n_tokens) * m.top_k > kMoeMaxSlots)
+        return fail(QMM_EINVAL, "n_tokens * top_k = %lld exceeds %d per call",
+                    static_cast<long long>(m.n_tokens) * m.top_k, kMoeMaxSlots);
+    if (m.hidden % block_elems(wf) || m.inter % block_elems(wf))
+        return fail(QMM_EALIGN, "hidden and inter must be multiples of %d", block_elems(wf));
+    if (!idx || !gate_w || !x || !y) return fail(QMM_EINVAL, "null idx, gate_w, x or y");
+    if (!aligned16(x)) return fail(QMM_EALIGN, "x must be 16-byte aligned");
+    for (int e = 0; e < m.n_experts; ++e)
+        if (!m.w_gate[e] || !m.w_up[e] || !m.w_down[e] || !aligned16(m.w_gate[e]) ||
+            !aligned16(m.w_up[e]) || !aligned16(m.w_down[e]))
+            return fail(QMM_EALIGN, "expert %d: matrices must be non-null and 16-byte aligned", e);
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    const size_t need = moe_workspace_bytes(m.n_tokens, m.top_k, m.hidden, m.inter, bf16);
+    if (need > t_ws_bytes || !t_ws)
+        return fail(QMM_ENOWORKSPACE, "moe_gemv needs %zu bytes of workspace, %zu set", need,
+                    t_ws_bytes);
+    cudaError_t e = moe_launch(wf, m.n_experts, m.hidden, m.inter, m.n_tokens, m.top_k, m.w_gate,
+                               m.w_up, m.w_down, idx, gate_w, x, bf16, y, t_ws, d->sms, t_stream,
+                               d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe launch");
+    return QMM_OK;
 }
 
 size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts) {
-    (void)experts;
-    return 0;
+    if (!experts || experts->n_tokens <= 0 || experts->top_k <= 0 || experts->hidden <= 0 ||
+        experts->inter <= 0)
+        return 0;
+    return moe_workspace_bytes(experts->n_tokens, experts->top_k, experts->hidden, experts->inter,
+                               false);
 }
 
 int qmm_route_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx, float* gate_w) {
     qmm_init();
-    (void)logits; (void)T; (void)E; (void)k; (void)idx; (void)gate_w;
-    return fail(QMM_EUNSUPPORTED, "routing is not built yet");
+    if (!logits || !idx || !gate_w) return fail(QMM_EINVAL, "null pointer");
+    if (T < 1 || E < 1 || E > kMoeMaxExperts)
+        return fail(QMM_EINVAL, "T = %d, E = %d (1 <= E <= %d)", T, E, kMoeMaxExperts);
+    if (k < 1 || k > 32 || k > E) return fail(QMM_EINVAL, "k = %d outside 1..min(32, E)", k);
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = route_launch(logits, T, E, k, idx, gate_w, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    return QMM_OK;
 }
 
 size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
@@ -496,6 +541,9 @@ int qmm_sync_check(void) {
     if (err) {
         unsigned int zero = 0;
         cudaMemcpy(d->st.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (err & DERR_MOE_BAD_INDEX)
+            return fail(QMM_EINVAL, "moe_gemv: an expert index was outside 0..n_experts-1; "
+                                    "its slot contributed nothing (flags 0x%x)", err);
         return fail(QMM_EDEVICE_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", err);
     }
     return QMM_OK;

@@ -19,6 +19,7 @@ enum : uint32_t {
     DERR_GEMV_TIMEOUT = 1u << 0,
     DERR_GEMM_TIMEOUT = 1u << 1,
     DERR_MOE_TIMEOUT = 1u << 2,
+    DERR_MOE_BAD_INDEX = 1u << 3,
 };
 
 // Pointers to the library's device-resident state, passed to every kernel.

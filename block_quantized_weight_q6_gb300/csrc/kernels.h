@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "qmm.h"
 
 namespace qmm {
 
@@ -85,6 +86,21 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t s, DevState st, int live_slot,
                         float* dbg = nullptr);
+
+// ---------------------------------------------------------------- MoE
+constexpr int kMoeMaxExperts = 1024;
+constexpr int kMoeMaxSlots = 1024;  // tokens x top_k per call
+constexpr int QMM_LIVE_ROUTE_SLOT = QMM_LIVE_ROUTE;
+constexpr int QMM_LIVE_MOE_GATE_UP_SLOT = QMM_LIVE_MOE_GATE_UP;
+constexpr int QMM_LIVE_MOE_DOWN_SLOT = QMM_LIVE_MOE_DOWN;
+constexpr int QMM_LIVE_MOE_COMBINE_SLOT = QMM_LIVE_MOE_COMBINE;
+size_t moe_workspace_bytes(int T, int k, int H, int I, bool x_bf16);
+cudaError_t moe_launch(int fmt, int E, int H, int I, int T, int k, const void* const* wg,
+                       const void* const* wu, const void* const* wd, const int32_t* idx,
+                       const float* gate, const void* x, int x_bf16, float* y, void* ws, int sms,
+                       cudaStream_t s, DevState st);
+cudaError_t route_launch(const float* logits, int T, int E, int k, int32_t* idx, float* gate,
+                         cudaStream_t s, DevState st);
 
 // ---------------------------------------------------------------- plane
 cudaError_t plane_build_launch(const uint8_t* W, int64_t N, int64_t K, int8_t* plane,

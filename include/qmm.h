@@ -238,8 +238,9 @@ int qmm_route_topk_softmax(const float* logits, int T, int E, int k, int32_t* id
 int qmm_liveness_read(int64_t* counts, int n);
 int qmm_liveness_reset(void);
 
-/* Synchronizes the current stream and reports QMM_EDEVICE_TIMEOUT if any
- * kernel gave up a bounded wait since the last check (the flag is cleared). */
+/* Synchronizes the current stream and reports what kernels flagged since the
+ * last check (the flags are cleared): QMM_EDEVICE_TIMEOUT if a kernel gave up
+ * a bounded wait, QMM_EINVAL if moe_gemv met an expert index out of range. */
 int qmm_sync_check(void);
 
 /* Reason for the calling thread's last non-OK return. */

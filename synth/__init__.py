@@ -155,3 +155,29 @@ def normal_bf16(seed: int, shape) -> np.ndarray:
 
 def workload_seed(config_id: int, matrix_id: int) -> int:
     return 0x5EED0000 + config_id * 16 + matrix_id
+
+
+def matrix_torch(fmt: int, seed: int, N: int, K: int, device, count: int = 1):
+    """`count` N x K matrices of format `fmt` drawn on `device` with torch's
+    seeded generator (for workloads too large to draw on the host): the same
+    per-field distributions as the numpy generators above, but a different
+    random stream. Returns a uint8 tensor [count, bytes per matrix]."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed & 0x7FFFFFFFFFFFFFFF)
+    be, bb = BLOCK_ELEMS[fmt], BLOCK_BYTES[fmt]
+    nb = N * (K // be)
+    out = torch.randint(0, 256, (count, nb, bb), dtype=torch.uint8, device=device, generator=g)
+    d = (torch.randn((count, nb), generator=g, device=device).abs() * 2e-4).half()
+    d_bytes = d.view(torch.uint8).view(count, nb, 2)
+    if fmt == Q6_K:
+        sc = torch.randint(-32, 32, (count, nb, 16), dtype=torch.int8, device=device, generator=g)
+        out[:, :, 192:208] = sc.view(torch.uint8)
+        out[:, :, 208:210] = d_bytes
+    elif fmt == Q4_0:
+        out[:, :, 0:2] = d_bytes
+    else:
+        qs = torch.randint(-127, 128, (count, nb, 32), dtype=torch.int8, device=device, generator=g)
+        out[:, :, 2:34] = qs.view(torch.uint8)
+        out[:, :, 0:2] = d_bytes
+    return out.view(count, nb * bb)
