@@ -1,15 +1,19 @@
 #!/usr/bin/env python3
 """Benchmark of the block-quantized matmul hot path on GB300.
 
-One step = one pass of the hot path over one batch of seeded synthetic input:
-  decode: the 7B-shaped decode matvec set (Q4_0 wq/wk/wo 4096x4096, w1/w3
+One step = one pass of the whole hot path over one batch of seeded synthetic
+input, each part replayed from its own CUDA graph of public-API calls:
+  decode  the 7B-shaped decode matvec set (Q4_0 wq/wk/wo 4096x4096, w1/w3
           11008x4096; q6_K attn_v 4096x4096, ffn_down 4096x11008, output
           32000x4096; Q8_0 wq 4096x4096), bf16 activations, batch 1 and 8,
           float activation mode; each batch size streams its own copy of the
-          weights (510 MB per step > the 129 MB L2, so every step reads HBM).
-The headline value is the decode set's weight bytes divided by the time of
-the decode part of the step (weight GB/s). Steps are replayed from a CUDA
-graph of the public API calls.
+          weights (510 MB per step, larger than the 129 MB L2);
+  gemm    prefill GEMM, q6_K ffn_down 4096x11008, 512 bf16 tokens quantized
+          per 32, with the W_exp plane and with in-kernel expansion;
+  moe     routed expert FFN, 256 Q4_0 experts (hidden 7168, intermediate
+          2048, 6.3 GB resident), top-8 softmax routing, 1 and 16 tokens.
+The headline value is the decode set's weight bytes over the decode part's
+time (weight GB/s); the GEMM's TOPS and the MoE's GB/s are reported beside it.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Prints one JSON line (rank 0).
@@ -173,6 +177,75 @@ class DecodeSet:
             self.qmm.gemv(FMT_CODE[fmt], W, x, y, N, K, self.act)
 
 
+class GemmCase:
+    """q6_K ffn_down prefill: M=512 bf16 tokens, N=4096, K=11008."""
+    M, N, K = 512, 4096, 11008
+
+    def __init__(self, torch, device):
+        import synth
+        import block_quantized_weight_q6_gb300 as qmm
+        self.torch, self.qmm = torch, qmm
+        W = synth.q6k_matrix(synth.workload_seed(2, 0), self.N, self.K)
+        self.W = torch.from_numpy(W).to(device)
+        X = synth.normal_bf16(synth.workload_seed(2, 1), (self.M, self.K))
+        self.X = torch.from_numpy(X.view(np.int16)).to(device).view(torch.bfloat16)
+        self.Y1 = torch.empty((self.M, self.N), dtype=torch.float32, device=device)
+        self.Y2 = torch.empty_like(self.Y1)
+        torch.cuda.synchronize(device)
+        free0 = torch.cuda.mem_get_info(device)[0]
+        self.plane = qmm.plane_build(self.W, self.N, self.K)
+        torch.cuda.synchronize(device)
+        self.plane_delta = free0 - torch.cuda.mem_get_info(device)[0]
+        self.ops = 2 * self.M * self.N * self.K
+
+    def run_exp(self):
+        self.qmm.gemm(self.qmm.Q6_K, self.W, self.X, self.Y1, self.M, self.N, self.K, self.plane)
+
+    def run_in_kernel(self):
+        self.qmm.gemm(self.qmm.Q6_K, self.W, self.X, self.Y2, self.M, self.N, self.K, None)
+
+
+class MoeWeights:
+    """256 Q4_0 experts (gate/up 2048x7168, down 7168x2048) resident in HBM."""
+    E, H, I, k = 256, 7168, 2048, 8
+
+    def __init__(self, torch, device):
+        import synth
+        E, H, I = self.E, self.H, self.I
+        self.g = synth.matrix_torch(synth.Q4_0, synth.workload_seed(3, 0), I, H, device, E)
+        self.u = synth.matrix_torch(synth.Q4_0, synth.workload_seed(3, 1), I, H, device, E)
+        self.d = synth.matrix_torch(synth.Q4_0, synth.workload_seed(3, 2), H, I, device, E)
+
+
+class MoeCase:
+    """Routed expert FFN over MoeWeights: top-8 of 256 N(0,1) router logits,
+    softmax gates; T tokens of bf16 N(0,1)."""
+
+    def __init__(self, torch, device, wts, T):
+        import synth
+        import block_quantized_weight_q6_gb300 as qmm
+        self.torch, self.qmm, self.T, self.k = torch, qmm, T, wts.k
+        E, H, I = wts.E, wts.H, wts.I
+        self.experts = qmm.moe_experts(list(wts.g), list(wts.u), list(wts.d), H, I, self.k, T)
+        self.logits = torch.from_numpy(
+            synth.normal_f32(synth.workload_seed(3, 10 + T), (T, E))).to(device)
+        x = synth.normal_bf16(synth.workload_seed(3, 20 + T), (T, H))
+        self.x = torch.from_numpy(x.view(np.int16)).to(device).view(torch.bfloat16)
+        self.idx = torch.empty((T, self.k), dtype=torch.int32, device=device)
+        self.gate = torch.empty((T, self.k), dtype=torch.float32, device=device)
+        self.y = torch.empty((T, H), dtype=torch.float32, device=device)
+        self.expert_bytes = 2 * synth.matrix_bytes(synth.Q4_0, I, H) + synth.matrix_bytes(
+            synth.Q4_0, H, I)
+        qmm.route_topk_softmax(self.logits, self.k, self.idx, self.gate)
+        torch.cuda.synchronize(device)
+        self.distinct = len(set(self.idx.cpu().numpy().ravel().tolist()))
+        self.bytes = self.distinct * self.expert_bytes
+
+    def run(self):
+        self.qmm.route_topk_softmax(self.logits, self.k, self.idx, self.gate)
+        self.qmm.moe(self.qmm.Q4_0, self.experts, self.idx, self.gate, self.x, self.y)
+
+
 def capture(torch, fn, device):
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream(device))
@@ -290,26 +363,59 @@ def main():
     pk = peaks()
 
     dec = DecodeSet(torch, device)
-    g_dec = capture(torch, dec.run, device)
+    gem = GemmCase(torch, device)
+    moe_w = MoeWeights(torch, device)
+    moe1 = MoeCase(torch, device, moe_w, 1)
+    moe16 = MoeCase(torch, device, moe_w, 16)
+    # writing this buffer evicts the 129 MB L2 between the parts of a step
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    # the step's parts, each as one CUDA graph
+    parts = [("decode", dec.run), ("gemm_exp_plane", gem.run_exp),
+             ("gemm_in_kernel", gem.run_in_kernel), ("moe_t1", moe1.run), ("moe_t16", moe16.run)]
+    graphs = [(name, capture(torch, fn, device)) for name, fn in parts]
     for _ in range(args.warmup):
-        g_dec.replay()
+        for _, g in graphs:
+            flush.zero_()
+            g.replay()
     torch.cuda.synchronize(device)
 
-    # launches of our kernels per step, from the kernels' own liveness counters
+    # launches of our kernels per step, counted by the kernels themselves
     qmm.liveness_reset()
-    g_dec.replay()
+    for _, g in graphs:
+        g.replay()
     torch.cuda.synchronize(device)
     launches_per_step = sum(qmm.liveness().values())
 
+    # timed region: K steps; a pair of events around each part (the L2 flush
+    # before each part lies outside them)
     barrier(world)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in graphs] for _ in range(args.steps)]
     with ClockSampler(local) as clk:
-        ms_dec = time_graph(torch, g_dec, args.steps, device)
+        torch.cuda.synchronize(device)
+        for st in range(args.steps):
+            for i, (_, g) in enumerate(graphs):
+                flush.zero_()
+                ev[st][i][0].record()
+                g.replay()
+                ev[st][i][1].record()
+        torch.cuda.synchronize(device)
     barrier(world)
-    ms_dec = max_over_ranks(world, ms_dec, device)
     clocks = clk.summary()
+    part_ms = {}
+    for i, (name, _) in enumerate(graphs):
+        t = sum(ev[st][i][0].elapsed_time(ev[st][i][1]) for st in range(args.steps)) / args.steps
+        part_ms[name] = max_over_ranks(world, t, device)
+    step_ms = sum(part_ms.values())
 
+    ms_dec = part_ms["decode"]
     gbs = dec.weight_bytes / (ms_dec * 1e-3) / 1e9
     value = gbs * world
+    tops = {n: gem.ops / (part_ms[n] * 1e-3) / 1e12 for n in ("gemm_exp_plane", "gemm_in_kernel")}
+    moe_gbs = {"moe_t1": moe1.bytes / (part_ms["moe_t1"] * 1e-3) / 1e9,
+               "moe_t16": moe16.bytes / (part_ms["moe_t16"] * 1e-3) / 1e9}
+    # GEMM outputs of the two variants are bitwise identical by construction
+    gem_identical = bool(torch.equal(gem.Y1.view(torch.int32), gem.Y2.view(torch.int32)))
 
     # the same decode set with per-32 quantized activations (integer dot products)
     dec8 = DecodeSet(torch, device, act=qmm.ACT_Q8)
@@ -319,7 +425,8 @@ def main():
     ms_dec8 = max_over_ranks(world, time_graph(torch, g_dec8, args.steps, device), device)
     del dec8, g_dec8
 
-    # end to end: pinned host activations in, results out, every step
+    # end to end on the decode part: pinned host activations in, results out
+    g_dec = graphs[0][1]
     host_x = [it[6].cpu().pin_memory() for it in dec.items]
     host_y = [torch.empty(it[7].shape, dtype=torch.float32).pin_memory() for it in dec.items]
     torch.cuda.synchronize(device)
@@ -338,12 +445,27 @@ def main():
     ms_e2e = max_over_ranks(world, t0.elapsed_time(t1) / e2e_steps, device)
     e2e_gbs = dec.weight_bytes / (ms_e2e * 1e-3) / 1e9 * world
 
-    # dominant kernel: the matvec kernel family (all decode launches)
-    achieved = dec.algo_bytes / (ms_dec * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None,
-                "kernel": "gemv_kernel (all decode-set launches, per-launch average)",
-                "peak_source": pk["source"]}
+    # roofline of the part that takes the most time in the step
+    hbm = pk["hbm_gbs"]
+    tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
+    seg = {
+        "decode": {"bound": "hbm", "achieved": dec.algo_bytes / (ms_dec * 1e-3) / 1e9, "peak": hbm,
+                   "unit": "GB/s", "kernel": "gemv_kernel (decode set, average over launches)"},
+        "gemm_exp_plane": {"bound": "tensor", "achieved": tops["gemm_exp_plane"], "peak": tc_peak,
+                           "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, plane> + quantize"},
+        "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,
+                           "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, in-kernel> + quantize"},
+        "moe_t1": {"bound": "hbm", "achieved": moe_gbs["moe_t1"], "peak": hbm, "unit": "GB/s",
+                   "kernel": "moe route+plan+gather+gate_up+down+combine, T=1"},
+        "moe_t16": {"bound": "hbm", "achieved": moe_gbs["moe_t16"], "peak": hbm, "unit": "GB/s",
+                    "kernel": "moe route+plan+gather+gate_up+down+combine, T=16"},
+    }
+    for k2, v in seg.items():
+        v["frac"] = v["achieved"] / v["peak"]
+        v["ms"] = part_ms[k2]
+    dominant = max(part_ms, key=part_ms.get)
+    roofline = dict(seg[dominant])
+    roofline.update({"part": dominant, "traffic": None, "peak_source": pk["source"]})
 
     cpu = None
     if rank == 0:
@@ -353,14 +475,16 @@ def main():
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_dec,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "7B-shaped decode GEMV set, batch 1 and 8, bf16 activations, "
-                                   "float mode",
+            "config": {"workload": "decode GEMV set (batch 1 and 8, bf16 x, float mode) + q6_K "
+                                   "ffn_down prefill GEMM (M=512, plane and in-kernel) + routed "
+                                   "MoE (256 Q4_0 experts, top-8, T=1 and 16)",
+                       "value_is": "decode-set weight bytes / decode time",
                        "matrices": [f"{n} {f} {N}x{K}" for (n, f, N, K) in DECODE_SET],
                        "batches": list(BATCHES), "weight_bytes_per_step": dec.weight_bytes,
-                       "l2": "inputs larger than L2 (510 MB of distinct weights per step)",
+                       "l2": "flushed before each part (256 MB write outside the part's events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -368,10 +492,19 @@ def main():
                     "d2h_bytes_per_step": dec.d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
-            "hbm_frac_of_measured": gbs / pk["hbm_gbs"],
+            "parts_ms": part_ms,
+            "segments": seg,
+            "hbm_frac_of_measured": gbs / hbm,
             "q8_mode": {"value": dec.weight_bytes / (ms_dec8 * 1e-3) / 1e9 * world, "unit": "GB/s",
                         "ms_per_step": ms_dec8,
                         "note": "same decode set, activations quantized per 32 (int8 dot products)"},
+            "gemm": {"tops_exp_plane": tops["gemm_exp_plane"], "tops_in_kernel": tops["gemm_in_kernel"],
+                     "unit": "TOPS (2*M*N*K / time, incl. activation quantize)",
+                     "plane_vs_in_kernel_bitwise_equal": gem_identical,
+                     "plane_bytes": gem.N * gem.K, "plane_mem_delta_bytes": gem.plane_delta},
+            "moe": {"t1_gbps": moe_gbs["moe_t1"], "t16_gbps": moe_gbs["moe_t16"],
+                    "t16_distinct_experts": moe16.distinct, "t1_bytes": moe1.bytes,
+                    "t16_bytes": moe16.bytes},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

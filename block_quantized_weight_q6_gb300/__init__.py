@@ -24,8 +24,9 @@ LIVE = {
     "gemv_float": 0, "gemv_q8": 1, "gemv_splitk_reduce": 2, "quantize": 3, "plane_build": 4,
     "gemm_exp_plane": 5, "gemm_in_kernel": 6, "gemm_exp_off": 7, "gemm_fallback": 8,
     "gemm_q4_0": 9, "route": 10, "moe_gate_up": 11, "moe_down": 12, "moe_combine": 13,
+    "x_widen": 14, "moe_plan": 15, "moe_gather": 16,
 }
-LIVE_COUNT = 16
+LIVE_COUNT = 24
 
 BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210}
@@ -98,6 +99,7 @@ def _check(rc: int):
 # ---------------------------------------------------------------- marshalling
 
 _ws = {}
+_ws_outgrown = []
 
 
 def _torch():
@@ -107,13 +109,17 @@ def _torch():
 
 def _prepare(device, nbytes: int):
     """Point the library at torch's current stream and a workspace of at least
-    nbytes on `device` (cached per device, grown on demand)."""
+    nbytes on `device` (cached per device, grown on demand). A workspace that
+    is outgrown stays allocated: CUDA graphs captured earlier still hold its
+    address."""
     torch = _torch()
     stream = torch.cuda.current_stream(device)
     _check(lib.qmm_set_stream(C.c_void_p(stream.cuda_stream)))
     key = device.index if device.index is not None else torch.cuda.current_device()
     buf = _ws.get(key)
     if nbytes and (buf is None or buf.numel() < nbytes):
+        if buf is not None:
+            _ws_outgrown.append(buf)
         buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _ws[key] = buf
     if buf is not None:

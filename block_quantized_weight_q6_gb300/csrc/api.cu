@@ -278,7 +278,8 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if (p.xf) {
         if (bf16) {
             a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
-            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream);
+            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream,
+                                d->st);
             if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
         } else {
             a.xf = static_cast<const float*>(x);
@@ -615,7 +616,8 @@ int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64
     if (p.xf) {
         if (bf16) {
             a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
-            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream);
+            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream,
+                                d->st);
             if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
         } else {
             a.xf = static_cast<const float*>(x);

@@ -69,20 +69,23 @@ cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t 
 
 // ------------------------------------------------------------ bf16 -> fp32
 
-__global__ void x_to_f32_kernel(const uint16_t* __restrict__ x, float* __restrict__ o, int64_t n) {
+__global__ void x_to_f32_kernel(const uint16_t* __restrict__ x, float* __restrict__ o, int64_t n,
+                                DevState st) {
     grid_launch_dependents();
     grid_dependency_wait();
+    live_bump(st, QMM_LIVE_X_WIDEN);
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
         o[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
 }
 
-cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s) {
+cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s,
+                            DevState st) {
     const int threads = 256;
     int64_t blocks = (n + threads - 1) / threads;
     if (blocks > 1024) blocks = 1024;
     cudaError_t e = launch_pdl(x_to_f32_kernel, dim3(static_cast<int>(blocks)), dim3(threads), 0, s,
-                               static_cast<const uint16_t*>(x_bf16), out, n);
+                               static_cast<const uint16_t*>(x_bf16), out, n, st);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

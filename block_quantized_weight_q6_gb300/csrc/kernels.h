@@ -66,7 +66,8 @@ cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t 
 int gemv_occupancy(int fmt, bool q8, int NB, int R);
 
 // bf16 [n] -> fp32 [n]
-cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s);
+cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s,
+                            DevState st);
 
 cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
                                  cudaStream_t s, DevState st);
@@ -94,6 +95,8 @@ constexpr int QMM_LIVE_ROUTE_SLOT = QMM_LIVE_ROUTE;
 constexpr int QMM_LIVE_MOE_GATE_UP_SLOT = QMM_LIVE_MOE_GATE_UP;
 constexpr int QMM_LIVE_MOE_DOWN_SLOT = QMM_LIVE_MOE_DOWN;
 constexpr int QMM_LIVE_MOE_COMBINE_SLOT = QMM_LIVE_MOE_COMBINE;
+constexpr int QMM_LIVE_MOE_PLAN_SLOT = QMM_LIVE_MOE_PLAN;
+constexpr int QMM_LIVE_MOE_GATHER_SLOT = QMM_LIVE_MOE_GATHER;
 size_t moe_workspace_bytes(int T, int k, int H, int I, bool x_bf16);
 cudaError_t moe_launch(int fmt, int E, int H, int I, int T, int k, const void* const* wg,
                        const void* const* wu, const void* const* wd, const int32_t* idx,

@@ -68,6 +68,7 @@ struct MoeArgs {
 __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
     grid_launch_dependents();
     grid_dependency_wait();
+    live_bump(a.st, QMM_LIVE_MOE_PLAN_SLOT);
     extern __shared__ int sm[];
     int* cnt = sm;                    // [E]
     int* off = cnt + a.E;             // [E] slot offsets
@@ -122,6 +123,7 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
 __global__ void moe_gather_kernel(const MoeArgs a) {
     grid_launch_dependents();
     grid_dependency_wait();
+    live_bump(a.st, QMM_LIVE_MOE_GATHER_SLOT);
     const int S = a.T * a.k;
     const int esz = a.x_bf16 ? 2 : 4;
     const int64_t words = static_cast<int64_t>(a.H) * esz / 16;  // 16-byte units per row

@@ -148,7 +148,7 @@ def test_moe_liveness_and_bad_index_flag():
     run_moe(fmt, ws, ws, wd, H, I, idx, gate, x)
     live = qmm.liveness()
     assert live["route"] == 1 and live["moe_gate_up"] == 1 and live["moe_down"] == 1
-    assert live["moe_combine"] == 1
+    assert live["moe_combine"] == 1 and live["moe_plan"] == 1 and live["moe_gather"] == 1
     # an expert index out of range is flagged on the device and contributes 0
     bad = idx.copy()
     bad[0, 0] = E + 3
