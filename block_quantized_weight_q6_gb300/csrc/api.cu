@@ -134,62 +134,98 @@ int check_fmt(uint32_t fmt, int* wf, bool* bf16, bool* q8) {
     return QMM_OK;
 }
 
-// ---------------------------------------------------------------- GEMV plan
+// ---------------------------------------------------------------- matvec plan
+// The tensor-core matvec (tcmv.cuh): work item = 128-row tile x a range of
+// `sps` 256-wide K stages. The stage range is chosen so that the items fill
+// the resident CTAs in whole waves, preferring long ranges (each item ends
+// with one exposed accumulator drain); ranges shorter than K leave partial
+// sums that a deterministic fixed-order reduction adds up.
 struct GemvPlan {
-    int NB, R, splits, cps, nchunks, grid;
-    int64_t n_items;
-    bool xf;                                         // needs the fp32 activation copy
-    size_t ws_xq, ws_xs, ws_xf, ws_part, ws_total;   // workspace byte offsets / total
+    int NB, S, ncol, grid;
+    int64_t nst, tiles, sps, pieces, items;
+    size_t ws_xt, ws_xs, ws_part, ws_total;   // workspace byte offsets / total
 };
 
 int plan_gemv(int fmt, bool q8, bool bf16, int B, int64_t N, int64_t K, int sms, GemvPlan* p) {
     p->NB = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+    p->S = (q8 || bf16) ? 1 : 3;
+    p->ncol = tcmv_ncol(p->NB, p->S);
     const int64_t nb = K / block_elems(fmt);
-    p->nchunks = static_cast<int>((nb + gemv_chunk_blocks(fmt) - 1) / gemv_chunk_blocks(fmt));
-    int R = gemv_preferred_rows(q8, p->NB);
-    int occ = gemv_occupancy(fmt, q8, p->NB, R);
-    if (R > 1) {
-        // group rows only while the items still cover most warp slots
-        const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
-        if ((N + R - 1) / R * p->nchunks * 2 < cap) {
-            R = 1;
-            occ = gemv_occupancy(fmt, q8, p->NB, R);
+    const int bps = tcmv_stage_blocks(fmt);
+    p->nst = (nb + bps - 1) / bps;
+    p->tiles = (N + 127) / 128;
+    const int occ = tcmv_occupancy(fmt, q8, p->NB, p->S);
+    if (occ <= 0)
+        return fail(QMM_ECUDA, "matvec kernel (fmt %d, NB %d, S %d) cannot launch", fmt, p->NB, p->S);
+    const int64_t slots = static_cast<int64_t>(sms) * occ;
+    double best = -1.0;
+    int64_t best_sps = p->nst;
+    for (int64_t sps = p->nst; sps >= 1; --sps) {
+        const int64_t pieces = (p->nst + sps - 1) / sps;
+        if (sps < p->nst && (pieces - 1) * sps >= p->nst) continue;  // same split as a longer sps
+        const int64_t items = p->tiles * pieces;
+        const int64_t waves = (items + slots - 1) / slots;
+        const double fill = static_cast<double>(items) / static_cast<double>(waves * slots);
+        const double score = fill * static_cast<double>(sps) / (static_cast<double>(sps) + 0.5);
+        if (score > best + 1e-9) {
+            best = score;
+            best_sps = sps;
         }
     }
-    if (occ <= 0) return fail(QMM_ECUDA, "gemv kernel (fmt %d, NB %d, R %d) cannot launch", fmt,
-                              p->NB, R);
-    p->R = R;
-    p->xf = gemv_needs_xf(q8, p->NB, R);
-    const int64_t cap = static_cast<int64_t>(sms) * occ * kGemvWarps;
-    const int64_t groups = (N + R - 1) / R;
-    int splits = 1;
-    if (groups < cap) {
-        int64_t s = (cap + groups - 1) / groups;
-        splits = static_cast<int>(s < p->nchunks ? s : p->nchunks);
-    }
-    p->cps = (p->nchunks + splits - 1) / splits;
-    p->splits = (p->nchunks + p->cps - 1) / p->cps;
-    p->n_items = groups * p->splits;
-    int64_t grid = (p->n_items + kGemvWarps - 1) / kGemvWarps;
-    const int64_t maxg = static_cast<int64_t>(sms) * occ;
-    p->grid = static_cast<int>(grid < maxg ? grid : maxg);
+    p->sps = best_sps;
+    p->pieces = (p->nst + p->sps - 1) / p->sps;
+    p->items = p->tiles * p->pieces;
+    p->grid = static_cast<int>(p->items < slots ? p->items : slots);
     size_t off = 0;
-    p->ws_xq = p->ws_xs = p->ws_xf = p->ws_part = 0;
-    if (q8) {
-        p->ws_xq = off;
-        off = round_up(off + static_cast<size_t>(B) * K, 256);
-        p->ws_xs = off;
-        off = round_up(off + static_cast<size_t>(B) * (K / 32) * 4, 256);
-    }
-    if (p->xf && bf16) {
-        p->ws_xf = off;
-        off = round_up(off + static_cast<size_t>(B) * K * 4, 256);
-    }
-    if (p->splits > 1) {
-        p->ws_part = off;
-        off = round_up(off + static_cast<size_t>(p->splits) * B * N * 4, 256);
-    }
+    p->ws_xt = off;
+    off = round_up(off + static_cast<size_t>(p->nst) * p->ncol * 256 * 2, 256);
+    p->ws_xs = off;
+    if (q8) off = round_up(off + static_cast<size_t>(p->nst) * 8 * p->NB * 4, 256);
+    p->ws_part = off;
+    if (p->pieces > 1) off = round_up(off + static_cast<size_t>(p->pieces) * B * N * 4, 256);
     p->ws_total = off;
+    return QMM_OK;
+}
+
+// Launches the activation layout (or quantizer), the matvec and, for partial
+// sums, the reduction, with workspace `ws` (at least p.ws_total bytes).
+int run_gemv(int wf, bool q8, bool bf16, const void* W, const void* x, float* y, int64_t N,
+             int64_t K, int B, const GemvPlan& p, uint8_t* ws, const DevInfo* d) {
+    TcmvArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.N = N;
+    a.K = K;
+    a.nb = K / block_elems(wf);
+    a.total_bytes = N * a.nb * block_bytes(wf);
+    a.rowbytes = a.nb * block_bytes(wf);
+    a.n8 = N / 8 * 8;
+    a.xt = reinterpret_cast<const uint16_t*>(ws + p.ws_xt);
+    a.xs = q8 ? reinterpret_cast<const float*>(ws + p.ws_xs) : nullptr;
+    a.B = B;
+    a.y = y;
+    a.part = p.pieces > 1 ? reinterpret_cast<float*>(ws + p.ws_part) : nullptr;
+    a.tiles = p.tiles;
+    a.nst = p.nst;
+    a.sps = p.sps;
+    a.pieces = p.pieces;
+    a.items = p.items;
+    a.st = d->st;
+    a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
+    cudaError_t e;
+    if (q8)
+        e = q8_tile_launch(x, bf16, B, K, p.NB, p.ncol, p.nst, const_cast<uint16_t*>(a.xt),
+                           const_cast<float*>(a.xs), t_stream, d->st);
+    else
+        e = x_tile_launch(x, bf16, B, K, p.S, p.ncol, p.nst, const_cast<uint16_t*>(a.xt), t_stream,
+                          d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
+    e = tcmv_launch(wf, q8, p.NB, p.S, p.grid, t_stream, a);
+    if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
+    if (p.pieces > 1) {
+        e = splitk_reduce_launch(a.part, y, static_cast<int>(p.pieces), static_cast<int64_t>(B) * N,
+                                 t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+    }
     return QMM_OK;
 }
 
@@ -250,49 +286,7 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
         return fail(QMM_ENOWORKSPACE, "qmm_gemv needs %zu bytes of workspace, %zu set", p.ws_total,
                     t_ws_bytes);
-    uint8_t* ws = static_cast<uint8_t*>(t_ws);
-    GemvArgs a{};
-    a.W = static_cast<const uint8_t*>(W);
-    a.N = N;
-    a.K = K;
-    a.nb = K / block_elems(wf);
-    a.total_bytes = N * a.nb * block_bytes(wf);
-    a.x = x;
-    a.x_bf16 = bf16;
-    a.B = B;
-    a.y = y;
-    a.splits = p.splits;
-    a.cps = p.cps;
-    a.nchunks = p.nchunks;
-    a.n_items = p.n_items;
-    a.st = d->st;
-    a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
-    cudaError_t e;
-    if (q8) {
-        a.xq = reinterpret_cast<int8_t*>(ws + p.ws_xq);
-        a.xs = reinterpret_cast<float*>(ws + p.ws_xs);
-        e = quantize_q8_launch(x, bf16, B, K, const_cast<int8_t*>(a.xq), const_cast<float*>(a.xs),
-                               nullptr, t_stream, d->st);
-        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
-    }
-    if (p.xf) {
-        if (bf16) {
-            a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
-            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream,
-                                d->st);
-            if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
-        } else {
-            a.xf = static_cast<const float*>(x);
-        }
-    }
-    if (p.splits > 1) a.part = reinterpret_cast<float*>(ws + p.ws_part);
-    e = gemv_launch(wf, q8, p.NB, p.R, p.grid, t_stream, a);
-    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
-    if (p.splits > 1) {
-        e = splitk_reduce_launch(a.part, y, p.splits, static_cast<int64_t>(B) * N, t_stream, d->st);
-        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
-    }
-    return QMM_OK;
+    return run_gemv(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(t_ws), d);
 }
 
 int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int8_t* xq,
@@ -588,49 +582,7 @@ int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64
                     p.ws_total, QMM_NOALLOC_SCRATCH_BYTES);
     void* scratch = nullptr;
     if ((rc = noalloc_scratch(&scratch))) return rc;
-    uint8_t* ws = static_cast<uint8_t*>(scratch);
-    GemvArgs a{};
-    a.W = static_cast<const uint8_t*>(W);
-    a.N = N;
-    a.K = K;
-    a.nb = K / block_elems(wf);
-    a.total_bytes = N * a.nb * block_bytes(wf);
-    a.x = x;
-    a.x_bf16 = bf16;
-    a.B = B;
-    a.y = y;
-    a.splits = p.splits;
-    a.cps = p.cps;
-    a.nchunks = p.nchunks;
-    a.n_items = p.n_items;
-    a.st = d->st;
-    a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
-    cudaError_t e;
-    if (q8) {
-        a.xq = reinterpret_cast<int8_t*>(ws + p.ws_xq);
-        a.xs = reinterpret_cast<float*>(ws + p.ws_xs);
-        e = quantize_q8_launch(x, bf16, B, K, const_cast<int8_t*>(a.xq), const_cast<float*>(a.xs),
-                               nullptr, t_stream, d->st);
-        if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
-    }
-    if (p.xf) {
-        if (bf16) {
-            a.xf = reinterpret_cast<float*>(ws + p.ws_xf);
-            e = x_to_f32_launch(x, const_cast<float*>(a.xf), static_cast<int64_t>(B) * K, t_stream,
-                                d->st);
-            if (e != cudaSuccess) return cuda_fail(e, "activation copy launch");
-        } else {
-            a.xf = static_cast<const float*>(x);
-        }
-    }
-    if (p.splits > 1) a.part = reinterpret_cast<float*>(ws + p.ws_part);
-    e = gemv_launch(wf, q8, p.NB, p.R, p.grid, t_stream, a);
-    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
-    if (p.splits > 1) {
-        e = splitk_reduce_launch(a.part, y, p.splits, static_cast<int64_t>(B) * N, t_stream, d->st);
-        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
-    }
-    return QMM_OK;
+    return run_gemv(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(scratch), d);
 }
 
 const char* qmm_last_error(void) { return t_err; }

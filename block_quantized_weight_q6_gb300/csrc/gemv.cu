@@ -1,93 +1,14 @@
-// gemv.cu -- host-side dispatch of the matvec kernels (their device code is
-// in gemv_impl.cuh, instantiated per format), and the small kernels around
-// them: the per-32 activation quantizer, the bf16 -> fp32 activation copy,
-// the split-K reduction and the W_exp plane build.
+// gemv.cu -- the small kernels around the matvec and the GEMM: the split-K
+// reduction, the per-32 activation quantizer (with the GEMM's A-operand
+// tiles) and the W_exp plane build.
 #include <map>
 #include <mutex>
 #include <utility>
 
-#include "gemv_impl.cuh"
+#include "kernels.h"
+#include "quant.cuh"
 
 namespace qmm {
-
-// ------------------------------------------------------------ dispatch
-
-size_t gemv_smem_bytes(int fmt, int R) {
-    const int seg = fmt == FMT_Q6_K ? seg_stride<FMT_Q6_K>()
-                                    : (fmt == FMT_Q4_0 ? seg_stride<FMT_Q4_0>() : seg_stride<FMT_Q8_0>());
-    const int ns = R >= 4 ? slots_for<4>() : (R == 2 ? slots_for<2>() : slots_for<1>());
-    return static_cast<size_t>(kGemvWarps) * ns * seg * R + kGemvWarps * ns * 8;
-}
-
-int gemv_chunk_blocks(int fmt) {
-    return fmt == FMT_Q6_K ? Fmt<FMT_Q6_K>::CB : Fmt<FMT_Q4_0>::CB;
-}
-
-static GemvKernel pick_kernel(int fmt, bool q8, int NB, int R) {
-    switch (fmt) {
-    case FMT_Q6_K: return gemv_pick_q6k(q8, NB, R);
-    case FMT_Q4_0: return gemv_pick_q4_0(q8, NB, R);
-    case FMT_Q8_0: return gemv_pick_q8_0(q8, NB, R);
-    }
-    return nullptr;
-}
-
-// Sets the kernel's shared-memory opt-in and returns its resident CTAs per SM;
-// both are computed once per (kernel, device) and cached.
-int gemv_occupancy(int fmt, bool q8, int NB, int R) {
-    GemvKernel k = pick_kernel(fmt, q8, NB, R);
-    if (!k) return 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    static std::mutex mu;
-    static std::map<std::pair<int, GemvKernel>, int> cache;
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = cache.find({dev, k});
-    if (it != cache.end()) return it->second;
-    const size_t smem = gemv_smem_bytes(fmt, R);
-    int n = 0;
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, kGemvThreads, smem) != cudaSuccess)
-        n = 0;
-    cache[{dev, k}] = n;
-    return n;
-}
-
-cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t s,
-                        const GemvArgs& a) {
-    GemvKernel k = pick_kernel(fmt, q8, NB, R);
-    if (!k) return cudaErrorInvalidValue;
-    const size_t smem = gemv_smem_bytes(fmt, R);
-    // the shared-memory opt-in is set once per kernel (gemv_occupancy, called
-    // by the planner before the first launch), so that a launch inside a
-    // stream capture issues nothing but the launch itself
-    if (gemv_occupancy(fmt, q8, NB, R) <= 0) return cudaErrorInvalidConfiguration;
-    cudaError_t e = launch_pdl(k, dim3(grid), dim3(kGemvThreads), smem, s, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-// ------------------------------------------------------------ bf16 -> fp32
-
-__global__ void x_to_f32_kernel(const uint16_t* __restrict__ x, float* __restrict__ o, int64_t n,
-                                DevState st) {
-    grid_launch_dependents();
-    grid_dependency_wait();
-    live_bump(st, QMM_LIVE_X_WIDEN);
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        o[i] = __uint_as_float(static_cast<uint32_t>(x[i]) << 16);
-}
-
-cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s,
-                            DevState st) {
-    const int threads = 256;
-    int64_t blocks = (n + threads - 1) / threads;
-    if (blocks > 1024) blocks = 1024;
-    cudaError_t e = launch_pdl(x_to_f32_kernel, dim3(static_cast<int>(blocks)), dim3(threads), 0, s,
-                               static_cast<const uint16_t*>(x_bf16), out, n, st);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
 
 // ------------------------------------------------------------ split-K reduce
 
@@ -136,44 +57,8 @@ __global__ void quantize_q8_kernel(const void* __restrict__ x, int x_bf16, int64
         int q[32];
         if (r < rows) {
             float v[32];
-            if (x_bf16) {
-                const uint4* p = reinterpret_cast<const uint4*>(
-                    static_cast<const uint16_t*>(x) + r * K + kb * 32);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 u = __ldg(p + i);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-                        v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-                    }
-                }
-            } else {
-                const float4* p =
-                    reinterpret_cast<const float4*>(static_cast<const float*>(x) + r * K + kb * 32);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 u = __ldg(p + i);
-                    v[4 * i] = u.x;
-                    v[4 * i + 1] = u.y;
-                    v[4 * i + 2] = u.z;
-                    v[4 * i + 3] = u.w;
-                }
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            const float s = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                int t = 0;
-                if (s != 0.0f) {
-                    t = __float2int_rn(__fdiv_rn(v[i], s));
-                    t = max(-127, min(127, t));
-                }
-                q[i] = t;
-            }
+            load_x32(x, x_bf16, K, r, kb, v);
+            const float s = quantize_block32(v, q);
             if (xq) {
                 uint32_t pk[8];
 #pragma unroll

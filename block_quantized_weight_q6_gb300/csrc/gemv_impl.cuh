@@ -532,173 +532,4 @@ __device__ __forceinline__ void chunk_q32_narrow(const GemvArgs& a, uint32_t slo
     }
 }
 
-// ------------------------------------------------------------ the kernel
-
-template <int R>
-__host__ __device__ constexpr int slots_for() {
-    return R >= 4 ? 2 : (R == 2 ? 3 : 4);
-}
-
-struct ItemCursor {
-    int64_t item, row0;
-    int c, c_end;
-};
-
-__device__ __forceinline__ void cursor_set(const GemvArgs& a, ItemCursor& cur, int64_t item,
-                                           int R) {
-    cur.item = item;
-    if (item < a.n_items) {
-        const int64_t g = item / a.splits;
-        const int s = static_cast<int>(item - g * a.splits);
-        cur.row0 = g * R;
-        cur.c = s * a.cps;
-        cur.c_end = min(cur.c + a.cps, a.nchunks);
-    }
-}
-
-template <int FMT, bool Q8, int NB, int R>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
-    using F = Fmt<FMT>;
-    constexpr int SEG = seg_stride<FMT>();
-    constexpr int SLOT = SEG * R;
-    constexpr int NS = slots_for<R>();
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ring = smem_u32(smem) + warp * (NS * SLOT);
-    const uint32_t bars = smem_u32(smem) + kGemvWarps * NS * SLOT + warp * NS * 8;
-    grid_launch_dependents();
-    live_bump(a.st, a.live_slot);
-    if (lane == 0) {
-        for (int s = 0; s < NS; ++s) mbar_init(bars + 8 * s, 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * kGemvWarps + warp;
-    const int64_t tw = static_cast<int64_t>(gridDim.x) * kGemvWarps;
-    const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
-
-    // issue cursor: every lane tracks it, lane 0 performs the copies
-    ItemCursor ic;
-    cursor_set(a, ic, gw, R);
-    uint32_t issued = 0;
-    auto issue_next = [&]() {
-        if (ic.item >= a.n_items) return;
-        const uint32_t sidx = issued % NS;
-        const uint32_t dst = ring + sidx * SLOT;
-        const uint32_t bar = bars + 8 * sidx;
-        const int64_t row0 = ic.row0;
-        const int64_t kb0 = static_cast<int64_t>(ic.c) * F::CB;
-        const int64_t len = min(static_cast<int64_t>(F::CB), a.nb - kb0) * F::BB;
-        if (lane == 0) {
-            uint32_t total = 0;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int64_t row = row0 + r;
-                if (row >= a.N) break;
-                const int64_t st = (row * a.nb + kb0) * F::BB;
-                const int64_t s16 = st & ~static_cast<int64_t>(15);
-                const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                if (e16 > s16) total += static_cast<uint32_t>(e16 - s16);
-                // bytes past the last 16-byte boundary of W: plain loads
-                for (int64_t q = max(e16, s16); q < st + len; ++q)
-                    sts_u8(dst + r * SEG + static_cast<uint32_t>(q - s16), a.W[q]);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, total);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int64_t row = row0 + r;
-                if (row >= a.N) break;
-                const int64_t st = (row * a.nb + kb0) * F::BB;
-                const int64_t s16 = st & ~static_cast<int64_t>(15);
-                const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                if (e16 > s16)
-                    bulk_g2s(dst + r * SEG, a.W + s16, static_cast<uint32_t>(e16 - s16), bar);
-            }
-        }
-        ++issued;
-        if (++ic.c >= ic.c_end) cursor_set(a, ic, ic.item + tw, R);
-    };
-    // Weights are read-only: their first copies go out before waiting for the
-    // kernel this launch depends on (programmatic dependent launch); the
-    // activations and outputs are touched only after the wait.
-    for (int s = 0; s < NS; ++s) issue_next();
-    grid_dependency_wait();
-
-    uint32_t used = 0;
-    for (int64_t item = gw; item < a.n_items; item += tw) {
-        const int64_t row0 = (item / a.splits) * R;
-        const int split = static_cast<int>(item % a.splits);
-        const int c0 = split * a.cps, c1 = min(c0 + a.cps, a.nchunks);
-        float acc[R][NB];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-            for (int b = 0; b < NB; ++b) acc[r][b] = 0.0f;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t sidx = used % NS;
-            if (!mbar_wait(bars + 8 * sidx, (used / NS) & 1u)) {
-                // give up: wait (bounded) for this warp's copies in flight, flag, leave
-                for (uint32_t u = used + 1; u < issued; ++u)
-                    (void)mbar_wait(bars + 8 * (u % NS), (u / NS) & 1u);
-                if (lane == 0) atomicOr(a.st.err, DERR_GEMV_TIMEOUT);
-                return;
-            }
-            const int64_t kb0 = static_cast<int64_t>(c) * F::CB;
-            const int ncb = static_cast<int>(min(static_cast<int64_t>(F::CB), a.nb - kb0));
-            const uint32_t slot = ring + sidx * SLOT;
-            if constexpr (FMT == FMT_Q6_K) {
-                if constexpr (Wide<Q8, NB>::value)
-                    chunk_q6k_wide<Q8, NB, R>(a, slot, row0, kb0, ncb, lane, acc);
-                else
-                    chunk_q6k_narrow<Q8, NB, R>(a, slot, row0, kb0, ncb, lane, acc);
-            } else {
-                if constexpr (Wide<Q8, NB>::value)
-                    chunk_q32_wide<FMT, Q8, NB, R>(a, slot, row0, kb0, ncb, lane, acc);
-                else
-                    chunk_q32_narrow<FMT, Q8, NB, R>(a, slot, row0, kb0, ncb, lane, acc);
-            }
-            __syncwarp();
-            ++used;
-            issue_next();
-        }
-        // deterministic butterfly reduction, then one store per (row, batch)
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int64_t row = row0 + r;
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const float v = warp_sum(acc[r][b]);
-                if (lane == ((r * NB + b) & 31) && row < a.N && b < a.B) {
-                    if (a.splits == 1)
-                        a.y[b * a.N + row] = v;
-                    else
-                        a.part[(static_cast<int64_t>(split) * a.B + b) * a.N + row] = v;
-                }
-            }
-        }
-    }
-}
-
-// The (NB, R) variants built for each format and mode: R = 4 rows per item
-// (activations reused across rows) or R = 1 (short N).
-template <int FMT, bool Q8>
-GemvKernel gemv_pick(int NB, int R) {
-    if (R == 4) {
-        if (NB == 1) return gemv_kernel<FMT, Q8, 1, 4>;
-        if (NB == 2) return gemv_kernel<FMT, Q8, 2, 4>;
-        if (NB == 4) return gemv_kernel<FMT, Q8, 4, 4>;
-        if (NB == 8) return gemv_kernel<FMT, Q8, 8, 4>;
-        if (NB == 16) return gemv_kernel<FMT, Q8, 16, 4>;
-    } else if (R == 1) {
-        if (NB == 1) return gemv_kernel<FMT, Q8, 1, 1>;
-        if (NB == 2) return gemv_kernel<FMT, Q8, 2, 1>;
-        if (NB == 4) return gemv_kernel<FMT, Q8, 4, 1>;
-        if (NB == 8) return gemv_kernel<FMT, Q8, 8, 1>;
-        if (NB == 16) return gemv_kernel<FMT, Q8, 16, 1>;
-    }
-    return nullptr;
-}
-
 }  // namespace qmm

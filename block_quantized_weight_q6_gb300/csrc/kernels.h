@@ -2,6 +2,7 @@
 // kernel translation units. Not part of the public C interface.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -10,12 +11,11 @@
 
 namespace qmm {
 
-// ---------------------------------------------------------------- GEMV
-// One warp owns a run of (row group, K split) items; each item is R
-// consecutive rows over a range of K chunks. A chunk is CB consecutive
-// blocks of a row (q6_K: 8 super-blocks, Q4_0 / Q8_0: 32 blocks). The warp
-// streams its chunks into a private ring of shared-memory slots with 1-D
-// bulk TMA copies and decodes them from there.
+// ---------------------------------------------------------------- CUDA-core matvec pieces
+// The routed-expert kernels (moe.cu) stream weight rows per warp: a warp owns
+// (row group, K range) items, copies each chunk of CB consecutive blocks of
+// its rows into a private ring of shared-memory slots with 1-D bulk TMA
+// copies, and decodes them there (gemv_impl.cuh).
 constexpr int kGemvWarps = 12;
 constexpr int kGemvThreads = kGemvWarps * 32;
 
@@ -37,40 +37,55 @@ struct GemvArgs {
     int live_slot;
 };
 
-using GemvKernel = void (*)(const GemvArgs);
-GemvKernel gemv_pick_q6k(bool q8, int NB, int R);
-GemvKernel gemv_pick_q4_0(bool q8, int NB, int R);
-GemvKernel gemv_pick_q8_0(bool q8, int NB, int R);
-
-// rows per item the variants prefer when N is large enough
-inline int gemv_preferred_rows(bool q8, int NB) {
-    (void)q8;
-    (void)NB;
-    return 4;
-}
-// whether the (mode, NB) variant reads its activations from the fp32 copy
-// a.xf (the narrow, many-batch-row float variants)
-inline bool gemv_needs_xf(bool q8, int NB, int R) {
-    (void)R;
-    return !q8 && NB >= 4;
-}
-
-// shared memory bytes of one CTA of the (fmt, R) kernel
-size_t gemv_smem_bytes(int fmt, int R);
-int gemv_chunk_blocks(int fmt);
-// launches the kernel instantiation for (fmt, q8, NB, R); returns
-// cudaErrorInvalidValue if that instantiation is not built.
-cudaError_t gemv_launch(int fmt, bool q8, int NB, int R, int grid, cudaStream_t s,
-                        const GemvArgs& a);
-// max resident CTAs per SM for (fmt, q8, NB, R) (0 if not built)
-int gemv_occupancy(int fmt, bool q8, int NB, int R);
-
-// bf16 [n] -> fp32 [n]
-cudaError_t x_to_f32_launch(const void* x_bf16, float* out, int64_t n, cudaStream_t s,
-                            DevState st);
-
 cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
                                  cudaStream_t s, DevState st);
+
+// ---------------------------------------------------------------- tensor-core matvec
+// Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
+constexpr int kTcThreads = 448;
+struct TcmvArgs {
+    const uint8_t* W;
+    int64_t N, K, nb;      // rows, columns, blocks per row
+    int64_t total_bytes;   // bytes of W
+    int64_t rowbytes;      // bytes per row
+    int64_t n8;            // rows reached through the tensor map: 8 * floor(N / 8)
+    const uint16_t* xt;    // activation tile [nst][ncol / 8][32][8][8] bf16
+    const float* xs;       // q8 mode: activation scales [K / 32 rounded to stages][NB]
+    int B;
+    float* y;              // [B][N] when pieces == 1
+    float* part;           // [pieces][B][N] when pieces > 1
+    int64_t tiles, nst, sps, pieces, items;  // items = tiles * pieces
+    DevState st;
+    int live_slot;
+};
+
+using TcmvKernel = void (*)(const TcmvArgs, const CUtensorMap);
+TcmvKernel tcmv_pick_q6k(bool q8, int NB, int S);
+TcmvKernel tcmv_pick_q4_0(bool q8, int NB, int S);
+TcmvKernel tcmv_pick_q8_0(bool q8, int NB, int S);
+uint32_t tcmv_smem_q6k(int NB, int S);
+uint32_t tcmv_smem_q4_0(int NB, int S);
+uint32_t tcmv_smem_q8_0(int NB, int S);
+
+// MMA columns for NB activation rows split S ways (16, 32 or 48)
+inline int tcmv_ncol(int NB, int S) {
+    const int nc = NB * S;
+    return nc <= 16 ? 16 : (nc <= 32 ? 32 : 48);
+}
+inline int tcmv_stage_blocks(int fmt) { return fmt == FMT_Q6_K ? 1 : 8; }
+// resident CTAs per SM of the (fmt, q8, NB, S) kernel (0 if not built)
+int tcmv_occupancy(int fmt, bool q8, int NB, int S);
+// builds the weights' tensor map (W seen as rows of 8 weight rows) and launches
+cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s,
+                        const TcmvArgs& a);
+// activations [B][K] (fp32 or bf16) -> the bf16 activation tile, S = 1 (bf16
+// as is) or 3 (fp32 split exactly into hi + mid + lo columns)
+cudaError_t x_tile_launch(const void* x, int x_bf16, int B, int64_t K, int S, int ncol,
+                          int64_t nst, uint16_t* xt, cudaStream_t s, DevState st);
+// activations quantized per 32 (as quantize_q8_launch) -> the tile of the
+// int8 codes as bf16 and the scales as [block][NB]
+cudaError_t q8_tile_launch(const void* x, int x_bf16, int B, int64_t K, int NB, int ncol,
+                           int64_t nst, uint16_t* xt, float* xs, cudaStream_t s, DevState st);
 
 // ---------------------------------------------------------------- quantizer
 // x [rows][K] (fp32 or bf16) -> xq [rows][K] int8, xs [rows][K/32] fp32.

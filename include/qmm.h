@@ -93,7 +93,8 @@ enum {
     QMM_LIVE_MOE_GATE_UP = 11,
     QMM_LIVE_MOE_DOWN = 12,
     QMM_LIVE_MOE_COMBINE = 13,
-    QMM_LIVE_X_WIDEN = 14,            /* bf16 activations widened to fp32    */
+    QMM_LIVE_X_TILE = 14,             /* activations laid out as the matvec's
+                                         tensor-core operand                 */
     QMM_LIVE_MOE_PLAN = 15,
     QMM_LIVE_MOE_GATHER = 16,
     QMM_LIVE_COUNT = 24

@@ -208,10 +208,7 @@ def test_liveness_counts_each_launch():
     live = qmm.liveness()
     assert live["gemv_float"] == 1 and live["gemv_q8"] == 1 and live["quantize"] == 1
     assert live["gemv_splitk_reduce"] == 2  # short N is split along K
-    assert live["x_widen"] == 0             # fp32 activations are read in place
-    xb = synth.normal_bf16(2, (8, K))      # bf16 at batch 8: widened once to fp32
-    run_gemv(qmm.Q6_K, W, xb, N, K)
-    assert qmm.liveness()["x_widen"] == 1
+    assert live["x_tile"] == 1              # float mode lays the activations out once
 
 
 def test_missing_workspace_is_an_error():

@@ -34,8 +34,8 @@ def _x(x):
 
 CASES = [
     # (format, N, K, B, activation mode, activations): short N (split-K
-    # partials in scratch), q8 (quantized activations in scratch), batch 8
-    # float (fp32 activation copy in scratch)
+    # partials in scratch), q8 (quantized activation tile and scales in
+    # scratch), batch 8 float (bf16 activation tile in scratch)
     (qmm.Q6_K, 1024, 4096, 1, qmm.ACT_FLOAT, "f32"),
     (qmm.Q4_0, 512, 4096, 8, qmm.ACT_Q8, "bf16"),
     (qmm.Q8_0, 256, 2048, 8, qmm.ACT_FLOAT, "bf16"),
