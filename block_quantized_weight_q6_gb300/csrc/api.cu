@@ -212,12 +212,8 @@ int run_gemv(int wf, bool q8, bool bf16, const void* W, const void* x, float* y,
     a.st = d->st;
     a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
     cudaError_t e;
-    if (q8)
-        e = q8_tile_launch(x, bf16, B, K, p.NB, p.ncol, p.nst, const_cast<uint16_t*>(a.xt),
-                           const_cast<float*>(a.xs), t_stream, d->st);
-    else
-        e = x_tile_launch(x, bf16, B, K, p.S, p.ncol, p.nst, const_cast<uint16_t*>(a.xt), t_stream,
-                          d->st);
+    e = act_tile_launch(x, bf16, B, K, wf, p.NB, p.S, p.ncol, p.nst, q8, const_cast<uint16_t*>(a.xt),
+                        const_cast<float*>(a.xs), t_stream, d->st);
     if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
     e = tcmv_launch(wf, q8, p.NB, p.S, p.grid, t_stream, a);
     if (e != cudaSuccess) return cuda_fail(e, "matvec launch");

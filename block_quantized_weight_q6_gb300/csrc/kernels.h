@@ -42,7 +42,7 @@ cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_
 
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
-constexpr int kTcThreads = 448;
+constexpr int kTcThreads = 480;
 struct TcmvArgs {
     const uint8_t* W;
     int64_t N, K, nb;      // rows, columns, blocks per row
@@ -78,14 +78,12 @@ int tcmv_occupancy(int fmt, bool q8, int NB, int S);
 // builds the weights' tensor map (W seen as rows of 8 weight rows) and launches
 cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s,
                         const TcmvArgs& a);
-// activations [B][K] (fp32 or bf16) -> the bf16 activation tile, S = 1 (bf16
-// as is) or 3 (fp32 split exactly into hi + mid + lo columns)
-cudaError_t x_tile_launch(const void* x, int x_bf16, int B, int64_t K, int S, int ncol,
-                          int64_t nst, uint16_t* xt, cudaStream_t s, DevState st);
-// activations quantized per 32 (as quantize_q8_launch) -> the tile of the
-// int8 codes as bf16 and the scales as [block][NB]
-cudaError_t q8_tile_launch(const void* x, int x_bf16, int B, int64_t K, int NB, int ncol,
-                           int64_t nst, uint16_t* xt, float* xs, cudaStream_t s, DevState st);
+// activations [B][K] (fp32 or bf16) -> the matvec's bf16 activation operand
+// for weight format fmt (tcmv.cu); q8 mode quantizes per 32 first and also
+// writes the scales as [block][NB]
+cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt, int NB, int S,
+                            int ncol, int64_t nst, bool q8, uint16_t* xt, float* xs, cudaStream_t s,
+                            DevState st);
 
 // ---------------------------------------------------------------- quantizer
 // x [rows][K] (fp32 or bf16) -> xq [rows][K] int8, xs [rows][K/32] fp32.

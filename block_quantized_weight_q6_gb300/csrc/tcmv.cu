@@ -28,11 +28,11 @@ uint32_t smem_of(int fmt, int NB, int S) {
     return 0;
 }
 
-// element offset of activation column c, K index k in the tile: per 256-wide
-// stage, core matrices [c / 8][(k % 256) / 8][c % 8][k % 8]
-__device__ __forceinline__ int64_t tile_off(int ncol, int c, int64_t k) {
-    return (k >> 8) * (static_cast<int64_t>(ncol) * 256) + (c >> 3) * 2048 + ((k & 255) >> 3) * 64 +
-           (c & 7) * 8;
+// K offset within a 256-wide stage of the group with issue index i (the
+// matvec issues a stage's groups quad by quad: q6_K quad Q holds the 16-wide
+// groups Q, Q+4, Q+8, Q+12; Q4_0 / Q8_0 quad Q the 32-wide blocks 4Q..4Q+3)
+__device__ __forceinline__ int group_k(int fmt, int i) {
+    return fmt == FMT_Q6_K ? 16 * ((i >> 2) + 4 * (i & 3)) : 32 * i;
 }
 
 __device__ __forceinline__ uint32_t bf16_bits(float f) {
@@ -40,89 +40,82 @@ __device__ __forceinline__ uint32_t bf16_bits(float f) {
 }
 __device__ __forceinline__ float bf16_val(uint32_t h) { return __uint_as_float(h << 16); }
 
-// one thread per 8 consecutive tile elements (16 bytes): tile column c,
-// K indices k0..k0+7
-__global__ void x_tile_kernel(const void* __restrict__ x, int x_bf16, int B, int64_t K, int S,
-                              int ncol, int64_t nst, uint16_t* __restrict__ xt, DevState st) {
-    grid_launch_dependents();
-    grid_dependency_wait();
-    live_bump(st, QMM_LIVE_X_TILE);
-    const int64_t units = nst * ncol * 32;
-    for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        // u enumerates [stage][c / 8][k8][c % 8]: consecutive threads write
-        // consecutive 16-byte pieces
-        const int c8 = static_cast<int>(u & 7);
-        const int64_t k8 = (u >> 3) & 31;
-        const int64_t rest = u >> 8;
-        const int cg = static_cast<int>(rest % (ncol / 8));
-        const int64_t stg = rest / (ncol / 8);
-        const int c = cg * 8 + c8;
-        const int64_t k0 = stg * 256 + k8 * 8;
-        const int b = c / S, j = c % S;
-        uint32_t h[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            float f = 0.0f;
-            const int64_t k = k0 + t;
-            if (b < B && k < K) {
-                if (x_bf16)
-                    f = bf16_val(static_cast<const uint16_t*>(x)[b * K + k]);
-                else
-                    f = static_cast<const float*>(x)[b * K + k];
-            }
-            if (S == 1) {
-                h[t] = bf16_bits(f);
-            } else {
-                // f = hi + mid + lo exactly (8 + 8 + 8 significant bits)
-                const uint32_t hi = bf16_bits(f);
-                const float r1 = f - bf16_val(hi);
-                const uint32_t mid = bf16_bits(r1);
-                const uint32_t lo = bf16_bits(r1 - bf16_val(mid));
-                h[t] = j == 0 ? hi : (j == 1 ? mid : lo);
-            }
-        }
-        uint4* o = reinterpret_cast<uint4*>(xt + tile_off(ncol, c, k0));
-        *o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                        h[6] | (h[7] << 16));
-    }
+__device__ __forceinline__ float x_at(const void* x, int x_bf16, int64_t K, int b, int64_t k) {
+    return x_bf16 ? bf16_val(static_cast<const uint16_t*>(x)[b * K + k])
+                  : static_cast<const float*>(x)[b * K + k];
 }
 
-// one thread per (tile column r, 32-wide block kb): quantizes row r < B of
-// the activations and writes its codes (exact bf16) and scale; columns
-// B..ncol-1 and blocks past K are zeros
-__global__ void q8_tile_kernel(const void* __restrict__ x, int x_bf16, int B, int64_t K, int NB,
-                               int ncol, int64_t nst, uint16_t* __restrict__ xt,
-                               float* __restrict__ xs, DevState st) {
+// The matvec's activation operand. Per 256-wide stage: 16 K16 steps t (group
+// i = t / steps_per_group in issue order, half kk = t % steps_per_group), each
+// an ncol x 16 bf16 matrix in core-matrix order [row / 8][k / 8][row % 8][k % 8].
+// Row (i % G) * nc + c holds activation column c (batch row c / S, split
+// c % S) at the group's K positions; all other rows are zero. Float mode: bf16
+// activations as they are (S = 1) or fp32 ones split exactly as hi + mid + lo
+// (S = 3). q8 mode: the per-32 int8 codes (exact in bf16), and the scales
+// s[block][NB]. One thread per 16 bytes of the tile.
+__global__ void act_tile_kernel(const void* __restrict__ x, int x_bf16, int B, int64_t K, int fmt,
+                                int NB, int S, int ncol, int64_t nst, int q8,
+                                uint16_t* __restrict__ xt, float* __restrict__ xs, DevState st) {
     grid_launch_dependents();
     grid_dependency_wait();
-    live_bump(st, QMM_LIVE_QUANTIZE);
-    const int64_t nkb = nst * 8;
-    const int64_t units = nkb * ncol;
+    live_bump(st, q8 ? QMM_LIVE_QUANTIZE : QMM_LIVE_X_TILE);
+    const int nc = NB * S, G = ncol / nc;
+    const int spg = fmt == FMT_Q6_K ? 1 : 2;  // K16 steps per group
+    const int64_t units = nst * 16 * ncol * 2;
     for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(u % ncol);
-        const int64_t kb = u / ncol;
-        int q[32];
-        float s = 0.0f;
-        if (r < B && kb < K / 32) {
-            float v[32];
-            load_x32(x, x_bf16, K, r, kb, v);
-            s = quantize_block32(v, q);
-        } else {
+        // u enumerates [stage][t][row / 8][k8 (2)][row % 8]: consecutive
+        // threads write consecutive 16-byte pieces
+        const int r8 = static_cast<int>(u & 7);
+        const int o = static_cast<int>((u >> 3) & 1);
+        const int64_t rest = u >> 4;
+        const int rg = static_cast<int>(rest % (ncol / 8));
+        const int t = static_cast<int>((rest / (ncol / 8)) & 15);
+        const int64_t stg = rest / (ncol / 8) / 16;
+        const int r = rg * 8 + r8;
+        const int i = t / spg, kk = t % spg;
+        const int64_t k0 = stg * 256 + group_k(fmt, i) + 16 * kk + 8 * o;
+        uint32_t h[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (r < G * nc && r / nc == i % G) {
+            const int c = r % nc;
+            const int b = c / S, j = c % S;
+            if (q8) {
+                // the 32-block of row b holding k0 (its 8 values are a quarter of it)
+                const int64_t kb = k0 >> 5;
+                float v[32];
+                if (b < B && kb < K / 32)
+                    load_x32(x, x_bf16, K, b, kb, v);
+                else
+                    for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+                int q[32];
+                const float sc = quantize_block32(v, q);
+                const int off = static_cast<int>(k0 & 31);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) q[i] = 0;
+                for (int e = 0; e < 8; ++e) h[e] = bf16_bits(static_cast<float>(q[off + e]));
+                if (off == 0) xs[kb * NB + b] = sc;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t k = k0 + e;
+                    const float f = (b < B && k < K) ? x_at(x, x_bf16, K, b, k) : 0.0f;
+                    if (S == 1) {
+                        h[e] = bf16_bits(f);
+                    } else {
+                        // f = hi + mid + lo exactly (8 + 8 + 8 significant bits)
+                        const uint32_t hi = bf16_bits(f);
+                        const float r1 = f - bf16_val(hi);
+                        const uint32_t mid = bf16_bits(r1);
+                        const uint32_t lo = bf16_bits(r1 - bf16_val(mid));
+                        h[e] = j == 0 ? hi : (j == 1 ? mid : lo);
+                    }
+                }
+            }
         }
-        if (r < NB) xs[kb * NB + r] = s;
-#pragma unroll
-        for (int k8 = 0; k8 < 4; ++k8) {
-            uint32_t h[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) h[t] = bf16_bits(static_cast<float>(q[8 * k8 + t]));
-            uint4* o = reinterpret_cast<uint4*>(xt + tile_off(ncol, r, kb * 32 + 8 * k8));
-            *o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                            h[6] | (h[7] << 16));
-        }
+        uint4* dst = reinterpret_cast<uint4*>(
+            xt + stg * (static_cast<int64_t>(ncol) * 256) + static_cast<int64_t>(t) * ncol * 16 +
+            (rg * 2 + o) * 64 + r8 * 8);
+        *dst = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                          h[6] | (h[7] << 16));
     }
 }
 
@@ -210,19 +203,13 @@ cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t 
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t x_tile_launch(const void* x, int x_bf16, int B, int64_t K, int S, int ncol,
-                          int64_t nst, uint16_t* xt, cudaStream_t s, DevState st) {
+cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt, int NB, int S,
+                            int ncol, int64_t nst, bool q8, uint16_t* xt, float* xs, cudaStream_t s,
+                            DevState st) {
     const int threads = 256;
-    cudaError_t e = launch_pdl(x_tile_kernel, dim3(grid_for(nst * ncol * 32, threads)),
-                               dim3(threads), 0, s, x, x_bf16, B, K, S, ncol, nst, xt, st);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t q8_tile_launch(const void* x, int x_bf16, int B, int64_t K, int NB, int ncol,
-                           int64_t nst, uint16_t* xt, float* xs, cudaStream_t s, DevState st) {
-    const int threads = 128;
-    cudaError_t e = launch_pdl(q8_tile_kernel, dim3(grid_for(nst * 8 * ncol, threads)),
-                               dim3(threads), 0, s, x, x_bf16, B, K, NB, ncol, nst, xt, xs, st);
+    cudaError_t e = launch_pdl(act_tile_kernel, dim3(grid_for(nst * 16 * ncol * 2, threads)),
+                               dim3(threads), 0, s, x, x_bf16, B, K, fmt, NB, S, ncol, nst,
+                               q8 ? 1 : 0, xt, xs, st);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

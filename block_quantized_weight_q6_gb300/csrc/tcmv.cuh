@@ -28,7 +28,7 @@
 // Here the unpack ends at an exact bf16 code (one byte-permute and one packed
 // bf16 FMA per two weights) and the activation rows ride in MMA columns.
 //
-// CTA (448 threads, one per SM, persistent over work items = 128-row tile x
+// CTA (480 threads, one per SM, persistent over work items = 128-row tile x
 // a range of 256-wide K stages):
 //   warps 0-7   decode weights -> A; two sets of 4 warps take alternate
 //               stages (row = 32 * (warp % 4) + lane)
@@ -39,7 +39,8 @@
 //               16-byte multiple, and one copy brings row j of 16 such groups),
 //               1-D bulk copies for the rows past the last whole group of 8,
 //               and one 1-D bulk copy of the stage's activation tile
-//   warp 13     owns the tensor memory; lane 0 issues the MMAs
+//   warps 13-14 issue the MMAs (one thread each, for the stages of one
+//               decode set); warp 13 owns the tensor memory
 // Rings: raw stages (producer -> decoders, drainers, MMA), A slots per
 // decode set (decoders -> MMA), D slots (MMA -> drainers), each with a
 // full / empty mbarrier pair, every wait bounded in time.
@@ -101,19 +102,29 @@ struct TcLayout {
     static constexpr uint32_t XT = static_cast<uint32_t>(NCOL) * kTcStageK * 2;
     static constexpr uint32_t STAGE = RAW + XT;
     static constexpr int QA = 4 * F::GA;                       // A columns per quad
-    static constexpr int NAH = (FMT != FMT_Q6_K && NCOL == 48) ? 1 : 2;  // A slots per set
-    static constexpr int NA = 2 * NAH;
-    static constexpr int ND = NCOL == 16 ? 4 : 2;              // D slots (quads)
-    static constexpr uint32_t DCOL0 = NA * QA;                 // first D column
-    static constexpr uint32_t TNEED = DCOL0 + ND * 4 * NCOL;
+    static constexpr int SA = F::QPS * QA;                     // A columns per stage (128)
+    // D windows: NCOL columns (one MMA's N), aligned. A window collects the
+    // partial sums of G = NCOL / NC consecutive groups (issue order i = 4Q + g):
+    // group i's activations fill rows (i % G) * NC .. + NC - 1 of its B
+    // operand and every other row is zero, so each group's MMAs add only into
+    // its own NC columns; the first MMA into a window starts it from zero.
+    static constexpr int NC = NB * S;                          // columns per group
+    static constexpr int GPS = 4 * F::QPS;                     // groups per stage
+    static constexpr int G = NCOL / NC;                        // groups per window
+    static constexpr int W = (GPS + G - 1) / G;                // windows per stage
+    static constexpr uint32_t DCOL0 = 2 * SA;                  // one A stage per decode set
+    static constexpr int NW0 = static_cast<int>((512 - DCOL0) / NCOL);
+    static constexpr int NW = NW0 > 16 ? 16 : NW0;             // windows in flight
+    static_assert(G >= 1 && NW >= 1, "tensor memory");
+    static constexpr uint32_t TNEED = DCOL0 + NW * NCOL;
     static_assert(TNEED <= 512, "tensor memory");
-    // barriers: raw_full[NR], raw_empty[NR], a_full[NA], a_empty[NA],
-    // d_full[ND], d_empty[ND], final
+    // barriers: raw_full[NR], raw_empty[NR], a_full[2], a_empty[2],
+    // d_full[NW], d_empty[NW], final
     static constexpr int NR0 = static_cast<int>((kTcSmemCap - 512) / STAGE);
     static constexpr int NR = NR0 > 6 ? 6 : NR0;               // raw stages in flight
     static_assert(NR >= 3, "raw stages");
     static constexpr uint32_t BARS = NR * STAGE;
-    static constexpr uint32_t NBARS = 2 * NR + 2 * NA + 2 * ND + 1;
+    static constexpr uint32_t NBARS = 2 * NR + 4 + 2 * NW + 1;
     static constexpr uint32_t TSLOT = BARS + 8 * NBARS;
     static constexpr uint32_t ABORT = TSLOT + 4;
     static constexpr uint32_t USED = (ABORT + 4 + 127) / 128 * 128;
@@ -223,162 +234,271 @@ __device__ __forceinline__ int tc_group_xblk(int Q, int g) {
     return tc_group_k<FMT>(Q, g) >> 5;
 }
 
-// ------------------------------------------------------------ decode a quad
-// Writes the A operand of the 4 groups of quad Q of this thread's row into
-// tensor-memory columns `acol` (lane = this row).
+// ------------------------------------------------------------ decode a stage
+// Writes the A operand of every group of this thread's row in the stage into
+// tensor-memory columns from `acol` (lane = this row): quad Q at acol + Q * QA,
+// group g of the quad GA columns further per g. All shared-memory loads of
+// the stage are issued before any arithmetic, and one wait covers all stores.
 template <int FMT>
-__device__ __forceinline__ void tc_decode_quad(uint32_t rowp, int Q, uint32_t acol) {
+__device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
     using F = TcF<FMT>;
+    constexpr int QA = 4 * F::GA;
     if constexpr (FMT == FMT_Q6_K) {
-        uint32_t qh[4], qa[4], qb[4];
-        lds_words_unaligned<4>(rowp + 128 + 16 * Q, qh);
-        lds_words_unaligned<4>(rowp + 16 * Q, qa);
-        lds_words_unaligned<4>(rowp + 64 + 16 * Q, qb);
+        uint32_t qh[4][4], qa[4][4], qb[4][4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            // group j = Q + 4g: ql run (j & 7), nibble j >> 3, qh field j >> 2 = g
-            uint32_t A[8];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const uint32_t base = (g & 1) ? qb[w] : qa[w];
-                const uint32_t nib = (g < 2) ? base : (base >> 4);
-                uint32_t h;
-                if (g == 0) h = (qh[w] & 0x03030303u) << 4;
-                else if (g == 1) h = (qh[w] & 0x0C0C0C0Cu) << 2;
-                else if (g == 2) h = qh[w] & 0x30303030u;
-                else h = (qh[w] >> 2) & 0x30303030u;
-                const uint32_t c = (nib & 0x0F0F0F0Fu) | h;
-                A[2 * w] = bf_add(bf_pair_lo(c), kBfNeg160);
-                A[2 * w + 1] = bf_add(bf_pair_hi(c), kBfNeg160);
-            }
-            tc::st8(acol + F::GA * g, A);
+        for (int Q = 0; Q < 4; ++Q) {
+            lds_words_unaligned<4>(rowp + 128 + 16 * Q, qh[Q]);
+            lds_words_unaligned<4>(rowp + 16 * Q, qa[Q]);
+            lds_words_unaligned<4>(rowp + 64 + 16 * Q, qb[Q]);
         }
-    } else {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const uint32_t blk = rowp + F::BB * (4 * Q + g);
-            uint32_t A[16];
-            if constexpr (FMT == FMT_Q4_0) {
-                uint32_t qs[4];
-                lds_words_unaligned<4>(blk + 2, qs);
+        for (int Q = 0; Q < 4; ++Q) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                // group j = Q + 4g: ql run (j & 7), nibble j >> 3, qh field j >> 2 = g
+                uint32_t A[8];
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    const uint32_t lo = qs[w] & 0x0F0F0F0Fu;         // elements 4w..4w+3
-                    const uint32_t hi = (qs[w] >> 4) & 0x0F0F0F0Fu;  // elements 16+4w..
-                    A[2 * w] = bf_add(bf_pair_lo(lo), kBfNeg136);
-                    A[2 * w + 1] = bf_add(bf_pair_hi(lo), kBfNeg136);
-                    A[8 + 2 * w] = bf_add(bf_pair_lo(hi), kBfNeg136);
-                    A[8 + 2 * w + 1] = bf_add(bf_pair_hi(hi), kBfNeg136);
+                    const uint32_t base = (g & 1) ? qb[Q][w] : qa[Q][w];
+                    const uint32_t nib = (g < 2) ? base : (base >> 4);
+                    uint32_t h;
+                    if (g == 0) h = (qh[Q][w] & 0x03030303u) << 4;
+                    else if (g == 1) h = (qh[Q][w] & 0x0C0C0C0Cu) << 2;
+                    else if (g == 2) h = qh[Q][w] & 0x30303030u;
+                    else h = (qh[Q][w] >> 2) & 0x30303030u;
+                    const uint32_t c = (nib & 0x0F0F0F0Fu) | h;
+                    A[2 * w] = bf_add(bf_pair_lo(c), kBfNeg160);
+                    A[2 * w + 1] = bf_add(bf_pair_hi(c), kBfNeg160);
                 }
-            } else {
-                uint32_t qs[8];
-                lds_words_unaligned<8>(blk + 2, qs);
-#pragma unroll
-                for (int w = 0; w < 8; ++w) q8_bf_pairs(qs[w], A[2 * w], A[2 * w + 1]);
+                tc::st8(acol + QA * Q + F::GA * g, A);
             }
-            tc::st16(acol + F::GA * g, A);
         }
-    }
-}
-
-// The 4 group scales of quad Q of this thread's row, read from the raw stage.
-// Blocks past the end of the row (last stage of a ragged K) hold stale bytes;
-// their activations are zero and their scale is 0.
-template <int FMT>
-__device__ __forceinline__ void tc_quad_scales(uint32_t rowp, int Q, int nblk, float (&s)[4]) {
-    if constexpr (FMT == FMT_Q6_K) {
-        const float d = half_bits_to_float(lds_u16(rowp + 208));
+    } else if constexpr (FMT == FMT_Q4_0) {
+        uint32_t qs[8][4];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) s[g] = d * static_cast<float>(lds_s8(rowp + 192 + Q + 4 * g));
-        (void)nblk;
+        for (int i = 0; i < 8; ++i) lds_words_unaligned<4>(rowp + F::BB * i + 2, qs[i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t A[16];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t lo = qs[i][w] & 0x0F0F0F0Fu;         // elements 4w..4w+3
+                const uint32_t hi = (qs[i][w] >> 4) & 0x0F0F0F0Fu;  // elements 16+4w..
+                A[2 * w] = bf_add(bf_pair_lo(lo), kBfNeg136);
+                A[2 * w + 1] = bf_add(bf_pair_hi(lo), kBfNeg136);
+                A[8 + 2 * w] = bf_add(bf_pair_lo(hi), kBfNeg136);
+                A[8 + 2 * w + 1] = bf_add(bf_pair_hi(hi), kBfNeg136);
+            }
+            tc::st16(acol + QA * (i >> 2) + F::GA * (i & 3), A);
+        }
     } else {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int i = 4 * Q + g;
-            const float d = half_bits_to_float(lds_u16(rowp + TcF<FMT>::BB * i));
-            s[g] = i < nblk ? d : 0.0f;
+        for (int i = 0; i < 8; ++i) {
+            uint32_t qs[8];
+            lds_words_unaligned<8>(rowp + F::BB * i + 2, qs);
+            uint32_t A[16];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) q8_bf_pairs(qs[w], A[2 * w], A[2 * w + 1]);
+            tc::st16(acol + QA * (i >> 2) + F::GA * (i & 3), A);
         }
     }
 }
 
-// ------------------------------------------------------------ drain a quad
-// Loads the 4 accumulators of a quad (this thread's row) and adds
-// s * (activation scale) * P to acc[b] for every activation row b.
-template <int NC>
-struct TcLd {
-    static constexpr int N = NC <= 1 ? 1 : NC <= 2 ? 2 : NC <= 4 ? 4 : NC <= 8 ? 8 : NC <= 16 ? 16
-                             : NC <= 32 ? 32 : 48;
-};
+// ------------------------------------------------------------ aligned decode
+// When the row pitch is a multiple of 16 bytes every row of a stage has the
+// same lead, so the decode is specialized on it: 16-byte shared loads from
+// the 16-byte aligned row slot, and byte realignment by compile-time shifts.
 
-template <int NL>
-__device__ __forceinline__ void tc_ld_cols(uint32_t taddr, uint32_t (&v)[NL]) {
-    if constexpr (NL == 48) {
+__device__ __forceinline__ void lds128(uint32_t a, uint32_t* w) {
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(a));
+}
+
+// the 16 bytes at slot + OFF (OFF even, known at compile time) as 4 words
+template <int OFF>
+__device__ __forceinline__ void tc_run16(uint32_t slot, uint32_t (&o)[4]) {
+    constexpr int A = OFF & ~15, Q = (OFF & 15) >> 2, SH = (OFF & 3) * 8;
+    uint32_t w[8];
+    lds128(slot + A, w);
+    if constexpr (Q > 0 || SH > 0) lds128(slot + A + 16, w + 4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = SH ? __funnelshift_r(w[Q + k], w[Q + k + 1], SH) : w[Q + k];
+}
+
+// q6_K: quad Q of a super-block whose bytes start at slot + LEAD
+template <int LEAD, int Q>
+__device__ __forceinline__ void tc_q6k_quad_aligned(uint32_t slot, uint32_t acol) {
+    using F = TcF<FMT_Q6_K>;
+    uint32_t qh[4], qa[4], qb[4];
+    tc_run16<LEAD + 128 + 16 * Q>(slot, qh);
+    tc_run16<LEAD + 16 * Q>(slot, qa);
+    tc_run16<LEAD + 64 + 16 * Q>(slot, qb);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        uint32_t A[8];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t base = (g & 1) ? qb[w] : qa[w];
+            const uint32_t nib = (g < 2) ? base : (base >> 4);
+            uint32_t h;
+            if (g == 0) h = (qh[w] & 0x03030303u) << 4;
+            else if (g == 1) h = (qh[w] & 0x0C0C0C0Cu) << 2;
+            else if (g == 2) h = qh[w] & 0x30303030u;
+            else h = (qh[w] >> 2) & 0x30303030u;
+            const uint32_t c = (nib & 0x0F0F0F0Fu) | h;
+            A[2 * w] = bf_add(bf_pair_lo(c), kBfNeg160);
+            A[2 * w + 1] = bf_add(bf_pair_hi(c), kBfNeg160);
+        }
+        tc::st8(acol + 4 * F::GA * Q + F::GA * g, A);
+    }
+}
+
+// Q4_0 / Q8_0: block I of the stage, bytes from slot + LEAD + BB * I
+template <int FMT, int LEAD, int I>
+__device__ __forceinline__ void tc_q32_block_aligned(uint32_t slot, uint32_t acol) {
+    using F = TcF<FMT>;
+    constexpr int OFF = LEAD + F::BB * I + 2;
+    uint32_t A[16];
+    if constexpr (FMT == FMT_Q4_0) {
+        uint32_t qs[4];
+        tc_run16<OFF>(slot, qs);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t lo = qs[w] & 0x0F0F0F0Fu;
+            const uint32_t hi = (qs[w] >> 4) & 0x0F0F0F0Fu;
+            A[2 * w] = bf_add(bf_pair_lo(lo), kBfNeg136);
+            A[2 * w + 1] = bf_add(bf_pair_hi(lo), kBfNeg136);
+            A[8 + 2 * w] = bf_add(bf_pair_lo(hi), kBfNeg136);
+            A[8 + 2 * w + 1] = bf_add(bf_pair_hi(hi), kBfNeg136);
+        }
+    } else {
+        uint32_t q0[4], q1[4];
+        tc_run16<OFF>(slot, q0);
+        tc_run16<OFF + 16>(slot, q1);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            q8_bf_pairs(q0[w], A[2 * w], A[2 * w + 1]);
+            q8_bf_pairs(q1[w], A[8 + 2 * w], A[8 + 2 * w + 1]);
+        }
+    }
+    tc::st16(acol + 4 * F::GA * (I >> 2) + F::GA * (I & 3), A);
+}
+
+template <int FMT, int LEAD>
+__device__ __forceinline__ void tc_decode_stage_aligned(uint32_t slot, uint32_t acol) {
+    if constexpr (FMT == FMT_Q6_K) {
+        tc_q6k_quad_aligned<LEAD, 0>(slot, acol);
+        tc_q6k_quad_aligned<LEAD, 1>(slot, acol);
+        tc_q6k_quad_aligned<LEAD, 2>(slot, acol);
+        tc_q6k_quad_aligned<LEAD, 3>(slot, acol);
+    } else {
+        tc_q32_block_aligned<FMT, LEAD, 0>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 1>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 2>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 3>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 4>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 5>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 6>(slot, acol);
+        tc_q32_block_aligned<FMT, LEAD, 7>(slot, acol);
+    }
+}
+
+// Decode of a stage: the specialized form when the lead is the same for every
+// row (warp-uniform branch), else the general per-row realignment.
+template <int FMT>
+__device__ __forceinline__ void tc_decode_stage_any(uint32_t slot, uint32_t lead, bool uniform,
+                                                    uint32_t acol) {
+    if (uniform) {
+        switch (lead) {
+            case 0: tc_decode_stage_aligned<FMT, 0>(slot, acol); return;
+            case 2: tc_decode_stage_aligned<FMT, 2>(slot, acol); return;
+            case 4: tc_decode_stage_aligned<FMT, 4>(slot, acol); return;
+            case 6: tc_decode_stage_aligned<FMT, 6>(slot, acol); return;
+            case 8: tc_decode_stage_aligned<FMT, 8>(slot, acol); return;
+            case 10: tc_decode_stage_aligned<FMT, 10>(slot, acol); return;
+            case 12: tc_decode_stage_aligned<FMT, 12>(slot, acol); return;
+            default: tc_decode_stage_aligned<FMT, 14>(slot, acol); return;
+        }
+    }
+    tc_decode_stage<FMT>(slot + lead, acol);
+}
+
+// Scale of group i (issue order) of this thread's row, read from the raw
+// stage. Blocks past the end of the row (last stage of a ragged K) hold
+// stale bytes; their activations are zero and their scale is 0.
+template <int FMT>
+__device__ __forceinline__ float tc_group_scale(uint32_t rowp, int i, int nblk) {
+    if constexpr (FMT == FMT_Q6_K) {
+        const int j = (i >> 2) + 4 * (i & 3);  // the group's index in the super-block
+        (void)nblk;
+        return half_bits_to_float(lds_u16(rowp + 208)) * static_cast<float>(lds_s8(rowp + 192 + j));
+    } else {
+        const float d = half_bits_to_float(lds_u16(rowp + TcF<FMT>::BB * i));
+        return i < nblk ? d : 0.0f;
+    }
+}
+
+// ------------------------------------------------------------ drain a window
+// Loads the window (this thread's row) and adds s_i * (activation scale) * P
+// to acc[b] for every group i of the window and every activation row b.
+template <int NCOL>
+__device__ __forceinline__ void tc_ld_window(uint32_t taddr, uint32_t (&v)[NCOL]) {
+    if constexpr (NCOL == 48) {
         tc::ld<32>(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tc::ld<16>(taddr + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
     } else {
-        tc::ld<NL>(taddr, v);
+        tc::ld<NCOL>(taddr, v);
     }
 }
 
-template <int NB, int S, bool Q8>
-__device__ __forceinline__ void tc_drain_use(const uint32_t* v, float s, int64_t xblk,
-                                             const TcmvArgs& a, float (&acc)[NB]) {
-    float sc[NB];
+template <int FMT, int NB, int S, bool Q8>
+__device__ __forceinline__ void tc_drain_window(uint32_t dcol, uint32_t rowp, int w, int nblk,
+                                                int64_t xblk0, const TcmvArgs& a, float (&acc)[NB]) {
+    using L = TcLayout<FMT, NB, S>;
+    constexpr int NCOL = L::NCOL, NC = L::NC, G = L::G;
+    uint32_t v[NCOL];
+    tc_ld_window<NCOL>(dcol, v);
+    float sg[G];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) sc[b] = s;
-    if constexpr (Q8) {
-        // activation scales of this 32-block, stored [block][NB]
-        const float* xs = a.xs + xblk * NB;
-        if constexpr (NB >= 4) {
+    for (int u = 0; u < G; ++u) {
+        const int i = w * G + u;
+        sg[u] = i < L::GPS ? tc_group_scale<FMT>(rowp, i, nblk) : 0.0f;
+    }
+    tc::wait_ld();
 #pragma unroll
-            for (int b = 0; b < NB; b += 4) {
-                const float4 f = __ldg(reinterpret_cast<const float4*>(xs + b));
-                sc[b] *= f.x;
-                sc[b + 1] *= f.y;
-                sc[b + 2] *= f.z;
-                sc[b + 3] *= f.w;
+    for (int u = 0; u < G; ++u) {
+        const int i = w * G + u;
+        if (i >= L::GPS) break;
+        float sc[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) sc[b] = sg[u];
+        if constexpr (Q8) {
+            // activation scales of the group's 32-block, stored [block][NB]
+            const float* xs = a.xs + (xblk0 + (tc_group_k<FMT>(i >> 2, i & 3) >> 5)) * NB;
+            if constexpr (NB >= 4) {
+#pragma unroll
+                for (int b = 0; b < NB; b += 4) {
+                    const float4 f = __ldg(reinterpret_cast<const float4*>(xs + b));
+                    sc[b] *= f.x;
+                    sc[b + 1] *= f.y;
+                    sc[b + 2] *= f.z;
+                    sc[b + 3] *= f.w;
+                }
+            } else {
+#pragma unroll
+                for (int b = 0; b < NB; ++b) sc[b] *= __ldg(xs + b);
             }
-        } else {
-#pragma unroll
-            for (int b = 0; b < NB; ++b) sc[b] *= __ldg(xs + b);
         }
-    }
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-        float p;
-        if constexpr (S == 1)
-            p = __uint_as_float(v[b]);
-        else
-            p = __uint_as_float(v[3 * b]) + __uint_as_float(v[3 * b + 1]) +
-                __uint_as_float(v[3 * b + 2]);
-        acc[b] = fmaf(sc[b], p, acc[b]);
-    }
-}
-
-template <int NB, int S, bool Q8, int FMT>
-__device__ __forceinline__ void tc_drain_quad(uint32_t dcol, uint32_t rowp, int Q, int nblk,
-                                              int64_t xblk0, const TcmvArgs& a, float (&acc)[NB]) {
-    constexpr int NCOL = TcCols<NB, S>::NCOL;
-    constexpr int NL = TcLd<NB * S>::N;
-    float s[4];
-    if constexpr (NB * S <= 16) {
-        // all four loads in flight, the scales read meanwhile, one wait
-        uint32_t v[4][NL];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) tc_ld_cols<NL>(dcol + NCOL * g, v[g]);
-        tc_quad_scales<FMT>(rowp, Q, nblk, s);
-        tc::wait_ld();
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-            tc_drain_use<NB, S, Q8>(v[g], s[g], xblk0 + tc_group_xblk<FMT>(Q, g), a, acc);
-    } else {
-        tc_quad_scales<FMT>(rowp, Q, nblk, s);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            uint32_t v[NL];
-            tc_ld_cols<NL>(dcol + NCOL * g, v);
-            tc::wait_ld();
-            tc_drain_use<NB, S, Q8>(v, s[g], xblk0 + tc_group_xblk<FMT>(Q, g), a, acc);
+        for (int b = 0; b < NB; ++b) {
+            const int c = u * NC + b * S;
+            float p;
+            if constexpr (S == 1)
+                p = __uint_as_float(v[c]);
+            else
+                p = __uint_as_float(v[c]) + __uint_as_float(v[c + 1]) + __uint_as_float(v[c + 2]);
+            acc[b] = fmaf(sc[b], p, acc[b]);
         }
     }
 }
@@ -393,17 +513,29 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Shared address of row m's data in a raw stage (lead = the row segment's
-// offset from the 16-byte boundary below it).
+// Tile row held by tensor-memory lane m (the A row an MMA reads): row
+// 8 * i + j, with the 8 lanes of every quarter warp taking 8 consecutive i of
+// one j. Row 8i + j sits in box j at slot i, so those 8 lanes read 8 different
+// slots, RS = 16 * odd bytes apart: a 16-byte shared load of theirs touches 8
+// different bank groups.
+__device__ __forceinline__ int tc_lane_row(int m) {
+    const int l = m & 31, wq = m >> 5;
+    const int i = (l & 7) + 8 * (wq & 1);
+    const int j = (l >> 3) + 4 * (wq >> 1);
+    return 8 * i + j;
+}
+
+// Shared address of tile row r's slot in a raw stage (16-byte aligned), and
+// the row segment's offset from it (`lead`, the distance from the 16-byte
+// boundary below the segment).
 template <int FMT, int NB, int S>
-__device__ __forceinline__ uint32_t tc_row_ptr(const TcmvArgs& a, uint32_t stage, int64_t tile, int m,
-                                               int64_t koff) {
+__device__ __forceinline__ uint32_t tc_row_slot(const TcmvArgs& a, uint32_t stage, int64_t tile, int r,
+                                                int64_t koff, uint32_t& lead) {
     using L = TcLayout<FMT, NB, S>;
-    const int64_t n = tile * 128 + m;
-    const uint32_t lead = static_cast<uint32_t>((n * a.rowbytes + koff) & 15);
-    if (n < a.n8) return stage + (m & 7) * L::BOXP + (m >> 3) * TcF<FMT>::RS + lead;
-    return stage + L::TAIL + static_cast<uint32_t>(min(n - a.n8, static_cast<int64_t>(7))) * TcF<FMT>::RS +
-           lead;
+    const int64_t n = tile * 128 + r;
+    lead = static_cast<uint32_t>((n * a.rowbytes + koff) & 15);
+    if (n < a.n8) return stage + (r & 7) * L::BOXP + (r >> 3) * TcF<FMT>::RS;
+    return stage + L::TAIL + static_cast<uint32_t>(min(n - a.n8, static_cast<int64_t>(7))) * TcF<FMT>::RS;
 }
 
 // ------------------------------------------------------------ work walk
@@ -431,17 +563,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     using F = TcF<FMT>;
     using L = TcLayout<FMT, NB, S>;
     constexpr int NCOL = L::NCOL;
-    constexpr int NR = L::NR, NA = L::NA, NAH = L::NAH, ND = L::ND;
+    constexpr int NR = L::NR, NW = L::NW;
     constexpr uint32_t IDESC = tc::idesc_bf16(128, NCOL);
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const uint32_t b_rfull = sb + L::BARS;
     const uint32_t b_rempty = b_rfull + 8 * NR;
     const uint32_t b_afull = b_rempty + 8 * NR;
-    const uint32_t b_aempty = b_afull + 8 * NA;
-    const uint32_t b_dfull = b_aempty + 8 * NA;
-    const uint32_t b_dempty = b_dfull + 8 * ND;
-    const uint32_t b_final = b_dempty + 8 * ND;
+    const uint32_t b_aempty = b_afull + 16;
+    const uint32_t b_dfull = b_aempty + 16;
+    const uint32_t b_dempty = b_dfull + 8 * NW;
+    const uint32_t b_final = b_dempty + 8 * NW;
     const uint32_t flag = sb + L::ABORT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned int* err = a.st.err;
@@ -453,15 +585,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(b_rfull + 8 * r, 1);
             mbar_init(b_rempty + 8 * r, 9);  // 4 decoders + 4 drainers + the MMA commit
         }
-        for (int q = 0; q < NA; ++q) {
+        for (int q = 0; q < 2; ++q) {
             mbar_init(b_afull + 8 * q, 4);
             mbar_init(b_aempty + 8 * q, 1);
         }
-        for (int q = 0; q < ND; ++q) {
+        for (int q = 0; q < NW; ++q) {
             mbar_init(b_dfull + 8 * q, 1);
             mbar_init(b_dempty + 8 * q, 4);
         }
-        mbar_init(b_final, 1);
+        mbar_init(b_final, 2);  // one commit per MMA issuer
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(flag), "r"(0u) : "memory");
         fence_mbar_init();
     }
@@ -558,51 +690,61 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // wait (bounded) for the copies still in flight before leaving
         for (uint32_t u = issued > static_cast<uint32_t>(NR) ? issued - NR : 0; u < issued; ++u)
             (void)tcmv_wait_warp(b_rfull + 8 * (u % NR), (u / NR) & 1u, flag, err);
-    } else if (warp == 13) {
-        // ---------------------------------------------------- MMA issue
+    } else if (warp >= 13) {
+        // ---------------------------------------------------- MMA issue (set = warp - 13)
+        const uint32_t myset = static_cast<uint32_t>(warp - 13);
         if (lane == 0) {
-            uint32_t qc = 0, sc = 0;
+            uint32_t sc = 0;  // stages walked
             bool ok = true;
             for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
                 const TcItem it = tc_item(a, item);
                 for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
-                    const uint32_t slot = sc % NR;
                     const uint32_t set = sc & 1u;
+                    if (set != myset) continue;
+                    const uint32_t slot = sc % NR;
+                    const uint32_t wc = sc * L::W;  // windows of the earlier stages
                     if (!tcmv_wait_one(b_rfull + 8 * slot, (sc / NR) & 1u, flag, err)) {
                         ok = false;
                         break;
                     }
-                    TCMV_TRACE(1, sc);
-                    const uint32_t xaddr = sb + slot * L::STAGE + L::RAW;
-#pragma unroll 1
-                    for (int Q = 0; Q < F::QPS; ++Q, ++qc) {
-                        const uint32_t lq = (sc >> 1) * F::QPS + Q;  // quad count of the set
-                        const uint32_t as = set * NAH + lq % NAH;
-                        const uint32_t ds = qc % ND;
-                        if (!tcmv_wait_one(b_afull + 8 * as, (lq / NAH) & 1u, flag, err) ||
-                            (qc >= static_cast<uint32_t>(ND) &&
-                             !tcmv_wait_one(b_dempty + 8 * ds, ((qc / ND) - 1) & 1u, flag, err))) {
-                            ok = false;
-                            break;
-                        }
-                        TCMV_TRACE(7, qc);
-                        tc::fence_after();
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const uint32_t dcol = tmem + L::DCOL0 + ds * 4 * NCOL + NCOL * g;
-                            const uint32_t acol = tmem + as * L::QA + F::GA * g;
-                            const int k0 = tc_group_k<FMT>(Q, g);
-#pragma unroll
-                            for (int kk = 0; kk < F::GK / 16; ++kk) {
-                                const uint64_t bd = tc::smem_desc(
-                                    xaddr + static_cast<uint32_t>((k0 / 8 + 2 * kk) * 128), 128,
-                                    kTcStageK / 8 * 128);
-                                tc::mma_ts(dcol, acol + 8 * kk, bd, IDESC, kk > 0 ? 1u : 0u);
-                            }
-                        }
-                        tc::commit(b_aempty + 8 * as);
-                        tc::commit(b_dfull + 8 * ds);
+                    // the set's A stage: sets take alternate stages
+                    if (!tcmv_wait_one(b_afull + 8 * set, (sc >> 1) & 1u, flag, err)) {
+                        ok = false;
+                        break;
                     }
+                    TCMV_TRACE(1, sc);
+                    tc::fence_after();
+                    // descriptors and addresses: per-stage bases plus compile-time
+                    // offsets, so the issue loop is a run of MMAs. B operand of
+                    // K16 step t: NCOL rows x 16 K at t * NCOL * 32 bytes, core
+                    // matrices 128 bytes apart along K, 256 between 8-row groups.
+                    const uint64_t bdesc0 = tc::smem_desc(sb + slot * L::STAGE + L::RAW, 128, 256);
+                    const uint32_t abase = tmem + set * L::SA;
+                    uint32_t dbase = 0, ws = 0;
+#pragma unroll
+                    for (int i = 0; i < L::GPS; ++i) {
+                        if (i % L::G == 0) {
+                            const uint32_t wg = wc + i / L::G;
+                            ws = wg % NW;
+                            if (wg >= static_cast<uint32_t>(NW) &&
+                                !tcmv_wait_one(b_dempty + 8 * ws, ((wg / NW) - 1) & 1u, flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after();
+                            dbase = tmem + L::DCOL0 + ws * NCOL;
+                        }
+                        const uint32_t acol = abase + (i >> 2) * L::QA + F::GA * (i & 3);
+#pragma unroll
+                        for (int kk = 0; kk < F::GK / 16; ++kk) {
+                            const int t = i * (F::GK / 16) + kk;
+                            tc::mma_ts(dbase, acol + 8 * kk,
+                                       bdesc0 + static_cast<uint64_t>((t * NCOL * 32) >> 4), IDESC,
+                                       (i % L::G != 0 || kk > 0) ? 1u : 0u);
+                        }
+                        if (i % L::G == L::G - 1 || i == L::GPS - 1) tc::commit(b_dfull + 8 * ws);
+                    }
+                    tc::commit(b_aempty + 8 * set);
                     tc::commit(b_rempty + 8 * slot);
                     TCMV_TRACE(2, sc);
                 }
@@ -615,7 +757,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp < 8) {
         // ---------------------------------------------------- decode (set = warp / 4)
         const uint32_t myset = static_cast<uint32_t>(warp >> 2);
-        const int m = 32 * (warp & 3) + lane;
+        const int r = tc_lane_row(32 * (warp & 3) + lane);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         uint32_t sc = 0;
         bool ok = true;
@@ -628,25 +770,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t rowp = tc_row_ptr<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, m,
-                                                             s * F::BPS * F::BB);
+                uint32_t lead;
+                const uint32_t rslot = tc_row_slot<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, r, s * F::BPS * F::BB, lead);
                 if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(3, sc);
-#pragma unroll 1
-                for (int Q = 0; Q < F::QPS; ++Q) {
-                    const uint32_t lq = (sc >> 1) * F::QPS + Q;
-                    const uint32_t as = myset * NAH + lq % NAH;
-                    if (lq >= static_cast<uint32_t>(NAH) &&
-                        !tcmv_wait_warp(b_aempty + 8 * as, ((lq / NAH) - 1) & 1u, flag, err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    tc_decode_quad<FMT>(rowp, Q, lane_base + as * L::QA);
-                    tc::wait_st();
-                    tc::fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_afull + 8 * as);
+                // this set's previous A stage has been read by its MMAs
+                const uint32_t ls = sc >> 1;
+                if (ls >= 1 && !tcmv_wait_warp(b_aempty + 8 * myset, (ls - 1) & 1u, flag, err)) {
+                    ok = false;
+                    break;
                 }
+                tc::fence_after();
+                tc_decode_stage_any<FMT>(rslot, lead, a.rowbytes % 16 == 0, lane_base + myset * L::SA);
+                tc::wait_st();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_afull + 8 * myset);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_rempty + 8 * slot);
                 if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(4, sc);
@@ -654,14 +792,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else {
         // ---------------------------------------------------- drain
-        const int m = 32 * (warp & 3) + lane;
+        const int r = tc_lane_row(32 * (warp & 3) + lane);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         grid_dependency_wait();  // y, the partial sums and the activation scales
-        uint32_t qc = 0, sc = 0;
+        uint32_t wc = 0, sc = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
             const TcItem it = tc_item(a, item);
-            const int64_t n = it.tile * 128 + m;
+            const int64_t n = it.tile * 128 + r;
             float acc[NB];
 #pragma unroll
             for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
@@ -673,23 +811,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const int64_t kb0 = s * F::BPS;
                 const int nblk = static_cast<int>(min(static_cast<int64_t>(F::BPS), a.nb - kb0));
-                const uint32_t rowp = tc_row_ptr<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, m,
-                                                             kb0 * F::BB);
+                uint32_t lead;
+                const uint32_t rowp =
+                    tc_row_slot<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, r, kb0 * F::BB, lead) + lead;
 #pragma unroll 1
-                for (int Q = 0; Q < F::QPS; ++Q, ++qc) {
-                    const uint32_t ds = qc % ND;
-                    if (!tcmv_wait_warp(b_dfull + 8 * ds, (qc / ND) & 1u, flag, err)) {
+                for (int w = 0; w < L::W; ++w, ++wc) {
+                    const uint32_t ws = wc % NW;
+                    if (!tcmv_wait_warp(b_dfull + 8 * ws, (wc / NW) & 1u, flag, err)) {
                         ok = false;
                         break;
                     }
-                    if (warp == 8 && lane == 0) TCMV_TRACE(5, qc);
+                    if (warp == 8 && lane == 0) TCMV_TRACE(5, wc);
                     tc::fence_after();
-                    tc_drain_quad<NB, S, Q8, FMT>(lane_base + L::DCOL0 + ds * 4 * NCOL, rowp, Q, nblk,
-                                                  s * (kTcStageK / 32), a, acc);
+                    tc_drain_window<FMT, NB, S, Q8>(lane_base + L::DCOL0 + ws * NCOL, rowp, w, nblk,
+                                                    s * (kTcStageK / 32), a, acc);
                     tc::fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(b_dempty + 8 * ds);
-                    if (warp == 8 && lane == 0) TCMV_TRACE(6, qc);
+                    if (lane == 0) mbar_arrive(b_dempty + 8 * ws);
+                    if (warp == 8 && lane == 0) TCMV_TRACE(6, wc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_rempty + 8 * slot);
