@@ -118,13 +118,13 @@ struct TcLayout {
     static_assert(G >= 1 && NW >= 1, "tensor memory");
     static constexpr uint32_t TNEED = DCOL0 + NW * NCOL;
     static_assert(TNEED <= 512, "tensor memory");
-    // barriers: raw_full[NR], raw_empty[NR], a_full[2], a_empty[2],
-    // d_full[NW], d_empty[NW], final
+    // barriers: raw_full[NR], raw_empty[NR], a_full[2][2], a_empty[2][2]
+    // ([decode set][half stage]), d_full[NW], d_empty[NW], final
     static constexpr int NR0 = static_cast<int>((kTcSmemCap - 512) / STAGE);
     static constexpr int NR = NR0 > 6 ? 6 : NR0;               // raw stages in flight
     static_assert(NR >= 3, "raw stages");
     static constexpr uint32_t BARS = NR * STAGE;
-    static constexpr uint32_t NBARS = 2 * NR + 4 + 2 * NW + 1;
+    static constexpr uint32_t NBARS = 2 * NR + 8 + 2 * NW + 1;
     static constexpr uint32_t TSLOT = BARS + 8 * NBARS;
     static constexpr uint32_t ABORT = TSLOT + 4;
     static constexpr uint32_t USED = (ABORT + 4 + 127) / 128 * 128;
@@ -239,20 +239,20 @@ __device__ __forceinline__ int tc_group_xblk(int Q, int g) {
 // tensor-memory columns from `acol` (lane = this row): quad Q at acol + Q * QA,
 // group g of the quad GA columns further per g. All shared-memory loads of
 // the stage are issued before any arithmetic, and one wait covers all stores.
-template <int FMT>
+template <int FMT, int H>
 __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
     using F = TcF<FMT>;
     constexpr int QA = 4 * F::GA;
     if constexpr (FMT == FMT_Q6_K) {
         uint32_t qh[4][4], qa[4][4], qb[4][4];
 #pragma unroll
-        for (int Q = 0; Q < 4; ++Q) {
+        for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
             lds_words_unaligned<4>(rowp + 128 + 16 * Q, qh[Q]);
             lds_words_unaligned<4>(rowp + 16 * Q, qa[Q]);
             lds_words_unaligned<4>(rowp + 64 + 16 * Q, qb[Q]);
         }
 #pragma unroll
-        for (int Q = 0; Q < 4; ++Q) {
+        for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 // group j = Q + 4g: ql run (j & 7), nibble j >> 3, qh field j >> 2 = g
@@ -276,9 +276,9 @@ __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
     } else if constexpr (FMT == FMT_Q4_0) {
         uint32_t qs[8][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) lds_words_unaligned<4>(rowp + F::BB * i + 2, qs[i]);
+        for (int i = 4 * H; i < 4 * H + 4; ++i) lds_words_unaligned<4>(rowp + F::BB * i + 2, qs[i]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 4 * H; i < 4 * H + 4; ++i) {
             uint32_t A[16];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -293,7 +293,7 @@ __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 4 * H; i < 4 * H + 4; ++i) {
             uint32_t qs[8];
             lds_words_unaligned<8>(rowp + F::BB * i + 2, qs);
             uint32_t A[16];
@@ -326,14 +326,26 @@ __device__ __forceinline__ void tc_run16(uint32_t slot, uint32_t (&o)[4]) {
     for (int k = 0; k < 4; ++k) o[k] = SH ? __funnelshift_r(w[Q + k], w[Q + k + 1], SH) : w[Q + k];
 }
 
-// q6_K: quad Q of a super-block whose bytes start at slot + LEAD
-template <int LEAD, int Q>
-__device__ __forceinline__ void tc_q6k_quad_aligned(uint32_t slot, uint32_t acol) {
+// The 16 bytes at slot + off + 4 * QW + sh / 8 (off a multiple of 16, sh 0 or
+// 16) as 4 words: two 16-byte loads and a funnel shift per word.
+template <int QW>
+__device__ __forceinline__ void tc_run16_q(uint32_t addr, uint32_t sh, uint32_t (&o)[4]) {
+    uint32_t w[8];
+    lds128(addr, w);
+    lds128(addr + 16, w + 4);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(w[QW + k], w[QW + k + 1], sh);
+}
+
+// q6_K: quad Q (runtime) of a super-block whose bytes start at slot + 4 * QW +
+// sh / 8; one body per word offset QW keeps the code small
+template <int QW>
+__device__ __forceinline__ void tc_q6k_quad_q(uint32_t slot, int Q, uint32_t sh, uint32_t acol) {
     using F = TcF<FMT_Q6_K>;
     uint32_t qh[4], qa[4], qb[4];
-    tc_run16<LEAD + 128 + 16 * Q>(slot, qh);
-    tc_run16<LEAD + 16 * Q>(slot, qa);
-    tc_run16<LEAD + 64 + 16 * Q>(slot, qb);
+    tc_run16_q<QW>(slot + 128 + 16 * Q, sh, qh);
+    tc_run16_q<QW>(slot + 16 * Q, sh, qa);
+    tc_run16_q<QW>(slot + 64 + 16 * Q, sh, qb);
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
         uint32_t A[8];
@@ -385,43 +397,39 @@ __device__ __forceinline__ void tc_q32_block_aligned(uint32_t slot, uint32_t aco
     tc::st16(acol + 4 * F::GA * (I >> 2) + F::GA * (I & 3), A);
 }
 
-template <int FMT, int LEAD>
-__device__ __forceinline__ void tc_decode_stage_aligned(uint32_t slot, uint32_t acol) {
-    if constexpr (FMT == FMT_Q6_K) {
-        tc_q6k_quad_aligned<LEAD, 0>(slot, acol);
-        tc_q6k_quad_aligned<LEAD, 1>(slot, acol);
-        tc_q6k_quad_aligned<LEAD, 2>(slot, acol);
-        tc_q6k_quad_aligned<LEAD, 3>(slot, acol);
-    } else {
-        tc_q32_block_aligned<FMT, LEAD, 0>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 1>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 2>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 3>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 4>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 5>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 6>(slot, acol);
-        tc_q32_block_aligned<FMT, LEAD, 7>(slot, acol);
-    }
-}
-
-// Decode of a stage: the specialized form when the lead is the same for every
-// row (warp-uniform branch), else the general per-row realignment.
-template <int FMT>
-__device__ __forceinline__ void tc_decode_stage_any(uint32_t slot, uint32_t lead, bool uniform,
-                                                    uint32_t acol) {
+// Decode of half H of a stage (q6_K quads 2H, 2H+1; Q4_0 / Q8_0 blocks
+// 4H..4H+3). When every row has the same lead (row pitch a multiple of 16
+// bytes) the loads are 16-byte loads from the aligned slot: q6_K by word
+// offset of the lead (warp-uniform branch), Q4_0 / Q8_0 only at lead 0 (their
+// stages are 144 / 272 bytes, so every stage starts on a 16-byte boundary).
+// Otherwise the general per-row realignment.
+template <int FMT, int H>
+__device__ __forceinline__ void tc_decode_half(uint32_t slot, uint32_t lead, bool uniform,
+                                               uint32_t acol) {
     if (uniform) {
-        switch (lead) {
-            case 0: tc_decode_stage_aligned<FMT, 0>(slot, acol); return;
-            case 2: tc_decode_stage_aligned<FMT, 2>(slot, acol); return;
-            case 4: tc_decode_stage_aligned<FMT, 4>(slot, acol); return;
-            case 6: tc_decode_stage_aligned<FMT, 6>(slot, acol); return;
-            case 8: tc_decode_stage_aligned<FMT, 8>(slot, acol); return;
-            case 10: tc_decode_stage_aligned<FMT, 10>(slot, acol); return;
-            case 12: tc_decode_stage_aligned<FMT, 12>(slot, acol); return;
-            default: tc_decode_stage_aligned<FMT, 14>(slot, acol); return;
+        if constexpr (FMT == FMT_Q6_K) {
+            const uint32_t sh = (lead & 3u) * 8u;
+#pragma unroll 1
+            for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
+                switch (lead >> 2) {
+                    case 0: tc_q6k_quad_q<0>(slot, Q, sh, acol); break;
+                    case 1: tc_q6k_quad_q<1>(slot, Q, sh, acol); break;
+                    case 2: tc_q6k_quad_q<2>(slot, Q, sh, acol); break;
+                    default: tc_q6k_quad_q<3>(slot, Q, sh, acol); break;
+                }
+            }
+            return;
+        } else {
+            if (lead == 0) {
+                tc_q32_block_aligned<FMT, 0, 4 * H>(slot, acol);
+                tc_q32_block_aligned<FMT, 0, 4 * H + 1>(slot, acol);
+                tc_q32_block_aligned<FMT, 0, 4 * H + 2>(slot, acol);
+                tc_q32_block_aligned<FMT, 0, 4 * H + 3>(slot, acol);
+                return;
+            }
         }
     }
-    tc_decode_stage<FMT>(slot + lead, acol);
+    tc_decode_stage<FMT, H>(slot + lead, acol);
 }
 
 // Scale of group i (issue order) of this thread's row, read from the raw
@@ -570,8 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t b_rfull = sb + L::BARS;
     const uint32_t b_rempty = b_rfull + 8 * NR;
     const uint32_t b_afull = b_rempty + 8 * NR;
-    const uint32_t b_aempty = b_afull + 16;
-    const uint32_t b_dfull = b_aempty + 16;
+    const uint32_t b_aempty = b_afull + 32;
+    const uint32_t b_dfull = b_aempty + 32;
     const uint32_t b_dempty = b_dfull + 8 * NW;
     const uint32_t b_final = b_dempty + 8 * NW;
     const uint32_t flag = sb + L::ABORT;
@@ -585,7 +593,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(b_rfull + 8 * r, 1);
             mbar_init(b_rempty + 8 * r, 9);  // 4 decoders + 4 drainers + the MMA commit
         }
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < 4; ++q) {  // [set][half]
             mbar_init(b_afull + 8 * q, 4);
             mbar_init(b_aempty + 8 * q, 1);
         }
@@ -707,13 +715,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
-                    // the set's A stage: sets take alternate stages
-                    if (!tcmv_wait_one(b_afull + 8 * set, (sc >> 1) & 1u, flag, err)) {
-                        ok = false;
-                        break;
-                    }
                     TCMV_TRACE(1, sc);
-                    tc::fence_after();
                     // descriptors and addresses: per-stage bases plus compile-time
                     // offsets, so the issue loop is a run of MMAs. B operand of
                     // K16 step t: NCOL rows x 16 K at t * NCOL * 32 bytes, core
@@ -723,6 +725,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     uint32_t dbase = 0, ws = 0;
 #pragma unroll
                     for (int i = 0; i < L::GPS; ++i) {
+                        if (i == 0 || i == L::GPS / 2) {
+                            // the half stage of A this group belongs to
+                            const uint32_t ab = 2 * set + (i == 0 ? 0u : 1u);
+                            if (i != 0) tc::commit(b_aempty + 8 * (2 * set));
+                            if (!tcmv_wait_one(b_afull + 8 * ab, (sc >> 1) & 1u, flag, err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc::fence_after();
+                        }
                         if (i % L::G == 0) {
                             const uint32_t wg = wc + i / L::G;
                             ws = wg % NW;
@@ -744,7 +756,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         if (i % L::G == L::G - 1 || i == L::GPS - 1) tc::commit(b_dfull + 8 * ws);
                     }
-                    tc::commit(b_aempty + 8 * set);
+                    tc::commit(b_aempty + 8 * (2 * set + 1));
                     tc::commit(b_rempty + 8 * slot);
                     TCMV_TRACE(2, sc);
                 }
@@ -773,18 +785,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t lead;
                 const uint32_t rslot = tc_row_slot<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, r, s * F::BPS * F::BB, lead);
                 if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(3, sc);
-                // this set's previous A stage has been read by its MMAs
+                // each half of the set's A stage, once its previous contents
+                // have been read by their MMAs: the MMAs of one half run while
+                // the other half is decoded
                 const uint32_t ls = sc >> 1;
-                if (ls >= 1 && !tcmv_wait_warp(b_aempty + 8 * myset, (ls - 1) & 1u, flag, err)) {
-                    ok = false;
-                    break;
+                const bool uni = a.rowbytes % 16 == 0;
+                const uint32_t acol = lane_base + myset * L::SA;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t ab = 2 * myset + h;
+                    if (ls >= 1 && !tcmv_wait_warp(b_aempty + 8 * ab, (ls - 1) & 1u, flag, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    if (h == 0)
+                        tc_decode_half<FMT, 0>(rslot, lead, uni, acol);
+                    else
+                        tc_decode_half<FMT, 1>(rslot, lead, uni, acol);
+                    tc::wait_st();
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_afull + 8 * ab);
                 }
-                tc::fence_after();
-                tc_decode_stage_any<FMT>(rslot, lead, a.rowbytes % 16 == 0, lane_base + myset * L::SA);
-                tc::wait_st();
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_afull + 8 * myset);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_rempty + 8 * slot);
                 if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(4, sc);
