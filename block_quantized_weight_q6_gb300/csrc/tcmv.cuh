@@ -28,22 +28,25 @@
 // Here the unpack ends at an exact bf16 code (one byte-permute and one packed
 // bf16 FMA per two weights) and the activation rows ride in MMA columns.
 //
-// CTA (480 threads, one per SM, persistent over work items = 128-row tile x
+// CTA (512 threads, one per SM, persistent over work items = 128-row tile x
 // a range of 256-wide K stages):
 //   warps 0-7   decode weights -> A; two sets of 4 warps take alternate
 //               stages (row = 32 * (warp % 4) + lane)
 //   warps 8-11  drain D: load the accumulators, apply the scales read from
 //               the raw stage, sum, store
-//   warp 12     producer: per stage, 8 tensor-map copies of the tile's raw
-//               blocks (W seen as rows of 8 weight rows: any row pitch becomes a
-//               16-byte multiple, and one copy brings row j of 16 such groups),
-//               1-D bulk copies for the rows past the last whole group of 8,
-//               and one 1-D bulk copy of the stage's activation tile
+//   warp 12     weight producer: per stage, 8 tensor-map copies of the tile's
+//               raw blocks (W seen as rows of 8 weight rows: any row pitch
+//               becomes a 16-byte multiple, and one copy brings row j of 16
+//               such groups), 1-D bulk copies for the rows past the last whole
+//               group of 8
+//   warp 15     activation producer: one 1-D bulk copy per stage
 //   warps 13-14 issue the MMAs (one thread each, for the stages of one
 //               decode set); warp 13 owns the tensor memory
-// Rings: raw stages (producer -> decoders, drainers, MMA), A slots per
-// decode set (decoders -> MMA), D slots (MMA -> drainers), each with a
-// full / empty mbarrier pair, every wait bounded in time.
+// Rings, each slot with a full / empty mbarrier pair, every wait bounded in
+// time: raw weight stages (producer -> decoders), activation stages
+// (producer -> MMA), group scales (decoders -> drainers), A half stages per
+// decode set (decoders -> MMA), D windows (MMA -> drainers). A raw stage is
+// free again as soon as it has been decoded.
 #pragma once
 
 #include "kernels.h"
@@ -91,25 +94,26 @@ template <int FMT, int NB, int S>
 struct TcLayout {
     using F = TcF<FMT>;
     static constexpr int NCOL = TcCols<NB, S>::NCOL;
-    // raw part of a stage: 8 boxes (row j of every group of 8 rows, 16 groups
-    // per tile), rows one slot RS apart, then a tail area for the up to 7
-    // rows past the last whole group of 8; tensor-map destinations are
-    // 128-byte aligned
+    // raw slot: 8 boxes (row j of every group of 8 rows, 16 groups per tile),
+    // rows one slot RS apart, then a tail area for the up to 7 rows past the
+    // last whole group of 8; tensor-map destinations are 128-byte aligned
     static constexpr uint32_t BOXP = 16u * F::RS;
     static_assert(BOXP % 128 == 0 && (8u * F::RS) % 128 == 0, "box alignment");
     static constexpr uint32_t TAIL = 8 * BOXP;
     static constexpr uint32_t RAW = TAIL + 8u * F::RS;
+    // activation slot: the stage's 16 K16-step B operands
     static constexpr uint32_t XT = static_cast<uint32_t>(NCOL) * kTcStageK * 2;
-    static constexpr uint32_t STAGE = RAW + XT;
     static constexpr int QA = 4 * F::GA;                       // A columns per quad
     static constexpr int SA = F::QPS * QA;                     // A columns per stage (128)
+    static constexpr int GPS = 4 * F::QPS;                     // scale groups per stage
+    // scale slot: the stage's group scales, [group][tensor-memory lane] fp32
+    static constexpr uint32_t SCB = static_cast<uint32_t>(GPS) * 128 * 4;
     // D windows: NCOL columns (one MMA's N), aligned. A window collects the
     // partial sums of G = NCOL / NC consecutive groups (issue order i = 4Q + g):
     // group i's activations fill rows (i % G) * NC .. + NC - 1 of its B
     // operand and every other row is zero, so each group's MMAs add only into
     // its own NC columns; the first MMA into a window starts it from zero.
     static constexpr int NC = NB * S;                          // columns per group
-    static constexpr int GPS = 4 * F::QPS;                     // groups per stage
     static constexpr int G = NCOL / NC;                        // groups per window
     static constexpr int W = (GPS + G - 1) / G;                // windows per stage
     static constexpr uint32_t DCOL0 = 2 * SA;                  // one A stage per decode set
@@ -118,13 +122,21 @@ struct TcLayout {
     static_assert(G >= 1 && NW >= 1, "tensor memory");
     static constexpr uint32_t TNEED = DCOL0 + NW * NCOL;
     static_assert(TNEED <= 512, "tensor memory");
-    // barriers: raw_full[NR], raw_empty[NR], a_full[2][2], a_empty[2][2]
-    // ([decode set][half stage]), d_full[NW], d_empty[NW], final
-    static constexpr int NR0 = static_cast<int>((kTcSmemCap - 512) / STAGE);
-    static constexpr int NR = NR0 > 6 ? 6 : NR0;               // raw stages in flight
+    // rings: raw (producer -> decoders), activations (producer -> MMA),
+    // scales (decoders -> drainers)
+    static constexpr int NX = NCOL == 16 ? 4 : 2;
+    static constexpr int NSC = 3;
+    static constexpr int NR0 =
+        static_cast<int>((kTcSmemCap - NX * XT - NSC * SCB - 1024) / RAW);
+    static constexpr int NR = NR0 > 6 ? 6 : NR0;
     static_assert(NR >= 3, "raw stages");
-    static constexpr uint32_t BARS = NR * STAGE;
-    static constexpr uint32_t NBARS = 2 * NR + 8 + 2 * NW + 1;
+    static constexpr uint32_t XOFF = NR * RAW;
+    static constexpr uint32_t SOFF = XOFF + NX * XT;
+    static constexpr uint32_t BARS = SOFF + NSC * SCB;
+    // barriers: r_full[NR], r_empty[NR], x_full[NX], x_empty[NX], s_full[NSC],
+    // s_empty[NSC], a_full[2][2], a_empty[2][2] ([decode set][half stage]),
+    // d_full[NW], d_empty[NW], final
+    static constexpr uint32_t NBARS = 2 * NR + 2 * NX + 2 * NSC + 8 + 2 * NW + 1;
     static constexpr uint32_t TSLOT = BARS + 8 * NBARS;
     static constexpr uint32_t ABORT = TSLOT + 4;
     static constexpr uint32_t USED = (ABORT + 4 + 127) / 128 * 128;
@@ -153,16 +165,33 @@ __device__ unsigned long long* g_tcmv_trace;
 #endif
 
 // ------------------------------------------------------------ bounded waits
+// A waiting thread sleeps inside try_wait (up to the hint, waking when the
+// phase completes) instead of spinning: the decoding warps share the issue
+// slots with every waiting role.
+constexpr uint32_t kTcSleepNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kTcSleepNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Warp-collective wait that also gives up once another role of the CTA gave
 // up; every lane leaves with the same answer (the tensor-memory operations
 // that follow are .sync.aligned).
 __device__ __forceinline__ bool tcmv_wait_warp(uint32_t bar, uint32_t parity, uint32_t flag,
                                                unsigned int* err) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-        if ((it & 63u) == 0) {
+        if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
+        if ((it & 3u) == 0) {
             int give_up = lds_u32(flag) != 0 ? 1 : 0;
             if (!give_up && globaltimer_ns() - t0 > kWaitLimitNs) give_up = 2;
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
@@ -181,11 +210,11 @@ __device__ __forceinline__ bool tcmv_wait_warp(uint32_t bar, uint32_t parity, ui
 // The same for a single thread.
 __device__ __forceinline__ bool tcmv_wait_one(uint32_t bar, uint32_t parity, uint32_t flag,
                                               unsigned int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        if (mbar_try_wait_sleep(bar, parity)) return true;
+        if ((it & 3u) == 0) {
             if (lds_u32(flag) != 0) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
                 asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(flag), "r"(1u) : "memory");
@@ -397,20 +426,29 @@ __device__ __forceinline__ void tc_q32_block_aligned(uint32_t slot, uint32_t aco
     tc::st16(acol + 4 * F::GA * (I >> 2) + F::GA * (I & 3), A);
 }
 
-// Decode of half H of a stage (q6_K quads 2H, 2H+1; Q4_0 / Q8_0 blocks
-// 4H..4H+3). When every row has the same lead (row pitch a multiple of 16
+// The general per-row realignment, for row pitches that are not multiples of
+// 16 bytes (kept out of line: the common case never runs it).
+template <int FMT>
+__device__ __noinline__ void tc_decode_half_general(uint32_t rowp, uint32_t acol, int h) {
+    if (h == 0)
+        tc_decode_stage<FMT, 0>(rowp, acol);
+    else
+        tc_decode_stage<FMT, 1>(rowp, acol);
+}
+
+// Decode of half h of a stage (q6_K quads 2h, 2h+1; Q4_0 / Q8_0 blocks
+// 4h..4h+3). When every row has the same lead (row pitch a multiple of 16
 // bytes) the loads are 16-byte loads from the aligned slot: q6_K by word
 // offset of the lead (warp-uniform branch), Q4_0 / Q8_0 only at lead 0 (their
 // stages are 144 / 272 bytes, so every stage starts on a 16-byte boundary).
-// Otherwise the general per-row realignment.
-template <int FMT, int H>
+template <int FMT>
 __device__ __forceinline__ void tc_decode_half(uint32_t slot, uint32_t lead, bool uniform,
-                                               uint32_t acol) {
+                                               uint32_t acol, int h) {
     if (uniform) {
         if constexpr (FMT == FMT_Q6_K) {
             const uint32_t sh = (lead & 3u) * 8u;
 #pragma unroll 1
-            for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
+            for (int Q = 2 * h; Q < 2 * h + 2; ++Q) {
                 switch (lead >> 2) {
                     case 0: tc_q6k_quad_q<0>(slot, Q, sh, acol); break;
                     case 1: tc_q6k_quad_q<1>(slot, Q, sh, acol); break;
@@ -421,30 +459,54 @@ __device__ __forceinline__ void tc_decode_half(uint32_t slot, uint32_t lead, boo
             return;
         } else {
             if (lead == 0) {
-                tc_q32_block_aligned<FMT, 0, 4 * H>(slot, acol);
-                tc_q32_block_aligned<FMT, 0, 4 * H + 1>(slot, acol);
-                tc_q32_block_aligned<FMT, 0, 4 * H + 2>(slot, acol);
-                tc_q32_block_aligned<FMT, 0, 4 * H + 3>(slot, acol);
+                if (h == 0) {
+                    tc_q32_block_aligned<FMT, 0, 0>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 1>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 2>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 3>(slot, acol);
+                } else {
+                    tc_q32_block_aligned<FMT, 0, 4>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 5>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 6>(slot, acol);
+                    tc_q32_block_aligned<FMT, 0, 7>(slot, acol);
+                }
                 return;
             }
         }
     }
-    tc_decode_stage<FMT, H>(slot + lead, acol);
+    tc_decode_half_general<FMT>(slot + lead, acol, h);
 }
 
-// Scale of group i (issue order) of this thread's row, read from the raw
-// stage. Blocks past the end of the row (last stage of a ragged K) hold
-// stale bytes; their activations are zero and their scale is 0.
+// The scale of every group of this thread's row in the stage (issue order),
+// stored into the scale slot at [group][lane m]. Blocks past the end of the
+// row (last stage of a ragged K) hold stale bytes; their activations are zero
+// and their scale is 0.
 template <int FMT>
-__device__ __forceinline__ float tc_group_scale(uint32_t rowp, int i, int nblk) {
+__device__ __forceinline__ void tc_store_scales(uint32_t rowp, int nblk, uint32_t sslot, int m) {
+    using F = TcF<FMT>;
     if constexpr (FMT == FMT_Q6_K) {
-        const int j = (i >> 2) + 4 * (i & 3);  // the group's index in the super-block
+        const float d = half_bits_to_float(lds_u16(rowp + 208));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int j = (i >> 2) + 4 * (i & 3);  // the group's index in the super-block
+            const float v = d * static_cast<float>(lds_s8(rowp + 192 + j));
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (i * 128 + m) * 4), "f"(v) : "memory");
+        }
         (void)nblk;
-        return half_bits_to_float(lds_u16(rowp + 208)) * static_cast<float>(lds_s8(rowp + 192 + j));
     } else {
-        const float d = half_bits_to_float(lds_u16(rowp + TcF<FMT>::BB * i));
-        return i < nblk ? d : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float d = half_bits_to_float(lds_u16(rowp + F::BB * i));
+            const float v = i < nblk ? d : 0.0f;
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (i * 128 + m) * 4), "f"(v) : "memory");
+        }
     }
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
 }
 
 // ------------------------------------------------------------ drain a window
@@ -461,7 +523,7 @@ __device__ __forceinline__ void tc_ld_window(uint32_t taddr, uint32_t (&v)[NCOL]
 }
 
 template <int FMT, int NB, int S, bool Q8>
-__device__ __forceinline__ void tc_drain_window(uint32_t dcol, uint32_t rowp, int w, int nblk,
+__device__ __forceinline__ void tc_drain_window(uint32_t dcol, uint32_t sslot, int m, int w,
                                                 int64_t xblk0, const TcmvArgs& a, float (&acc)[NB]) {
     using L = TcLayout<FMT, NB, S>;
     constexpr int NCOL = L::NCOL, NC = L::NC, G = L::G;
@@ -471,7 +533,7 @@ __device__ __forceinline__ void tc_drain_window(uint32_t dcol, uint32_t rowp, in
 #pragma unroll
     for (int u = 0; u < G; ++u) {
         const int i = w * G + u;
-        sg[u] = i < L::GPS ? tc_group_scale<FMT>(rowp, i, nblk) : 0.0f;
+        sg[u] = i < L::GPS ? lds_f32(sslot + (i * 128 + m) * 4) : 0.0f;
     }
     tc::wait_ld();
 #pragma unroll
@@ -571,13 +633,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     using F = TcF<FMT>;
     using L = TcLayout<FMT, NB, S>;
     constexpr int NCOL = L::NCOL;
-    constexpr int NR = L::NR, NW = L::NW;
+    constexpr int NR = L::NR, NX = L::NX, NSC = L::NSC, NW = L::NW;
     constexpr uint32_t IDESC = tc::idesc_bf16(128, NCOL);
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t sb = smem_u32(smem);
     const uint32_t b_rfull = sb + L::BARS;
     const uint32_t b_rempty = b_rfull + 8 * NR;
-    const uint32_t b_afull = b_rempty + 8 * NR;
+    const uint32_t b_xfull = b_rempty + 8 * NR;
+    const uint32_t b_xempty = b_xfull + 8 * NX;
+    const uint32_t b_sfull = b_xempty + 8 * NX;
+    const uint32_t b_sempty = b_sfull + 8 * NSC;
+    const uint32_t b_afull = b_sempty + 8 * NSC;
     const uint32_t b_aempty = b_afull + 32;
     const uint32_t b_dfull = b_aempty + 32;
     const uint32_t b_dempty = b_dfull + 8 * NW;
@@ -591,7 +657,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < NR; ++r) {
             mbar_init(b_rfull + 8 * r, 1);
-            mbar_init(b_rempty + 8 * r, 9);  // 4 decoders + 4 drainers + the MMA commit
+            mbar_init(b_rempty + 8 * r, 4);  // the 4 warps of the decode set
+        }
+        for (int r = 0; r < NX; ++r) {
+            mbar_init(b_xfull + 8 * r, 1);
+            mbar_init(b_xempty + 8 * r, 1);  // the MMA commit
+        }
+        for (int r = 0; r < NSC; ++r) {
+            mbar_init(b_sfull + 8 * r, 4);
+            mbar_init(b_sempty + 8 * r, 4);
         }
         for (int q = 0; q < 4; ++q) {  // [set][half]
             mbar_init(b_afull + 8 * q, 4);
@@ -612,27 +686,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = lds_u32(sb + L::TSLOT);
 
     if (warp == 12) {
-        // ---------------------------------------------------- producer
+        // ---------------------------------------------------- raw producer
+        // Weights only: they are constant, so no wait for the kernel that
+        // precedes this one.
         const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
-        uint32_t issued = 0;
-        bool waited = false, ok = true;
-        int64_t pend[NR];
-        int npend = 0;
-        auto issue_x = [&](uint32_t slot, int64_t s) {
-            if (lane == 0)
-                bulk_g2s(sb + slot * L::STAGE + L::RAW, a.xt + s * (NCOL * kTcStageK), L::XT,
-                         b_rfull + 8 * slot);
-        };
+        uint32_t sc = 0;
+        bool ok = true;
         for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
             const TcItem it = tc_item(a, item);
-            for (int64_t s = it.s0; s < it.s1; ++s) {
-                const uint32_t slot = issued % NR;
-                if (issued >= static_cast<uint32_t>(NR) &&
-                    !tcmv_wait_warp(b_rempty + 8 * slot, ((issued / NR) - 1) & 1u, flag, err)) {
+            for (int64_t s = it.s0; s < it.s1; ++s, ++sc) {
+                const uint32_t slot = sc % NR;
+                if (sc >= static_cast<uint32_t>(NR) &&
+                    !tcmv_wait_warp(b_rempty + 8 * slot, ((sc / NR) - 1) & 1u, flag, err)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst0 = sb + slot * L::STAGE;
+                const uint32_t dst0 = sb + slot * L::RAW;
                 const uint32_t bar = b_rfull + 8 * slot;
                 const int64_t kb0 = s * F::BPS;
                 const int64_t koff = kb0 * F::BB;  // byte offset of the stage within a row
@@ -664,8 +733,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive_expect_tx(bar, bytes + L::XT + (boxes ? 8u * 16u * F::RS : 0u));
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes + (boxes ? 8u * 16u * F::RS : 0u));
                 __syncwarp();
                 if (boxes && lane < 8) {
                     // box j: row j of the 16 groups of 8 rows of this tile
@@ -675,30 +743,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (ce > cs)
                     bulk_g2s(dst0 + L::TAIL + tr * F::RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
-                if (lane == 0) TCMV_TRACE(0, issued);
-                if (waited)
-                    issue_x(slot, s);
-                else
-                    pend[npend++] = s;
-                ++issued;
-                // the weights of the first stages go out before waiting for the
-                // kernel that wrote the activation tile
-                if (!waited && issued == static_cast<uint32_t>(NR)) {
-                    grid_dependency_wait();
-                    waited = true;
-                    for (int p = 0; p < npend; ++p) issue_x(static_cast<uint32_t>(p), pend[p]);
-                    npend = 0;
-                }
+                if (lane == 0) TCMV_TRACE(0, sc);
             }
         }
-        if (!waited) {
-            grid_dependency_wait();
-            for (int p = 0; p < npend; ++p) issue_x(static_cast<uint32_t>(p), pend[p]);
-        }
         // wait (bounded) for the copies still in flight before leaving
-        for (uint32_t u = issued > static_cast<uint32_t>(NR) ? issued - NR : 0; u < issued; ++u)
+        for (uint32_t u = sc > static_cast<uint32_t>(NR) ? sc - NR : 0; u < sc; ++u)
             (void)tcmv_wait_warp(b_rfull + 8 * (u % NR), (u / NR) & 1u, flag, err);
-    } else if (warp >= 13) {
+    } else if (warp == 15) {
+        // ---------------------------------------------------- activation producer
+        grid_dependency_wait();  // the activation tile is written by the previous kernel
+        uint32_t sc = 0;
+        bool ok = true;
+        for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
+            const TcItem it = tc_item(a, item);
+            for (int64_t s = it.s0; s < it.s1; ++s, ++sc) {
+                const uint32_t slot = sc % NX;
+                if (sc >= static_cast<uint32_t>(NX) &&
+                    !tcmv_wait_warp(b_xempty + 8 * slot, ((sc / NX) - 1) & 1u, flag, err)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(b_xfull + 8 * slot, L::XT);
+                    bulk_g2s(sb + L::XOFF + slot * L::XT, a.xt + s * (NCOL * kTcStageK), L::XT,
+                             b_xfull + 8 * slot);
+                }
+                __syncwarp();
+            }
+        }
+        for (uint32_t u = sc > static_cast<uint32_t>(NX) ? sc - NX : 0; u < sc; ++u)
+            (void)tcmv_wait_warp(b_xfull + 8 * (u % NX), (u / NX) & 1u, flag, err);
+    } else if (warp == 13 || warp == 14) {
         // ---------------------------------------------------- MMA issue (set = warp - 13)
         const uint32_t myset = static_cast<uint32_t>(warp - 13);
         if (lane == 0) {
@@ -709,9 +784,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
                     const uint32_t set = sc & 1u;
                     if (set != myset) continue;
-                    const uint32_t slot = sc % NR;
+                    const uint32_t xslot = sc % NX;
                     const uint32_t wc = sc * L::W;  // windows of the earlier stages
-                    if (!tcmv_wait_one(b_rfull + 8 * slot, (sc / NR) & 1u, flag, err)) {
+                    if (!tcmv_wait_one(b_xfull + 8 * xslot, (sc / NX) & 1u, flag, err)) {
                         ok = false;
                         break;
                     }
@@ -720,7 +795,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // offsets, so the issue loop is a run of MMAs. B operand of
                     // K16 step t: NCOL rows x 16 K at t * NCOL * 32 bytes, core
                     // matrices 128 bytes apart along K, 256 between 8-row groups.
-                    const uint64_t bdesc0 = tc::smem_desc(sb + slot * L::STAGE + L::RAW, 128, 256);
+                    const uint64_t bdesc0 = tc::smem_desc(sb + L::XOFF + xslot * L::XT, 128, 256);
                     const uint32_t abase = tmem + set * L::SA;
                     uint32_t dbase = 0, ws = 0;
 #pragma unroll
@@ -757,7 +832,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (i % L::G == L::G - 1 || i == L::GPS - 1) tc::commit(b_dfull + 8 * ws);
                     }
                     tc::commit(b_aempty + 8 * (2 * set + 1));
-                    tc::commit(b_rempty + 8 * slot);
+                    tc::commit(b_xempty + 8 * xslot);
                     TCMV_TRACE(2, sc);
                 }
             }
@@ -769,7 +844,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp < 8) {
         // ---------------------------------------------------- decode (set = warp / 4)
         const uint32_t myset = static_cast<uint32_t>(warp >> 2);
-        const int r = tc_lane_row(32 * (warp & 3) + lane);
+        const int m = 32 * (warp & 3) + lane;
+        const int r = tc_lane_row(m);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         uint32_t sc = 0;
         bool ok = true;
@@ -777,21 +853,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const TcItem it = tc_item(a, item);
             for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
                 if ((sc & 1u) != myset) continue;
-                const uint32_t slot = sc % NR;
+                const uint32_t slot = sc % NR, sslot = sc % NSC;
                 if (!tcmv_wait_warp(b_rfull + 8 * slot, (sc / NR) & 1u, flag, err)) {
                     ok = false;
                     break;
                 }
+                const int64_t kb0 = s * F::BPS;
+                const int nblk = static_cast<int>(min(static_cast<int64_t>(F::BPS), a.nb - kb0));
                 uint32_t lead;
-                const uint32_t rslot = tc_row_slot<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, r, s * F::BPS * F::BB, lead);
+                const uint32_t rslot =
+                    tc_row_slot<FMT, NB, S>(a, sb + slot * L::RAW, it.tile, r, kb0 * F::BB, lead);
                 if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(3, sc);
+                // the group scales, for the drainers
+                if (sc >= static_cast<uint32_t>(NSC) &&
+                    !tcmv_wait_warp(b_sempty + 8 * sslot, ((sc / NSC) - 1) & 1u, flag, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_store_scales<FMT>(rslot + lead, nblk, sb + L::SOFF + sslot * L::SCB, m);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_sfull + 8 * sslot);
                 // each half of the set's A stage, once its previous contents
                 // have been read by their MMAs: the MMAs of one half run while
                 // the other half is decoded
                 const uint32_t ls = sc >> 1;
                 const bool uni = a.rowbytes % 16 == 0;
                 const uint32_t acol = lane_base + myset * L::SA;
-#pragma unroll
+#pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t ab = 2 * myset + h;
                     if (ls >= 1 && !tcmv_wait_warp(b_aempty + 8 * ab, (ls - 1) & 1u, flag, err)) {
@@ -799,10 +887,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    if (h == 0)
-                        tc_decode_half<FMT, 0>(rslot, lead, uni, acol);
-                    else
-                        tc_decode_half<FMT, 1>(rslot, lead, uni, acol);
+                    tc_decode_half<FMT>(rslot, lead, uni, acol, h);
                     tc::wait_st();
                     tc::fence_before();
                     __syncwarp();
@@ -814,8 +899,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
     } else {
-        // ---------------------------------------------------- drain
-        const int r = tc_lane_row(32 * (warp & 3) + lane);
+        // ---------------------------------------------------- drain (warps 8-11)
+        const int m = 32 * (warp & 3) + lane;
+        const int r = tc_lane_row(m);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         grid_dependency_wait();  // y, the partial sums and the activation scales
         uint32_t wc = 0, sc = 0;
@@ -827,16 +913,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int b = 0; b < NB; ++b) acc[b] = 0.0f;
             for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
-                const uint32_t slot = sc % NR;
-                if (!tcmv_wait_warp(b_rfull + 8 * slot, (sc / NR) & 1u, flag, err)) {
+                const uint32_t sslot = sc % NSC;
+                if (!tcmv_wait_warp(b_sfull + 8 * sslot, (sc / NSC) & 1u, flag, err)) {
                     ok = false;
                     break;
                 }
-                const int64_t kb0 = s * F::BPS;
-                const int nblk = static_cast<int>(min(static_cast<int64_t>(F::BPS), a.nb - kb0));
-                uint32_t lead;
-                const uint32_t rowp =
-                    tc_row_slot<FMT, NB, S>(a, sb + slot * L::STAGE, it.tile, r, kb0 * F::BB, lead) + lead;
+                const uint32_t scales = sb + L::SOFF + sslot * L::SCB;
 #pragma unroll 1
                 for (int w = 0; w < L::W; ++w, ++wc) {
                     const uint32_t ws = wc % NW;
@@ -846,7 +928,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     if (warp == 8 && lane == 0) TCMV_TRACE(5, wc);
                     tc::fence_after();
-                    tc_drain_window<FMT, NB, S, Q8>(lane_base + L::DCOL0 + ws * NCOL, rowp, w, nblk,
+                    tc_drain_window<FMT, NB, S, Q8>(lane_base + L::DCOL0 + ws * NCOL, scales, m, w,
                                                     s * (kTcStageK / 32), a, acc);
                     tc::fence_before();
                     __syncwarp();
@@ -854,7 +936,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (warp == 8 && lane == 0) TCMV_TRACE(6, wc);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(b_rempty + 8 * slot);
+                if (lane == 0) mbar_arrive(b_sempty + 8 * sslot);
             }
             if (ok && n < a.N) {
 #pragma unroll
