@@ -119,7 +119,11 @@ struct TcLayout {
     static constexpr uint32_t DCOL0 = 2 * SA;                  // one A stage per decode set
     static constexpr int NW0 = static_cast<int>((512 - DCOL0) / NCOL);
     static constexpr int NW = NW0 > 16 ? 16 : NW0;             // windows in flight
-    static_assert(G >= 1 && NW >= 1, "tensor memory");
+    // each MMA issuer (decode set) has its own NWS windows, so a window is
+    // reused only after the drain of that issuer's previous use of it, and
+    // every wait targets the latest phase of its barrier
+    static constexpr int NWS = NW / 2;
+    static_assert(G >= 1 && NWS >= 1, "tensor memory");
     static constexpr uint32_t TNEED = DCOL0 + NW * NCOL;
     static_assert(TNEED <= 512, "tensor memory");
     // rings: raw (producer -> decoders), activations (producer -> MMA),
@@ -785,7 +789,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t set = sc & 1u;
                     if (set != myset) continue;
                     const uint32_t xslot = sc % NX;
-                    const uint32_t wc = sc * L::W;  // windows of the earlier stages
+                    const uint32_t wc = (sc >> 1) * L::W;  // this set's earlier windows
                     if (!tcmv_wait_one(b_xfull + 8 * xslot, (sc / NX) & 1u, flag, err)) {
                         ok = false;
                         break;
@@ -812,9 +816,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         if (i % L::G == 0) {
                             const uint32_t wg = wc + i / L::G;
-                            ws = wg % NW;
-                            if (wg >= static_cast<uint32_t>(NW) &&
-                                !tcmv_wait_one(b_dempty + 8 * ws, ((wg / NW) - 1) & 1u, flag, err)) {
+                            ws = set * L::NWS + wg % L::NWS;
+                            if (wg >= static_cast<uint32_t>(L::NWS) &&
+                                !tcmv_wait_one(b_dempty + 8 * ws, ((wg / L::NWS) - 1) & 1u, flag, err)) {
                                 ok = false;
                                 break;
                             }
@@ -904,7 +908,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r = tc_lane_row(m);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         grid_dependency_wait();  // y, the partial sums and the activation scales
-        uint32_t wc = 0, sc = 0;
+        uint32_t sc = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
             const TcItem it = tc_item(a, item);
@@ -919,10 +923,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     break;
                 }
                 const uint32_t scales = sb + L::SOFF + sslot * L::SCB;
+                const uint32_t set = sc & 1u;
 #pragma unroll 1
-                for (int w = 0; w < L::W; ++w, ++wc) {
-                    const uint32_t ws = wc % NW;
-                    if (!tcmv_wait_warp(b_dfull + 8 * ws, (wc / NW) & 1u, flag, err)) {
+                for (int w = 0; w < L::W; ++w) {
+                    const uint32_t wc = (sc >> 1) * L::W + w;  // the set's window count
+                    const uint32_t ws = set * L::NWS + wc % L::NWS;
+                    if (!tcmv_wait_warp(b_dfull + 8 * ws, (wc / L::NWS) & 1u, flag, err)) {
                         ok = false;
                         break;
                     }
