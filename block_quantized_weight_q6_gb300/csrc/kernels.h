@@ -42,7 +42,7 @@ cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_
 
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
-constexpr int kTcThreads = 512;
+constexpr int kTcThreads = 768;
 struct TcmvArgs {
     const uint8_t* W;
     int64_t N, K, nb;      // rows, columns, blocks per row

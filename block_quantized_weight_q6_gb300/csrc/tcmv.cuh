@@ -28,20 +28,18 @@
 // Here the unpack ends at an exact bf16 code (one byte-permute and one packed
 // bf16 FMA per two weights) and the activation rows ride in MMA columns.
 //
-// CTA (512 threads, one per SM, persistent over work items = 128-row tile x
-// a range of 256-wide K stages):
-//   warps 0-7   decode weights -> A; two sets of 4 warps take alternate
-//               stages (row = 32 * (warp % 4) + lane)
-//   warps 8-11  drain D: load the accumulators, apply the scales read from
-//               the raw stage, sum, store
-//   warp 12     weight producer: per stage, 8 tensor-map copies of the tile's
-//               raw blocks (W seen as rows of 8 weight rows: any row pitch
-//               becomes a 16-byte multiple, and one copy brings row j of 16
-//               such groups), 1-D bulk copies for the rows past the last whole
-//               group of 8
-//   warp 15     activation producer: one 1-D bulk copy per stage
-//   warps 13-14 issue the MMAs (one thread each, for the stages of one
-//               decode set); warp 13 owns the tensor memory
+// CTA (768 threads, one per SM, persistent over work items = 128-row tile x
+// a range of 256-wide K stages), warps by role:
+//   0-15   decoders: two sets of 8 warps take alternate stages; in a set,
+//          warps w and w + 4 cover the same tensor-memory lanes and split the
+//          quads of each half stage (row = tc_lane_row(32 * (warp % 4) + lane))
+//   16-19  drainers: load the accumulators, apply the scales, sum, store
+//   20     weight producer: per stage, 8 tensor-map copies of the tile's raw
+//          blocks (W seen as rows of 8 weight rows: any row pitch becomes a
+//          16-byte multiple, and one copy brings row j of 16 such groups),
+//          1-D bulk copies for the rows past the last whole group of 8
+//   21-22  MMA issue, one thread per decode set; warp 21 owns the tensor memory
+//   23     activation producer: one 1-D bulk copy per stage
 // Rings, each slot with a full / empty mbarrier pair, every wait bounded in
 // time: raw weight stages (producer -> decoders), activation stages
 // (producer -> MMA), group scales (decoders -> drainers), A half stages per
@@ -272,20 +270,22 @@ __device__ __forceinline__ int tc_group_xblk(int Q, int g) {
 // tensor-memory columns from `acol` (lane = this row): quad Q at acol + Q * QA,
 // group g of the quad GA columns further per g. All shared-memory loads of
 // the stage are issued before any arithmetic, and one wait covers all stores.
-template <int FMT, int H>
+// part P of half H of the stage: q6_K quad 2H + P; Q4_0 / Q8_0 blocks
+// 4H + 2P and 4H + 2P + 1
+template <int FMT, int H, int P>
 __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
     using F = TcF<FMT>;
     constexpr int QA = 4 * F::GA;
     if constexpr (FMT == FMT_Q6_K) {
         uint32_t qh[4][4], qa[4][4], qb[4][4];
 #pragma unroll
-        for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
+        for (int Q = 2 * H + P; Q < 2 * H + P + 1; ++Q) {
             lds_words_unaligned<4>(rowp + 128 + 16 * Q, qh[Q]);
             lds_words_unaligned<4>(rowp + 16 * Q, qa[Q]);
             lds_words_unaligned<4>(rowp + 64 + 16 * Q, qb[Q]);
         }
 #pragma unroll
-        for (int Q = 2 * H; Q < 2 * H + 2; ++Q) {
+        for (int Q = 2 * H + P; Q < 2 * H + P + 1; ++Q) {
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 // group j = Q + 4g: ql run (j & 7), nibble j >> 3, qh field j >> 2 = g
@@ -309,9 +309,9 @@ __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
     } else if constexpr (FMT == FMT_Q4_0) {
         uint32_t qs[8][4];
 #pragma unroll
-        for (int i = 4 * H; i < 4 * H + 4; ++i) lds_words_unaligned<4>(rowp + F::BB * i + 2, qs[i]);
+        for (int i = 4 * H + 2 * P; i < 4 * H + 2 * P + 2; ++i) lds_words_unaligned<4>(rowp + F::BB * i + 2, qs[i]);
 #pragma unroll
-        for (int i = 4 * H; i < 4 * H + 4; ++i) {
+        for (int i = 4 * H + 2 * P; i < 4 * H + 2 * P + 2; ++i) {
             uint32_t A[16];
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -326,7 +326,7 @@ __device__ __forceinline__ void tc_decode_stage(uint32_t rowp, uint32_t acol) {
         }
     } else {
 #pragma unroll
-        for (int i = 4 * H; i < 4 * H + 4; ++i) {
+        for (int i = 4 * H + 2 * P; i < 4 * H + 2 * P + 2; ++i) {
             uint32_t qs[8];
             lds_words_unaligned<8>(rowp + F::BB * i + 2, qs);
             uint32_t A[16];
@@ -433,52 +433,61 @@ __device__ __forceinline__ void tc_q32_block_aligned(uint32_t slot, uint32_t aco
 // The general per-row realignment, for row pitches that are not multiples of
 // 16 bytes (kept out of line: the common case never runs it).
 template <int FMT>
-__device__ __noinline__ void tc_decode_half_general(uint32_t rowp, uint32_t acol, int h) {
-    if (h == 0)
-        tc_decode_stage<FMT, 0>(rowp, acol);
-    else
-        tc_decode_stage<FMT, 1>(rowp, acol);
+__device__ __noinline__ void tc_decode_half_general(uint32_t rowp, uint32_t acol, int h, int p) {
+    if (h == 0) {
+        if (p == 0) tc_decode_stage<FMT, 0, 0>(rowp, acol);
+        else tc_decode_stage<FMT, 0, 1>(rowp, acol);
+    } else {
+        if (p == 0) tc_decode_stage<FMT, 1, 0>(rowp, acol);
+        else tc_decode_stage<FMT, 1, 1>(rowp, acol);
+    }
 }
 
-// Decode of half h of a stage (q6_K quads 2h, 2h+1; Q4_0 / Q8_0 blocks
-// 4h..4h+3). When every row has the same lead (row pitch a multiple of 16
-// bytes) the loads are 16-byte loads from the aligned slot: q6_K by word
+// Decode of part p of half h of a stage (q6_K quad 2h + p; Q4_0 / Q8_0
+// blocks 4h + 2p, 4h + 2p + 1): the two 4-warp parts of a decode set share
+// each half stage. When every row has the same lead (row pitch a multiple of
+// 16 bytes) the loads are 16-byte loads from the aligned slot: q6_K by word
 // offset of the lead (warp-uniform branch), Q4_0 / Q8_0 only at lead 0 (their
 // stages are 144 / 272 bytes, so every stage starts on a 16-byte boundary).
 template <int FMT>
 __device__ __forceinline__ void tc_decode_half(uint32_t slot, uint32_t lead, bool uniform,
-                                               uint32_t acol, int h) {
+                                               uint32_t acol, int h, int p) {
     if (uniform) {
         if constexpr (FMT == FMT_Q6_K) {
             const uint32_t sh = (lead & 3u) * 8u;
-#pragma unroll 1
-            for (int Q = 2 * h; Q < 2 * h + 2; ++Q) {
-                switch (lead >> 2) {
-                    case 0: tc_q6k_quad_q<0>(slot, Q, sh, acol); break;
-                    case 1: tc_q6k_quad_q<1>(slot, Q, sh, acol); break;
-                    case 2: tc_q6k_quad_q<2>(slot, Q, sh, acol); break;
-                    default: tc_q6k_quad_q<3>(slot, Q, sh, acol); break;
-                }
+            const int Q = 2 * h + p;
+            switch (lead >> 2) {
+                case 0: tc_q6k_quad_q<0>(slot, Q, sh, acol); break;
+                case 1: tc_q6k_quad_q<1>(slot, Q, sh, acol); break;
+                case 2: tc_q6k_quad_q<2>(slot, Q, sh, acol); break;
+                default: tc_q6k_quad_q<3>(slot, Q, sh, acol); break;
             }
             return;
         } else {
             if (lead == 0) {
-                if (h == 0) {
-                    tc_q32_block_aligned<FMT, 0, 0>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 1>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 2>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 3>(slot, acol);
-                } else {
-                    tc_q32_block_aligned<FMT, 0, 4>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 5>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 6>(slot, acol);
-                    tc_q32_block_aligned<FMT, 0, 7>(slot, acol);
+                switch (2 * h + p) {
+                    case 0:
+                        tc_q32_block_aligned<FMT, 0, 0>(slot, acol);
+                        tc_q32_block_aligned<FMT, 0, 1>(slot, acol);
+                        break;
+                    case 1:
+                        tc_q32_block_aligned<FMT, 0, 2>(slot, acol);
+                        tc_q32_block_aligned<FMT, 0, 3>(slot, acol);
+                        break;
+                    case 2:
+                        tc_q32_block_aligned<FMT, 0, 4>(slot, acol);
+                        tc_q32_block_aligned<FMT, 0, 5>(slot, acol);
+                        break;
+                    default:
+                        tc_q32_block_aligned<FMT, 0, 6>(slot, acol);
+                        tc_q32_block_aligned<FMT, 0, 7>(slot, acol);
+                        break;
                 }
                 return;
             }
         }
     }
-    tc_decode_half_general<FMT>(slot + lead, acol, h);
+    tc_decode_half_general<FMT>(slot + lead, acol, h, p);
 }
 
 // The scale of every group of this thread's row in the stage (issue order),
@@ -486,20 +495,24 @@ __device__ __forceinline__ void tc_decode_half(uint32_t slot, uint32_t lead, boo
 // row (last stage of a ragged K) hold stale bytes; their activations are zero
 // and their scale is 0.
 template <int FMT>
-__device__ __forceinline__ void tc_store_scales(uint32_t rowp, int nblk, uint32_t sslot, int m) {
+__device__ __forceinline__ void tc_store_scales(uint32_t rowp, int nblk, uint32_t sslot, int m, int p) {
     using F = TcF<FMT>;
     if constexpr (FMT == FMT_Q6_K) {
+        // part p: the groups of quads p and p + 2 (issue order i = 4Q + g)
         const float d = half_bits_to_float(lds_u16(rowp + 208));
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int u = 0; u < 8; ++u) {
+            const int i = 4 * (p + 2 * (u >> 2)) + (u & 3);
             const int j = (i >> 2) + 4 * (i & 3);  // the group's index in the super-block
             const float v = d * static_cast<float>(lds_s8(rowp + 192 + j));
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (i * 128 + m) * 4), "f"(v) : "memory");
         }
         (void)nblk;
     } else {
+        // part p: blocks 2p, 2p + 1, 4 + 2p, 5 + 2p
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int u = 0; u < 4; ++u) {
+            const int i = 2 * p + (u & 1) + 4 * (u >> 1);
             const float d = half_bits_to_float(lds_u16(rowp + F::BB * i));
             const float v = i < nblk ? d : 0.0f;
             asm volatile("st.shared.f32 [%0], %1;" ::"r"(sslot + (i * 128 + m) * 4), "f"(v) : "memory");
@@ -661,18 +674,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (threadIdx.x == 0) {
         for (int r = 0; r < NR; ++r) {
             mbar_init(b_rfull + 8 * r, 1);
-            mbar_init(b_rempty + 8 * r, 4);  // the 4 warps of the decode set
+            mbar_init(b_rempty + 8 * r, 8);  // the 8 warps of the decode set
         }
         for (int r = 0; r < NX; ++r) {
             mbar_init(b_xfull + 8 * r, 1);
             mbar_init(b_xempty + 8 * r, 1);  // the MMA commit
         }
         for (int r = 0; r < NSC; ++r) {
-            mbar_init(b_sfull + 8 * r, 4);
+            mbar_init(b_sfull + 8 * r, 8);
             mbar_init(b_sempty + 8 * r, 4);
         }
         for (int q = 0; q < 4; ++q) {  // [set][half]
-            mbar_init(b_afull + 8 * q, 4);
+            mbar_init(b_afull + 8 * q, 8);
             mbar_init(b_aempty + 8 * q, 1);
         }
         for (int q = 0; q < NW; ++q) {
@@ -683,13 +696,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(flag), "r"(0u) : "memory");
         fence_mbar_init();
     }
-    if (warp == 13) tc::alloc(sb + L::TSLOT, 512);
+    // warps: 0-15 decode (set = warp / 8, part = warp / 4 % 2), 16-19 drain,
+    // 20 weight producer, 21-22 MMA issue, 23 activation producer
+    constexpr int kDrain0 = 16, kProdW = 20, kMma0 = 21, kProdX = 23;
+    if (warp == kMma0) tc::alloc(sb + L::TSLOT, 512);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = lds_u32(sb + L::TSLOT);
 
-    if (warp == 12) {
+    if (warp == kProdW) {
         // ---------------------------------------------------- raw producer
         // Weights only: they are constant, so no wait for the kernel that
         // precedes this one.
@@ -753,7 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // wait (bounded) for the copies still in flight before leaving
         for (uint32_t u = sc > static_cast<uint32_t>(NR) ? sc - NR : 0; u < sc; ++u)
             (void)tcmv_wait_warp(b_rfull + 8 * (u % NR), (u / NR) & 1u, flag, err);
-    } else if (warp == 15) {
+    } else if (warp == kProdX) {
         // ---------------------------------------------------- activation producer
         grid_dependency_wait();  // the activation tile is written by the previous kernel
         uint32_t sc = 0;
@@ -777,9 +793,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (uint32_t u = sc > static_cast<uint32_t>(NX) ? sc - NX : 0; u < sc; ++u)
             (void)tcmv_wait_warp(b_xfull + 8 * (u % NX), (u / NX) & 1u, flag, err);
-    } else if (warp == 13 || warp == 14) {
-        // ---------------------------------------------------- MMA issue (set = warp - 13)
-        const uint32_t myset = static_cast<uint32_t>(warp - 13);
+    } else if (warp == kMma0 || warp == kMma0 + 1) {
+        // ---------------------------------------------------- MMA issue (set = warp - kMma0)
+        const uint32_t myset = static_cast<uint32_t>(warp - kMma0);
         if (lane == 0) {
             uint32_t sc = 0;  // stages walked
             bool ok = true;
@@ -845,9 +861,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             (void)tcmv_wait_one(b_final, 0, flag, err);
         }
         __syncwarp();
-    } else if (warp < 8) {
+    } else if (warp < kDrain0) {
         // ---------------------------------------------------- decode (set = warp / 4)
-        const uint32_t myset = static_cast<uint32_t>(warp >> 2);
+        const uint32_t myset = static_cast<uint32_t>(warp >> 3);
+        const int part = (warp >> 2) & 1;
         const int m = 32 * (warp & 3) + lane;
         const int r = tc_lane_row(m);
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
@@ -867,14 +884,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t lead;
                 const uint32_t rslot =
                     tc_row_slot<FMT, NB, S>(a, sb + slot * L::RAW, it.tile, r, kb0 * F::BB, lead);
-                if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(3, sc);
+                if ((warp & 7) == 0 && lane == 0) TCMV_TRACE(3, sc);
                 // the group scales, for the drainers
                 if (sc >= static_cast<uint32_t>(NSC) &&
                     !tcmv_wait_warp(b_sempty + 8 * sslot, ((sc / NSC) - 1) & 1u, flag, err)) {
                     ok = false;
                     break;
                 }
-                tc_store_scales<FMT>(rslot + lead, nblk, sb + L::SOFF + sslot * L::SCB, m);
+                tc_store_scales<FMT>(rslot + lead, nblk, sb + L::SOFF + sslot * L::SCB, m, part);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_sfull + 8 * sslot);
                 // each half of the set's A stage, once its previous contents
@@ -891,7 +908,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    tc_decode_half<FMT>(rslot, lead, uni, acol, h);
+                    tc_decode_half<FMT>(rslot, lead, uni, acol, h, part);
                     tc::wait_st();
                     tc::fence_before();
                     __syncwarp();
@@ -899,7 +916,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_rempty + 8 * slot);
-                if ((warp & 3) == 0 && lane == 0) TCMV_TRACE(4, sc);
+                if ((warp & 7) == 0 && lane == 0) TCMV_TRACE(4, sc);
             }
         }
     } else {
@@ -932,14 +949,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (warp == 8 && lane == 0) TCMV_TRACE(5, wc);
+                    if (warp == kDrain0 && lane == 0) TCMV_TRACE(5, wc);
                     tc::fence_after();
                     tc_drain_window<FMT, NB, S, Q8>(lane_base + L::DCOL0 + ws * NCOL, scales, m, w,
                                                     s * (kTcStageK / 32), a, acc);
                     tc::fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(b_dempty + 8 * ws);
-                    if (warp == 8 && lane == 0) TCMV_TRACE(6, wc);
+                    if (warp == kDrain0 && lane == 0) TCMV_TRACE(6, wc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_sempty + 8 * sslot);
@@ -959,7 +976,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     tc::fence_before();
     __syncthreads();
-    if (warp == 13) {
+    if (warp == kMma0) {
         tc::fence_after();
         tc::dealloc(tmem, 512);
     }
