@@ -177,8 +177,10 @@ int plan_gemv(int fmt, bool q8, bool bf16, int B, int64_t N, int64_t K, int sms,
     p->items = p->tiles * p->pieces;
     p->grid = static_cast<int>(p->items < slots ? p->items : slots);
     size_t off = 0;
+    // the prepared activation operand (q8 mode and fp32 float mode; bf16
+    // float mode gathers its operand inside the matvec) and the q8 scales
     p->ws_xt = off;
-    off = round_up(off + static_cast<size_t>(p->nst) * p->ncol * 256 * 2, 256);
+    if (q8 || !bf16) off = round_up(off + static_cast<size_t>(p->nst) * p->ncol * 256 * 2, 256);
     p->ws_xs = off;
     if (q8) off = round_up(off + static_cast<size_t>(p->nst) * 8 * p->NB * 4, 256);
     p->ws_part = off;
@@ -199,7 +201,10 @@ int run_gemv(int wf, bool q8, bool bf16, const void* W, const void* x, float* y,
     a.total_bytes = N * a.nb * block_bytes(wf);
     a.rowbytes = a.nb * block_bytes(wf);
     a.n8 = N / 8 * 8;
-    a.xt = reinterpret_cast<const uint16_t*>(ws + p.ws_xt);
+    a.x = x;
+    a.x_bf16 = bf16 ? 1 : 0;
+    const bool tile = q8 || !bf16;
+    a.xt = tile ? reinterpret_cast<const uint16_t*>(ws + p.ws_xt) : nullptr;
     a.xs = q8 ? reinterpret_cast<const float*>(ws + p.ws_xs) : nullptr;
     a.B = B;
     a.y = y;
@@ -212,9 +217,11 @@ int run_gemv(int wf, bool q8, bool bf16, const void* W, const void* x, float* y,
     a.st = d->st;
     a.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
     cudaError_t e;
-    e = act_tile_launch(x, bf16, B, K, wf, p.NB, p.S, p.ncol, p.nst, q8, const_cast<uint16_t*>(a.xt),
-                        const_cast<float*>(a.xs), t_stream, d->st);
-    if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
+    if (tile) {
+        e = act_tile_launch(x, bf16, B, K, wf, p.NB, p.S, p.ncol, p.nst, q8,
+                            const_cast<uint16_t*>(a.xt), const_cast<float*>(a.xs), t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
+    }
     e = tcmv_launch(wf, q8, p.NB, p.S, p.grid, t_stream, a);
     if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
     if (p.pieces > 1) {

@@ -49,7 +49,9 @@ struct TcmvArgs {
     int64_t total_bytes;   // bytes of W
     int64_t rowbytes;      // bytes per row
     int64_t n8;            // rows reached through the tensor map: 8 * floor(N / 8)
-    const uint16_t* xt;    // activation tile [nst][ncol / 8][32][8][8] bf16
+    const void* x;         // the activations [B][K] as given
+    int x_bf16;            //   ... bf16 (else fp32); bf16 float mode gathers them in the matvec
+    const uint16_t* xt;    // q8 and fp32 float mode: the prepared activation operand (tcmv.cu)
     const float* xs;       // q8 mode: activation scales [K / 32 rounded to stages][NB]
     int B;
     float* y;              // [B][N] when pieces == 1

@@ -39,13 +39,16 @@
 //          16-byte multiple, and one copy brings row j of 16 such groups),
 //          1-D bulk copies for the rows past the last whole group of 8
 //   21-22  MMA issue, one thread per decode set; warp 21 owns the tensor memory
-//   23     activation producer: one 1-D bulk copy per stage
+//   23     activation producer: builds each stage's B operand (float mode) or
+//          copies the prepared one (q8 mode)
 // Rings, each slot with a full / empty mbarrier pair, every wait bounded in
 // time: raw weight stages (producer -> decoders), activation stages
 // (producer -> MMA), group scales (decoders -> drainers), A half stages per
 // decode set (decoders -> MMA), D windows (MMA -> drainers). A raw stage is
 // free again as soon as it has been decoded.
 #pragma once
+
+#include <cuda_bf16.h>
 
 #include "kernels.h"
 #include "tc.cuh"
@@ -642,6 +645,43 @@ __device__ __forceinline__ TcItem tc_item(const TcmvArgs& a, int64_t item) {
     return it;
 }
 
+// Gathers stage s of the bf16 activations into its B operand slot with
+// 16-byte asynchronous copies; every lane then arrives on `bar` (without
+// counting itself in) once its copies have landed, so the producer never
+// waits for them. Piece u = lane + 32 j is (column c, k octet o, K16 step t)
+// with c = u % NB, o = (u / NB) % 2, t = u / (2 NB): the 8 activations of
+// batch row c at the stage's position of step t, into row (i % G) * NC + c of
+// the step's operand (i = the step's scale group). Columns at or past B are
+// never written (zeroed once); pieces past K are zero-filled.
+template <int FMT, int NB>
+__device__ __forceinline__ void tc_gather_x_stage(const TcmvArgs& a, int64_t s, uint32_t xslot, int lane,
+                                                  uint32_t bar) {
+    using L = TcLayout<FMT, NB, 1>;
+    using F = TcF<FMT>;
+    constexpr int NC = L::NC, G = L::G, NCOL = L::NCOL, SPG = F::GK / 16;
+    static_assert(32 % NB == 0, "batch bucket");
+    const int c = lane % NB;
+    if (c < a.B) {
+        const uint16_t* xrow = static_cast<const uint16_t*>(a.x) + c * a.K + s * kTcStageK;
+        const int64_t krem = a.K - s * kTcStageK;  // K left from the stage start
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int q = lane / NB + j * (32 / NB);
+            const int o = q & 1, t = q >> 1;
+            const int i = t / SPG, kk = t % SPG;
+            const int k = tc_group_k<FMT>(i >> 2, i & 3) + 16 * kk + 8 * o;
+            const bool in = k < krem;
+            const int row = (i % G) * NC + c;
+            const uint32_t dst = xslot + static_cast<uint32_t>(t * NCOL * 32) +
+                                 static_cast<uint32_t>(((row >> 3) * 2 + o) * 128 + (row & 7) * 16);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst),
+                         "l"(in ? xrow + k : xrow), "r"(in ? 16 : 0)
+                         : "memory");
+        }
+    }
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ------------------------------------------------------------ the kernel
 
 template <int FMT, bool Q8, int NB, int S>
@@ -677,7 +717,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(b_rempty + 8 * r, 8);  // the 8 warps of the decode set
         }
         for (int r = 0; r < NX; ++r) {
-            mbar_init(b_xfull + 8 * r, 1);
+            // bf16 float mode: one arrival per producer lane, when its copies land
+            mbar_init(b_xfull + 8 * r, !Q8 && S == 1 ? 32 : 1);
             mbar_init(b_xempty + 8 * r, 1);  // the MMA commit
         }
         for (int r = 0; r < NSC; ++r) {
@@ -700,6 +741,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // 20 weight producer, 21-22 MMA issue, 23 activation producer
     constexpr int kDrain0 = 16, kProdW = 20, kMma0 = 21, kProdX = 23;
     if (warp == kMma0) tc::alloc(sb + L::TSLOT, 512);
+    if constexpr (!Q8 && S == 1) {
+        // bf16 float mode: the rows of the activation slots that no stage
+        // writes stay zero
+        for (uint32_t u = threadIdx.x; u < NX * L::XT / 16; u += blockDim.x)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sb + L::XOFF + 16 * u), "r"(0u)
+                         : "memory");
+    }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
@@ -771,7 +819,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             (void)tcmv_wait_warp(b_rfull + 8 * (u % NR), (u / NR) & 1u, flag, err);
     } else if (warp == kProdX) {
         // ---------------------------------------------------- activation producer
-        grid_dependency_wait();  // the activation tile is written by the previous kernel
+        // bf16 float mode gathers each stage's B operand from the activations
+        // (the rows that hold activations are rewritten per stage, all other
+        // rows were zeroed at the start); fp32 float mode and q8 mode copy the operand
+        // that the preceding kernel prepared (with the exact three-way split
+        // or the quantization).
+        constexpr bool GATHER = !Q8 && S == 1;
+        grid_dependency_wait();  // the activations come from the previous kernel
         uint32_t sc = 0;
         bool ok = true;
         for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
@@ -783,10 +837,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(b_xfull + 8 * slot, L::XT);
-                    bulk_g2s(sb + L::XOFF + slot * L::XT, a.xt + s * (NCOL * kTcStageK), L::XT,
-                             b_xfull + 8 * slot);
+                const uint32_t bar = b_xfull + 8 * slot, dst = sb + L::XOFF + slot * L::XT;
+                if constexpr (GATHER) {
+                    tc_gather_x_stage<FMT, NB>(a, s, dst, lane, bar);
+                } else if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, L::XT);
+                    bulk_g2s(dst, a.xt + s * (NCOL * kTcStageK), L::XT, bar);
                 }
                 __syncwarp();
             }
@@ -810,6 +866,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
+                    // bf16 float mode wrote the operand with generic-proxy copies
+                    // (and the zero rows with plain stores): order them before the
+                    // tensor core's async-proxy reads
+                    if constexpr (!Q8 && S == 1) fence_proxy_async_smem();
                     TCMV_TRACE(1, sc);
                     // descriptors and addresses: per-stage bases plus compile-time
                     // offsets, so the issue loop is a run of MMAs. B operand of

@@ -208,7 +208,10 @@ def test_liveness_counts_each_launch():
     live = qmm.liveness()
     assert live["gemv_float"] == 1 and live["gemv_q8"] == 1 and live["quantize"] == 1
     assert live["gemv_splitk_reduce"] == 2  # short N is split along K
-    assert live["x_tile"] == 1              # float mode lays the activations out once
+    assert live["x_tile"] == 1              # fp32 float mode lays the activations out once
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)
+    live = qmm.liveness()
+    assert live["gemv_float"] == 2 and live["x_tile"] == 1  # bf16: gathered inside the matvec
 
 
 def test_missing_workspace_is_an_error():
