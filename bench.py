@@ -17,6 +17,11 @@ time (weight GB/s); the GEMM's TOPS and the MoE's GB/s are reported beside it.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Prints one JSON line (rank 0).
+
+python bench.py --profile PART runs one part W + K times without timing it,
+for profilers: PART is decode, decode:NAME:B (one matvec of the decode set,
+e.g. decode:output:1), gemm_exp_plane, gemm_in_kernel, moe_t1 or moe_t16.
+Only that part's inputs are made.
 """
 from __future__ import annotations
 
@@ -338,6 +343,36 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ main
 
+def run_profile(args):
+    """One part of the step (or one matvec of the decode set), W + K times."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    part = args.profile.split(":")
+    if part[0] == "decode":
+        dec = DecodeSet(torch, device)
+        if len(part) == 3:
+            name, B = part[1], int(part[2])
+            items = [it for it in dec.items if it[0] == name and it[4] == B]
+            if not items:
+                raise SystemExit(f"no decode matvec {name} at batch {B}")
+            dec.items = items
+        fn = dec.run
+    elif part[0] in ("gemm_exp_plane", "gemm_in_kernel"):
+        gem = GemmCase(torch, device)
+        fn = gem.run_exp if part[0] == "gemm_exp_plane" else gem.run_in_kernel
+    elif part[0] in ("moe_t1", "moe_t16"):
+        fn = MoeCase(torch, device, MoeWeights(torch, device), 1 if part[0] == "moe_t1" else 16).run
+    else:
+        raise SystemExit(f"unknown part {args.profile}")
+    for _ in range(args.warmup + args.steps):
+        fn()
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile": args.profile, "calls": args.warmup + args.steps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -346,7 +381,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of CPU work for the oracle baseline")
+    ap.add_argument("--profile", default=None,
+                    help="run one part untimed (for profilers) and exit")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

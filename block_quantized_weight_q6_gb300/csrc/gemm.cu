@@ -18,15 +18,21 @@
 // after that is shared code, so their outputs are bitwise identical (section
 // 2.3: identity by construction).
 //
-// CTA roles (448 threads):
-//   warp 0      producer: 1-D bulk TMA copies of the A tiles (quantized
-//               activations, pre-tiled by the quantizer) and of the raw
-//               weight rows (or plane rows and scales)
+// CTA roles (480 threads):
+//   warp 0      A producer: 1-D bulk TMA copies of the A tiles (quantized
+//               activations, pre-tiled by the quantizer), up to NA blocks
+//               ahead of the MMAs
+//   warp 14     raw producer: the weight stages, up to NR 256-column chunks
+//               ahead of the converters: q6_K / Q4_0 rows through a tensor
+//               map (W as groups of 8 rows), plane rows and scales as 1-D
+//               copies
 //   warp 1      owns the tensor memory; one lane issues tcgen05.mma
-//   warps 2-5   converters: weights -> fp16 B tile (core-matrix layout)
+//   warps 2-5   converters: weights -> fp16 B tile (core-matrix layout);
+//               warp cw converts the rows 8 g + j, j = 2 cw, 2 cw + 1
 //   warps 6-13  epilogue: tcgen05.ld of the accumulator, scaling, output
 #include <cuda_fp16.h>
 
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -39,15 +45,23 @@ namespace {
 
 constexpr int BM = 128;           // tokens per tile (tensor-memory lanes)
 constexpr int BN = 128;           // weight rows per tile (accumulator columns)
-constexpr int NS = 4;             // A / B stages (one 32-wide K block each)
-constexpr int NR = 2;             // raw weight stages (256 columns each)
+constexpr int NS = 4;             // B stages (one 32-wide K block each)
+constexpr int NA = 8;             // A stages: the activation copies run up to NA blocks ahead
+constexpr int NR = 3;             // raw weight stages (256 columns each)
 constexpr int NBUF = 3;           // accumulator buffers in tensor memory
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
 constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
-constexpr int kThreads = 448;
+constexpr int kThreads = 480;                // 15 warps: 128 registers a thread
+constexpr int kRawWarp = 14;                // raw weight producer
+constexpr int kConv0 = 2, kConvWarps = 4;   // converter warps
+constexpr int kEpi0 = 6;                    // epilogue warps kEpi0 .. kEpi0 + 7
 constexpr int kTmemCols = 512;    // NBUF * BN accumulators + BN for y
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
-constexpr int kBTile = BN * 32 * 2;   // bytes of one B stage
+// B stage: 16 groups of 8 weight rows, kBSbo bytes apart (a 16-byte odd
+// multiple past 512, so that 8 lanes storing one row each of 8 different
+// groups hit 8 different bank groups); core matrices 128 bytes apart along K
+constexpr int kBSbo = 528;
+constexpr int kBTile = 16 * kBSbo;    // bytes of one B stage
 
 // raw stage row strides (16-byte multiples with room for the lead-in)
 constexpr int kRawQ6K = 240;      // one 210-byte super-block
@@ -55,9 +69,17 @@ constexpr int kRawQ40 = 176;      // up to 8 18-byte blocks
 constexpr int kRawPlane = 304;    // 256 plane bytes + 48 for scales and d
 
 struct SmemLayout {
-    uint32_t a, b, raw, dv, bars, tslot, abort_flag;
+    uint32_t a, b, raw, rawslot, dv, bars, tslot, abort_flag;
     uint32_t total;
 };
+
+// Raw stage of q6_K / Q4_0 rows (tensor-map layout): 8 boxes, box j holding
+// row j of each of the tile's 16 groups of 8 rows at RS-byte slots, then a
+// tail area for the up to 7 rows past the last whole group of 8 rows of W.
+// A plane stage holds row n = 8 g + j at (16 j + g) * kRawPlane.
+__host__ __device__ constexpr uint32_t raw_slot_bytes(int rs, bool exp) {
+    return exp ? static_cast<uint32_t>(BN) * rs : 8u * 16u * rs + 8u * rs;
+}
 
 __host__ __device__ constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
@@ -67,16 +89,17 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     const uint32_t dr = fmt == FMT_Q6_K ? DR_Q6K : DR_Q40;
     uint32_t o = 0;
     L.a = o;
-    o += NS * kATile;
+    o += NA * kATile;
     L.b = o;
     o += NS * kBTile;
     L.raw = o;
-    o += NR * BN * rs;
+    L.rawslot = raw_slot_bytes(static_cast<int>(rs), exp);
+    o += NR * L.rawslot;
     L.dv = o;
     o += dr * BN * 4;
     o = align_up(o, 8);
     L.bars = o;
-    o += 8 * (4 * NS + 2 * NR + 2 * NBUF + dr);
+    o += 8 * (2 * NA + 2 * NS + 2 * NR + 2 * NBUF + dr);
     L.tslot = o;
     o += 4;
     L.abort_flag = o;
@@ -85,18 +108,24 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     return L;
 }
 
-// barrier indices
+// barrier indices: a_full[NA], a_empty[NA], b_full[NS], b_empty[NS],
+// raw_full[NR], raw_empty[NR], acc_full[NBUF], acc_empty[NBUF], dv_full[DR]
 __device__ __forceinline__ uint32_t bar_a_full(uint32_t B, int s) { return B + 8 * s; }
-__device__ __forceinline__ uint32_t bar_b_full(uint32_t B, int s) { return B + 8 * (NS + s); }
-__device__ __forceinline__ uint32_t bar_stage_empty(uint32_t B, int s) { return B + 8 * (2 * NS + s); }
-__device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (3 * NS + r); }
-__device__ __forceinline__ uint32_t bar_raw_empty(uint32_t B, int r) { return B + 8 * (3 * NS + NR + r); }
-__device__ __forceinline__ uint32_t bar_acc_full(uint32_t B, int i) { return B + 8 * (3 * NS + 2 * NR + i); }
+__device__ __forceinline__ uint32_t bar_a_empty(uint32_t B, int s) { return B + 8 * (NA + s); }
+__device__ __forceinline__ uint32_t bar_b_full(uint32_t B, int s) { return B + 8 * (2 * NA + s); }
+__device__ __forceinline__ uint32_t bar_stage_empty(uint32_t B, int s) { return B + 8 * (2 * NA + NS + s); }
+__device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (2 * NA + 2 * NS + r); }
+__device__ __forceinline__ uint32_t bar_raw_empty(uint32_t B, int r) {
+    return B + 8 * (2 * NA + 2 * NS + NR + r);
+}
+__device__ __forceinline__ uint32_t bar_acc_full(uint32_t B, int i) {
+    return B + 8 * (2 * NA + 2 * NS + 2 * NR + i);
+}
 __device__ __forceinline__ uint32_t bar_acc_empty(uint32_t B, int i) {
-    return B + 8 * (3 * NS + 2 * NR + NBUF + i);
+    return B + 8 * (2 * NA + 2 * NS + 2 * NR + NBUF + i);
 }
 __device__ __forceinline__ uint32_t bar_dv_full(uint32_t B, int i) {
-    return B + 8 * (3 * NS + 2 * NR + 2 * NBUF + i);
+    return B + 8 * (2 * NA + 2 * NS + 2 * NR + 2 * NBUF + i);
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -104,11 +133,11 @@ __device__ __forceinline__ uint32_t bar_dv_full(uint32_t B, int i) {
 // Shared-memory matrix descriptor, K-major operand without swizzle: core
 // matrices of 8 rows x 16 bytes, adjacent along K 128 bytes apart (leading
 // byte offset), adjacent 8-row groups 512 bytes apart (stride byte offset).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t sbo = 512) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
     d |= static_cast<uint64_t>((128u >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((512u >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;  // descriptor version of the sm_100 family
     return d;
 }
@@ -157,21 +186,29 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16};" ::"r"(taddr),
         "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
         "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
         "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
         "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "r"(__float_as_uint(v[15]))
         : "memory");
 }
 
@@ -202,17 +239,33 @@ __device__ unsigned* qmm_gemm_trace;
 
 __device__ __forceinline__ bool aborted(uint32_t flag) { return lds_u32(flag) != 0; }
 
+// try_wait that may suspend the thread (up to a 20 us hint, resuming when
+// the phase completes) instead of spinning: the converter warps share the
+// issue slots with every waiting role.
+__device__ __forceinline__ bool mbar_wait_hint(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait that also gives up once another role of the CTA has given up.
-// Warp-collective: every lane of the calling warp polls, and all lanes leave
+// Warp-collective: every lane of the calling warp polls (a converged warp
+// resumes promptly from the suspending try_wait), and all lanes leave
 // together with the same result, so the warp is converged afterwards (the
 // tensor-memory loads and stores that follow are .sync.aligned).
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t flag,
                                               unsigned int* err) {
-    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    if (__all_sync(0xffffffffu, mbar_wait_hint(bar, parity))) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-        if ((it & 63u) == 0) {
+        if (__all_sync(0xffffffffu, mbar_wait_hint(bar, parity))) return true;
+        if ((it & 3u) == 0) {
             int give_up = aborted(flag) ? 1 : 0;
             if (!give_up && globaltimer_ns() - t0 > kWaitLimitNs) give_up = 2;
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
@@ -250,6 +303,33 @@ __device__ __forceinline__ uint32_t half2_bits(float x) {
     return h | (h << 16);
 }
 
+// The 16 bytes at base + 4 * QW + sh / 8 (base 16-byte aligned, sh 0, 8, 16
+// or 24) as 4 words: two 16-byte loads and a funnel shift per word.
+template <int QW>
+__device__ __forceinline__ void run16(uint32_t base, uint32_t sh, uint32_t (&o)[4]) {
+    uint32_t w[8];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(base));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "r"(base + 16));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(w[QW + k], w[QW + k + 1], sh);
+}
+
+// The same with the word offset QW a runtime value that is uniform across
+// the warp (a branch, not a per-lane selection).
+__device__ __forceinline__ void run16_u(uint32_t addr, uint32_t (&o)[4]) {
+    const uint32_t base = addr & ~15u, sh = (addr & 3u) * 8u;
+    switch ((addr >> 2) & 3u) {
+        case 0: run16<0>(base, sh, o); break;
+        case 1: run16<1>(base, sh, o); break;
+        case 2: run16<2>(base, sh, o); break;
+        default: run16<3>(base, sh, o); break;
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- kernel
@@ -262,13 +342,16 @@ struct GemmArgs {
     float* Y;              // [M][N]
     int64_t M, N, K, nb;   // nb: blocks per row
     int64_t total_bytes;   // bytes of W
+    int64_t rowbytes;      // bytes per row of W
+    int64_t n8;            // rows of W reached through the tensor map: 8 * floor(N / 8)
     DevState st;
     int live_slot;
     float* dbg;            // optional [M][N]: the raw accumulator of the first K block
 };
 
 template <int FMT, bool EXP>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap wmap) {
     constexpr bool Q6 = (FMT == FMT_Q6_K);
     constexpr int DR = Q6 ? DR_Q6K : DR_Q40;
     constexpr int RS = EXP ? kRawPlane : (Q6 ? kRawQ6K : kRawQ40);
@@ -286,20 +369,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     grid_launch_dependents();
     live_bump(a.st, a.live_slot);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NA; ++s) {
             mbar_init(bar_a_full(BARS, s), 1);
-            mbar_init(bar_b_full(BARS, s), 4);
-            mbar_init(bar_stage_empty(BARS, s), 1);
+            mbar_init(bar_a_empty(BARS, s), 1);  // the MMA commit
+        }
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(bar_b_full(BARS, s), kConvWarps);
+            mbar_init(bar_stage_empty(BARS, s), 1);  // the MMA commit
         }
         for (int r = 0; r < NR; ++r) {
             mbar_init(bar_raw_full(BARS, r), 1);
-            mbar_init(bar_raw_empty(BARS, r), 4);
+            mbar_init(bar_raw_empty(BARS, r), kConvWarps);
         }
         for (int i = 0; i < NBUF; ++i) {
             mbar_init(bar_acc_full(BARS, i), 1);
-            mbar_init(bar_acc_empty(BARS, i), 8);
+            mbar_init(bar_acc_empty(BARS, i), 8);  // the epilogue warps
         }
-        for (int i = 0; i < DR; ++i) mbar_init(bar_dv_full(BARS, i), 4);
+        for (int i = 0; i < DR; ++i) mbar_init(bar_dv_full(BARS, i), 4);  // converters of rows 0..127
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(FLAG), "r"(0u) : "memory");
         fence_mbar_init();
     }
@@ -316,95 +402,122 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
     // the quantized activations come from the previous kernel on the stream
     grid_dependency_wait();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == kRawWarp) {
+        // ------------------------------------------------------------ producers
         const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
-        for (int64_t kb = 0; kb < nkb; ++kb) {
-            const int s = static_cast<int>(kb % NS);
-            if ((kb & 7) == 0) {
-                const int64_t sc = kb >> 3;
-                const int r = static_cast<int>(sc % NR);
-                QMM_TRACE(1, kb);
-                if (sc >= NR &&
-                    !wait_or_abort(bar_raw_empty(BARS, r), ((sc / NR) - 1) & 1, FLAG, a.st.err))
-                    break;
-                const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * BN * RS;
-                // this lane's rows: byte ranges and manual tails
-                uint32_t bytes = 0;
+        // raw stage of 256-column chunk sc into slot sc % NR
+        auto issue_raw = [&](int64_t sc) {
+            const int r = static_cast<int>(sc % NR);
+            const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
+            const uint32_t bar = bar_raw_full(BARS, r);
+            uint32_t bytes = 0;
+            if (EXP) {
+                // plane rows (256 bytes) and the block's scales and d, per row
                 for (int n = lane; n < BN; n += 32) {
                     const int64_t ng = n0 + n;
                     if (ng >= a.N) break;
-                    int64_t st, len;
-                    if (EXP) {
-                        st = (ng * a.nb + sc) * 210 + 192;  // the scales and d of the block
-                        len = 18;
-                        bytes += 256;                       // plane row chunk
-                    } else if (Q6) {
-                        st = (ng * a.nb + sc) * 210;
-                        len = 210;
-                    } else {
-                        const int64_t b0 = sc * 8;
-                        st = (ng * a.nb + b0) * 18;
-                        len = min(static_cast<int64_t>(8), a.nb - b0) * 18;
-                    }
+                    const int64_t st = (ng * a.nb + sc) * 210 + 192;
                     const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                    const int64_t e16 = min((st + 18 + 15) & ~static_cast<int64_t>(15), tb16);
+                    bytes += 256;
                     if (e16 > s16) bytes += static_cast<uint32_t>(e16 - s16);
-                    const uint32_t rdst = dst0 + n * RS + (EXP ? 256 : 0);
-                    for (int64_t q = max(e16, s16); q < st + len; ++q)
+                    const uint32_t rdst = dst0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS + 256;
+                    for (int64_t q = max(e16, s16); q < st + 18; ++q)
                         sts_u8(rdst + static_cast<uint32_t>(q - s16), a.W[q]);
                 }
                 fence_proxy_async_smem();
                 bytes = __reduce_add_sync(0xffffffffu, bytes);
-                if (lane == 0) mbar_arrive_expect_tx(bar_raw_full(BARS, r), bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
                 __syncwarp();
                 for (int n = lane; n < BN; n += 32) {
                     const int64_t ng = n0 + n;
                     if (ng >= a.N) break;
-                    int64_t st, len;
-                    if (EXP) {
-                        bulk_g2s(dst0 + n * RS, a.plane + ng * a.K + sc * 256, 256,
-                                 bar_raw_full(BARS, r));
-                        st = (ng * a.nb + sc) * 210 + 192;
-                        len = 18;
-                    } else if (Q6) {
-                        st = (ng * a.nb + sc) * 210;
-                        len = 210;
-                    } else {
-                        const int64_t b0 = sc * 8;
-                        st = (ng * a.nb + b0) * 18;
-                        len = min(static_cast<int64_t>(8), a.nb - b0) * 18;
-                    }
+                    const uint32_t rdst = dst0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS;
+                    bulk_g2s(rdst, a.plane + ng * a.K + sc * 256, 256, bar);
+                    const int64_t st = (ng * a.nb + sc) * 210 + 192;
                     const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                    const int64_t e16 = min((st + 18 + 15) & ~static_cast<int64_t>(15), tb16);
                     if (e16 > s16)
-                        bulk_g2s(dst0 + n * RS + (EXP ? 256 : 0), a.W + s16,
-                                 static_cast<uint32_t>(e16 - s16), bar_raw_full(BARS, r));
+                        bulk_g2s(rdst + 256, a.W + s16, static_cast<uint32_t>(e16 - s16), bar);
                 }
+            } else {
+                // rows of whole groups of 8 through the tensor map (8 boxes),
+                // the up to 7 rows past them as 1-D copies from the 16-byte
+                // boundary at or below each row segment (plain loads for bytes
+                // past the last 16-byte boundary of W)
+                const int64_t koff = Q6 ? sc * 210 : sc * 8 * 18;
+                const int64_t len = Q6 ? 210 : min(static_cast<int64_t>(8), a.nb - sc * 8) * 18;
+                const bool boxes = n0 < a.n8;
+                int64_t cs = 0, ce = 0;
+                int tr = -1;
+                {
+                    const int64_t ng = a.n8 + lane;
+                    if (lane < 8 && ng < a.N && ng >= n0 && ng < n0 + BN) {
+                        tr = lane;
+                        const int64_t st = ng * a.rowbytes + koff;
+                        const int64_t s16 = st & ~static_cast<int64_t>(15);
+                        const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                        if (e16 > s16) {
+                            cs = s16;
+                            ce = e16;
+                            bytes = static_cast<uint32_t>(e16 - s16);
+                        }
+                        for (int64_t q = max(e16, s16); q < st + len; ++q)
+                            sts_u8(dst0 + 8u * 16u * RS + tr * RS + static_cast<uint32_t>(q - s16), a.W[q]);
+                    }
+                }
+                fence_proxy_async_smem();
+                bytes = __reduce_add_sync(0xffffffffu, bytes);
+                if (lane == 0) mbar_arrive_expect_tx(bar, bytes + (boxes ? 8u * 16u * RS : 0u));
+                __syncwarp();
+                if (boxes && lane < 8) {
+                    const int64_t xb = (lane * a.rowbytes + koff) & ~static_cast<int64_t>(15);
+                    tma_load_2d(dst0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2),
+                                static_cast<int>(n0 / 8), bar);
+                }
+                if (ce > cs)
+                    bulk_g2s(dst0 + 8u * 16u * RS + tr * RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
             }
-            QMM_TRACE(2, kb);
-            if (kb >= NS &&
-                !wait_or_abort(bar_stage_empty(BARS, s), ((kb / NS) - 1) & 1, FLAG, a.st.err))
-                break;
-            QMM_TRACE(3, kb);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bar_a_full(BARS, s), kATile);
-                bulk_g2s(S + L.a + s * kATile, a.a16 + (mt * nkb + kb) * (BM * 32), kATile,
-                         bar_a_full(BARS, s));
+        };
+        if (warp == kRawWarp) {
+            for (int64_t sc = 0; sc < nsc; ++sc) {
+                QMM_TRACE(1, sc);
+                if (sc >= NR &&
+                    !wait_or_abort(bar_raw_empty(BARS, static_cast<int>(sc % NR)), ((sc / NR) - 1) & 1, FLAG,
+                                   a.st.err))
+                    break;
+                issue_raw(sc);
             }
-            __syncwarp();
+            // the copies still in flight land before the CTA ends
+            for (int64_t sc = nsc > NR ? nsc - NR : 0; sc < nsc; ++sc)
+                (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(sc % NR)), (sc / NR) & 1, FLAG, a.st.err);
+        } else {
+            for (int64_t kb = 0; kb < nkb; ++kb) {
+                QMM_TRACE(2, kb);
+                const int sa = static_cast<int>(kb % NA);
+                if (kb >= NA &&
+                    !wait_or_abort(bar_a_empty(BARS, sa), ((kb / NA) - 1) & 1, FLAG, a.st.err))
+                    break;
+                QMM_TRACE(3, kb);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar_a_full(BARS, sa), kATile);
+                    bulk_g2s(S + L.a + sa * kATile, a.a16 + (mt * nkb + kb) * (BM * 32), kATile,
+                             bar_a_full(BARS, sa));
+                }
+                __syncwarp();
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc = idesc_f16(BM, BN);
         for (int64_t kb = 0; kb < nkb; ++kb) {
             const int s = static_cast<int>(kb % NS);
+            const int sa = static_cast<int>(kb % NA);
             const int ab = static_cast<int>(kb % NBUF);
-            const uint32_t ph = (kb / NS) & 1;
             QMM_TRACE(10, kb);
-            if (!wait_or_abort(bar_a_full(BARS, s), ph, FLAG, a.st.err)) break;
+            if (!wait_or_abort(bar_a_full(BARS, sa), (kb / NA) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(11, kb);
-            if (!wait_or_abort(bar_b_full(BARS, s), ph, FLAG, a.st.err)) break;
+            if (!wait_or_abort(bar_b_full(BARS, s), (kb / NS) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(12, kb);
             if (kb >= NBUF &&
                 !wait_or_abort(bar_acc_empty(BARS, ab), ((kb / NBUF) - 1) & 1, FLAG, a.st.err))
@@ -412,126 +525,161 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             QMM_TRACE(13, kb);
             tc_fence_after();
             if (lane == 0) {
-                const uint64_t ad = smem_desc(S + L.a + s * kATile);
-                const uint64_t bd = smem_desc(S + L.b + s * kBTile);
+                const uint64_t ad = smem_desc(S + L.a + sa * kATile);
+                const uint64_t bd = smem_desc(S + L.b + s * kBTile, kBSbo);
                 const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
                 tc_mma(d, ad, bd, idesc, 0u);
                 tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
                 tc_commit(bar_stage_empty(BARS, s));
+                tc_commit(bar_a_empty(BARS, sa));
                 tc_commit(bar_acc_full(BARS, ab));
             }
             __syncwarp();
         }
-    } else if (warp < 6) {
+    } else if (warp < kEpi0) {
         // ------------------------------------------------------------ converters
-        const int cw = warp - 2;              // 0..3
-        const int tid = threadIdx.x - 64;     // 0..127: this thread's row for d
-        const int kc = lane >> 3, rw = lane & 7;
-        for (int64_t kb = 0; kb < nkb; ++kb) {
-            const int s = static_cast<int>(kb % NS);
-            const int64_t sc = kb >> 3;
-            const int j = static_cast<int>(kb & 7);
+        // Two K blocks (one B stage each) per pass: one wait for both stages,
+        // one proxy fence and one arrival per stage. Warp cw converts the rows
+        // 8 g + j of the tile for j = 2 cw, 2 cw + 1: lane (g = lane % 16,
+        // h = lane / 16) the 16 columns 16 h .. 16 h + 15 of each block. A
+        // row's offset inside its raw slot depends only on j, so the
+        // realignment of its bytes is the same for the whole warp.
+        const int cw = warp - kConv0;
+        const int tid = threadIdx.x - 32 * kConv0;  // rows 0..127 store d
+        const int g = lane & 15, hh = lane >> 4;
+        for (int64_t kb0 = 0; kb0 < nkb; kb0 += 2) {
+            const int nbk = nkb - kb0 < 2 ? 1 : 2;
+            const int64_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
+            const int j0 = static_cast<int>(kb0 & 7);
             const int r = static_cast<int>(sc % NR);
-            const uint32_t raw0 = S + L.raw + static_cast<uint32_t>(r) * BN * RS;
-            QMM_TRACE(20, kb);
-            if (j == 0 && !wait_or_abort(bar_raw_full(BARS, r), (sc / NR) & 1, FLAG, a.st.err)) break;
-            QMM_TRACE(21, kb);
+            const uint32_t raw0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
+            // row n of the tile within the raw stage
+            auto rowaddr = [&](int n) -> uint32_t {
+                if (EXP) return raw0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS;
+                const int64_t ng = n0 + n;
+                if (ng < a.n8) return raw0 + static_cast<uint32_t>(n & 7) * 16u * RS + static_cast<uint32_t>(n >> 3) * RS;
+                return raw0 + 8u * 16u * RS + static_cast<uint32_t>(ng - a.n8) * RS;
+            };
             // lead-in of row n's data inside its raw stage row
             auto lead = [&](int64_t ng) -> uint32_t {
                 if (EXP) return static_cast<uint32_t>(((ng * a.nb + sc) * 210 + 192) & 15);
                 if (Q6) return static_cast<uint32_t>(((ng * a.nb + sc) * 210) & 15);
                 return static_cast<uint32_t>(((ng * a.nb + sc * 8) * 18) & 15);
             };
-            // d of this thread's row (q6_K: once per super-block, Q4_0: per block)
-            if (Q6 ? (j == 0) : true) {
-                const int di = static_cast<int>(Q6 ? (sc % DR) : (kb % DR));
-                float dval = 0.0f;
+            QMM_TRACE(20, kb0);
+            if (j0 == 0 && !wait_or_abort(bar_raw_full(BARS, r), (sc / NR) & 1, FLAG, a.st.err)) break;
+            QMM_TRACE(21, kb0);
+            // d of row tid (q6_K: once per super-block, Q4_0: per block)
+            {
                 const int64_t ng = n0 + tid;
-                if (ng < a.N) {
-                    const uint32_t rowb = raw0 + tid * RS + (EXP ? 256 : 0) + lead(ng);
-                    const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * j);
-                    dval = half_bits_to_float(lds_u16(rowb + doff));
+                for (int bi = 0; bi < (Q6 ? (j0 == 0 ? 1 : 0) : nbk); ++bi) {
+                    const int64_t kb = kb0 + bi;
+                    const int di = static_cast<int>(Q6 ? (sc % DR) : (kb % DR));
+                    float dval = 0.0f;
+                    if (ng < a.N) {
+                        const uint32_t rowb = rowaddr(tid) + (EXP ? 256 : 0) + lead(ng);
+                        const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * (j0 + bi));
+                        dval = half_bits_to_float(lds_u16(rowb + doff));
+                    }
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(S + L.dv + (di * BN + tid) * 4), "f"(dval)
+                                 : "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_dv_full(BARS, di));
                 }
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(S + L.dv + (di * BN + tid) * 4), "f"(dval)
-                             : "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_dv_full(BARS, di));
             }
-            if (kb >= NS &&
-                !wait_or_abort(bar_stage_empty(BARS, s), ((kb / NS) - 1) & 1, FLAG, a.st.err))
-                break;
-            QMM_TRACE(22, kb);
-            const uint32_t bt = S + L.b + s * kBTile;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int rg = cw + 4 * t;
-                const int n = rg * 8 + rw;
+            bool ok = true;
+            for (int bi = 0; bi < nbk; ++bi) {
+                const int64_t kb = kb0 + bi;
+                if (kb >= NS &&
+                    !wait_or_abort(bar_stage_empty(BARS, static_cast<int>(kb % NS)), ((kb / NS) - 1) & 1, FLAG,
+                                   a.st.err))
+                    ok = false;
+            }
+            if (!ok) break;
+            QMM_TRACE(22, kb0);
+#pragma unroll 1
+            for (int u = 0; u < 2 * nbk; ++u) {
+                const int bi = u >> 1, j = 2 * cw + (u & 1);
+                const int64_t kb = kb0 + bi;
+                const int n = 8 * g + j;
                 const int64_t ng = n0 + n;
-                uint32_t h[4] = {0u, 0u, 0u, 0u};
+                const int e = 32 * (j0 + bi) + 16 * hh;  // this lane's first column within the chunk
+                uint32_t hv[8];
                 if (ng < a.N) {
-                    const uint32_t rowb = raw0 + n * RS;
-                    const int e = 32 * j + 8 * kc;  // first column of the 8 within the chunk
+                    // warp-uniform: the lead of rows 8 g + j (whole groups, or the tail rows)
+                    const uint32_t rb = rowaddr(n) + lead(ng);
                     if (Q6) {
-                        uint32_t c[2];
-                        float scf;
+                        uint32_t c[4];
+                        int scv;
                         if (EXP) {
-                            // centered int8 plane bytes -> 1152 + v as fp16 pairs
-                            const uint32_t p0 = lds_u32(rowb + e) ^ 0x80808080u;
-                            const uint32_t p1 = lds_u32(rowb + e + 4) ^ 0x80808080u;
-                            c[0] = p0;
-                            c[1] = p1;
-                            scf = static_cast<float>(lds_s8(rowb + 256 + lead(ng) + (e >> 4)));
+                            const uint32_t pb = rowaddr(n) + e;  // 16-byte aligned plane bytes
+                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                                         : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
+                                         : "r"(pb));
+                            scv = lds_s8(rowaddr(n) + 256 + lead(ng) + (e >> 4));
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) c[w] ^= 0x80808080u;
                         } else {
-                            const uint32_t rb = rowb + lead(ng);
-                            uint32_t lw[2], hw[2];
-                            lds_words_unaligned<2>(rb + (e & 127), lw);
-                            lds_words_unaligned<2>(rb + 128 + (e & 63), hw);
+                            uint32_t ql[4], qh[4];
+                            run16_u(rb + (e & 127), ql);
+                            run16_u(rb + 128 + (e & 63), qh);
+                            scv = lds_s8(rb + 192 + (e >> 4));
                             const uint32_t ns = 4u * static_cast<uint32_t>(e >> 7);
                             const uint32_t hs = 2u * static_cast<uint32_t>(e >> 6);
-                            c[0] = ((lw[0] >> ns) & 0x0F0F0F0Fu) | (((hw[0] >> hs) & 0x03030303u) << 4);
-                            c[1] = ((lw[1] >> ns) & 0x0F0F0F0Fu) | (((hw[1] >> hs) & 0x03030303u) << 4);
-                            scf = static_cast<float>(lds_s8(rb + 192 + (e >> 4)));
+#pragma unroll
+                            for (int w = 0; w < 4; ++w)
+                                c[w] = ((ql[w] >> ns) & 0x0F0F0F0Fu) | (((qh[w] >> hs) & 0x03030303u) << 4);
                         }
                         // sc * (v - off) exactly: (off + v) * sc - off * sc, one rounding
+                        const float scf = static_cast<float>(scv);
                         const float off = EXP ? 1152.0f : 1056.0f;
                         const uint32_t sc2 = half2_bits(scf);
                         const uint32_t bias = half2_bits(-off * scf);
-                        h[0] = hfma2_u(half_pair_lo(c[0]), sc2, bias);
-                        h[1] = hfma2_u(half_pair_hi(c[0]), sc2, bias);
-                        h[2] = hfma2_u(half_pair_lo(c[1]), sc2, bias);
-                        h[3] = hfma2_u(half_pair_hi(c[1]), sc2, bias);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            hv[2 * w] = hfma2_u(half_pair_lo(c[w]), sc2, bias);
+                            hv[2 * w + 1] = hfma2_u(half_pair_hi(c[w]), sc2, bias);
+                        }
                     } else {
-                        // Q4_0 block j of the chunk: nibbles of qs bytes 8*(kc%2).., nibble kc/2
-                        const uint32_t rb = rowb + lead(ng) + 18 * j;
-                        uint32_t qw[2];
-                        lds_words_unaligned<2>(rb + 2 + 8 * (kc & 1), qw);
-                        const uint32_t ns = 4u * static_cast<uint32_t>(kc >> 1);
-                        const uint32_t c0 = (qw[0] >> ns) & 0x0F0F0F0Fu;
-                        const uint32_t c1 = (qw[1] >> ns) & 0x0F0F0F0Fu;
+                        // Q4_0 block: nibble hh of the 16 qs bytes
+                        uint32_t q[4];
+                        run16_u(rb + 18 * (j0 + bi) + 2, q);
+                        const uint32_t ns = 4u * static_cast<uint32_t>(hh);
                         const uint32_t one = 0x3C003C00u, bias = half2_bits(-1032.0f);
-                        h[0] = hfma2_u(half_pair_lo(c0), one, bias);
-                        h[1] = hfma2_u(half_pair_hi(c0), one, bias);
-                        h[2] = hfma2_u(half_pair_lo(c1), one, bias);
-                        h[3] = hfma2_u(half_pair_hi(c1), one, bias);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint32_t cq = (q[w] >> ns) & 0x0F0F0F0Fu;
+                            hv[2 * w] = hfma2_u(half_pair_lo(cq), one, bias);
+                            hv[2 * w + 1] = hfma2_u(half_pair_hi(cq), one, bias);
+                        }
                     }
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) hv[w] = 0u;
                 }
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                 bt + rg * 512 + kc * 128 + rw * 16),
-                             "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                // row n: group g, row j of the group; columns 16 hh .. + 15 are
+                // the K octets 2 hh and 2 hh + 1
+                const uint32_t bt = S + L.b + static_cast<uint32_t>(kb % NS) * kBTile + g * kBSbo + j * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh) * 128),
+                             "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
+                             : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh + 1) * 128),
+                             "r"(hv[4]), "r"(hv[5]), "r"(hv[6]), "r"(hv[7])
                              : "memory");
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_b_full(BARS, s));
-            if (j == 7 || kb == nkb - 1) {
+            if (lane == 0)
+                for (int bi = 0; bi < nbk; ++bi) mbar_arrive(bar_b_full(BARS, static_cast<int>((kb0 + bi) % NS)));
+            if (j0 + nbk == 8 || kb0 + nbk == nkb) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
             }
         }
     } else {
         // ------------------------------------------------------------ epilogue
-        const int quad = warp & 3;      // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
-        const int h = (warp - 6) >> 2;  // columns 64*h .. +63 of the tile
+        const int quad = warp & 3;           // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
+        const int h = (warp - kEpi0) >> 2;   // columns 64*h .. +63 of the tile
         const int64_t m = mt * BM + 32 * quad + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
         // q6_K: z (this super-block's s_x-weighted sums) in registers, the
@@ -551,27 +699,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
             }
             QMM_TRACE(31, kb);
             tc_fence_after();
-            float v[64];
-            tc_ld32(tl + ab * BN + 64 * h, *reinterpret_cast<float(*)[32]>(v));
-            tc_ld32(tl + ab * BN + 64 * h + 32, *reinterpret_cast<float(*)[32]>(v + 32));
-            tc_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
-            QMM_TRACE(32, kb);
-            if (a.dbg != nullptr && kb == 0 && m < a.M) {
-                for (int c = 0; c < 64; ++c)
-                    if (n0 + 64 * h + c < a.N) a.dbg[m * a.N + n0 + 64 * h + c] = v[c];
-            }
             const float sx = (m < a.M) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
             const float2 s2 = make_float2(sx, sx);
+            float v[32];
             if (Q6) {
+                // z += s_x * I, one 32-column half at a time (fewer registers)
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2, make_float2(z[c], z[c + 1]));
-                    z[c] = t.x;
-                    z[c + 1] = t.y;
+                for (int half = 0; half < 2; ++half) {
+                    tc_ld32(tl + ab * BN + 64 * h + 32 * half, v);
+                    tc_wait_ld();
+                    if (half == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
+                    }
+                    if (a.dbg != nullptr && kb == 0 && m < a.M) {
+                        for (int c = 0; c < 32; ++c)
+                            if (n0 + 64 * h + 32 * half + c < a.N)
+                                a.dbg[m * a.N + n0 + 64 * h + 32 * half + c] = v[c];
+                    }
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2,
+                                               make_float2(z[32 * half + c], z[32 * half + c + 1]));
+                        z[32 * half + c] = t.x;
+                        z[32 * half + c + 1] = t.y;
+                    }
                 }
+                QMM_TRACE(32, kb);
                 if ((kb & 7) == 7 || kb == nkb - 1) {
                     const int64_t sb = kb >> 3;
                     const int di = static_cast<int>(sb % DR);
@@ -581,30 +736,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                         break;
                     }
                     const uint32_t dv = S + L.dv + (di * BN + 64 * h) * 4;
+                    // y += d * z, 16 columns at a time (z is live throughout)
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float yv[32];
+                    for (int q = 0; q < 4; ++q) {
+                        float yv[16];
                         if (sb > 0) {
-                            tc_ld32(ty + 32 * half, yv);
+                            tc_ld16(ty + 16 * q, yv);
                             tc_wait_ld();
                         } else {
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) yv[c] = 0.0f;
+                            for (int c = 0; c < 16; ++c) yv[c] = 0.0f;
                         }
 #pragma unroll
-                        for (int c = 0; c < 32; c += 2) {
+                        for (int c = 0; c < 16; c += 2) {
                             float2 d2;
                             asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
                                          : "=f"(d2.x), "=f"(d2.y)
-                                         : "r"(dv + 4 * (32 * half + c)));
-                            const float2 t = ffma2(d2, make_float2(z[32 * half + c], z[32 * half + c + 1]),
+                                         : "r"(dv + 4 * (16 * q + c)));
+                            const float2 t = ffma2(d2, make_float2(z[16 * q + c], z[16 * q + c + 1]),
                                                    make_float2(yv[c], yv[c + 1]));
                             yv[c] = t.x;
                             yv[c + 1] = t.y;
-                            z[32 * half + c] = 0.0f;
-                            z[32 * half + c + 1] = 0.0f;
+                            z[16 * q + c] = 0.0f;
+                            z[16 * q + c + 1] = 0.0f;
                         }
-                        tc_st32(ty + 32 * half, yv);
+                        tc_st16(ty + 16 * q, yv);
                     }
                     tc_wait_st();
                     QMM_TRACE(34, kb);
@@ -615,15 +771,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
                     ok = false;
                     break;
                 }
-                const uint32_t dv = S + L.dv + (di * BN + 64 * h) * 4;
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float2 d2;
-                    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
-                    const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
-                                           make_float2(z[c], z[c + 1]));
-                    z[c] = t.x;  // Q4_0: z holds y
-                    z[c + 1] = t.y;
+                for (int half = 0; half < 2; ++half) {
+                    tc_ld32(tl + ab * BN + 64 * h + 32 * half, v);
+                    tc_wait_ld();
+                    if (half == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
+                    }
+                    if (a.dbg != nullptr && kb == 0 && m < a.M) {
+                        for (int c = 0; c < 32; ++c)
+                            if (n0 + 64 * h + 32 * half + c < a.N)
+                                a.dbg[m * a.N + n0 + 64 * h + 32 * half + c] = v[c];
+                    }
+                    const uint32_t dv = S + L.dv + (di * BN + 64 * h + 32 * half) * 4;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float2 d2;
+                        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
+                        const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
+                                               make_float2(z[32 * half + c], z[32 * half + c + 1]));
+                        z[32 * half + c] = t.x;  // Q4_0: z holds y
+                        z[32 * half + c + 1] = t.y;
+                    }
                 }
             }
         }
@@ -670,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs a) {
 
 // ---------------------------------------------------------------- launch
 
-using GemmKernel = void (*)(const GemmArgs);
+using GemmKernel = void (*)(const GemmArgs, const CUtensorMap);
 
 static GemmKernel pick_gemm(int fmt, bool exp) {
     if (fmt == FMT_Q6_K) return exp ? gemm_kernel<FMT_Q6_K, true> : gemm_kernel<FMT_Q6_K, false>;
@@ -713,11 +884,31 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
     a.K = K;
     a.nb = K / (fmt == FMT_Q6_K ? 256 : 32);
     a.total_bytes = N * a.nb * (fmt == FMT_Q6_K ? 210 : 18);
+    a.rowbytes = a.nb * (fmt == FMT_Q6_K ? 210 : 18);
+    a.n8 = N / 8 * 8;
     a.st = st;
     a.live_slot = live_slot;
     a.dbg = dbg;
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
-    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a);
+    // q6_K / Q4_0 rows: W as [N / 8][8 * rowbytes] bytes of 16-bit elements
+    // (the pitch of 8 rows is a multiple of 16 bytes for both formats); a box
+    // is one row slot wide and 16 groups of 8 rows high
+    CUtensorMap wmap;
+    memset(&wmap, 0, sizeof wmap);
+    if (!exp && a.n8 > 0) {
+        EncodeTiledFn enc = tensor_map_encoder();
+        if (!enc) return cudaErrorNotSupported;
+        const int rs = fmt == FMT_Q6_K ? kRawQ6K : kRawQ40;
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(a.n8 / 8)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(rs / 2), 16u};
+        const cuuint32_t es[2] = {1u, 1u};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(W), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a, wmap);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

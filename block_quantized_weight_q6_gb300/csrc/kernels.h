@@ -62,6 +62,14 @@ struct TcmvArgs {
 };
 
 using TcmvKernel = void (*)(const TcmvArgs, const CUtensorMap);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (null if
+// the driver has none)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tensor_map_encoder();
 TcmvKernel tcmv_pick_q6k(bool q8, int NB, int S);
 TcmvKernel tcmv_pick_q4_0(bool q8, int NB, int S);
 TcmvKernel tcmv_pick_q8_0(bool q8, int NB, int S);

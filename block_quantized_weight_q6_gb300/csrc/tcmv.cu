@@ -153,14 +153,7 @@ int tcmv_occupancy(int fmt, bool q8, int NB, int S) {
     return occ;
 }
 
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
+EncodeTiledFn tensor_map_encoder() {
     static EncodeTiledFn fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -172,6 +165,8 @@ EncodeTiledFn encode_fn() {
     }();
     return fn;
 }
+
+namespace {
 
 int row_slot_bytes(int fmt) { return fmt == FMT_Q6_K ? 240 : (fmt == FMT_Q4_0 ? 176 : 304); }
 
@@ -187,7 +182,7 @@ cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t 
     CUtensorMap map;
     memset(&map, 0, sizeof map);
     if (a.n8 > 0) {
-        EncodeTiledFn enc = encode_fn();
+        EncodeTiledFn enc = tensor_map_encoder();
         if (!enc) return cudaErrorNotSupported;
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes),
                                     static_cast<cuuint64_t>(a.n8 / 8)};

@@ -117,7 +117,11 @@ struct TcLayout {
     static constexpr int NC = NB * S;                          // columns per group
     static constexpr int G = NCOL / NC;                        // groups per window
     static constexpr int W = (GPS + G - 1) / G;                // windows per stage
-    static constexpr uint32_t DCOL0 = 2 * SA;                  // one A stage per decode set
+    // A half stages (SA / 2 columns) per decode set: three when a stage needs
+    // at most two windows (the MMAs of a half then have a further half stage
+    // of decoding to finish in), else two
+    static constexpr int NAH = (NCOL == 16 && W <= 2) ? 3 : 2;
+    static constexpr uint32_t DCOL0 = 2 * NAH * (SA / 2);
     static constexpr int NW0 = static_cast<int>((512 - DCOL0) / NCOL);
     static constexpr int NW = NW0 > 16 ? 16 : NW0;             // windows in flight
     // each MMA issuer (decode set) has its own NWS windows, so a window is
@@ -139,9 +143,9 @@ struct TcLayout {
     static constexpr uint32_t SOFF = XOFF + NX * XT;
     static constexpr uint32_t BARS = SOFF + NSC * SCB;
     // barriers: r_full[NR], r_empty[NR], x_full[NX], x_empty[NX], s_full[NSC],
-    // s_empty[NSC], a_full[2][2], a_empty[2][2] ([decode set][half stage]),
+    // s_empty[NSC], a_full[2][NAH], a_empty[2][NAH] ([decode set][half slot]),
     // d_full[NW], d_empty[NW], final
-    static constexpr uint32_t NBARS = 2 * NR + 2 * NX + 2 * NSC + 8 + 2 * NW + 1;
+    static constexpr uint32_t NBARS = 2 * NR + 2 * NX + 2 * NSC + 4 * NAH + 2 * NW + 1;
     static constexpr uint32_t TSLOT = BARS + 8 * NBARS;
     static constexpr uint32_t ABORT = TSLOT + 4;
     static constexpr uint32_t USED = (ABORT + 4 + 127) / 128 * 128;
@@ -593,16 +597,6 @@ __device__ __forceinline__ void tc_drain_window(uint32_t dcol, uint32_t sslot, i
     }
 }
 
-// ------------------------------------------------------------ tensor-map copy
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
-        "{%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
-
 // Tile row held by tensor-memory lane m (the A row an MMA reads): row
 // 8 * i + j, with the 8 lanes of every quarter warp taking 8 consecutive i of
 // one j. Row 8i + j sits in box j at slot i, so those 8 lanes read 8 different
@@ -701,8 +695,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t b_sfull = b_xempty + 8 * NX;
     const uint32_t b_sempty = b_sfull + 8 * NSC;
     const uint32_t b_afull = b_sempty + 8 * NSC;
-    const uint32_t b_aempty = b_afull + 32;
-    const uint32_t b_dfull = b_aempty + 32;
+    const uint32_t b_aempty = b_afull + 8 * 2 * L::NAH;
+    const uint32_t b_dfull = b_aempty + 8 * 2 * L::NAH;
     const uint32_t b_dempty = b_dfull + 8 * NW;
     const uint32_t b_final = b_dempty + 8 * NW;
     const uint32_t flag = sb + L::ABORT;
@@ -725,7 +719,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(b_sfull + 8 * r, 8);
             mbar_init(b_sempty + 8 * r, 4);
         }
-        for (int q = 0; q < 4; ++q) {  // [set][half]
+        for (int q = 0; q < 2 * L::NAH; ++q) {  // [set][half slot]
             mbar_init(b_afull + 8 * q, 8);
             mbar_init(b_aempty + 8 * q, 1);
         }
@@ -876,19 +870,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // K16 step t: NCOL rows x 16 K at t * NCOL * 32 bytes, core
                     // matrices 128 bytes apart along K, 256 between 8-row groups.
                     const uint64_t bdesc0 = tc::smem_desc(sb + L::XOFF + xslot * L::XT, 128, 256);
-                    const uint32_t abase = tmem + set * L::SA;
+                    // half stage h of this set's stage ls is the set's half hs =
+                    // 2 ls + h, in A slot hs % NAH (use hs / NAH)
+                    const uint32_t hs0 = 2 * (sc >> 1);
+                    uint32_t abase = 0, aslot = 0;
                     uint32_t dbase = 0, ws = 0;
 #pragma unroll
                     for (int i = 0; i < L::GPS; ++i) {
                         if (i == 0 || i == L::GPS / 2) {
-                            // the half stage of A this group belongs to
-                            const uint32_t ab = 2 * set + (i == 0 ? 0u : 1u);
-                            if (i != 0) tc::commit(b_aempty + 8 * (2 * set));
-                            if (!tcmv_wait_one(b_afull + 8 * ab, (sc >> 1) & 1u, flag, err)) {
+                            const uint32_t hs = hs0 + (i == 0 ? 0u : 1u);
+                            if (i != 0) tc::commit(b_aempty + 8 * aslot);
+                            aslot = set * L::NAH + hs % L::NAH;
+                            if (!tcmv_wait_one(b_afull + 8 * aslot, (hs / L::NAH) & 1u, flag, err)) {
                                 ok = false;
                                 break;
                             }
                             tc::fence_after();
+                            // the half's columns start at the slot; group i's offset
+                            // within its stage is taken relative to the half
+                            abase = tmem + aslot * (L::SA / 2) - (i == 0 ? 0u : L::SA / 2);
                         }
                         if (i % L::G == 0) {
                             const uint32_t wg = wc + i / L::G;
@@ -911,7 +911,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                         if (i % L::G == L::G - 1 || i == L::GPS - 1) tc::commit(b_dfull + 8 * ws);
                     }
-                    tc::commit(b_aempty + 8 * (2 * set + 1));
+                    tc::commit(b_aempty + 8 * aslot);
                     tc::commit(b_xempty + 8 * xslot);
                     TCMV_TRACE(2, sc);
                 }
@@ -959,15 +959,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // the other half is decoded
                 const uint32_t ls = sc >> 1;
                 const bool uni = a.rowbytes % 16 == 0;
-                const uint32_t acol = lane_base + myset * L::SA;
 #pragma unroll 1
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t ab = 2 * myset + h;
-                    if (ls >= 1 && !tcmv_wait_warp(b_aempty + 8 * ab, (ls - 1) & 1u, flag, err)) {
+                    // the set's half hs = 2 ls + h goes to A slot hs % NAH, once the
+                    // MMAs of the slot's previous half have read it
+                    const uint32_t hs = 2 * ls + h;
+                    const uint32_t ab = myset * L::NAH + hs % L::NAH;
+                    if (hs >= static_cast<uint32_t>(L::NAH) &&
+                        !tcmv_wait_warp(b_aempty + 8 * ab, ((hs / L::NAH) - 1) & 1u, flag, err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
+                    const uint32_t acol = lane_base + ab * (L::SA / 2) - static_cast<uint32_t>(h) * (L::SA / 2);
                     tc_decode_half<FMT>(rslot, lead, uni, acol, h, part);
                     tc::wait_st();
                     tc::fence_before();
