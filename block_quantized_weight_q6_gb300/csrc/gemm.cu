@@ -10,6 +10,13 @@
 // accumulator holds I exactly. The accumulator is drained once per K block
 // and the scales are applied on the CUDA cores.
 //
+// Exactness of the B values: sc * (q - 32) is formed as (off + c) * sc -
+// off * sc with one rounding (off = 1056 from the raw bits, 1152 from the
+// plane), so off * sc must be a finite fp16 and the result an exact one:
+// |sc| <= kScMax = 56 keeps both (|sc * (q - 32)| <= 1792). The synthetic
+// workloads draw sc on -32..31; a block with a larger scale sets
+// DERR_GEMM_SCALE, and the call reports an error instead of a wrong result.
+//
 // The two q6_K variants of "57 - r54 MINFER_MMQ_Q6K_EXP" section 2.1:
 //   EXP  : the B tile comes from the centered-int8 W_exp plane (one byte per
 //          weight, a plain copy; only the sub-block scale is applied);
@@ -47,6 +54,7 @@ constexpr int BM = 128;           // tokens per tile (tensor-memory lanes)
 constexpr int BN = 128;           // weight rows per tile (accumulator columns)
 constexpr int NS = 4;             // B stages (one 32-wide K block each)
 constexpr int NA = 8;             // A stages: the activation copies run up to NA blocks ahead
+constexpr int kScMax = 56;        // largest |q6_K sub-block scale| the fp16 B tile holds exactly
 constexpr int NR = 3;             // raw weight stages (256 columns each)
 constexpr int NBUF = 3;           // accumulator buffers in tensor memory
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
@@ -547,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cw = warp - kConv0;
         const int tid = threadIdx.x - 32 * kConv0;  // rows 0..127 store d
         const int g = lane & 15, hh = lane >> 4;
+        bool scale_bad = false;
         for (int64_t kb0 = 0; kb0 < nkb; kb0 += 2) {
             const int nbk = nkb - kb0 < 2 ? 1 : 2;
             const int64_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
@@ -631,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 c[w] = ((ql[w] >> ns) & 0x0F0F0F0Fu) | (((qh[w] >> hs) & 0x03030303u) << 4);
                         }
                         // sc * (v - off) exactly: (off + v) * sc - off * sc, one rounding
+                        if (scv > kScMax || scv < -kScMax) scale_bad = true;
                         const float scf = static_cast<float>(scv);
                         const float off = EXP ? 1152.0f : 1056.0f;
                         const uint32_t sc2 = half2_bits(scf);
@@ -676,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
             }
         }
+        if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;           // tensor-memory lanes 32*quad .. +31 (warp id mod 4)

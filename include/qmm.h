@@ -181,6 +181,11 @@ int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int
  *   plane must come from qmm_plane_build for this same W, N and K, else
  *   QMM_EPLANE.
  * Q4_0: in-kernel expansion only; exp_plane must be NULL.
+ * Range: the fp16 B tile holds sc * (q - 32) exactly for q6_K sub-block
+ *   scales in -56..56 (the synthetic workloads draw -32..31). A matrix with a
+ *   larger scale makes the next qmm_sync_check return QMM_EUNSUPPORTED, and
+ *   Y is then not valid. The matvec (qmm_gemv) has no such limit: it applies
+ *   the scales in fp32.
  * Needs workspace (quantized X). */
 int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M,
              int64_t N, int64_t K, const int8_t* exp_plane);

@@ -227,3 +227,45 @@ print(int(wanted), l["gemm_exp_off"], l["gemm_fallback"], l["gemm_in_kernel"], l
     assert r.returncode == 0, r.stderr
     assert r.stdout.split() == ["1", "0", "1", "0", "0"]
     assert "fallback!" in r.stderr
+
+
+@pytest.mark.gpu
+def test_q6k_gemm_scale_range():
+    """Sub-block scales up to +-56 stay exact in the fp16 B tile (both
+    variants, against the oracle); a larger scale is reported by
+    qmm_sync_check instead of yielding a wrong Y. The matvec, which applies
+    the scales in fp32, takes the large scale exactly."""
+    M, N, K = 40, 136, 512
+    W = synth.q6k_matrix(71, N, K)
+    X = synth.normal_bf16(72, (M, K))
+    W = W.copy()
+    W.reshape(-1, 210)[::7, 192 + 3] = np.uint8(56)               # +56 on some blocks
+    W.reshape(-1, 210)[1::7, 192 + 9] = np.uint8(256 - 56)        # -56 on others
+    Wt = dev(W)
+    Y2 = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    plane = qmm.plane_build(Wt, N, K)
+    Y1 = run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)
+    qmm.plane_release(Wt)
+    assert np.array_equal(Y1.view(np.int32), Y2.view(np.int32))
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemv_q8(qmm.Q6_K, W, xq, s, N, K)
+    assert_within(Y2, ref, absum, "q6_K GEMM, scales +-56")
+
+    Wbig = W.copy()
+    Wbig.reshape(-1, 210)[5, 192 + 2] = np.uint8(100)
+    Wb = dev(Wbig)
+    Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    qmm.gemm(qmm.Q6_K, Wb, x_tensor(X), Y, M, N, K, None)
+    torch.cuda.synchronize()
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.sync_check()
+    assert ei.value.code == qmm.EUNSUPPORTED
+    qmm.sync_check()  # the error word was cleared by the report
+
+    x1 = synth.normal_bf16(73, (2, K))
+    y = torch.empty((2, N), dtype=torch.float32, device="cuda")
+    qmm.gemv(qmm.Q6_K, Wb, x_tensor(x1), y, N, K)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    ref, absum = oracle.gemv_float(qmm.Q6_K, Wbig, x1, N, K)
+    assert_within(y.cpu().numpy(), ref, absum, "q6_K matvec, scale 100")
