@@ -20,8 +20,16 @@ Prints one JSON line (rank 0).
 
 python bench.py --profile PART runs one part W + K times without timing it,
 for profilers: PART is decode, decode:NAME:B (one matvec of the decode set,
-e.g. decode:output:1), gemm_exp_plane, gemm_in_kernel, moe_t1 or moe_t16.
+e.g. decode:output:1), gemm_exp_plane, gemm_in_kernel, moe_t1 or moe_t16
+(moe_t16:E routes over E experts instead of 256, for small captures).
 Only that part's inputs are made.
+
+python bench.py --sweep runs the 32-layer 7B-shaped prefill sweep instead:
+every layer's Q4_0 wq/wk/wo/w1/w3 through the GEMM with in-kernel expansion,
+its q6_K attn_v/ffn_down and the q6_K output matrix with the W_exp plane on
+and off, at M = 128, 512 and 2048 bf16 tokens; it prints one JSON line with
+whole-sweep TOPS per M and variant and the measured device-memory delta of
+the planes.
 """
 from __future__ import annotations
 
@@ -211,11 +219,14 @@ class GemmCase:
 
 
 class MoeWeights:
-    """256 Q4_0 experts (gate/up 2048x7168, down 7168x2048) resident in HBM."""
+    """256 Q4_0 experts (gate/up 2048x7168, down 7168x2048) resident in HBM
+    (fewer, for profiler captures that must stay small)."""
     E, H, I, k = 256, 7168, 2048, 8
 
-    def __init__(self, torch, device):
+    def __init__(self, torch, device, n_experts=None):
         import synth
+        if n_experts is not None:
+            self.E = n_experts
         E, H, I = self.E, self.H, self.I
         self.g = synth.matrix_torch(synth.Q4_0, synth.workload_seed(3, 0), I, H, device, E)
         self.u = synth.matrix_torch(synth.Q4_0, synth.workload_seed(3, 1), I, H, device, E)
@@ -343,6 +354,74 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ main
 
+# read + write DRAM bytes of the MoE part per distinct expert (ncu, 24 experts, T=16)
+MOE_DRAM_BYTES_PER_EXPERT = (9216 + 244992 + 398277120 + 991232 + 199352576 + 2329088 + 3683328) / 24
+
+SWEEP_LAYER = [  # (name, fmt name, N, K) of one layer
+    ("wq", "Q4_0", 4096, 4096), ("wk", "Q4_0", 4096, 4096), ("wo", "Q4_0", 4096, 4096),
+    ("w1", "Q4_0", 11008, 4096), ("w3", "Q4_0", 11008, 4096),
+    ("attn_v", "q6_K", 4096, 4096), ("ffn_down", "q6_K", 4096, 11008),
+]
+SWEEP_OUTPUT = ("output", "q6_K", 32000, 4096)
+
+
+def run_sweep(args):
+    """The 32-layer prefill sweep: whole-sweep TOPS at M = 128, 512, 2048 with
+    the q6_K planes on and off, and the planes' device-memory delta."""
+    import torch
+    import synth
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_quantized_weight_q6_gb300 as qmm
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    mats = []  # (fmt code, N, K, W)
+    for layer in range(args.sweep_layers):
+        for mid, (name, fmt, N, K) in enumerate(SWEEP_LAYER):
+            W = synth.matrix_torch(FMT_CODE[fmt], synth.workload_seed(4, 16 * layer + mid), N, K, device)[0]
+            mats.append((FMT_CODE[fmt], N, K, W))
+    name, fmt, N, K = SWEEP_OUTPUT
+    mats.append((FMT_CODE[fmt], N, K, synth.matrix_torch(FMT_CODE[fmt], synth.workload_seed(4, 15), N, K, device)[0]))
+    torch.cuda.synchronize(device)
+    # the planes, and the device memory they take
+    q6 = [(N, K, W) for f, N, K, W in mats if f == synth.Q6_K]
+    free0, _ = torch.cuda.mem_get_info(device)
+    planes = [qmm.plane_build(W, N, K) for N, K, W in q6]
+    torch.cuda.synchronize(device)
+    free1, _ = torch.cuda.mem_get_info(device)
+    plane_bytes = sum(qmm.plane_bytes(N, K) for N, K, _ in q6)
+    ops_per_token = sum(2 * N * K for _, N, K, _ in mats)
+    out = {"sweep": f"{args.sweep_layers} layers x (Q4_0 wq/wk/wo/w1/w3 + q6_K attn_v/ffn_down) + q6_K output",
+           "data": "synthetic", "plane_bytes": plane_bytes,
+           "plane_mem_delta_bytes": int(free0 - free1), "results": {}}
+    for M in (128, 512, 2048):
+        xs = {K: torch.from_numpy(synth.normal_bf16(synth.workload_seed(4, 100 + K % 97 + M), (M, K)).view(np.int16)
+                                  ).to(device).view(torch.bfloat16) for K in (4096, 11008)}
+        Y = torch.empty((M, 32000), dtype=torch.float32, device=device)
+        res = {}
+        for variant in ("plane_on", "plane_off"):
+            pl = {id(W): p for (N, K, W), p in zip(q6, planes)} if variant == "plane_on" else {}
+
+            def fn():
+                for f, N, K, W in mats:
+                    qmm.gemm(f, W, xs[K], Y.view(-1)[: M * N], M, N, K, pl.get(id(W)))
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(device)
+            qmm.sync_check()
+            ms = e0.elapsed_time(e1)
+            res[variant] = {"ms": ms, "tops": ops_per_token * M / (ms * 1e-3) / 1e12}
+        out["results"][str(M)] = res
+    for N, K, W in q6:
+        qmm.plane_release(W)
+    print(json.dumps(out))
+
+
 def run_profile(args):
     """One part of the step (or one matvec of the decode set), W + K times."""
     import torch
@@ -364,7 +443,10 @@ def run_profile(args):
         gem = GemmCase(torch, device)
         fn = gem.run_exp if part[0] == "gemm_exp_plane" else gem.run_in_kernel
     elif part[0] in ("moe_t1", "moe_t16"):
-        fn = MoeCase(torch, device, MoeWeights(torch, device), 1 if part[0] == "moe_t1" else 16).run
+        ne = int(part[1]) if len(part) > 1 else None
+        case = MoeCase(torch, device, MoeWeights(torch, device, ne), 1 if part[0] == "moe_t1" else 16)
+        print(json.dumps({"moe_distinct_experts": case.distinct, "expert_bytes": case.expert_bytes}))
+        fn = case.run
     else:
         raise SystemExit(f"unknown part {args.profile}")
     for _ in range(args.warmup + args.steps):
@@ -383,9 +465,15 @@ def main():
                     help="seconds of CPU work for the oracle baseline")
     ap.add_argument("--profile", default=None,
                     help="run one part untimed (for profilers) and exit")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the 32-layer prefill sweep (plane on/off, M = 128, 512, 2048)")
+    ap.add_argument("--sweep-layers", type=int, default=32)
     args = ap.parse_args()
     if args.profile:
         run_profile(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":
@@ -490,7 +578,7 @@ def main():
     tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
     seg = {
         "decode": {"bound": "hbm", "achieved": dec.algo_bytes / (ms_dec * 1e-3) / 1e9, "peak": hbm,
-                   "unit": "GB/s", "kernel": "gemv_kernel (decode set, average over launches)"},
+                   "unit": "GB/s", "kernel": "tcmv_kernel (tensor-core matvec) + split-K reduce, decode set: part time over all launches"},
         "gemm_exp_plane": {"bound": "tensor", "achieved": tops["gemm_exp_plane"], "peak": tc_peak,
                            "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, plane> + quantize"},
         "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,
@@ -506,6 +594,13 @@ def main():
     dominant = max(part_ms, key=part_ms.get)
     roofline = dict(seg[dominant])
     roofline.update({"part": dominant, "traffic": None, "peak_source": pk["source"]})
+    # DRAM bytes (read + write) per expert touched by the MoE part, from the
+    # ncu capture in profiles/moe_mv_q4_0_t16_24experts.md (all five kernels
+    # of one call over 24 experts), scaled to the experts this step touches
+    if dominant in ("moe_t1", "moe_t16"):
+        case = moe1 if dominant == "moe_t1" else moe16
+        roofline["traffic"] = MOE_DRAM_BYTES_PER_EXPERT * case.distinct
+        roofline["traffic_note"] = "scaled from a 24-expert ncu capture by distinct experts"
 
     cpu = None
     if rank == 0:
