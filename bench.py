@@ -185,7 +185,22 @@ class DecodeSet:
                 self.h2d += 2 * B * K
                 self.d2h += 4 * B * N
 
+        # one grouped matvec call per (batch, format): the set's 18 matvecs in 6 launches
+        self.groups = []
+        for B in BATCHES:
+            for fmt in ("Q4_0", "q6_K", "Q8_0"):
+                its = [it for it in self.items if it[4] == B and it[1] == fmt]
+                self.groups.append(qmm.GemvGroup(FMT_CODE[fmt], [it[5] for it in its], [it[6] for it in its],
+                                                 [it[7] for it in its], [it[2] for it in its],
+                                                 [it[3] for it in its], act))
+
     def run(self):
+        """The set as grouped calls (the step's decode part)."""
+        for g in self.groups:
+            self.qmm.gemv_group(g)
+
+    def run_per_call(self):
+        """The same set as 18 single matvec calls."""
         for (name, fmt, N, K, B, W, x, y) in self.items:
             self.qmm.gemv(FMT_CODE[fmt], W, x, y, N, K, self.act)
 
@@ -545,6 +560,13 @@ def main():
     # GEMM outputs of the two variants are bitwise identical by construction
     gem_identical = bool(torch.equal(gem.Y1.view(torch.int32), gem.Y2.view(torch.int32)))
 
+    # the decode set as 18 single matvec calls (reported beside the grouped part)
+    g_dpc = capture(torch, dec.run_per_call, device)
+    for _ in range(args.warmup):
+        g_dpc.replay()
+    ms_dec_pc = max_over_ranks(world, time_graph(torch, g_dpc, args.steps, device), device)
+    del g_dpc
+
     # the same decode set with per-32 quantized activations (integer dot products)
     dec8 = DecodeSet(torch, device, act=qmm.ACT_Q8)
     g_dec8 = capture(torch, dec8.run, device)
@@ -630,6 +652,10 @@ def main():
             "parts_ms": part_ms,
             "segments": seg,
             "hbm_frac_of_measured": gbs / hbm,
+            "decode_per_call": {"value": dec.weight_bytes / (ms_dec_pc * 1e-3) / 1e9 * world,
+                                "unit": "GB/s", "ms_per_step": ms_dec_pc,
+                                "note": "the decode set as 18 single qmm_gemv calls (the step's decode "
+                                        "part makes one grouped call per batch and format)"},
             "q8_mode": {"value": dec.weight_bytes / (ms_dec8 * 1e-3) / 1e9 * world, "unit": "GB/s",
                         "ms_per_step": ms_dec8,
                         "note": "same decode set, activations quantized per 32 (int8 dot products)"},

@@ -58,6 +58,9 @@ def _load():
         "qmm_gemv": (I, [U32, P, P, P, I64, I64, I]),
         "qmm_quantize_q8": (I, [U32, P, I64, I64, P, P]),
         "qmm_gemv_noalloc": (I, [U32, P, P, P, I64, I64, I]),
+        "qmm_gemv_group": (I, [U32, I, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                               C.POINTER(C.c_void_p), C.POINTER(C.c_int64), C.POINTER(C.c_int64), I]),
+        "qmm_gemv_group_workspace_bytes": (SZ, [U32, I, C.POINTER(C.c_int64), C.POINTER(C.c_int64), I]),
         "qmm_gemm": (I, [U32, P, P, P, I64, I64, I64, P]),
         "qmm_plane_bytes": (SZ, [I64, I64]),
         "qmm_plane_wanted": (I, [I64, I64]),
@@ -148,6 +151,36 @@ def gemv(fmt: int, W, x, y, N: int, K: int, act: int = ACT_FLOAT):
     _prepare(x.device, lib.qmm_workspace_bytes(code, B, N, K))
     with _torch().cuda.device(x.device):
         _check(lib.qmm_gemv(code, _ptr(W), _ptr(x), _ptr(y), N, K, B))
+
+
+class GemvGroup:
+    """A fixed set of matvecs of one format and batch for gemv_group: the
+    host arrays of the call, built once (keep the object while it is used)."""
+
+    def __init__(self, fmt: int, Ws, xs, ys, Ns, Ks, act: int = ACT_FLOAT):
+        n = len(Ws)
+        if not (len(xs) == len(ys) == len(Ns) == len(Ks) == n):
+            raise ValueError("Ws, xs, ys, Ns, Ks must have the same length")
+        B = xs[0].shape[0]
+        self.n, self.B, self.device = n, B, xs[0].device
+        self.code = fmt | _act_bits(xs[0]) | act
+        P = C.c_void_p * n
+        L = C.c_int64 * n
+        self._W = P(*[t.data_ptr() for t in Ws])
+        self._x = P(*[t.data_ptr() for t in xs])
+        self._y = P(*[t.data_ptr() for t in ys])
+        self._N = L(*Ns)
+        self._K = L(*Ks)
+        self._keep = (list(Ws), list(xs), list(ys))
+        self.ws = lib.qmm_gemv_group_workspace_bytes(self.code, n, self._N, self._K, B)
+
+
+def gemv_group(group: GemvGroup):
+    """y[i] = W[i] x[i] for every matvec of the group, in one launch."""
+    _prepare(group.device, group.ws)
+    with _torch().cuda.device(group.device):
+        _check(lib.qmm_gemv_group(group.code, group.n, group._W, group._x, group._y, group._N,
+                                  group._K, group.B))
 
 
 def quantize_q8(x, xq, s):

@@ -7,7 +7,10 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <vector>
+#include <algorithm>
 #include <unordered_map>
 
 #include "kernels.h"
@@ -232,6 +235,170 @@ int run_gemv(int wf, bool q8, bool bf16, const void* W, const void* x, float* y,
     return QMM_OK;
 }
 
+// ---------------------------------------------------------------- grouped matvec plan
+// Several matvecs of one format and batch in one launch (tcmv over a
+// TcmvGroup): one stage range `sps` for all of them, chosen by simulating
+// the launch's round-robin walk of the items (CTA c takes items c, c + grid,
+// ...): an item costs its stages plus kItemFill stage-times of pipeline fill
+// and drain, and partial sums cost kReduce more for their reductions.
+struct GroupPlan {
+    int NB, S, ncol, grid, n;
+    int64_t sps, items;
+    int64_t nst[kTcMaxMats], tiles[kTcMaxMats], pieces[kTcMaxMats], item0[kTcMaxMats];
+    size_t ws_xt[kTcMaxMats], ws_xs[kTcMaxMats], ws_part[kTcMaxMats], ws_total;
+};
+
+constexpr double kItemFill = 2.0, kReduce = 3.0;
+
+double group_makespan(const GroupPlan& p, int64_t sps, int64_t slots, int64_t* items_out) {
+    std::vector<double> cost;
+    bool split = false;
+    for (int m = 0; m < p.n; ++m) {
+        const int64_t pieces = (p.nst[m] + sps - 1) / sps;
+        split = split || pieces > 1;
+        for (int64_t pc = 0; pc < pieces; ++pc) {
+            const double c = static_cast<double>(std::min(sps, p.nst[m] - pc * sps)) + kItemFill;
+            for (int64_t t = 0; t < p.tiles[m]; ++t) cost.push_back(c);
+        }
+    }
+    const int64_t items = static_cast<int64_t>(cost.size());
+    const int64_t grid = items < slots ? items : slots;
+    double worst = 0.0;
+    for (int64_t c = 0; c < grid; ++c) {
+        double t = 0.0;
+        for (int64_t i = c; i < items; i += grid) t += cost[i];
+        worst = std::max(worst, t);
+    }
+    *items_out = items;
+    return worst + (split ? kReduce : 0.0);
+}
+
+int plan_gemv_group(int fmt, bool q8, bool bf16, int B, int n, const int64_t* N, const int64_t* K, int sms,
+                    GroupPlan* p) {
+    p->n = n;
+    p->NB = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+    p->S = (q8 || bf16) ? 1 : 3;
+    p->ncol = tcmv_ncol(p->NB, p->S);
+    const int bps = tcmv_stage_blocks(fmt);
+    int64_t max_nst = 1;
+    for (int m = 0; m < n; ++m) {
+        p->nst[m] = (K[m] / block_elems(fmt) + bps - 1) / bps;
+        p->tiles[m] = (N[m] + 127) / 128;
+        max_nst = std::max(max_nst, p->nst[m]);
+    }
+    const int occ = tcmv_occupancy(fmt, q8, p->NB, p->S);
+    if (occ <= 0)
+        return fail(QMM_ECUDA, "matvec kernel (fmt %d, NB %d, S %d) cannot launch", fmt, p->NB, p->S);
+    const int64_t slots = static_cast<int64_t>(sms) * occ;
+    double best = 1e300;
+    int64_t best_sps = max_nst, prev_pieces = -1;
+    for (int64_t sps = max_nst; sps >= 1; --sps) {
+        const int64_t pieces = (max_nst + sps - 1) / sps;
+        if (pieces == prev_pieces) continue;  // the same split of the longest matrix
+        prev_pieces = pieces;
+        int64_t items = 0;
+        const double t = group_makespan(*p, sps, slots, &items);
+        if (t < best - 1e-9) {
+            best = t;
+            best_sps = sps;
+        }
+    }
+    p->sps = best_sps;
+    p->items = 0;
+    size_t off = 0;
+    for (int m = 0; m < n; ++m) {
+        p->pieces[m] = (p->nst[m] + p->sps - 1) / p->sps;
+        p->item0[m] = p->items;
+        p->items += p->tiles[m] * p->pieces[m];
+        p->ws_xt[m] = off;
+        if (q8 || !bf16) off = round_up(off + static_cast<size_t>(p->nst[m]) * p->ncol * 256 * 2, 256);
+        p->ws_xs[m] = off;
+        if (q8) off = round_up(off + static_cast<size_t>(p->nst[m]) * 8 * p->NB * 4, 256);
+        p->ws_part[m] = off;
+        if (p->pieces[m] > 1) off = round_up(off + static_cast<size_t>(p->pieces[m]) * B * N[m] * 4, 256);
+    }
+    p->ws_total = off;
+    p->grid = static_cast<int>(p->items < slots ? p->items : slots);
+    return QMM_OK;
+}
+
+// Plans are cached per shape: the simulation costs a few hundred microseconds.
+int plan_gemv_group_cached(int fmt, bool q8, bool bf16, int B, int n, const int64_t* N, const int64_t* K,
+                           int sms, GroupPlan* p) {
+    static std::mutex mu;
+    static std::map<std::vector<int64_t>, GroupPlan> cache;
+    std::vector<int64_t> key = {fmt, q8 ? 1 : 0, bf16 ? 1 : 0, B, n, sms};
+    for (int m = 0; m < n; ++m) {
+        key.push_back(N[m]);
+        key.push_back(K[m]);
+    }
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *p = it->second;
+            return QMM_OK;
+        }
+    }
+    int rc = plan_gemv_group(fmt, q8, bf16, B, n, N, K, sms, p);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = *p;
+    return QMM_OK;
+}
+
+int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void* const* x, float* const* y,
+                   const int64_t* N, const int64_t* K, int B, const GroupPlan& p, uint8_t* ws,
+                   const DevInfo* d) {
+    static thread_local TcmvGroup g;  // large: kept off the stack
+    g.nmat = p.n;
+    g.items = p.items;
+    g.st = d->st;
+    g.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
+    const bool tile = q8 || !bf16;
+    cudaError_t e;
+    for (int m = 0; m < p.n; ++m) {
+        TcmvArgs& a = g.m[m];
+        a = TcmvArgs{};
+        a.W = static_cast<const uint8_t*>(W[m]);
+        a.N = N[m];
+        a.K = K[m];
+        a.nb = K[m] / block_elems(wf);
+        a.total_bytes = N[m] * a.nb * block_bytes(wf);
+        a.rowbytes = a.nb * block_bytes(wf);
+        a.n8 = N[m] / 8 * 8;
+        a.x = x[m];
+        a.x_bf16 = bf16 ? 1 : 0;
+        a.xt = tile ? reinterpret_cast<const uint16_t*>(ws + p.ws_xt[m]) : nullptr;
+        a.xs = q8 ? reinterpret_cast<const float*>(ws + p.ws_xs[m]) : nullptr;
+        a.B = B;
+        a.y = y[m];
+        a.part = p.pieces[m] > 1 ? reinterpret_cast<float*>(ws + p.ws_part[m]) : nullptr;
+        a.tiles = p.tiles[m];
+        a.nst = p.nst[m];
+        a.sps = p.sps;
+        a.pieces = p.pieces[m];
+        a.items = p.tiles[m] * p.pieces[m];
+        a.item0 = p.item0[m];
+        a.st = d->st;
+        a.live_slot = g.live_slot;
+        if (tile) {
+            e = act_tile_launch(x[m], bf16, B, K[m], wf, p.NB, p.S, p.ncol, p.nst[m], q8,
+                                const_cast<uint16_t*>(a.xt), const_cast<float*>(a.xs), t_stream, d->st);
+            if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
+        }
+    }
+    e = tcmv_launch_group(wf, q8, p.NB, p.S, p.grid, t_stream, g);
+    if (e != cudaSuccess) return cuda_fail(e, "grouped matvec launch");
+    for (int m = 0; m < p.n; ++m) {
+        if (p.pieces[m] <= 1) continue;
+        e = splitk_reduce_launch(g.m[m].part, y[m], static_cast<int>(p.pieces[m]),
+                                 static_cast<int64_t>(B) * N[m], t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
+    }
+    return QMM_OK;
+}
+
 int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, int64_t N,
                     int64_t K, int B, int* wf, bool* bf16, bool* q8) {
     int rc = check_fmt(fmt, wf, bf16, q8);
@@ -290,6 +457,49 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
         return fail(QMM_ENOWORKSPACE, "qmm_gemv needs %zu bytes of workspace, %zu set", p.ws_total,
                     t_ws_bytes);
     return run_gemv(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(t_ws), d);
+}
+
+static int check_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const* x,
+                            float* const* y, const int64_t* N, const int64_t* K, int B, int* wf, bool* bf16,
+                            bool* q8) {
+    if (n < 1 || n > kTcMaxMats) return fail(QMM_EINVAL, "n = %d outside 1..%d", n, kTcMaxMats);
+    if (!W || !x || !y || !N || !K) return fail(QMM_EINVAL, "null array");
+    for (int m = 0; m < n; ++m) {
+        int rc = check_gemv_args(fmt, W[m], x[m], y[m], N[m], K[m], B, wf, bf16, q8);
+        if (rc) return rc;
+    }
+    return QMM_OK;
+}
+
+int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const* x, float* const* y,
+                   const int64_t* N, const int64_t* K, int B) {
+    qmm_init();
+    int wf;
+    bool bf16, q8;
+    int rc = check_gemv_group(fmt, n, W, x, y, N, K, B, &wf, &bf16, &q8);
+    if (rc) return rc;
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    GroupPlan p;
+    if ((rc = plan_gemv_group_cached(wf, q8, bf16, B, n, N, K, d->sms, &p))) return rc;
+    if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
+        return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set", p.ws_total,
+                    t_ws_bytes);
+    return run_gemv_group(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(t_ws), d);
+}
+
+size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, const int64_t* K, int B) {
+    qmm_init();
+    int wf;
+    bool bf16, q8;
+    if (check_fmt(fmt, &wf, &bf16, &q8) || n < 1 || n > kTcMaxMats || !N || !K || B < 1 || B > 16) return 0;
+    for (int m = 0; m < n; ++m)
+        if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf)) return 0;
+    DevInfo* d;
+    if (dev_info(&d)) return 0;
+    GroupPlan p;
+    if (plan_gemv_group_cached(wf, q8, bf16, B, n, N, K, d->sms, &p)) return 0;
+    return p.ws_total;
 }
 
 int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int8_t* xq,

@@ -57,11 +57,25 @@ struct TcmvArgs {
     float* y;              // [B][N] when pieces == 1
     float* part;           // [pieces][B][N] when pieces > 1
     int64_t tiles, nst, sps, pieces, items;  // items = tiles * pieces
+    int64_t item0;         // in a group: the first item of this matrix
     DevState st;
     int live_slot;
 };
 
-using TcmvKernel = void (*)(const TcmvArgs, const CUtensorMap);
+// One matvec launch over up to kTcMaxMats matrices of one format and batch:
+// the items of matrix m are item0 .. item0 + items - 1 of the launch, in
+// matrix order; map[m] is matrix m's weight tensor map (tcmv.cu).
+constexpr int kTcMaxMats = 12;
+struct TcmvGroup {
+    CUtensorMap map[kTcMaxMats];
+    TcmvArgs m[kTcMaxMats];
+    int nmat;
+    int64_t items;
+    DevState st;
+    int live_slot;
+};
+
+using TcmvKernel = void (*)(const TcmvGroup);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (null if
 // the driver has none)
@@ -88,6 +102,9 @@ int tcmv_occupancy(int fmt, bool q8, int NB, int S);
 // builds the weights' tensor map (W seen as rows of 8 weight rows) and launches
 cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s,
                         const TcmvArgs& a);
+// the same for a group (g.m[0 .. nmat-1], items and item0 filled in; the
+// maps are filled here)
+cudaError_t tcmv_launch_group(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s, TcmvGroup& g);
 // activations [B][K] (fp32 or bf16) -> the matvec's bf16 activation operand
 // for weight format fmt (tcmv.cu); q8 mode quantizes per 32 first and also
 // writes the scales as [block][NB]

@@ -172,30 +172,51 @@ int row_slot_bytes(int fmt) { return fmt == FMT_Q6_K ? 240 : (fmt == FMT_Q4_0 ? 
 
 }  // namespace
 
-cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s,
-                        const TcmvArgs& a) {
+namespace {
+
+// W as [N / 8][8 * rowbytes] bytes of 16-bit elements: the pitch of 8 rows is
+// a multiple of 16 bytes for every even row size; a box is one row slot wide
+// and 16 groups of 8 rows high. No map (zeros) when W has fewer than 8 rows.
+cudaError_t weight_map(int fmt, const TcmvArgs& a, CUtensorMap* map) {
+    memset(map, 0, sizeof *map);
+    if (a.n8 <= 0) return cudaSuccess;
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(a.n8 / 8)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_slot_bytes(fmt) / 2), 16u};
+    const cuuint32_t es[2] = {1u, 1u};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(a.W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t tcmv_launch_group(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s, TcmvGroup& g) {
     TcmvKernel k = pick(fmt, q8, NB, S);
     if (!k || tcmv_occupancy(fmt, q8, NB, S) <= 0) return cudaErrorInvalidValue;
-    // W as [N / 8][8 * rowbytes] bytes of 16-bit elements: the pitch of 8 rows
-    // is a multiple of 16 bytes for every even row size; a box is one row
-    // slot wide and 16 groups of 8 rows high
-    CUtensorMap map;
-    memset(&map, 0, sizeof map);
-    if (a.n8 > 0) {
-        EncodeTiledFn enc = tensor_map_encoder();
-        if (!enc) return cudaErrorNotSupported;
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes),
-                                    static_cast<cuuint64_t>(a.n8 / 8)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
-        const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_slot_bytes(fmt) / 2), 16u};
-        const cuuint32_t es[2] = {1u, 1u};
-        if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(a.W), dims, strides,
-                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+    if (g.nmat < 1 || g.nmat > kTcMaxMats) return cudaErrorInvalidValue;
+    for (int m = 0; m < g.nmat; ++m) {
+        cudaError_t e = weight_map(fmt, g.m[m], &g.map[m]);
+        if (e != cudaSuccess) return e;
     }
-    cudaError_t e = launch_pdl(k, dim3(grid), dim3(kTcThreads), smem_of(fmt, NB, S), s, a, map);
+    cudaError_t e = launch_pdl(k, dim3(grid), dim3(kTcThreads), smem_of(fmt, NB, S), s, g);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t s,
+                        const TcmvArgs& a) {
+    static thread_local TcmvGroup g;  // large: kept off the stack
+    g.nmat = 1;
+    g.m[0] = a;
+    g.m[0].item0 = 0;
+    g.items = a.items;
+    g.st = a.st;
+    g.live_slot = a.live_slot;
+    return tcmv_launch_group(fmt, q8, NB, S, grid, s, g);
 }
 
 cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt, int NB, int S,

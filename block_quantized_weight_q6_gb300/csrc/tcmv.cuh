@@ -627,13 +627,19 @@ __device__ __forceinline__ uint32_t tc_row_slot(const TcmvArgs& a, uint32_t stag
 // same sequence of (item, stage) pairs, so stage k of the walk uses raw slot
 // k % NR in every role.
 struct TcItem {
+    int m;  // the group's matrix
     int64_t tile, piece, s0, s1;
 };
 
-__device__ __forceinline__ TcItem tc_item(const TcmvArgs& a, int64_t item) {
+__device__ __forceinline__ TcItem tc_item(const TcmvGroup& g, int64_t item) {
     TcItem it;
-    it.tile = item % a.tiles;
-    it.piece = item / a.tiles;
+    it.m = 0;
+    for (int m = 1; m < g.nmat; ++m)
+        if (item >= g.m[m].item0) it.m = m;
+    const TcmvArgs& a = g.m[it.m];
+    const int64_t local = item - a.item0;
+    it.tile = local % a.tiles;
+    it.piece = local / a.tiles;
     it.s0 = it.piece * a.sps;
     it.s1 = min(it.s0 + a.sps, a.nst);
     return it;
@@ -680,7 +686,7 @@ __device__ __forceinline__ void tc_gather_x_stage(const TcmvArgs& a, int64_t s, 
 
 template <int FMT, bool Q8, int NB, int S>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tcmv_kernel(const TcmvArgs a, const __grid_constant__ CUtensorMap tmap) {
+    tcmv_kernel(const __grid_constant__ TcmvGroup g) {
     using F = TcF<FMT>;
     using L = TcLayout<FMT, NB, S>;
     constexpr int NCOL = L::NCOL;
@@ -701,10 +707,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t b_final = b_dempty + 8 * NW;
     const uint32_t flag = sb + L::ABORT;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    unsigned int* err = a.st.err;
+    unsigned int* err = g.st.err;
 
     grid_launch_dependents();
-    live_bump(a.st, a.live_slot);
+    live_bump(g.st, g.live_slot);
     if (threadIdx.x == 0) {
         for (int r = 0; r < NR; ++r) {
             mbar_init(b_rfull + 8 * r, 1);
@@ -751,11 +757,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------------------------------------------- raw producer
         // Weights only: they are constant, so no wait for the kernel that
         // precedes this one.
-        const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
         uint32_t sc = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-            const TcItem it = tc_item(a, item);
+        for (int64_t item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+            const TcItem it = tc_item(g, item);
+            const TcmvArgs& a = g.m[it.m];
+            const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
             for (int64_t s = it.s0; s < it.s1; ++s, ++sc) {
                 const uint32_t slot = sc % NR;
                 if (sc >= static_cast<uint32_t>(NR) &&
@@ -800,7 +807,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (boxes && lane < 8) {
                     // box j: row j of the 16 groups of 8 rows of this tile
                     const int64_t xb = (lane * a.rowbytes + koff) & ~static_cast<int64_t>(15);
-                    tma_load_2d(dst0 + lane * L::BOXP, &tmap, static_cast<int>(xb / 2),
+                    tma_load_2d(dst0 + lane * L::BOXP, &g.map[it.m], static_cast<int>(xb / 2),
                                 static_cast<int>(it.tile * 16), bar);
                 }
                 if (ce > cs)
@@ -822,8 +829,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         grid_dependency_wait();  // the activations come from the previous kernel
         uint32_t sc = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-            const TcItem it = tc_item(a, item);
+        for (int64_t item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+            const TcItem it = tc_item(g, item);
+            const TcmvArgs& a = g.m[it.m];
             for (int64_t s = it.s0; s < it.s1; ++s, ++sc) {
                 const uint32_t slot = sc % NX;
                 if (sc >= static_cast<uint32_t>(NX) &&
@@ -849,8 +857,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             uint32_t sc = 0;  // stages walked
             bool ok = true;
-            for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-                const TcItem it = tc_item(a, item);
+            for (int64_t item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+                const TcItem it = tc_item(g, item);
+                const TcmvArgs& a = g.m[it.m];
                 for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
                     const uint32_t set = sc & 1u;
                     if (set != myset) continue;
@@ -930,8 +939,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
         uint32_t sc = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-            const TcItem it = tc_item(a, item);
+        for (int64_t item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+            const TcItem it = tc_item(g, item);
+            const TcmvArgs& a = g.m[it.m];
             for (int64_t s = it.s0; ok && s < it.s1; ++s, ++sc) {
                 if ((sc & 1u) != myset) continue;
                 const uint32_t slot = sc % NR, sslot = sc % NSC;
@@ -991,8 +1001,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         grid_dependency_wait();  // y, the partial sums and the activation scales
         uint32_t sc = 0;
         bool ok = true;
-        for (int64_t item = blockIdx.x; ok && item < a.items; item += gridDim.x) {
-            const TcItem it = tc_item(a, item);
+        for (int64_t item = blockIdx.x; ok && item < g.items; item += gridDim.x) {
+            const TcItem it = tc_item(g, item);
+            const TcmvArgs& a = g.m[it.m];
             const int64_t n = it.tile * 128 + r;
             float acc[NB];
 #pragma unroll

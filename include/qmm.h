@@ -135,6 +135,25 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
 int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
              int64_t K, int B);
 
+/* Several decode matvecs in one launch: y[i] = W[i] x[i] for i < n <= 12,
+ * each exactly as qmm_gemv(fmt, W[i], x[i], y[i], N[i], K[i], B) computes
+ * it (the same format, activation type, mode and batch B for all). W, x, y,
+ * N, K are host arrays of n entries; the pointers they hold are device
+ * pointers with qmm_gemv's layouts and alignment. The launch walks the
+ * 128-row tiles of all n matrices, so a short matrix does not leave the GPU
+ * idle behind it (the 7B-shaped decode set runs as one call per format and
+ * batch). Errors and workspace as qmm_gemv; the workspace size comes from
+ * qmm_gemv_group_workspace_bytes. The split of K may differ from the single
+ * call's, so results agree with qmm_gemv within the float bound, not
+ * bitwise. */
+int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const* x,
+                   float* const* y, const int64_t* N, const int64_t* K, int B);
+
+/* Workspace that qmm_gemv_group needs for these shapes; 0 if none or if the
+ * arguments are invalid. */
+size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, const int64_t* K,
+                                      int B);
+
 /* Size of the fixed scratch array that qmm_gemv_noalloc uses (4 MiB). */
 #define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -114,3 +114,19 @@ def _gate_in_fresh_process(env_value):
 def test_plane_gate_default_on_zero_opts_out(L, value, expect):
     """unset means on; only an explicit "0" opts out; K % 256 gates it too"""
     assert _gate_in_fresh_process(value) == expect
+
+
+def test_gemv_group_argument_errors(L):
+    P = C.c_void_p * 1
+    I64 = C.c_int64 * 1
+    W, x, y = P(FAKE), P(FAKE), P(FAKE)
+    N, K = I64(64), I64(256)
+    fn = L.lib.qmm_gemv_group
+    assert _rc(L, "qmm_gemv_group", 0x03, 0, W, x, y, N, K, 1)[0] == -1    # n = 0
+    assert _rc(L, "qmm_gemv_group", 0x03, 13, W, x, y, N, K, 1)[0] == -1   # n above 12
+    assert _rc(L, "qmm_gemv_group", 0x03, 1, None, x, y, N, K, 1)[0] == -1  # null array
+    assert _rc(L, "qmm_gemv_group", 0x03, 1, W, x, y, I64(0), K, 1)[0] == -1  # N = 0
+    assert _rc(L, "qmm_gemv_group", 0x03, 1, W, x, y, N, I64(100), 1)[0] == -3  # K not a block multiple
+    assert _rc(L, "qmm_gemv_group", 0x03, 1, W, x, y, N, K, 17)[0] == -1   # B above 16
+    assert fn is not None
+    assert L.lib.qmm_gemv_group_workspace_bytes(0x03, 0, N, K, 1) == 0

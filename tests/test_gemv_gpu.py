@@ -222,3 +222,35 @@ def test_missing_workspace_is_an_error():
     qmm.lib.qmm_set_workspace(None, 0)
     rc = qmm.lib.qmm_gemv(qmm.Q6_K | qmm.ACT_Q8, qmm._ptr(Wt), qmm._ptr(xt), qmm._ptr(y), N, K, 1)
     assert rc == qmm.ENOWORKSPACE
+
+
+GROUP_SHAPES = {  # ragged rows, several K, more than one 128-row tile
+    "q6_K": [(37, 256 * 3), (300, 256 * 5), (129, 256 * 16), (8, 256)],
+    "Q4_0": [(53, 32 * 7), (260, 32 * 40), (128, 32 * 128)],
+    "Q8_0": [(29, 32 * 9), (200, 32 * 64)],
+}
+
+
+@pytest.mark.parametrize("name", ["q6_K", "Q4_0", "Q8_0"])
+@pytest.mark.parametrize("B", [1, 3, 8, 16])
+@pytest.mark.parametrize("xdt,act", [("bf16", "float"), ("f32", "float"), ("bf16", "q8")])
+def test_gemv_group_matches_oracle(name, B, xdt, act):
+    fmt = FMTS[name]
+    shapes = GROUP_SHAPES[name]
+    Ws = [synth.matrix(fmt, 300 + i, N, K) for i, (N, K) in enumerate(shapes)]
+    mk = synth.normal_bf16 if xdt == "bf16" else synth.normal_f32
+    xs = [mk(400 + i, (B, K)) for i, (N, K) in enumerate(shapes)]
+    ys = [torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda") for N, K in shapes]
+    mode = qmm.ACT_Q8 if act == "q8" else qmm.ACT_FLOAT
+    grp = qmm.GemvGroup(fmt, [dev(W) for W in Ws], [x_tensor(x) for x in xs], ys,
+                        [N for N, K in shapes], [K for N, K in shapes], mode)
+    qmm.gemv_group(grp)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    for (N, K), W, x, y in zip(shapes, Ws, xs, ys):
+        if act == "q8":
+            xq, s = oracle.quantize_q8(x)
+            ref, absum = oracle.gemv_q8(fmt, W, xq, s, N, K)
+        else:
+            ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+        assert_within(y.cpu().numpy(), ref, absum, f"group {name} {N}x{K} B={B} {xdt} {act}")
