@@ -91,10 +91,10 @@ uint32_t tcmv_smem_q6k(int NB, int S);
 uint32_t tcmv_smem_q4_0(int NB, int S);
 uint32_t tcmv_smem_q8_0(int NB, int S);
 
-// MMA columns for NB activation rows split S ways (16, 32 or 48)
+// MMA columns for NB activation rows split S ways (the matvec's NCOL)
 inline int tcmv_ncol(int NB, int S) {
     const int nc = NB * S;
-    return nc <= 16 ? 16 : (nc <= 32 ? 32 : 48);
+    return (nc >= 6 && nc <= 8) ? 64 : (nc >= 4 && nc <= 5) ? 32 : (nc <= 16 ? 16 : (nc <= 32 ? 32 : 48));
 }
 inline int tcmv_stage_blocks(int fmt) { return fmt == FMT_Q6_K ? 1 : 8; }
 // resident CTAs per SM of the (fmt, q8, NB, S) kernel (0 if not built)

@@ -88,7 +88,13 @@ static_assert(210 + 28 <= 240 && 8 * 18 + 28 <= 176 && 8 * 34 + 28 <= 304, "row 
 template <int NB, int S>
 struct TcCols {
     static constexpr int NC = NB * S;  // activation columns in use
-    static constexpr int NCOL = NC <= 16 ? 16 : (NC <= 32 ? 32 : 48);  // MMA N
+    // MMA N: wider than a group needs when a group takes 4 to 8 columns (32
+    // for 4-5, 64 for 6-8), so that a D window collects several groups and a
+    // stage needs few windows (fewer drains); else the smallest of 16, 32, 48
+    // that holds a group
+    static constexpr int NCOL = (NC >= 6 && NC <= 8) ? 64
+                              : (NC >= 4 && NC <= 5) ? 32
+                              : (NC <= 16 ? 16 : (NC <= 32 ? 32 : 48));
 };
 
 template <int FMT, int NB, int S>
@@ -538,7 +544,10 @@ __device__ __forceinline__ float lds_f32(uint32_t a) {
 // to acc[b] for every group i of the window and every activation row b.
 template <int NCOL>
 __device__ __forceinline__ void tc_ld_window(uint32_t taddr, uint32_t (&v)[NCOL]) {
-    if constexpr (NCOL == 48) {
+    if constexpr (NCOL == 64) {
+        tc::ld<32>(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tc::ld<32>(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+    } else if constexpr (NCOL == 48) {
         tc::ld<32>(taddr, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tc::ld<16>(taddr + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
     } else {
