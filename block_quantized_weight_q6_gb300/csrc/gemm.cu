@@ -52,24 +52,25 @@ namespace {
 
 constexpr int BM = 128;           // tokens per tile (tensor-memory lanes)
 constexpr int BN = 128;           // weight rows per tile (accumulator columns)
-constexpr int NS = 4;             // B stages (one 32-wide K block each)
-constexpr int NA = 8;             // A stages: the activation copies run up to NA blocks ahead
+constexpr int KP = 2;             // K blocks (32 wide) per stage: one handoff per pair of blocks
+constexpr int NS = 3;             // stages, each the A and B tiles of KP blocks
 constexpr int kScMax = 56;        // largest |q6_K sub-block scale| the fp16 B tile holds exactly
 constexpr int NR = 3;             // raw weight stages (256 columns each)
-constexpr int NBUF = 3;           // accumulator buffers in tensor memory
+constexpr int NBUF = 4;           // accumulator buffers in tensor memory, used in pairs
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
 constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
 constexpr int kThreads = 480;                // 15 warps: 128 registers a thread
 constexpr int kRawWarp = 14;                // raw weight producer
 constexpr int kConv0 = 2, kConvWarps = 4;   // converter warps
 constexpr int kEpi0 = 6;                    // epilogue warps kEpi0 .. kEpi0 + 7
-constexpr int kTmemCols = 512;    // NBUF * BN accumulators + BN for y
+constexpr int kTmemCols = 512;    // NBUF * BN accumulators
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
 // B stage: 16 groups of 8 weight rows, kBSbo bytes apart (a 16-byte odd
 // multiple past 512, so that 8 lanes storing one row each of 8 different
 // groups hit 8 different bank groups); core matrices 128 bytes apart along K
 constexpr int kBSbo = 528;
-constexpr int kBTile = 16 * kBSbo;    // bytes of one B stage
+constexpr int kBTile = 16 * kBSbo;    // bytes of one block's B tile
+constexpr int kAStage = KP * kATile, kBStage = KP * kBTile;
 
 // raw stage row strides (16-byte multiples with room for the lead-in)
 constexpr int kRawQ6K = 240;      // one 210-byte super-block
@@ -97,9 +98,9 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     const uint32_t dr = fmt == FMT_Q6_K ? DR_Q6K : DR_Q40;
     uint32_t o = 0;
     L.a = o;
-    o += NA * kATile;
+    o += NS * kAStage;
     L.b = o;
-    o += NS * kBTile;
+    o += NS * kBStage;
     L.raw = o;
     L.rawslot = raw_slot_bytes(static_cast<int>(rs), exp);
     o += NR * L.rawslot;
@@ -107,7 +108,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     o += dr * BN * 4;
     o = align_up(o, 8);
     L.bars = o;
-    o += 8 * (2 * NA + 2 * NS + 2 * NR + 2 * NBUF + dr);
+    o += 8 * (2 * NS + 2 * NR + 2 * (NBUF / KP) + dr);
     L.tslot = o;
     o += 4;
     L.abort_flag = o;
@@ -116,24 +117,20 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     return L;
 }
 
-// barrier indices: a_full[NA], a_empty[NA], b_full[NS], b_empty[NS],
-// raw_full[NR], raw_empty[NR], acc_full[NBUF], acc_empty[NBUF], dv_full[DR]
-__device__ __forceinline__ uint32_t bar_a_full(uint32_t B, int s) { return B + 8 * s; }
-__device__ __forceinline__ uint32_t bar_a_empty(uint32_t B, int s) { return B + 8 * (NA + s); }
-__device__ __forceinline__ uint32_t bar_b_full(uint32_t B, int s) { return B + 8 * (2 * NA + s); }
-__device__ __forceinline__ uint32_t bar_stage_empty(uint32_t B, int s) { return B + 8 * (2 * NA + NS + s); }
-__device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (2 * NA + 2 * NS + r); }
-__device__ __forceinline__ uint32_t bar_raw_empty(uint32_t B, int r) {
-    return B + 8 * (2 * NA + 2 * NS + NR + r);
-}
-__device__ __forceinline__ uint32_t bar_acc_full(uint32_t B, int i) {
-    return B + 8 * (2 * NA + 2 * NS + 2 * NR + i);
-}
+// barrier indices: full[NS] (the A copy's bytes and the converters),
+// empty[NS], raw_full[NR], raw_empty[NR], acc_full[2], acc_empty[2] (pairs of
+// accumulator buffers), dv_full[DR]
+constexpr int NP = NBUF / KP;  // accumulator pairs
+__device__ __forceinline__ uint32_t bar_full(uint32_t B, int s) { return B + 8 * s; }
+__device__ __forceinline__ uint32_t bar_empty(uint32_t B, int s) { return B + 8 * (NS + s); }
+__device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (2 * NS + r); }
+__device__ __forceinline__ uint32_t bar_raw_empty(uint32_t B, int r) { return B + 8 * (2 * NS + NR + r); }
+__device__ __forceinline__ uint32_t bar_acc_full(uint32_t B, int i) { return B + 8 * (2 * NS + 2 * NR + i); }
 __device__ __forceinline__ uint32_t bar_acc_empty(uint32_t B, int i) {
-    return B + 8 * (2 * NA + 2 * NS + 2 * NR + NBUF + i);
+    return B + 8 * (2 * NS + 2 * NR + NP + i);
 }
 __device__ __forceinline__ uint32_t bar_dv_full(uint32_t B, int i) {
-    return B + 8 * (2 * NA + 2 * NS + 2 * NR + 2 * NBUF + i);
+    return B + 8 * (2 * NS + 2 * NR + 2 * NP + i);
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -194,34 +191,9 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-        "%14,%15,%16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
-}
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- trace
 // Diagnostic builds define QMM_GEMM_TRACE and point qmm_gemm_trace at mapped
@@ -377,19 +349,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_launch_dependents();
     live_bump(a.st, a.live_slot);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NA; ++s) {
-            mbar_init(bar_a_full(BARS, s), 1);
-            mbar_init(bar_a_empty(BARS, s), 1);  // the MMA commit
-        }
         for (int s = 0; s < NS; ++s) {
-            mbar_init(bar_b_full(BARS, s), kConvWarps);
-            mbar_init(bar_stage_empty(BARS, s), 1);  // the MMA commit
+            mbar_init(bar_full(BARS, s), 1 + kConvWarps);  // the A copy (with its bytes) and the converters
+            mbar_init(bar_empty(BARS, s), 1);              // the MMA commit
         }
         for (int r = 0; r < NR; ++r) {
             mbar_init(bar_raw_full(BARS, r), 1);
             mbar_init(bar_raw_empty(BARS, r), kConvWarps);
         }
-        for (int i = 0; i < NBUF; ++i) {
+        for (int i = 0; i < NP; ++i) {
             mbar_init(bar_acc_full(BARS, i), 1);
             mbar_init(bar_acc_empty(BARS, i), 8);  // the epilogue warps
         }
@@ -500,17 +468,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t sc = nsc > NR ? nsc - NR : 0; sc < nsc; ++sc)
                 (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(sc % NR)), (sc / NR) & 1, FLAG, a.st.err);
         } else {
-            for (int64_t kb = 0; kb < nkb; ++kb) {
-                QMM_TRACE(2, kb);
-                const int sa = static_cast<int>(kb % NA);
-                if (kb >= NA &&
-                    !wait_or_abort(bar_a_empty(BARS, sa), ((kb / NA) - 1) & 1, FLAG, a.st.err))
+            for (int64_t q = 0; q * KP < nkb; ++q) {
+                // the A tiles of blocks KP q .. (consecutive in the pre-tiled operand)
+                const int64_t kb0 = q * KP;
+                const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
+                const int st = static_cast<int>(q % NS);
+                QMM_TRACE(2, kb0);
+                if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err))
                     break;
-                QMM_TRACE(3, kb);
+                QMM_TRACE(3, kb0);
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(bar_a_full(BARS, sa), kATile);
-                    bulk_g2s(S + L.a + sa * kATile, a.a16 + (mt * nkb + kb) * (BM * 32), kATile,
-                             bar_a_full(BARS, sa));
+                    mbar_arrive_expect_tx(bar_full(BARS, st), nbk * kATile);
+                    bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kb0) * (BM * 32), nbk * kATile,
+                             bar_full(BARS, st));
                 }
                 __syncwarp();
             }
@@ -518,36 +488,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc = idesc_f16(BM, BN);
-        for (int64_t kb = 0; kb < nkb; ++kb) {
-            const int s = static_cast<int>(kb % NS);
-            const int sa = static_cast<int>(kb % NA);
-            const int ab = static_cast<int>(kb % NBUF);
-            QMM_TRACE(10, kb);
-            if (!wait_or_abort(bar_a_full(BARS, sa), (kb / NA) & 1, FLAG, a.st.err)) break;
-            QMM_TRACE(11, kb);
-            if (!wait_or_abort(bar_b_full(BARS, s), (kb / NS) & 1, FLAG, a.st.err)) break;
-            QMM_TRACE(12, kb);
-            if (kb >= NBUF &&
-                !wait_or_abort(bar_acc_empty(BARS, ab), ((kb / NBUF) - 1) & 1, FLAG, a.st.err))
+        for (int64_t q = 0; q * KP < nkb; ++q) {
+            const int64_t kb0 = q * KP;
+            const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
+            const int st = static_cast<int>(q % NS);
+            const int pr = static_cast<int>(q % NP);
+            QMM_TRACE(10, kb0);
+            if (!wait_or_abort(bar_full(BARS, st), (q / NS) & 1, FLAG, a.st.err)) break;
+            QMM_TRACE(12, kb0);
+            if (q >= NP && !wait_or_abort(bar_acc_empty(BARS, pr), ((q / NP) - 1) & 1, FLAG, a.st.err))
                 break;
-            QMM_TRACE(13, kb);
+            QMM_TRACE(13, kb0);
             tc_fence_after();
             if (lane == 0) {
-                const uint64_t ad = smem_desc(S + L.a + sa * kATile);
-                const uint64_t bd = smem_desc(S + L.b + s * kBTile, kBSbo);
-                const uint32_t d = tmem + static_cast<uint32_t>(ab * BN);
-                tc_mma(d, ad, bd, idesc, 0u);
-                tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
-                tc_commit(bar_stage_empty(BARS, s));
-                tc_commit(bar_a_empty(BARS, sa));
-                tc_commit(bar_acc_full(BARS, ab));
+                for (int bi = 0; bi < nbk; ++bi) {
+                    const uint64_t ad = smem_desc(S + L.a + st * kAStage + bi * kATile);
+                    const uint64_t bd = smem_desc(S + L.b + st * kBStage + bi * kBTile, kBSbo);
+                    const uint32_t d = tmem + static_cast<uint32_t>((KP * pr + bi) * BN);
+                    tc_mma(d, ad, bd, idesc, 0u);
+                    tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
+                }
+                tc_commit(bar_empty(BARS, st));
+                tc_commit(bar_acc_full(BARS, pr));
             }
             __syncwarp();
         }
     } else if (warp < kEpi0) {
         // ------------------------------------------------------------ converters
-        // Two K blocks (one B stage each) per pass: one wait for both stages,
-        // one proxy fence and one arrival per stage. Warp cw converts the rows
+        // One stage (two K blocks) per pass: one wait, one proxy fence and one
+        // arrival. Warp cw converts the rows
         // 8 g + j of the tile for j = 2 cw, 2 cw + 1: lane (g = lane % 16,
         // h = lane / 16) the 16 columns 16 h .. 16 h + 15 of each block. A
         // row's offset inside its raw slot depends only on j, so the
@@ -596,20 +565,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(bar_dv_full(BARS, di));
                 }
             }
-            bool ok = true;
-            for (int bi = 0; bi < nbk; ++bi) {
-                const int64_t kb = kb0 + bi;
-                if (kb >= NS &&
-                    !wait_or_abort(bar_stage_empty(BARS, static_cast<int>(kb % NS)), ((kb / NS) - 1) & 1, FLAG,
-                                   a.st.err))
-                    ok = false;
-            }
-            if (!ok) break;
+            static_assert(KP == 2, "a converter pass is one stage of two blocks");
+            const int64_t q = kb0 / KP;
+            const int st = static_cast<int>(q % NS);
+            if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(22, kb0);
 #pragma unroll 1
             for (int u = 0; u < 2 * nbk; ++u) {
                 const int bi = u >> 1, j = 2 * cw + (u & 1);
-                const int64_t kb = kb0 + bi;
                 const int n = 8 * g + j;
                 const int64_t ng = n0 + n;
                 const int e = 32 * (j0 + bi) + 16 * hh;  // this lane's first column within the chunk
@@ -669,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // row n: group g, row j of the group; columns 16 hh .. + 15 are
                 // the K octets 2 hh and 2 hh + 1
-                const uint32_t bt = S + L.b + static_cast<uint32_t>(kb % NS) * kBTile + g * kBSbo + j * 16;
+                const uint32_t bt = S + L.b + static_cast<uint32_t>(st) * kBStage + static_cast<uint32_t>(bi) * kBTile +
+                                    g * kBSbo + j * 16;
                 asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh) * 128),
                              "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
                              : "memory");
@@ -679,8 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0)
-                for (int bi = 0; bi < nbk; ++bi) mbar_arrive(bar_b_full(BARS, static_cast<int>((kb0 + bi) % NS)));
+            if (lane == 0) mbar_arrive(bar_full(BARS, st));
             if (j0 + nbk == 8 || kb0 + nbk == nkb) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
@@ -689,108 +652,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue
+        // Per K block b: y += (d * s_x[m][b]) * I_b, with y (64 columns of this
+        // thread's token row) in registers; d per 256 columns (q6_K) or per
+        // block (Q4_0) comes from the converters through shared memory. The
+        // accumulators of one stage (two blocks) are released together.
         const int quad = warp & 3;           // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
         const int h = (warp - kEpi0) >> 2;   // columns 64*h .. +63 of the tile
         const int64_t m = mt * BM + 32 * quad + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-        // q6_K: z (this super-block's s_x-weighted sums) in registers, the
-        // running output y in tensor memory after the accumulator buffers;
-        // Q4_0: y in registers (d changes every block)
-        const uint32_t ty = tl + NBUF * BN + 64 * h;
-        float z[64];
+        float y[64];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) z[c] = 0.0f;
+        for (int c = 0; c < 64; ++c) y[c] = 0.0f;
         bool ok = true;
-        for (int64_t kb = 0; kb < nkb; ++kb) {
-            const int ab = static_cast<int>(kb % NBUF);
-            QMM_TRACE(30, kb);
-            if (!wait_or_abort(bar_acc_full(BARS, ab), (kb / NBUF) & 1, FLAG, a.st.err)) {
+        for (int64_t q = 0; ok && q * KP < nkb; ++q) {
+            const int64_t kb0 = q * KP;
+            const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
+            const int pr = static_cast<int>(q % NP);
+            QMM_TRACE(30, kb0);
+            if (!wait_or_abort(bar_acc_full(BARS, pr), (q / NP) & 1, FLAG, a.st.err)) {
                 ok = false;
                 break;
             }
-            QMM_TRACE(31, kb);
+            QMM_TRACE(31, kb0);
             tc_fence_after();
-            const float sx = (m < a.M) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
-            const float2 s2 = make_float2(sx, sx);
-            float v[32];
-            if (Q6) {
-                // z += s_x * I, one 32-column half at a time (fewer registers)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    tc_ld32(tl + ab * BN + 64 * h + 32 * half, v);
-                    tc_wait_ld();
-                    if (half == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
-                    }
-                    if (a.dbg != nullptr && kb == 0 && m < a.M) {
-                        for (int c = 0; c < 32; ++c)
-                            if (n0 + 64 * h + 32 * half + c < a.N)
-                                a.dbg[m * a.N + n0 + 64 * h + 32 * half + c] = v[c];
-                    }
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2,
-                                               make_float2(z[32 * half + c], z[32 * half + c + 1]));
-                        z[32 * half + c] = t.x;
-                        z[32 * half + c + 1] = t.y;
-                    }
-                }
-                QMM_TRACE(32, kb);
-                if ((kb & 7) == 7 || kb == nkb - 1) {
-                    const int64_t sb = kb >> 3;
-                    const int di = static_cast<int>(sb % DR);
-                    QMM_TRACE(33, kb);
-                    if (!wait_or_abort(bar_dv_full(BARS, di), (sb / DR) & 1, FLAG, a.st.err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dv = S + L.dv + (di * BN + 64 * h) * 4;
-                    // y += d * z, 16 columns at a time (z is live throughout)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float yv[16];
-                        if (sb > 0) {
-                            tc_ld16(ty + 16 * q, yv);
-                            tc_wait_ld();
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) yv[c] = 0.0f;
-                        }
-#pragma unroll
-                        for (int c = 0; c < 16; c += 2) {
-                            float2 d2;
-                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                                         : "=f"(d2.x), "=f"(d2.y)
-                                         : "r"(dv + 4 * (16 * q + c)));
-                            const float2 t = ffma2(d2, make_float2(z[16 * q + c], z[16 * q + c + 1]),
-                                                   make_float2(yv[c], yv[c + 1]));
-                            yv[c] = t.x;
-                            yv[c + 1] = t.y;
-                            z[16 * q + c] = 0.0f;
-                            z[16 * q + c + 1] = 0.0f;
-                        }
-                        tc_st16(ty + 16 * q, yv);
-                    }
-                    tc_wait_st();
-                    QMM_TRACE(34, kb);
-                }
-            } else {
-                const int di = static_cast<int>(kb % DR);
-                if (!wait_or_abort(bar_dv_full(BARS, di), (kb / DR) & 1, FLAG, a.st.err)) {
+            for (int bi = 0; bi < nbk; ++bi) {
+                const int64_t kb = kb0 + bi;
+                const float sx = (m < a.M) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
+                const float2 s2 = make_float2(sx, sx);
+                // this block's d (q6_K: its super-block's, Q4_0: its own)
+                const int64_t dk = Q6 ? (kb >> 3) : kb;
+                const int di = static_cast<int>(dk % DR);
+                if ((Q6 ? (kb & 7) == 0 : true) &&
+                    !wait_or_abort(bar_dv_full(BARS, di), (dk / DR) & 1, FLAG, a.st.err)) {
                     ok = false;
                     break;
                 }
+                const uint32_t acc = tl + static_cast<uint32_t>((KP * pr + bi) * BN) + 64 * h;
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    tc_ld32(tl + ab * BN + 64 * h + 32 * half, v);
+                    float v[32];
+                    tc_ld32(acc + 32 * half, v);
                     tc_wait_ld();
-                    if (half == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar_acc_empty(BARS, ab));
-                    }
                     if (a.dbg != nullptr && kb == 0 && m < a.M) {
                         for (int c = 0; c < 32; ++c)
                             if (n0 + 64 * h + 32 * half + c < a.N)
@@ -802,40 +704,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float2 d2;
                         asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
                         const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
-                                               make_float2(z[32 * half + c], z[32 * half + c + 1]));
-                        z[32 * half + c] = t.x;  // Q4_0: z holds y
-                        z[32 * half + c + 1] = t.y;
+                                               make_float2(y[32 * half + c], y[32 * half + c + 1]));
+                        y[32 * half + c] = t.x;
+                        y[32 * half + c + 1] = t.y;
                     }
                 }
             }
+            if (!ok) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, pr));
+            QMM_TRACE(32, kb0);
         }
-        // ok is warp-uniform, so the whole warp takes this branch: the tensor
-        // memory loads are warp-collective and run for every lane; only the
-        // stores depend on the lane's row
-        if (ok) {
+        if (ok && m < a.M) {
             const int64_t nb0 = n0 + 64 * h;
             float* out = a.Y + m * a.N + nb0;
+            if (nb0 + 64 <= a.N && (a.N & 3) == 0) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float yv[32];
-                if (Q6) {
-                    tc_ld32(ty + 32 * half, yv);
-                    tc_wait_ld();
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) yv[c] = z[32 * half + c];
-                }
-                if (m >= a.M) continue;
-                const int64_t c0 = nb0 + 32 * half;
-                if (c0 + 32 <= a.N && (a.N & 3) == 0) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4*>(out + 32 * half + c) =
-                            make_float4(yv[c], yv[c + 1], yv[c + 2], yv[c + 3]);
-                } else {
-                    for (int c = 0; c < 32; ++c)
-                        if (c0 + c < a.N) out[32 * half + c] = yv[c];
-                }
+                for (int c = 0; c < 64; c += 4)
+                    *reinterpret_cast<float4*>(out + c) = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
+            } else {
+                for (int c = 0; c < 64; ++c)
+                    if (nb0 + c < a.N) out[c] = y[c];
             }
         }
     }
