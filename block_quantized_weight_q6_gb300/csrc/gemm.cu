@@ -54,6 +54,7 @@ constexpr int BM = 128;           // tokens per tile (tensor-memory lanes)
 constexpr int BN = 128;           // weight rows per tile (accumulator columns)
 constexpr int KP = 2;             // K blocks (32 wide) per stage: one handoff per pair of blocks
 constexpr int NS = 3;             // stages, each the A and B tiles of KP blocks
+constexpr int kPrefetch = 8;      // stages of A tiles prefetched into L2 ahead of their copy
 constexpr int kScMax = 56;        // largest |q6_K sub-block scale| the fp16 B tile holds exactly
 constexpr int NR = 3;             // raw weight stages (256 columns each)
 constexpr int NBUF = 4;           // accumulator buffers in tensor memory, used in pairs
@@ -283,6 +284,11 @@ __device__ __forceinline__ uint32_t half2_bits(float x) {
     return h | (h << 16);
 }
 
+// Bulk prefetch of global memory into L2 (bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // The 16 bytes at base + 4 * QW + sh / 8 (base 16-byte aligned, sh 0, 8, 16
 // or 24) as 4 words: two 16-byte loads and a funnel shift per word.
 template <int QW>
@@ -478,6 +484,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 QMM_TRACE(3, kb0);
                 if (lane == 0) {
+                    // pull the tiles kPrefetch stages ahead into L2 first: the
+                    // copy into shared memory then waits on L2, not on DRAM
+                    const int64_t pk = kb0 + kPrefetch * KP;
+                    if (q == 0)
+                        for (int64_t k = 0; k < pk && k < nkb; k += KP)
+                            prefetch_l2(a.a16 + (mt * nkb + k) * (BM * 32),
+                                        (nkb - k < KP ? static_cast<uint32_t>(nkb - k) : KP) * kATile);
+                    if (pk < nkb)
+                        prefetch_l2(a.a16 + (mt * nkb + pk) * (BM * 32),
+                                    (nkb - pk < KP ? static_cast<uint32_t>(nkb - pk) : KP) * kATile);
                     mbar_arrive_expect_tx(bar_full(BARS, st), nbk * kATile);
                     bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kb0) * (BM * 32), nbk * kATile,
                              bar_full(BARS, st));
