@@ -289,31 +289,50 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// The 16 bytes at base + 4 * QW + sh / 8 (base 16-byte aligned, sh 0, 8, 16
-// or 24) as 4 words: two 16-byte loads and a funnel shift per word.
-template <int QW>
-__device__ __forceinline__ void run16(uint32_t base, uint32_t sh, uint32_t (&o)[4]) {
-    uint32_t w[8];
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t* w) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                 : "r"(base));
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                 : "r"(base + 16));
+                 : "r"(addr));
+}
+
+// The 16 bytes at byte offset QW * 4 + sh / 8 of the 32 bytes w (sh 0, 8,
+// 16 or 24): a funnel shift per word.
+template <int QW>
+__device__ __forceinline__ void pick16_at(const uint32_t (&w)[8], uint32_t sh, uint32_t (&o)[4]) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) o[k] = __funnelshift_r(w[QW + k], w[QW + k + 1], sh);
 }
 
-// The same with the word offset QW a runtime value that is uniform across
-// the warp (a branch, not a per-lane selection).
-__device__ __forceinline__ void run16_u(uint32_t addr, uint32_t (&o)[4]) {
-    const uint32_t base = addr & ~15u, sh = (addr & 3u) * 8u;
-    switch ((addr >> 2) & 3u) {
-        case 0: run16<0>(base, sh, o); break;
-        case 1: run16<1>(base, sh, o); break;
-        case 2: run16<2>(base, sh, o); break;
-        default: run16<3>(base, sh, o); break;
+// The 16 bytes at byte offset off (0..15, the same in every lane of the
+// warp) of the 32 bytes w: a warp-uniform branch on the word offset.
+__device__ __forceinline__ void pick16(const uint32_t (&w)[8], uint32_t off, uint32_t (&o)[4]) {
+    const uint32_t sh = (off & 3u) * 8u;
+    switch (off >> 2) {
+        case 0: pick16_at<0>(w, sh, o); break;
+        case 1: pick16_at<1>(w, sh, o); break;
+        case 2: pick16_at<2>(w, sh, o); break;
+        default: pick16_at<3>(w, sh, o); break;
     }
+}
+
+// pick16 of four 32-byte runs at one offset, under one branch
+__device__ __forceinline__ void pick16x4(const uint32_t (&w0)[8], const uint32_t (&w1)[8],
+                                         const uint32_t (&w2)[8], const uint32_t (&w3)[8], uint32_t off,
+                                         uint32_t (&o0)[4], uint32_t (&o1)[4], uint32_t (&o2)[4],
+                                         uint32_t (&o3)[4]) {
+    const uint32_t sh = (off & 3u) * 8u;
+#define QMM_PICK4(QW)                \
+    pick16_at<QW>(w0, sh, o0);      \
+    pick16_at<QW>(w1, sh, o1);      \
+    pick16_at<QW>(w2, sh, o2);      \
+    pick16_at<QW>(w3, sh, o3);
+    switch (off >> 2) {
+        case 0: QMM_PICK4(0) break;
+        case 1: QMM_PICK4(1) break;
+        case 2: QMM_PICK4(2) break;
+        default: QMM_PICK4(3) break;
+    }
+#undef QMM_PICK4
 }
 
 }  // namespace
@@ -332,7 +351,6 @@ struct GemmArgs {
     int64_t n8;            // rows of W reached through the tensor map: 8 * floor(N / 8)
     DevState st;
     int live_slot;
-    float* dbg;            // optional [M][N]: the raw accumulator of the first K block
 };
 
 template <int FMT, bool EXP>
@@ -586,76 +604,127 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = static_cast<int>(q % NS);
             if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(22, kb0);
+            // Rows 8 g + j of the tile, j = 2 cw and 2 cw + 1: per row, the raw
+            // bytes of both blocks of the stage are loaded first, then realigned
+            // by the row's lead (warp-uniform), expanded and stored.
 #pragma unroll 1
-            for (int u = 0; u < 2 * nbk; ++u) {
-                const int bi = u >> 1, j = 2 * cw + (u & 1);
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * cw + jj;
                 const int n = 8 * g + j;
                 const int64_t ng = n0 + n;
-                const int e = 32 * (j0 + bi) + 16 * hh;  // this lane's first column within the chunk
-                uint32_t hv[8];
-                if (ng < a.N) {
-                    // warp-uniform: the lead of rows 8 g + j (whole groups, or the tail rows)
-                    const uint32_t rb = rowaddr(n) + lead(ng);
-                    if (Q6) {
-                        uint32_t c[4];
-                        int scv;
-                        if (EXP) {
-                            const uint32_t pb = rowaddr(n) + e;  // 16-byte aligned plane bytes
-                            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                                         : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
-                                         : "r"(pb));
-                            scv = lds_s8(rowaddr(n) + 256 + lead(ng) + (e >> 4));
+                const bool live = ng < a.N;
+                const uint32_t rb = rowaddr(n) + lead(ng);  // lead: warp-uniform
+                uint32_t hv[KP][8];
+                if (Q6) {
+                    uint32_t c[KP][4];
+                    int scv[KP];
+                    if (EXP) {
 #pragma unroll
-                            for (int w = 0; w < 4; ++w) c[w] ^= 0x80808080u;
-                        } else {
-                            uint32_t ql[4], qh[4];
-                            run16_u(rb + (e & 127), ql);
-                            run16_u(rb + 128 + (e & 63), qh);
-                            scv = lds_s8(rb + 192 + (e >> 4));
+                        for (int bi = 0; bi < KP; ++bi) {
+                            const int e = 32 * (j0 + bi) + 16 * hh;
+                            if (live && bi < nbk) {
+                                lds_v4(rowaddr(n) + e, c[bi]);  // 16-byte aligned plane bytes
+                                scv[bi] = lds_s8(rb + 256 + (e >> 4));
+                            } else {
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) c[bi][w] = 0x80808080u;
+                                scv[bi] = 0;
+                            }
+                        }
+#pragma unroll
+                        for (int bi = 0; bi < KP; ++bi)
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) c[bi][w] ^= 0x80808080u;
+                    } else {
+                        uint32_t wl[KP][8], wh[KP][8];
+                        const uint32_t ab = rb & ~15u;
+#pragma unroll
+                        for (int bi = 0; bi < KP; ++bi) {
+                            const int e = 32 * (j0 + bi) + 16 * hh;
+                            if (live && bi < nbk) {
+                                lds_v4(ab + (e & 127), wl[bi]);
+                                lds_v4(ab + (e & 127) + 16, wl[bi] + 4);
+                                lds_v4(ab + 128 + (e & 63), wh[bi]);
+                                lds_v4(ab + 128 + (e & 63) + 16, wh[bi] + 4);
+                                scv[bi] = lds_s8(rb + 192 + (e >> 4));
+                            } else {
+#pragma unroll
+                                for (int w = 0; w < 8; ++w) wl[bi][w] = wh[bi][w] = 0u;
+                                scv[bi] = 0;
+                            }
+                        }
+                        uint32_t ql[KP][4], qh[KP][4];
+                        pick16x4(wl[0], wl[1], wh[0], wh[1], rb & 15u, ql[0], ql[1], qh[0], qh[1]);
+#pragma unroll
+                        for (int bi = 0; bi < KP; ++bi) {
+                            const int e = 32 * (j0 + bi) + 16 * hh;
                             const uint32_t ns = 4u * static_cast<uint32_t>(e >> 7);
                             const uint32_t hs = 2u * static_cast<uint32_t>(e >> 6);
 #pragma unroll
                             for (int w = 0; w < 4; ++w)
-                                c[w] = ((ql[w] >> ns) & 0x0F0F0F0Fu) | (((qh[w] >> hs) & 0x03030303u) << 4);
+                                c[bi][w] = ((ql[bi][w] >> ns) & 0x0F0F0F0Fu) | (((qh[bi][w] >> hs) & 0x03030303u) << 4);
                         }
+                    }
+#pragma unroll
+                    for (int bi = 0; bi < KP; ++bi) {
                         // sc * (v - off) exactly: (off + v) * sc - off * sc, one rounding
-                        if (scv > kScMax || scv < -kScMax) scale_bad = true;
-                        const float scf = static_cast<float>(scv);
+                        if (scv[bi] > kScMax || scv[bi] < -kScMax) scale_bad = true;
+                        const float scf = static_cast<float>(scv[bi]);
                         const float off = EXP ? 1152.0f : 1056.0f;
                         const uint32_t sc2 = half2_bits(scf);
                         const uint32_t bias = half2_bits(-off * scf);
 #pragma unroll
                         for (int w = 0; w < 4; ++w) {
-                            hv[2 * w] = hfma2_u(half_pair_lo(c[w]), sc2, bias);
-                            hv[2 * w + 1] = hfma2_u(half_pair_hi(c[w]), sc2, bias);
-                        }
-                    } else {
-                        // Q4_0 block: nibble hh of the 16 qs bytes
-                        uint32_t q[4];
-                        run16_u(rb + 18 * (j0 + bi) + 2, q);
-                        const uint32_t ns = 4u * static_cast<uint32_t>(hh);
-                        const uint32_t one = 0x3C003C00u, bias = half2_bits(-1032.0f);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const uint32_t cq = (q[w] >> ns) & 0x0F0F0F0Fu;
-                            hv[2 * w] = hfma2_u(half_pair_lo(cq), one, bias);
-                            hv[2 * w + 1] = hfma2_u(half_pair_hi(cq), one, bias);
+                            hv[bi][2 * w] = hfma2_u(half_pair_lo(c[bi][w]), sc2, bias);
+                            hv[bi][2 * w + 1] = hfma2_u(half_pair_hi(c[bi][w]), sc2, bias);
                         }
                     }
                 } else {
+                    // Q4_0 block: nibble hh of the 16 qs bytes
+                    uint32_t wq[KP][8];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) hv[w] = 0u;
+                    for (int bi = 0; bi < KP; ++bi) {
+                        const uint32_t qa = rb + 18 * (j0 + bi) + 2;
+                        if (live && bi < nbk) {
+                            lds_v4(qa & ~15u, wq[bi]);
+                            lds_v4((qa & ~15u) + 16, wq[bi] + 4);
+                        } else {
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) wq[bi][w] = 0u;
+                        }
+                    }
+                    const uint32_t ns = 4u * static_cast<uint32_t>(hh);
+                    const uint32_t one = 0x3C003C00u, bias = half2_bits(-1032.0f);
+#pragma unroll
+                    for (int bi = 0; bi < KP; ++bi) {
+                        uint32_t q[4];
+                        pick16(wq[bi], (rb + 18 * (j0 + bi) + 2) & 15u, q);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const uint32_t cq = (q[w] >> ns) & 0x0F0F0F0Fu;
+                            hv[bi][2 * w] = hfma2_u(half_pair_lo(cq), one, bias);
+                            hv[bi][2 * w + 1] = hfma2_u(half_pair_hi(cq), one, bias);
+                        }
+                    }
                 }
                 // row n: group g, row j of the group; columns 16 hh .. + 15 are
                 // the K octets 2 hh and 2 hh + 1
-                const uint32_t bt = S + L.b + static_cast<uint32_t>(st) * kBStage + static_cast<uint32_t>(bi) * kBTile +
-                                    g * kBSbo + j * 16;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh) * 128),
-                             "r"(hv[0]), "r"(hv[1]), "r"(hv[2]), "r"(hv[3])
-                             : "memory");
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh + 1) * 128),
-                             "r"(hv[4]), "r"(hv[5]), "r"(hv[6]), "r"(hv[7])
-                             : "memory");
+#pragma unroll
+                for (int bi = 0; bi < KP; ++bi) {
+                    if (bi >= nbk) break;
+                    if (!live) {
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) hv[bi][w] = 0u;
+                    }
+                    const uint32_t bt = S + L.b + static_cast<uint32_t>(st) * kBStage +
+                                        static_cast<uint32_t>(bi) * kBTile + g * kBSbo + j * 16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh) * 128),
+                                 "r"(hv[bi][0]), "r"(hv[bi][1]), "r"(hv[bi][2]), "r"(hv[bi][3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh + 1) * 128),
+                                 "r"(hv[bi][4]), "r"(hv[bi][5]), "r"(hv[bi][6]), "r"(hv[bi][7])
+                                 : "memory");
+                }
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -679,11 +748,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float y[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+        // s_x of this thread's row, loaded one stage ahead of their use (the
+        // rows are strided in memory: each lane's load is its own transaction)
+        float sxa[KP], sxb[KP];
+        auto load_sx = [&](int64_t q, float (&o)[KP]) {
+#pragma unroll
+            for (int bi = 0; bi < KP; ++bi) {
+                const int64_t kb = q * KP + bi;
+                o[bi] = (m < a.M && kb < nkb) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
+            }
+        };
+        load_sx(0, sxa);
         bool ok = true;
         for (int64_t q = 0; ok && q * KP < nkb; ++q) {
             const int64_t kb0 = q * KP;
             const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
             const int pr = static_cast<int>(q % NP);
+            load_sx(q + 1, sxb);
             QMM_TRACE(30, kb0);
             if (!wait_or_abort(bar_acc_full(BARS, pr), (q / NP) & 1, FLAG, a.st.err)) {
                 ok = false;
@@ -693,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             for (int bi = 0; bi < nbk; ++bi) {
                 const int64_t kb = kb0 + bi;
-                const float sx = (m < a.M) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
+                const float sx = sxa[bi];
                 const float2 s2 = make_float2(sx, sx);
                 // this block's d (q6_K: its super-block's, Q4_0: its own)
                 const int64_t dk = Q6 ? (kb >> 3) : kb;
@@ -709,11 +790,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[32];
                     tc_ld32(acc + 32 * half, v);
                     tc_wait_ld();
-                    if (a.dbg != nullptr && kb == 0 && m < a.M) {
-                        for (int c = 0; c < 32; ++c)
-                            if (n0 + 64 * h + 32 * half + c < a.N)
-                                a.dbg[m * a.N + n0 + 64 * h + 32 * half + c] = v[c];
-                    }
                     const uint32_t dv = S + L.dv + (di * BN + 64 * h + 32 * half) * 4;
 #pragma unroll
                     for (int c = 0; c < 32; c += 2) {
@@ -731,6 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_acc_empty(BARS, pr));
             QMM_TRACE(32, kb0);
+#pragma unroll
+            for (int bi = 0; bi < KP; ++bi) sxa[bi] = sxb[bi];
         }
         if (ok && m < a.M) {
             const int64_t nb0 = n0 + 64 * h;
@@ -772,7 +850,7 @@ size_t gemm_a16_bytes(int64_t M, int64_t K) {
 
 cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, DevState st, int live_slot, float* dbg) {
+                        int64_t K, cudaStream_t s, DevState st, int live_slot) {
     GemmKernel k = pick_gemm(fmt, exp);
     if (!k) return cudaErrorInvalidValue;
     const SmemLayout L = smem_layout(fmt, exp);
@@ -805,7 +883,6 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
     a.n8 = N / 8 * 8;
     a.st = st;
     a.live_slot = live_slot;
-    a.dbg = dbg;
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
     // q6_K / Q4_0 rows: W as [N / 8][8 * rowbytes] bytes of 16-bit elements
     // (the pitch of 8 rows is a multiple of 16 bytes for both formats); a box

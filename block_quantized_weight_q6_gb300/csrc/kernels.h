@@ -125,8 +125,7 @@ size_t gemm_a16_bytes(int64_t M, int64_t K);
 // fmt FMT_Q6_K (exp: plane variant) or FMT_Q4_0 (exp false)
 cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, DevState st, int live_slot,
-                        float* dbg = nullptr);
+                        int64_t K, cudaStream_t s, DevState st, int live_slot);
 
 // ---------------------------------------------------------------- MoE
 constexpr int kMoeMaxExperts = 1024;
