@@ -76,7 +76,8 @@ constexpr int kAStage = KP * kATile, kBStage = KP * kBTile;
 // raw stage row strides (16-byte multiples with room for the lead-in)
 constexpr int kRawQ6K = 240;      // one 210-byte super-block
 constexpr int kRawQ40 = 176;      // up to 8 18-byte blocks
-constexpr int kRawPlane = 304;    // 256 plane bytes + 48 for scales and d
+constexpr int kRawScale = 48;     // plane variant: a super-block's 16 scales and d with their lead-in
+constexpr int kPlaneTile = 16 * BN * 16;  // plane variant: 256 columns of 128 rows, [16-column chunk][row][16]
 
 struct SmemLayout {
     uint32_t a, b, raw, rawslot, dv, bars, tslot, abort_flag;
@@ -86,16 +87,18 @@ struct SmemLayout {
 // Raw stage of q6_K / Q4_0 rows (tensor-map layout): 8 boxes, box j holding
 // row j of each of the tile's 16 groups of 8 rows at RS-byte slots, then a
 // tail area for the up to 7 rows past the last whole group of 8 rows of W.
-// A plane stage holds row n = 8 g + j at (16 j + g) * kRawPlane.
+// A plane stage is the plane tile (16-byte column chunk c of row n at
+// 2048 c + 16 n) followed by such a row area of kRawScale-byte slots that
+// holds each row's scales and d.
 __host__ __device__ constexpr uint32_t raw_slot_bytes(int rs, bool exp) {
-    return exp ? static_cast<uint32_t>(BN) * rs : 8u * 16u * rs + 8u * rs;
+    return (exp ? static_cast<uint32_t>(kPlaneTile) : 0u) + 8u * 16u * rs + 8u * rs;
 }
 
 __host__ __device__ constexpr uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     SmemLayout L{};
-    const uint32_t rs = exp ? kRawPlane : (fmt == FMT_Q6_K ? kRawQ6K : kRawQ40);
+    const uint32_t rs = exp ? kRawScale : (fmt == FMT_Q6_K ? kRawQ6K : kRawQ40);
     const uint32_t dr = fmt == FMT_Q6_K ? DR_Q6K : DR_Q40;
     uint32_t o = 0;
     L.a = o;
@@ -355,10 +358,12 @@ struct GemmArgs {
 
 template <int FMT, bool EXP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap wmap) {
+    gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap wmap,
+                const __grid_constant__ CUtensorMap pmap) {
     constexpr bool Q6 = (FMT == FMT_Q6_K);
     constexpr int DR = Q6 ? DR_Q6K : DR_Q40;
-    constexpr int RS = EXP ? kRawPlane : (Q6 ? kRawQ6K : kRawQ40);
+    constexpr int RS = EXP ? kRawScale : (Q6 ? kRawQ6K : kRawQ40);
+    constexpr uint32_t RW = EXP ? kPlaneTile : 0u;  // offset of the row area in a raw stage
     const SmemLayout L = smem_layout(FMT, EXP);
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t S = smem_u32(smem);
@@ -411,73 +416,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
             const uint32_t bar = bar_raw_full(BARS, r);
             uint32_t bytes = 0;
-            if (EXP) {
-                // plane rows (256 bytes) and the block's scales and d, per row
-                for (int n = lane; n < BN; n += 32) {
-                    const int64_t ng = n0 + n;
-                    if (ng >= a.N) break;
-                    const int64_t st = (ng * a.nb + sc) * 210 + 192;
+            // rows of whole groups of 8 through the tensor map (8 boxes),
+            // the up to 7 rows past them as 1-D copies from the 16-byte
+            // boundary at or below each row segment (plain loads for bytes
+            // past the last 16-byte boundary of W); the plane variant takes
+            // only each row's scales and d from W, and its plane tile as 16
+            // boxes of 16 columns
+            const int64_t koff = EXP ? sc * 210 + 192 : (Q6 ? sc * 210 : sc * 8 * 18);
+            const int64_t len = EXP ? 18 : (Q6 ? 210 : min(static_cast<int64_t>(8), a.nb - sc * 8) * 18);
+            const uint32_t rw0 = dst0 + RW;
+            const bool boxes = n0 < a.n8;
+            int64_t cs = 0, ce = 0;
+            int tr = -1;
+            {
+                const int64_t ng = a.n8 + lane;
+                if (lane < 8 && ng < a.N && ng >= n0 && ng < n0 + BN) {
+                    tr = lane;
+                    const int64_t st = ng * a.rowbytes + koff;
                     const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + 18 + 15) & ~static_cast<int64_t>(15), tb16);
-                    bytes += 256;
-                    if (e16 > s16) bytes += static_cast<uint32_t>(e16 - s16);
-                    const uint32_t rdst = dst0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS + 256;
-                    for (int64_t q = max(e16, s16); q < st + 18; ++q)
-                        sts_u8(rdst + static_cast<uint32_t>(q - s16), a.W[q]);
-                }
-                fence_proxy_async_smem();
-                bytes = __reduce_add_sync(0xffffffffu, bytes);
-                if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-                __syncwarp();
-                for (int n = lane; n < BN; n += 32) {
-                    const int64_t ng = n0 + n;
-                    if (ng >= a.N) break;
-                    const uint32_t rdst = dst0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS;
-                    bulk_g2s(rdst, a.plane + ng * a.K + sc * 256, 256, bar);
-                    const int64_t st = (ng * a.nb + sc) * 210 + 192;
-                    const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + 18 + 15) & ~static_cast<int64_t>(15), tb16);
-                    if (e16 > s16)
-                        bulk_g2s(rdst + 256, a.W + s16, static_cast<uint32_t>(e16 - s16), bar);
-                }
-            } else {
-                // rows of whole groups of 8 through the tensor map (8 boxes),
-                // the up to 7 rows past them as 1-D copies from the 16-byte
-                // boundary at or below each row segment (plain loads for bytes
-                // past the last 16-byte boundary of W)
-                const int64_t koff = Q6 ? sc * 210 : sc * 8 * 18;
-                const int64_t len = Q6 ? 210 : min(static_cast<int64_t>(8), a.nb - sc * 8) * 18;
-                const bool boxes = n0 < a.n8;
-                int64_t cs = 0, ce = 0;
-                int tr = -1;
-                {
-                    const int64_t ng = a.n8 + lane;
-                    if (lane < 8 && ng < a.N && ng >= n0 && ng < n0 + BN) {
-                        tr = lane;
-                        const int64_t st = ng * a.rowbytes + koff;
-                        const int64_t s16 = st & ~static_cast<int64_t>(15);
-                        const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                        if (e16 > s16) {
-                            cs = s16;
-                            ce = e16;
-                            bytes = static_cast<uint32_t>(e16 - s16);
-                        }
-                        for (int64_t q = max(e16, s16); q < st + len; ++q)
-                            sts_u8(dst0 + 8u * 16u * RS + tr * RS + static_cast<uint32_t>(q - s16), a.W[q]);
+                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+                    if (e16 > s16) {
+                        cs = s16;
+                        ce = e16;
+                        bytes = static_cast<uint32_t>(e16 - s16);
                     }
+                    for (int64_t q = max(e16, s16); q < st + len; ++q)
+                        sts_u8(rw0 + 8u * 16u * RS + tr * RS + static_cast<uint32_t>(q - s16), a.W[q]);
                 }
-                fence_proxy_async_smem();
-                bytes = __reduce_add_sync(0xffffffffu, bytes);
-                if (lane == 0) mbar_arrive_expect_tx(bar, bytes + (boxes ? 8u * 16u * RS : 0u));
-                __syncwarp();
-                if (boxes && lane < 8) {
-                    const int64_t xb = (lane * a.rowbytes + koff) & ~static_cast<int64_t>(15);
-                    tma_load_2d(dst0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2),
-                                static_cast<int>(n0 / 8), bar);
-                }
-                if (ce > cs)
-                    bulk_g2s(dst0 + 8u * 16u * RS + tr * RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
             }
+            fence_proxy_async_smem();
+            bytes = __reduce_add_sync(0xffffffffu, bytes);
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar, bytes + (boxes ? 8u * 16u * RS : 0u) + RW);
+            __syncwarp();
+            if (boxes && lane < 8) {
+                const int64_t xb = (lane * a.rowbytes + koff) & ~static_cast<int64_t>(15);
+                tma_load_2d(rw0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2), static_cast<int>(n0 / 8),
+                            bar);
+            }
+            if (EXP && lane < 16)
+                tma_load_2d(dst0 + lane * (BN * 16u), &pmap, static_cast<int>(sc * 256 + 16 * lane),
+                            static_cast<int>(n0), bar);
+            if (ce > cs)
+                bulk_g2s(rw0 + 8u * 16u * RS + tr * RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
         };
         if (warp == kRawWarp) {
             for (int64_t sc = 0; sc < nsc; ++sc) {
@@ -566,11 +547,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = static_cast<int>(sc % NR);
             const uint32_t raw0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
             // row n of the tile within the raw stage
+            // (the plane variant: its scales and d)
             auto rowaddr = [&](int n) -> uint32_t {
-                if (EXP) return raw0 + static_cast<uint32_t>(16 * (n & 7) + (n >> 3)) * RS;
                 const int64_t ng = n0 + n;
-                if (ng < a.n8) return raw0 + static_cast<uint32_t>(n & 7) * 16u * RS + static_cast<uint32_t>(n >> 3) * RS;
-                return raw0 + 8u * 16u * RS + static_cast<uint32_t>(ng - a.n8) * RS;
+                if (ng < a.n8)
+                    return raw0 + RW + static_cast<uint32_t>(n & 7) * 16u * RS + static_cast<uint32_t>(n >> 3) * RS;
+                return raw0 + RW + 8u * 16u * RS + static_cast<uint32_t>(ng - a.n8) * RS;
             };
             // lead-in of row n's data inside its raw stage row
             auto lead = [&](int64_t ng) -> uint32_t {
@@ -589,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int di = static_cast<int>(Q6 ? (sc % DR) : (kb % DR));
                     float dval = 0.0f;
                     if (ng < a.N) {
-                        const uint32_t rowb = rowaddr(tid) + (EXP ? 256 : 0) + lead(ng);
+                        const uint32_t rowb = rowaddr(tid) + lead(ng);
                         const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * (j0 + bi));
                         dval = half_bits_to_float(lds_u16(rowb + doff));
                     }
@@ -604,16 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = static_cast<int>(q % NS);
             if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(22, kb0);
-            // Rows 8 g + j of the tile, j = 2 cw and 2 cw + 1: per row, the raw
-            // bytes of both blocks of the stage are loaded first, then realigned
-            // by the row's lead (warp-uniform), expanded and stored.
+            // Rows 8 g + j of the tile, j = 2 cw and 2 cw + 1 (the plane
+            // variant: rows g + 16 j, consecutive rows in consecutive lanes):
+            // per row, the raw bytes of both blocks of the stage are loaded
+            // first, then realigned by the row's lead (warp-uniform for rows
+            // 8 g + j), expanded and stored.
 #pragma unroll 1
             for (int jj = 0; jj < 2; ++jj) {
                 const int j = 2 * cw + jj;
-                const int n = 8 * g + j;
+                const int n = EXP ? g + 16 * j : 8 * g + j;
                 const int64_t ng = n0 + n;
                 const bool live = ng < a.N;
-                const uint32_t rb = rowaddr(n) + lead(ng);  // lead: warp-uniform
+                const uint32_t rb = rowaddr(n) + lead(ng);
                 uint32_t hv[KP][8];
                 if (Q6) {
                     uint32_t c[KP][4];
@@ -623,8 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int bi = 0; bi < KP; ++bi) {
                             const int e = 32 * (j0 + bi) + 16 * hh;
                             if (live && bi < nbk) {
-                                lds_v4(rowaddr(n) + e, c[bi]);  // 16-byte aligned plane bytes
-                                scv[bi] = lds_s8(rb + 256 + (e >> 4));
+                                lds_v4(raw0 + (e >> 4) * (BN * 16) + n * 16, c[bi]);
+                                scv[bi] = lds_s8(rb + (e >> 4));
                             } else {
 #pragma unroll
                                 for (int w = 0; w < 4; ++w) c[bi][w] = 0x80808080u;
@@ -707,8 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // row n: group g, row j of the group; columns 16 hh .. + 15 are
-                // the K octets 2 hh and 2 hh + 1
+                // row n: group n / 8, row n % 8 of the group; columns 16 hh ..
+                // + 15 are the K octets 2 hh and 2 hh + 1
 #pragma unroll
                 for (int bi = 0; bi < KP; ++bi) {
                     if (bi >= nbk) break;
@@ -717,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int w = 0; w < 8; ++w) hv[bi][w] = 0u;
                     }
                     const uint32_t bt = S + L.b + static_cast<uint32_t>(st) * kBStage +
-                                        static_cast<uint32_t>(bi) * kBTile + g * kBSbo + j * 16;
+                                        static_cast<uint32_t>(bi) * kBTile + (n >> 3) * kBSbo + (n & 7) * 16;
                     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bt + (2 * hh) * 128),
                                  "r"(hv[bi][0]), "r"(hv[bi][1]), "r"(hv[bi][2]), "r"(hv[bi][3])
                                  : "memory");
@@ -836,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- launch
 
-using GemmKernel = void (*)(const GemmArgs, const CUtensorMap);
+using GemmKernel = void (*)(const GemmArgs, const CUtensorMap, const CUtensorMap);
 
 static GemmKernel pick_gemm(int fmt, bool exp) {
     if (fmt == FMT_Q6_K) return exp ? gemm_kernel<FMT_Q6_K, true> : gemm_kernel<FMT_Q6_K, false>;
@@ -887,12 +871,25 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
     // q6_K / Q4_0 rows: W as [N / 8][8 * rowbytes] bytes of 16-bit elements
     // (the pitch of 8 rows is a multiple of 16 bytes for both formats); a box
     // is one row slot wide and 16 groups of 8 rows high
-    CUtensorMap wmap;
+    // (the plane variant: 48-byte boxes of each row's scales and d); the
+    // plane as [N][K] bytes, a box 16 columns wide and 128 rows high
+    CUtensorMap wmap, pmap;
     memset(&wmap, 0, sizeof wmap);
-    if (!exp && a.n8 > 0) {
-        EncodeTiledFn enc = tensor_map_encoder();
-        if (!enc) return cudaErrorNotSupported;
-        const int rs = fmt == FMT_Q6_K ? kRawQ6K : kRawQ40;
+    memset(&pmap, 0, sizeof pmap);
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    if (exp) {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+        const cuuint32_t box[2] = {16u, static_cast<cuuint32_t>(BN)};
+        const cuuint32_t es[2] = {1u, 1u};
+        if (enc(&pmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(plane), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    if (a.n8 > 0) {
+        const int rs = exp ? kRawScale : (fmt == FMT_Q6_K ? kRawQ6K : kRawQ40);
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(a.n8 / 8)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
         const cuuint32_t box[2] = {static_cast<cuuint32_t>(rs / 2), 16u};
@@ -902,7 +899,7 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a, wmap);
+    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a, wmap, pmap);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
