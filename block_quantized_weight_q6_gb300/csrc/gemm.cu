@@ -527,15 +527,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(bar_acc_full(BARS, pr));
             }
             __syncwarp();
+            QMM_TRACE(14, kb0);
         }
     } else if (warp < kEpi0) {
         // ------------------------------------------------------------ converters
         // One stage (two K blocks) per pass: one wait, one proxy fence and one
-        // arrival. Warp cw converts the rows
-        // 8 g + j of the tile for j = 2 cw, 2 cw + 1: lane (g = lane % 16,
-        // h = lane / 16) the 16 columns 16 h .. 16 h + 15 of each block. A
-        // row's offset inside its raw slot depends only on j, so the
-        // realignment of its bytes is the same for the whole warp.
+        // arrival. Warp cw converts the rows 8 g + j of the tile (the plane
+        // variant: g + 16 j) for j = 2 cw, 2 cw + 1: lane (g = lane % 16,
+        // h = lane / 16) the 16 columns 16 h .. 16 h + 15 of each block. In
+        // the raw stage of q6_K / Q4_0 rows, a row's offset inside its slot
+        // depends only on j, so the realignment of its bytes is the same for
+        // the whole warp; plane bytes need none.
         const int cw = warp - kConv0;
         const int tid = threadIdx.x - 32 * kConv0;  // rows 0..127 store d
         const int g = lane & 15, hh = lane >> 4;
@@ -713,6 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_full(BARS, st));
+            QMM_TRACE(23, kb0);
             if (j0 + nbk == 8 || kb0 + nbk == nkb) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
