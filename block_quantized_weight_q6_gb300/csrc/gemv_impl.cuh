@@ -393,42 +393,51 @@ __device__ __forceinline__ float dot32(const float2 (&w)[16], const float2 (&x)[
     return s.x + s.y;
 }
 
-// WIDE: lane = block i of the chunk (32 weights)
-template <int FMT, bool Q8, int NB, int R>
+// WIDE: lane = block i of the chunk (32 weights). The activations of the
+// lane's block come in xv (chunk_x32), so that a caller can load them before
+// it waits for the weights and use them for several matrices.
+template <int NB>
+__device__ __forceinline__ void chunk_x32(const GemvArgs& a, int64_t kb0, int ncb, int lane,
+                                          float2 (&xv)[NB][16]) {
+    if (lane >= ncb) return;
+    const int64_t k0 = (kb0 + lane) * 32;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (b >= a.B) break;
+        float2 t0[8], t1[8];
+        load_x16(a, b, k0, t0);
+        load_x16(a, b, k0 + 16, t1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            xv[b][k] = t0[k];
+            xv[b][8 + k] = t1[k];
+        }
+    }
+}
+
+// pulls the lane's activations of the chunk at kb0 into L1 (a hint)
+template <int NB>
+__device__ __forceinline__ void chunk_x32_prefetch(const GemvArgs& a, int64_t kb0, int ncb, int lane) {
+    if (lane >= ncb) return;
+    const int64_t k0 = (kb0 + lane) * 32;
+    const int es = a.x_bf16 ? 2 : 4;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        if (b >= a.B) break;
+        const uint8_t* p = static_cast<const uint8_t*>(a.x) + (b * a.K + k0) * es;
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+        if (es == 4) asm volatile("prefetch.global.L1 [%0];" ::"l"(p + 64));
+    }
+}
+
+template <int FMT, int NB, int R>
 __device__ __forceinline__ void chunk_q32_wide(const GemvArgs& a, uint32_t slot, int64_t row0,
                                                int64_t kb0, int ncb, int lane,
-                                               float (&acc)[R][NB]) {
+                                               const float2 (&xv)[NB][16], float (&acc)[R][NB]) {
     constexpr int BB = Fmt<FMT>::BB;
     constexpr int SEG = seg_stride<FMT>();
     const int i = lane;
     if (i >= ncb) return;
-    const int64_t kb = kb0 + i;
-    const int64_t k0 = kb * 32;
-    float2 xv[Q8 ? 1 : NB][16];
-    uint32_t xw8[Q8 ? NB : 1][8];
-    int i0[Q8 ? NB : 1];
-    float fs[Q8 ? NB : 1];
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-        if (b >= a.B) break;
-        if (Q8) {
-            load_xq<8>(a, b, k0, xw8[b]);
-            int sm = 0;
-#pragma unroll
-            for (int m = 0; m < 8; ++m) sm = __dp4a(static_cast<int>(xw8[b][m]), 0x01010101, sm);
-            i0[b] = (FMT == FMT_Q4_0) ? kMagicI - 8 * sm : kMagicI;
-            fs[b] = __ldg(a.xs + b * (a.K / 32) + kb);
-        } else {
-            float2 t0[8], t1[8];
-            load_x16(a, b, k0, t0);
-            load_x16(a, b, k0 + 16, t1);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                xv[b][k] = t0[k];
-                xv[b][8 + k] = t1[k];
-            }
-        }
-    }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         if (row0 + r >= a.N) break;
@@ -437,24 +446,12 @@ __device__ __forceinline__ void chunk_q32_wide(const GemvArgs& a, uint32_t slot,
         const float d = half_bits_to_float(lds_u16(blk));
         uint32_t c[8];
         q32_codes<FMT>(blk, c);
-        if (Q8) {
+        float2 w[16];
+        q32_pairs<FMT>(c, 8, w);
 #pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b >= a.B) break;
-                int I = i0[b];
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    I = __dp4a(static_cast<int>(c[m]), static_cast<int>(xw8[b][m]), I);
-                acc[r][b] = fmaf((__int_as_float(I) - kMagicIF) * d, fs[b], acc[r][b]);
-            }
-        } else {
-            float2 w[16];
-            q32_pairs<FMT>(c, 8, w);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                if (b >= a.B) break;
-                acc[r][b] = fmaf(d, dot32(w, xv[b]), acc[r][b]);
-            }
+        for (int b = 0; b < NB; ++b) {
+            if (b >= a.B) break;
+            acc[r][b] = fmaf(d, dot32(w, xv[b]), acc[r][b]);
         }
     }
 }

@@ -26,11 +26,14 @@ namespace qmm {
 
 namespace {
 
-// rows per item: 4, except 2 for the fused q6_K kernel (its 1712-byte chunk
-// segments of two matrices would not fit 12 warps' rings otherwise)
+// rows per item: a lane's activations serve every row of the item, so more
+// rows mean fewer activation reads per weight byte. 8 for the Q4_0 / Q8_0
+// down projection (its fp32 activations are the widest), 4 for their fused
+// gate/up (two matrices), 4 and 2 for q6_K (its 1712-byte chunk segments
+// would not fit 12 warps' rings otherwise).
 template <int FMT, bool FUSED>
 __host__ __device__ constexpr int moe_rows() {
-    return (FMT == FMT_Q6_K && FUSED) ? 2 : 4;
+    return FMT == FMT_Q6_K ? (FUSED ? 2 : 4) : (FUSED ? 4 : 8);
 }
 constexpr int kMoeNB = 2;       // tokens per task
 constexpr int kMoeSlots = 2;    // ring slots per warp
@@ -192,39 +195,29 @@ __global__ void __launch_bounds__(kGemvThreads) moe_mv_kernel(const MoeArgs a, c
         const int e = a.tasks[task].expert;
         const int64_t kb0 = static_cast<int64_t>(ic_c) * F::CB;
         const int64_t len = min(static_cast<int64_t>(F::CB), nb - kb0) * F::BB;
-        if (lane == 0) {
-            uint32_t total = 0;
-            for (int mtx = 0; mtx < NM; ++mtx) {
-                const uint8_t* W = FUSED ? tab.p[mtx * a.E + e] : tab.p[2 * a.E + e];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int64_t row = row0 + r;
-                    if (row >= rows) break;
-                    const int64_t st = (row * nb + kb0) * F::BB;
-                    const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                    if (e16 > s16) total += static_cast<uint32_t>(e16 - s16);
-                    for (int64_t q = max(e16, s16); q < st + len; ++q)
-                        sts_u8(dst + (mtx * R + r) * SEG + static_cast<uint32_t>(q - s16), W[q]);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(bar, total);
-            for (int mtx = 0; mtx < NM; ++mtx) {
-                const uint8_t* W = FUSED ? tab.p[mtx * a.E + e] : tab.p[2 * a.E + e];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const int64_t row = row0 + r;
-                    if (row >= rows) break;
-                    const int64_t st = (row * nb + kb0) * F::BB;
-                    const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                    if (e16 > s16)
-                        bulk_g2s(dst + (mtx * R + r) * SEG, W + s16, static_cast<uint32_t>(e16 - s16),
-                                 bar);
-                }
-            }
+        // lane (mtx * R + r) copies row row0 + r of matrix mtx: from the
+        // 16-byte boundary at or below its segment, with plain loads for the
+        // bytes past the last 16-byte boundary of the matrix
+        static_assert(NM * R <= 32, "one lane per row segment");
+        const int mtx = lane / R, r = lane % R;
+        const int64_t row = row0 + r;
+        const bool mine = mtx < NM && row < rows;
+        const uint8_t* W = !mine ? nullptr : (FUSED ? tab.p[mtx * a.E + e] : tab.p[2 * a.E + e]);
+        int64_t s16 = 0, e16 = 0;
+        uint32_t bytes = 0;
+        if (mine) {
+            const int64_t st = (row * nb + kb0) * F::BB;
+            s16 = st & ~static_cast<int64_t>(15);
+            e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+            if (e16 > s16) bytes = static_cast<uint32_t>(e16 - s16);
+            for (int64_t q = max(e16, s16); q < st + len; ++q)
+                sts_u8(dst + (mtx * R + r) * SEG + static_cast<uint32_t>(q - s16), W[q]);
         }
+        fence_proxy_async_smem();
+        const uint32_t total = __reduce_add_sync(0xffffffffu, bytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar, total);
+        __syncwarp();
+        if (bytes) bulk_g2s(dst + (mtx * R + r) * SEG, W + s16, bytes, bar);
         ++issued;
         if (++ic_c >= nchunks) {
             ic_c = 0;
@@ -260,21 +253,33 @@ __global__ void __launch_bounds__(kGemvThreads) moe_mv_kernel(const MoeArgs a, c
                 for (int b = 0; b < NB; ++b) acc[mtx][r][b] = 0.0f;
         for (int c = 0; c < nchunks; ++c) {
             const uint32_t sidx = used % NS;
+            const int64_t kb0 = static_cast<int64_t>(c) * F::CB;
+            const int ncb = static_cast<int>(min(static_cast<int64_t>(F::CB), nb - kb0));
+            // Q4_0 / Q8_0: this chunk's activations are loaded once for all
+            // the item's matrices, before the wait for its weights; the next
+            // chunk's are pulled into L1 meanwhile
+            float2 xv[NB][16];
+            if constexpr (FMT != FMT_Q6_K) {
+                chunk_x32<NB>(ga, kb0, ncb, lane, xv);
+                if (c + 1 < nchunks) {
+                    const int64_t kb1 = kb0 + F::CB;
+                    chunk_x32_prefetch<NB>(ga, kb1, static_cast<int>(min(static_cast<int64_t>(F::CB), nb - kb1)),
+                                           lane);
+                }
+            }
             if (!mbar_wait(bars + 8 * sidx, (used / NS) & 1u)) {
                 for (uint32_t u = used + 1; u < issued; ++u)
                     (void)mbar_wait(bars + 8 * (u % NS), (u / NS) & 1u);
                 if (lane == 0) atomicOr(a.st.err, DERR_MOE_TIMEOUT);
                 return;
             }
-            const int64_t kb0 = static_cast<int64_t>(c) * F::CB;
-            const int ncb = static_cast<int>(min(static_cast<int64_t>(F::CB), nb - kb0));
 #pragma unroll
             for (int mtx = 0; mtx < NM; ++mtx) {
                 const uint32_t slot = ring + sidx * SLOT + mtx * R * SEG;
                 if constexpr (FMT == FMT_Q6_K)
                     chunk_q6k_wide<false, NB, R>(ga, slot, row0, kb0, ncb, lane, acc[mtx]);
                 else
-                    chunk_q32_wide<FMT, false, NB, R>(ga, slot, row0, kb0, ncb, lane, acc[mtx]);
+                    chunk_q32_wide<FMT, NB, R>(ga, slot, row0, kb0, ncb, lane, xv, acc[mtx]);
             }
             __syncwarp();
             ++used;
