@@ -27,13 +27,13 @@ namespace qmm {
 namespace {
 
 // rows per item: a lane's activations serve every row of the item, so more
-// rows mean fewer activation reads per weight byte. 8 for the Q4_0 / Q8_0
-// down projection (its fp32 activations are the widest), 4 for their fused
-// gate/up (two matrices), 4 and 2 for q6_K (its 1712-byte chunk segments
-// would not fit 12 warps' rings otherwise).
+// rows mean fewer activation reads per weight byte; the two-slot rings of 12
+// warps bound them (Q4_0 segments are 608 bytes, Q8_0 1120, q6_K 1712). The
+// down projection (fp32 activations) gets the most; the fused gate/up kernel
+// holds two matrices' rows per item.
 template <int FMT, bool FUSED>
 __host__ __device__ constexpr int moe_rows() {
-    return FMT == FMT_Q6_K ? (FUSED ? 2 : 4) : (FUSED ? 4 : 8);
+    return FMT == FMT_Q6_K ? (FUSED ? 2 : 4) : FMT == FMT_Q8_0 ? (FUSED ? 4 : 8) : (FUSED ? 6 : 12);
 }
 constexpr int kMoeNB = 2;       // tokens per task
 constexpr int kMoeSlots = 2;    // ring slots per warp
