@@ -370,7 +370,7 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------ main
 
 # read + write DRAM bytes of the MoE part per distinct expert (ncu, 24 experts, T=16)
-MOE_DRAM_BYTES_PER_EXPERT = (9216 + 244992 + 398277120 + 991232 + 199352576 + 2329088 + 3683328) / 24
+MOE_DRAM_BYTES_PER_EXPERT = (8448 + 244736 + 398921472 + 927232 + 199356928 + 2423552 + 3683584) / 24
 
 SWEEP_LAYER = [  # (name, fmt name, N, K) of one layer
     ("wq", "Q4_0", 4096, 4096), ("wk", "Q4_0", 4096, 4096), ("wo", "Q4_0", 4096, 4096),
