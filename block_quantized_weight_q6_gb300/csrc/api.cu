@@ -390,10 +390,21 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
     }
     e = tcmv_launch_group(wf, q8, p.NB, p.S, p.grid, t_stream, g);
     if (e != cudaSuccess) return cuda_fail(e, "grouped matvec launch");
+    // one reduction launch for all the split matrices of the group
+    static_assert(kReduceSetMax >= kTcMaxMats, "a reduction set covers a group");
+    SplitReduceSet rs{};
     for (int m = 0; m < p.n; ++m) {
         if (p.pieces[m] <= 1) continue;
-        e = splitk_reduce_launch(g.m[m].part, y[m], static_cast<int>(p.pieces[m]),
-                                 static_cast<int64_t>(B) * N[m], t_stream, d->st);
+        rs.part[rs.n] = g.m[m].part;
+        rs.y[rs.n] = y[m];
+        rs.count[rs.n] = static_cast<int64_t>(B) * N[m];
+        rs.start[rs.n] = rs.total;
+        rs.splits[rs.n] = static_cast<int>(p.pieces[m]);
+        rs.total += rs.count[rs.n];
+        ++rs.n;
+    }
+    if (rs.n > 0) {
+        e = splitk_reduce_set_launch(rs, t_stream, d->st);
         if (e != cudaSuccess) return cuda_fail(e, "split-K reduce launch");
     }
     return QMM_OK;

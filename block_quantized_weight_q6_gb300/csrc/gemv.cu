@@ -25,6 +25,35 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __re
     }
 }
 
+// The same for the split matrices of one grouped matvec, in one launch:
+// element i of the set belongs to the matrix m with start[m] <= i < start[m + 1].
+__global__ void splitk_reduce_set_kernel(const SplitReduceSet r, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, 2);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < r.total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int m = 0;
+        for (int q = 1; q < r.n; ++q)
+            if (i >= r.start[q]) m = q;
+        const int64_t j = i - r.start[m], count = r.count[m];
+        const float* part = r.part[m];
+        float v = 0.0f;
+        for (int s = 0; s < r.splits[m]; ++s) v += part[s * count + j];
+        r.y[m][j] = v;
+    }
+}
+
+cudaError_t splitk_reduce_set_launch(const SplitReduceSet& r, cudaStream_t s, DevState st) {
+    const int threads = 256;
+    int64_t blocks = (r.total + threads - 1) / threads;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    cudaError_t e = launch_pdl(splitk_reduce_set_kernel, dim3(static_cast<int>(blocks)), dim3(threads), 0, s,
+                               r, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
                                  cudaStream_t s, DevState st) {
     const int threads = 256;

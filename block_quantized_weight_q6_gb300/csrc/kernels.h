@@ -39,6 +39,18 @@ struct GemvArgs {
 
 cudaError_t splitk_reduce_launch(const float* part, float* y, int splits, int64_t count,
                                  cudaStream_t s, DevState st);
+// the split matrices of a grouped matvec, reduced in one launch (same order)
+constexpr int kReduceSetMax = 12;
+struct SplitReduceSet {
+    const float* part[kReduceSetMax];
+    float* y[kReduceSetMax];
+    int64_t count[kReduceSetMax];  // B * N
+    int64_t start[kReduceSetMax];  // first element of each matrix in the set
+    int splits[kReduceSetMax];
+    int n;
+    int64_t total;
+};
+cudaError_t splitk_reduce_set_launch(const SplitReduceSet& r, cudaStream_t s, DevState st);
 
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
