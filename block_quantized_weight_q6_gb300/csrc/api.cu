@@ -356,6 +356,14 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
     g.st = d->st;
     g.live_slot = q8 ? QMM_LIVE_GEMV_Q8 : QMM_LIVE_GEMV_FLOAT;
     const bool tile = q8 || !bf16;
+    ActTileSet ts{};
+    ts.x_bf16 = bf16 ? 1 : 0;
+    ts.B = B;
+    ts.fmt = wf;
+    ts.NB = p.NB;
+    ts.S = p.S;
+    ts.ncol = p.ncol;
+    ts.q8 = q8 ? 1 : 0;
     cudaError_t e;
     for (int m = 0; m < p.n; ++m) {
         TcmvArgs& a = g.m[m];
@@ -383,10 +391,19 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
         a.st = d->st;
         a.live_slot = g.live_slot;
         if (tile) {
-            e = act_tile_launch(x[m], bf16, B, K[m], wf, p.NB, p.S, p.ncol, p.nst[m], q8,
-                                const_cast<uint16_t*>(a.xt), const_cast<float*>(a.xs), t_stream, d->st);
-            if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
+            ts.x[ts.n] = x[m];
+            ts.K[ts.n] = K[m];
+            ts.xt[ts.n] = const_cast<uint16_t*>(a.xt);
+            ts.xs[ts.n] = const_cast<float*>(a.xs);
+            ts.start[ts.n] = ts.total;
+            ts.total += p.nst[m] * 16 * p.ncol * 2;
+            ++ts.n;
         }
+    }
+    if (ts.n > 0) {
+        // every matrix's activation operand in one launch
+        e = act_tile_set_launch(ts, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "activation tile launch");
     }
     e = tcmv_launch_group(wf, q8, p.NB, p.S, p.grid, t_stream, g);
     if (e != cudaSuccess) return cuda_fail(e, "grouped matvec launch");

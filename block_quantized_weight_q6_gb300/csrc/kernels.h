@@ -123,6 +123,17 @@ cudaError_t tcmv_launch_group(int fmt, bool q8, int NB, int S, int grid, cudaStr
 cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt, int NB, int S,
                             int ncol, int64_t nst, bool q8, uint16_t* xt, float* xs, cudaStream_t s,
                             DevState st);
+// the same for the matrices of a grouped matvec, in one launch
+struct ActTileSet {
+    const void* x[kTcMaxMats];
+    int64_t K[kTcMaxMats];
+    uint16_t* xt[kTcMaxMats];
+    float* xs[kTcMaxMats];
+    int64_t start[kTcMaxMats];  // first unit (16 bytes of operand) of each matrix
+    int n, x_bf16, B, fmt, NB, S, ncol, q8;
+    int64_t total;
+};
+cudaError_t act_tile_set_launch(const ActTileSet& r, cudaStream_t s, DevState st);
 
 // ---------------------------------------------------------------- quantizer
 // x [rows][K] (fp32 or bf16) -> xq [rows][K] int8, xs [rows][K/32] fp32.

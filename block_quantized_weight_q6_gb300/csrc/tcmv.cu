@@ -53,17 +53,12 @@ __device__ __forceinline__ float x_at(const void* x, int x_bf16, int64_t K, int 
 // activations as they are (S = 1) or fp32 ones split exactly as hi + mid + lo
 // (S = 3). q8 mode: the per-32 int8 codes (exact in bf16), and the scales
 // s[block][NB]. One thread per 16 bytes of the tile.
-__global__ void act_tile_kernel(const void* __restrict__ x, int x_bf16, int B, int64_t K, int fmt,
-                                int NB, int S, int ncol, int64_t nst, int q8,
-                                uint16_t* __restrict__ xt, float* __restrict__ xs, DevState st) {
-    grid_launch_dependents();
-    grid_dependency_wait();
-    live_bump(st, q8 ? QMM_LIVE_QUANTIZE : QMM_LIVE_X_TILE);
+__device__ __forceinline__ void act_tile_unit(const void* __restrict__ x, int x_bf16, int B, int64_t K,
+                                              int fmt, int NB, int S, int ncol, int q8,
+                                              uint16_t* __restrict__ xt, float* __restrict__ xs, int64_t u) {
     const int nc = NB * S, G = ncol / nc;
     const int spg = fmt == FMT_Q6_K ? 1 : 2;  // K16 steps per group
-    const int64_t units = nst * 16 * ncol * 2;
-    for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
-         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    {
         // u enumerates [stage][t][row / 8][k8 (2)][row % 8]: consecutive
         // threads write consecutive 16-byte pieces
         const int r8 = static_cast<int>(u & 7);
@@ -116,6 +111,34 @@ __global__ void act_tile_kernel(const void* __restrict__ x, int x_bf16, int B, i
             (rg * 2 + o) * 64 + r8 * 8);
         *dst = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
                           h[6] | (h[7] << 16));
+    }
+}
+
+__global__ void act_tile_kernel(const void* __restrict__ x, int x_bf16, int B, int64_t K, int fmt,
+                                int NB, int S, int ncol, int64_t nst, int q8,
+                                uint16_t* __restrict__ xt, float* __restrict__ xs, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, q8 ? QMM_LIVE_QUANTIZE : QMM_LIVE_X_TILE);
+    const int64_t units = nst * 16 * ncol * 2;
+    for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < units;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        act_tile_unit(x, x_bf16, B, K, fmt, NB, S, ncol, q8, xt, xs, u);
+}
+
+// The same for the matrices of one grouped matvec in one launch: unit i
+// belongs to the matrix m with start[m] <= i < start[m + 1].
+__global__ void act_tile_set_kernel(const ActTileSet r, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, r.q8 ? QMM_LIVE_QUANTIZE : QMM_LIVE_X_TILE);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < r.total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int m = 0;
+        for (int q = 1; q < r.n; ++q)
+            if (i >= r.start[q]) m = q;
+        act_tile_unit(r.x[m], r.x_bf16, r.B, r.K[m], r.fmt, r.NB, r.S, r.ncol, r.q8, r.xt[m], r.xs[m],
+                      i - r.start[m]);
     }
 }
 
@@ -217,6 +240,12 @@ cudaError_t tcmv_launch(int fmt, bool q8, int NB, int S, int grid, cudaStream_t 
     g.st = a.st;
     g.live_slot = a.live_slot;
     return tcmv_launch_group(fmt, q8, NB, S, grid, s, g);
+}
+
+cudaError_t act_tile_set_launch(const ActTileSet& r, cudaStream_t s, DevState st) {
+    const int threads = 256;
+    cudaError_t e = launch_pdl(act_tile_set_kernel, dim3(grid_for(r.total, threads)), dim3(threads), 0, s, r, st);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt, int NB, int S,

@@ -254,3 +254,26 @@ def test_gemv_group_matches_oracle(name, B, xdt, act):
         else:
             ref, absum = oracle.gemv_float(fmt, W, x, N, K)
         assert_within(y.cpu().numpy(), ref, absum, f"group {name} {N}x{K} B={B} {xdt} {act}")
+
+
+def test_gemv_group_launches_once_per_step():
+    """A grouped call launches the activation layout, the matvec and the
+    split-K reduction once each, whatever the number of matrices."""
+    fmt = qmm.Q6_K
+    shapes = [(37, 256 * 12), (60, 256 * 16), (20, 256 * 8)]  # short N: split along K
+    Ws = [synth.matrix(fmt, 500 + i, N, K) for i, (N, K) in enumerate(shapes)]
+    xs = [synth.normal_f32(600 + i, (1, K)) for i, (N, K) in enumerate(shapes)]
+    ys = [torch.empty((1, N), dtype=torch.float32, device="cuda") for N, K in shapes]
+    grp = qmm.GemvGroup(fmt, [dev(W) for W in Ws], [x_tensor(x) for x in xs], ys,
+                        [N for N, K in shapes], [K for N, K in shapes], qmm.ACT_Q8)
+    qmm.liveness_reset()
+    qmm.gemv_group(grp)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    live = qmm.liveness()
+    assert live["gemv_q8"] == 1 and live["quantize"] == 1
+    assert live["gemv_splitk_reduce"] == 1
+    for (N, K), W, x, y in zip(shapes, Ws, xs, ys):
+        xq, s = oracle.quantize_q8(x)
+        ref, absum = oracle.gemv_q8(fmt, W, xq, s, N, K)
+        assert_within(y.cpu().numpy(), ref, absum, f"group launches {N}x{K}")
