@@ -510,15 +510,23 @@ def main():
     moe_w = MoeWeights(torch, device)
     moe1 = MoeCase(torch, device, moe_w, 1)
     moe16 = MoeCase(torch, device, moe_w, 16)
-    # writing this buffer evicts the 129 MB L2 between the parts of a step
+    # writing one buffer larger than the 129 MB L2 evicts it between the parts
+    # of a step; reading a second one then evicts the written (dirty) lines,
+    # so that their write-back to HBM falls before the part's events, not
+    # inside them
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=device)
+
+    def l2_flush():
+        flush.zero_()
+        flush_rd.sum()
     # the step's parts, each as one CUDA graph
     parts = [("decode", dec.run), ("gemm_exp_plane", gem.run_exp),
              ("gemm_in_kernel", gem.run_in_kernel), ("moe_t1", moe1.run), ("moe_t16", moe16.run)]
     graphs = [(name, capture(torch, fn, device)) for name, fn in parts]
     for _ in range(args.warmup):
         for _, g in graphs:
-            flush.zero_()
+            l2_flush()
             g.replay()
     torch.cuda.synchronize(device)
 
@@ -538,7 +546,7 @@ def main():
         torch.cuda.synchronize(device)
         for st in range(args.steps):
             for i, (_, g) in enumerate(graphs):
-                flush.zero_()
+                l2_flush()
                 ev[st][i][0].record()
                 g.replay()
                 ev[st][i][1].record()
@@ -641,7 +649,7 @@ def main():
                        "value_is": "decode-set weight bytes / decode time",
                        "matrices": [f"{n} {f} {N}x{K}" for (n, f, N, K) in DECODE_SET],
                        "batches": list(BATCHES), "weight_bytes_per_step": dec.weight_bytes,
-                       "l2": "flushed before each part (256 MB write outside the part's events)",
+                       "l2": "flushed before each part (256 MB write, then a 256 MB read that evicts the written lines; both outside the part's events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "cpu_baseline": cpu,

@@ -56,6 +56,7 @@ struct Env {
     bool exp_on = true;
     bool debug_label = false;
     bool fault_plane_alloc = false;
+    bool mv1_on = true;
 };
 Env g_env;
 std::once_flag g_env_once;
@@ -67,6 +68,8 @@ void read_env() {
     g_env.debug_label = d && std::strcmp(d, "1") == 0;
     const char* f = std::getenv("QMM_FAULT");
     g_env.fault_plane_alloc = f && std::strcmp(f, "plane_alloc") == 0;
+    const char* mv = std::getenv("QMM_MV1");
+    g_env.mv1_on = !(mv && std::strcmp(mv, "0") == 0);
     const char* pdl = std::getenv("QMM_PDL");
     qmm::g_pdl_enabled = !(pdl && std::strcmp(pdl, "0") == 0);
 }
@@ -427,6 +430,66 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
     return QMM_OK;
 }
 
+// ---------------------------------------------------------------- batch-1 matvec
+// One activation row in float mode goes to the CUDA-core matvec (mv1.cuh)
+// when its K suits it; QMM_MV1=0 sends it to the tensor-core matvec instead.
+bool use_mv1(int wf, bool q8, int B, int64_t K) {
+    return g_env.mv1_on && !q8 && B == 1 && mv1_supported(wf, K);
+}
+
+// Launches mv1 over matrices sel[0 .. n-1] (same K) of the arrays.
+int run_mv1(int wf, bool bf16, int n, const int* sel, const void* const* W, const void* const* x,
+            float* const* y, const int64_t* N, int64_t K, const DevInfo* d) {
+    Mv1Group g{};
+    g.nmat = n;
+    g.K = K;
+    g.rowbytes = K / block_elems(wf) * block_bytes(wf);
+    g.pieces = static_cast<int>((K + 2047) / 2048);
+    g.full_pieces = static_cast<int>(K / 2048);
+    g.aligned = g.rowbytes % 16 == 0;
+    g.x_bf16 = bf16 ? 1 : 0;
+    g.st = d->st;
+    g.live_slot = QMM_LIVE_GEMV_MV1;
+    int64_t items = 0;
+    for (int i = 0; i < n; ++i) {
+        const int m = sel[i];
+        Mv1Mat& a = g.m[i];
+        a.W = static_cast<const uint8_t*>(W[m]);
+        a.x = x[m];
+        a.y = y[m];
+        a.N = N[m];
+        a.item0 = static_cast<int>(items);
+        items += (N[m] + kMv1RowBlock - 1) / kMv1RowBlock;
+        if (reinterpret_cast<uintptr_t>(W[m]) % 16) g.aligned = 0;
+    }
+    if (items > (int64_t{1} << 30)) return fail(QMM_EUNSUPPORTED, "batch-1 matvec: %lld row blocks", (long long)items);
+    g.items = static_cast<int>(items);
+    const int occ = mv1_occupancy(wf);
+    if (occ <= 0) return fail(QMM_ECUDA, "batch-1 matvec (fmt %d) cannot launch", wf);
+    const int64_t slots = static_cast<int64_t>(d->sms) * occ;
+    const int grid = static_cast<int>(items < slots ? items : slots);
+    cudaError_t e = mv1_launch(wf, grid, t_stream, g);
+    if (e != cudaSuccess) return cuda_fail(e, "batch-1 matvec launch");
+    return QMM_OK;
+}
+
+// Splits a group into the matrices that mv1 takes (those with the K of the
+// first one it takes) and the rest; returns how many go to mv1.
+int mv1_partition(int wf, bool q8, int B, int n, const int64_t* K, int* mv, int* rest, int* nrest) {
+    int nm = 0;
+    *nrest = 0;
+    int64_t k1 = -1;
+    for (int m = 0; m < n; ++m) {
+        if (use_mv1(wf, q8, B, K[m]) && (k1 < 0 || K[m] == k1)) {
+            k1 = K[m];
+            mv[nm++] = m;
+        } else {
+            rest[(*nrest)++] = m;
+        }
+    }
+    return nm;
+}
+
 int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, int64_t N,
                     int64_t K, int B, int* wf, bool* bf16, bool* q8) {
     int rc = check_fmt(fmt, wf, bf16, q8);
@@ -479,6 +542,10 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if (rc) return rc;
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
+    if (use_mv1(wf, q8, B, K)) {
+        const int sel = 0;
+        return run_mv1(wf, bf16, 1, &sel, &W, &x, &y, &N, K, d);
+    }
     GemvPlan p;
     if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
     if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
@@ -508,12 +575,32 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
     if (rc) return rc;
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
+    // the matrices the batch-1 matvec takes, in one launch; the rest in one
+    // tensor-core matvec launch
+    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0;
+    const int nmv = mv1_partition(wf, q8, B, n, K, mv, rest, &nrest);
+    const void* Wr[kTcMaxMats];
+    const void* xr[kTcMaxMats];
+    float* yr[kTcMaxMats];
+    int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
+    for (int i = 0; i < nrest; ++i) {
+        const int m = rest[i];
+        Wr[i] = W[m];
+        xr[i] = x[m];
+        yr[i] = y[m];
+        Nr[i] = N[m];
+        Kr[i] = K[m];
+    }
     GroupPlan p;
-    if ((rc = plan_gemv_group_cached(wf, q8, bf16, B, n, N, K, d->sms, &p))) return rc;
-    if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
-        return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set", p.ws_total,
-                    t_ws_bytes);
-    return run_gemv_group(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(t_ws), d);
+    if (nrest > 0) {
+        if ((rc = plan_gemv_group_cached(wf, q8, bf16, B, nrest, Nr, Kr, d->sms, &p))) return rc;
+        if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
+            return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set",
+                        p.ws_total, t_ws_bytes);
+    }
+    if (nmv > 0 && (rc = run_mv1(wf, bf16, nmv, mv, W, x, y, N, K[mv[0]], d))) return rc;
+    if (nrest > 0) return run_gemv_group(wf, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, static_cast<uint8_t*>(t_ws), d);
+    return QMM_OK;
 }
 
 size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, const int64_t* K, int B) {
@@ -525,8 +612,16 @@ size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, con
         if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf)) return 0;
     DevInfo* d;
     if (dev_info(&d)) return 0;
+    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0;
+    (void)mv1_partition(wf, q8, B, n, K, mv, rest, &nrest);
+    if (nrest == 0) return 0;
+    int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
+    for (int i = 0; i < nrest; ++i) {
+        Nr[i] = N[rest[i]];
+        Kr[i] = K[rest[i]];
+    }
     GroupPlan p;
-    if (plan_gemv_group_cached(wf, q8, bf16, B, n, N, K, d->sms, &p)) return 0;
+    if (plan_gemv_group_cached(wf, q8, bf16, B, nrest, Nr, Kr, d->sms, &p)) return 0;
     return p.ws_total;
 }
 

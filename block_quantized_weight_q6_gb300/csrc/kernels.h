@@ -52,6 +52,33 @@ struct SplitReduceSet {
 };
 cudaError_t splitk_reduce_set_launch(const SplitReduceSet& r, cudaStream_t s, DevState st);
 
+// ---------------------------------------------------------------- batch-1 matvec
+// One activation row, float mode, on the CUDA cores (mv1.cuh): work item =
+// block of kMv1RowBlock rows of one matrix, all of K. Matrices of one launch
+// share format and K, and K % 256 == 0.
+constexpr int kMv1RowBlock = 4;
+struct Mv1Mat {
+    const uint8_t* W;
+    const void* x;   // [K] fp32 or bf16
+    float* y;        // [N]
+    int64_t N;
+    int item0;       // first item of this matrix in the launch
+};
+struct Mv1Group {
+    Mv1Mat m[12];
+    int nmat, items;
+    int64_t K, rowbytes;
+    int pieces, full_pieces;  // ceil(K / 2048), floor(K / 2048)
+    int aligned;              // every W and the row pitch are 16-byte multiples
+    int x_bf16;
+    DevState st;
+    int live_slot;
+};
+// whether mv1 takes this (format, K) and resident CTAs per SM; launch
+bool mv1_supported(int fmt, int64_t K);
+int mv1_occupancy(int fmt);
+cudaError_t mv1_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
+
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
 constexpr int kTcThreads = 768;

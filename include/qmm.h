@@ -97,6 +97,8 @@ enum {
                                          tensor-core operand                 */
     QMM_LIVE_MOE_PLAN = 15,
     QMM_LIVE_MOE_GATHER = 16,
+    QMM_LIVE_GEMV_MV1 = 17,           /* batch-1 float matvec on the CUDA
+                                         cores                               */
     QMM_LIVE_COUNT = 24
 };
 

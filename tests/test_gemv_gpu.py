@@ -112,12 +112,14 @@ def _unit_scale(fmt, N, K, rng):
 
 @pytest.mark.parametrize("name", ["q6_K", "Q4_0", "Q8_0"])
 @pytest.mark.parametrize("B", [1, 8])
-def test_gemv_integer_paths_bitwise(name, B):
+@pytest.mark.parametrize("K", [512, 2048])
+def test_gemv_integer_paths_bitwise(name, B, K):
     """d = 1, sub-scales 1, integer activations with amax 127 per 32: the q8
     path is an exact integer matmul; so is the float path (all partial sums
-    are integers below 2^24). Both must equal the oracle bitwise."""
+    are integers below 2^24). Both must equal the oracle bitwise. (K = 2048
+    at batch 1 runs every format through the CUDA-core batch-1 matvec.)"""
     fmt = FMTS[name]
-    N, K = 24, 512
+    N = 24
     rng = np.random.default_rng(fmt * 10 + B)
     W, wint = _unit_scale(fmt, N, K, rng)
     xi = rng.integers(-127, 128, (B, K))
@@ -202,16 +204,20 @@ def test_liveness_counts_each_launch():
     qmm.liveness_reset()
     N, K = 64, 4096
     W = synth.q6k_matrix(1, N, K)
-    x = synth.normal_f32(2, (1, K))
+    x = synth.normal_f32(2, (2, K))  # batch 2: the tensor-core matvec
     run_gemv(qmm.Q6_K, W, x, N, K)
-    run_gemv(qmm.Q6_K, W, x, N, K, qmm.ACT_Q8)
+    run_gemv(qmm.Q6_K, W, x[:1], N, K, qmm.ACT_Q8)
     live = qmm.liveness()
     assert live["gemv_float"] == 1 and live["gemv_q8"] == 1 and live["quantize"] == 1
     assert live["gemv_splitk_reduce"] == 2  # short N is split along K
     assert live["x_tile"] == 1              # fp32 float mode lays the activations out once
-    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (2, K)), N, K)
     live = qmm.liveness()
     assert live["gemv_float"] == 2 and live["x_tile"] == 1  # bf16: gathered inside the matvec
+    assert live["gemv_mv1"] == 0 and live["gemv_splitk_reduce"] == 3
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)  # batch 1, float: one mv1 launch, no split
+    live = qmm.liveness()
+    assert live["gemv_mv1"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
 
 
 def test_missing_workspace_is_an_error():
@@ -277,3 +283,58 @@ def test_gemv_group_launches_once_per_step():
         xq, s = oracle.quantize_q8(x)
         ref, absum = oracle.gemv_q8(fmt, W, xq, s, N, K)
         assert_within(y.cpu().numpy(), ref, absum, f"group launches {N}x{K}")
+
+
+# The batch-1 float matvec on the CUDA cores (mv1): taken for B = 1, float
+# mode, K % 256 == 0. Ragged row counts (not a multiple of the 16-row item),
+# K pieces of 2048 with a partial last piece, q6_K rows that are not a
+# multiple of 16 bytes (K / 256 not a multiple of 8: rows start at any even
+# offset), more items than warps in the grid, fp32 and bf16 activations.
+MV1_SHAPES = [("q6_K", 37, 2048), ("q6_K", 2053, 4096), ("q6_K", 300, 8192),
+              ("q6_K", 61, 11008), ("q6_K", 33, 768), ("q6_K", 4099, 11008), ("q6_K", 3, 256),
+              ("Q4_0", 1001, 4096), ("Q4_0", 70, 2816), ("Q4_0", 19500, 4096), ("Q4_0", 5, 256),
+              ("Q8_0", 515, 4096), ("Q8_0", 33, 768), ("Q8_0", 16, 6144)]
+
+
+@pytest.mark.parametrize("name,N,K", MV1_SHAPES)
+@pytest.mark.parametrize("xdt", ["f32", "bf16"])
+def test_mv1_matches_oracle(name, N, K, xdt):
+    fmt = FMTS[name]
+    W = synth.matrix(fmt, 700 + N, N, K)
+    x = synth.normal_f32(710 + N, (1, K)) if xdt == "f32" else synth.normal_bf16(710 + N, (1, K))
+    qmm.liveness_reset()
+    y = run_gemv(fmt, W, x, N, K)
+    assert qmm.liveness()["gemv_mv1"] == 1
+    if N * K <= 4096 * 4096:
+        ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+        assert_within(y, ref, absum, f"mv1 {name} {N}x{K} {xdt}")
+    else:  # large: sampled outputs, computed one by one
+        rng = np.random.default_rng(N)
+        ns = np.concatenate([rng.integers(0, N, 300), [0, N - 1, N - 16, N - 17]])
+        ref, absum = oracle.gemv_float_pairs(fmt, W, K, x, np.zeros(len(ns), int), ns)
+        assert_within(y[0, ns], ref, absum, f"mv1 {name} {N}x{K} {xdt}")
+    # the order of the sums is fixed: a second call is bitwise identical
+    y2 = run_gemv(fmt, W, x, N, K)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+def test_mv1_zero_weights_and_identity_are_exact():
+    """w = 0 gives exactly 0 and a one-hot row gives exactly its x, through
+    the batch-1 matvec of each format"""
+    n = 2048
+    x = synth.normal_f32(9, (1, n))
+    one = pack.f16_bits(1.0)
+    codes = np.full((n, n), 32)
+    np.fill_diagonal(codes, 33)
+    W6 = pack.pack_q6k_matrix(codes, np.ones((n, n // 16), int), np.full((n, n // 256), one))
+    c4 = np.full((n, n), 8)
+    np.fill_diagonal(c4, 9)
+    W4 = pack.pack_q4_0_matrix(c4, np.full((n, n // 32), one))
+    v8 = np.zeros((n, n), int)
+    np.fill_diagonal(v8, 1)
+    W8 = pack.pack_q8_0_matrix(v8, np.full((n, n // 32), one))
+    for fmt, W in [(qmm.Q6_K, W6), (qmm.Q4_0, W4), (qmm.Q8_0, W8)]:
+        qmm.liveness_reset()
+        y = run_gemv(fmt, W, x, n, n)
+        assert qmm.liveness()["gemv_mv1"] == 1
+        assert np.array_equal(y, x), f"fmt {fmt}"
