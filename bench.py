@@ -453,7 +453,9 @@ def run_profile(args):
             if not items:
                 raise SystemExit(f"no decode matvec {name} at batch {B}")
             dec.items = items
-        fn = dec.run
+            fn = dec.run_per_call  # that matvec alone
+        else:
+            fn = dec.run
     elif part[0] in ("gemm_exp_plane", "gemm_in_kernel"):
         gem = GemmCase(torch, device)
         fn = gem.run_exp if part[0] == "gemm_exp_plane" else gem.run_in_kernel
@@ -608,7 +610,7 @@ def main():
     tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
     seg = {
         "decode": {"bound": "hbm", "achieved": dec.algo_bytes / (ms_dec * 1e-3) / 1e9, "peak": hbm,
-                   "unit": "GB/s", "kernel": "tcmv_kernel (tensor-core matvec) + split-K reduce, decode set: part time over all launches"},
+                   "unit": "GB/s", "kernel": "mv1_kernel (batch 1, CUDA cores) + tcmv_kernel (batch 8, tensor cores) + split-K reduce, decode set: part time over all launches"},
         "gemm_exp_plane": {"bound": "tensor", "achieved": tops["gemm_exp_plane"], "peak": tc_peak,
                            "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, plane> + quantize"},
         "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,
