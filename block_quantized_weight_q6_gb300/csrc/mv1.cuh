@@ -157,45 +157,41 @@ __device__ __forceinline__ void mv1_x_load_f32(const float* x, int64_t K, int64_
 // Q4_0 block (d fp16 | qs[16]); qs byte j holds weights j (low nibble) and
 // j + 16 (high nibble), w = d * (q - 8). The lane's two blocks start at
 // 36 lane (4-byte aligned): block 0's qs at bytes 2..17, block 1's at 20..35.
-// The four nibbles of a 16-bit half (bytes 2t, 2t + 1 of qs: weights 2t,
-// 2t + 16, 2t + 1, 2t + 17) become floats by one mask-and-or each into the
-// mantissa of 2^23: 2^23 + 16^n q for nibble n of the half (exact, below
-// 2^24). Subtracting 2^23 + 16^n 8 leaves 16^n (q - 8) exactly; the four
-// scales 1, 16, 256, 4096 each keep their own accumulator lane and are
-// divided out (exactly) once per block.
-template <int N>
-__device__ __forceinline__ float q40_nib(uint32_t h) {
-    return __uint_as_float((h & (0xFu << (4 * N))) | 0x4B000000u);
-}
-
+// (Masking each nibble straight into a magic float's mantissa, four scales
+// in four accumulator lanes, costs fewer instructions but ran slower here.)
 __device__ __forceinline__ float mv1_dec_q4_0(uint32_t row, int lane, const float2 (&x)[32]) {
     const uint32_t a = row + 36u * static_cast<uint32_t>(lane);
     uint32_t w[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) w[i] = lds_u32(a + 4 * i);
-    // (lo of byte 2t, lo of 2t+1) and (hi of 2t, hi of 2t+1)
-    const float2 negA = make_float2(-(8388608.0f + 8.0f), -(8388608.0f + 8.0f * 256.0f));
-    const float2 negB = make_float2(-(8388608.0f + 8.0f * 16.0f), -(8388608.0f + 8.0f * 4096.0f));
+    uint32_t lo[9], hi[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        lo[i] = w[i] & 0x0F0F0F0Fu;
+        hi[i] = (w[i] >> 4) & 0x0F0F0F0Fu;
+    }
+    const float2 neg = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
     float r = 0.0f;
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         const int p0 = 18 * b;
         const uint32_t dbits = (p0 & 3) == 0 ? (w[p0 >> 2] & 0xFFFFu) : (w[p0 >> 2] >> 16);
-        float2 sA = make_float2(0.0f, 0.0f), sB = make_float2(0.0f, 0.0f);
+        float2 s0 = make_float2(0.0f, 0.0f), s1 = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const int pa = p0 + 2 + 2 * t;  // first byte of the half (even)
-            const uint32_t h = (pa & 3) == 0 ? w[pa >> 2] : (w[pa >> 2] >> 16);
-            const float2 lo = fadd2(make_float2(q40_nib<0>(h), q40_nib<2>(h)), negA);
-            const float2 hi = fadd2(make_float2(q40_nib<1>(h), q40_nib<3>(h)), negB);
-            sA = ffma2(lo, x[16 * b + t], sA);
-            sB = ffma2(hi, x[16 * b + 8 + t], sB);
+        for (int j = 0; j < 16; j += 2) {
+            const int pa = p0 + 2 + j;  // even: the pair shares a word
+            const int wi = pa >> 2, bj = pa & 3;
+            const float2 ql = fadd2(make_float2(__uint_as_float(__byte_perm(lo[wi], 0x4B000000u, 0x7540u + bj)),
+                                                __uint_as_float(__byte_perm(lo[wi], 0x4B000000u, 0x7541u + bj))),
+                                    neg);
+            const float2 qh = fadd2(make_float2(__uint_as_float(__byte_perm(hi[wi], 0x4B000000u, 0x7540u + bj)),
+                                                __uint_as_float(__byte_perm(hi[wi], 0x4B000000u, 0x7541u + bj))),
+                                    neg);
+            s0 = ffma2(ql, x[16 * b + j / 2], s0);
+            s1 = ffma2(qh, x[16 * b + 8 + j / 2], s1);
         }
-        // the block's sum: the scaled lanes brought back to weight 1
-        float s = fmaf(sA.y, 1.0f / 256.0f, sA.x);
-        s = fmaf(sB.x, 1.0f / 16.0f, s);
-        s = fmaf(sB.y, 1.0f / 4096.0f, s);
-        r = fmaf(half_bits_to_float(dbits), s, r);
+        const float2 s = fadd2(s0, s1);
+        r = fmaf(half_bits_to_float(dbits), s.x + s.y, r);
     }
     return r;
 }
