@@ -57,6 +57,7 @@ struct Env {
     bool debug_label = false;
     bool fault_plane_alloc = false;
     bool mv1_on = true;
+    bool mv8_on = true;
 };
 Env g_env;
 std::once_flag g_env_once;
@@ -70,6 +71,8 @@ void read_env() {
     g_env.fault_plane_alloc = f && std::strcmp(f, "plane_alloc") == 0;
     const char* mv = std::getenv("QMM_MV1");
     g_env.mv1_on = !(mv && std::strcmp(mv, "0") == 0);
+    const char* m8 = std::getenv("QMM_MV8");
+    g_env.mv8_on = !(m8 && std::strcmp(m8, "0") == 0);
     const char* pdl = std::getenv("QMM_PDL");
     qmm::g_pdl_enabled = !(pdl && std::strcmp(pdl, "0") == 0);
 }
@@ -430,26 +433,35 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
     return QMM_OK;
 }
 
-// ---------------------------------------------------------------- batch-1 matvec
-// One activation row in float mode goes to the CUDA-core matvec (mv1.cuh)
-// when its K suits it; QMM_MV1=0 sends it to the tensor-core matvec instead.
-bool use_mv1(int wf, bool q8, int B, int64_t K) {
-    return g_env.mv1_on && !q8 && B == 1 && mv1_supported(wf, K);
+// ---------------------------------------------------------------- batch 1-8 matvecs
+// Float mode with K % 256 == 0: one activation row goes to the CUDA-core
+// matvec (mv1.cuh), 2..8 bf16 rows to the warp-level MMA matvec (mv8.cuh);
+// QMM_MV1=0 / QMM_MV8=0 send them to the tensor-memory matvec instead.
+enum { FAST_NONE = 0, FAST_MV1 = 1, FAST_MV8 = 8 };
+
+int fast_path(int wf, bool q8, bool bf16, int B, int64_t K) {
+    if (q8) return FAST_NONE;
+    if (B == 1 && g_env.mv1_on && mv1_supported(wf, K)) return FAST_MV1;
+    if (B >= 2 && B <= 8 && bf16 && g_env.mv8_on && mv8_supported(wf, K)) return FAST_MV8;
+    return FAST_NONE;
 }
 
-// Launches mv1 over matrices sel[0 .. n-1] (same K) of the arrays.
-int run_mv1(int wf, bool bf16, int n, const int* sel, const void* const* W, const void* const* x,
-            float* const* y, const int64_t* N, int64_t K, const DevInfo* d) {
+// Launches mv1 or mv8 over matrices sel[0 .. n-1] (same K) of the arrays.
+int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const void* const* W,
+             const void* const* x, float* const* y, const int64_t* N, int64_t K, const DevInfo* d) {
+    const int64_t rb = path == FAST_MV1 ? kMv1RowBlock : kMv8RowBlock;
+    const int64_t piece = path == FAST_MV1 ? 2048 : 256;
     Mv1Group g{};
     g.nmat = n;
     g.K = K;
     g.rowbytes = K / block_elems(wf) * block_bytes(wf);
-    g.pieces = static_cast<int>((K + 2047) / 2048);
-    g.full_pieces = static_cast<int>(K / 2048);
+    g.pieces = static_cast<int>((K + piece - 1) / piece);
+    g.full_pieces = static_cast<int>(K / piece);
     g.aligned = g.rowbytes % 16 == 0;
     g.x_bf16 = bf16 ? 1 : 0;
+    g.B = B;
     g.st = d->st;
-    g.live_slot = QMM_LIVE_GEMV_MV1;
+    g.live_slot = path == FAST_MV1 ? QMM_LIVE_GEMV_MV1 : QMM_LIVE_GEMV_MV8;
     int64_t items = 0;
     for (int i = 0; i < n; ++i) {
         const int m = sel[i];
@@ -459,29 +471,44 @@ int run_mv1(int wf, bool bf16, int n, const int* sel, const void* const* W, cons
         a.y = y[m];
         a.N = N[m];
         a.item0 = static_cast<int>(items);
-        items += (N[m] + kMv1RowBlock - 1) / kMv1RowBlock;
+        items += (N[m] + rb - 1) / rb;
         if (reinterpret_cast<uintptr_t>(W[m]) % 16) g.aligned = 0;
     }
-    if (items > (int64_t{1} << 30)) return fail(QMM_EUNSUPPORTED, "batch-1 matvec: %lld row blocks", (long long)items);
+    if (items > (int64_t{1} << 30)) return fail(QMM_EUNSUPPORTED, "matvec: %lld row blocks", (long long)items);
     g.items = static_cast<int>(items);
-    const int occ = mv1_occupancy(wf);
-    if (occ <= 0) return fail(QMM_ECUDA, "batch-1 matvec (fmt %d) cannot launch", wf);
+    const int occ = path == FAST_MV1 ? mv1_occupancy(wf) : mv8_occupancy(wf);
+    if (occ <= 0) return fail(QMM_ECUDA, "matvec (fmt %d, path %d) cannot launch", wf, path);
     const int64_t slots = static_cast<int64_t>(d->sms) * occ;
-    const int grid = static_cast<int>(items < slots ? items : slots);
-    cudaError_t e = mv1_launch(wf, grid, t_stream, g);
-    if (e != cudaSuccess) return cuda_fail(e, "batch-1 matvec launch");
+    int grid = static_cast<int>(items < slots ? items : slots);
+    g.ks = 1;
+    if (path == FAST_MV8) {
+        // warps per item: enough that the items keep every warp of the grid
+        // busy, at most the item's stages
+        const int64_t warps = slots * 8;
+        while (g.ks < 8 && 2 * g.ks <= g.pieces && items * g.ks < warps) g.ks *= 2;
+        const int64_t teams = slots * (8 / g.ks);
+        grid = static_cast<int>(items * 1 < teams ? (items + 8 / g.ks - 1) / (8 / g.ks) : slots);
+        if (grid < 1) grid = 1;
+        if (grid > slots) grid = static_cast<int>(slots);
+    }
+    cudaError_t e = path == FAST_MV1 ? mv1_launch(wf, grid, t_stream, g) : mv8_launch(wf, grid, t_stream, g);
+    if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
     return QMM_OK;
 }
 
-// Splits a group into the matrices that mv1 takes (those with the K of the
-// first one it takes) and the rest; returns how many go to mv1.
-int mv1_partition(int wf, bool q8, int B, int n, const int64_t* K, int* mv, int* rest, int* nrest) {
+// Splits a group into the matrices that mv1 / mv8 take (those with the K of
+// the first one taken) and the rest; returns how many are taken and the path.
+int fast_partition(int wf, bool q8, bool bf16, int B, int n, const int64_t* K, int* mv, int* rest, int* nrest,
+                   int* path) {
     int nm = 0;
     *nrest = 0;
+    *path = FAST_NONE;
     int64_t k1 = -1;
     for (int m = 0; m < n; ++m) {
-        if (use_mv1(wf, q8, B, K[m]) && (k1 < 0 || K[m] == k1)) {
+        const int pth = fast_path(wf, q8, bf16, B, K[m]);
+        if (pth != FAST_NONE && (k1 < 0 || K[m] == k1)) {
             k1 = K[m];
+            *path = pth;
             mv[nm++] = m;
         } else {
             rest[(*nrest)++] = m;
@@ -542,9 +569,9 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if (rc) return rc;
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
-    if (use_mv1(wf, q8, B, K)) {
+    if (const int path = fast_path(wf, q8, bf16, B, K)) {
         const int sel = 0;
-        return run_mv1(wf, bf16, 1, &sel, &W, &x, &y, &N, K, d);
+        return run_fast(path, wf, bf16, B, 1, &sel, &W, &x, &y, &N, K, d);
     }
     GemvPlan p;
     if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
@@ -577,8 +604,8 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
     if ((rc = dev_info(&d))) return rc;
     // the matrices the batch-1 matvec takes, in one launch; the rest in one
     // tensor-core matvec launch
-    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0;
-    const int nmv = mv1_partition(wf, q8, B, n, K, mv, rest, &nrest);
+    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0, path = 0;
+    const int nmv = fast_partition(wf, q8, bf16, B, n, K, mv, rest, &nrest, &path);
     const void* Wr[kTcMaxMats];
     const void* xr[kTcMaxMats];
     float* yr[kTcMaxMats];
@@ -598,7 +625,7 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
             return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set",
                         p.ws_total, t_ws_bytes);
     }
-    if (nmv > 0 && (rc = run_mv1(wf, bf16, nmv, mv, W, x, y, N, K[mv[0]], d))) return rc;
+    if (nmv > 0 && (rc = run_fast(path, wf, bf16, B, nmv, mv, W, x, y, N, K[mv[0]], d))) return rc;
     if (nrest > 0) return run_gemv_group(wf, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, static_cast<uint8_t*>(t_ws), d);
     return QMM_OK;
 }
@@ -612,8 +639,8 @@ size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, con
         if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf)) return 0;
     DevInfo* d;
     if (dev_info(&d)) return 0;
-    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0;
-    (void)mv1_partition(wf, q8, B, n, K, mv, rest, &nrest);
+    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0, path = 0;
+    (void)fast_partition(wf, q8, bf16, B, n, K, mv, rest, &nrest, &path);
     if (nrest == 0) return 0;
     int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
     for (int i = 0; i < nrest; ++i) {

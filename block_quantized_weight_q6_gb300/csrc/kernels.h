@@ -71,6 +71,8 @@ struct Mv1Group {
     int pieces, full_pieces;  // ceil(K / 2048), floor(K / 2048)
     int aligned;              // every W and the row pitch are 16-byte multiples
     int x_bf16;
+    int B;                    // activation rows (mv8: 2..8)
+    int ks;                   // mv8: warps that share an item (1, 2, 4 or 8)
     DevState st;
     int live_slot;
 };
@@ -78,6 +80,16 @@ struct Mv1Group {
 bool mv1_supported(int fmt, int64_t K);
 int mv1_occupancy(int fmt);
 cudaError_t mv1_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
+
+// ---------------------------------------------------------------- batch 2-8 matvec
+// 2..8 bf16 activation rows, float mode, on the warp-level MMA (mv8.cuh):
+// work item = block of kMv8RowBlock rows of one matrix, all of K, in stages
+// of 256 K. The same group description as mv1 (pieces = K / 256, items of
+// kMv8RowBlock rows); K % 256 == 0.
+constexpr int kMv8RowBlock = 32;
+bool mv8_supported(int fmt, int64_t K);
+int mv8_occupancy(int fmt);
+cudaError_t mv8_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
 
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.

@@ -99,6 +99,8 @@ enum {
     QMM_LIVE_MOE_GATHER = 16,
     QMM_LIVE_GEMV_MV1 = 17,           /* batch-1 float matvec on the CUDA
                                          cores                               */
+    QMM_LIVE_GEMV_MV8 = 18,           /* batch 2-8 float matvec on the
+                                         warp-level MMA                      */
     QMM_LIVE_COUNT = 24
 };
 

@@ -211,13 +211,16 @@ def test_liveness_counts_each_launch():
     assert live["gemv_float"] == 1 and live["gemv_q8"] == 1 and live["quantize"] == 1
     assert live["gemv_splitk_reduce"] == 2  # short N is split along K
     assert live["x_tile"] == 1              # fp32 float mode lays the activations out once
-    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (2, K)), N, K)
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (9, K)), N, K)  # batch 9: the tensor-core matvec
     live = qmm.liveness()
     assert live["gemv_float"] == 2 and live["x_tile"] == 1  # bf16: gathered inside the matvec
     assert live["gemv_mv1"] == 0 and live["gemv_splitk_reduce"] == 3
     run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)  # batch 1, float: one mv1 launch, no split
     live = qmm.liveness()
     assert live["gemv_mv1"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (4, K)), N, K)  # batch 4, bf16: one mv8 launch (K split across warps)
+    live = qmm.liveness()
+    assert live["gemv_mv8"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
 
 
 def test_missing_workspace_is_an_error():
@@ -338,3 +341,51 @@ def test_mv1_zero_weights_and_identity_are_exact():
         y = run_gemv(fmt, W, x, n, n)
         assert qmm.liveness()["gemv_mv1"] == 1
         assert np.array_equal(y, x), f"fmt {fmt}"
+
+
+# The batch 2-8 float matvec on the warp-level MMA (mv8): taken for 2 <= B <= 8,
+# bf16 activations, float mode, K % 256 == 0. Ragged rows (not a multiple of
+# the 32-row item or of a 16-row MMA tile), activation rows short of 8,
+# q6_K rows at any even offset, more items than warps.
+MV8_SHAPES = [("q6_K", 37, 256), ("q6_K", 2053, 4096), ("q6_K", 61, 11008), ("q6_K", 4100, 11008),
+              ("Q4_0", 1001, 4096), ("Q4_0", 70, 2816), ("Q4_0", 13000, 4096), ("Q4_0", 5, 256),
+              ("Q8_0", 515, 4096), ("Q8_0", 33, 768)]
+
+
+@pytest.mark.parametrize("name,N,K", MV8_SHAPES)
+@pytest.mark.parametrize("B", [2, 5, 8])
+def test_mv8_matches_oracle(name, N, K, B):
+    fmt = FMTS[name]
+    W = synth.matrix(fmt, 800 + N, N, K)
+    x = synth.normal_bf16(810 + N + B, (B, K))
+    qmm.liveness_reset()
+    y = run_gemv(fmt, W, x, N, K)
+    assert qmm.liveness()["gemv_mv8"] == 1
+    if N * K <= 4096 * 4096:
+        ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+        assert_within(y, ref, absum, f"mv8 {name} {N}x{K} B={B}")
+    else:
+        rng = np.random.default_rng(N + B)
+        ns = np.concatenate([rng.integers(0, N, 200), [0, N - 1, N - 16, N - 33]])
+        bs = rng.integers(0, B, len(ns))
+        ref, absum = oracle.gemv_float_pairs(fmt, W, K, x, bs, ns)
+        assert_within(y[bs, ns], ref, absum, f"mv8 {name} {N}x{K} B={B}")
+    y2 = run_gemv(fmt, W, x, N, K)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["q6_K", "Q4_0", "Q8_0"])
+def test_mv8_integer_path_bitwise(name):
+    """unit scales and integer activations (exact in bf16): the MMA's sums are
+    integers below 2^24, so the batch 2-8 matvec equals the exact product"""
+    fmt = FMTS[name]
+    N, K, B = 40, 1024, 8
+    rng = np.random.default_rng(fmt * 10 + 7)
+    W, wint = _unit_scale(fmt, N, K, rng)
+    xi = rng.integers(-127, 128, (B, K))
+    x = synth.to_bf16_bits(xi.astype(np.float32))  # integers below 256: exact in bf16
+    exact = (xi @ wint.T).astype(np.float64)
+    qmm.liveness_reset()
+    y = run_gemv(fmt, W, x, N, K)
+    assert qmm.liveness()["gemv_mv8"] == 1
+    assert np.array_equal(y.astype(np.float64), exact)
