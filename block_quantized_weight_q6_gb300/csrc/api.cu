@@ -434,35 +434,34 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
 }
 
 // ---------------------------------------------------------------- batch 1-8 matvecs
-// Float mode with K % 256 == 0: one activation row goes to the CUDA-core
-// matvec (mv1.cuh), 2..8 bf16 rows to the warp-level MMA matvec (mv8.cuh);
-// QMM_MV1=0 / QMM_MV8=0 send them to the tensor-memory matvec instead.
+// Float mode with K % 256 == 0 and rows of whole 16-byte pieces (Q4_0, Q8_0;
+// q6_K with K % 2048 == 0): one activation row goes to the CUDA-core matvec
+// (mv1.cuh), 2..8 bf16 rows to the warp-level MMA matvec (mv8.cuh). Other
+// rows (q6_K rows of 210 * K / 256 bytes start at any even offset) went
+// faster through the tensor-memory matvec's 8-row tensor map, as does
+// everything with QMM_MV1=0 / QMM_MV8=0.
 enum { FAST_NONE = 0, FAST_MV1 = 1, FAST_MV8 = 8 };
 
 int fast_path(int wf, bool q8, bool bf16, int B, int64_t K) {
-    if (q8) return FAST_NONE;
+    if (q8 || K % block_elems(wf) != 0 || (K / block_elems(wf) * block_bytes(wf)) % 16 != 0) return FAST_NONE;
     if (B == 1 && g_env.mv1_on && mv1_supported(wf, K)) return FAST_MV1;
     if (B >= 2 && B <= 8 && bf16 && g_env.mv8_on && mv8_supported(wf, K)) return FAST_MV8;
     return FAST_NONE;
 }
 
-// Launches mv1 or mv8 over matrices sel[0 .. n-1] (same K) of the arrays.
+// Launches mv1 or mv8 over matrices sel[0 .. n-1] of the arrays.
 int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const void* const* W,
-             const void* const* x, float* const* y, const int64_t* N, int64_t K, const DevInfo* d) {
+             const void* const* x, float* const* y, const int64_t* N, const int64_t* K, const DevInfo* d) {
     const int64_t rb = path == FAST_MV1 ? kMv1RowBlock : kMv8RowBlock;
     const int64_t piece = path == FAST_MV1 ? 2048 : 256;
     Mv1Group g{};
     g.nmat = n;
-    g.K = K;
-    g.rowbytes = K / block_elems(wf) * block_bytes(wf);
-    g.pieces = static_cast<int>((K + piece - 1) / piece);
-    g.full_pieces = static_cast<int>(K / piece);
-    g.aligned = g.rowbytes % 16 == 0;
     g.x_bf16 = bf16 ? 1 : 0;
     g.B = B;
     g.st = d->st;
     g.live_slot = path == FAST_MV1 ? QMM_LIVE_GEMV_MV1 : QMM_LIVE_GEMV_MV8;
     int64_t items = 0;
+    int min_pieces = 1 << 30;
     for (int i = 0; i < n; ++i) {
         const int m = sel[i];
         Mv1Mat& a = g.m[i];
@@ -470,9 +469,14 @@ int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const vo
         a.x = x[m];
         a.y = y[m];
         a.N = N[m];
+        a.K = K[m];
+        a.rowbytes = K[m] / block_elems(wf) * block_bytes(wf);
+        a.pieces = static_cast<int>((K[m] + piece - 1) / piece);
+        a.full_pieces = static_cast<int>(K[m] / piece);
+        a.aligned = a.rowbytes % 16 == 0 && reinterpret_cast<uintptr_t>(W[m]) % 16 == 0;
         a.item0 = static_cast<int>(items);
         items += (N[m] + rb - 1) / rb;
-        if (reinterpret_cast<uintptr_t>(W[m]) % 16) g.aligned = 0;
+        min_pieces = std::min(min_pieces, a.pieces);
     }
     if (items > (int64_t{1} << 30)) return fail(QMM_EUNSUPPORTED, "matvec: %lld row blocks", (long long)items);
     g.items = static_cast<int>(items);
@@ -483,31 +487,27 @@ int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const vo
     g.ks = 1;
     if (path == FAST_MV8) {
         // warps per item: enough that the items keep every warp of the grid
-        // busy, at most the item's stages
+        // busy, at most any matrix's stages
         const int64_t warps = slots * 8;
-        while (g.ks < 8 && 2 * g.ks <= g.pieces && items * g.ks < warps) g.ks *= 2;
-        const int64_t teams = slots * (8 / g.ks);
-        grid = static_cast<int>(items * 1 < teams ? (items + 8 / g.ks - 1) / (8 / g.ks) : slots);
-        if (grid < 1) grid = 1;
-        if (grid > slots) grid = static_cast<int>(slots);
+        while (g.ks < 8 && 2 * g.ks <= min_pieces && items * g.ks < warps) g.ks *= 2;
+        const int64_t per_cta = 8 / g.ks;  // teams per CTA
+        grid = static_cast<int>(std::min<int64_t>(slots, (items + per_cta - 1) / per_cta));
     }
     cudaError_t e = path == FAST_MV1 ? mv1_launch(wf, grid, t_stream, g) : mv8_launch(wf, grid, t_stream, g);
     if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
     return QMM_OK;
 }
 
-// Splits a group into the matrices that mv1 / mv8 take (those with the K of
-// the first one taken) and the rest; returns how many are taken and the path.
+// Splits a group into the matrices that mv1 / mv8 take and the rest; returns
+// how many are taken and the path.
 int fast_partition(int wf, bool q8, bool bf16, int B, int n, const int64_t* K, int* mv, int* rest, int* nrest,
                    int* path) {
     int nm = 0;
     *nrest = 0;
     *path = FAST_NONE;
-    int64_t k1 = -1;
     for (int m = 0; m < n; ++m) {
         const int pth = fast_path(wf, q8, bf16, B, K[m]);
-        if (pth != FAST_NONE && (k1 < 0 || K[m] == k1)) {
-            k1 = K[m];
+        if (pth != FAST_NONE) {
             *path = pth;
             mv[nm++] = m;
         } else {
@@ -571,7 +571,7 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if ((rc = dev_info(&d))) return rc;
     if (const int path = fast_path(wf, q8, bf16, B, K)) {
         const int sel = 0;
-        return run_fast(path, wf, bf16, B, 1, &sel, &W, &x, &y, &N, K, d);
+        return run_fast(path, wf, bf16, B, 1, &sel, &W, &x, &y, &N, &K, d);
     }
     GemvPlan p;
     if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
@@ -625,7 +625,7 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
             return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set",
                         p.ws_total, t_ws_bytes);
     }
-    if (nmv > 0 && (rc = run_fast(path, wf, bf16, B, nmv, mv, W, x, y, N, K[mv[0]], d))) return rc;
+    if (nmv > 0 && (rc = run_fast(path, wf, bf16, B, nmv, mv, W, x, y, N, K, d))) return rc;
     if (nrest > 0) return run_gemv_group(wf, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, static_cast<uint8_t*>(t_ws), d);
     return QMM_OK;
 }

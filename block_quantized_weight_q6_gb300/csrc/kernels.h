@@ -54,22 +54,21 @@ cudaError_t splitk_reduce_set_launch(const SplitReduceSet& r, cudaStream_t s, De
 
 // ---------------------------------------------------------------- batch-1 matvec
 // One activation row, float mode, on the CUDA cores (mv1.cuh): work item =
-// block of kMv1RowBlock rows of one matrix, all of K. Matrices of one launch
-// share format and K, and K % 256 == 0.
+// block of kMv1RowBlock rows of one matrix, all of its K. Matrices of one
+// launch share the format; K % 256 == 0.
 constexpr int kMv1RowBlock = 4;
 struct Mv1Mat {
     const uint8_t* W;
-    const void* x;   // [K] fp32 or bf16
-    float* y;        // [N]
-    int64_t N;
-    int item0;       // first item of this matrix in the launch
+    const void* x;   // [B][K] fp32 or bf16
+    float* y;        // [B][N]
+    int64_t N, K, rowbytes;
+    int pieces, full_pieces;  // K in the kernel's pieces (2048 for mv1, 256 for mv8), partial one included / not
+    int aligned;              // W and the row pitch are 16-byte multiples
+    int item0;                // first item of this matrix in the launch
 };
 struct Mv1Group {
     Mv1Mat m[12];
     int nmat, items;
-    int64_t K, rowbytes;
-    int pieces, full_pieces;  // ceil(K / 2048), floor(K / 2048)
-    int aligned;              // every W and the row pitch are 16-byte multiples
     int x_bf16;
     int B;                    // activation rows (mv8: 2..8)
     int ks;                   // mv8: warps that share an item (1, 2, 4 or 8)
@@ -83,9 +82,9 @@ cudaError_t mv1_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
 
 // ---------------------------------------------------------------- batch 2-8 matvec
 // 2..8 bf16 activation rows, float mode, on the warp-level MMA (mv8.cuh):
-// work item = block of kMv8RowBlock rows of one matrix, all of K, in stages
-// of 256 K. The same group description as mv1 (pieces = K / 256, items of
-// kMv8RowBlock rows); K % 256 == 0.
+// work item = block of kMv8RowBlock rows of one matrix, all of its K, in
+// stages of 256 K. The same group description as mv1 (pieces = K / 256,
+// items of kMv8RowBlock rows); K % 256 == 0.
 constexpr int kMv8RowBlock = 32;
 bool mv8_supported(int fmt, int64_t K);
 int mv8_occupancy(int fmt);

@@ -6,7 +6,7 @@ namespace qmm {
 
 bool mv1_supported(int fmt, int64_t K) {
     if (K <= 0) return false;
-    if (fmt == FMT_Q6_K) return K % 256 == 0;
+    if (fmt == FMT_Q6_K) return K % 256 == 0;  // (the dispatch also wants 16-byte rows)
     return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0) && K % 256 == 0;
 }
 

@@ -288,7 +288,7 @@ template <int SPP>
 __device__ __forceinline__ void mv1_advance(const Mv1Group& g, int nw, Mv1Cursor& c) {
     if (++c.u < SPP) return;
     c.u = 0;
-    if (++c.p < g.pieces) return;
+    if (++c.p < g.m[c.m].pieces) return;
     c.p = 0;
     c.it += nw;
     while (c.m + 1 < g.nmat && c.it >= g.m[c.m + 1].item0) ++c.m;
@@ -296,9 +296,9 @@ __device__ __forceinline__ void mv1_advance(const Mv1Group& g, int nw, Mv1Cursor
 
 // Byte offset of row `row`'s piece p from the 16-byte boundary below it.
 template <int FMT>
-__device__ __forceinline__ uint32_t mv1_lead(const Mv1Group& g, const Mv1Mat& a, int64_t row, int p) {
+__device__ __forceinline__ uint32_t mv1_lead(const Mv1Mat& a, int64_t row, int p) {
     if constexpr (FMT != FMT_Q6_K) return 0;
-    return static_cast<uint32_t>((reinterpret_cast<uintptr_t>(a.W) + row * g.rowbytes +
+    return static_cast<uint32_t>((reinterpret_cast<uintptr_t>(a.W) + row * a.rowbytes +
                                   static_cast<int64_t>(p) * Mv1F<FMT>::PB) & 15);
 }
 
@@ -333,8 +333,8 @@ __device__ __forceinline__ void mv1_issue(const Mv1Group& g, const Mv1Cursor& c,
     const Mv1Mat& a = g.m[c.m];
     const int64_t row0 = static_cast<int64_t>(c.it - a.item0) * kMv1RB + c.u * F::RC;
     const int64_t off = static_cast<int64_t>(c.p) * F::PB;
-    const uint8_t* base = a.W + row0 * g.rowbytes + off;
-    if (g.aligned && c.p < g.full_pieces && row0 + F::RC <= a.N) {
+    const uint8_t* base = a.W + row0 * a.rowbytes + off;
+    if (a.aligned && c.p < a.full_pieces && row0 + F::RC <= a.N) {
         // whole 16-byte pieces, as many per row as the format's full piece
 #pragma unroll
         for (int i = 0; i < C::N; ++i) {
@@ -347,10 +347,10 @@ __device__ __forceinline__ void mv1_issue(const Mv1Group& g, const Mv1Cursor& c,
     // the 16-byte pieces that cover each row's piece; the last piece of the
     // matrix is read only up to its end
     const int rows = static_cast<int>(min(static_cast<int64_t>(F::RC), a.N - row0));
-    const uintptr_t end = reinterpret_cast<uintptr_t>(a.W) + static_cast<uintptr_t>(a.N * g.rowbytes);
-    const int64_t len = min(static_cast<int64_t>(F::PB), g.rowbytes - off);
+    const uintptr_t end = reinterpret_cast<uintptr_t>(a.W) + static_cast<uintptr_t>(a.N * a.rowbytes);
+    const int64_t len = min(static_cast<int64_t>(F::PB), a.rowbytes - off);
     for (int r = 0; r < rows; ++r) {
-        const uintptr_t at = reinterpret_cast<uintptr_t>(base + r * g.rowbytes);
+        const uintptr_t at = reinterpret_cast<uintptr_t>(base + r * a.rowbytes);
         const uintptr_t start = at & ~static_cast<uintptr_t>(15);
         const int n16 = static_cast<int>((at - start + len + 15) / 16);
         for (int cc = lane; cc < n16; cc += 32) {
@@ -381,20 +381,26 @@ __global__ void __launch_bounds__(kMv1Warps * 32, 1) mv1_kernel(const __grid_con
     grid_launch_dependents();
     live_bump(g.st, g.live_slot);
     if (gw >= g.items) return;
-    Mv1Copies<FMT> cp;
-    mv1_copies_init<FMT>(cp, g.rowbytes, lane);
     // the weights do not depend on the previous kernel: their first copies
     // go out before waiting for it
     Mv1Cursor ic{gw, 0, 0, 0};
     while (ic.m + 1 < g.nmat && ic.it >= g.m[ic.m + 1].item0) ++ic.m;
     const int m0 = ic.m;
+    Mv1Copies<FMT> cp;  // this lane's copy offsets for the rows of matrix cp_m
+    int cp_m = m0;
+    mv1_copies_init<FMT>(cp, g.m[m0].rowbytes, lane);
+    auto issue = [&](uint32_t slot) {
+        if (ic.m != cp_m) {
+            cp_m = ic.m;
+            mv1_copies_init<FMT>(cp, g.m[cp_m].rowbytes, lane);
+        }
+        mv1_issue<FMT>(g, ic, cp, slot, lane);
+        mv1_advance<SPP>(g, nw, ic);
+    };
     int si = 0;  // ring slot of the next issue
 #pragma unroll
     for (int j = 0; j < NS - 1; ++j) {
-        if (ic.it < g.items) {
-            mv1_issue<FMT>(g, ic, cp, ring + si * SLOT, lane);
-            mv1_advance<SPP>(g, nw, ic);
-        }
+        if (ic.it < g.items) issue(ring + si * SLOT);
         cp_async_commit();
         si = si + 1 == NS ? 0 : si + 1;
     }
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kMv1Warps * 32, 1) mv1_kernel(const __grid_con
     uint4 xr[8];
     float acc[kMv1RB];
     int sc = 0;  // ring slot of the next stage to decode
-    if (g.x_bf16) mv1_x_fetch_bf16<FMT>(static_cast<const uint16_t*>(g.m[m0].x), g.K, 0, lane, xr);
+    if (g.x_bf16) mv1_x_fetch_bf16<FMT>(static_cast<const uint16_t*>(g.m[m0].x), g.m[m0].K, 0, lane, xr);
     int m = m0;
     for (int it = gw; it < g.items; it += nw) {
         while (m + 1 < g.nmat && it >= g.m[m + 1].item0) ++m;
@@ -412,30 +418,27 @@ __global__ void __launch_bounds__(kMv1Warps * 32, 1) mv1_kernel(const __grid_con
         const int64_t row0 = static_cast<int64_t>(it - a.item0) * kMv1RB;
 #pragma unroll
         for (int r = 0; r < kMv1RB; ++r) acc[r] = 0.0f;
-        for (int p = 0; p < g.pieces; ++p) {
+        for (int p = 0; p < a.pieces; ++p) {
             // this piece's activations into registers; the next piece's fetched
             if (g.x_bf16) {
                 mv1_x_from_bf16(xr, xf);
-                const bool last = p + 1 == g.pieces;
+                const bool last = p + 1 == a.pieces;
                 if (!last || it + nw < g.items) {
                     int mn = m;
                     if (last)
                         while (mn + 1 < g.nmat && it + nw >= g.m[mn + 1].item0) ++mn;
-                    mv1_x_fetch_bf16<FMT>(static_cast<const uint16_t*>(g.m[mn].x), g.K, last ? 0 : p + 1, lane,
+                    mv1_x_fetch_bf16<FMT>(static_cast<const uint16_t*>(g.m[mn].x), g.m[mn].K, last ? 0 : p + 1, lane,
                                           xr);
                 }
             } else {
-                mv1_x_load_f32<FMT>(static_cast<const float*>(a.x), g.K, p, lane, xf);
+                mv1_x_load_f32<FMT>(static_cast<const float*>(a.x), a.K, p, lane, xf);
             }
             // lanes past K in a partial last piece add nothing
             const bool active = static_cast<int64_t>(p) * kMv1PieceK +
-                                    (FMT == FMT_Q6_K ? 256 * (lane >> 2) : 64 * lane) < g.K;
+                                    (FMT == FMT_Q6_K ? 256 * (lane >> 2) : 64 * lane) < a.K;
 #pragma unroll
             for (int u = 0; u < SPP; ++u) {
-                if (ic.it < g.items) {
-                    mv1_issue<FMT>(g, ic, cp, ring + si * SLOT, lane);
-                    mv1_advance<SPP>(g, nw, ic);
-                }
+                if (ic.it < g.items) issue(ring + si * SLOT);
                 cp_async_commit();
                 si = si + 1 == NS ? 0 : si + 1;
                 cp_async_wait<NS - 1>();
@@ -443,7 +446,7 @@ __global__ void __launch_bounds__(kMv1Warps * 32, 1) mv1_kernel(const __grid_con
                 const uint32_t slot = ring + sc * SLOT;
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
-                    const uint32_t lead = mv1_lead<FMT>(g, a, row0 + u * RC + r, p);
+                    const uint32_t lead = mv1_lead<FMT>(a, row0 + u * RC + r, p);
                     const float v = mv1_dec<FMT>(slot + r * F::RS + lead, lane, xf);
                     acc[u * RC + r] += active ? v : 0.0f;
                 }

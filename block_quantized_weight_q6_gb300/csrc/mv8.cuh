@@ -242,7 +242,7 @@ struct Mv8Cursor {
 
 __device__ __forceinline__ void mv8_advance(const Mv1Group& g, int ks, int member, int nteams, Mv8Cursor& c) {
     c.p += ks;
-    if (c.p < g.pieces) return;
+    if (c.p < g.m[c.m].pieces) return;
     c.p = member;
     c.it += nteams;
     while (c.m + 1 < g.nmat && c.it >= g.m[c.m + 1].item0) ++c.m;
@@ -255,7 +255,7 @@ __device__ __forceinline__ void mv8_issue(const Mv1Group& g, const Mv8Cursor& c,
     const Mv1Mat& a = g.m[c.m];
     const int64_t row0 = static_cast<int64_t>(c.it - a.item0) * kMv8RB;
     const int rows = static_cast<int>(min(static_cast<int64_t>(kMv8RB), a.N - row0));
-    const uint8_t* base = a.W + row0 * g.rowbytes + static_cast<int64_t>(c.p) * F::PB;
+    const uint8_t* base = a.W + row0 * a.rowbytes + static_cast<int64_t>(c.p) * F::PB;
     if constexpr (FMT != FMT_Q6_K) {
         // Q4_0 / Q8_0 rows (K % 256 == 0, W 16-byte aligned) are whole
         // 16-byte pieces: the stage's rows one after another
@@ -265,20 +265,20 @@ __device__ __forceinline__ void mv8_issue(const Mv1Group& g, const Mv8Cursor& c,
             const int q = lane + 32 * i;
             const int r = q / CPR, cc = q % CPR;
             if (q < kMv8RB * CPR && r < rows)
-                cp_async16(slot + static_cast<uint32_t>(r * F::RS + 16 * cc), base + r * g.rowbytes + 16 * cc);
+                cp_async16(slot + static_cast<uint32_t>(r * F::RS + 16 * cc), base + r * a.rowbytes + 16 * cc);
         }
         return;
     }
     // q6_K: the (at most 15) 16-byte pieces that cover each row's
     // super-block; the matrix's last piece is read only up to its end
-    const uintptr_t end = reinterpret_cast<uintptr_t>(a.W) + static_cast<uintptr_t>(a.N * g.rowbytes);
+    const uintptr_t end = reinterpret_cast<uintptr_t>(a.W) + static_cast<uintptr_t>(a.N * a.rowbytes);
     constexpr int NP = (F::PB + 15 + 15) / 16;
 #pragma unroll
     for (int i = 0; i < (kMv8RB * NP + 31) / 32; ++i) {
         const int q = lane + 32 * i;
         const int r = q / NP, cc = q % NP;
         if (q >= kMv8RB * NP || r >= rows) continue;
-        const uintptr_t at = reinterpret_cast<uintptr_t>(base + r * g.rowbytes);
+        const uintptr_t at = reinterpret_cast<uintptr_t>(base + r * a.rowbytes);
         const uintptr_t start = at & ~static_cast<uintptr_t>(15);
         if (static_cast<int64_t>(16 * cc) >= static_cast<int64_t>(at - start) + F::PB) continue;
         const uintptr_t src = start + 16 * cc;
@@ -295,7 +295,7 @@ __device__ __forceinline__ void mv8_issue(const Mv1Group& g, const Mv8Cursor& c,
 __device__ __forceinline__ void mv8_x_fetch(const Mv1Group& g, const Mv1Mat& a, int p, int lane, uint2 (&xb)[16]) {
     const int gr = lane >> 2, c = lane & 3;
     if (gr < g.B) {
-        const uint16_t* x = static_cast<const uint16_t*>(a.x) + static_cast<int64_t>(gr) * g.K +
+        const uint16_t* x = static_cast<const uint16_t*>(a.x) + static_cast<int64_t>(gr) * a.K +
                             static_cast<int64_t>(p) * kMv8StageK + 4 * c;
 #pragma unroll
         for (int s = 0; s < 16; ++s) xb[s] = __ldg(reinterpret_cast<const uint2*>(x + 16 * s));
@@ -361,11 +361,11 @@ __global__ void __launch_bounds__(kMv8Warps * 32, 1) mv8_kernel(const __grid_con
         for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[t][q] = 0.0f;
-        for (int p = member; p < g.pieces; p += ks) {
+        for (int p = member; p < a.pieces; p += ks) {
 #pragma unroll
             for (int s = 0; s < 16; ++s) xb[s] = xn[s];
             // the next stage's activations (this item's, or the next item's first)
-            if (p + ks < g.pieces) {
+            if (p + ks < a.pieces) {
                 mv8_x_fetch(g, a, p + ks, lane, xn);
             } else if (it + nteams < g.items) {
                 int mn = m;
@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(kMv8Warps * 32, 1) mv8_kernel(const __grid_con
                 if constexpr (FMT == FMT_Q6_K) {
                     // offset of each row's super-block in its first 16-byte piece
                     const uintptr_t w0 = reinterpret_cast<uintptr_t>(a.W) + static_cast<int64_t>(p) * F::PB;
-                    la = static_cast<uint32_t>((w0 + (row0 + ra) * g.rowbytes) & 15);
-                    lb = static_cast<uint32_t>((w0 + (row0 + rb) * g.rowbytes) & 15);
+                    la = static_cast<uint32_t>((w0 + (row0 + ra) * a.rowbytes) & 15);
+                    lb = static_cast<uint32_t>((w0 + (row0 + rb) * a.rowbytes) & 15);
                 }
                 mv8_stage<FMT>(slot + ra * F::RS + la, slot + rb * F::RS + lb, c, xb, acc[t]);
             }

@@ -289,12 +289,11 @@ def test_gemv_group_launches_once_per_step():
 
 
 # The batch-1 float matvec on the CUDA cores (mv1): taken for B = 1, float
-# mode, K % 256 == 0. Ragged row counts (not a multiple of the 16-row item),
-# K pieces of 2048 with a partial last piece, q6_K rows that are not a
-# multiple of 16 bytes (K / 256 not a multiple of 8: rows start at any even
-# offset), more items than warps in the grid, fp32 and bf16 activations.
-MV1_SHAPES = [("q6_K", 37, 2048), ("q6_K", 2053, 4096), ("q6_K", 300, 8192),
-              ("q6_K", 61, 11008), ("q6_K", 33, 768), ("q6_K", 4099, 11008), ("q6_K", 3, 256),
+# mode, K % 256 == 0 and rows of whole 16-byte pieces (q6_K: K % 2048 == 0).
+# Ragged row counts (not a multiple of the 4-row item), K pieces of 2048 with
+# a partial last piece, more items than warps in the grid, fp32 and bf16
+# activations.
+MV1_SHAPES = [("q6_K", 37, 2048), ("q6_K", 2053, 4096), ("q6_K", 300, 8192), ("q6_K", 3, 6144),
               ("Q4_0", 1001, 4096), ("Q4_0", 70, 2816), ("Q4_0", 19500, 4096), ("Q4_0", 5, 256),
               ("Q8_0", 515, 4096), ("Q8_0", 33, 768), ("Q8_0", 16, 6144)]
 
@@ -344,10 +343,12 @@ def test_mv1_zero_weights_and_identity_are_exact():
 
 
 # The batch 2-8 float matvec on the warp-level MMA (mv8): taken for 2 <= B <= 8,
-# bf16 activations, float mode, K % 256 == 0. Ragged rows (not a multiple of
-# the 32-row item or of a 16-row MMA tile), activation rows short of 8,
-# q6_K rows at any even offset, more items than warps.
-MV8_SHAPES = [("q6_K", 37, 256), ("q6_K", 2053, 4096), ("q6_K", 61, 11008), ("q6_K", 4100, 11008),
+# bf16 activations, float mode, K % 256 == 0 and rows of whole 16-byte
+# pieces. Ragged rows (not a multiple of the 32-row item or of a 16-row MMA
+# tile), activation rows short of 8, K split over several warps (short N, long
+# K), q6_K super-blocks at every even offset of their 16-byte piece, more
+# items than warps.
+MV8_SHAPES = [("q6_K", 37, 2048), ("q6_K", 2053, 4096), ("q6_K", 61, 16384), ("q6_K", 4100, 6144),
               ("Q4_0", 1001, 4096), ("Q4_0", 70, 2816), ("Q4_0", 13000, 4096), ("Q4_0", 5, 256),
               ("Q8_0", 515, 4096), ("Q8_0", 33, 768)]
 
@@ -379,7 +380,7 @@ def test_mv8_integer_path_bitwise(name):
     """unit scales and integer activations (exact in bf16): the MMA's sums are
     integers below 2^24, so the batch 2-8 matvec equals the exact product"""
     fmt = FMTS[name]
-    N, K, B = 40, 1024, 8
+    N, K, B = 40, 2048, 8
     rng = np.random.default_rng(fmt * 10 + 7)
     W, wint = _unit_scale(fmt, N, K, rng)
     xi = rng.integers(-127, 128, (B, K))
@@ -389,3 +390,18 @@ def test_mv8_integer_path_bitwise(name):
     y = run_gemv(fmt, W, x, N, K)
     assert qmm.liveness()["gemv_mv8"] == 1
     assert np.array_equal(y.astype(np.float64), exact)
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_unaligned_q6k_rows_take_the_tensor_core_matvec(B):
+    """q6_K rows that are not whole 16-byte pieces (K / 256 not a multiple of
+    8) go to the tensor-memory matvec, also at batch 1-8"""
+    N, K = 61, 11008
+    W = synth.matrix(qmm.Q6_K, 900, N, K)
+    x = synth.normal_bf16(901, (B, K))
+    qmm.liveness_reset()
+    y = run_gemv(qmm.Q6_K, W, x, N, K)
+    live = qmm.liveness()
+    assert live["gemv_mv1"] == 0 and live["gemv_mv8"] == 0 and live["gemv_float"] == 1
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+    assert_within(y, ref, absum, f"unaligned q6_K B={B}")
