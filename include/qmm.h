@@ -110,9 +110,10 @@ enum {
  * prints one stderr line per q6_K GEMM launch naming its path, section 2.4),
  * QMM_FAULT ("plane_alloc" makes qmm_plane_wanted's caller-side allocation be
  * treated as failed; host-side fault injection only), QMM_MV1 ("0" sends
- * batch-1 float matvecs to the tensor-core matvec instead of the CUDA-core
- * one), QMM_PDL ("0" launches without programmatic dependent launch). Called
- * implicitly by every entry point; calling it again is a no-op. */
+ * batch-1 float matvecs to the tensor-memory matvec instead of the CUDA-core
+ * one), QMM_MV8 ("0" does the same for batch 2-8 instead of the warp-level
+ * MMA one), QMM_PDL ("0" launches without programmatic dependent launch).
+ * Called implicitly by every entry point; calling it again is a no-op. */
 int qmm_init(void);
 
 /* Sets the CUDA stream (a cudaStream_t, e.g. torch's current stream) that the
@@ -136,11 +137,14 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
  * QMM_ACT_FLOAT: fp32 products and sums of the activations as given.
  * QMM_ACT_Q8: x is first quantized per 32 (needs workspace), then
  *   y = sum_g s_x * d * sc_g * I_g with exact int32 group partials I_g.
- * B = 1 in float mode with K % 256 == 0 runs on the CUDA cores (lanes along
- * K, activations in registers; no workspace, no split); every other case on
- * the tensor cores, where short N is split along K and the partial sums are
- * added in a fixed order by a second launch. Either way the order of the
- * sums is fixed, so results are bitwise reproducible. */
+ * Float mode with rows of whole 16-byte pieces (K % 256 == 0; q6_K K % 2048
+ * == 0): B = 1 runs on the CUDA cores (lanes along K, activations in
+ * registers), B = 2..8 with bf16 x on the warp-level MMA (K split over the
+ * warps of a CTA for short N, added in a fixed order); neither uses
+ * workspace. Every other case runs on the tensor-memory matvec, where short N
+ * is split along K and the partial sums are added in a fixed order by a
+ * second launch. Either way the order of the sums is fixed, so results are
+ * bitwise reproducible. */
 int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
              int64_t K, int B);
 
