@@ -405,3 +405,36 @@ def test_unaligned_q6k_rows_take_the_tensor_core_matvec(B):
     assert live["gemv_mv1"] == 0 and live["gemv_mv8"] == 0 and live["gemv_float"] == 1
     ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
     assert_within(y, ref, absum, f"unaligned q6_K B={B}")
+
+
+def test_fast_paths_opt_out_gate():
+    """QMM_MV1=0 and QMM_MV8=0 (read once per process) send batch 1 and
+    batch 2-8 to the tensor-memory matvec; the results stay within the bound"""
+    import os
+    import subprocess
+    import sys
+    code = r"""
+import numpy as np, torch, sys
+sys.path.insert(0, {root!r})
+import block_quantized_weight_q6_gb300 as qmm, oracle, synth
+N, K = 48, 2048
+W = synth.q6k_matrix(3, N, K)
+Wt = torch.from_numpy(W).cuda()
+for B in (1, 4):
+    x = synth.normal_bf16(4 + B, (B, K))
+    xt = torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16)
+    y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+    qmm.liveness_reset()
+    qmm.gemv(qmm.Q6_K, Wt, xt, y, N, K)
+    torch.cuda.synchronize()
+    live = qmm.liveness()
+    assert live["gemv_mv1"] == 0 and live["gemv_mv8"] == 0 and live["gemv_float"] == 1, live
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+    assert (np.abs(y.cpu().numpy() - ref) <= 1e-4 * absum + 1e-6).all()
+print("gate ok")
+"""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, QMM_MV1="0", QMM_MV8="0")
+    r = subprocess.run([sys.executable, "-c", code.format(root=root)], env=env, capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and "gate ok" in r.stdout, r.stdout + r.stderr
