@@ -303,9 +303,9 @@ __device__ __forceinline__ uint32_t mv1_lead(const Mv1Mat& a, int64_t row, int p
 }
 
 // This lane's 16-byte copies of a full stage (RC rows x a full piece): the
-// shared-memory destinations are compile-time offsets, the source offsets
-// from the stage's first byte depend on the row pitch only (kMv1CopyMax
-// copies at most; unused entries are -1).
+// source offsets from the stage's first byte depend on the row pitch only,
+// so they are computed once per matrix (N copies at most; unused entries are
+// -1).
 template <int FMT>
 struct Mv1Copies {
     static constexpr int CPR = Mv1F<FMT>::PB / 16;
