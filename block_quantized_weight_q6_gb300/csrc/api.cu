@@ -434,17 +434,18 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
 }
 
 // ---------------------------------------------------------------- batch 1-8 matvecs
-// Float mode with K % 256 == 0 and rows of whole 16-byte pieces (Q4_0, Q8_0;
-// q6_K with K % 2048 == 0): one activation row goes to the CUDA-core matvec
-// (mv1.cuh), 2..8 bf16 rows to the warp-level MMA matvec (mv8.cuh). Other
-// rows (q6_K rows of 210 * K / 256 bytes start at any even offset) went
-// faster through the tensor-memory matvec's 8-row tensor map, as does
-// everything with QMM_MV1=0 / QMM_MV8=0.
+// Float mode with K % 256 == 0: one activation row goes to the CUDA-core
+// matvec (mv1.cuh) when rows are whole 16-byte pieces (Q4_0, Q8_0; q6_K with
+// K % 2048 == 0: other q6_K rows, 210 * K / 256 bytes, start at any even
+// offset and went faster through the tensor-memory matvec's 8-row tensor
+// map); 2..8 bf16 rows go to the warp-level MMA matvec (mv8.cuh). QMM_MV1=0
+// / QMM_MV8=0 send them to the tensor-memory matvec instead.
 enum { FAST_NONE = 0, FAST_MV1 = 1, FAST_MV8 = 8 };
 
 int fast_path(int wf, bool q8, bool bf16, int B, int64_t K) {
-    if (q8 || K % block_elems(wf) != 0 || (K / block_elems(wf) * block_bytes(wf)) % 16 != 0) return FAST_NONE;
-    if (B == 1 && g_env.mv1_on && mv1_supported(wf, K)) return FAST_MV1;
+    if (q8 || K % block_elems(wf) != 0) return FAST_NONE;
+    const bool rows16 = (K / block_elems(wf) * block_bytes(wf)) % 16 == 0;
+    if (B == 1 && rows16 && g_env.mv1_on && mv1_supported(wf, K)) return FAST_MV1;
     if (B >= 2 && B <= 8 && bf16 && g_env.mv8_on && mv8_supported(wf, K)) return FAST_MV8;
     return FAST_NONE;
 }
@@ -625,7 +626,16 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
             return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set",
                         p.ws_total, t_ws_bytes);
     }
-    if (nmv > 0 && (rc = run_fast(path, wf, bf16, B, nmv, mv, W, x, y, N, K, d))) return rc;
+    // one launch per K, so that each gets the K split its own items need
+    for (int i = 0; i < nmv; ++i) {
+        bool first = true;
+        for (int j = 0; j < i; ++j) first = first && K[mv[j]] != K[mv[i]];
+        if (!first) continue;
+        int sel[kTcMaxMats], ns = 0;
+        for (int j = i; j < nmv; ++j)
+            if (K[mv[j]] == K[mv[i]]) sel[ns++] = mv[j];
+        if ((rc = run_fast(path, wf, bf16, B, ns, sel, W, x, y, N, K, d))) return rc;
+    }
     if (nrest > 0) return run_gemv_group(wf, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, static_cast<uint8_t*>(t_ws), d);
     return QMM_OK;
 }

@@ -269,23 +269,38 @@ __device__ __forceinline__ void mv8_issue(const Mv1Group& g, const Mv8Cursor& c,
         }
         return;
     }
-    // q6_K (rows of whole 16-byte pieces, so every row of the stage starts
-    // its super-block at the same offset): the 14 16-byte pieces from the
-    // boundary below it; only the matrix's last super-block can end inside
-    // its last piece, and is read up to the matrix's end
+    // q6_K: the 14 16-byte pieces from the boundary below each row's
+    // super-block (rows of whole 16-byte pieces share one start offset);
+    // only the matrix's last super-block can end inside its last piece, and
+    // is read up to the matrix's end
     constexpr int NP = 14;
-    const uint8_t* start = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(base) & ~uintptr_t{15});
     const bool tail = rows == static_cast<int>(a.N - row0) && c.p + 1 == a.pieces;
     const uint8_t* end = a.W + a.N * a.rowbytes;
+    if (a.aligned) {
+        const uint8_t* start = reinterpret_cast<const uint8_t*>(reinterpret_cast<uintptr_t>(base) & ~uintptr_t{15});
 #pragma unroll
-    for (int i = 0; i < (kMv8RB * NP + 31) / 32; ++i) {
-        const int q = lane + 32 * i;
-        const int r = q / NP, cc = q % NP;
-        if (r >= rows) continue;
-        const uint8_t* s16 = start + r * a.rowbytes + 16 * cc;
-        const uint32_t dst = slot + static_cast<uint32_t>(r * F::RS + 16 * cc);
-        if (!tail || s16 + 16 <= end) cp_async16(dst, s16);
-        else if (s16 < end) cp_async16_part(dst, s16, static_cast<uint32_t>(end - s16));
+        for (int i = 0; i < (kMv8RB * NP + 31) / 32; ++i) {
+            const int q = lane + 32 * i;
+            const int r = q / NP, cc = q % NP;
+            if (r >= rows) continue;
+            const uint8_t* s16 = start + r * a.rowbytes + 16 * cc;
+            const uint32_t dst = slot + static_cast<uint32_t>(r * F::RS + 16 * cc);
+            if (!tail || s16 + 16 <= end) cp_async16(dst, s16);
+            else if (s16 < end) cp_async16_part(dst, s16, static_cast<uint32_t>(end - s16));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < (kMv8RB * NP + 31) / 32; ++i) {
+            const int q = lane + 32 * i;
+            const int r = q / NP, cc = q % NP;
+            if (r >= rows) continue;
+            const uint8_t* start = reinterpret_cast<const uint8_t*>(
+                reinterpret_cast<uintptr_t>(base + r * a.rowbytes) & ~uintptr_t{15});
+            const uint8_t* s16 = start + 16 * cc;
+            const uint32_t dst = slot + static_cast<uint32_t>(r * F::RS + 16 * cc);
+            if (!tail || s16 + 16 <= end) cp_async16(dst, s16);
+            else if (s16 < end) cp_async16_part(dst, s16, static_cast<uint32_t>(end - s16));
+        }
     }
 }
 
@@ -385,10 +400,10 @@ __global__ void __launch_bounds__(kMv8Warps * 32, 1) mv8_kernel(const __grid_con
                 const int ra = 16 * t + gr, rb = ra + 8;
                 uint32_t la = 0, lb = 0;
                 if constexpr (FMT == FMT_Q6_K) {
-                    // offset of the super-block in its first 16-byte piece
-                    // (the same for every row: rows are whole 16-byte pieces)
-                    la = lb = static_cast<uint32_t>(
-                        (reinterpret_cast<uintptr_t>(a.W) + static_cast<int64_t>(p) * F::PB) & 15);
+                    // offset of each row's super-block in its first 16-byte piece
+                    const uintptr_t w0 = reinterpret_cast<uintptr_t>(a.W) + static_cast<int64_t>(p) * F::PB;
+                    la = static_cast<uint32_t>((w0 + (row0 + ra) * a.rowbytes) & 15);
+                    lb = static_cast<uint32_t>((w0 + (row0 + rb) * a.rowbytes) & 15);
                 }
                 mv8_stage<FMT>(slot + ra * F::RS + la, slot + rb * F::RS + lb, c, xb, acc[t]);
             }

@@ -343,12 +343,13 @@ def test_mv1_zero_weights_and_identity_are_exact():
 
 
 # The batch 2-8 float matvec on the warp-level MMA (mv8): taken for 2 <= B <= 8,
-# bf16 activations, float mode, K % 256 == 0 and rows of whole 16-byte
-# pieces. Ragged rows (not a multiple of the 32-row item or of a 16-row MMA
-# tile), activation rows short of 8, K split over several warps (short N, long
-# K), q6_K super-blocks at every even offset of their 16-byte piece, more
-# items than warps.
+# bf16 activations, float mode, K % 256 == 0. Ragged rows (not a multiple of
+# the 32-row item or of a 16-row MMA tile), activation rows short of 8, K
+# split over several warps (short N, long K), q6_K super-blocks at every even
+# offset of their 16-byte piece, q6_K rows that are not whole 16-byte pieces
+# (each row at its own offset), more items than warps.
 MV8_SHAPES = [("q6_K", 37, 2048), ("q6_K", 2053, 4096), ("q6_K", 61, 16384), ("q6_K", 4100, 6144),
+              ("q6_K", 61, 11008), ("q6_K", 33, 768), ("q6_K", 4099, 11008),
               ("Q4_0", 1001, 4096), ("Q4_0", 70, 2816), ("Q4_0", 13000, 4096), ("Q4_0", 5, 256),
               ("Q8_0", 515, 4096), ("Q8_0", 33, 768)]
 
@@ -392,19 +393,39 @@ def test_mv8_integer_path_bitwise(name):
     assert np.array_equal(y.astype(np.float64), exact)
 
 
-@pytest.mark.parametrize("B", [1, 4])
-def test_unaligned_q6k_rows_take_the_tensor_core_matvec(B):
+def test_unaligned_q6k_rows_at_batch_1_take_the_tensor_core_matvec():
     """q6_K rows that are not whole 16-byte pieces (K / 256 not a multiple of
-    8) go to the tensor-memory matvec, also at batch 1-8"""
+    8) go to the tensor-memory matvec at batch 1 (to the warp-level MMA at
+    batch 2-8, above)"""
     N, K = 61, 11008
     W = synth.matrix(qmm.Q6_K, 900, N, K)
-    x = synth.normal_bf16(901, (B, K))
+    x = synth.normal_bf16(901, (1, K))
     qmm.liveness_reset()
     y = run_gemv(qmm.Q6_K, W, x, N, K)
     live = qmm.liveness()
     assert live["gemv_mv1"] == 0 and live["gemv_mv8"] == 0 and live["gemv_float"] == 1
     ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
-    assert_within(y, ref, absum, f"unaligned q6_K B={B}")
+    assert_within(y, ref, absum, "unaligned q6_K B=1")
+
+
+def test_group_makes_one_fast_launch_per_k():
+    """a grouped batch-8 call over matrices of two K (one of them with rows
+    that are not whole 16-byte pieces) makes one warp-MMA launch per K"""
+    shapes = [(100, 4096), (70, 11008), (40, 4096)]
+    Ws = [synth.matrix(qmm.Q6_K, 950 + i, N, K) for i, (N, K) in enumerate(shapes)]
+    xs = [synth.normal_bf16(960 + i, (8, K)) for i, (N, K) in enumerate(shapes)]
+    ys = [torch.full((8, N), float("nan"), dtype=torch.float32, device="cuda") for N, K in shapes]
+    grp = qmm.GemvGroup(qmm.Q6_K, [dev(W) for W in Ws], [x_tensor(x) for x in xs], ys,
+                        [N for N, K in shapes], [K for N, K in shapes], qmm.ACT_FLOAT)
+    qmm.liveness_reset()
+    qmm.gemv_group(grp)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    live = qmm.liveness()
+    assert live["gemv_mv8"] == 2 and live["gemv_float"] == 0
+    for (N, K), W, x, y in zip(shapes, Ws, xs, ys):
+        ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+        assert_within(y.cpu().numpy(), ref, absum, f"group per K {N}x{K}")
 
 
 def test_fast_paths_opt_out_gate():
