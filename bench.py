@@ -619,7 +619,7 @@ def main():
     tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
     seg = {
         "decode": {"bound": "hbm", "achieved": dec.algo_bytes / (ms_dec * 1e-3) / 1e9, "peak": hbm,
-                   "unit": "GB/s", "kernel": "mv1_kernel (batch 1, CUDA cores) + tcmv_kernel (batch 8, tensor cores) + split-K reduce, decode set: part time over all launches"},
+                   "unit": "GB/s", "kernel": "mv1_kernel (batch 1, CUDA cores) + mv8_kernel (batch 8, warp-level MMA) + tcmv_kernel and split-K reduce (q6_K ffn_down at batch 1), decode set: part time over all launches"},
         "gemm_exp_plane": {"bound": "tensor", "achieved": tops["gemm_exp_plane"], "peak": tc_peak,
                            "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, plane> + quantize"},
         "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,
