@@ -352,6 +352,20 @@ def oracle_decode_sample(budget_s: float, batch: int = 1, seed_base: int = 0):
     return done_bytes, t_used, desc
 
 
+def step_config(world):
+    """The workload of a step, as both arms report it."""
+    return {"workload": "decode GEMV set (batch 1 and 8, bf16 x, float mode) + q6_K "
+                        "ffn_down prefill GEMM (M=512, plane and in-kernel) + routed "
+                        "MoE (256 Q4_0 experts, top-8, T=1 and 16)",
+            "value_is": "decode-set weight bytes / decode time",
+            "matrices": [f"{n} {f} {N}x{K}" for (n, f, N, K) in DECODE_SET],
+            "batches": list(BATCHES),
+            "weight_bytes_per_step": sum(weight_bytes(f, N, K) for _ in BATCHES for (_, f, N, K) in DECODE_SET),
+            "l2": "flushed before each part (256 MB write, then a 256 MB read that evicts the written "
+                  "lines; both outside the part's events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle as it stands, on the host cores."""
     if rank != 0:
@@ -370,7 +384,7 @@ def run_reference(args, world, rank):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode GEMV set sample (CPU oracle)", "batch": 1},
+            "config": step_config(world),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -654,14 +668,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": "decode GEMV set (batch 1 and 8, bf16 x, float mode) + q6_K "
-                                   "ffn_down prefill GEMM (M=512, plane and in-kernel) + routed "
-                                   "MoE (256 Q4_0 experts, top-8, T=1 and 16)",
-                       "value_is": "decode-set weight bytes / decode time",
-                       "matrices": [f"{n} {f} {N}x{K}" for (n, f, N, K) in DECODE_SET],
-                       "batches": list(BATCHES), "weight_bytes_per_step": dec.weight_bytes,
-                       "l2": "flushed before each part (256 MB write, then a 256 MB read that evicts the written lines; both outside the part's events)",
-                       "parallelism": f"replicas x{world}"},
+            "config": step_config(world),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": dec.h2d,
