@@ -315,41 +315,153 @@ def time_graph(torch, g, steps, device):
 
 # ------------------------------------------------------------------ CPU baseline
 
-def oracle_decode_sample(budget_s: float, batch: int = 1, seed_base: int = 0):
-    """The oracle on a bounded sample of the decode set: leading rows of each
-    matrix at batch `batch`, until budget_s seconds of CPU work. Returns
+def host_threads():
+    """Host cores the oracle legs use (ctypes releases the GIL during each
+    oracle call, so Python threads run the C oracle in parallel)."""
+    return max(1, os.cpu_count() or 1)
+
+
+def _run_tasks(tasks, fn, budget_s, threads):
+    """Runs fn(task) over tasks on `threads` host threads, in rounds of
+    `threads` tasks, until the tasks or the time budget run out. Returns the
+    results of the tasks done and the wall time."""
+    from concurrent.futures import ThreadPoolExecutor
+    done = []
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        for i in range(0, len(tasks), threads):
+            done += list(ex.map(fn, tasks[i:i + threads]))
+            if time.perf_counter() - t0 >= budget_s:
+                break
+    return done, time.perf_counter() - t0
+
+
+def oracle_decode_sample(budget_s: float, threads: int, batch: int = 1):
+    """The oracle on a bounded sample of the decode set, without a GPU:
+    leading rows of each matrix at batch `batch` (inputs drawn on the host
+    with the bench's seeds), until budget_s seconds of wall time. Returns
     (weight bytes processed, seconds, description)."""
     import oracle
     import synth
-    done_bytes, t_used, rows_done = 0, 0.0, []
-    chunk = 64
     mats = []
     for mid, (name, fmt, N, K) in enumerate(DECODE_SET):
         e, b = BLOCK[fmt]
-        rows = min(N, 256)
+        rows = min(N, 64 * threads)
         W = synth.matrix(FMT_CODE[fmt], synth.workload_seed(1, 32 * batch + mid), rows, K)
         x = synth.normal_bf16(synth.workload_seed(1, 64 + 8 * batch + mid), (batch, K))
-        mats.append((name, fmt, rows, K, W, x, (K // e) * b))
-    while t_used < budget_s:
-        progressed = False
-        for (name, fmt, rows, K, W, x, rb) in mats:
-            for r0 in range(0, rows, chunk):
-                r1 = min(rows, r0 + chunk)
-                Wr = W[r0 * rb:r1 * rb]
-                t0 = time.perf_counter()
-                oracle.gemv_float(FMT_CODE[fmt], Wr, x, r1 - r0, K)
-                t_used += time.perf_counter() - t0
-                done_bytes += (r1 - r0) * rb
-                progressed = True
-                if t_used >= budget_s:
-                    break
-            if t_used >= budget_s:
-                break
-        if not progressed:
-            break
-    desc = (f"oracle float matvec (fp64, 1 thread) over leading rows of each decode-set matrix, "
-            f"batch {batch}, {done_bytes / 1e6:.1f} MB of weights in {t_used:.1f} s")
-    return done_bytes, t_used, desc
+        mats.append((fmt, K, W, x, (K // e) * b, rows))
+    tasks = [(m, r0) for r0 in range(0, 64 * threads, 64) for m in range(len(mats)) if r0 < mats[m][5]]
+
+    def one(task):
+        fmt, K, W, x, rb, rows = mats[task[0]]
+        r1 = min(rows, task[1] + 64)
+        oracle.gemv_float(FMT_CODE[fmt], W[task[1] * rb:r1 * rb], x, r1 - task[1], K)
+        return (r1 - task[1]) * rb
+
+    done, t = _run_tasks(tasks, one, budget_s, threads)
+    nbytes = sum(done)
+    desc = (f"oracle float matvec (fp64) over leading 64-row blocks of each decode-set matrix, batch {batch}, "
+            f"{threads} host threads: {nbytes / 1e6:.1f} MB of weights in {t:.1f} s")
+    return nbytes, t, desc
+
+
+def _bf16_host(t):
+    return t.view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+
+
+def _worst(got, ref, bound):
+    """largest |got - ref| / bound over the samples (<= 1 passes; nan or inf fails)"""
+    r = np.abs(np.asarray(got, np.float64) - ref) / bound
+    return float(np.nan_to_num(r, nan=np.inf).max()) if r.size else 0.0
+
+
+def oracle_leg(dec, gem, moe1, moe16, moe_w, budget_s, threads):
+    """Before the timed region (rank 0): the oracle on bounded samples of
+    every part of the step, compared with the outputs of the parts' own last
+    run (the warm-up replays of their graphs), and timed on the host cores.
+    Returns (parity record, cpu_baseline record)."""
+    import oracle
+    torch = dec.torch
+    parity, rates = {}, {}
+
+    # decode: 64-row blocks of every matvec (all its batch rows), round-robin
+    items = []
+    for (name, fmt, N, K, B, Wt, xt, yt) in dec.items:
+        e, bb = BLOCK[fmt]
+        rb = (K // e) * bb
+        rows = min(N, 64 * threads)
+        items.append((name, FMT_CODE[fmt], K, B, rb, Wt[:rows * rb].cpu().numpy(), _bf16_host(xt),
+                      yt[:, :rows].cpu().numpy(), rows))
+    tasks = [(i, r0) for r0 in range(0, 64 * threads, 64) for i in range(len(items)) if r0 < items[i][8]]
+
+    def dec_one(task):
+        name, f, K, B, rb, W, x, y, rows = items[task[0]]
+        r0, r1 = task[1], min(rows, task[1] + 64)
+        ref, absum = oracle.gemv_float(f, W[r0 * rb:r1 * rb], x, r1 - r0, K)
+        return (r1 - r0) * rb * B, _worst(y[:, r0:r1], ref, 1e-4 * absum + 1e-6), (r1 - r0) * B
+
+    done, t = _run_tasks(tasks, dec_one, 0.45 * budget_s, threads)
+    parity["decode"] = {"outputs": sum(d[2] for d in done), "max_err_over_bound": max(d[1] for d in done)}
+    rates["decode"] = {"value": sum(d[0] for d in done) / t / 1e9, "unit": "GB/s",
+                       "sample": f"oracle float matvec on 64-row blocks of every decode-set matvec "
+                                 f"(weight bytes x batch rows), {len(done)} blocks in {t:.1f} s"}
+
+    # GEMM: sampled outputs of both variants (bitwise equal to each other)
+    W = gem.W.cpu().numpy()
+    xq, sx = oracle.quantize_q8(_bf16_host(gem.X))
+    Y1, Y2 = gem.Y1.cpu().numpy(), gem.Y2.cpu().numpy()
+    rng = np.random.default_rng(11)
+    ms, ns = rng.integers(0, gem.M, 64 * 4096), rng.integers(0, gem.N, 64 * 4096)
+
+    def gemm_one(i):
+        sl = slice(64 * i, 64 * i + 64)
+        ref, absum = oracle.gemm_q8_pairs(FMT_CODE["q6_K"], W, gem.K, xq, sx, ms[sl], ns[sl])
+        b = 1e-4 * absum + 1e-6
+        return 64, max(_worst(Y1[ms[sl], ns[sl]], ref, b), _worst(Y2[ms[sl], ns[sl]], ref, b))
+
+    done, t = _run_tasks(list(range(4096)), gemm_one, 0.25 * budget_s, threads)
+    n = sum(d[0] for d in done)
+    parity["gemm"] = {"outputs": n, "max_err_over_bound": max(d[1] for d in done),
+                      "plane_vs_in_kernel_bitwise_equal": bool(np.array_equal(Y1.view(np.uint32),
+                                                                              Y2.view(np.uint32)))}
+    rates["gemm"] = {"value": 2.0 * gem.K * n / t / 1e12, "unit": "TOPS",
+                     "sample": f"oracle q8 dot products of {n} sampled outputs of the ffn_down "
+                               f"prefill in {t:.1f} s"}
+
+    # MoE: whole tokens through the oracle's expert FFN (the selected experts only)
+    dummy = np.zeros(18, np.uint8)
+    jobs = [(moe1, 0), (moe16, 0), (moe16, moe16.T - 1)]
+    host = {}
+    for case, tk in jobs:
+        idx = case.idx.cpu().numpy()
+        for e in idx[tk]:
+            e = int(e)
+            if e not in host:
+                host[e] = (moe_w.g[e].cpu().numpy(), moe_w.u[e].cpu().numpy(), moe_w.d[e].cpu().numpy())
+
+    def moe_one(job):
+        case, tk = job
+        idx = case.idx.cpu().numpy()[tk:tk + 1]
+        gate = case.gate.cpu().numpy()[tk:tk + 1].astype(np.float64)
+        wg = [host[e][0] if e in host else dummy for e in range(moe_w.E)]
+        wu = [host[e][1] if e in host else dummy for e in range(moe_w.E)]
+        wd = [host[e][2] if e in host else dummy for e in range(moe_w.E)]
+        ref, bound = oracle.moe_float(FMT_CODE["Q4_0"], moe_w.H, moe_w.I, wg, wu, wd, idx, gate,
+                                      _bf16_host(case.x)[tk:tk + 1])
+        return _worst(case.y[tk].cpu().numpy(), ref[0], bound[0]), idx.size * case.expert_bytes
+
+    done, t = _run_tasks(jobs, moe_one, float("inf"), threads)
+    parity["moe_t1"] = {"tokens": 1, "max_err_over_bound": done[0][0]}
+    parity["moe_t16"] = {"tokens": 2, "max_err_over_bound": max(done[1][0], done[2][0])}
+    rates["moe"] = {"value": sum(d[1] for d in done) / t / 1e9, "unit": "GB/s",
+                    "sample": f"oracle expert FFN of 3 whole tokens (8 experts each, weight bytes "
+                              f"per token-expert) in {t:.1f} s"}
+    for v in parity.values():
+        v["ok"] = bool(v["max_err_over_bound"] <= 1.0) and v.get("plane_vs_in_kernel_bitwise_equal", True)
+    cpu = {"value": rates["decode"]["value"], "unit": "GB/s", "cores": threads,
+           "host_cores": os.cpu_count(), "kind": "oracle", "sample": rates["decode"]["sample"],
+           "parts": rates}
+    return parity, cpu
 
 
 def step_config(world):
@@ -373,8 +485,9 @@ def run_reference(args, world, rank):
     per_step = []
     total_bytes = 0
     desc = ""
+    threads = host_threads()
     for i in range(args.warmup + args.steps):
-        b, t, desc = oracle_decode_sample(budget_s=0.5)
+        b, t, desc = oracle_decode_sample(budget_s=0.5, threads=threads)
         if i >= args.warmup:
             per_step.append(t)
             total_bytes += b
@@ -385,8 +498,8 @@ def run_reference(args, world, rank):
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": step_config(world),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                             "host_cores": os.cpu_count(), "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -556,6 +669,14 @@ def main():
             l2_flush()
             g.replay()
     torch.cuda.synchronize(device)
+    qmm.sync_check()
+
+    # the oracle leg, before timing: sampled outputs of every part (from the
+    # warm-up replays) against the oracle, and the oracle's own speed
+    parity, cpu = None, None
+    if rank == 0:
+        parity, cpu = oracle_leg(dec, gem, moe1, moe16, moe_w, args.cpu_budget, host_threads())
+    barrier(world)
 
     # launches of our kernels per step, counted by the kernels themselves
     qmm.liveness_reset()
@@ -649,18 +770,13 @@ def main():
     dominant = max(part_ms, key=part_ms.get)
     roofline = dict(seg[dominant])
     roofline.update({"part": dominant, "traffic": None, "peak_source": pk["source"]})
-    # DRAM bytes (read + write) per expert touched by the MoE part, from the
-    # ncu capture in profiles/moe_mv_q4_0_t16_24experts.md (all five kernels
-    # of one call over 24 experts), scaled to the experts this step touches
+    # DRAM bytes (read + write) per expert touched by the MoE part, from an
+    # ncu capture of one call over 24 experts (all its kernels), scaled to
+    # the experts this step touches
     if dominant in ("moe_t1", "moe_t16"):
         case = moe1 if dominant == "moe_t1" else moe16
         roofline["traffic"] = MOE_DRAM_BYTES_PER_EXPERT * case.distinct
         roofline["traffic_note"] = "scaled from a 24-expert ncu capture by distinct experts"
-
-    cpu = None
-    if rank == 0:
-        b, t, desc = oracle_decode_sample(args.cpu_budget)
-        cpu = {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
 
     if rank == 0:
         line = {
@@ -671,6 +787,7 @@ def main():
             "config": step_config(world),
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": {"value": e2e_gbs, "unit": "GB/s", "h2d_bytes_per_step": dec.h2d,
                     "d2h_bytes_per_step": dec.d2h},
             "gpu_launches": launches_per_step * args.steps,

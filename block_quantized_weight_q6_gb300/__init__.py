@@ -72,6 +72,7 @@ def _load():
         "qmm_liveness_read": (I, [C.POINTER(C.c_int64), I]),
         "qmm_liveness_reset": (I, []),
         "qmm_sync_check": (I, []),
+        "qmm_wait_probe": (I, [U32]),
         "qmm_last_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -276,3 +277,13 @@ def liveness_reset():
 
 def sync_check():
     _check(lib.qmm_sync_check())
+
+
+def wait_probe(limit_us: int, device=None):
+    """Launches the bounded-wait probe (a wait that must give up after
+    limit_us microseconds) on torch's current stream."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    _prepare(dev, 0)
+    with torch.cuda.device(dev):
+        _check(lib.qmm_wait_probe(limit_us))

@@ -962,6 +962,18 @@ int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64
     return run_gemv(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(scratch), d);
 }
 
+int qmm_wait_probe(uint32_t limit_us) {
+    qmm_init();
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(QMM_EINVAL, "limit_us = %u outside 1..1000000", limit_us);
+    DevInfo* d;
+    int rc = dev_info(&d);
+    if (rc) return rc;
+    cudaError_t e = wait_probe_launch(static_cast<unsigned long long>(limit_us) * 1000ull, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "wait probe launch");
+    return QMM_OK;
+}
+
 const char* qmm_last_error(void) { return t_err; }
 
 }  // extern "C"

@@ -173,6 +173,10 @@ struct ActTileSet {
 };
 cudaError_t act_tile_set_launch(const ActTileSet& r, cudaStream_t s, DevState st);
 
+// one warp that waits on an mbarrier nothing completes, giving up after
+// limit_ns (test aid for the bounded waits; tcmv.cu)
+cudaError_t wait_probe_launch(unsigned long long limit_ns, cudaStream_t s, DevState st);
+
 // ---------------------------------------------------------------- quantizer
 // x [rows][K] (fp32 or bf16) -> xq [rows][K] int8, xs [rows][K/32] fp32.
 // If a16 != nullptr, also writes the quantized values as fp16 in the GEMM's

@@ -9,6 +9,7 @@
 
 #include "kernels.h"
 #include "quant.cuh"
+#include "tcmv.cuh"
 
 namespace qmm {
 
@@ -256,6 +257,31 @@ cudaError_t act_tile_launch(const void* x, int x_bf16, int B, int64_t K, int fmt
                                dim3(threads), 0, s, x, x_bf16, B, K, fmt, NB, S, ncol, nst,
                                q8 ? 1 : 0, xt, xs, st);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ------------------------------------------------------------ wait probe
+// Test aid for the bounded waits: one warp waits, through the matvec's own
+// warp-collective wait, on an mbarrier that nothing ever completes. After
+// limit_ns of %globaltimer the wait gives up, raises the CTA's abort flag and
+// the timeout bit of the error word, and the kernel returns. Nothing else is
+// in flight in this kernel (no copies, no tensor memory), so the context
+// stays usable and the next call runs normally.
+__global__ void wait_probe_kernel(DevState st, unsigned long long limit_ns) {
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ uint32_t flag;
+    const uint32_t b = smem_u32(&bar), f = smem_u32(&flag);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(f), "r"(0u) : "memory");
+        fence_mbar_init();
+    }
+    __syncwarp();
+    (void)tcmv_wait_warp(b, 0, f, st.err, limit_ns);
+}
+
+cudaError_t wait_probe_launch(unsigned long long limit_ns, cudaStream_t s, DevState st) {
+    wait_probe_kernel<<<1, 32, 0, s>>>(st, limit_ns);
+    return cudaGetLastError();
 }
 
 }  // namespace qmm

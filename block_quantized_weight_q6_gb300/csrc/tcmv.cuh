@@ -201,14 +201,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // up; every lane leaves with the same answer (the tensor-memory operations
 // that follow are .sync.aligned).
 __device__ __forceinline__ bool tcmv_wait_warp(uint32_t bar, uint32_t parity, uint32_t flag,
-                                               unsigned int* err) {
+                                               unsigned int* err,
+                                               unsigned long long limit_ns = kWaitLimitNs) {
     if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
     const unsigned long long t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (__all_sync(0xffffffffu, mbar_try_wait_sleep(bar, parity))) return true;
         if ((it & 3u) == 0) {
             int give_up = lds_u32(flag) != 0 ? 1 : 0;
-            if (!give_up && globaltimer_ns() - t0 > kWaitLimitNs) give_up = 2;
+            if (!give_up && globaltimer_ns() - t0 > limit_ns) give_up = 2;
             give_up = __shfl_sync(0xffffffffu, give_up, 0);
             if (give_up) {
                 if (give_up == 2 && (threadIdx.x & 31) == 0) {

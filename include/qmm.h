@@ -132,7 +132,10 @@ int qmm_set_workspace(void* dev, size_t bytes);
  * these sizes; 0 if none. */
 size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
 
-/* Batched decode matvec, y[b][n] = sum_k w[n][k] * x[b][k], b < B <= 16.
+/* Batched decode matvec, y[b][n] = sum_k w[n][k] * x[b][k], b < B <= 16:
+ * the fused dequantize-and-multiply of quantprobe "LAWS.md", Law 4 and its
+ * amendment L-15 (decode reads every weight once per token; the format's
+ * unpack work, not its bit width, sets the cost).
  * x: [B][K] fp32 or bf16 (fmt bits), y: [B][N] fp32 (overwritten).
  * QMM_ACT_FLOAT: fp32 products and sums of the activations as given.
  * QMM_ACT_Q8: x is first quantized per 32 (needs workspace), then
@@ -170,8 +173,8 @@ size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, con
 /* Size of the fixed scratch array that qmm_gemv_noalloc uses (4 MiB). */
 #define QMM_NOALLOC_SCRATCH_BYTES (4u << 20)
 
-/* The same batched matvec as qmm_gemv (same arguments, same kernels, same
- * results), for callers that cannot allocate device memory when they call:
+/* The batched matvec of qmm_gemv (same arguments, same definition of y),
+ * for callers that cannot allocate device memory when they call:
  * code hosted by an engine or framework that owns all device memory and
  * hands out only the input and output buffers, and latency-critical loops
  * that must not call into an allocator after start-up (cudaMalloc can block
@@ -186,8 +189,13 @@ size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, con
  * QMM_ENOWORKSPACE before anything is launched. Every call uses the same
  * array and leaves its contents behind (each call overwrites what it reads),
  * so two calls that run at the same time on the GPU (e.g. on two streams)
- * race: keep them ordered on one stream. The pages have no counterpart to
- * this entry point. */
+ * race: keep them ordered on one stream. It always runs the tensor-memory
+ * matvec (the kernel that needs scratch), at every batch size, whereas
+ * qmm_gemv sends float-mode batches of 1..8 with K % 256 == 0 to kernels
+ * that use none; the two therefore agree within the float bound
+ * |y - y'| <= 1e-4 * sum_k |w x| + 1e-6, not bitwise (q8 mode and the shapes
+ * that qmm_gemv also sends to the tensor-memory matvec give the same bits).
+ * The pages have no counterpart to this entry point. */
 int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
                      int64_t K, int B);
 
@@ -269,7 +277,10 @@ int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
 size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts);
 
 /* Router helper: per token, the k largest of E fp32 logits (ties go to the
- * lower expert index) and their softmax over those k. logits: [T][E],
+ * lower expert index) and their softmax over those k, the routing of the
+ * 256-expert top-8 layer whose selected experts "Chasing x100" (section
+ * "Where the wall actually fell: inversion") keeps resident and decodes in
+ * place; softmax over the k selected logits, so the k gates sum to 1. logits: [T][E],
  * idx: [T][k] int32, gate_w: [T][k] fp32. E <= 1024, k <= 32. */
 int qmm_route_topk_softmax(const float* logits, int T, int E, int k, int32_t* idx,
                            float* gate_w);
@@ -283,6 +294,15 @@ int qmm_liveness_reset(void);
  * last check (the flags are cleared): QMM_EDEVICE_TIMEOUT if a kernel gave up
  * a bounded wait, QMM_EINVAL if moe_gemv met an expert index out of range. */
 int qmm_sync_check(void);
+
+/* Test aid for the bounded device waits: launches one warp that waits,
+ * through the same warp-collective bounded wait as the tensor-memory matvec,
+ * on an mbarrier that nothing ever completes. After limit_us microseconds
+ * (1..1000000) the wait gives up and sets the timeout bit of the error word,
+ * so the next qmm_sync_check returns QMM_EDEVICE_TIMEOUT (and clears it);
+ * the kernel holds no copies or tensor memory, so the context stays usable.
+ * The pages have no counterpart to this entry point. */
+int qmm_wait_probe(uint32_t limit_us);
 
 /* Reason for the calling thread's last non-OK return. */
 const char* qmm_last_error(void);

@@ -269,3 +269,38 @@ def test_q6k_gemm_scale_range():
     qmm.sync_check()
     ref, absum = oracle.gemv_float(qmm.Q6_K, Wbig, x1, N, K)
     assert_within(y.cpu().numpy(), ref, absum, "q6_K matvec, scale 100")
+
+
+# The 32-layer prefill sweep's GEMM shapes (7B-shaped layer: Q4_0 wq/wk/wo
+# 4096 x 4096, w1/w3 11008 x 4096; q6_K attn_v 4096 x 4096 and the output
+# matrix 32000 x 4096, both with the plane and with in-kernel expansion; the
+# ffn_down shape is covered above), at the sweep's smallest and largest M.
+SWEEP_SHAPES = [("wq", "Q4_0", 4096, 4096, 0), ("w1", "Q4_0", 11008, 4096, 3),
+                ("attn_v", "q6_K", 4096, 4096, 5), ("output", "q6_K", 32000, 4096, 15)]
+
+
+@pytest.mark.parametrize("M", [128, 2048])
+@pytest.mark.parametrize("name,fmt_name,N,K,mid", SWEEP_SHAPES)
+def test_sweep_shapes_vs_oracle(name, fmt_name, N, K, mid, M):
+    """Weights drawn on the device as the sweep draws them; 512 sampled
+    outputs against the oracle; the q6_K plane and in-kernel outputs bitwise
+    equal over the whole Y."""
+    fmt = {"Q4_0": qmm.Q4_0, "q6_K": qmm.Q6_K}[fmt_name]
+    Wt = synth.matrix_torch(fmt, synth.workload_seed(4, mid), N, K, "cuda")[0]
+    X = synth.normal_bf16(synth.workload_seed(4, 100 + K % 97 + M), (M, K))
+    Y2 = run_gemm(fmt, None, X, N, K, Wt=Wt)
+    if fmt == qmm.Q6_K:
+        plane = qmm.plane_build(Wt, N, K)
+        Y1 = run_gemm(fmt, None, X, N, K, plane=plane, Wt=Wt)
+        qmm.plane_release(Wt)
+        del plane
+        assert np.array_equal(Y1.view(np.uint32), Y2.view(np.uint32)), f"{name} M={M}: variants differ"
+        del Y1
+    assert np.isfinite(Y2).all()
+    W = Wt.cpu().numpy()
+    rng = np.random.default_rng(M + N + mid)
+    ms = np.concatenate([rng.integers(0, M, 508), [0, M - 1, 0, M - 1]])
+    ns = np.concatenate([rng.integers(0, N, 508), [0, N - 1, N - 1, 0]])
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemm_q8_pairs(fmt, W, K, xq, s, ms, ns)
+    assert_within(Y2[ms, ns], ref, absum, f"sweep {name} {N}x{K} M={M}")
