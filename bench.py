@@ -196,19 +196,18 @@ class DecodeSet:
                 self.h2d += 2 * B * K
                 self.d2h += 4 * B * N
 
-        # one grouped matvec call per (batch, format): the set's 18 matvecs in 6 launches
+        # one call per batch size over all formats (one decode step's matvecs)
         self.groups = []
         for B in BATCHES:
-            for fmt in ("Q4_0", "q6_K", "Q8_0"):
-                its = [it for it in self.items if it[4] == B and it[1] == fmt]
-                self.groups.append(qmm.GemvGroup(FMT_CODE[fmt], [it[5] for it in its], [it[6] for it in its],
-                                                 [it[7] for it in its], [it[2] for it in its],
-                                                 [it[3] for it in its], act))
+            its = [it for it in self.items if it[4] == B]
+            self.groups.append(qmm.GemvMulti([FMT_CODE[it[1]] for it in its], [it[5] for it in its],
+                                             [it[6] for it in its], [it[7] for it in its],
+                                             [it[2] for it in its], [it[3] for it in its], act))
 
     def run(self):
-        """The set as grouped calls (the step's decode part)."""
+        """The set as one call per batch size (the step's decode part)."""
         for g in self.groups:
-            self.qmm.gemv_group(g)
+            self.qmm.gemv_multi(g)
 
     def run_per_call(self):
         """The same set as 18 single matvec calls."""
@@ -754,7 +753,8 @@ def main():
     tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
     seg = {
         "decode": {"bound": "hbm", "achieved": dec.algo_bytes / (ms_dec * 1e-3) / 1e9, "peak": hbm,
-                   "unit": "GB/s", "kernel": "mv1_kernel (batch 1, CUDA cores) + mv8_kernel (batch 8, warp-level MMA) + tcmv_kernel and split-K reduce (q6_K ffn_down at batch 1), decode set: part time over all launches"},
+                   "unit": "GB/s", "kernel": "mvh_prep_kernel + mvh_kernel (fp16 warp-level MMA, all formats "
+                                             "of a batch size in one launch), decode set: part time over all launches"},
         "gemm_exp_plane": {"bound": "tensor", "achieved": tops["gemm_exp_plane"], "peak": tc_peak,
                            "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, plane> + quantize"},
         "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,

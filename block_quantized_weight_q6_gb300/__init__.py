@@ -61,6 +61,10 @@ def _load():
         "qmm_gemv_group": (I, [U32, I, C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
                                C.POINTER(C.c_void_p), C.POINTER(C.c_int64), C.POINTER(C.c_int64), I]),
         "qmm_gemv_group_workspace_bytes": (SZ, [U32, I, C.POINTER(C.c_int64), C.POINTER(C.c_int64), I]),
+        "qmm_gemv_multi": (I, [I, C.POINTER(C.c_uint32), C.POINTER(C.c_void_p), C.POINTER(C.c_void_p),
+                               C.POINTER(C.c_void_p), C.POINTER(C.c_int64), C.POINTER(C.c_int64), I]),
+        "qmm_gemv_multi_workspace_bytes": (SZ, [I, C.POINTER(C.c_uint32), C.POINTER(C.c_int64),
+                                                C.POINTER(C.c_int64), I]),
         "qmm_gemm": (I, [U32, P, P, P, I64, I64, I64, P]),
         "qmm_plane_bytes": (SZ, [I64, I64]),
         "qmm_plane_wanted": (I, [I64, I64]),
@@ -182,6 +186,37 @@ def gemv_group(group: GemvGroup):
     with _torch().cuda.device(group.device):
         _check(lib.qmm_gemv_group(group.code, group.n, group._W, group._x, group._y, group._N,
                                   group._K, group.B))
+
+
+class GemvMulti:
+    """A fixed set of matvecs of possibly different weight formats (the same
+    activation type, mode and batch) for gemv_multi: the host arrays of the
+    call, built once (keep the object while it is used)."""
+
+    def __init__(self, fmts, Ws, xs, ys, Ns, Ks, act: int = ACT_FLOAT):
+        n = len(Ws)
+        if not (len(fmts) == len(xs) == len(ys) == len(Ns) == len(Ks) == n):
+            raise ValueError("fmts, Ws, xs, ys, Ns, Ks must have the same length")
+        B = xs[0].shape[0]
+        self.n, self.B, self.device = n, B, xs[0].device
+        self._fmt = (C.c_uint32 * n)(*[f | _act_bits(x) | act for f, x in zip(fmts, xs)])
+        P = C.c_void_p * n
+        L = C.c_int64 * n
+        self._W = P(*[t.data_ptr() for t in Ws])
+        self._x = P(*[t.data_ptr() for t in xs])
+        self._y = P(*[t.data_ptr() for t in ys])
+        self._N = L(*Ns)
+        self._K = L(*Ks)
+        self._keep = (list(Ws), list(xs), list(ys))
+        self.ws = lib.qmm_gemv_multi_workspace_bytes(n, self._fmt, self._N, self._K, B)
+
+
+def gemv_multi(multi: GemvMulti):
+    """y[i] = W[i] x[i] for every matvec of the set (formats may differ)."""
+    _prepare(multi.device, multi.ws)
+    with _torch().cuda.device(multi.device):
+        _check(lib.qmm_gemv_multi(multi.n, multi._fmt, multi._W, multi._x, multi._y, multi._N,
+                                  multi._K, multi.B))
 
 
 def quantize_q8(x, xq, s):

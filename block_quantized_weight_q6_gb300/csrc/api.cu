@@ -58,6 +58,7 @@ struct Env {
     bool fault_plane_alloc = false;
     bool mv1_on = true;
     bool mv8_on = true;
+    bool mvh_on = true;
 };
 Env g_env;
 std::once_flag g_env_once;
@@ -73,6 +74,8 @@ void read_env() {
     g_env.mv1_on = !(mv && std::strcmp(mv, "0") == 0);
     const char* m8 = std::getenv("QMM_MV8");
     g_env.mv8_on = !(m8 && std::strcmp(m8, "0") == 0);
+    const char* mh = std::getenv("QMM_MVH");
+    g_env.mvh_on = !(mh && std::strcmp(mh, "0") == 0);
     const char* pdl = std::getenv("QMM_PDL");
     qmm::g_pdl_enabled = !(pdl && std::strcmp(pdl, "0") == 0);
 }
@@ -434,16 +437,18 @@ int run_gemv_group(int wf, bool q8, bool bf16, const void* const* W, const void*
 }
 
 // ---------------------------------------------------------------- batch 1-8 matvecs
-// Float mode with K % 256 == 0: one activation row goes to the CUDA-core
+// Float mode, K % 256 == 0: bf16 activations, 1..8 rows and N % 8 == 0 go to
+// the fp16-MMA matvec (mvh.cuh), every such matrix of a call in one launch
+// whatever its format. The rest: one fp32 activation row to the CUDA-core
 // matvec (mv1.cuh) when rows are whole 16-byte pieces (Q4_0, Q8_0; q6_K with
-// K % 2048 == 0: other q6_K rows, 210 * K / 256 bytes, start at any even
-// offset and went faster through the tensor-memory matvec's 8-row tensor
-// map); 2..8 bf16 rows go to the warp-level MMA matvec (mv8.cuh). QMM_MV1=0
-// / QMM_MV8=0 send them to the tensor-memory matvec instead.
-enum { FAST_NONE = 0, FAST_MV1 = 1, FAST_MV8 = 8 };
+// K % 2048 == 0); 2..8 bf16 rows whose N is not a multiple of 8 to the
+// bf16 warp-level MMA matvec (mv8.cuh); everything else to the
+// tensor-memory matvec. QMM_MVH=0, QMM_MV1=0, QMM_MV8=0 switch a path off.
+enum { FAST_NONE = 0, FAST_MV1 = 1, FAST_MV8 = 8, FAST_MVH = 16 };
 
-int fast_path(int wf, bool q8, bool bf16, int B, int64_t K) {
+int fast_path(int wf, bool q8, bool bf16, int B, int64_t N, int64_t K) {
     if (q8 || K % block_elems(wf) != 0) return FAST_NONE;
+    if (bf16 && B <= 8 && g_env.mvh_on && mvh_supported(wf, N, K)) return FAST_MVH;
     const bool rows16 = (K / block_elems(wf) * block_bytes(wf)) % 16 == 0;
     if (B == 1 && rows16 && g_env.mv1_on && mv1_supported(wf, K)) return FAST_MV1;
     if (B >= 2 && B <= 8 && bf16 && g_env.mv8_on && mv8_supported(wf, K)) return FAST_MV8;
@@ -499,23 +504,88 @@ int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const vo
     return QMM_OK;
 }
 
-// Splits a group into the matrices that mv1 / mv8 take and the rest; returns
-// how many are taken and the path.
-int fast_partition(int wf, bool q8, bool bf16, int B, int n, const int64_t* K, int* mv, int* rest, int* nrest,
-                   int* path) {
-    int nm = 0;
-    *nrest = 0;
-    *path = FAST_NONE;
+// Workspace of the fp16-MMA matvec for these matrices, as if no two shared
+// their activations (the launch shares equal ones, so it never needs more).
+size_t mvh_ws_bound(int n, const int* sel, const int64_t* K, int B) {
+    size_t t = 0;
+    for (int i = 0; i < n; ++i)
+        t += round_up(static_cast<size_t>(B) * K[sel[i]] * 2, 256) + round_up(static_cast<size_t>(B) * 4, 256);
+    return t;
+}
+
+// A set of matvecs of any formats wf[0 .. n-1] sharing activation type, mode
+// and batch: the fp16-MMA matvec takes every matrix it can, in one launch;
+// per format, the others go to the batch-1 / batch 2-8 kernels (one launch
+// per K, so that each K gets the split its own items need) or to one
+// tensor-memory matvec launch. Workspace regions follow each other in that
+// order. With ws == nullptr nothing is launched and *need is set to the
+// workspace the call needs.
+int gemv_set(int n, const int* wf, bool q8, bool bf16, int B, const void* const* W, const void* const* x,
+             float* const* y, const int64_t* N, const int64_t* K, const DevInfo* d, uint8_t* ws, size_t* need) {
+    int path[kTcMaxMats];
+    int hsel[kTcMaxMats], nh = 0;
     for (int m = 0; m < n; ++m) {
-        const int pth = fast_path(wf, q8, bf16, B, K[m]);
-        if (pth != FAST_NONE) {
-            *path = pth;
-            mv[nm++] = m;
-        } else {
-            rest[(*nrest)++] = m;
-        }
+        path[m] = fast_path(wf[m], q8, bf16, B, N[m], K[m]);
+        if (path[m] == FAST_MVH) hsel[nh++] = m;
     }
-    return nm;
+    size_t off = nh > 0 ? round_up(mvh_ws_bound(nh, hsel, K, B), 256) : 0;
+    if (ws && nh > 0) {
+        cudaError_t e = mvh_run(nh, hsel, wf, W, x, y, N, K, B, ws, d->sms, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "matvec launch");
+    }
+    for (int f : {QMM_Q4_0, QMM_Q8_0, QMM_Q6_K}) {
+        // this format's matrices the batch-1 / batch 2-8 kernels take, one launch per K
+        for (int i = 0; i < n; ++i) {
+            if (wf[i] != f || (path[i] != FAST_MV1 && path[i] != FAST_MV8)) continue;
+            bool first = true;
+            for (int j = 0; j < i; ++j) first = first && !(wf[j] == f && path[j] == path[i] && K[j] == K[i]);
+            if (!first) continue;
+            int sel[kTcMaxMats], ns = 0;
+            for (int j = i; j < n; ++j)
+                if (wf[j] == f && path[j] == path[i] && K[j] == K[i]) sel[ns++] = j;
+            if (ws) {
+                int rc = run_fast(path[i], f, bf16, B, ns, sel, W, x, y, N, K, d);
+                if (rc) return rc;
+            }
+        }
+        // the rest of this format: one tensor-memory matvec launch
+        const void* Wr[kTcMaxMats];
+        const void* xr[kTcMaxMats];
+        float* yr[kTcMaxMats];
+        int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
+        int nr = 0;
+        for (int i = 0; i < n; ++i) {
+            if (wf[i] != f || path[i] != FAST_NONE) continue;
+            Wr[nr] = W ? W[i] : nullptr;
+            xr[nr] = x ? x[i] : nullptr;
+            yr[nr] = y ? y[i] : nullptr;
+            Nr[nr] = N[i];
+            Kr[nr] = K[i];
+            ++nr;
+        }
+        if (nr == 0) continue;
+        GroupPlan p;
+        int rc = plan_gemv_group_cached(f, q8, bf16, B, nr, Nr, Kr, d->sms, &p);
+        if (rc) return rc;
+        if (ws) {
+            rc = run_gemv_group(f, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, ws + off, d);
+            if (rc) return rc;
+        }
+        off = round_up(off + p.ws_total, 256);
+    }
+    *need = off;
+    return QMM_OK;
+}
+
+// Checks the workspace a set needs against the one set, then runs it.
+int gemv_set_run(const char* who, int n, const int* wf, bool q8, bool bf16, int B, const void* const* W,
+                 const void* const* x, float* const* y, const int64_t* N, const int64_t* K, const DevInfo* d) {
+    size_t need = 0;
+    int rc = gemv_set(n, wf, q8, bf16, B, nullptr, nullptr, nullptr, N, K, d, nullptr, &need);
+    if (rc) return rc;
+    if (need > t_ws_bytes || (need && !t_ws))
+        return fail(QMM_ENOWORKSPACE, "%s needs %zu bytes of workspace, %zu set", who, need, t_ws_bytes);
+    return gemv_set(n, wf, q8, bf16, B, W, x, y, N, K, d, static_cast<uint8_t*>(t_ws), &need);
 }
 
 int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, int64_t N,
@@ -530,6 +600,26 @@ int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, 
                                           (long long)K, block_elems(*wf));
     if (!aligned16(W) || !aligned16(x)) return fail(QMM_EALIGN, "W and x must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(y) & 3u) return fail(QMM_EALIGN, "y must be 4-byte aligned");
+    return QMM_OK;
+}
+
+// Arguments of a set of matvecs: formats may differ (multi) or not; the
+// activation type and mode must agree.
+int check_gemv_set(int n, const uint32_t* fmts, uint32_t fmt1, const void* const* W, const void* const* x,
+                   float* const* y, const int64_t* N, const int64_t* K, int B, int* wf, bool* bf16, bool* q8) {
+    if (n < 1 || n > kTcMaxMats) return fail(QMM_EINVAL, "n = %d outside 1..%d", n, kTcMaxMats);
+    if (!W || !x || !y || !N || !K) return fail(QMM_EINVAL, "null array");
+    for (int m = 0; m < n; ++m) {
+        const uint32_t f = fmts ? fmts[m] : fmt1;
+        if (fmts && m > 0 && (f & ~static_cast<uint32_t>(QMM_FMT_MASK)) !=
+                                 (fmts[0] & ~static_cast<uint32_t>(QMM_FMT_MASK)))
+            return fail(QMM_EINVAL, "matvec %d: activation type and mode differ from matvec 0", m);
+        bool b16, aq8;
+        int rc = check_gemv_args(f, W[m], x[m], y[m], N[m], K[m], B, &wf[m], &b16, &aq8);
+        if (rc) return rc;
+        *bf16 = b16;
+        *q8 = aq8;
+    }
     return QMM_OK;
 }
 
@@ -570,96 +660,59 @@ int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N, in
     if (rc) return rc;
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
-    if (const int path = fast_path(wf, q8, bf16, B, K)) {
-        const int sel = 0;
-        return run_fast(path, wf, bf16, B, 1, &sel, &W, &x, &y, &N, &K, d);
-    }
-    GemvPlan p;
-    if ((rc = plan_gemv(wf, q8, bf16, B, N, K, d->sms, &p))) return rc;
-    if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
-        return fail(QMM_ENOWORKSPACE, "qmm_gemv needs %zu bytes of workspace, %zu set", p.ws_total,
-                    t_ws_bytes);
-    return run_gemv(wf, q8, bf16, W, x, y, N, K, B, p, static_cast<uint8_t*>(t_ws), d);
-}
-
-static int check_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const* x,
-                            float* const* y, const int64_t* N, const int64_t* K, int B, int* wf, bool* bf16,
-                            bool* q8) {
-    if (n < 1 || n > kTcMaxMats) return fail(QMM_EINVAL, "n = %d outside 1..%d", n, kTcMaxMats);
-    if (!W || !x || !y || !N || !K) return fail(QMM_EINVAL, "null array");
-    for (int m = 0; m < n; ++m) {
-        int rc = check_gemv_args(fmt, W[m], x[m], y[m], N[m], K[m], B, wf, bf16, q8);
-        if (rc) return rc;
-    }
-    return QMM_OK;
+    return gemv_set_run("qmm_gemv", 1, &wf, q8, bf16, B, &W, &x, &y, &N, &K, d);
 }
 
 int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const* x, float* const* y,
                    const int64_t* N, const int64_t* K, int B) {
     qmm_init();
-    int wf;
-    bool bf16, q8;
-    int rc = check_gemv_group(fmt, n, W, x, y, N, K, B, &wf, &bf16, &q8);
+    int wf[kTcMaxMats];
+    bool bf16 = false, q8 = false;
+    int rc = check_gemv_set(n, nullptr, fmt, W, x, y, N, K, B, wf, &bf16, &q8);
     if (rc) return rc;
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
-    // the matrices the batch-1 matvec takes, in one launch; the rest in one
-    // tensor-core matvec launch
-    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0, path = 0;
-    const int nmv = fast_partition(wf, q8, bf16, B, n, K, mv, rest, &nrest, &path);
-    const void* Wr[kTcMaxMats];
-    const void* xr[kTcMaxMats];
-    float* yr[kTcMaxMats];
-    int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
-    for (int i = 0; i < nrest; ++i) {
-        const int m = rest[i];
-        Wr[i] = W[m];
-        xr[i] = x[m];
-        yr[i] = y[m];
-        Nr[i] = N[m];
-        Kr[i] = K[m];
+    return gemv_set_run("qmm_gemv_group", n, wf, q8, bf16, B, W, x, y, N, K, d);
+}
+
+int qmm_gemv_multi(int n, const uint32_t* fmt, const void* const* W, const void* const* x, float* const* y,
+                   const int64_t* N, const int64_t* K, int B) {
+    qmm_init();
+    int wf[kTcMaxMats];
+    bool bf16 = false, q8 = false;
+    if (!fmt) return fail(QMM_EINVAL, "null fmt array");
+    int rc = check_gemv_set(n, fmt, 0, W, x, y, N, K, B, wf, &bf16, &q8);
+    if (rc) return rc;
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    return gemv_set_run("qmm_gemv_multi", n, wf, q8, bf16, B, W, x, y, N, K, d);
+}
+
+static size_t set_workspace_bytes(int n, const uint32_t* fmts, uint32_t fmt1, const int64_t* N, const int64_t* K,
+                                  int B) {
+    qmm_init();
+    if (n < 1 || n > kTcMaxMats || !N || !K || B < 1 || B > 16) return 0;
+    int wf[kTcMaxMats];
+    bool bf16 = false, q8 = false;
+    for (int m = 0; m < n; ++m) {
+        const uint32_t f = fmts ? fmts[m] : fmt1;
+        if (check_fmt(f, &wf[m], &bf16, &q8)) return 0;
+        if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf[m])) return 0;
     }
-    GroupPlan p;
-    if (nrest > 0) {
-        if ((rc = plan_gemv_group_cached(wf, q8, bf16, B, nrest, Nr, Kr, d->sms, &p))) return rc;
-        if (p.ws_total > t_ws_bytes || (p.ws_total && !t_ws))
-            return fail(QMM_ENOWORKSPACE, "qmm_gemv_group needs %zu bytes of workspace, %zu set",
-                        p.ws_total, t_ws_bytes);
-    }
-    // one launch per K, so that each gets the K split its own items need
-    for (int i = 0; i < nmv; ++i) {
-        bool first = true;
-        for (int j = 0; j < i; ++j) first = first && K[mv[j]] != K[mv[i]];
-        if (!first) continue;
-        int sel[kTcMaxMats], ns = 0;
-        for (int j = i; j < nmv; ++j)
-            if (K[mv[j]] == K[mv[i]]) sel[ns++] = mv[j];
-        if ((rc = run_fast(path, wf, bf16, B, ns, sel, W, x, y, N, K, d))) return rc;
-    }
-    if (nrest > 0) return run_gemv_group(wf, q8, bf16, Wr, xr, yr, Nr, Kr, B, p, static_cast<uint8_t*>(t_ws), d);
-    return QMM_OK;
+    DevInfo* d;
+    if (dev_info(&d)) return 0;
+    size_t need = 0;
+    if (gemv_set(n, wf, q8, bf16, B, nullptr, nullptr, nullptr, N, K, d, nullptr, &need)) return 0;
+    return need;
 }
 
 size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, const int64_t* K, int B) {
-    qmm_init();
-    int wf;
-    bool bf16, q8;
-    if (check_fmt(fmt, &wf, &bf16, &q8) || n < 1 || n > kTcMaxMats || !N || !K || B < 1 || B > 16) return 0;
-    for (int m = 0; m < n; ++m)
-        if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf)) return 0;
-    DevInfo* d;
-    if (dev_info(&d)) return 0;
-    int mv[kTcMaxMats], rest[kTcMaxMats], nrest = 0, path = 0;
-    (void)fast_partition(wf, q8, bf16, B, n, K, mv, rest, &nrest, &path);
-    if (nrest == 0) return 0;
-    int64_t Nr[kTcMaxMats], Kr[kTcMaxMats];
-    for (int i = 0; i < nrest; ++i) {
-        Nr[i] = N[rest[i]];
-        Kr[i] = K[rest[i]];
-    }
-    GroupPlan p;
-    if (plan_gemv_group_cached(wf, q8, bf16, B, nrest, Nr, Kr, d->sms, &p)) return 0;
-    return p.ws_total;
+    return set_workspace_bytes(n, nullptr, fmt, N, K, B);
+}
+
+size_t qmm_gemv_multi_workspace_bytes(int n, const uint32_t* fmt, const int64_t* N, const int64_t* K, int B) {
+    if (!fmt) return 0;
+    return set_workspace_bytes(n, fmt, 0, N, K, B);
 }
 
 int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int8_t* xq,
@@ -866,9 +919,11 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
     if (M_or_B > 16) return gemm;
     DevInfo* d;
     if (dev_info(&d)) return gemm;
-    GemvPlan p;
-    if (plan_gemv(wf, q8, bf16, static_cast<int>(M_or_B), N, K, d->sms, &p)) return gemm;
-    return p.ws_total > gemm ? p.ws_total : gemm;
+    size_t need = 0;
+    if (gemv_set(1, &wf, q8, bf16, static_cast<int>(M_or_B), nullptr, nullptr, nullptr, &N, &K, d, nullptr,
+                 &need))
+        return gemm;
+    return need > gemm ? need : gemm;
 }
 
 int qmm_liveness_read(int64_t* counts, int n) {

@@ -90,6 +90,37 @@ bool mv8_supported(int fmt, int64_t K);
 int mv8_occupancy(int fmt);
 cudaError_t mv8_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
 
+// ---------------------------------------------------------------- batch 1-8 fp16-MMA matvec
+// 1..8 bf16 activation rows, float mode, any mix of the three formats in one
+// launch, on the warp-level MMA with fp16 operands (mvh.cuh): work item = 32
+// rows of one matrix at stride 8, all of its K. Needs K % 256 == 0 and
+// N % 8 == 0, and workspace for the fp16 activations (mvh_workspace_bytes).
+constexpr int kMvhWarps = 8;
+constexpr int kMvhMaxMats = 12;
+struct MvhMat {
+    const uint8_t* W;
+    const uint16_t* xh;   // the activations as fp16 x * 2^e per batch row, [B][K]
+    const float* xinv;    // 2^-e per batch row
+    float* y;             // [B][N]
+    int64_t N, K, rowbytes;
+    int fmt, stages, item0;
+};
+struct MvhGroup {
+    CUtensorMap map[kMvhMaxMats];  // W as [N / 8][8 * rowbytes] 16-bit elements, boxes 8 x 32
+    MvhMat m[kMvhMaxMats];
+    int nmat, items, B, ks;
+    DevState st;
+    int live_slot;
+};
+bool mvh_supported(int fmt, int64_t N, int64_t K);
+// workspace for n matvecs whose activations are x[i] (equal pointers and K share it)
+size_t mvh_workspace_bytes(int n, const void* const* x, const int64_t* K, int B);
+// the prep kernel (bf16 -> scaled fp16) and the matvec over matrices
+// sel[0 .. n-1] of the arrays, formats fmt[]
+cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W, const void* const* x,
+                    float* const* y, const int64_t* N, const int64_t* K, int B, void* ws, int sms,
+                    cudaStream_t s, DevState st);
+
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
 constexpr int kTcThreads = 768;

@@ -99,8 +99,8 @@ enum {
     QMM_LIVE_MOE_GATHER = 16,
     QMM_LIVE_GEMV_MV1 = 17,           /* batch-1 float matvec on the CUDA
                                          cores                               */
-    QMM_LIVE_GEMV_MV8 = 18,           /* batch 2-8 float matvec on the
-                                         warp-level MMA                      */
+    QMM_LIVE_GEMV_MV8 = 18,           /* batch 1-8 float matvec on the
+                                         warp-level MMA (fp16 or bf16)       */
     QMM_LIVE_COUNT = 24
 };
 
@@ -111,8 +111,10 @@ enum {
  * QMM_FAULT ("plane_alloc" makes qmm_plane_wanted's caller-side allocation be
  * treated as failed; host-side fault injection only), QMM_MV1 ("0" sends
  * batch-1 float matvecs to the tensor-memory matvec instead of the CUDA-core
- * one), QMM_MV8 ("0" does the same for batch 2-8 instead of the warp-level
- * MMA one), QMM_PDL ("0" launches without programmatic dependent launch).
+ * one), QMM_MV8 ("0" does the same for the bf16 warp-level MMA matvec at
+ * batch 2-8), QMM_MVH ("0" turns the fp16-MMA matvec for bf16 batches 1-8
+ * off, so those batches take the paths above), QMM_PDL ("0" launches
+ * without programmatic dependent launch).
  * Called implicitly by every entry point; calling it again is a no-op. */
 int qmm_init(void);
 
@@ -140,14 +142,16 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K);
  * QMM_ACT_FLOAT: fp32 products and sums of the activations as given.
  * QMM_ACT_Q8: x is first quantized per 32 (needs workspace), then
  *   y = sum_g s_x * d * sc_g * I_g with exact int32 group partials I_g.
- * Float mode with rows of whole 16-byte pieces (K % 256 == 0; q6_K K % 2048
- * == 0): B = 1 runs on the CUDA cores (lanes along K, activations in
- * registers), B = 2..8 with bf16 x on the warp-level MMA (K split over the
- * warps of a CTA for short N, added in a fixed order); neither uses
- * workspace. Every other case runs on the tensor-memory matvec, where short N
- * is split along K and the partial sums are added in a fixed order by a
- * second launch. Either way the order of the sums is fixed, so results are
- * bitwise reproducible. */
+ * Float mode, K % 256 == 0: bf16 x with B = 1..8 and N % 8 == 0 runs on the
+ * warp-level MMA with fp16 operands (x laid out once as fp16 scaled by a
+ * power of two per row, in workspace; K split over the warps of a CTA for
+ * short N, added in a fixed order); otherwise fp32 x at B = 1 with rows of
+ * whole 16-byte pieces (q6_K K % 2048 == 0) runs on the CUDA cores, and bf16
+ * x at B = 2..8 on the bf16 warp-level MMA (neither uses workspace). Every
+ * other case runs on the tensor-memory matvec, where short N is split along
+ * K and the partial sums are added in a fixed order by a second launch.
+ * Either way the order of the sums is fixed, so results are bitwise
+ * reproducible. */
 int qmm_gemv(uint32_t fmt, const void* W, const void* x, float* y, int64_t N,
              int64_t K, int B);
 
@@ -168,6 +172,29 @@ int qmm_gemv_group(uint32_t fmt, int n, const void* const* W, const void* const*
 /* Workspace that qmm_gemv_group needs for these shapes; 0 if none or if the
  * arguments are invalid. */
 size_t qmm_gemv_group_workspace_bytes(uint32_t fmt, int n, const int64_t* N, const int64_t* K,
+                                      int B);
+
+/* Several decode matvecs whose weights may be of DIFFERENT formats, as one
+ * call: y[i] = W[i] x[i] for i < n <= 12, each as qmm_gemv(fmt[i], W[i],
+ * x[i], y[i], N[i], K[i], B) defines it (quantprobe "LAWS.md", Law 4: the
+ * matvecs of one decode step read every weight once). All fmt[i] must share
+ * the activation type and mode bits; the weight format bits may differ. In
+ * float mode with bf16 activations, B <= 8, K % 256 == 0 and N % 8 == 0,
+ * every matrix runs in ONE launch of the fp16-MMA matvec (after one launch
+ * that lays the activations out), so a 7B-shaped decode step of mixed Q4_0 /
+ * q6_K / Q8_0 weights is two launches; other matrices run per format as
+ * qmm_gemv_group would run them. W, x, y, N, K, fmt are host arrays of n
+ * entries (device pointers with qmm_gemv's layouts and alignment). Results
+ * agree with qmm_gemv within the float bound (the order of the sums inside
+ * a matrix may differ with the split of K). Workspace from
+ * qmm_gemv_multi_workspace_bytes; errors as qmm_gemv. */
+int qmm_gemv_multi(int n, const uint32_t* fmt, const void* const* W, const void* const* x,
+                   float* const* y, const int64_t* N, const int64_t* K, int B);
+
+/* Workspace that qmm_gemv_multi needs for these shapes (assuming no two
+ * matvecs share their activations); 0 if none or if the arguments are
+ * invalid. */
+size_t qmm_gemv_multi_workspace_bytes(int n, const uint32_t* fmt, const int64_t* N, const int64_t* K,
                                       int B);
 
 /* Size of the fixed scratch array that qmm_gemv_noalloc uses (4 MiB). */

@@ -215,12 +215,16 @@ def test_liveness_counts_each_launch():
     live = qmm.liveness()
     assert live["gemv_float"] == 2 and live["x_tile"] == 1  # bf16: gathered inside the matvec
     assert live["gemv_mv1"] == 0 and live["gemv_splitk_reduce"] == 3
-    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)  # batch 1, float: one mv1 launch, no split
+    run_gemv(qmm.Q6_K, W, synth.normal_f32(3, (1, K)), N, K)  # batch 1, fp32: one mv1 launch, no split
     live = qmm.liveness()
     assert live["gemv_mv1"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
-    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (4, K)), N, K)  # batch 4, bf16: one mv8 launch (K split across warps)
+    # batch 1 and 4, bf16, N % 8 == 0: the fp16-MMA matvec, one launch each
+    # after one activation layout launch (K split across warps, no reduce)
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (1, K)), N, K)
+    run_gemv(qmm.Q6_K, W, synth.normal_bf16(3, (4, K)), N, K)
     live = qmm.liveness()
-    assert live["gemv_mv8"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
+    assert live["gemv_mv8"] == 2 and live["x_tile"] == 3
+    assert live["gemv_mv1"] == 1 and live["gemv_float"] == 2 and live["gemv_splitk_reduce"] == 3
 
 
 def test_missing_workspace_is_an_error():
@@ -306,7 +310,9 @@ def test_mv1_matches_oracle(name, N, K, xdt):
     x = synth.normal_f32(710 + N, (1, K)) if xdt == "f32" else synth.normal_bf16(710 + N, (1, K))
     qmm.liveness_reset()
     y = run_gemv(fmt, W, x, N, K)
-    assert qmm.liveness()["gemv_mv1"] == 1
+    # bf16 rows with N % 8 == 0 take the fp16-MMA matvec instead
+    mvh = xdt == "bf16" and N % 8 == 0
+    assert qmm.liveness()["gemv_mv8" if mvh else "gemv_mv1"] == 1
     if N * K <= 4096 * 4096:
         ref, absum = oracle.gemv_float(fmt, W, x, N, K)
         assert_within(y, ref, absum, f"mv1 {name} {N}x{K} {xdt}")
@@ -411,7 +417,7 @@ def test_unaligned_q6k_rows_at_batch_1_take_the_tensor_core_matvec():
 def test_group_makes_one_fast_launch_per_k():
     """a grouped batch-8 call over matrices of two K (one of them with rows
     that are not whole 16-byte pieces) makes one warp-MMA launch per K"""
-    shapes = [(100, 4096), (70, 11008), (40, 4096)]
+    shapes = [(100, 4096), (70, 11008), (44, 4096)]  # N % 8 != 0: not the fp16-MMA matvec
     Ws = [synth.matrix(qmm.Q6_K, 950 + i, N, K) for i, (N, K) in enumerate(shapes)]
     xs = [synth.normal_bf16(960 + i, (8, K)) for i, (N, K) in enumerate(shapes)]
     ys = [torch.full((8, N), float("nan"), dtype=torch.float32, device="cuda") for N, K in shapes]
@@ -429,8 +435,9 @@ def test_group_makes_one_fast_launch_per_k():
 
 
 def test_fast_paths_opt_out_gate():
-    """QMM_MV1=0 and QMM_MV8=0 (read once per process) send batch 1 and
-    batch 2-8 to the tensor-memory matvec; the results stay within the bound"""
+    """QMM_MVH=0, QMM_MV1=0 and QMM_MV8=0 (read once per process) send batch
+    1 and batch 2-8 to the tensor-memory matvec; the results stay within the
+    bound"""
     import os
     import subprocess
     import sys
@@ -455,7 +462,176 @@ for B in (1, 4):
 print("gate ok")
 """
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, QMM_MV1="0", QMM_MV8="0")
+    env = dict(os.environ, QMM_MV1="0", QMM_MV8="0", QMM_MVH="0")
     r = subprocess.run([sys.executable, "-c", code.format(root=root)], env=env, capture_output=True,
                        text=True, timeout=300)
     assert r.returncode == 0 and "gate ok" in r.stdout, r.stdout + r.stderr
+
+
+# The batch 1-8 matvec on the warp-level MMA with fp16 operands (mvh): taken
+# for bf16 activations, 1 <= B <= 8, float mode, K % 256 == 0, N % 8 == 0, any
+# mix of formats in one launch. Rows not a multiple of the 256-row block of 8
+# stride-8 items (partial items), a single 8-row group, K split over several
+# warps (short N, long K), q6_K super-blocks at every even lead (K = 11008:
+# rows of 9030 bytes), Q8_0 stages at both leads (K / 128 odd and even).
+MVH_SHAPES = [("q6_K", 8, 256), ("q6_K", 264, 768), ("q6_K", 1000, 11008), ("q6_K", 520, 4096),
+              ("q6_K", 4104, 2304), ("Q4_0", 8, 256), ("Q4_0", 392, 1280), ("Q4_0", 4104, 512),
+              ("Q4_0", 136, 11008), ("Q8_0", 16, 256), ("Q8_0", 264, 2304), ("Q8_0", 8200, 768)]
+
+
+@pytest.mark.parametrize("name,N,K", MVH_SHAPES)
+@pytest.mark.parametrize("B", [1, 3, 8])
+def test_mvh_matches_oracle(name, N, K, B):
+    fmt = FMTS[name]
+    W = synth.matrix(fmt, 1200 + N, N, K)
+    x = synth.normal_bf16(1210 + N + B, (B, K))
+    qmm.liveness_reset()
+    y = run_gemv(fmt, W, x, N, K)
+    live = qmm.liveness()
+    assert live["gemv_mv8"] == 1 and live["x_tile"] == 1 and live["gemv_float"] == 0
+    if N * K <= 2048 * 4096:
+        ref, absum = oracle.gemv_float(fmt, W, x, N, K)
+        assert_within(y, ref, absum, f"mvh {name} {N}x{K} B={B}")
+    else:
+        rng = np.random.default_rng(N + B)
+        ns = np.concatenate([rng.integers(0, N, 300), [0, N - 1, N - 8, N - 9, 255, 256]])
+        bs = rng.integers(0, B, len(ns))
+        ref, absum = oracle.gemv_float_pairs(fmt, W, K, x, bs, ns)
+        assert_within(y[bs, ns], ref, absum, f"mvh {name} {N}x{K} B={B}")
+    # the order of the sums is fixed: a second call is bitwise identical
+    y2 = run_gemv(fmt, W, x, N, K)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["q6_K", "Q4_0", "Q8_0"])
+@pytest.mark.parametrize("B", [1, 8])
+def test_mvh_integer_path_bitwise(name, B):
+    """unit scales, integer activations (exact in bf16 and, scaled by a power
+    of two, in fp16): every partial sum is an exact integer multiple of the
+    scale, so the fp16-MMA matvec equals the exact product bitwise"""
+    fmt = FMTS[name]
+    N, K = 48, 2048
+    rng = np.random.default_rng(fmt * 10 + B)
+    W, wint = _unit_scale(fmt, N, K, rng)
+    xi = rng.integers(-127, 128, (B, K))
+    x = synth.to_bf16_bits(xi.astype(np.float32))
+    qmm.liveness_reset()
+    y = run_gemv(fmt, W, x, N, K)
+    assert qmm.liveness()["gemv_mv8"] == 1
+    assert np.array_equal(y.astype(np.float64), (xi @ wint.T).astype(np.float64))
+
+
+def test_mvh_identity_and_zero_rows_are_exact():
+    """a one-hot row returns its bf16 activation bitwise; an all-zero weight
+    row and an all-zero activation row give exactly 0"""
+    n = 1024
+    one = pack.f16_bits(1.0)
+    codes = np.full((n, n), 32)
+    np.fill_diagonal(codes, 33)
+    codes[5] = 32  # an all-zero weight row
+    W = pack.pack_q6k_matrix(codes, np.ones((n, n // 16), int), np.full((n, n // 256), one))
+    x = synth.normal_bf16(21, (3, n))
+    x[1] = 0  # an all-zero activation row
+    y = run_gemv(qmm.Q6_K, W, x, n, n)
+    xf = synth.bf16_bits_to_f32(x)
+    expect = xf.copy()
+    expect[:, 5] = 0.0
+    assert np.array_equal(y, expect)
+
+
+def test_mvh_activation_range_extremes():
+    """activation rows of very large and very small magnitude (each row gets
+    its own power-of-two scale) and a row mixing magnitudes 2^40 apart"""
+    N, K = 64, 4096
+    W = synth.q6k_matrix(31, N, K)
+    xf = synth.normal_f32(32, (4, K))
+    xf[0] *= 1e30
+    xf[1] *= 1e-30
+    xf[2, ::2] *= 2.0 ** 20
+    xf[2, 1::2] *= 2.0 ** -20
+    x = synth.to_bf16_bits(xf)
+    y = run_gemv(qmm.Q6_K, W, x, N, K)
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+    assert_within(y, ref, absum, "activation extremes")
+
+
+@pytest.mark.parametrize("B", [1, 6])
+def test_mvh_q6k_large_scales_exact_form(B):
+    """q6_K sub-block scales outside -62..62 (up to -128 and 127) take the
+    exact two-MMA form of the tile; the result stays within the bound, and
+    with unit d and integer activations it is exact"""
+    N, K = 96, 1024
+    W = synth.q6k_matrix(41, N, K).copy()
+    blk = W.reshape(-1, 210)
+    blk[::5, 192 + 3] = np.uint8(127)
+    blk[2::5, 192 + 11] = np.uint8(128)   # -128
+    blk[3::7, 192 + 0] = np.uint8(256 - 90)
+    x = synth.normal_bf16(42 + B, (B, K))
+    y = run_gemv(qmm.Q6_K, W, x, N, K)
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x, N, K)
+    assert_within(y, ref, absum, "q6_K large scales")
+    rng = np.random.default_rng(43)
+    codes = rng.integers(0, 64, (N, K))
+    sc = rng.integers(-128, 128, (N, K // 16))
+    Wu = pack.pack_q6k_matrix(codes, sc, np.full((N, K // 256), pack.f16_bits(1.0)))
+    xi = rng.integers(-8, 9, (B, K))
+    yu = run_gemv(qmm.Q6_K, Wu, synth.to_bf16_bits(xi.astype(np.float32)), N, K)
+    wint = (codes - 32) * np.repeat(sc, 16, axis=1)
+    assert np.array_equal(yu.astype(np.float64), (xi @ wint.T).astype(np.float64))
+
+
+@pytest.mark.parametrize("B", [1, 3, 8])
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_gemv_multi_mixed_formats(B, xdt):
+    """matvecs of all three formats in one call: with bf16 activations the
+    ones with N % 8 == 0 run in one fp16-MMA launch whatever their format, the
+    others per format; with fp32 activations all run per format"""
+    spec = [("Q4_0", 264, 512), ("q6_K", 520, 4096), ("Q8_0", 40, 768), ("q6_K", 37, 256 * 5),
+            ("Q4_0", 53, 32 * 16), ("q6_K", 256, 11008)]
+    Ws = [synth.matrix(FMTS[f], 1300 + i, N, K) for i, (f, N, K) in enumerate(spec)]
+    mk = synth.normal_bf16 if xdt == "bf16" else synth.normal_f32
+    xs = [mk(1310 + i, (B, K)) for i, (f, N, K) in enumerate(spec)]
+    ys = [torch.full((B, N), float("nan"), dtype=torch.float32, device="cuda") for f, N, K in spec]
+    multi = qmm.GemvMulti([FMTS[f] for f, N, K in spec], [dev(W) for W in Ws], [x_tensor(x) for x in xs],
+                          ys, [N for f, N, K in spec], [K for f, N, K in spec])
+    qmm.liveness_reset()
+    qmm.gemv_multi(multi)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    live = qmm.liveness()
+    if xdt == "bf16":
+        assert live["gemv_mv8"] >= 1 and live["x_tile"] == 1
+    for (f, N, K), W, x, y in zip(spec, Ws, xs, ys):
+        ref, absum = oracle.gemv_float(FMTS[f], W, x, N, K)
+        assert_within(y.cpu().numpy(), ref, absum, f"multi {f} {N}x{K} B={B} {xdt}")
+
+
+def test_gemv_multi_shares_equal_activations():
+    """matvecs that read the same activation tensor (q, k, v of one layer)
+    share one fp16 copy of it; results as separate calls within the bound"""
+    K, B = 4096, 2
+    x = synth.normal_bf16(1400, (B, K))
+    xt = x_tensor(x)
+    spec = [("Q4_0", 512), ("Q4_0", 512), ("q6_K", 512)]
+    Ws = [synth.matrix(FMTS[f], 1410 + i, N, K) for i, (f, N) in enumerate(spec)]
+    ys = [torch.empty((B, N), dtype=torch.float32, device="cuda") for f, N in spec]
+    multi = qmm.GemvMulti([FMTS[f] for f, N in spec], [dev(W) for W in Ws], [xt, xt, xt], ys,
+                          [N for f, N in spec], [K] * 3)
+    qmm.gemv_multi(multi)
+    torch.cuda.synchronize()
+    qmm.sync_check()
+    for (f, N), W, y in zip(spec, Ws, ys):
+        ref, absum = oracle.gemv_float(FMTS[f], W, x, N, K)
+        assert_within(y.cpu().numpy(), ref, absum, f"shared x {f}")
+
+
+def test_gemv_multi_argument_errors():
+    xt = x_tensor(synth.normal_bf16(1, (1, 256)))
+    Wt = dev(synth.q6k_matrix(1, 8, 256))
+    y = torch.empty((1, 8), dtype=torch.float32, device="cuda")
+    # activation bits that differ between entries
+    m = qmm.GemvMulti([qmm.Q6_K, qmm.Q6_K], [Wt, Wt], [xt, xt], [y, y], [8, 8], [256, 256])
+    m._fmt[1] = qmm.Q6_K | qmm.X_F32
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.gemv_multi(m)
+    assert ei.value.code == qmm.EINVAL
