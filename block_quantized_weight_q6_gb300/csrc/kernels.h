@@ -106,7 +106,7 @@ struct MvhMat {
     int fmt, stages, item0;
 };
 struct MvhGroup {
-    CUtensorMap map[kMvhMaxMats];  // W as [N / 8][8 * rowbytes] 16-bit elements, boxes 8 x 32
+    CUtensorMap map[kMvhMaxMats];  // W as [N / 8][8 * rowbytes] 16-bit elements, boxes 32 rows high
     MvhMat m[kMvhMaxMats];
     int nmat, items, B, ks;
     DevState st;

@@ -193,7 +193,7 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
         min_stages = std::min(min_stages, a.stages);
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(N[m] / 8)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
-        const cuuint32_t box[2] = {8u, static_cast<cuuint32_t>(kMvhRows)};
+        const cuuint32_t box[2] = {mvh_box_w(a.fmt) / 2, static_cast<cuuint32_t>(kMvhRows)};
         const cuuint32_t es[2] = {1u, 1u};
         if (enc(&g.map[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint8_t*>(a.W), dims, strides, box, es,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

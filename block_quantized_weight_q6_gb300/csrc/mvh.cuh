@@ -35,10 +35,12 @@
 // multiple of 16 for every even row size), so the byte lead of a stage is
 // the same for all 32 rows of an item and the realignment of the code bytes
 // is warp-uniform. A stage arrives by 2-D TMA with W seen as
-// [N / 8][8 * rowbytes] 16-bit elements: one box per 16-byte piece, 32 rows
-// high, landing as [piece][32 rows][16 B] with pieces 544 bytes apart, so the
-// 128-bit loads of one load phase (rows 2k and 2k + 1, c = 0..3) hit 32
-// different banks.
+// [N / 8][8 * rowbytes] 16-bit elements, in boxes 32 rows high that land
+// row after row: q6_K four boxes 64 bytes wide (the 14 pieces of 16 bytes a
+// super-block and its lead cover, and 2 more), so the 128-bit loads of one
+// load phase (rows 2k and 2k + 1, lanes c = 0..3 reading pieces c + s) hit 32
+// different banks; Q4_0 / Q8_0 three boxes 48 bytes wide (their 144 bytes
+// exactly), read with 32-bit loads. Box destinations are 128-byte aligned.
 //
 // Each warp streams its own items through a private ring of NS stages (an
 // mbarrier per slot, waits bounded in time); a team of KS warps of a CTA may
@@ -55,10 +57,10 @@ namespace qmm {
 
 constexpr int kMvhNS = 3;
 constexpr int kMvhRows = 32;                // rows per item: two 16-row MMA tiles
-constexpr uint32_t kMvhPitch = 544;         // bytes between the 16-byte pieces of a stage
-constexpr uint32_t kMvhBox = 32 * 16;       // bytes of one piece (32 rows)
-constexpr int kMvhMaxPieces = 14;           // q6_K: a super-block and its lead-in
-constexpr uint32_t kMvhSlot = kMvhMaxPieces * kMvhPitch;
+// box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 3 x 48
+__host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 48u; }
+__host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 4 : 3; }
+constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 8 KB
 constexpr uint32_t kMvhPartOff = kMvhWarps * kMvhNS * kMvhSlot;  // team sums, after the rings
 constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 8 * 32 * 4;
 constexpr uint32_t kMvhSmem = kMvhBarOff + kMvhWarps * kMvhNS * 8;
@@ -109,25 +111,33 @@ __device__ __forceinline__ void mvh_lds_v4(uint32_t a, uint32_t* w) {
                  : "r"(a));
 }
 
+// q6_K stage slot: shared address of 16-byte piece p of row r (four boxes of
+// [32 rows][64 B], 2 KB apart).
+__device__ __forceinline__ uint32_t q6k_piece(uint32_t slot, int r, int p) {
+    return slot + static_cast<uint32_t>(p >> 2) * 2048u + 64u * static_cast<uint32_t>(r) +
+           16u * static_cast<uint32_t>(p & 3);
+}
+
 // The 16 bytes at byte lead L (even, < 16; QW = L / 4 and sel shifts by
-// L % 4) of the piece at a and the next one (kMvhPitch further).
+// L % 4) of piece p of row r and the next piece.
 template <int QW>
-__device__ __forceinline__ void mvh_seg(uint32_t a, uint32_t sel, uint32_t (&o)[4]) {
+__device__ __forceinline__ void mvh_seg(uint32_t slot, int r, int p, uint32_t sel, uint32_t (&o)[4]) {
     uint32_t w[8];
-    mvh_lds_v4(a, w);
-    mvh_lds_v4(a + kMvhPitch, w + 4);
+    mvh_lds_v4(q6k_piece(slot, r, p), w);
+    mvh_lds_v4(q6k_piece(slot, r, p + 1), w + 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = __byte_perm(w[QW + i], w[QW + i + 1], sel);
 }
 
-// Shared address of logical byte o of row r of a stage slot.
+// Q4_0 / Q8_0 stage slot: shared address of logical byte o of row r (three
+// boxes of [32 rows][48 B], 1536 bytes apart).
 __device__ __forceinline__ uint32_t mvh_addr(uint32_t slot, int r, uint32_t o) {
-    return slot + (o >> 4) * kMvhPitch + 16u * static_cast<uint32_t>(r) + (o & 15u);
+    return slot + (o / 48u) * 1536u + 48u * static_cast<uint32_t>(r) + (o % 48u);
 }
 
 // Four bytes at logical byte o of row r; ALIGNED says whether o % 4 == 0
 // (else o % 4 == 2, and the word is put together from the aligned words
-// around it, each inside its own piece).
+// around it; an aligned word never straddles two boxes).
 template <bool ALIGNED>
 __device__ __forceinline__ uint32_t mvh_word(uint32_t slot, int r, uint32_t o) {
     if constexpr (ALIGNED) {
@@ -170,9 +180,8 @@ template <int QW>
 __device__ __forceinline__ bool q6k_tile_fast(uint32_t slot, int ra, int rb, int c, uint32_t sel, uint32_t selc,
                                               const uint32_t (&x)[32], float (&D)[4]) {
     uint32_t qa0[4], qa1[4], ha[4], sa[4], qb0[4], qb1[4], hb[4], sb[4];
-    const uint32_t pa = slot + 16u * ra, pb = slot + 16u * rb;
-    mvh_seg<QW>(pa + 12 * kMvhPitch, sel, sa);
-    mvh_seg<QW>(pb + 12 * kMvhPitch, sel, sb);
+    mvh_seg<QW>(slot, ra, 12, sel, sa);
+    mvh_seg<QW>(slot, rb, 12, sel, sb);
     bool big = false;
 #pragma unroll
     for (int Q = 0; Q < 4; ++Q) {
@@ -180,12 +189,12 @@ __device__ __forceinline__ bool q6k_tile_fast(uint32_t slot, int ra, int rb, int
         big = big || s0 > 62 || s0 < -62 || s1 > 62 || s1 < -62;
     }
     if (__any_sync(0xffffffffu, big)) return false;
-    mvh_seg<QW>(pa + c * kMvhPitch, sel, qa0);
-    mvh_seg<QW>(pa + (4 + c) * kMvhPitch, sel, qa1);
-    mvh_seg<QW>(pa + (8 + c) * kMvhPitch, sel, ha);
-    mvh_seg<QW>(pb + c * kMvhPitch, sel, qb0);
-    mvh_seg<QW>(pb + (4 + c) * kMvhPitch, sel, qb1);
-    mvh_seg<QW>(pb + (8 + c) * kMvhPitch, sel, hb);
+    mvh_seg<QW>(slot, ra, c, sel, qa0);
+    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
+    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
+    mvh_seg<QW>(slot, rb, c, sel, qb0);
+    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
+    mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
 #define QMM_MVH_Q6K_QUAD(Q)                                                                     \
     {                                                                                           \
         const uint32_t s2a = h2_add(__byte_perm(sa[Q] ^ 0x80808080u, 0x64646464u, selc), kH2M1152); \
@@ -215,15 +224,14 @@ template <int QW>
 __device__ __forceinline__ void q6k_tile_exact(uint32_t slot, int ra, int rb, int c, uint32_t sel,
                                             const uint32_t (&x)[32], float (&D)[4]) {
     uint32_t qa0[4], qa1[4], ha[4], sa[4], qb0[4], qb1[4], hb[4], sb[4];
-    const uint32_t pa = slot + 16u * ra, pb = slot + 16u * rb;
-    mvh_seg<QW>(pa + c * kMvhPitch, sel, qa0);
-    mvh_seg<QW>(pa + (4 + c) * kMvhPitch, sel, qa1);
-    mvh_seg<QW>(pa + (8 + c) * kMvhPitch, sel, ha);
-    mvh_seg<QW>(pa + 12 * kMvhPitch, sel, sa);
-    mvh_seg<QW>(pb + c * kMvhPitch, sel, qb0);
-    mvh_seg<QW>(pb + (4 + c) * kMvhPitch, sel, qb1);
-    mvh_seg<QW>(pb + (8 + c) * kMvhPitch, sel, hb);
-    mvh_seg<QW>(pb + 12 * kMvhPitch, sel, sb);
+    mvh_seg<QW>(slot, ra, c, sel, qa0);
+    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
+    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
+    mvh_seg<QW>(slot, ra, 12, sel, sa);
+    mvh_seg<QW>(slot, rb, c, sel, qb0);
+    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
+    mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
+    mvh_seg<QW>(slot, rb, 12, sel, sb);
 #pragma unroll
     for (int Q = 0; Q < 4; ++Q) {
         const int s0 = q6k_sc(sa[Q], c), s1 = q6k_sc(sb[Q], c);
@@ -264,7 +272,9 @@ __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t 
         const int ra = 16 * t + g, rb = ra + 8;
         float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (!q6k_tile_fast<QW>(slot, ra, rb, c, sel, selc, x, D)) q6k_tile_exact<QW>(slot, ra, rb, c, sel, x, D);
-        const float da = mvh_half(slot, ra, 208 + L), db = mvh_half(slot, rb, 208 + L);
+        // d at byte 208 + L: piece 13, byte L of it (16 + L into box 3)
+        const float da = half_bits_to_float(lds_u16(q6k_piece(slot, ra, 13) + L));
+        const float db = half_bits_to_float(lds_u16(q6k_piece(slot, rb, 13) + L));
         acc[t][0] = fmaf(da, D[0], acc[t][0]);
         acc[t][1] = fmaf(da, D[1], acc[t][1]);
         acc[t][2] = fmaf(db, D[2], acc[t][2]);
@@ -372,7 +382,6 @@ __host__ __device__ constexpr int mvh_stage_k(int fmt) { return fmt == FMT_Q8_0 
 __host__ __device__ constexpr int mvh_stage_bytes(int fmt) {
     return fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q4_0 ? 144 : 136);
 }
-__host__ __device__ constexpr int mvh_pieces(int fmt) { return fmt == FMT_Q6_K ? 14 : 9; }
 
 struct MvhCursor {
     int it, p, m;  // item, stage of the item, matrix
@@ -393,19 +402,21 @@ __device__ __forceinline__ int64_t mvh_stage_off(const MvhMat& a, int j, int p) 
 }
 
 // Issues the TMA copies of the stage at cursor c into `slot` (completing on
-// bar): one box per 16-byte piece, lane p issues piece p.
+// bar): lane k issues box k, from the 16-byte boundary at or below the
+// stage's first byte.
 __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c, uint32_t slot, uint32_t bar,
                                           int lane) {
     const MvhMat& a = g.m[c.m];
     const int li = c.it - a.item0;
     const int j = li & 7, G0 = (li >> 3) * kMvhRows;
-    const int np = mvh_pieces(a.fmt);
+    const int nb = mvh_boxes(a.fmt);
+    const uint32_t bw = mvh_box_w(a.fmt);
     const int64_t off = mvh_stage_off(a, j, c.p) & ~static_cast<int64_t>(15);
-    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * kMvhBox);
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb) * bw * kMvhRows);
     __syncwarp();
-    if (lane < np)
-        tma_load_2d(slot + static_cast<uint32_t>(lane) * kMvhPitch, &g.map[c.m],
-                    static_cast<int>(off / 2) + 8 * lane, G0, bar);
+    if (lane < nb)
+        tma_load_2d(slot + static_cast<uint32_t>(lane) * bw * kMvhRows, &g.map[c.m],
+                    static_cast<int>(off / 2) + static_cast<int>(bw / 2) * lane, G0, bar);
 }
 
 // The lane's activations of stage p of matrix a (batch row g; zero past B).
