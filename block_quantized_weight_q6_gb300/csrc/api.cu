@@ -507,7 +507,7 @@ int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const vo
 // Workspace of the fp16-MMA matvec for these matrices, as if no two shared
 // their activations (the launch shares equal ones, so it never needs more).
 size_t mvh_ws_bound(int n, const int* sel, const int64_t* K, int B) {
-    size_t t = 0;
+    size_t t = 256;  // the item counter
     for (int i = 0; i < n; ++i)
         t += round_up(static_cast<size_t>(B) * K[sel[i]] * 2, 256) + round_up(static_cast<size_t>(B) * 4, 256);
     return t;

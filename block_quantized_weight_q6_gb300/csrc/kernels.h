@@ -95,7 +95,7 @@ cudaError_t mv8_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
 // launch, on the warp-level MMA with fp16 operands (mvh.cuh): work item = 32
 // rows of one matrix at stride 8, all of its K. Needs K % 256 == 0 and
 // N % 8 == 0, and workspace for the fp16 activations (mvh_workspace_bytes).
-constexpr int kMvhWarps = 8;
+constexpr int kMvhWarps = 12;
 constexpr int kMvhMaxMats = 12;
 struct MvhMat {
     const uint8_t* W;
@@ -108,6 +108,7 @@ struct MvhMat {
 struct MvhGroup {
     CUtensorMap map[kMvhMaxMats];  // W as [N / 8][8 * rowbytes] 16-bit elements, boxes 32 rows high
     MvhMat m[kMvhMaxMats];
+    int* ctr;             // the next unclaimed item past the first wave (reset by the prep kernel)
     int nmat, items, B, ks;
     DevState st;
     int live_slot;

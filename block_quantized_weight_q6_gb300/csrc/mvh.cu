@@ -20,13 +20,15 @@ struct MvhPrep {
     uint16_t* xh[kPrepMax];
     float* xinv[kPrepMax];
     int64_t K[kPrepMax];
+    int* ctr;  // the matvec's item counter, reset here
     int n, B;
 };
 
 __global__ void __launch_bounds__(256) mvh_prep_kernel(const __grid_constant__ MvhPrep p, DevState st) {
     grid_launch_dependents();
-    grid_dependency_wait();  // x comes from the previous kernel
+    grid_dependency_wait();  // x comes from the previous kernel, which no longer uses the counter
     live_bump(st, QMM_LIVE_X_TILE);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.ctr = 0;
     const int i = blockIdx.x / p.B, b = blockIdx.x % p.B;
     const int64_t K = p.K[i];
     const uint16_t* x = p.x[i] + static_cast<int64_t>(b) * K;
@@ -93,7 +95,7 @@ struct XPlan {
 
 void plan_x(int n, const void* const* x, const int64_t* K, int B, XPlan* p) {
     p->nd = 0;
-    p->total = 0;
+    p->total = 256;  // the item counter
     for (int i = 0; i < n; ++i) {
         int d = -1;
         for (int q = 0; q < p->nd; ++q)
@@ -155,6 +157,7 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     plan_x(n, xs, Ks, B, &xp);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     MvhPrep pr{};
+    pr.ctr = reinterpret_cast<int*>(wsb);
     pr.n = xp.nd;
     pr.B = B;
     for (int d = 0; d < xp.nd; ++d) {
@@ -169,6 +172,7 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     static thread_local MvhGroup g;  // large: kept off the stack
     memset(&g, 0, sizeof g);
     g.nmat = n;
+    g.ctr = pr.ctr;
     g.B = B;
     g.st = st;
     g.live_slot = QMM_LIVE_GEMV_MV8;
@@ -205,8 +209,13 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     // warps per item: enough that the items keep every warp of the grid
     // busy, at most any matrix's stages
     const int64_t warps = static_cast<int64_t>(sms) * kMvhWarps;
+    // (a divisor of the CTA's warps: teams never span two CTAs)
     g.ks = 1;
-    while (g.ks < kMvhWarps && 2 * g.ks <= min_stages && items * g.ks < warps) g.ks *= 2;
+    for (int k : {1, 2, 3, 4, 6, 12}) {
+        if (k > min_stages) break;
+        g.ks = k;
+        if (items * k >= warps) break;
+    }
     const int64_t per_cta = kMvhWarps / g.ks;
     const int grid = static_cast<int>(std::min<int64_t>(sms, (items + per_cta - 1) / per_cta));
     e = launch_pdl(mvh_kernel, dim3(grid), dim3(kMvhWarps * 32), kMvhSmem, s, g);

@@ -55,7 +55,7 @@
 
 namespace qmm {
 
-constexpr int kMvhNS = 3;
+constexpr int kMvhNS = 2;
 constexpr int kMvhRows = 32;                // rows per item: two 16-row MMA tiles
 // box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 3 x 48
 __host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 48u; }
@@ -63,7 +63,8 @@ __host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 
 constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 8 KB
 constexpr uint32_t kMvhPartOff = kMvhWarps * kMvhNS * kMvhSlot;  // team sums, after the rings
 constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 8 * 32 * 4;
-constexpr uint32_t kMvhSmem = kMvhBarOff + kMvhWarps * kMvhNS * 8;
+constexpr uint32_t kMvhFifoOff = kMvhBarOff + kMvhWarps * kMvhNS * 8;  // per warp: 4 item numbers
+constexpr uint32_t kMvhSmem = kMvhFifoOff + kMvhWarps * 16;
 static_assert(kMvhSmem <= 227u * 1024, "shared memory");
 
 // D = A B + C, m16n8k16, fp16 A (row) and B (col), fp32 C and D
@@ -129,6 +130,19 @@ __device__ __forceinline__ void mvh_seg(uint32_t slot, int r, int p, uint32_t se
     for (int i = 0; i < 4; ++i) o[i] = __byte_perm(w[QW + i], w[QW + i + 1], sel);
 }
 
+// The scale segment (16 bytes at lead L of pieces 12, 13) and the
+// super-block's d, which follows it (bytes 208, 209 of the super-block).
+template <int QW>
+__device__ __forceinline__ uint32_t mvh_seg_sc_d(uint32_t slot, int r, uint32_t sel, uint32_t L,
+                                                 uint32_t (&o)[4]) {
+    uint32_t w[8];
+    mvh_lds_v4(q6k_piece(slot, r, 12), w);
+    mvh_lds_v4(q6k_piece(slot, r, 13), w + 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = __byte_perm(w[QW + i], w[QW + i + 1], sel);
+    return (w[4 + QW] >> (8u * (L & 2u))) & 0xFFFFu;
+}
+
 // Q4_0 / Q8_0 stage slot: shared address of logical byte o of row r (three
 // boxes of [32 rows][48 B], 1536 bytes apart).
 __device__ __forceinline__ uint32_t mvh_addr(uint32_t slot, int r, uint32_t o) {
@@ -150,6 +164,12 @@ __device__ __forceinline__ uint32_t mvh_word(uint32_t slot, int r, uint32_t o) {
 
 __device__ __forceinline__ float mvh_half(uint32_t slot, int r, uint32_t o) {
     return half_bits_to_float(lds_u16(mvh_addr(slot, r, o)));
+}
+
+// Eight activations (16 bytes) at element offset off of the lane's row xr;
+// zeros for a lane past the batch (xr null).
+__device__ __forceinline__ uint4 mvh_x8(const uint16_t* xr, int off) {
+    return xr ? __ldg(reinterpret_cast<const uint4*>(xr + off)) : make_uint4(0u, 0u, 0u, 0u);
 }
 
 // ------------------------------------------------------------ q6_K stage
@@ -174,111 +194,139 @@ __device__ __forceinline__ int q6k_sc(uint32_t w, int c) {
     return static_cast<int>(static_cast<int8_t>(static_cast<uint8_t>(w >> (8 * c))));
 }
 
-// Adds the tile's products of one super-block into D (not cleared here).
-// Returns false (doing nothing) if a scale of the tile lies outside -62..62.
+// The tile's sum over one super-block: sc * (q - 32) from (1024 + c) * sc -
+// 1056 * sc in one fp16 FMA, exact for |sc| <= 62. A scale outside that range
+// makes the bias -1056 * sc overflow to an infinity, so the sum is not finite
+// and the caller recomputes the tile in the exact form. Two accumulator
+// chains (even and odd group quads) halve the MMA dependency chain.
 template <int QW>
-__device__ __forceinline__ bool q6k_tile_fast(uint32_t slot, int ra, int rb, int c, uint32_t sel, uint32_t selc,
-                                              const uint32_t (&x)[32], float (&D)[4]) {
+__device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, int c, uint32_t sel, uint32_t L,
+                                                uint32_t selc, const uint16_t* xr, float& da, float& db) {
     uint32_t qa0[4], qa1[4], ha[4], sa[4], qb0[4], qb1[4], hb[4], sb[4];
-    mvh_seg<QW>(slot, ra, 12, sel, sa);
-    mvh_seg<QW>(slot, rb, 12, sel, sb);
-    bool big = false;
-#pragma unroll
-    for (int Q = 0; Q < 4; ++Q) {
-        const int s0 = q6k_sc(sa[Q], c), s1 = q6k_sc(sb[Q], c);
-        big = big || s0 > 62 || s0 < -62 || s1 > 62 || s1 < -62;
-    }
-    if (__any_sync(0xffffffffu, big)) return false;
+    da = half_bits_to_float(mvh_seg_sc_d<QW>(slot, ra, sel, L, sa));
+    db = half_bits_to_float(mvh_seg_sc_d<QW>(slot, rb, sel, L, sb));
     mvh_seg<QW>(slot, ra, c, sel, qa0);
-    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
-    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
     mvh_seg<QW>(slot, rb, c, sel, qb0);
-    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
+    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
     mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
-#define QMM_MVH_Q6K_QUAD(Q)                                                                     \
-    {                                                                                           \
-        const uint32_t s2a = h2_add(__byte_perm(sa[Q] ^ 0x80808080u, 0x64646464u, selc), kH2M1152); \
-        const uint32_t s2b = h2_add(__byte_perm(sb[Q] ^ 0x80808080u, 0x64646464u, selc), kH2M1152); \
-        const uint32_t b2a = h2_mul(s2a, kH2M1056), b2b = h2_mul(s2b, kH2M1056);                \
-        _Pragma("unroll") for (int u = 0; u < 4; ++u) {                                         \
-            const uint32_t ca = q6k_code<Q>(qa0, qa1, ha, u), cb = q6k_code<Q>(qb0, qb1, hb, u); \
-            uint32_t A[4];                                                                      \
-            A[0] = h2_fma(h_pair01(ca), s2a, b2a);                                              \
-            A[1] = h2_fma(h_pair01(cb), s2b, b2b);                                              \
-            A[2] = h2_fma(h_pair23(ca), s2a, b2a);                                              \
-            A[3] = h2_fma(h_pair23(cb), s2b, b2b);                                              \
-            mma_f16_16816(D, A, x[8 * (Q) + 2 * u], x[8 * (Q) + 2 * u + 1]);                    \
-        }                                                                                       \
+    float D0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#define QMM_MVH_Q6K_QUAD(Q, DQ)                                                                      \
+    {                                                                                                \
+        const uint4 x0 = mvh_x8(xr, 16 * (c + 4 * (Q))), x1 = mvh_x8(xr, 16 * (c + 4 * (Q)) + 8);    \
+        const uint32_t xq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};                   \
+        const uint32_t s2a = h2_add(__byte_perm(sa[Q] ^ 0x80808080u, 0x64646464u, selc), kH2M1152);   \
+        const uint32_t s2b = h2_add(__byte_perm(sb[Q] ^ 0x80808080u, 0x64646464u, selc), kH2M1152);   \
+        const uint32_t b2a = h2_mul(s2a, kH2M1056), b2b = h2_mul(s2b, kH2M1056);                     \
+        _Pragma("unroll") for (int u = 0; u < 4; ++u) {                                              \
+            const uint32_t ca = q6k_code<Q>(qa0, qa1, ha, u), cb = q6k_code<Q>(qb0, qb1, hb, u);      \
+            uint32_t A[4];                                                                           \
+            A[0] = h2_fma(h_pair01(ca), s2a, b2a);                                                   \
+            A[1] = h2_fma(h_pair01(cb), s2b, b2b);                                                   \
+            A[2] = h2_fma(h_pair23(ca), s2a, b2a);                                                   \
+            A[3] = h2_fma(h_pair23(cb), s2b, b2b);                                                   \
+            mma_f16_16816(DQ, A, xq[2 * u], xq[2 * u + 1]);                                          \
+        }                                                                                            \
     }
-    QMM_MVH_Q6K_QUAD(0)
-    QMM_MVH_Q6K_QUAD(1)
-    QMM_MVH_Q6K_QUAD(2)
-    QMM_MVH_Q6K_QUAD(3)
+    // the low-nibble quads of ql 16c.. (Q = 0, 2) first, then ql 64 + 16c.. (Q = 1, 3)
+    QMM_MVH_Q6K_QUAD(0, D0)
+    QMM_MVH_Q6K_QUAD(2, D1)
+    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
+    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
+    QMM_MVH_Q6K_QUAD(1, D0)
+    QMM_MVH_Q6K_QUAD(3, D1)
 #undef QMM_MVH_Q6K_QUAD
-    return true;
+    return make_float4(D0[0] + D1[0], D0[1] + D1[1], D0[2] + D1[2], D0[3] + D1[3]);
 }
 
-// The same for any int8 scale: sc * (q - 32) as lo * (q - 32) + 8 hi * (q -
-// 32), both exact in fp16, in two MMAs.
-template <int QW>
-__device__ __forceinline__ void q6k_tile_exact(uint32_t slot, int ra, int rb, int c, uint32_t sel,
-                                            const uint32_t (&x)[32], float (&D)[4]) {
-    uint32_t qa0[4], qa1[4], ha[4], sa[4], qb0[4], qb1[4], hb[4], sb[4];
-    mvh_seg<QW>(slot, ra, c, sel, qa0);
-    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
-    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
-    mvh_seg<QW>(slot, ra, 12, sel, sa);
-    mvh_seg<QW>(slot, rb, c, sel, qb0);
-    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
-    mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
-    mvh_seg<QW>(slot, rb, 12, sel, sb);
-#pragma unroll
+// The same tile sum for any int8 scale, as lo * (q - 32) + 8 hi * (q - 32)
+// (sc = lo + 8 hi, 0 <= lo < 8), both exact in fp16, in two MMAs. Kept out
+// of line (it only runs for scales outside -62..62): it reads the lead, the
+// code bytes and the activations itself.
+__device__ __noinline__ float4 q6k_tile_exact(uint32_t slot, int ra, int rb, int c, uint32_t L,
+                                              const uint16_t* xrow) {
+    uint32_t seg[2][4][4];  // row, segment (ql c, ql 4 + c, qh c, scales), word
+    const int rows[2] = {ra, rb};
+    const int piece[4] = {c, 4 + c, 8 + c, 12};
+    for (int r = 0; r < 2; ++r)
+        for (int q = 0; q < 4; ++q)
+            for (int i = 0; i < 4; ++i) {
+                // word i of the 16 bytes at lead L of the piece, byte by byte
+                uint32_t w = 0;
+                for (int bt = 0; bt < 4; ++bt) {
+                    const uint32_t o = L + 4 * i + bt;  // byte inside the piece pair
+                    const uint32_t v = lds_u16(q6k_piece(slot, rows[r], piece[q] + static_cast<int>(o >> 4)) +
+                                               ((o & 15u) & ~1u));
+                    w |= ((v >> (8 * (o & 1u))) & 0xFFu) << (8 * bt);
+                }
+                seg[r][q][i] = w;
+            }
+    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int Q = 0; Q < 4; ++Q) {
-        const int s0 = q6k_sc(sa[Q], c), s1 = q6k_sc(sb[Q], c);
-        const int l0 = s0 & 7, l1 = s1 & 7;
-        const uint32_t lo_a = h2_splat(l0), lo_b = h2_splat(l1);
-        const uint32_t hi_a = h2_splat(s0 - l0), hi_b = h2_splat(s1 - l1);
-#pragma unroll
+        uint32_t lo2[2], hi2[2];
+        for (int r = 0; r < 2; ++r) {
+            const int sc = q6k_sc(seg[r][3][Q], c);
+            lo2[r] = h2_splat(sc & 7);
+            hi2[r] = h2_splat(sc - (sc & 7));
+        }
         for (int u = 0; u < 4; ++u) {
-            uint32_t ca, cb;
-            if (Q == 0) { ca = q6k_code<0>(qa0, qa1, ha, u); cb = q6k_code<0>(qb0, qb1, hb, u); }
-            else if (Q == 1) { ca = q6k_code<1>(qa0, qa1, ha, u); cb = q6k_code<1>(qb0, qb1, hb, u); }
-            else if (Q == 2) { ca = q6k_code<2>(qa0, qa1, ha, u); cb = q6k_code<2>(qb0, qb1, hb, u); }
-            else { ca = q6k_code<3>(qa0, qa1, ha, u); cb = q6k_code<3>(qb0, qb1, hb, u); }
-            const uint32_t ea0 = h2_add(h_pair01(ca), kH2M1056), eb0 = h2_add(h_pair01(cb), kH2M1056);
-            const uint32_t ea1 = h2_add(h_pair23(ca), kH2M1056), eb1 = h2_add(h_pair23(cb), kH2M1056);
-            uint32_t A[4];
-            A[0] = h2_mul(ea0, lo_a);
-            A[1] = h2_mul(eb0, lo_b);
-            A[2] = h2_mul(ea1, lo_a);
-            A[3] = h2_mul(eb1, lo_b);
-            mma_f16_16816(D, A, x[8 * Q + 2 * u], x[8 * Q + 2 * u + 1]);
-            A[0] = h2_mul(ea0, hi_a);
-            A[1] = h2_mul(eb0, hi_b);
-            A[2] = h2_mul(ea1, hi_a);
-            A[3] = h2_mul(eb1, hi_b);
-            mma_f16_16816(D, A, x[8 * Q + 2 * u], x[8 * Q + 2 * u + 1]);
+            uint32_t cw[2];
+            for (int r = 0; r < 2; ++r) {
+                const uint32_t l = seg[r][Q & 1][u];
+                const uint32_t lo = (Q >> 1) ? (l >> 4) : l;
+                const uint32_t hi = ((seg[r][2][u] >> (2 * Q)) & 0x03030303u) << 4;
+                cw[r] = (lo & 0x0F0F0F0Fu) | hi;
+            }
+            uint32_t b0 = 0, b1 = 0;
+            if (xrow) {
+                const uint32_t* xs = reinterpret_cast<const uint32_t*>(xrow + 16 * (c + 4 * Q) + 4 * u);
+                b0 = xs[0];
+                b1 = xs[1];
+            }
+            const uint32_t e[4] = {h2_add(h_pair01(cw[0]), kH2M1056), h2_add(h_pair01(cw[1]), kH2M1056),
+                                   h2_add(h_pair23(cw[0]), kH2M1056), h2_add(h_pair23(cw[1]), kH2M1056)};
+            uint32_t A[4] = {h2_mul(e[0], lo2[0]), h2_mul(e[1], lo2[1]), h2_mul(e[2], lo2[0]),
+                             h2_mul(e[3], lo2[1])};
+            mma_f16_16816(D, A, b0, b1);
+            const uint32_t Ah[4] = {h2_mul(e[0], hi2[0]), h2_mul(e[1], hi2[1]), h2_mul(e[2], hi2[0]),
+                                    h2_mul(e[3], hi2[1])};
+            mma_f16_16816(D, Ah, b0, b1);
         }
     }
+    return make_float4(D[0], D[1], D[2], D[3]);
+}
+
+__device__ __forceinline__ bool f4_finite(float4 v) {
+    return isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w);
 }
 
 // One q6_K stage of both tiles of an item: acc[t] += d * (tile t's sum).
-template <int QW>
+// xr: the lane's activation row at the stage's first K (null past B).
 __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t L, uint32_t selc,
-                                          const uint32_t (&x)[32], float (&acc)[2][4]) {
+                                          const uint16_t* xr, float (&acc0)[4], float (&acc1)[4]) {
     const uint32_t sel = (L & 2u) ? 0x5432u : 0x3210u;
-#pragma unroll
+#pragma unroll 1
     for (int t = 0; t < 2; ++t) {
         const int ra = 16 * t + g, rb = ra + 8;
-        float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (!q6k_tile_fast<QW>(slot, ra, rb, c, sel, selc, x, D)) q6k_tile_exact<QW>(slot, ra, rb, c, sel, x, D);
-        // d at byte 208 + L: piece 13, byte L of it (16 + L into box 3)
-        const float da = half_bits_to_float(lds_u16(q6k_piece(slot, ra, 13) + L));
-        const float db = half_bits_to_float(lds_u16(q6k_piece(slot, rb, 13) + L));
-        acc[t][0] = fmaf(da, D[0], acc[t][0]);
-        acc[t][1] = fmaf(da, D[1], acc[t][1]);
-        acc[t][2] = fmaf(db, D[2], acc[t][2]);
-        acc[t][3] = fmaf(db, D[3], acc[t][3]);
+        float4 D;
+        float da, db;
+        switch (L >> 2) {
+            case 0: D = q6k_tile_fast<0>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
+            case 1: D = q6k_tile_fast<1>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
+            case 2: D = q6k_tile_fast<2>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
+            default: D = q6k_tile_fast<3>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
+        }
+        if (__any_sync(0xffffffffu, !f4_finite(D))) D = q6k_tile_exact(slot, ra, rb, c, L, xr);
+        if (t == 0) {
+            acc0[0] = fmaf(da, D.x, acc0[0]);
+            acc0[1] = fmaf(da, D.y, acc0[1]);
+            acc0[2] = fmaf(db, D.z, acc0[2]);
+            acc0[3] = fmaf(db, D.w, acc0[3]);
+        } else {
+            acc1[0] = fmaf(da, D.x, acc1[0]);
+            acc1[1] = fmaf(da, D.y, acc1[1]);
+            acc1[2] = fmaf(db, D.z, acc1[2]);
+            acc1[3] = fmaf(db, D.w, acc1[3]);
+        }
     }
 }
 
@@ -288,8 +336,9 @@ __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t 
 // Q4_0 (18 B: d | qs[16]): weight e is nibble e / 16 of qs[e % 16], so the
 // lane's codes are nibble c / 2 of qs[8 (c % 2) .. + 7].
 template <int BLK>
-__device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c, const uint32_t (&x)[32],
+__device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c, const uint16_t* xr,
                                            float (&acc)[4]) {
+    const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
     constexpr uint32_t o = 18 * BLK + 2;          // qs of block BLK (o % 4 is 0 for odd BLK, 2 for even)
     constexpr bool AL = (o % 4) == 0;
     const uint32_t oq = o + 8u * static_cast<uint32_t>(c & 1);
@@ -304,12 +353,12 @@ __device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c,
     A[1] = h2_add(h_pair01(b0), kH2M1032);
     A[2] = h2_add(h_pair23(a0), kH2M1032);
     A[3] = h2_add(h_pair23(b0), kH2M1032);
-    mma_f16_16816(D, A, x[4 * BLK], x[4 * BLK + 1]);
+    mma_f16_16816(D, A, xv.x, xv.y);
     A[0] = h2_add(h_pair01(a1), kH2M1032);
     A[1] = h2_add(h_pair01(b1), kH2M1032);
     A[2] = h2_add(h_pair23(a1), kH2M1032);
     A[3] = h2_add(h_pair23(b1), kH2M1032);
-    mma_f16_16816(D, A, x[4 * BLK + 2], x[4 * BLK + 3]);
+    mma_f16_16816(D, A, xv.z, xv.w);
     const float da = mvh_half(slot, ra, 18 * BLK), db = mvh_half(slot, rb, 18 * BLK);
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
@@ -320,8 +369,9 @@ __device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c,
 // Q8_0 (34 B: d | qs[32] int8), blocks at lead L (0 or 8); the lane's codes
 // are qs[8c .. 8c + 7].
 template <int BLK>
-__device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c, uint32_t L,
-                                           const uint32_t (&x)[32], float (&acc)[4]) {
+__device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c, uint32_t L, const uint16_t* xr,
+                                           float (&acc)[4]) {
+    const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
     constexpr uint32_t o = 34 * BLK + 2;          // o % 4 is 0 for odd BLK, 2 for even (L % 4 == 0)
     constexpr bool AL = (o % 4) == 0;
     const uint32_t oq = L + o + 8u * static_cast<uint32_t>(c);
@@ -335,12 +385,12 @@ __device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c,
     A[1] = h2_add(h_pair01(b0), kH2M1152);
     A[2] = h2_add(h_pair23(a0), kH2M1152);
     A[3] = h2_add(h_pair23(b0), kH2M1152);
-    mma_f16_16816(D, A, x[4 * BLK], x[4 * BLK + 1]);
+    mma_f16_16816(D, A, xv.x, xv.y);
     A[0] = h2_add(h_pair01(a1), kH2M1152);
     A[1] = h2_add(h_pair01(b1), kH2M1152);
     A[2] = h2_add(h_pair23(a1), kH2M1152);
     A[3] = h2_add(h_pair23(b1), kH2M1152);
-    mma_f16_16816(D, A, x[4 * BLK + 2], x[4 * BLK + 3]);
+    mma_f16_16816(D, A, xv.z, xv.w);
     const float da = mvh_half(slot, ra, L + 34 * BLK), db = mvh_half(slot, rb, L + 34 * BLK);
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
@@ -348,31 +398,43 @@ __device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c,
     acc[3] = fmaf(db, D[3], acc[3]);
 }
 
-__device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint32_t (&x)[32],
-                                           float (&acc)[2][4]) {
-#pragma unroll
+__device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint16_t* xr, float (&acc0)[4],
+                                           float (&acc1)[4]) {
+#pragma unroll 1
     for (int t = 0; t < 2; ++t) {
         const int ra = 16 * t + g, rb = ra + 8;
-        q4_0_block<0>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<1>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<2>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<3>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<4>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<5>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<6>(slot, ra, rb, c, x, acc[t]);
-        q4_0_block<7>(slot, ra, rb, c, x, acc[t]);
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        q4_0_block<0>(slot, ra, rb, c, xr, a);
+        q4_0_block<1>(slot, ra, rb, c, xr, a);
+        q4_0_block<2>(slot, ra, rb, c, xr, a);
+        q4_0_block<3>(slot, ra, rb, c, xr, a);
+        q4_0_block<4>(slot, ra, rb, c, xr, a);
+        q4_0_block<5>(slot, ra, rb, c, xr, a);
+        q4_0_block<6>(slot, ra, rb, c, xr, a);
+        q4_0_block<7>(slot, ra, rb, c, xr, a);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (t == 0) acc0[q] += a[q];
+            else acc1[q] += a[q];
+        }
     }
 }
 
-__device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t L, const uint32_t (&x)[32],
-                                           float (&acc)[2][4]) {
-#pragma unroll
+__device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t L, const uint16_t* xr,
+                                           float (&acc0)[4], float (&acc1)[4]) {
+#pragma unroll 1
     for (int t = 0; t < 2; ++t) {
         const int ra = 16 * t + g, rb = ra + 8;
-        q8_0_block<0>(slot, ra, rb, c, L, x, acc[t]);
-        q8_0_block<1>(slot, ra, rb, c, L, x, acc[t]);
-        q8_0_block<2>(slot, ra, rb, c, L, x, acc[t]);
-        q8_0_block<3>(slot, ra, rb, c, L, x, acc[t]);
+        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        q8_0_block<0>(slot, ra, rb, c, L, xr, a);
+        q8_0_block<1>(slot, ra, rb, c, L, xr, a);
+        q8_0_block<2>(slot, ra, rb, c, L, xr, a);
+        q8_0_block<3>(slot, ra, rb, c, L, xr, a);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (t == 0) acc0[q] += a[q];
+            else acc1[q] += a[q];
+        }
     }
 }
 
@@ -383,20 +445,34 @@ __host__ __device__ constexpr int mvh_stage_bytes(int fmt) {
     return fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q4_0 ? 144 : 136);
 }
 
+// The walk of a warp's (or team's) stages. Teams (KS > 1) take items t,
+// t + T, ... (T teams) and member m the stages m, m + KS, ... of each. Single
+// warps (KS == 1) take item w (their number in the grid) first, then the next
+// unclaimed item of a counter in global memory (reset by the prep kernel),
+// so that items of very different lengths (a mixed-format launch) spread
+// evenly; each item is still summed by one warp in stage order.
 struct MvhCursor {
-    int it, p, m;  // item, stage of the item, matrix
+    int it, p, m;
+    bool fetch;  // the item ended; the next one is claimed before the next copy
 };
+
+__device__ __forceinline__ void mvh_set_matrix(const MvhGroup& g, MvhCursor& c) {
+    while (c.m + 1 < g.nmat && c.it >= g.m[c.m + 1].item0) ++c.m;
+}
 
 __device__ __forceinline__ void mvh_advance(const MvhGroup& g, int ks, int member, int nteams, MvhCursor& c) {
     c.p += ks;
     if (c.p < g.m[c.m].stages) return;
+    if (ks == 1) {
+        c.fetch = true;
+        return;
+    }
     c.p = member;
     c.it += nteams;
-    while (c.m + 1 < g.nmat && c.it >= g.m[c.m + 1].item0) ++c.m;
+    mvh_set_matrix(g, c);
 }
 
-// byte offset of stage p of row j (of every group) in a view row of W, and
-// the stage's lead in its first 16-byte piece
+// byte offset of stage p of row j (of every group) in a view row of W
 __device__ __forceinline__ int64_t mvh_stage_off(const MvhMat& a, int j, int p) {
     return static_cast<int64_t>(j) * a.rowbytes + static_cast<int64_t>(p) * mvh_stage_bytes(a.fmt);
 }
@@ -419,34 +495,11 @@ __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c,
                     static_cast<int>(off / 2) + static_cast<int>(bw / 2) * lane, G0, bar);
 }
 
-// The lane's activations of stage p of matrix a (batch row g; zero past B).
-__device__ __forceinline__ void mvh_x_fetch(const MvhGroup& g, const MvhMat& a, int p, int lane,
-                                            uint32_t (&x)[32]) {
-    const int gr = lane >> 2, c = lane & 3;
-    if (gr < g.B) {
-        const int64_t k0 = static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
-        const __half* xr = reinterpret_cast<const __half*>(a.xh) + static_cast<int64_t>(gr) * a.K + k0;
-        if (a.fmt == FMT_Q6_K) {
-#pragma unroll
-            for (int Q = 0; Q < 4; ++Q) {
-                const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * (c + 4 * Q)));
-                const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(xr + 16 * (c + 4 * Q) + 8));
-                x[8 * Q + 0] = v0.x; x[8 * Q + 1] = v0.y; x[8 * Q + 2] = v0.z; x[8 * Q + 3] = v0.w;
-                x[8 * Q + 4] = v1.x; x[8 * Q + 5] = v1.y; x[8 * Q + 6] = v1.z; x[8 * Q + 7] = v1.w;
-            }
-        } else {
-            const int nb = mvh_stage_k(a.fmt) / 32;
-#pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (b < nb) v = __ldg(reinterpret_cast<const uint4*>(xr + 32 * b + 8 * c));
-                x[4 * b + 0] = v.x; x[4 * b + 1] = v.y; x[4 * b + 2] = v.z; x[4 * b + 3] = v.w;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = 0u;
-    }
+// The lane's activation row at the first K of stage p of matrix a (null past B).
+__device__ __forceinline__ const uint16_t* mvh_xrow(const MvhGroup& g, const MvhMat& a, int p, int lane) {
+    const int gr = lane >> 2;
+    if (gr >= g.B) return nullptr;
+    return a.xh + static_cast<int64_t>(gr) * a.K + static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
 }
 
 // Bounded wait for the TMA copies of a slot; false (and the error word set)
@@ -481,6 +534,7 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
     const uint32_t ring = S + static_cast<uint32_t>(warp) * kMvhNS * kMvhSlot;
     const uint32_t bars = S + kMvhBarOff + static_cast<uint32_t>(warp) * kMvhNS * 8;
     float* part = reinterpret_cast<float*>(smem + kMvhPartOff);
+    int* fifo = reinterpret_cast<int*>(smem + kMvhFifoOff) + 4 * warp;
     const int nteams = static_cast<int>(gridDim.x) * (kMvhWarps / ks);
     const int gt = team * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
     // byte selector: byte c of a word into the low bytes of two fp16 (1024 + byte)
@@ -493,43 +547,44 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
     fence_mbar_init();
     __syncwarp();
 
-    // the weights do not depend on the previous kernel: the first copies go
-    // out before waiting for it
-    MvhCursor ic{gt, member, 0};
-    while (ic.m + 1 < g.nmat && ic.it >= g.m[ic.m + 1].item0) ++ic.m;
+    // The weights do not depend on the previous kernel: the first copies (of
+    // the first item only: later items may come from the counter, which the
+    // previous kernel resets) go out before waiting for it.
+    MvhCursor ic{gt, member, 0, false};
+    mvh_set_matrix(g, ic);
     const int m0 = ic.m;
     uint32_t issued = 0, used = 0;
-    for (int j = 0; j < kMvhNS - 1 && ic.it < g.items; ++j) {
+    int fifo_head = 0, fifo_tail = 0;
+    for (int j = 0; j < kMvhNS - 1 && !ic.fetch; ++j) {
         mvh_issue(g, ic, ring + (issued % kMvhNS) * kMvhSlot, bars + 8 * (issued % kMvhNS), lane);
         ++issued;
         mvh_advance(g, ks, member, nteams, ic);
     }
-    grid_dependency_wait();  // x comes from the prep kernel
+    grid_dependency_wait();  // x and the counter come from the prep kernel
+    const int first_claim = static_cast<int>(gridDim.x) * kMvhWarps;
 
     bool ok = true;
-    uint32_t x[32], xn[32];
-    mvh_x_fetch(g, g.m[m0], member, lane, xn);
     int m = m0;
-    for (int it = gt; it < g.items; it += nteams) {
-        while (m + 1 < g.nmat && it >= g.m[m + 1].item0) ++m;
+    int it = gt;
+    while (it < g.items) {
+        while (m + 1 < g.nmat && it >= g.m[m + 1].item0) ++m;  // items only increase
         const MvhMat& a = g.m[m];
         const int li = it - a.item0;
         const int j = li & 7, G0 = (li >> 3) * kMvhRows;
-        float acc[2][4];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[t][q] = 0.0f;
+        float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int p = member; p < a.stages; p += ks) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = xn[i];
-            // the next stage's activations (this item's, or the next item's first)
-            if (p + ks < a.stages) {
-                mvh_x_fetch(g, a, p + ks, lane, xn);
-            } else if (it + nteams < g.items) {
-                int mn = m;
-                while (mn + 1 < g.nmat && it + nteams >= g.m[mn + 1].item0) ++mn;
-                mvh_x_fetch(g, g.m[mn], member, lane, xn);
+            // the next item of a single warp's walk, claimed once the
+            // copies have reached the end of the current one
+            if (ic.fetch) {
+                int nx = 0;
+                if (lane == 0) nx = first_claim + atomicAdd(g.ctr, 1);
+                nx = __shfl_sync(0xffffffffu, nx, 0);
+                ic.it = nx;
+                ic.p = 0;
+                ic.fetch = false;
+                mvh_set_matrix(g, ic);
+                if (lane == 0) fifo[fifo_tail & 3] = nx;
+                ++fifo_tail;
             }
             // the copies NS - 1 stages ahead, into the slot consumed last
             if (ic.it < g.items) {
@@ -539,23 +594,21 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
                 ++issued;
                 mvh_advance(g, ks, member, nteams, ic);
             }
+            const uint16_t* xr = mvh_xrow(g, a, p, lane);
             const uint32_t slot = ring + (used % kMvhNS) * kMvhSlot;
             if (ok) ok = mvh_wait(bars + 8 * (used % kMvhNS), (used / kMvhNS) & 1u, g.st.err);
             ++used;
             const uint32_t L = static_cast<uint32_t>(mvh_stage_off(a, j, p) & 15);
-            if (a.fmt == FMT_Q6_K) {
-                switch (L >> 2) {
-                    case 0: q6k_stage<0>(slot, gr, c, L, selc, x, acc); break;
-                    case 1: q6k_stage<1>(slot, gr, c, L, selc, x, acc); break;
-                    case 2: q6k_stage<2>(slot, gr, c, L, selc, x, acc); break;
-                    default: q6k_stage<3>(slot, gr, c, L, selc, x, acc); break;
-                }
-            } else if (a.fmt == FMT_Q4_0) {
-                q4_0_stage(slot, gr, c, x, acc);
-            } else {
-                q8_0_stage(slot, gr, c, L, x, acc);
-            }
+            if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, L, selc, xr, acc0, acc1);
+            else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc0, acc1);
+            else q8_0_stage(slot, gr, c, L, xr, acc0, acc1);
             __syncwarp();
+        }
+        float acc[2][4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc[0][q] = acc0[q];
+            acc[1][q] = acc1[q];
         }
         // the team's sums of the item, added by member 0 in member order
         if (ks > 1) {
@@ -584,6 +637,13 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
                         if (n < a.N) a.y[static_cast<int64_t>(b) * a.N + n] = acc[t][2 * h + b2] * sc;
                     }
             }
+        }
+        if (ks > 1) {
+            it += nteams;
+        } else {
+            __syncwarp();  // the cursor's lane 0 wrote the next item before this
+            it = fifo[fifo_head & 3];
+            ++fifo_head;
         }
     }
     // a slot whose wait gave up may still be receiving: wait for it (bounded)
