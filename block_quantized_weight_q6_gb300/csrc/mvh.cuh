@@ -166,10 +166,11 @@ __device__ __forceinline__ float mvh_half(uint32_t slot, int r, uint32_t o) {
     return half_bits_to_float(lds_u16(mvh_addr(slot, r, o)));
 }
 
-// Eight activations (16 bytes) at element offset off of the lane's row xr;
-// zeros for a lane past the batch (xr null).
+// Eight activations (16 bytes) at element offset off of the lane's row xr.
+// (A lane past the batch reads a valid row too: its MMA column is never
+// stored, so no load needs a predicate.)
 __device__ __forceinline__ uint4 mvh_x8(const uint16_t* xr, int off) {
-    return xr ? __ldg(reinterpret_cast<const uint4*>(xr + off)) : make_uint4(0u, 0u, 0u, 0u);
+    return __ldg(reinterpret_cast<const uint4*>(xr + off));
 }
 
 // ------------------------------------------------------------ q6_K stage
@@ -197,8 +198,8 @@ __device__ __forceinline__ int q6k_sc(uint32_t w, int c) {
 // The tile's sum over one super-block: sc * (q - 32) from (1024 + c) * sc -
 // 1056 * sc in one fp16 FMA, exact for |sc| <= 62. A scale outside that range
 // makes the bias -1056 * sc overflow to an infinity, so the sum is not finite
-// and the caller recomputes the tile in the exact form. Two accumulator
-// chains (even and odd group quads) halve the MMA dependency chain.
+// and the caller recomputes the tile in the exact form. Four accumulator
+// chains (one per position u in the group) keep consecutive MMAs independent.
 template <int QW>
 __device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, int c, uint32_t sel, uint32_t L,
                                                 uint32_t selc, const uint16_t* xr, float& da, float& db) {
@@ -209,8 +210,13 @@ __device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, i
     mvh_seg<QW>(slot, rb, c, sel, qb0);
     mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
     mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
-    float D0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#define QMM_MVH_Q6K_QUAD(Q, DQ)                                                                      \
+    // one accumulator per u: the four MMAs of a quad are independent
+    float D[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) D[u][q] = 0.0f;
+#define QMM_MVH_Q6K_QUAD(Q)                                                                          \
     {                                                                                                \
         const uint4 x0 = mvh_x8(xr, 16 * (c + 4 * (Q))), x1 = mvh_x8(xr, 16 * (c + 4 * (Q)) + 8);    \
         const uint32_t xq[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};                   \
@@ -224,18 +230,19 @@ __device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, i
             A[1] = h2_fma(h_pair01(cb), s2b, b2b);                                                   \
             A[2] = h2_fma(h_pair23(ca), s2a, b2a);                                                   \
             A[3] = h2_fma(h_pair23(cb), s2b, b2b);                                                   \
-            mma_f16_16816(DQ, A, xq[2 * u], xq[2 * u + 1]);                                          \
+            mma_f16_16816(D[u], A, xq[2 * u], xq[2 * u + 1]);                                        \
         }                                                                                            \
     }
     // the low-nibble quads of ql 16c.. (Q = 0, 2) first, then ql 64 + 16c.. (Q = 1, 3)
-    QMM_MVH_Q6K_QUAD(0, D0)
-    QMM_MVH_Q6K_QUAD(2, D1)
+    QMM_MVH_Q6K_QUAD(0)
+    QMM_MVH_Q6K_QUAD(2)
     mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
     mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
-    QMM_MVH_Q6K_QUAD(1, D0)
-    QMM_MVH_Q6K_QUAD(3, D1)
+    QMM_MVH_Q6K_QUAD(1)
+    QMM_MVH_Q6K_QUAD(3)
 #undef QMM_MVH_Q6K_QUAD
-    return make_float4(D0[0] + D1[0], D0[1] + D1[1], D0[2] + D1[2], D0[3] + D1[3]);
+    return make_float4((D[0][0] + D[1][0]) + (D[2][0] + D[3][0]), (D[0][1] + D[1][1]) + (D[2][1] + D[3][1]),
+                       (D[0][2] + D[1][2]) + (D[2][2] + D[3][2]), (D[0][3] + D[1][3]) + (D[2][3] + D[3][3]));
 }
 
 // The same tile sum for any int8 scale, as lo * (q - 32) + 8 hi * (q - 32)
@@ -276,12 +283,8 @@ __device__ __noinline__ float4 q6k_tile_exact(uint32_t slot, int ra, int rb, int
                 const uint32_t hi = ((seg[r][2][u] >> (2 * Q)) & 0x03030303u) << 4;
                 cw[r] = (lo & 0x0F0F0F0Fu) | hi;
             }
-            uint32_t b0 = 0, b1 = 0;
-            if (xrow) {
-                const uint32_t* xs = reinterpret_cast<const uint32_t*>(xrow + 16 * (c + 4 * Q) + 4 * u);
-                b0 = xs[0];
-                b1 = xs[1];
-            }
+            const uint32_t* xs = reinterpret_cast<const uint32_t*>(xrow + 16 * (c + 4 * Q) + 4 * u);
+            const uint32_t b0 = xs[0], b1 = xs[1];
             const uint32_t e[4] = {h2_add(h_pair01(cw[0]), kH2M1056), h2_add(h_pair01(cw[1]), kH2M1056),
                                    h2_add(h_pair23(cw[0]), kH2M1056), h2_add(h_pair23(cw[1]), kH2M1056)};
             uint32_t A[4] = {h2_mul(e[0], lo2[0]), h2_mul(e[1], lo2[1]), h2_mul(e[2], lo2[0]),
@@ -300,7 +303,7 @@ __device__ __forceinline__ bool f4_finite(float4 v) {
 }
 
 // One q6_K stage of both tiles of an item: acc[t] += d * (tile t's sum).
-// xr: the lane's activation row at the stage's first K (null past B).
+// xr: the lane's activation row at the stage's first K.
 __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t L, uint32_t selc,
                                           const uint16_t* xr, float (&acc0)[4], float (&acc1)[4]) {
     const uint32_t sel = (L & 2u) ? 0x5432u : 0x3210u;
@@ -495,10 +498,10 @@ __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c,
                     static_cast<int>(off / 2) + static_cast<int>(bw / 2) * lane, G0, bar);
 }
 
-// The lane's activation row at the first K of stage p of matrix a (null past B).
+// The lane's activation row at the first K of stage p of matrix a (a lane
+// past the batch takes row gr % B: its results are never stored).
 __device__ __forceinline__ const uint16_t* mvh_xrow(const MvhGroup& g, const MvhMat& a, int p, int lane) {
-    const int gr = lane >> 2;
-    if (gr >= g.B) return nullptr;
+    const int gr = (lane >> 2) % g.B;
     return a.xh + static_cast<int64_t>(gr) * a.K + static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
 }
 
