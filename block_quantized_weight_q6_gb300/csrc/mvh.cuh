@@ -39,8 +39,9 @@
 // row after row: q6_K four boxes 64 bytes wide (the 14 pieces of 16 bytes a
 // super-block and its lead cover, and 2 more), so the 128-bit loads of one
 // load phase (rows 2k and 2k + 1, lanes c = 0..3 reading pieces c + s) hit 32
-// different banks; Q4_0 / Q8_0 three boxes 48 bytes wide (their 144 bytes
-// exactly), read with 32-bit loads. Box destinations are 128-byte aligned.
+// different banks; Q4_0 / Q8_0 one box 144 bytes wide (their stage, lead
+// included), read with 32-bit loads at a row base plus a constant. Box
+// destinations are 128-byte aligned.
 //
 // Each warp streams its own items through a private ring of NS stages (an
 // mbarrier per slot, waits bounded in time); a team of KS warps of a CTA may
@@ -57,9 +58,10 @@ namespace qmm {
 
 constexpr int kMvhNS = 2;
 constexpr int kMvhRows = 32;                // rows per item: two 16-row MMA tiles
-// box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 3 x 48
-__host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 48u; }
-__host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 4 : 3; }
+// box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 1 x 144
+__host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 144u; }
+__host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 4 : 1; }
+constexpr uint32_t kMvhRow32 = 144;  // Q4_0 / Q8_0 row stride in a stage slot
 constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 8 KB
 constexpr uint32_t kMvhPartOff = kMvhWarps * kMvhNS * kMvhSlot;  // team sums, after the rings
 constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 8 * 32 * 4;
@@ -112,20 +114,25 @@ __device__ __forceinline__ void mvh_lds_v4(uint32_t a, uint32_t* w) {
                  : "r"(a));
 }
 
-// q6_K stage slot: shared address of 16-byte piece p of row r (four boxes of
-// [32 rows][64 B], 2 KB apart).
-__device__ __forceinline__ uint32_t q6k_piece(uint32_t slot, int r, int p) {
-    return slot + static_cast<uint32_t>(p >> 2) * 2048u + 64u * static_cast<uint32_t>(r) +
-           16u * static_cast<uint32_t>(p & 3);
+// q6_K stage slot: offset of 16-byte piece p of a row from the row's base
+// (slot + 64 r): four boxes of [32 rows][64 B], 2 KB apart.
+__host__ __device__ constexpr uint32_t q6k_poff(int p) {
+    return static_cast<uint32_t>(p >> 2) * 2048u + 16u * static_cast<uint32_t>(p & 3);
 }
 
+// The lane's piece offsets (pieces c, c + 1, 4 + c, 5 + c, 8 + c, 9 + c),
+// computed once.
+struct Q6Off {
+    uint32_t o[6];
+};
+
 // The 16 bytes at byte lead L (even, < 16; QW = L / 4 and sel shifts by
-// L % 4) of piece p of row r and the next piece.
+// L % 4) of the pieces at row base + oa and row base + ob.
 template <int QW>
-__device__ __forceinline__ void mvh_seg(uint32_t slot, int r, int p, uint32_t sel, uint32_t (&o)[4]) {
+__device__ __forceinline__ void mvh_seg(uint32_t row, uint32_t oa, uint32_t ob, uint32_t sel, uint32_t (&o)[4]) {
     uint32_t w[8];
-    mvh_lds_v4(q6k_piece(slot, r, p), w);
-    mvh_lds_v4(q6k_piece(slot, r, p + 1), w + 4);
+    mvh_lds_v4(row + oa, w);
+    mvh_lds_v4(row + ob, w + 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = __byte_perm(w[QW + i], w[QW + i + 1], sel);
 }
@@ -133,37 +140,26 @@ __device__ __forceinline__ void mvh_seg(uint32_t slot, int r, int p, uint32_t se
 // The scale segment (16 bytes at lead L of pieces 12, 13) and the
 // super-block's d, which follows it (bytes 208, 209 of the super-block).
 template <int QW>
-__device__ __forceinline__ uint32_t mvh_seg_sc_d(uint32_t slot, int r, uint32_t sel, uint32_t L,
-                                                 uint32_t (&o)[4]) {
+__device__ __forceinline__ uint32_t mvh_seg_sc_d(uint32_t row, uint32_t sel, uint32_t L, uint32_t (&o)[4]) {
     uint32_t w[8];
-    mvh_lds_v4(q6k_piece(slot, r, 12), w);
-    mvh_lds_v4(q6k_piece(slot, r, 13), w + 4);
+    mvh_lds_v4(row + q6k_poff(12), w);
+    mvh_lds_v4(row + q6k_poff(13), w + 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = __byte_perm(w[QW + i], w[QW + i + 1], sel);
     return (w[4 + QW] >> (8u * (L & 2u))) & 0xFFFFu;
 }
 
-// Q4_0 / Q8_0 stage slot: shared address of logical byte o of row r (three
-// boxes of [32 rows][48 B], 1536 bytes apart).
-__device__ __forceinline__ uint32_t mvh_addr(uint32_t slot, int r, uint32_t o) {
-    return slot + (o / 48u) * 1536u + 48u * static_cast<uint32_t>(r) + (o % 48u);
-}
-
-// Four bytes at logical byte o of row r; ALIGNED says whether o % 4 == 0
-// (else o % 4 == 2, and the word is put together from the aligned words
-// around it; an aligned word never straddles two boxes).
-template <bool ALIGNED>
-__device__ __forceinline__ uint32_t mvh_word(uint32_t slot, int r, uint32_t o) {
+// Q4_0 / Q8_0: four bytes at offset o (a compile-time constant) from the
+// lane's row base; ALIGNED says whether the base + o is a multiple of 4
+// (else it is 2 past one, and the word is put together from the aligned
+// words around it).
+template <bool ALIGNED, uint32_t O>
+__device__ __forceinline__ uint32_t mvh_word(uint32_t base) {
     if constexpr (ALIGNED) {
-        return lds_u32(mvh_addr(slot, r, o));
+        return lds_u32(base + O);
     } else {
-        const uint32_t o0 = o - 2;
-        return __byte_perm(lds_u32(mvh_addr(slot, r, o0)), lds_u32(mvh_addr(slot, r, o0 + 4)), 0x5432);
+        return __byte_perm(lds_u32(base + O - 2), lds_u32(base + O + 2), 0x5432);
     }
-}
-
-__device__ __forceinline__ float mvh_half(uint32_t slot, int r, uint32_t o) {
-    return half_bits_to_float(lds_u16(mvh_addr(slot, r, o)));
 }
 
 // Eight activations (16 bytes) at element offset off of the lane's row xr.
@@ -200,16 +196,17 @@ __device__ __forceinline__ int q6k_sc(uint32_t w, int c) {
 // makes the bias -1056 * sc overflow to an infinity, so the sum is not finite
 // and the caller recomputes the tile in the exact form. Four accumulator
 // chains (one per position u in the group) keep consecutive MMAs independent.
+// pa, pb: the bases (slot + 64 r) of the tile's rows g and g + 8.
 template <int QW>
-__device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, int c, uint32_t sel, uint32_t L,
-                                                uint32_t selc, const uint16_t* xr, float& da, float& db) {
+__device__ __forceinline__ float4 q6k_tile_fast(uint32_t pa, uint32_t pb, const Q6Off& po, uint32_t sel, uint32_t L,
+                                                uint32_t selc, const uint16_t* xr, int c, float& da, float& db) {
     uint32_t qa0[4], qa1[4], ha[4], sa[4], qb0[4], qb1[4], hb[4], sb[4];
-    da = half_bits_to_float(mvh_seg_sc_d<QW>(slot, ra, sel, L, sa));
-    db = half_bits_to_float(mvh_seg_sc_d<QW>(slot, rb, sel, L, sb));
-    mvh_seg<QW>(slot, ra, c, sel, qa0);
-    mvh_seg<QW>(slot, rb, c, sel, qb0);
-    mvh_seg<QW>(slot, ra, 8 + c, sel, ha);
-    mvh_seg<QW>(slot, rb, 8 + c, sel, hb);
+    da = half_bits_to_float(mvh_seg_sc_d<QW>(pa, sel, L, sa));
+    db = half_bits_to_float(mvh_seg_sc_d<QW>(pb, sel, L, sb));
+    mvh_seg<QW>(pa, po.o[0], po.o[1], sel, qa0);
+    mvh_seg<QW>(pb, po.o[0], po.o[1], sel, qb0);
+    mvh_seg<QW>(pa, po.o[4], po.o[5], sel, ha);
+    mvh_seg<QW>(pb, po.o[4], po.o[5], sel, hb);
     // one accumulator per u: the four MMAs of a quad are independent
     float D[4][4];
 #pragma unroll
@@ -236,8 +233,8 @@ __device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, i
     // the low-nibble quads of ql 16c.. (Q = 0, 2) first, then ql 64 + 16c.. (Q = 1, 3)
     QMM_MVH_Q6K_QUAD(0)
     QMM_MVH_Q6K_QUAD(2)
-    mvh_seg<QW>(slot, ra, 4 + c, sel, qa1);
-    mvh_seg<QW>(slot, rb, 4 + c, sel, qb1);
+    mvh_seg<QW>(pa, po.o[2], po.o[3], sel, qa1);
+    mvh_seg<QW>(pb, po.o[2], po.o[3], sel, qb1);
     QMM_MVH_Q6K_QUAD(1)
     QMM_MVH_Q6K_QUAD(3)
 #undef QMM_MVH_Q6K_QUAD
@@ -247,22 +244,20 @@ __device__ __forceinline__ float4 q6k_tile_fast(uint32_t slot, int ra, int rb, i
 
 // The same tile sum for any int8 scale, as lo * (q - 32) + 8 hi * (q - 32)
 // (sc = lo + 8 hi, 0 <= lo < 8), both exact in fp16, in two MMAs. Kept out
-// of line (it only runs for scales outside -62..62): it reads the lead, the
-// code bytes and the activations itself.
-__device__ __noinline__ float4 q6k_tile_exact(uint32_t slot, int ra, int rb, int c, uint32_t L,
-                                              const uint16_t* xrow) {
+// of line (it only runs for scales outside -62..62): it reads the code bytes
+// byte by byte and the activations itself.
+__device__ __noinline__ float4 q6k_tile_exact(uint32_t pa, uint32_t pb, int c, uint32_t L, const uint16_t* xrow) {
     uint32_t seg[2][4][4];  // row, segment (ql c, ql 4 + c, qh c, scales), word
-    const int rows[2] = {ra, rb};
+    const uint32_t rows[2] = {pa, pb};
     const int piece[4] = {c, 4 + c, 8 + c, 12};
     for (int r = 0; r < 2; ++r)
         for (int q = 0; q < 4; ++q)
             for (int i = 0; i < 4; ++i) {
-                // word i of the 16 bytes at lead L of the piece, byte by byte
                 uint32_t w = 0;
                 for (int bt = 0; bt < 4; ++bt) {
                     const uint32_t o = L + 4 * i + bt;  // byte inside the piece pair
-                    const uint32_t v = lds_u16(q6k_piece(slot, rows[r], piece[q] + static_cast<int>(o >> 4)) +
-                                               ((o & 15u) & ~1u));
+                    const uint32_t v =
+                        lds_u16(rows[r] + q6k_poff(piece[q] + static_cast<int>(o >> 4)) + ((o & 15u) & ~1u));
                     w |= ((v >> (8 * (o & 1u))) & 0xFFu) << (8 * bt);
                 }
                 seg[r][q][i] = w;
@@ -304,21 +299,21 @@ __device__ __forceinline__ bool f4_finite(float4 v) {
 
 // One q6_K stage of both tiles of an item: acc[t] += d * (tile t's sum).
 // xr: the lane's activation row at the stage's first K.
-__device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t L, uint32_t selc,
+__device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, const Q6Off& po, uint32_t L, uint32_t selc,
                                           const uint16_t* xr, float (&acc0)[4], float (&acc1)[4]) {
     const uint32_t sel = (L & 2u) ? 0x5432u : 0x3210u;
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
-        const int ra = 16 * t + g, rb = ra + 8;
+        const uint32_t pa = slot + 64u * static_cast<uint32_t>(16 * t + g), pb = pa + 64u * 8u;
         float4 D;
         float da, db;
         switch (L >> 2) {
-            case 0: D = q6k_tile_fast<0>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
-            case 1: D = q6k_tile_fast<1>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
-            case 2: D = q6k_tile_fast<2>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
-            default: D = q6k_tile_fast<3>(slot, ra, rb, c, sel, L, selc, xr, da, db); break;
+            case 0: D = q6k_tile_fast<0>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+            case 1: D = q6k_tile_fast<1>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+            case 2: D = q6k_tile_fast<2>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+            default: D = q6k_tile_fast<3>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
         }
-        if (__any_sync(0xffffffffu, !f4_finite(D))) D = q6k_tile_exact(slot, ra, rb, c, L, xr);
+        if (__any_sync(0xffffffffu, !f4_finite(D))) D = q6k_tile_exact(pa, pb, c, L, xr);
         if (t == 0) {
             acc0[0] = fmaf(da, D.x, acc0[0]);
             acc0[1] = fmaf(da, D.y, acc0[1]);
@@ -334,22 +329,21 @@ __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, uint32_t 
 }
 
 // ------------------------------------------------------------ Q4_0 / Q8_0 stages
-// Block b of the stage; lane c's weights 8c .. 8c + 7 (MMA u = 0: 8c .. + 3,
-// u = 1: 8c + 4 .. + 7), whose activations are x[4b .. 4b + 3].
-// Q4_0 (18 B: d | qs[16]): weight e is nibble e / 16 of qs[e % 16], so the
-// lane's codes are nibble c / 2 of qs[8 (c % 2) .. + 7].
+// Block BLK of the stage; lane c's weights 8c .. 8c + 7 (MMA u = 0: 8c .. + 3,
+// u = 1: 8c + 4 .. + 7). Rows are 144 bytes apart in the slot.
+// Q4_0 (18 B: d | qs[16]), lead 0: weight e is nibble e / 16 of qs[e % 16],
+// so the lane's codes are nibble c / 2 of qs[8 (c % 2) .. + 7]. ra, rb: the
+// rows' bases (slot + 144 r); la, lb: the same plus 8 (c % 2).
 template <int BLK>
-__device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c, const uint16_t* xr,
-                                           float (&acc)[4]) {
+__device__ __forceinline__ void q4_0_block(uint32_t ra, uint32_t rb, uint32_t la, uint32_t lb, uint32_t sh, int c,
+                                           const uint16_t* xr, float (&acc)[4]) {
+    constexpr uint32_t O = 18 * BLK + 2;  // qs of block BLK: O % 4 is 0 for odd BLK, 2 for even
+    constexpr bool AL = (O % 4) == 0;
     const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
-    constexpr uint32_t o = 18 * BLK + 2;          // qs of block BLK (o % 4 is 0 for odd BLK, 2 for even)
-    constexpr bool AL = (o % 4) == 0;
-    const uint32_t oq = o + 8u * static_cast<uint32_t>(c & 1);
-    const uint32_t sh = 4u * static_cast<uint32_t>(c >> 1);
-    const uint32_t a0 = (mvh_word<AL>(slot, ra, oq) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t a1 = (mvh_word<AL>(slot, ra, oq + 4) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t b0 = (mvh_word<AL>(slot, rb, oq) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t b1 = (mvh_word<AL>(slot, rb, oq + 4) >> sh) & 0x0F0F0F0Fu;
+    const uint32_t a0 = (mvh_word<AL, O>(la) >> sh) & 0x0F0F0F0Fu;
+    const uint32_t a1 = (mvh_word<AL, O + 4>(la) >> sh) & 0x0F0F0F0Fu;
+    const uint32_t b0 = (mvh_word<AL, O>(lb) >> sh) & 0x0F0F0F0Fu;
+    const uint32_t b1 = (mvh_word<AL, O + 4>(lb) >> sh) & 0x0F0F0F0Fu;
     float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     uint32_t A[4];
     A[0] = h2_add(h_pair01(a0), kH2M1032);
@@ -362,7 +356,7 @@ __device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c,
     A[2] = h2_add(h_pair23(a1), kH2M1032);
     A[3] = h2_add(h_pair23(b1), kH2M1032);
     mma_f16_16816(D, A, xv.z, xv.w);
-    const float da = mvh_half(slot, ra, 18 * BLK), db = mvh_half(slot, rb, 18 * BLK);
+    const float da = half_bits_to_float(lds_u16(ra + 18 * BLK)), db = half_bits_to_float(lds_u16(rb + 18 * BLK));
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
     acc[2] = fmaf(db, D[2], acc[2]);
@@ -370,18 +364,17 @@ __device__ __forceinline__ void q4_0_block(uint32_t slot, int ra, int rb, int c,
 }
 
 // Q8_0 (34 B: d | qs[32] int8), blocks at lead L (0 or 8); the lane's codes
-// are qs[8c .. 8c + 7].
+// are qs[8c .. 8c + 7]. ra, rb: the rows' bases plus L; la, lb: plus 8c more.
 template <int BLK>
-__device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c, uint32_t L, const uint16_t* xr,
-                                           float (&acc)[4]) {
+__device__ __forceinline__ void q8_0_block(uint32_t ra, uint32_t rb, uint32_t la, uint32_t lb, int c,
+                                           const uint16_t* xr, float (&acc)[4]) {
+    constexpr uint32_t O = 34 * BLK + 2;  // O % 4 is 0 for odd BLK, 2 for even (L % 4 == 0)
+    constexpr bool AL = (O % 4) == 0;
     const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
-    constexpr uint32_t o = 34 * BLK + 2;          // o % 4 is 0 for odd BLK, 2 for even (L % 4 == 0)
-    constexpr bool AL = (o % 4) == 0;
-    const uint32_t oq = L + o + 8u * static_cast<uint32_t>(c);
-    const uint32_t a0 = mvh_word<AL>(slot, ra, oq) ^ 0x80808080u;
-    const uint32_t a1 = mvh_word<AL>(slot, ra, oq + 4) ^ 0x80808080u;
-    const uint32_t b0 = mvh_word<AL>(slot, rb, oq) ^ 0x80808080u;
-    const uint32_t b1 = mvh_word<AL>(slot, rb, oq + 4) ^ 0x80808080u;
+    const uint32_t a0 = mvh_word<AL, O>(la) ^ 0x80808080u;
+    const uint32_t a1 = mvh_word<AL, O + 4>(la) ^ 0x80808080u;
+    const uint32_t b0 = mvh_word<AL, O>(lb) ^ 0x80808080u;
+    const uint32_t b1 = mvh_word<AL, O + 4>(lb) ^ 0x80808080u;
     float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     uint32_t A[4];
     A[0] = h2_add(h_pair01(a0), kH2M1152);
@@ -394,7 +387,7 @@ __device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c,
     A[2] = h2_add(h_pair23(a1), kH2M1152);
     A[3] = h2_add(h_pair23(b1), kH2M1152);
     mma_f16_16816(D, A, xv.z, xv.w);
-    const float da = mvh_half(slot, ra, L + 34 * BLK), db = mvh_half(slot, rb, L + 34 * BLK);
+    const float da = half_bits_to_float(lds_u16(ra + 34 * BLK)), db = half_bits_to_float(lds_u16(rb + 34 * BLK));
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
     acc[2] = fmaf(db, D[2], acc[2]);
@@ -403,18 +396,20 @@ __device__ __forceinline__ void q8_0_block(uint32_t slot, int ra, int rb, int c,
 
 __device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint16_t* xr, float (&acc0)[4],
                                            float (&acc1)[4]) {
+    const uint32_t sh = 4u * static_cast<uint32_t>(c >> 1), lo = 8u * static_cast<uint32_t>(c & 1);
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
-        const int ra = 16 * t + g, rb = ra + 8;
+        const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(16 * t + g), rb = ra + 8u * kMvhRow32;
+        const uint32_t la = ra + lo, lb = rb + lo;
         float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        q4_0_block<0>(slot, ra, rb, c, xr, a);
-        q4_0_block<1>(slot, ra, rb, c, xr, a);
-        q4_0_block<2>(slot, ra, rb, c, xr, a);
-        q4_0_block<3>(slot, ra, rb, c, xr, a);
-        q4_0_block<4>(slot, ra, rb, c, xr, a);
-        q4_0_block<5>(slot, ra, rb, c, xr, a);
-        q4_0_block<6>(slot, ra, rb, c, xr, a);
-        q4_0_block<7>(slot, ra, rb, c, xr, a);
+        q4_0_block<0>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<1>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<2>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<3>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<4>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<5>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<6>(ra, rb, la, lb, sh, c, xr, a);
+        q4_0_block<7>(ra, rb, la, lb, sh, c, xr, a);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (t == 0) acc0[q] += a[q];
@@ -427,12 +422,13 @@ __device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t
                                            float (&acc0)[4], float (&acc1)[4]) {
 #pragma unroll 1
     for (int t = 0; t < 2; ++t) {
-        const int ra = 16 * t + g, rb = ra + 8;
+        const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(16 * t + g) + L, rb = ra + 8u * kMvhRow32;
+        const uint32_t la = ra + 8u * static_cast<uint32_t>(c), lb = rb + 8u * static_cast<uint32_t>(c);
         float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        q8_0_block<0>(slot, ra, rb, c, L, xr, a);
-        q8_0_block<1>(slot, ra, rb, c, L, xr, a);
-        q8_0_block<2>(slot, ra, rb, c, L, xr, a);
-        q8_0_block<3>(slot, ra, rb, c, L, xr, a);
+        q8_0_block<0>(ra, rb, la, lb, c, xr, a);
+        q8_0_block<1>(ra, rb, la, lb, c, xr, a);
+        q8_0_block<2>(ra, rb, la, lb, c, xr, a);
+        q8_0_block<3>(ra, rb, la, lb, c, xr, a);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             if (t == 0) acc0[q] += a[q];
@@ -498,11 +494,9 @@ __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c,
                     static_cast<int>(off / 2) + static_cast<int>(bw / 2) * lane, G0, bar);
 }
 
-// The lane's activation row at the first K of stage p of matrix a (a lane
-// past the batch takes row gr % B: its results are never stored).
-__device__ __forceinline__ const uint16_t* mvh_xrow(const MvhGroup& g, const MvhMat& a, int p, int lane) {
-    const int gr = (lane >> 2) % g.B;
-    return a.xh + static_cast<int64_t>(gr) * a.K + static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
+// The lane's activation row (xb: its batch row) at the first K of stage p.
+__device__ __forceinline__ const uint16_t* mvh_xrow(const MvhMat& a, int xb, int p) {
+    return a.xh + static_cast<int64_t>(xb) * a.K + static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
 }
 
 // Bounded wait for the TMA copies of a slot; false (and the error word set)
@@ -542,6 +536,14 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
     const int gt = team * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
     // byte selector: byte c of a word into the low bytes of two fp16 (1024 + byte)
     const uint32_t selc = 0x4040u | (static_cast<uint32_t>(c) << 8) | static_cast<uint32_t>(c);
+    Q6Off po;
+    po.o[0] = q6k_poff(c);
+    po.o[1] = q6k_poff(c + 1);
+    po.o[2] = q6k_poff(4 + c);
+    po.o[3] = q6k_poff(5 + c);
+    po.o[4] = q6k_poff(8 + c);
+    po.o[5] = q6k_poff(9 + c);
+    const int xrow_b = gr % g.B;  // a lane past the batch reads a valid row (never stored)
 
     grid_launch_dependents();
     live_bump(g.st, g.live_slot);
@@ -597,12 +599,12 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
                 ++issued;
                 mvh_advance(g, ks, member, nteams, ic);
             }
-            const uint16_t* xr = mvh_xrow(g, a, p, lane);
+            const uint16_t* xr = mvh_xrow(a, xrow_b, p);
             const uint32_t slot = ring + (used % kMvhNS) * kMvhSlot;
             if (ok) ok = mvh_wait(bars + 8 * (used % kMvhNS), (used / kMvhNS) & 1u, g.st.err);
             ++used;
             const uint32_t L = static_cast<uint32_t>(mvh_stage_off(a, j, p) & 15);
-            if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, L, selc, xr, acc0, acc1);
+            if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc0, acc1);
             else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc0, acc1);
             else q8_0_stage(slot, gr, c, L, xr, acc0, acc1);
             __syncwarp();
