@@ -92,10 +92,10 @@ cudaError_t mv8_launch(int fmt, int grid, cudaStream_t s, const Mv1Group& g);
 
 // ---------------------------------------------------------------- batch 1-8 fp16-MMA matvec
 // 1..8 bf16 activation rows, float mode, any mix of the three formats in one
-// launch, on the warp-level MMA with fp16 operands (mvh.cuh): work item = 32
+// launch, on the warp-level MMA with fp16 operands (mvh.cuh): work item = 16
 // rows of one matrix at stride 8, all of its K. Needs K % 256 == 0 and
 // N % 8 == 0, and workspace for the fp16 activations (mvh_workspace_bytes).
-constexpr int kMvhWarps = 12;
+constexpr int kMvhWarps = 16;
 constexpr int kMvhMaxMats = 12;
 struct MvhMat {
     const uint8_t* W;

@@ -193,7 +193,7 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
         a.rowbytes = K[m] / block_elems(a.fmt) * block_bytes(a.fmt);
         a.stages = static_cast<int>(K[m] / (a.fmt == FMT_Q8_0 ? 128 : 256));
         a.item0 = static_cast<int>(items);
-        items += (N[m] + 255) / 256 * 8;
+        items += (N[m] + 8 * kMvhRows - 1) / (8 * kMvhRows) * 8;
         min_stages = std::min(min_stages, a.stages);
         const cuuint64_t dims[2] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(N[m] / 8)};
         const cuuint64_t strides[1] = {static_cast<cuuint64_t>(8 * a.rowbytes)};
@@ -211,7 +211,7 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     const int64_t warps = static_cast<int64_t>(sms) * kMvhWarps;
     // (a divisor of the CTA's warps: teams never span two CTAs)
     g.ks = 1;
-    for (int k : {1, 2, 3, 4, 6, 12}) {
+    for (int k : {1, 2, 4, 8, 16}) {
         if (k > min_stages) break;
         g.ks = k;
         if (items * k >= warps) break;

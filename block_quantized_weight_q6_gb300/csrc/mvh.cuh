@@ -29,13 +29,13 @@
 //   bytes are three 16-byte runs of ql / qh; Q4_0 / Q8_0: weights 8c .. 8c + 7
 //   of each block. Its activations are runs of 16 bytes.
 //
-// Work item: 32 rows of one matrix at stride 8 (rows j + 8 (G + i), i < 32),
+// Work item: 16 rows of one matrix at stride 8 (rows j + 8 (G + i), i < 16),
 // all of K in stages (q6_K one super-block, Q4_0 8 blocks, Q8_0 4 blocks).
 // Rows 8 apart start at the same offset modulo 16 (the pitch of 8 rows is a
 // multiple of 16 for every even row size), so the byte lead of a stage is
-// the same for all 32 rows of an item and the realignment of the code bytes
+// the same for all 16 rows of an item and the realignment of the code bytes
 // is warp-uniform. A stage arrives by 2-D TMA with W seen as
-// [N / 8][8 * rowbytes] 16-bit elements, in boxes 32 rows high that land
+// [N / 8][8 * rowbytes] 16-bit elements, in boxes 16 rows high that land
 // row after row: q6_K four boxes 64 bytes wide (the 14 pieces of 16 bytes a
 // super-block and its lead cover, and 2 more), so the 128-bit loads of one
 // load phase (rows 2k and 2k + 1, lanes c = 0..3 reading pieces c + s) hit 32
@@ -56,15 +56,15 @@
 
 namespace qmm {
 
-constexpr int kMvhNS = 2;
-constexpr int kMvhRows = 32;                // rows per item: two 16-row MMA tiles
+constexpr int kMvhNS = 3;
+constexpr int kMvhRows = 16;                // rows per item: one 16-row MMA tile
 // box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 1 x 144
 __host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 144u; }
 __host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 4 : 1; }
 constexpr uint32_t kMvhRow32 = 144;  // Q4_0 / Q8_0 row stride in a stage slot
-constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 8 KB
+constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 4 KB
 constexpr uint32_t kMvhPartOff = kMvhWarps * kMvhNS * kMvhSlot;  // team sums, after the rings
-constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 8 * 32 * 4;
+constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 4 * 32 * 4;
 constexpr uint32_t kMvhFifoOff = kMvhBarOff + kMvhWarps * kMvhNS * 8;  // per warp: 4 item numbers
 constexpr uint32_t kMvhSmem = kMvhFifoOff + kMvhWarps * 16;
 static_assert(kMvhSmem <= 227u * 1024, "shared memory");
@@ -115,9 +115,9 @@ __device__ __forceinline__ void mvh_lds_v4(uint32_t a, uint32_t* w) {
 }
 
 // q6_K stage slot: offset of 16-byte piece p of a row from the row's base
-// (slot + 64 r): four boxes of [32 rows][64 B], 2 KB apart.
+// (slot + 64 r): four boxes of [kMvhRows rows][64 B].
 __host__ __device__ constexpr uint32_t q6k_poff(int p) {
-    return static_cast<uint32_t>(p >> 2) * 2048u + 16u * static_cast<uint32_t>(p & 3);
+    return static_cast<uint32_t>(p >> 2) * (64u * kMvhRows) + 16u * static_cast<uint32_t>(p & 3);
 }
 
 // The lane's piece offsets (pieces c, c + 1, 4 + c, 5 + c, 8 + c, 9 + c),
@@ -170,7 +170,7 @@ __device__ __forceinline__ uint4 mvh_x8(const uint16_t* xr, int off) {
 }
 
 // ------------------------------------------------------------ q6_K stage
-// One 16-row tile: rows ra (lane row g) and rb (g + 8) of the stage. Lane c's
+// The 16-row tile: rows g and g + 8 of the stage for lane (g, c). Lane c's
 // scale groups are c + 4Q (Q = 0..3): ql bytes 16c .. (Q = 0 low nibble, Q = 2
 // high) and 64 + 16c .. (Q = 1 low, Q = 3 high), qh bytes 16c .. (2-bit
 // field Q), scale byte c of scale word Q. MMA (Q, u) takes the lane's weights
@@ -297,35 +297,25 @@ __device__ __forceinline__ bool f4_finite(float4 v) {
     return isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w);
 }
 
-// One q6_K stage of both tiles of an item: acc[t] += d * (tile t's sum).
+// One q6_K stage of the item's tile: acc += d * (the tile's sum).
 // xr: the lane's activation row at the stage's first K.
 __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, const Q6Off& po, uint32_t L, uint32_t selc,
-                                          const uint16_t* xr, float (&acc0)[4], float (&acc1)[4]) {
+                                          const uint16_t* xr, float (&acc)[4]) {
     const uint32_t sel = (L & 2u) ? 0x5432u : 0x3210u;
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        const uint32_t pa = slot + 64u * static_cast<uint32_t>(16 * t + g), pb = pa + 64u * 8u;
-        float4 D;
-        float da, db;
-        switch (L >> 2) {
-            case 0: D = q6k_tile_fast<0>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
-            case 1: D = q6k_tile_fast<1>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
-            case 2: D = q6k_tile_fast<2>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
-            default: D = q6k_tile_fast<3>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
-        }
-        if (__any_sync(0xffffffffu, !f4_finite(D))) D = q6k_tile_exact(pa, pb, c, L, xr);
-        if (t == 0) {
-            acc0[0] = fmaf(da, D.x, acc0[0]);
-            acc0[1] = fmaf(da, D.y, acc0[1]);
-            acc0[2] = fmaf(db, D.z, acc0[2]);
-            acc0[3] = fmaf(db, D.w, acc0[3]);
-        } else {
-            acc1[0] = fmaf(da, D.x, acc1[0]);
-            acc1[1] = fmaf(da, D.y, acc1[1]);
-            acc1[2] = fmaf(db, D.z, acc1[2]);
-            acc1[3] = fmaf(db, D.w, acc1[3]);
-        }
+    const uint32_t pa = slot + 64u * static_cast<uint32_t>(g), pb = pa + 64u * 8u;
+    float4 D;
+    float da, db;
+    switch (L >> 2) {
+        case 0: D = q6k_tile_fast<0>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+        case 1: D = q6k_tile_fast<1>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+        case 2: D = q6k_tile_fast<2>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
+        default: D = q6k_tile_fast<3>(pa, pb, po, sel, L, selc, xr, c, da, db); break;
     }
+    if (__any_sync(0xffffffffu, !f4_finite(D))) D = q6k_tile_exact(pa, pb, c, L, xr);
+    acc[0] = fmaf(da, D.x, acc[0]);
+    acc[1] = fmaf(da, D.y, acc[1]);
+    acc[2] = fmaf(db, D.z, acc[2]);
+    acc[3] = fmaf(db, D.w, acc[3]);
 }
 
 // ------------------------------------------------------------ Q4_0 / Q8_0 stages
@@ -394,47 +384,28 @@ __device__ __forceinline__ void q8_0_block(uint32_t ra, uint32_t rb, uint32_t la
     acc[3] = fmaf(db, D[3], acc[3]);
 }
 
-__device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint16_t* xr, float (&acc0)[4],
-                                           float (&acc1)[4]) {
+__device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint16_t* xr, float (&acc)[4]) {
     const uint32_t sh = 4u * static_cast<uint32_t>(c >> 1), lo = 8u * static_cast<uint32_t>(c & 1);
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(16 * t + g), rb = ra + 8u * kMvhRow32;
-        const uint32_t la = ra + lo, lb = rb + lo;
-        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        q4_0_block<0>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<1>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<2>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<3>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<4>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<5>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<6>(ra, rb, la, lb, sh, c, xr, a);
-        q4_0_block<7>(ra, rb, la, lb, sh, c, xr, a);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (t == 0) acc0[q] += a[q];
-            else acc1[q] += a[q];
-        }
-    }
+    const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(g), rb = ra + 8u * kMvhRow32;
+    const uint32_t la = ra + lo, lb = rb + lo;
+    q4_0_block<0>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<1>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<2>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<3>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<4>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<5>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<6>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<7>(ra, rb, la, lb, sh, c, xr, acc);
 }
 
 __device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t L, const uint16_t* xr,
-                                           float (&acc0)[4], float (&acc1)[4]) {
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(16 * t + g) + L, rb = ra + 8u * kMvhRow32;
-        const uint32_t la = ra + 8u * static_cast<uint32_t>(c), lb = rb + 8u * static_cast<uint32_t>(c);
-        float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        q8_0_block<0>(ra, rb, la, lb, c, xr, a);
-        q8_0_block<1>(ra, rb, la, lb, c, xr, a);
-        q8_0_block<2>(ra, rb, la, lb, c, xr, a);
-        q8_0_block<3>(ra, rb, la, lb, c, xr, a);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (t == 0) acc0[q] += a[q];
-            else acc1[q] += a[q];
-        }
-    }
+                                           float (&acc)[4]) {
+    const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(g) + L, rb = ra + 8u * kMvhRow32;
+    const uint32_t la = ra + 8u * static_cast<uint32_t>(c), lb = rb + 8u * static_cast<uint32_t>(c);
+    q8_0_block<0>(ra, rb, la, lb, c, xr, acc);
+    q8_0_block<1>(ra, rb, la, lb, c, xr, acc);
+    q8_0_block<2>(ra, rb, la, lb, c, xr, acc);
+    q8_0_block<3>(ra, rb, la, lb, c, xr, acc);
 }
 
 // ------------------------------------------------------------ the kernel
@@ -576,7 +547,7 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
         const MvhMat& a = g.m[m];
         const int li = it - a.item0;
         const int j = li & 7, G0 = (li >> 3) * kMvhRows;
-        float acc0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, acc1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int p = member; p < a.stages; p += ks) {
             // the next item of a single warp's walk, claimed once the
             // copies have reached the end of the current one
@@ -604,43 +575,35 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
             if (ok) ok = mvh_wait(bars + 8 * (used % kMvhNS), (used / kMvhNS) & 1u, g.st.err);
             ++used;
             const uint32_t L = static_cast<uint32_t>(mvh_stage_off(a, j, p) & 15);
-            if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc0, acc1);
-            else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc0, acc1);
-            else q8_0_stage(slot, gr, c, L, xr, acc0, acc1);
+            if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc);
+            else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc);
+            else q8_0_stage(slot, gr, c, L, xr, acc);
             __syncwarp();
-        }
-        float acc[2][4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            acc[0][q] = acc0[q];
-            acc[1][q] = acc1[q];
         }
         // the team's sums of the item, added by member 0 in member order
         if (ks > 1) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) part[(warp * 8 + q) * 32 + lane] = acc[q >> 2][q & 3];
+            for (int q = 0; q < 4; ++q) part[(warp * 4 + q) * 32 + lane] = acc[q];
             mvh_team_sync(team, ks);
             if (member == 0) {
                 for (int t2 = 1; t2 < ks; ++t2)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[q >> 2][q & 3] += part[((warp + t2) * 8 + q) * 32 + lane];
+                    for (int q = 0; q < 4; ++q) acc[q] += part[((warp + t2) * 4 + q) * 32 + lane];
             }
             mvh_team_sync(team, ks);  // the partial sums are read before they are overwritten
         }
         if (member == 0) {
-            // lane (g, c): item rows 16t + g and 16t + g + 8, batch rows 2c, 2c + 1
+            // lane (g, c): item rows g and g + 8, batch rows 2c, 2c + 1
 #pragma unroll
             for (int b2 = 0; b2 < 2; ++b2) {
                 const int b = 2 * c + b2;
                 if (b >= g.B) continue;
                 const float sc = a.xinv[b];
 #pragma unroll
-                for (int t = 0; t < 2; ++t)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t n = static_cast<int64_t>(j) + 8 * (G0 + 16 * t + gr + 8 * h);
-                        if (n < a.N) a.y[static_cast<int64_t>(b) * a.N + n] = acc[t][2 * h + b2] * sc;
-                    }
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t n = static_cast<int64_t>(j) + 8 * (G0 + gr + 8 * h);
+                    if (n < a.N) a.y[static_cast<int64_t>(b) * a.N + n] = acc[2 * h + b2] * sc;
+                }
             }
         }
         if (ks > 1) {
