@@ -24,7 +24,7 @@ LIVE = {
     "gemv_float": 0, "gemv_q8": 1, "gemv_splitk_reduce": 2, "quantize": 3, "plane_build": 4,
     "gemm_exp_plane": 5, "gemm_in_kernel": 6, "gemm_exp_off": 7, "gemm_fallback": 8,
     "gemm_q4_0": 9, "route": 10, "moe_gate_up": 11, "moe_down": 12, "moe_combine": 13,
-    "x_tile": 14, "moe_plan": 15, "moe_gather": 16, "gemv_mv1": 17, "gemv_mv8": 18,
+    "x_tile": 14, "moe_plan": 15, "moe_gather": 16, "gemv_mv1": 17, "gemv_mv8": 18, "moe_silu": 19,
 }
 LIVE_COUNT = 24
 

@@ -74,6 +74,8 @@ void read_env() {
     g_env.mv1_on = !(mv && std::strcmp(mv, "0") == 0);
     const char* m8 = std::getenv("QMM_MV8");
     g_env.mv8_on = !(m8 && std::strcmp(m8, "0") == 0);
+    const char* mm = std::getenv("QMM_MOE_MMA");
+    qmm::g_moe_mvh_enabled = !(mm && std::strcmp(mm, "0") == 0);
     const char* mh = std::getenv("QMM_MVH");
     g_env.mvh_on = !(mh && std::strcmp(mh, "0") == 0);
     const char* pdl = std::getenv("QMM_PDL");

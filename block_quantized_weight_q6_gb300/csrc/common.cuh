@@ -127,6 +127,17 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 3-D tiled tensor-map copy global -> shared (this CTA), completing on an
+// mbarrier. x (innermost) times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, "
+        "{%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared accesses before later
 // async-proxy (TMA / tensor core) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {

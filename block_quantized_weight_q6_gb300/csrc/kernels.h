@@ -122,6 +122,28 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
                     float* const* y, const int64_t* N, const int64_t* K, int B, void* ws, int sms,
                     cudaStream_t s, DevState st);
 
+// The routed-expert matvecs on the same kernel (mvh.cu): the tasks (expert,
+// first grouped slot, tokens) come from moe.cu's plan kernel; an expert
+// table is one tensor map with the expert as its third coordinate, so the
+// experts of a table must lie at one fixed stride.
+struct MoeTask {
+    int expert, pos, n;  // expert, first grouped slot, tokens
+};
+struct MvhMoeTables {
+    const void* base[3];   // gate, up, down of expert 0
+    int64_t stride[3];     // bytes from one expert's matrix to the next
+};
+// rows a task of the fp16-MMA expert matvec holds (tokens per task)
+constexpr int kMoeMvhTask = 4;
+size_t moe_mvh_workspace_bytes(int T, int k, int H, int I);
+// gate/up matvec, silu(g) * u, down matvec, over the plan in ws (see moe.cu)
+cudaError_t moe_mvh_run(int fmt, int E, int H, int I, int T, int k, const MvhMoeTables& tab, const void* x,
+                        const int* n_tasks, const MoeTask* tasks, const int* pos_slot, void* ws, float* o,
+                        int sms, cudaStream_t s, DevState st);
+bool moe_mvh_supported(int fmt, int H, int I);
+// QMM_MOE_MMA=0 (read once by qmm_init) keeps moe_gemv on the CUDA-core expert matvec
+extern bool g_moe_mvh_enabled;
+
 // ---------------------------------------------------------------- tensor-core matvec
 // Work item = (128-row tile, range of 256-wide K stages); see tcmv.cuh.
 constexpr int kTcThreads = 768;

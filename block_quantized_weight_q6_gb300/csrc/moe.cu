@@ -24,6 +24,8 @@
 
 namespace qmm {
 
+bool g_moe_mvh_enabled = true;
+
 namespace {
 
 // rows per item: a lane's activations serve every row of the item, so more
@@ -42,10 +44,6 @@ struct MoeTable {
     const uint8_t* p[3 * kMoeMaxExperts];  // gate[E], up[E], down[E]
 };
 
-struct MoeTask {
-    int expert, pos, n;  // expert, first grouped slot, tokens (1..2)
-};
-
 struct MoeArgs {
     int E, H, I, T, k;
     int x_bf16;
@@ -54,9 +52,11 @@ struct MoeArgs {
     const void* x;        // [T][H]
     float* y;             // [T][H]
     // workspace
+    int task_nb;          // tokens per task at most
     int* n_tasks;         // [1]
     MoeTask* tasks;       // [T*k]
     int* slot_pos;        // [T*k] grouped position of slot (t, j)
+    int* pos_slot;        // [T*k] slot of each grouped position (-1 past the used ones)
     void* xg;             // [T*k][H] grouped activations (x's type)
     float* h;             // [T*k][I]
     float* o;             // [T*k][H]
@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
     int* eidx = toff + a.E;           // [S]
     const int S = a.T * a.k;
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) cnt[e] = 0;
+    for (int s = threadIdx.x; s < a.T * a.k; s += blockDim.x) a.pos_slot[s] = -1;
     __syncthreads();
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         int e = a.idx[s];
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
             off[e] = so;
             toff[e] = to;
             so += cnt[e];
-            to += (cnt[e] + kMoeNB - 1) / kMoeNB;
+            to += (cnt[e] + a.task_nb - 1) / a.task_nb;
         }
         *a.n_tasks = to;
     }
@@ -111,12 +112,13 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
         for (int q = 0; q < s; ++q) rank += (eidx[q] == e);
         const int pos = off[e] + rank;
         a.slot_pos[s] = pos;
-        if (rank % kMoeNB == 0) {
+        a.pos_slot[pos] = s;
+        if (rank % a.task_nb == 0) {
             MoeTask t;
             t.expert = e;
             t.pos = pos;
-            t.n = min(kMoeNB, cnt[e] - rank);
-            a.tasks[toff[e] + rank / kMoeNB] = t;
+            t.n = min(a.task_nb, cnt[e] - rank);
+            a.tasks[toff[e] + rank / a.task_nb] = t;
         }
     }
 }
@@ -383,11 +385,28 @@ __global__ void route_topk_softmax_kernel(const float* __restrict__ logits, int 
 
 // ---------------------------------------------------------------- host side
 
+// Workspace: the plan (task count, tasks, slot <-> position maps), the
+// grouped slots' outputs o, then the intermediates of whichever expert path
+// runs (the larger of the two is reserved).
 size_t moe_workspace_bytes(int T, int k, int H, int I, bool x_bf16) {
     const size_t S = static_cast<size_t>(T) * k;
     auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
-    return r256(sizeof(int)) + r256(S * sizeof(MoeTask)) + r256(S * sizeof(int)) +
-           r256(S * H * (x_bf16 ? 2 : 4)) + r256(S * I * 4) + r256(S * H * 4);
+    const size_t plan = r256(sizeof(int)) + r256(S * sizeof(MoeTask)) + 2 * r256(S * sizeof(int)) + r256(S * H * 4);
+    const size_t cuda_core = r256(S * H * (x_bf16 ? 2 : 4)) + r256(S * I * 4);
+    const size_t mma = moe_mvh_workspace_bytes(T, k, H, I);
+    return plan + (cuda_core > mma ? cuda_core : mma);
+}
+
+// The experts of a table lie at one fixed stride (a multiple of 16 bytes)?
+static bool table_stride(const void* const* w, int E, int64_t bytes, int64_t* stride) {
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(w[0]);
+    const int64_t st = E > 1 ? static_cast<int64_t>(reinterpret_cast<uintptr_t>(w[1]) - b0) : bytes;
+    if (st < bytes || st % 16 != 0) return false;
+    for (int e = 0; e < E; ++e)
+        if (reinterpret_cast<uintptr_t>(w[e]) != b0 + static_cast<uintptr_t>(e) * static_cast<uintptr_t>(st))
+            return false;
+    *stride = st;
+    return true;
 }
 
 static int mv_occupancy(void (*k)(const MoeArgs, const MoeTable), size_t smem) {
@@ -454,11 +473,23 @@ cudaError_t moe_launch(int fmt, int E, int H, int I, int T, int k, const void* c
     p += r256(S * sizeof(MoeTask));
     a.slot_pos = reinterpret_cast<int*>(p);
     p += r256(S * sizeof(int));
+    a.pos_slot = reinterpret_cast<int*>(p);
+    p += r256(S * sizeof(int));
+    a.o = reinterpret_cast<float*>(p);
+    p += r256(S * H * 4);
+    uint8_t* rest = p;
     a.xg = p;
     p += r256(S * H * (x_bf16 ? 2 : 4));
     a.h = reinterpret_cast<float*>(p);
-    p += r256(S * I * 4);
-    a.o = reinterpret_cast<float*>(p);
+    // the fp16-MMA expert matvecs: bf16 activations, expert tables at a fixed
+    // stride, shapes the stages fit (otherwise the CUDA-core expert matvec)
+    const int be = fmt == FMT_Q6_K ? 256 : 32, bb = fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q4_0 ? 18 : 34);
+    const int64_t gu_bytes = static_cast<int64_t>(I) * (H / be) * bb, d_bytes = static_cast<int64_t>(H) * (I / be) * bb;
+    MvhMoeTables mt{};
+    const bool mma = x_bf16 && moe_mvh_supported(fmt, H, I) && g_moe_mvh_enabled &&
+                     table_stride(wg, E, gu_bytes, &mt.stride[0]) && table_stride(wu, E, gu_bytes, &mt.stride[1]) &&
+                     table_stride(wd, E, d_bytes, &mt.stride[2]);
+    a.task_nb = mma ? kMoeMvhTask : kMoeNB;
     MoeTable tab;
     for (int e = 0; e < E; ++e) {
         tab.p[e] = static_cast<const uint8_t*>(wg[e]);
@@ -471,6 +502,17 @@ cudaError_t moe_launch(int fmt, int E, int H, int I, int T, int k, const void* c
     if (e != cudaSuccess) return e;
     e = launch_pdl(moe_plan_kernel, dim3(1), dim3(1024), plan_smem, s, a);
     if (e != cudaSuccess) return e;
+    if (mma) {
+        mt.base[0] = wg[0];
+        mt.base[1] = wu[0];
+        mt.base[2] = wd[0];
+        e = moe_mvh_run(fmt, E, H, I, T, k, mt, x, a.n_tasks, a.tasks, a.pos_slot, rest, a.o, sms, s, st);
+        if (e != cudaSuccess) return e;
+        int64_t cb = (static_cast<int64_t>(T) * H + 255) / 256;
+        if (cb > 4 * sms) cb = 4 * sms;
+        e = launch_pdl(moe_combine_kernel, dim3(static_cast<unsigned>(cb)), dim3(256), 0, s, a);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const int64_t gwords = static_cast<int64_t>(S) * H * (x_bf16 ? 2 : 4) / 16;
     int64_t gb = (gwords + 255) / 256;
     if (gb > 4 * sms) gb = 4 * sms;

@@ -222,4 +222,405 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// ================================================================ routed experts
+// The expert matvecs of moe_gemv on the same stages and tiles. An item is
+// (task, matrix of the launch, 16-row block at stride 8); the task gives the
+// expert (the third coordinate of the table's tensor map), the task's first
+// grouped slot and its tokens. gate/up launch: two matrices, B = tokens, each
+// token's activations one fp16 row (scaled per slot). down launch: one
+// matrix, each token's h as two fp16 rows hi + lo (22 bits of its fp32
+// value), B = 2 tokens, and a token's output is the sum of its two columns.
+struct MvhMoeArgs {
+    CUtensorMap map[2];      // W as [E][N / 8][8 * rowbytes] 16-bit elements
+    const int* n_tasks;
+    const MoeTask* tasks;
+    const uint16_t* xh;      // fp16 activation rows (slot, or 2 slot + part)
+    const float* xinv;       // [slots] 2^-e of each slot's rows
+    float* out[2];           // [slots][N]
+    int64_t N, K, rowbytes;
+    int nmat, split, ks;
+    int* ctr;
+    DevState st;
+    int live_slot;
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kMvhWarps * 32, 1) moe_mvh_kernel(const __grid_constant__ MvhMoeArgs g) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gr = lane >> 2, c = lane & 3;
+    const int ks = g.ks;
+    const int team = warp / ks, member = warp % ks;
+    const uint32_t S = smem_u32(smem);
+    const uint32_t ring = S + static_cast<uint32_t>(warp) * kMvhNS * kMvhSlot;
+    const uint32_t bars = S + kMvhBarOff + static_cast<uint32_t>(warp) * kMvhNS * 8;
+    float* part = reinterpret_cast<float*>(smem + kMvhPartOff);
+    int* fifo = reinterpret_cast<int*>(smem + kMvhFifoOff) + 4 * warp;
+    const int nteams = static_cast<int>(gridDim.x) * (kMvhWarps / ks);
+    const int gt = team * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x);
+    const uint32_t selc = 0x4040u | (static_cast<uint32_t>(c) << 8) | static_cast<uint32_t>(c);
+    Q6Off po;
+    po.o[0] = q6k_poff(c);
+    po.o[1] = q6k_poff(c + 1);
+    po.o[2] = q6k_poff(4 + c);
+    po.o[3] = q6k_poff(5 + c);
+    po.o[4] = q6k_poff(8 + c);
+    po.o[5] = q6k_poff(9 + c);
+    constexpr int SB = mvh_stage_bytes(FMT), SK = mvh_stage_k(FMT);
+    constexpr int NBX = mvh_boxes(FMT);
+    constexpr uint32_t BW = mvh_box_w(FMT);
+    const int stages = static_cast<int>(g.K / SK);
+    const int ipm = static_cast<int>((g.N + 8 * kMvhRows - 1) / (8 * kMvhRows)) * 8;  // items per matrix
+
+    grid_launch_dependents();
+    live_bump(g.st, g.live_slot);
+    if (lane < kMvhNS) mbar_init(bars + 8 * lane, 1);
+    fence_mbar_init();
+    __syncwarp();
+    // the tasks, the activations and the counter come from earlier kernels
+    grid_dependency_wait();
+    const int items = *g.n_tasks * g.nmat * ipm;
+    if (gt >= items) return;  // the whole team
+    const int first_claim = static_cast<int>(gridDim.x) * kMvhWarps;
+
+    // cursor over the stages to copy (it, p) and the item's expert / matrix / rows
+    int cit = gt, cp = member;
+    bool cfetch = false;
+    uint32_t issued = 0, used = 0;
+    int fifo_head = 0, fifo_tail = 0;
+    auto issue = [&]() {
+        const int task = cit / (g.nmat * ipm), rem = cit % (g.nmat * ipm);
+        const int mi = rem / ipm, li = rem % ipm;
+        const int e = g.tasks[task].expert;
+        const int j = li & 7, G0 = (li >> 3) * kMvhRows;
+        const int64_t off = (static_cast<int64_t>(j) * g.rowbytes + static_cast<int64_t>(cp) * SB) &
+                            ~static_cast<int64_t>(15);
+        const uint32_t slot = ring + (issued % kMvhNS) * kMvhSlot, bar = bars + 8 * (issued % kMvhNS);
+        if (lane == 0) mbar_arrive_expect_tx(bar, NBX * BW * kMvhRows);
+        __syncwarp();
+        if (lane < NBX)
+            tma_load_3d(slot + static_cast<uint32_t>(lane) * BW * kMvhRows, &g.map[mi],
+                        static_cast<int>(off / 2) + static_cast<int>(BW / 2) * lane, G0, e, bar);
+        ++issued;
+        cp += ks;
+        if (cp < stages) return;
+        if (ks == 1) {
+            cfetch = true;
+        } else {
+            cp = member;
+            cit += nteams;
+        }
+    };
+    for (int q = 0; q < kMvhNS - 1 && !cfetch && cit < items; ++q) issue();
+
+    bool ok = true;
+    int it = gt;
+    while (it < items) {
+        const int task = it / (g.nmat * ipm), rem = it % (g.nmat * ipm);
+        const int mi = rem / ipm, li = rem % ipm;
+        const MoeTask tk = g.tasks[task];
+        const int j = li & 7, G0 = (li >> 3) * kMvhRows;
+        const int bcols = g.split ? 2 * tk.n : tk.n;
+        const int xrow = (g.split ? 2 * tk.pos : tk.pos) + gr % bcols;  // past the batch: a valid row
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int p = member; p < stages; p += ks) {
+            if (cfetch) {
+                int nx = 0;
+                if (lane == 0) nx = first_claim + atomicAdd(g.ctr, 1);
+                nx = __shfl_sync(0xffffffffu, nx, 0);
+                cit = nx;
+                cp = 0;
+                cfetch = false;
+                if (lane == 0) fifo[fifo_tail & 3] = nx;
+                ++fifo_tail;
+            }
+            if (cit < items) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                issue();
+            }
+            const uint16_t* xr = g.xh + static_cast<int64_t>(xrow) * g.K + static_cast<int64_t>(p) * SK;
+            const uint32_t slot = ring + (used % kMvhNS) * kMvhSlot;
+            if (ok) ok = mvh_wait(bars + 8 * (used % kMvhNS), (used / kMvhNS) & 1u, g.st.err);
+            ++used;
+            const uint32_t L = static_cast<uint32_t>(
+                (static_cast<int64_t>(j) * g.rowbytes + static_cast<int64_t>(p) * SB) & 15);
+            if constexpr (FMT == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc);
+            else if constexpr (FMT == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc);
+            else q8_0_stage(slot, gr, c, L, xr, acc);
+            __syncwarp();
+        }
+        if (ks > 1) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) part[(warp * 4 + q) * 32 + lane] = acc[q];
+            mvh_team_sync(team, ks);
+            if (member == 0) {
+                for (int t2 = 1; t2 < ks; ++t2)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) acc[q] += part[((warp + t2) * 4 + q) * 32 + lane];
+            }
+            mvh_team_sync(team, ks);
+        }
+        if (member == 0) {
+            float* out = g.out[mi];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t n = static_cast<int64_t>(j) + 8 * (G0 + gr + 8 * h);
+                if (n >= g.N) continue;
+                if (g.split) {
+                    // columns 2c, 2c + 1: token c's hi and lo rows
+                    if (c < tk.n)
+                        out[static_cast<int64_t>(tk.pos + c) * g.N + n] =
+                            (acc[2 * h] + acc[2 * h + 1]) * g.xinv[tk.pos + c];
+                } else {
+#pragma unroll
+                    for (int b2 = 0; b2 < 2; ++b2) {
+                        const int b = 2 * c + b2;
+                        if (b < tk.n)
+                            out[static_cast<int64_t>(tk.pos + b) * g.N + n] = acc[2 * h + b2] * g.xinv[tk.pos + b];
+                    }
+                }
+            }
+        }
+        if (ks > 1) {
+            it += nteams;
+        } else {
+            __syncwarp();
+            it = fifo[fifo_head & 3];
+            ++fifo_head;
+        }
+    }
+    if (!ok)
+        for (uint32_t u = used > kMvhNS ? used - kMvhNS : 0; u < issued; ++u)
+            (void)mvh_wait(bars + 8 * (u % kMvhNS), (u / kMvhNS) & 1u, g.st.err);
+}
+
+// Largest magnitude of the block's values (fp32 bits of |v|, 0 if none),
+// reduced over the CTA (blockDim.x a multiple of 32, at most 1024).
+__device__ __forceinline__ float block_amax(float m) {
+    __shared__ float red[32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+    __syncthreads();
+    return m;
+}
+
+// 2^s with the largest magnitude times 2^s in [2^14, 2^15) (1 for 0, inf, NaN)
+__device__ __forceinline__ int fp16_exponent(float amax) {
+    if (!(amax > 0.0f) || !(amax < INFINITY)) return 0;
+    int e;
+    (void)frexpf(amax, &e);
+    return min(126, max(-126, 15 - e));
+}
+
+// gate/up prep: one CTA per grouped slot, the slot's token row (bf16) as
+// scaled fp16; resets the matvec's item counter.
+__global__ void __launch_bounds__(256) moe_prep_gu_kernel(const uint16_t* __restrict__ x, int H, int k,
+                                                          const int* __restrict__ pos_slot, int S,
+                                                          uint16_t* __restrict__ xh, float* __restrict__ xinv,
+                                                          int* ctr, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, QMM_LIVE_MOE_GATHER);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ctr = 0;
+    for (int pos = blockIdx.x; pos < S; pos += gridDim.x) {
+        const int slot = pos_slot[pos];
+        if (slot < 0) continue;  // uniform over the CTA
+        const uint16_t* xr = x + static_cast<int64_t>(slot / k) * H;
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float(uint32_t(xr[i]) << 16)));
+        const int s = fp16_exponent(block_amax(m));
+        const float sc = ldexpf(1.0f, s);
+        for (int i = threadIdx.x; i < H; i += blockDim.x)
+            xh[static_cast<int64_t>(pos) * H + i] =
+                __half_as_ushort(__float2half_rn(__uint_as_float(uint32_t(xr[i]) << 16) * sc));
+        if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -s);
+    }
+}
+
+// down prep: one CTA per grouped slot: h = silu(g) * u in fp32, as two fp16
+// rows hi = fp16(h 2^s), lo = fp16(h 2^s - hi); resets the item counter.
+__global__ void __launch_bounds__(256) moe_prep_d_kernel(const float* __restrict__ gg, const float* __restrict__ uu,
+                                                         int I, const int* __restrict__ pos_slot, int S,
+                                                         uint16_t* __restrict__ xh, float* __restrict__ xinv,
+                                                         int* ctr, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, QMM_LIVE_MOE_SILU);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ctr = 0;
+    for (int pos = blockIdx.x; pos < S; pos += gridDim.x) {
+        if (pos_slot[pos] < 0) continue;
+        const float* g = gg + static_cast<int64_t>(pos) * I;
+        const float* u = uu + static_cast<int64_t>(pos) * I;
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < I; i += blockDim.x) {
+            const float v = g[i];
+            m = fmaxf(m, fabsf(v / (1.0f + expf(-v)) * u[i]));
+        }
+        const int s = fp16_exponent(block_amax(m));
+        const float sc = ldexpf(1.0f, s);
+        for (int i = threadIdx.x; i < I; i += blockDim.x) {
+            const float v = g[i];
+            const float hv = v / (1.0f + expf(-v)) * u[i] * sc;
+            const __half hi = __float2half_rn(hv);
+            const __half lo = __float2half_rn(hv - __half2float(hi));
+            xh[(2 * static_cast<int64_t>(pos)) * I + i] = __half_as_ushort(hi);
+            xh[(2 * static_cast<int64_t>(pos) + 1) * I + i] = __half_as_ushort(lo);
+        }
+        if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -s);
+    }
+}
+
+bool moe_mvh_supported(int fmt, int H, int I) {
+    return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0 || fmt == FMT_Q6_K) && H % 256 == 0 && I % 256 == 0 && H % 8 == 0 &&
+           I % 8 == 0;
+}
+
+namespace {
+
+struct MoeWs {
+    uint16_t* xh_gu;
+    float* xinv_gu;
+    float* g;
+    float* u;
+    uint16_t* xh_d;
+    float* xinv_d;
+    int* ctr;
+    size_t total;
+};
+
+MoeWs moe_ws_layout(uint8_t* base, int T, int k, int H, int I) {
+    const size_t S = static_cast<size_t>(T) * k;
+    MoeWs w{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        uint8_t* p = base ? base + o : nullptr;
+        o = round256(o + bytes);
+        return p;
+    };
+    w.ctr = reinterpret_cast<int*>(take(4));
+    w.xh_gu = reinterpret_cast<uint16_t*>(take(S * H * 2));
+    w.xinv_gu = reinterpret_cast<float*>(take(S * 4));
+    w.g = reinterpret_cast<float*>(take(S * I * 4));
+    w.u = reinterpret_cast<float*>(take(S * I * 4));
+    w.xh_d = reinterpret_cast<uint16_t*>(take(2 * S * I * 2));
+    w.xinv_d = reinterpret_cast<float*>(take(S * 4));
+    w.total = o;
+    return w;
+}
+
+template <int FMT>
+cudaError_t moe_mvh_prepare() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(moe_mvh_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kMvhSmem));
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(moe_mvh_kernel<FMT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       cudaSharedmemCarveoutMaxShared);
+    });
+    return err;
+}
+
+// a table as [E][N / 8][8 * rowbytes] 16-bit elements, boxes 16 rows high
+cudaError_t moe_map(CUtensorMap* map, int fmt, const void* base, int64_t stride, int E, int64_t N,
+                    int64_t rowbytes) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(4 * rowbytes), static_cast<cuuint64_t>(N / 8),
+                                static_cast<cuuint64_t>(E)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(8 * rowbytes), static_cast<cuuint64_t>(stride)};
+    const cuuint32_t box[3] = {mvh_box_w(fmt) / 2, static_cast<cuuint32_t>(kMvhRows), 1u};
+    const cuuint32_t es[3] = {1u, 1u, 1u};
+    if (enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+template <int FMT>
+cudaError_t moe_mvh_launch(MvhMoeArgs& a, int max_items, int sms, cudaStream_t s) {
+    cudaError_t e = moe_mvh_prepare<FMT>();
+    if (e != cudaSuccess) return e;
+    const int64_t warps = static_cast<int64_t>(sms) * kMvhWarps;
+    a.ks = 1;
+    const int stages = static_cast<int>(a.K / mvh_stage_k(FMT));
+    for (int kk : {1, 2, 4, 8, 16}) {
+        if (kk > stages) break;
+        a.ks = kk;
+        if (static_cast<int64_t>(max_items) * kk >= warps) break;
+    }
+    const int64_t per_cta = kMvhWarps / a.ks;
+    const int grid = static_cast<int>(std::min<int64_t>(sms, (max_items + per_cta - 1) / per_cta));
+    return launch_pdl(moe_mvh_kernel<FMT>, dim3(grid), dim3(kMvhWarps * 32), kMvhSmem, s, a);
+}
+
+}  // namespace
+
+size_t moe_mvh_workspace_bytes(int T, int k, int H, int I) { return moe_ws_layout(nullptr, T, k, H, I).total; }
+
+cudaError_t moe_mvh_run(int fmt, int E, int H, int I, int T, int k, const MvhMoeTables& tab, const void* x,
+                        const int* n_tasks, const MoeTask* tasks, const int* pos_slot, void* ws, float* o,
+                        int sms, cudaStream_t s, DevState st) {
+    const int S = T * k;
+    const MoeWs w = moe_ws_layout(static_cast<uint8_t*>(ws), T, k, H, I);
+    const int64_t rb_gu = H / block_elems(fmt) * block_bytes(fmt), rb_d = I / block_elems(fmt) * block_bytes(fmt);
+    // tasks at most: every slot its own task, or every expert one task per kMoeMvhTask tokens
+    const int max_tasks = S;
+    cudaError_t e = launch_pdl(moe_prep_gu_kernel, dim3(static_cast<unsigned>(S)), dim3(256), 0, s,
+                               static_cast<const uint16_t*>(x), H, k, pos_slot, S, w.xh_gu, w.xinv_gu, w.ctr, st);
+    if (e != cudaSuccess) return e;
+    static thread_local MvhMoeArgs a;
+    memset(&a, 0, sizeof a);
+    a.n_tasks = n_tasks;
+    a.tasks = tasks;
+    a.ctr = w.ctr;
+    a.st = st;
+    // gate and up
+    if ((e = moe_map(&a.map[0], fmt, tab.base[0], tab.stride[0], E, I, rb_gu)) != cudaSuccess) return e;
+    if ((e = moe_map(&a.map[1], fmt, tab.base[1], tab.stride[1], E, I, rb_gu)) != cudaSuccess) return e;
+    a.xh = w.xh_gu;
+    a.xinv = w.xinv_gu;
+    a.out[0] = w.g;
+    a.out[1] = w.u;
+    a.N = I;
+    a.K = H;
+    a.rowbytes = rb_gu;
+    a.nmat = 2;
+    a.split = 0;
+    a.live_slot = QMM_LIVE_MOE_GATE_UP;
+    int max_items = max_tasks * 2 * static_cast<int>((I + 8 * kMvhRows - 1) / (8 * kMvhRows) * 8);
+    e = fmt == FMT_Q6_K ? moe_mvh_launch<FMT_Q6_K>(a, max_items, sms, s)
+      : fmt == FMT_Q4_0 ? moe_mvh_launch<FMT_Q4_0>(a, max_items, sms, s)
+                        : moe_mvh_launch<FMT_Q8_0>(a, max_items, sms, s);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(moe_prep_d_kernel, dim3(static_cast<unsigned>(S)), dim3(256), 0, s,
+                   static_cast<const float*>(w.g), static_cast<const float*>(w.u), I, pos_slot, S, w.xh_d, w.xinv_d,
+                   w.ctr, st);
+    if (e != cudaSuccess) return e;
+    // down
+    if ((e = moe_map(&a.map[0], fmt, tab.base[2], tab.stride[2], E, H, rb_d)) != cudaSuccess) return e;
+    a.xh = w.xh_d;
+    a.xinv = w.xinv_d;
+    a.out[0] = o;
+    a.out[1] = nullptr;
+    a.N = H;
+    a.K = I;
+    a.rowbytes = rb_d;
+    a.nmat = 1;
+    a.split = 1;
+    a.live_slot = QMM_LIVE_MOE_DOWN;
+    max_items = max_tasks * static_cast<int>((H + 8 * kMvhRows - 1) / (8 * kMvhRows) * 8);
+    e = fmt == FMT_Q6_K ? moe_mvh_launch<FMT_Q6_K>(a, max_items, sms, s)
+      : fmt == FMT_Q4_0 ? moe_mvh_launch<FMT_Q4_0>(a, max_items, sms, s)
+                        : moe_mvh_launch<FMT_Q8_0>(a, max_items, sms, s);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace qmm

@@ -101,6 +101,8 @@ enum {
                                          cores                               */
     QMM_LIVE_GEMV_MV8 = 18,           /* batch 1-8 float matvec on the
                                          warp-level MMA (fp16 or bf16)       */
+    QMM_LIVE_MOE_SILU = 19,           /* silu(g) * u laid out for the expert
+                                         matvecs on the warp-level MMA       */
     QMM_LIVE_COUNT = 24
 };
 
@@ -114,7 +116,8 @@ enum {
  * one), QMM_MV8 ("0" does the same for the bf16 warp-level MMA matvec at
  * batch 2-8), QMM_MVH ("0" turns the fp16-MMA matvec for bf16 batches 1-8
  * off, so those batches take the paths above), QMM_PDL ("0" launches
- * without programmatic dependent launch).
+ * without programmatic dependent launch), QMM_MOE_MMA ("0" keeps moe_gemv on
+ * the CUDA-core expert matvec even where the warp-level MMA one applies).
  * Called implicitly by every entry point; calling it again is a no-op. */
 int qmm_init(void);
 
@@ -293,6 +296,12 @@ typedef struct {
  * place): for each token t and each of its top_k experts e = idx[t][j],
  * h = silu(Wg_e x_t) * (Wu_e x_t), o = Wd_e h, and
  * y[t] = sum_j gate_w[t][j] * o_j, summed in j order.
+ * With bf16 x, hidden and inter multiples of 256, and each of the three
+ * pointer tables at one fixed stride (w[e] = w[0] + e * stride, stride a
+ * multiple of 16 bytes: experts allocated as one tensor), the expert
+ * matvecs run on the warp-level MMA with fp16 operands (h enters the down
+ * projection as two fp16 terms, 22 bits of its fp32 value); otherwise on the
+ * CUDA cores. Either way each output is within the propagated float bound.
  * idx: [T][top_k] int32, gate_w: [T][top_k] fp32, x: [T][hidden] (fmt's
  * activation type), y: [T][hidden] fp32. Float activation mode only. Each
  * selected expert's matrices are read once per call however many of the

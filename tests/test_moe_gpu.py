@@ -158,3 +158,83 @@ def test_moe_liveness_and_bad_index_flag():
     torch.cuda.synchronize()
     with pytest.raises(qmm.QmmError):
         qmm.sync_check()
+
+
+# Expert tables at one fixed stride (experts drawn as one tensor, as an
+# engine allocates them): the expert matvecs run on the warp-level MMA
+# (fp16 operands; h as two fp16 terms). All three formats; tokens that share
+# experts (tasks of up to 4 tokens, an expert with more than 4 tokens), T=1.
+def _table(fmt, seed, N, K, E):
+    return synth.matrix_torch(fmt, seed, N, K, "cuda", E)
+
+
+@pytest.mark.parametrize("fmt,E,H,I", [(synth.Q4_0, 8, 512, 256), (synth.Q6_K, 6, 512, 768),
+                                       (synth.Q8_0, 5, 256, 512)])
+@pytest.mark.parametrize("T,k", [(1, 1), (1, 4), (5, 2), (16, 4), (9, 3)])
+def test_moe_strided_tables_vs_oracle(fmt, E, H, I, T, k):
+    g, u, d = _table(fmt, 1500, I, H, E), _table(fmt, 1501, I, H, E), _table(fmt, 1502, H, I, E)
+    x = synth.normal_bf16(1503 + T, (T, H))
+    logits = synth.normal_f32(1504 + T, (T, E))
+    idx, gate = oracle.route_topk_softmax(logits, k)
+    qmm.liveness_reset()
+    y = run_moe(fmt, list(g), list(u), list(d), H, I, idx, gate.astype(np.float32), x)
+    live = qmm.liveness()
+    assert live["moe_silu"] == 1 and live["moe_gate_up"] == 1 and live["moe_down"] == 1
+    ref, bound = oracle.moe_float(fmt, H, I, [w.cpu().numpy() for w in g], [w.cpu().numpy() for w in u],
+                                  [w.cpu().numpy() for w in d], idx, gate.astype(np.float32).astype(np.float64), x)
+    err = np.abs(y.astype(np.float64) - ref)
+    assert (err <= bound).all(), (err / bound).max()
+
+
+def test_moe_strided_one_expert_many_tokens():
+    """every token picks expert 2 and then expert 0: tasks of 4, 4, 3 tokens
+    per expert (11 tokens)"""
+    fmt, E, H, I, T = synth.Q4_0, 4, 256, 512, 11
+    g, u, d = _table(fmt, 1510, I, H, E), _table(fmt, 1511, I, H, E), _table(fmt, 1512, H, I, E)
+    x = synth.normal_bf16(1513, (T, H))
+    idx = np.full((T, 2), 2, np.int32)
+    idx[:, 1] = 0
+    gate = np.tile(np.array([[0.75, 0.25]], np.float32), (T, 1))
+    y = run_moe(fmt, list(g), list(u), list(d), H, I, idx, gate, x)
+    ref, bound = oracle.moe_float(fmt, H, I, [w.cpu().numpy() for w in g], [w.cpu().numpy() for w in u],
+                                  [w.cpu().numpy() for w in d], idx, gate.astype(np.float64), x)
+    assert (np.abs(y - ref) <= bound).all()
+
+
+def test_moe_strided_matches_cuda_core_path():
+    """the same call with QMM_MOE_MMA=0 (CUDA-core expert matvec) agrees
+    within twice the bound, in a fresh process"""
+    import os
+    import subprocess
+    import sys
+    code = r"""
+import numpy as np, torch, sys
+sys.path.insert(0, {root!r})
+import block_quantized_weight_q6_gb300 as qmm, synth, oracle
+E, H, I, T, k = 6, 512, 256, 3, 2
+g = synth.matrix_torch(synth.Q4_0, 1, I, H, "cuda", E)
+u = synth.matrix_torch(synth.Q4_0, 2, I, H, "cuda", E)
+d = synth.matrix_torch(synth.Q4_0, 3, H, I, "cuda", E)
+x = torch.from_numpy(synth.normal_bf16(4, (T, H)).view(np.int16)).cuda().view(torch.bfloat16)
+idx, gate = oracle.route_topk_softmax(synth.normal_f32(5, (T, E)), k)
+m = qmm.moe_experts(list(g), list(u), list(d), H, I, k, T)
+y = torch.empty((T, H), device="cuda")
+qmm.liveness_reset()
+qmm.moe(qmm.Q4_0, m, torch.from_numpy(idx).cuda(), torch.from_numpy(gate.astype(np.float32)).cuda(), x, y)
+torch.cuda.synchronize()
+print(qmm.liveness()["moe_silu"])
+np.save(sys.argv[1], y.cpu().numpy())
+"""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    import tempfile
+    outs = []
+    for flag in ("1", "0"):
+        f = tempfile.mktemp(suffix=".npy")
+        r = subprocess.run([sys.executable, "-c", code.format(root=root), f],
+                           env=dict(os.environ, QMM_MOE_MMA=flag), capture_output=True, text=True, timeout=300)
+        assert r.returncode == 0, r.stderr
+        assert r.stdout.split()[-1] == ("1" if flag == "1" else "0")
+        outs.append(np.load(f))
+        os.unlink(f)
+    scale = np.abs(outs[1]).max()
+    assert np.allclose(outs[0], outs[1], rtol=1e-4, atol=1e-4 * scale)
