@@ -548,14 +548,10 @@ template <int FMT>
 cudaError_t moe_mvh_launch(MvhMoeArgs& a, int max_items, int sms, cudaStream_t s) {
     cudaError_t e = moe_mvh_prepare<FMT>();
     if (e != cudaSuccess) return e;
-    const int64_t warps = static_cast<int64_t>(sms) * kMvhWarps;
-    a.ks = 1;
+    // the K split depends on the shape only (never on the tokens), so a
+    // token's output does not depend on which other tokens share the call
     const int stages = static_cast<int>(a.K / mvh_stage_k(FMT));
-    for (int kk : {1, 2, 4, 8, 16}) {
-        if (kk > stages) break;
-        a.ks = kk;
-        if (static_cast<int64_t>(max_items) * kk >= warps) break;
-    }
+    a.ks = stages >= 16 ? 2 : 1;
     const int64_t per_cta = kMvhWarps / a.ks;
     const int grid = static_cast<int>(std::min<int64_t>(sms, (max_items + per_cta - 1) / per_cta));
     return launch_pdl(moe_mvh_kernel<FMT>, dim3(grid), dim3(kMvhWarps * 32), kMvhSmem, s, a);
