@@ -507,7 +507,8 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------ main
 
 # read + write DRAM bytes of the MoE part per distinct expert (ncu, 24 experts, T=16)
-MOE_DRAM_BYTES_PER_EXPERT = (8448 + 244736 + 398921472 + 927232 + 199356928 + 2423552 + 3683584) / 24
+MOE_DRAM_BYTES_PER_EXPERT = (11264 + 237824 + 398583808 + 1786368 + 2106880 + 199277824 + 1957376
+                             + 3686656) / 24
 
 SWEEP_LAYER = [  # (name, fmt name, N, K) of one layer
     ("wq", "Q4_0", 4096, 4096), ("wk", "Q4_0", 4096, 4096), ("wo", "Q4_0", 4096, 4096),
@@ -760,9 +761,11 @@ def main():
         "gemm_in_kernel": {"bound": "tensor", "achieved": tops["gemm_in_kernel"], "peak": tc_peak,
                            "unit": "TFLOP/s", "kernel": "gemm_kernel<q6_K, in-kernel> + quantize"},
         "moe_t1": {"bound": "hbm", "achieved": moe_gbs["moe_t1"], "peak": hbm, "unit": "GB/s",
-                   "kernel": "moe route+plan+gather+gate_up+down+combine, T=1"},
+                   "kernel": "moe route + plan + gate/up prep + moe_mvh_kernel (gate, up) + silu prep + "
+                             "moe_mvh_kernel (down) + combine, T=1"},
         "moe_t16": {"bound": "hbm", "achieved": moe_gbs["moe_t16"], "peak": hbm, "unit": "GB/s",
-                    "kernel": "moe route+plan+gather+gate_up+down+combine, T=16"},
+                    "kernel": "moe route + plan + gate/up prep + moe_mvh_kernel (gate, up) + silu prep + "
+                              "moe_mvh_kernel (down) + combine, T=16"},
     }
     for k2, v in seg.items():
         v["frac"] = v["achieved"] / v["peak"]

@@ -418,7 +418,7 @@ __device__ __forceinline__ int fp16_exponent(float amax) {
 }
 
 // gate/up prep: one CTA per grouped slot, the slot's token row (bf16) as
-// scaled fp16; resets the matvec's item counter.
+// scaled fp16 (8 values per 16-byte load); resets the matvec's item counter.
 __global__ void __launch_bounds__(256) moe_prep_gu_kernel(const uint16_t* __restrict__ x, int H, int k,
                                                           const int* __restrict__ pos_slot, int S,
                                                           uint16_t* __restrict__ xh, float* __restrict__ xinv,
@@ -430,20 +430,38 @@ __global__ void __launch_bounds__(256) moe_prep_gu_kernel(const uint16_t* __rest
     for (int pos = blockIdx.x; pos < S; pos += gridDim.x) {
         const int slot = pos_slot[pos];
         if (slot < 0) continue;  // uniform over the CTA
-        const uint16_t* xr = x + static_cast<int64_t>(slot / k) * H;
-        float m = 0.0f;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) m = fmaxf(m, fabsf(__uint_as_float(uint32_t(xr[i]) << 16)));
-        const int s = fp16_exponent(block_amax(m));
+        const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(slot / k) * H);
+        uint4* out = reinterpret_cast<uint4*>(xh + static_cast<int64_t>(pos) * H);
+        const int nv = H / 8;
+        uint32_t mb = 0;  // magnitude bits of bf16 order like the magnitudes
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            const uint4 v = __ldg(xr + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) mb = max(mb, max(w[q] & 0x7FFFu, (w[q] >> 16) & 0x7FFFu));
+        }
+        const int s = fp16_exponent(block_amax(__uint_as_float(mb << 16)));
         const float sc = ldexpf(1.0f, s);
-        for (int i = threadIdx.x; i < H; i += blockDim.x)
-            xh[static_cast<int64_t>(pos) * H + i] =
-                __half_as_ushort(__float2half_rn(__uint_as_float(uint32_t(xr[i]) << 16) * sc));
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) {
+            const uint4 v = __ldg(xr + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const __half lo = __float2half_rn(__uint_as_float(w[q] << 16) * sc);
+                const __half hi = __float2half_rn(__uint_as_float(w[q] & 0xFFFF0000u) * sc);
+                o[q] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+            }
+            out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
         if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -s);
     }
 }
 
 // down prep: one CTA per grouped slot: h = silu(g) * u in fp32, as two fp16
-// rows hi = fp16(h 2^s), lo = fp16(h 2^s - hi); resets the item counter.
+// rows hi = fp16(h 2^s), lo = fp16(h 2^s - hi); resets the item counter. A
+// thread keeps the h of its 4-value groups in registers between the two
+// passes (I <= 256 * 4 * 8).
 __global__ void __launch_bounds__(256) moe_prep_d_kernel(const float* __restrict__ gg, const float* __restrict__ uu,
                                                          int I, const int* __restrict__ pos_slot, int S,
                                                          uint16_t* __restrict__ xh, float* __restrict__ xinv,
@@ -452,32 +470,52 @@ __global__ void __launch_bounds__(256) moe_prep_d_kernel(const float* __restrict
     grid_dependency_wait();
     live_bump(st, QMM_LIVE_MOE_SILU);
     if (blockIdx.x == 0 && threadIdx.x == 0) *ctr = 0;
+    constexpr int kPer = 8;  // 4-value groups per thread at most
     for (int pos = blockIdx.x; pos < S; pos += gridDim.x) {
         if (pos_slot[pos] < 0) continue;
-        const float* g = gg + static_cast<int64_t>(pos) * I;
-        const float* u = uu + static_cast<int64_t>(pos) * I;
+        const float4* g4 = reinterpret_cast<const float4*>(gg + static_cast<int64_t>(pos) * I);
+        const float4* u4 = reinterpret_cast<const float4*>(uu + static_cast<int64_t>(pos) * I);
+        const int nv = I / 4;
+        float4 h[kPer];
         float m = 0.0f;
-        for (int i = threadIdx.x; i < I; i += blockDim.x) {
-            const float v = g[i];
-            m = fmaxf(m, fabsf(v / (1.0f + expf(-v)) * u[i]));
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = threadIdx.x + q * static_cast<int>(blockDim.x);
+            h[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (i < nv) {
+                const float4 gv = __ldg(g4 + i), uv = __ldg(u4 + i);
+                h[q] = make_float4(gv.x / (1.0f + expf(-gv.x)) * uv.x, gv.y / (1.0f + expf(-gv.y)) * uv.y,
+                                   gv.z / (1.0f + expf(-gv.z)) * uv.z, gv.w / (1.0f + expf(-gv.w)) * uv.w);
+                m = fmaxf(m, fmaxf(fmaxf(fabsf(h[q].x), fabsf(h[q].y)), fmaxf(fabsf(h[q].z), fabsf(h[q].w))));
+            }
         }
         const int s = fp16_exponent(block_amax(m));
         const float sc = ldexpf(1.0f, s);
-        for (int i = threadIdx.x; i < I; i += blockDim.x) {
-            const float v = g[i];
-            const float hv = v / (1.0f + expf(-v)) * u[i] * sc;
-            const __half hi = __float2half_rn(hv);
-            const __half lo = __float2half_rn(hv - __half2float(hi));
-            xh[(2 * static_cast<int64_t>(pos)) * I + i] = __half_as_ushort(hi);
-            xh[(2 * static_cast<int64_t>(pos) + 1) * I + i] = __half_as_ushort(lo);
+        uint2* hi_row = reinterpret_cast<uint2*>(xh + (2 * static_cast<int64_t>(pos)) * I);
+        uint2* lo_row = reinterpret_cast<uint2*>(xh + (2 * static_cast<int64_t>(pos) + 1) * I);
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = threadIdx.x + q * static_cast<int>(blockDim.x);
+            if (i >= nv) continue;
+            const float v[4] = {h[q].x * sc, h[q].y * sc, h[q].z * sc, h[q].w * sc};
+            uint32_t hb[4], lb[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const __half hv = __float2half_rn(v[r]);
+                hb[r] = __half_as_ushort(hv);
+                lb[r] = __half_as_ushort(__float2half_rn(v[r] - __half2float(hv)));
+            }
+            hi_row[i] = make_uint2(hb[0] | (hb[1] << 16), hb[2] | (hb[3] << 16));
+            lo_row[i] = make_uint2(lb[0] | (lb[1] << 16), lb[2] | (lb[3] << 16));
         }
         if (threadIdx.x == 0) xinv[pos] = ldexpf(1.0f, -s);
     }
 }
 
 bool moe_mvh_supported(int fmt, int H, int I) {
-    return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0 || fmt == FMT_Q6_K) && H % 256 == 0 && I % 256 == 0 && H % 8 == 0 &&
-           I % 8 == 0;
+    // (the down prep holds a slot's h in registers: I <= 256 threads x 8 x 4)
+    return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0 || fmt == FMT_Q6_K) && H % 256 == 0 && I % 256 == 0 &&
+           I <= 256 * 8 * 4;
 }
 
 namespace {
