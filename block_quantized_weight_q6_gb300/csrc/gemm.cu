@@ -57,14 +57,15 @@ constexpr int NS = 3;             // stages, each the A and B tiles of KP blocks
 constexpr int kPrefetch = 8;      // stages of A tiles prefetched into L2 ahead of their copy
 constexpr int kScMax = 56;        // largest |q6_K sub-block scale| the fp16 B tile holds exactly
 constexpr int NR = 3;             // raw weight stages (256 columns each)
-constexpr int NBUF = 4;           // accumulator buffers in tensor memory, used in pairs
+constexpr int NACC = 3;           // per-block accumulator buffers in tensor memory (a ring)
+constexpr int kYCol = NACC * 128; // q6_K: the running output, columns kYCol .. kYCol + 127
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
 constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
 constexpr int kThreads = 480;                // 15 warps: 128 registers a thread
 constexpr int kRawWarp = 14;                // raw weight producer
 constexpr int kConv0 = 2, kConvWarps = 4;   // converter warps
 constexpr int kEpi0 = 6;                    // epilogue warps kEpi0 .. kEpi0 + 7
-constexpr int kTmemCols = 512;    // NBUF * BN accumulators
+constexpr int kTmemCols = 512;    // NACC * BN accumulators and the q6_K running output
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
 // B stage: 16 groups of 8 weight rows, kBSbo bytes apart (a 16-byte odd
 // multiple past 512, so that 8 lanes storing one row each of 8 different
@@ -112,7 +113,7 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
     o += dr * BN * 4;
     o = align_up(o, 8);
     L.bars = o;
-    o += 8 * (2 * NS + 2 * NR + 2 * (NBUF / KP) + dr);
+    o += 8 * (2 * NS + 2 * NR + 2 * NACC + dr);
     L.tslot = o;
     o += 4;
     L.abort_flag = o;
@@ -122,9 +123,9 @@ __host__ __device__ inline SmemLayout smem_layout(int fmt, bool exp) {
 }
 
 // barrier indices: full[NS] (the A copy's bytes and the converters),
-// empty[NS], raw_full[NR], raw_empty[NR], acc_full[2], acc_empty[2] (pairs of
-// accumulator buffers), dv_full[DR]
-constexpr int NP = NBUF / KP;  // accumulator pairs
+// empty[NS], raw_full[NR], raw_empty[NR], acc_full[NACC], acc_empty[NACC]
+// (one per accumulator buffer, i.e. per K block), dv_full[DR]
+constexpr int NP = NACC;
 __device__ __forceinline__ uint32_t bar_full(uint32_t B, int s) { return B + 8 * s; }
 __device__ __forceinline__ uint32_t bar_empty(uint32_t B, int s) { return B + 8 * (NS + s); }
 __device__ __forceinline__ uint32_t bar_raw_full(uint32_t B, int r) { return B + 8 * (2 * NS + r); }
@@ -198,6 +199,39 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- trace
 // Diagnostic builds define QMM_GEMM_TRACE and point qmm_gemm_trace at mapped
@@ -503,29 +537,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc = idesc_f16(BM, BN);
-        for (int64_t q = 0; q * KP < nkb; ++q) {
+        bool ok = true;
+        for (int64_t q = 0; ok && q * KP < nkb; ++q) {
             const int64_t kb0 = q * KP;
             const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
             const int st = static_cast<int>(q % NS);
-            const int pr = static_cast<int>(q % NP);
             QMM_TRACE(10, kb0);
             if (!wait_or_abort(bar_full(BARS, st), (q / NS) & 1, FLAG, a.st.err)) break;
             QMM_TRACE(12, kb0);
-            if (q >= NP && !wait_or_abort(bar_acc_empty(BARS, pr), ((q / NP) - 1) & 1, FLAG, a.st.err))
-                break;
-            QMM_TRACE(13, kb0);
-            tc_fence_after();
-            if (lane == 0) {
-                for (int bi = 0; bi < nbk; ++bi) {
+            for (int bi = 0; bi < nbk; ++bi) {
+                // block kb into accumulator buffer kb % NACC, once the
+                // epilogue has read that buffer's previous block
+                const int64_t kb = kb0 + bi;
+                const int buf = static_cast<int>(kb % NACC);
+                if (kb >= NACC &&
+                    !wait_or_abort(bar_acc_empty(BARS, buf), ((kb / NACC) - 1) & 1, FLAG, a.st.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
                     const uint64_t ad = smem_desc(S + L.a + st * kAStage + bi * kATile);
                     const uint64_t bd = smem_desc(S + L.b + st * kBStage + bi * kBTile, kBSbo);
-                    const uint32_t d = tmem + static_cast<uint32_t>((KP * pr + bi) * BN);
+                    const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
                     tc_mma(d, ad, bd, idesc, 0u);
                     tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
+                    tc_commit(bar_acc_full(BARS, buf));
                 }
-                tc_commit(bar_empty(BARS, st));
-                tc_commit(bar_acc_full(BARS, pr));
+                __syncwarp();
             }
+            if (!ok) break;
+            if (lane == 0) tc_commit(bar_empty(BARS, st));
             __syncwarp();
             QMM_TRACE(14, kb0);
         }
@@ -724,17 +766,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
         // ------------------------------------------------------------ epilogue
-        // Per K block b: y += (d * s_x[m][b]) * I_b, with y (64 columns of this
-        // thread's token row) in registers; d per 256 columns (q6_K) or per
-        // block (Q4_0) comes from the converters through shared memory. The
-        // accumulators of one stage (two blocks) are released together.
+        // Per K block b: I_b from its accumulator buffer. q6_K (d per 256
+        // columns): z += s_x[m][b] * I_b in registers (one packed FMA per two
+        // values), and at the end of each super-block y += d * z on the
+        // running output, which lives in tensor memory (columns kYCol ..);
+        // Q4_0 (d per block): y += (d * s_x[m][b]) * I_b with y in registers.
+        // A buffer is released as soon as it has been read.
         const int quad = warp & 3;           // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
         const int h = (warp - kEpi0) >> 2;   // columns 64*h .. +63 of the tile
         const int64_t m = mt * BM + 32 * quad + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-        float y[64];
+        const uint32_t ycol = tl + static_cast<uint32_t>(kYCol) + 64 * h;
+        float y[64];  // q6_K: z, the current super-block's sum; Q4_0: the output
 #pragma unroll
         for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+        if (Q6) {
+            float zero[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) zero[c] = 0.0f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) tc_st16(ycol + 16 * qq, zero);
+            tc_wait_st();
+        }
         // s_x of this thread's row, loaded one stage ahead of their use (the
         // rows are strided in memory: each lane's load is its own transaction)
         float sxa[KP], sxb[KP];
@@ -750,52 +803,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t q = 0; ok && q * KP < nkb; ++q) {
             const int64_t kb0 = q * KP;
             const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
-            const int pr = static_cast<int>(q % NP);
             load_sx(q + 1, sxb);
-            QMM_TRACE(30, kb0);
-            if (!wait_or_abort(bar_acc_full(BARS, pr), (q / NP) & 1, FLAG, a.st.err)) {
-                ok = false;
-                break;
-            }
-            QMM_TRACE(31, kb0);
-            tc_fence_after();
             for (int bi = 0; bi < nbk; ++bi) {
                 const int64_t kb = kb0 + bi;
-                const float sx = sxa[bi];
-                const float2 s2 = make_float2(sx, sx);
-                // this block's d (q6_K: its super-block's, Q4_0: its own)
-                const int64_t dk = Q6 ? (kb >> 3) : kb;
-                const int di = static_cast<int>(dk % DR);
-                if ((Q6 ? (kb & 7) == 0 : true) &&
-                    !wait_or_abort(bar_dv_full(BARS, di), (dk / DR) & 1, FLAG, a.st.err)) {
+                const int buf = static_cast<int>(kb % NACC);
+                QMM_TRACE(30, kb);
+                if (!wait_or_abort(bar_acc_full(BARS, buf), (kb / NACC) & 1, FLAG, a.st.err)) {
                     ok = false;
                     break;
                 }
-                const uint32_t acc = tl + static_cast<uint32_t>((KP * pr + bi) * BN) + 64 * h;
+                QMM_TRACE(31, kb);
+                tc_fence_after();
+                const float sx = sxa[bi];
+                const float2 s2 = make_float2(sx, sx);
+                const uint32_t acc = tl + static_cast<uint32_t>(buf * BN) + 64 * h;
+                if (Q6) {
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[32];
-                    tc_ld32(acc + 32 * half, v);
-                    tc_wait_ld();
-                    const uint32_t dv = S + L.dv + (di * BN + 64 * h + 32 * half) * 4;
+                    for (int qq = 0; qq < 4; ++qq) {
+                        float v[16];
+                        tc_ld16(acc + 16 * qq, v);
+                        tc_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        float2 d2;
-                        asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
-                        const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
-                                               make_float2(y[32 * half + c], y[32 * half + c + 1]));
-                        y[32 * half + c] = t.x;
-                        y[32 * half + c + 1] = t.y;
+                        for (int c = 0; c < 16; c += 2) {
+                            const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2,
+                                                   make_float2(y[16 * qq + c], y[16 * qq + c + 1]));
+                            y[16 * qq + c] = t.x;
+                            y[16 * qq + c + 1] = t.y;
+                        }
                     }
+                } else {
+                    // this block's d
+                    const int di = static_cast<int>(kb % DR);
+                    if (!wait_or_abort(bar_dv_full(BARS, di), (kb / DR) & 1, FLAG, a.st.err)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        float v[32];
+                        tc_ld32(acc + 32 * half, v);
+                        tc_wait_ld();
+                        const uint32_t dv = S + L.dv + (di * BN + 64 * h + 32 * half) * 4;
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            float2 d2;
+                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
+                            const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
+                                                   make_float2(y[32 * half + c], y[32 * half + c + 1]));
+                            y[32 * half + c] = t.x;
+                            y[32 * half + c + 1] = t.y;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acc_empty(BARS, buf));
+                QMM_TRACE(32, kb);
+                if (Q6 && ((kb & 7) == 7 || kb + 1 == nkb)) {
+                    // end of the super-block: y += d * z in tensor memory, z = 0
+                    const int64_t dk = kb >> 3;
+                    const int di = static_cast<int>(dk % DR);
+                    if (!wait_or_abort(bar_dv_full(BARS, di), (dk / DR) & 1, FLAG, a.st.err)) {
+                        ok = false;
+                        break;
+                    }
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        float yv[16];
+                        tc_ld16(ycol + 16 * qq, yv);
+                        tc_wait_ld();
+                        const uint32_t dv = S + L.dv + (di * BN + 64 * h + 16 * qq) * 4;
+#pragma unroll
+                        for (int c = 0; c < 16; c += 4) {
+                            float4 d4;
+                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                         : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
+                                         : "r"(dv + 4 * c));
+                            const float2 t0 = ffma2(make_float2(d4.x, d4.y),
+                                                    make_float2(y[16 * qq + c], y[16 * qq + c + 1]),
+                                                    make_float2(yv[c], yv[c + 1]));
+                            const float2 t1 = ffma2(make_float2(d4.z, d4.w),
+                                                    make_float2(y[16 * qq + c + 2], y[16 * qq + c + 3]),
+                                                    make_float2(yv[c + 2], yv[c + 3]));
+                            yv[c] = t0.x;
+                            yv[c + 1] = t0.y;
+                            yv[c + 2] = t1.x;
+                            yv[c + 3] = t1.y;
+                        }
+                        tc_st16(ycol + 16 * qq, yv);
+                    }
+                    tc_wait_st();
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) y[c] = 0.0f;
                 }
             }
             if (!ok) break;
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, pr));
-            QMM_TRACE(32, kb0);
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) sxa[bi] = sxb[bi];
+        }
+        if (ok && Q6) {
+            // the running output, out of tensor memory (every lane: the loads are warp-wide)
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                float v[16];
+                tc_ld16(ycol + 16 * qq, v);
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) y[16 * qq + c] = v[c];
+            }
         }
         if (ok && m < a.M) {
             const int64_t nb0 = n0 + 64 * h;
