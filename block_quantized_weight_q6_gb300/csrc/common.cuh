@@ -204,36 +204,12 @@ __device__ __forceinline__ float byte_as_magic_float(uint32_t codes) {
     return __uint_as_float(__byte_perm(codes, 0x4B000000u, 0x7540u + J));
 }
 
-// Packed fp32 pair arithmetic (sm_100 family): one instruction, two lanes.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n"
-        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n"
-        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n"
-        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
+// Packed fp32 pair arithmetic (sm_100 family): one instruction, two lanes,
+// each lane rounded as the scalar operation would be. The compiler builtins
+// let the register allocator keep the pairs in adjacent registers.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -25,18 +25,21 @@
 // after that is shared code, so their outputs are bitwise identical (section
 // 2.3: identity by construction).
 //
-// CTA roles (480 threads):
+// CTA roles (896 threads):
 //   warp 0      A producer: 1-D bulk TMA copies of the A tiles (quantized
 //               activations, pre-tiled by the quantizer), up to NA blocks
 //               ahead of the MMAs
-//   warp 14     raw producer: the weight stages, up to NR 256-column chunks
+//   warp 2      raw producer: the weight stages, up to NR 256-column chunks
 //               ahead of the converters: q6_K / Q4_0 rows through a tensor
 //               map (W as groups of 8 rows), plane rows and scales as 1-D
 //               copies
 //   warp 1      owns the tensor memory; one lane issues tcgen05.mma
-//   warps 2-5   converters: weights -> fp16 B tile (core-matrix layout);
+//   warps 4-11  converters: weights -> fp16 B tile (core-matrix layout);
 //               warp cw converts the rows 8 g + j, j = 2 cw, 2 cw + 1
-//   warps 6-13  epilogue: tcgen05.ld of the accumulator, scaling, output
+//   warps 12-27 epilogue: tcgen05.ld of the accumulator, scaling, output
+//   warp 3      idle
+// Registers are moved between warpgroups (setmaxnreg): the producers' and
+// the MMA's warpgroup gives up most of its share to the epilogue's.
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -61,10 +64,17 @@ constexpr int NACC = 3;           // per-block accumulator buffers in tensor mem
 constexpr int kYCol = NACC * 128; // q6_K: the running output, columns kYCol .. kYCol + 127
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
 constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
-constexpr int kThreads = 480;                // 15 warps: 128 registers a thread
-constexpr int kRawWarp = 14;                // raw weight producer
-constexpr int kConv0 = 2, kConvWarps = 4;   // converter warps
-constexpr int kEpi0 = 6;                    // epilogue warps kEpi0 .. kEpi0 + 7
+constexpr int kThreads = 896;                // 28 warps (7 warpgroups), 72 registers a thread at launch
+constexpr int kRawWarp = 2;                 // raw weight producer
+constexpr int kConv0 = 4, kConvWarps = 8;   // converter warps (warpgroups 1, 2)
+constexpr int kConvRows = 8 / kConvWarps;   // rows 8 g + j a converter lane takes per pass (j = kConvRows cw + jj)
+constexpr int kEpi0 = 12, kEpiWarps = 16;   // epilogue warps (warpgroups 3 .. 6)
+constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
+// registers per thread after the reallocation: 4 warps x 40 + 8 x 72 + 16 x 80 = 2016 x 32, the
+// 28 x 72 x 32 the block is launched with (an increase beyond that pool would never complete)
+constexpr int kRegsLow = 40, kRegsEpi = 80;
+static_assert(4 * kRegsLow + kConvWarps * 72 + kEpiWarps * kRegsEpi <= kThreads / 32 * 72, "register pool");
+static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
 constexpr int kTmemCols = 512;    // NACC * BN accumulators and the q6_K running output
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
 // B stage: 16 groups of 8 weight rows, kBSbo bytes apart (a 16-byte odd
@@ -200,26 +210,6 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
-        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15])
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -298,6 +288,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
         }
     }
 }
+
 
 // ---------------------------------------------------------------- B tile
 // Converter lane (kc = lane / 8, rw = lane % 8) writes 8 fp16 values: row
@@ -405,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t FLAG = S + L.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = a.K / 32;
+    const uint32_t nkb32 = static_cast<uint32_t>(nkb);
     const int64_t nsc = (a.K + 255) / 256;  // 256-column super-chunks
     const int64_t mt = blockIdx.y, nt = blockIdx.x;
     const int64_t n0 = nt * BN;
@@ -422,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < NP; ++i) {
             mbar_init(bar_acc_full(BARS, i), 1);
-            mbar_init(bar_acc_empty(BARS, i), 8);  // the epilogue warps
+            mbar_init(bar_acc_empty(BARS, i), kEpiWarps);  // the epilogue warps
         }
         for (int i = 0; i < DR; ++i) mbar_init(bar_dv_full(BARS, i), 4);  // converters of rows 0..127
         asm volatile("st.shared.u32 [%0], %1;" ::"r"(FLAG), "r"(0u) : "memory");
@@ -441,11 +433,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the quantized activations come from the previous kernel on the stream
     grid_dependency_wait();
 
+    // Registers move between warpgroups (warpgroup-wide instructions): the
+    // first warpgroup (producers, MMA issue, one idle warp) gives up most of
+    // its share, the epilogue's two warpgroups take it.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0 || warp == kRawWarp) {
         // ------------------------------------------------------------ producers
         const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
         // raw stage of 256-column chunk sc into slot sc % NR
-        auto issue_raw = [&](int64_t sc) {
+        auto issue_raw = [&](uint32_t sc) {
             const int r = static_cast<int>(sc % NR);
             const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
             const uint32_t bar = bar_raw_full(BARS, r);
@@ -495,63 +492,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bulk_g2s(rw0 + 8u * 16u * RS + tr * RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
         };
         if (warp == kRawWarp) {
-            for (int64_t sc = 0; sc < nsc; ++sc) {
+            uint32_t r = 0, eph = 1;  // raw slot; parity of its release ((sc / NR) - 1) & 1
+            const uint32_t nsc32 = static_cast<uint32_t>(nsc);
+            for (uint32_t sc = 0; sc < nsc32; ++sc) {
                 QMM_TRACE(1, sc);
-                if (sc >= NR &&
-                    !wait_or_abort(bar_raw_empty(BARS, static_cast<int>(sc % NR)), ((sc / NR) - 1) & 1, FLAG,
-                                   a.st.err))
-                    break;
+                if (sc >= NR && !wait_or_abort(bar_raw_empty(BARS, static_cast<int>(r)), eph, FLAG, a.st.err)) break;
                 issue_raw(sc);
+                if (++r == NR) {
+                    r = 0;
+                    eph ^= 1;
+                }
             }
             // the copies still in flight land before the CTA ends
             for (int64_t sc = nsc > NR ? nsc - NR : 0; sc < nsc; ++sc)
                 (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(sc % NR)), (sc / NR) & 1, FLAG, a.st.err);
         } else {
-            for (int64_t q = 0; q * KP < nkb; ++q) {
+            uint32_t st = 0, eph = 1;  // stage; parity of its release ((q / NS) - 1) & 1
+            for (uint32_t q = 0, kb0 = 0; kb0 < nkb32; ++q, kb0 += KP) {
                 // the A tiles of blocks KP q .. (consecutive in the pre-tiled operand)
-                const int64_t kb0 = q * KP;
-                const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
-                const int st = static_cast<int>(q % NS);
+                const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
                 QMM_TRACE(2, kb0);
-                if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err))
-                    break;
+                if (q >= NS && !wait_or_abort(bar_empty(BARS, static_cast<int>(st)), eph, FLAG, a.st.err)) break;
                 QMM_TRACE(3, kb0);
                 if (lane == 0) {
                     // pull the tiles kPrefetch stages ahead into L2 first: the
                     // copy into shared memory then waits on L2, not on DRAM
-                    const int64_t pk = kb0 + kPrefetch * KP;
+                    const uint32_t pk = kb0 + kPrefetch * KP;
                     if (q == 0)
-                        for (int64_t k = 0; k < pk && k < nkb; k += KP)
-                            prefetch_l2(a.a16 + (mt * nkb + k) * (BM * 32),
-                                        (nkb - k < KP ? static_cast<uint32_t>(nkb - k) : KP) * kATile);
-                    if (pk < nkb)
-                        prefetch_l2(a.a16 + (mt * nkb + pk) * (BM * 32),
-                                    (nkb - pk < KP ? static_cast<uint32_t>(nkb - pk) : KP) * kATile);
-                    mbar_arrive_expect_tx(bar_full(BARS, st), nbk * kATile);
+                        for (uint32_t k = 0; k < pk && k < nkb32; k += KP)
+                            prefetch_l2(a.a16 + (mt * nkb + k) * (BM * 32), (nkb32 - k < KP ? nkb32 - k : KP) * kATile);
+                    if (pk < nkb32)
+                        prefetch_l2(a.a16 + (mt * nkb + pk) * (BM * 32), (nkb32 - pk < KP ? nkb32 - pk : KP) * kATile);
+                    mbar_arrive_expect_tx(bar_full(BARS, static_cast<int>(st)), nbk * kATile);
                     bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kb0) * (BM * 32), nbk * kATile,
-                             bar_full(BARS, st));
+                             bar_full(BARS, static_cast<int>(st)));
                 }
                 __syncwarp();
+                if (++st == NS) {
+                    st = 0;
+                    eph ^= 1;
+                }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc = idesc_f16(BM, BN);
         bool ok = true;
-        for (int64_t q = 0; ok && q * KP < nkb; ++q) {
-            const int64_t kb0 = q * KP;
-            const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
-            const int st = static_cast<int>(q % NS);
+        uint32_t st = 0, fph = 0;   // stage; parity of its fill (q / NS) & 1
+        uint32_t buf = 0, eph = 1;  // accumulator buffer; parity of its release ((kb / NACC) - 1) & 1
+        for (uint32_t kb0 = 0; ok && kb0 < nkb32; kb0 += KP) {
+            const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
             QMM_TRACE(10, kb0);
-            if (!wait_or_abort(bar_full(BARS, st), (q / NS) & 1, FLAG, a.st.err)) break;
+            if (!wait_or_abort(bar_full(BARS, static_cast<int>(st)), fph, FLAG, a.st.err)) break;
             QMM_TRACE(12, kb0);
-            for (int bi = 0; bi < nbk; ++bi) {
+            for (uint32_t bi = 0; bi < nbk; ++bi) {
                 // block kb into accumulator buffer kb % NACC, once the
                 // epilogue has read that buffer's previous block
-                const int64_t kb = kb0 + bi;
-                const int buf = static_cast<int>(kb % NACC);
-                if (kb >= NACC &&
-                    !wait_or_abort(bar_acc_empty(BARS, buf), ((kb / NACC) - 1) & 1, FLAG, a.st.err)) {
+                const uint32_t kb = kb0 + bi;
+                if (kb >= NACC && !wait_or_abort(bar_acc_empty(BARS, static_cast<int>(buf)), eph, FLAG, a.st.err)) {
                     ok = false;
                     break;
                 }
@@ -559,89 +557,94 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     const uint64_t ad = smem_desc(S + L.a + st * kAStage + bi * kATile);
                     const uint64_t bd = smem_desc(S + L.b + st * kBStage + bi * kBTile, kBSbo);
-                    const uint32_t d = tmem + static_cast<uint32_t>(buf * BN);
+                    const uint32_t d = tmem + buf * BN;
                     tc_mma(d, ad, bd, idesc, 0u);
                     tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
-                    tc_commit(bar_acc_full(BARS, buf));
+                    tc_commit(bar_acc_full(BARS, static_cast<int>(buf)));
                 }
                 __syncwarp();
+                if (++buf == NACC) {
+                    buf = 0;
+                    eph ^= 1;
+                }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(bar_empty(BARS, st));
+            if (lane == 0) tc_commit(bar_empty(BARS, static_cast<int>(st)));
             __syncwarp();
+            if (++st == NS) {
+                st = 0;
+                fph ^= 1;
+            }
             QMM_TRACE(14, kb0);
         }
+    }
     } else if (warp < kEpi0) {
         // ------------------------------------------------------------ converters
         // One stage (two K blocks) per pass: one wait, one proxy fence and one
-        // arrival. Warp cw converts the rows 8 g + j of the tile (the plane
-        // variant: g + 16 j) for j = 2 cw, 2 cw + 1: lane (g = lane % 16,
-        // h = lane / 16) the 16 columns 16 h .. 16 h + 15 of each block. In
-        // the raw stage of q6_K / Q4_0 rows, a row's offset inside its slot
-        // depends only on j, so the realignment of its bytes is the same for
-        // the whole warp; plane bytes need none.
+        // arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
+        // variant: g + 16 cw): lane (g = lane % 16, hh = lane / 16) the 16
+        // columns 16 hh .. 16 hh + 15 of each block. In the raw stage of q6_K
+        // / Q4_0 rows, a row's offset inside its slot depends only on cw, so
+        // the realignment of its bytes is the same for the whole warp; plane
+        // bytes need none.
+        static_assert(kConvRows == 1 && KP == 2, "a converter pass is one row and one stage of two blocks");
+        static_assert((DR & (DR - 1)) == 0, "the d ring is a power of two");
         const int cw = warp - kConv0;
         const int tid = threadIdx.x - 32 * kConv0;  // rows 0..127 store d
         const int g = lane & 15, hh = lane >> 4;
+        // A row's place inside a raw stage (the plane variant: its scales and
+        // d), and the lead-in of its bytes there for the first 256-column
+        // chunk: each further chunk moves a q6_K row by 210 = 2 (mod 16)
+        // bytes and a Q4_0 row by 8 * 18 = 0 (mod 16).
+        auto row_off = [&](int nn) -> uint32_t {
+            const int64_t gg = n0 + nn;
+            if (gg < a.n8) return RW + static_cast<uint32_t>(nn & 7) * 16u * RS + static_cast<uint32_t>(nn >> 3) * RS;
+            return RW + 8u * 16u * RS + static_cast<uint32_t>(gg - a.n8) * RS;
+        };
+        auto lead0 = [&](int64_t gg) -> uint32_t {
+            return static_cast<uint32_t>((gg * a.rowbytes + (EXP ? 192 : 0)) & 15);
+        };
+        const int n = EXP ? g + 16 * cw : 8 * g + cw;  // this lane's row of the tile
+        const bool live = n0 + n < a.N;
+        const uint32_t ro = row_off(n), l0 = live ? lead0(n0 + n) : 0u;
+        const bool live_d = tid < BN && n0 + tid < a.N;  // row tid, whose d this lane stores
+        const uint32_t ro_d = live_d ? row_off(tid) : 0u, l0_d = live_d ? lead0(n0 + tid) : 0u;
         bool scale_bad = false;
-        for (int64_t kb0 = 0; kb0 < nkb; kb0 += 2) {
-            const int nbk = nkb - kb0 < 2 ? 1 : 2;
-            const int64_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
-            const int j0 = static_cast<int>(kb0 & 7);
-            const int r = static_cast<int>(sc % NR);
-            const uint32_t raw0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
-            // row n of the tile within the raw stage
-            // (the plane variant: its scales and d)
-            auto rowaddr = [&](int n) -> uint32_t {
-                const int64_t ng = n0 + n;
-                if (ng < a.n8)
-                    return raw0 + RW + static_cast<uint32_t>(n & 7) * 16u * RS + static_cast<uint32_t>(n >> 3) * RS;
-                return raw0 + RW + 8u * 16u * RS + static_cast<uint32_t>(ng - a.n8) * RS;
-            };
-            // lead-in of row n's data inside its raw stage row
-            auto lead = [&](int64_t ng) -> uint32_t {
-                if (EXP) return static_cast<uint32_t>(((ng * a.nb + sc) * 210 + 192) & 15);
-                if (Q6) return static_cast<uint32_t>(((ng * a.nb + sc) * 210) & 15);
-                return static_cast<uint32_t>(((ng * a.nb + sc * 8) * 18) & 15);
-            };
+        uint32_t r = 0, rph = 0;   // raw slot; parity of its fill (sc / NR) & 1
+        uint32_t st = 0, eph = 1;  // B stage; parity of its release ((q / NS) - 1) & 1
+        for (uint32_t q = 0, kb0 = 0; kb0 < nkb32; ++q, kb0 += 2) {
+            const uint32_t nbk = nkb32 - kb0 < 2 ? 1u : 2u;
+            const uint32_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
+            const uint32_t j0 = kb0 & 7;
+            const uint32_t raw0 = S + L.raw + r * L.rawslot;
+            const uint32_t ls = Q6 ? 2u * sc : 0u;
             QMM_TRACE(20, kb0);
-            if (j0 == 0 && !wait_or_abort(bar_raw_full(BARS, r), (sc / NR) & 1, FLAG, a.st.err)) break;
+            if (j0 == 0 && !wait_or_abort(bar_raw_full(BARS, static_cast<int>(r)), rph, FLAG, a.st.err)) break;
             QMM_TRACE(21, kb0);
-            // d of row tid (q6_K: once per super-block, Q4_0: per block)
-            {
-                const int64_t ng = n0 + tid;
-                for (int bi = 0; bi < (Q6 ? (j0 == 0 ? 1 : 0) : nbk); ++bi) {
-                    const int64_t kb = kb0 + bi;
-                    const int di = static_cast<int>(Q6 ? (sc % DR) : (kb % DR));
+            // d of row tid (q6_K: once per super-block, Q4_0: per block), by
+            // the first four converter warps (rows 0..127)
+            if (tid < BN) {
+                for (uint32_t bi = 0; bi < (Q6 ? (j0 == 0 ? 1u : 0u) : nbk); ++bi) {
+                    const uint32_t di = (Q6 ? sc : kb0 + bi) & (DR - 1);
                     float dval = 0.0f;
-                    if (ng < a.N) {
-                        const uint32_t rowb = rowaddr(tid) + lead(ng);
+                    if (live_d) {
+                        const uint32_t rowb = raw0 + ro_d + ((l0_d + ls) & 15u);
                         const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * (j0 + bi));
                         dval = half_bits_to_float(lds_u16(rowb + doff));
                     }
                     asm volatile("st.shared.f32 [%0], %1;" ::"r"(S + L.dv + (di * BN + tid) * 4), "f"(dval)
                                  : "memory");
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar_dv_full(BARS, di));
+                    if (lane == 0) mbar_arrive(bar_dv_full(BARS, static_cast<int>(di)));
                 }
             }
-            static_assert(KP == 2, "a converter pass is one stage of two blocks");
-            const int64_t q = kb0 / KP;
-            const int st = static_cast<int>(q % NS);
-            if (q >= NS && !wait_or_abort(bar_empty(BARS, st), ((q / NS) - 1) & 1, FLAG, a.st.err)) break;
+            if (q >= NS && !wait_or_abort(bar_empty(BARS, static_cast<int>(st)), eph, FLAG, a.st.err)) break;
             QMM_TRACE(22, kb0);
-            // Rows 8 g + j of the tile, j = 2 cw and 2 cw + 1 (the plane
-            // variant: rows g + 16 j, consecutive rows in consecutive lanes):
-            // per row, the raw bytes of both blocks of the stage are loaded
+            // Per row, the raw bytes of both blocks of the stage are loaded
             // first, then realigned by the row's lead (warp-uniform for rows
-            // 8 g + j), expanded and stored.
-#pragma unroll 1
-            for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * cw + jj;
-                const int n = EXP ? g + 16 * j : 8 * g + j;
-                const int64_t ng = n0 + n;
-                const bool live = ng < a.N;
-                const uint32_t rb = rowaddr(n) + lead(ng);
+            // 8 g + cw), expanded and stored.
+            {
+                const uint32_t rb = raw0 + ro + ((l0 + ls) & 15u);
                 uint32_t hv[KP][8];
                 if (Q6) {
                     uint32_t c[KP][4];
@@ -756,145 +759,150 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_full(BARS, st));
+            if (lane == 0) mbar_arrive(bar_full(BARS, static_cast<int>(st)));
             QMM_TRACE(23, kb0);
-            if (j0 + nbk == 8 || kb0 + nbk == nkb) {
+            if (++st == NS) {
+                st = 0;
+                eph ^= 1;
+            }
+            if (j0 + nbk == 8 || kb0 + nbk == nkb32) {
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar_raw_empty(BARS, r));
+                if (lane == 0) mbar_arrive(bar_raw_empty(BARS, static_cast<int>(r)));
+                if (++r == NR) {
+                    r = 0;
+                    rph ^= 1;
+                }
             }
         }
         if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ------------------------------------------------------------ epilogue
-        // Per K block b: I_b from its accumulator buffer. q6_K (d per 256
-        // columns): z += s_x[m][b] * I_b in registers (one packed FMA per two
-        // values), and at the end of each super-block y += d * z on the
-        // running output, which lives in tensor memory (columns kYCol ..);
-        // Q4_0 (d per block): y += (d * s_x[m][b]) * I_b with y in registers.
-        // A buffer is released as soon as it has been read.
-        const int quad = warp & 3;           // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
-        const int h = (warp - kEpi0) >> 2;   // columns 64*h .. +63 of the tile
+        // Per K block b: I_b from its accumulator buffer, one tensor-memory
+        // load of the thread's kEpiCols columns, after which the buffer is
+        // released at once. q6_K (d per 256 columns): z += s_x[m][b] * I_b in
+        // registers (one packed FMA per two values), and at the end of each
+        // super-block y += d * z on the running output, which lives in tensor
+        // memory (columns kYCol ..); Q4_0 (d per block): y += (d * s_x[m][b])
+        // * I_b with y in registers.
+        const int quad = warp & 3;                  // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
+        const int h = (warp - kEpi0) >> 2;          // columns kEpiCols*h .. of the tile
         const int64_t m = mt * BM + 32 * quad + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
-        const uint32_t ycol = tl + static_cast<uint32_t>(kYCol) + 64 * h;
-        float y[64];  // q6_K: z, the current super-block's sum; Q4_0: the output
+        const uint32_t c0 = static_cast<uint32_t>(kEpiCols * h);
+        const uint32_t ycol = tl + static_cast<uint32_t>(kYCol) + c0;
+        float y[kEpiCols];  // q6_K: z, the current super-block's sum; Q4_0: the output
 #pragma unroll
-        for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+        for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
         if (Q6) {
-            float zero[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) zero[c] = 0.0f;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) tc_st16(ycol + 16 * qq, zero);
+            tc_st32(ycol, y);
             tc_wait_st();
         }
         // s_x of this thread's row, loaded one stage ahead of their use (the
-        // rows are strided in memory: each lane's load is its own transaction)
+        // rows are strided in memory: each lane's load is its own
+        // transaction). The loads are volatile so that the compiler issues
+        // them here rather than next to their use, where their latency would
+        // be exposed once per stage.
         float sxa[KP], sxb[KP];
-        auto load_sx = [&](int64_t q, float (&o)[KP]) {
+        const float* xrow = a.xs + (m < a.M ? m : 0) * nkb;
+        auto load_sx = [&](uint32_t q, float (&o)[KP]) {
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) {
-                const int64_t kb = q * KP + bi;
-                o[bi] = (m < a.M && kb < nkb) ? __ldg(a.xs + m * nkb + kb) : 0.0f;
+                const uint32_t kb = q * KP + bi;
+                o[bi] = 0.0f;
+                if (m < a.M && kb < nkb32) asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(o[bi]) : "l"(xrow + kb));
             }
         };
         load_sx(0, sxa);
         bool ok = true;
-        for (int64_t q = 0; ok && q * KP < nkb; ++q) {
-            const int64_t kb0 = q * KP;
-            const int nbk = nkb - kb0 < KP ? static_cast<int>(nkb - kb0) : KP;
+        uint32_t buf = 0, fph = 0;  // accumulator buffer; parity of its fill (kb / NACC) & 1
+        for (uint32_t q = 0, kb0 = 0; ok && kb0 < nkb32; ++q, kb0 += KP) {
+            const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
             load_sx(q + 1, sxb);
-            for (int bi = 0; bi < nbk; ++bi) {
-                const int64_t kb = kb0 + bi;
-                const int buf = static_cast<int>(kb % NACC);
+            for (uint32_t bi = 0; bi < nbk; ++bi) {
+                const uint32_t kb = kb0 + bi;
                 QMM_TRACE(30, kb);
-                if (!wait_or_abort(bar_acc_full(BARS, buf), (kb / NACC) & 1, FLAG, a.st.err)) {
+                if (!wait_or_abort(bar_acc_full(BARS, static_cast<int>(buf)), fph, FLAG, a.st.err)) {
                     ok = false;
                     break;
                 }
                 QMM_TRACE(31, kb);
                 tc_fence_after();
+                float v[kEpiCols];
+                tc_ld32(tl + buf * BN + c0, v);
+                tc_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acc_empty(BARS, static_cast<int>(buf)));
+                if (++buf == NACC) {
+                    buf = 0;
+                    fph ^= 1;
+                }
                 const float sx = sxa[bi];
                 const float2 s2 = make_float2(sx, sx);
-                const uint32_t acc = tl + static_cast<uint32_t>(buf * BN) + 64 * h;
                 if (Q6) {
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        float v[16];
-                        tc_ld16(acc + 16 * qq, v);
-                        tc_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 16; c += 2) {
-                            const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2,
-                                                   make_float2(y[16 * qq + c], y[16 * qq + c + 1]));
-                            y[16 * qq + c] = t.x;
-                            y[16 * qq + c + 1] = t.y;
-                        }
+                    for (int c = 0; c < kEpiCols; c += 2) {
+                        const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2, make_float2(y[c], y[c + 1]));
+                        y[c] = t.x;
+                        y[c + 1] = t.y;
                     }
                 } else {
                     // this block's d
-                    const int di = static_cast<int>(kb % DR);
-                    if (!wait_or_abort(bar_dv_full(BARS, di), (kb / DR) & 1, FLAG, a.st.err)) {
+                    const uint32_t di = kb & (DR - 1);
+                    if (!wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (kb / DR) & 1, FLAG, a.st.err)) {
                         ok = false;
                         break;
                     }
+                    const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        float v[32];
-                        tc_ld32(acc + 32 * half, v);
-                        tc_wait_ld();
-                        const uint32_t dv = S + L.dv + (di * BN + 64 * h + 32 * half) * 4;
-#pragma unroll
-                        for (int c = 0; c < 32; c += 2) {
-                            float2 d2;
-                            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(d2.x), "=f"(d2.y) : "r"(dv + 4 * c));
-                            const float2 t = ffma2(fmul2(make_float2(v[c], v[c + 1]), d2), s2,
-                                                   make_float2(y[32 * half + c], y[32 * half + c + 1]));
-                            y[32 * half + c] = t.x;
-                            y[32 * half + c + 1] = t.y;
-                        }
+                    for (int c = 0; c < kEpiCols; c += 4) {
+                        float4 d4;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
+                                     : "r"(dv + 4 * c));
+                        const float2 t0 = ffma2(fmul2(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y)), s2,
+                                                make_float2(y[c], y[c + 1]));
+                        const float2 t1 = ffma2(fmul2(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w)), s2,
+                                                make_float2(y[c + 2], y[c + 3]));
+                        y[c] = t0.x;
+                        y[c + 1] = t0.y;
+                        y[c + 2] = t1.x;
+                        y[c + 3] = t1.y;
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acc_empty(BARS, buf));
                 QMM_TRACE(32, kb);
-                if (Q6 && ((kb & 7) == 7 || kb + 1 == nkb)) {
+                if (Q6 && ((kb & 7) == 7 || kb + 1 == nkb32)) {
                     // end of the super-block: y += d * z in tensor memory, z = 0
-                    const int64_t dk = kb >> 3;
-                    const int di = static_cast<int>(dk % DR);
-                    if (!wait_or_abort(bar_dv_full(BARS, di), (dk / DR) & 1, FLAG, a.st.err)) {
+                    const uint32_t dk = kb >> 3;
+                    const uint32_t di = dk & (DR - 1);
+                    if (!wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (dk / DR) & 1, FLAG, a.st.err)) {
                         ok = false;
                         break;
                     }
+                    float yv[kEpiCols];
+                    tc_ld32(ycol, yv);
+                    tc_wait_ld();
+                    const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        float yv[16];
-                        tc_ld16(ycol + 16 * qq, yv);
-                        tc_wait_ld();
-                        const uint32_t dv = S + L.dv + (di * BN + 64 * h + 16 * qq) * 4;
-#pragma unroll
-                        for (int c = 0; c < 16; c += 4) {
-                            float4 d4;
-                            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                         : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
-                                         : "r"(dv + 4 * c));
-                            const float2 t0 = ffma2(make_float2(d4.x, d4.y),
-                                                    make_float2(y[16 * qq + c], y[16 * qq + c + 1]),
-                                                    make_float2(yv[c], yv[c + 1]));
-                            const float2 t1 = ffma2(make_float2(d4.z, d4.w),
-                                                    make_float2(y[16 * qq + c + 2], y[16 * qq + c + 3]),
-                                                    make_float2(yv[c + 2], yv[c + 3]));
-                            yv[c] = t0.x;
-                            yv[c + 1] = t0.y;
-                            yv[c + 2] = t1.x;
-                            yv[c + 3] = t1.y;
-                        }
-                        tc_st16(ycol + 16 * qq, yv);
+                    for (int c = 0; c < kEpiCols; c += 4) {
+                        float4 d4;
+                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                     : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
+                                     : "r"(dv + 4 * c));
+                        const float2 t0 = ffma2(make_float2(d4.x, d4.y), make_float2(y[c], y[c + 1]),
+                                                make_float2(yv[c], yv[c + 1]));
+                        const float2 t1 = ffma2(make_float2(d4.z, d4.w), make_float2(y[c + 2], y[c + 3]),
+                                                make_float2(yv[c + 2], yv[c + 3]));
+                        yv[c] = t0.x;
+                        yv[c + 1] = t0.y;
+                        yv[c + 2] = t1.x;
+                        yv[c + 3] = t1.y;
                     }
+                    tc_st32(ycol, yv);
                     tc_wait_st();
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) y[c] = 0.0f;
+                    for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
                 }
             }
             if (!ok) break;
@@ -902,25 +910,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int bi = 0; bi < KP; ++bi) sxa[bi] = sxb[bi];
         }
         if (ok && Q6) {
-            // the running output, out of tensor memory (every lane: the loads are warp-wide)
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                float v[16];
-                tc_ld16(ycol + 16 * qq, v);
-                tc_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 16; ++c) y[16 * qq + c] = v[c];
-            }
+            // the running output, out of tensor memory (every lane: the load is warp-wide)
+            tc_ld32(ycol, y);
+            tc_wait_ld();
         }
         if (ok && m < a.M) {
-            const int64_t nb0 = n0 + 64 * h;
+            const int64_t nb0 = n0 + c0;
             float* out = a.Y + m * a.N + nb0;
-            if (nb0 + 64 <= a.N && (a.N & 3) == 0) {
+            if (nb0 + kEpiCols <= a.N && (a.N & 3) == 0) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 4)
+                for (int c = 0; c < kEpiCols; c += 4)
                     *reinterpret_cast<float4*>(out + c) = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
             } else {
-                for (int c = 0; c < 64; ++c)
+                for (int c = 0; c < kEpiCols; ++c)
                     if (nb0 + c < a.N) out[c] = y[c];
             }
         }
