@@ -27,19 +27,25 @@
 //
 // CTA roles (896 threads):
 //   warp 0      A producer: 1-D bulk TMA copies of the A tiles (quantized
-//               activations, pre-tiled by the quantizer), up to NA blocks
-//               ahead of the MMAs
+//               activations, pre-tiled by the quantizer), NS stages ahead
+//               of the MMAs
 //   warp 2      raw producer: the weight stages, up to NR 256-column chunks
 //               ahead of the converters: q6_K / Q4_0 rows through a tensor
-//               map (W as groups of 8 rows), plane rows and scales as 1-D
-//               copies
-//   warp 1      owns the tensor memory; one lane issues tcgen05.mma
+//               map (W as groups of 8 rows); the plane variant takes its
+//               plane tile and each row's scales and d the same way
+//   warp 1      owns the tensor memory; one lane issues tcgen05.mma, the
+//               KP blocks of a stage into two of the NACC = 4 accumulator
+//               buffers, and signals the epilogue once per stage
 //   warps 4-11  converters: weights -> fp16 B tile (core-matrix layout);
-//               warp cw converts the rows 8 g + j, j = 2 cw, 2 cw + 1
-//   warps 12-27 epilogue: tcgen05.ld of the accumulator, scaling, output
+//               warp cw converts the rows 8 g + cw (the plane variant:
+//               g + 16 cw)
+//   warps 12-27 epilogue: tcgen05.ld of the accumulators, scaling, output
 //   warp 3      idle
 // Registers are moved between warpgroups (setmaxnreg): the producers' and
 // the MMA's warpgroup gives up most of its share to the epilogue's.
+// Handing work between warps through an mbarrier costs a few hundred cycles
+// of a warp's time, so the epilogue and the MMA meet once per stage of KP
+// blocks rather than once per block.
 #include <cuda_fp16.h>
 
 #include <cstring>
@@ -60,8 +66,7 @@ constexpr int NS = 3;             // stages, each the A and B tiles of KP blocks
 constexpr int kPrefetch = 8;      // stages of A tiles prefetched into L2 ahead of their copy
 constexpr int kScMax = 56;        // largest |q6_K sub-block scale| the fp16 B tile holds exactly
 constexpr int NR = 3;             // raw weight stages (256 columns each)
-constexpr int NACC = 3;           // per-block accumulator buffers in tensor memory (a ring)
-constexpr int kYCol = NACC * 128; // q6_K: the running output, columns kYCol .. kYCol + 127
+constexpr int NACC = 4;           // accumulator buffers in tensor memory: two stages of KP blocks
 constexpr int DR_Q6K = 4;         // d ring depth, q6_K (per 256 columns)
 constexpr int DR_Q40 = 16;        // d ring depth, Q4_0 (per 32 columns)
 constexpr int kThreads = 896;                // 28 warps (7 warpgroups), 72 registers a thread at launch
@@ -75,7 +80,7 @@ constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogu
 constexpr int kRegsLow = 40, kRegsEpi = 80;
 static_assert(4 * kRegsLow + kConvWarps * 72 + kEpiWarps * kRegsEpi <= kThreads / 32 * 72, "register pool");
 static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
-constexpr int kTmemCols = 512;    // NACC * BN accumulators and the q6_K running output
+constexpr int kTmemCols = 512;    // NACC * BN accumulators
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
 // B stage: 16 groups of 8 weight rows, kBSbo bytes apart (a 16-byte odd
 // multiple past 512, so that 8 lanes storing one row each of 8 different
@@ -191,37 +196,18 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-
-
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
-        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
-        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
-        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
-        : "memory");
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ---------------------------------------------------------------- trace
 // Diagnostic builds define QMM_GEMM_TRACE and point qmm_gemm_trace at mapped
@@ -539,37 +525,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_f16(BM, BN);
         bool ok = true;
         uint32_t st = 0, fph = 0;   // stage; parity of its fill (q / NS) & 1
-        uint32_t buf = 0, eph = 1;  // accumulator buffer; parity of its release ((kb / NACC) - 1) & 1
-        for (uint32_t kb0 = 0; ok && kb0 < nkb32; kb0 += KP) {
+        for (uint32_t q = 0, kb0 = 0; ok && kb0 < nkb32; ++q, kb0 += KP) {
             const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
             QMM_TRACE(10, kb0);
             if (!wait_or_abort(bar_full(BARS, static_cast<int>(st)), fph, FLAG, a.st.err)) break;
+            // stage q accumulates into buffers 2 (q % 2) + bi, free once the
+            // epilogue has drained stage q - 2
+            if (q >= 2 && !wait_or_abort(bar_acc_empty(BARS, static_cast<int>(q & 1)), ((q >> 1) - 1) & 1, FLAG,
+                                         a.st.err))
+                break;
             QMM_TRACE(12, kb0);
-            for (uint32_t bi = 0; bi < nbk; ++bi) {
-                // block kb into accumulator buffer kb % NACC, once the
-                // epilogue has read that buffer's previous block
-                const uint32_t kb = kb0 + bi;
-                if (kb >= NACC && !wait_or_abort(bar_acc_empty(BARS, static_cast<int>(buf)), eph, FLAG, a.st.err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {
+            tc_fence_after();
+            if (lane == 0) {
+                for (uint32_t bi = 0; bi < nbk; ++bi) {
                     const uint64_t ad = smem_desc(S + L.a + st * kAStage + bi * kATile);
                     const uint64_t bd = smem_desc(S + L.b + st * kBStage + bi * kBTile, kBSbo);
-                    const uint32_t d = tmem + buf * BN;
+                    const uint32_t d = tmem + (2 * (q & 1) + bi) * BN;
                     tc_mma(d, ad, bd, idesc, 0u);
                     tc_mma(d, ad + (256 >> 4), bd + (256 >> 4), idesc, 1u);  // K columns 16..31
-                    tc_commit(bar_acc_full(BARS, static_cast<int>(buf)));
                 }
-                __syncwarp();
-                if (++buf == NACC) {
-                    buf = 0;
-                    eph ^= 1;
-                }
+                tc_commit(bar_acc_full(BARS, static_cast<int>(q & 1)));
+                tc_commit(bar_empty(BARS, static_cast<int>(st)));
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(bar_empty(BARS, static_cast<int>(st)));
             __syncwarp();
             if (++st == NS) {
                 st = 0;
@@ -778,31 +755,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
         // ------------------------------------------------------------ epilogue
-        // Per K block b: I_b from its accumulator buffer, one tensor-memory
-        // load of the thread's kEpiCols columns, after which the buffer is
-        // released at once. q6_K (d per 256 columns): z += s_x[m][b] * I_b in
-        // registers (one packed FMA per two values), and at the end of each
-        // super-block y += d * z on the running output, which lives in tensor
-        // memory (columns kYCol ..); Q4_0 (d per block): y += (d * s_x[m][b])
-        // * I_b with y in registers.
+        // One wait per stage of KP blocks (the MMA signals a stage once), then
+        // per K block b: I_b from its accumulator buffer in two 16-column
+        // tensor-memory loads and y += (I_b * D) * s_x[m][b] in registers (a
+        // packed multiply and a packed FMA per two values; D is d of the
+        // block's super-block for q6_K, of the block for Q4_0, read from
+        // shared memory). The stage's buffers are released together.
         const int quad = warp & 3;                  // tensor-memory lanes 32*quad .. +31 (warp id mod 4)
         const int h = (warp - kEpi0) >> 2;          // columns kEpiCols*h .. of the tile
         const int64_t m = mt * BM + 32 * quad + lane;
         const uint32_t tl = tmem + (static_cast<uint32_t>(32 * quad) << 16);
         const uint32_t c0 = static_cast<uint32_t>(kEpiCols * h);
-        const uint32_t ycol = tl + static_cast<uint32_t>(kYCol) + c0;
-        float y[kEpiCols];  // q6_K: z, the current super-block's sum; Q4_0: the output
+        float y[kEpiCols];  // the output
 #pragma unroll
         for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
-        if (Q6) {
-            tc_st32(ycol, y);
-            tc_wait_st();
-        }
-        // s_x of this thread's row, loaded one stage ahead of their use (the
-        // rows are strided in memory: each lane's load is its own
-        // transaction). The loads are volatile so that the compiler issues
-        // them here rather than next to their use, where their latency would
-        // be exposed once per stage.
         float sxa[KP], sxb[KP];
         const float* xrow = a.xs + (m < a.M ? m : 0) * nkb;
         auto load_sx = [&](uint32_t q, float (&o)[KP]) {
@@ -815,104 +781,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         load_sx(0, sxa);
         bool ok = true;
-        uint32_t buf = 0, fph = 0;  // accumulator buffer; parity of its fill (kb / NACC) & 1
         for (uint32_t q = 0, kb0 = 0; ok && kb0 < nkb32; ++q, kb0 += KP) {
             const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
             load_sx(q + 1, sxb);
+            QMM_TRACE(30, kb0);
+            if (!wait_or_abort(bar_acc_full(BARS, static_cast<int>(q & 1)), (q >> 1) & 1, FLAG, a.st.err)) break;
+            QMM_TRACE(31, kb0);
+            tc_fence_after();
             for (uint32_t bi = 0; bi < nbk; ++bi) {
                 const uint32_t kb = kb0 + bi;
-                QMM_TRACE(30, kb);
-                if (!wait_or_abort(bar_acc_full(BARS, static_cast<int>(buf)), fph, FLAG, a.st.err)) {
+                const uint32_t dk = Q6 ? kb >> 3 : kb;  // index of the d in use
+                const uint32_t di = dk & (DR - 1);
+                if ((!Q6 || (kb & 7) == 0) &&
+                    !wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (dk / DR) & 1, FLAG, a.st.err)) {
                     ok = false;
                     break;
                 }
-                QMM_TRACE(31, kb);
-                tc_fence_after();
-                float v[kEpiCols];
-                tc_ld32(tl + buf * BN + c0, v);
-                tc_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_acc_empty(BARS, static_cast<int>(buf)));
-                if (++buf == NACC) {
-                    buf = 0;
-                    fph ^= 1;
-                }
-                const float sx = sxa[bi];
+                const float sx = bi == 0 ? sxa[0] : sxa[1];
                 const float2 s2 = make_float2(sx, sx);
-                if (Q6) {
+                const uint32_t accb = tl + (2 * (q & 1) + bi) * BN + c0;
+                const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
 #pragma unroll
-                    for (int c = 0; c < kEpiCols; c += 2) {
-                        const float2 t = ffma2(make_float2(v[c], v[c + 1]), s2, make_float2(y[c], y[c + 1]));
-                        y[c] = t.x;
-                        y[c + 1] = t.y;
-                    }
-                } else {
-                    // this block's d
-                    const uint32_t di = kb & (DR - 1);
-                    if (!wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (kb / DR) & 1, FLAG, a.st.err)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
+                for (int hf = 0; hf < 2; ++hf) {
+                    float v[16];
+                    tc_ld16(accb + 16 * hf, v);
+                    tc_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < kEpiCols; c += 4) {
+                    for (int c = 0; c < 16; c += 4) {
                         float4 d4;
                         asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                                      : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
-                                     : "r"(dv + 4 * c));
+                                     : "r"(dv + 4 * (16 * hf + c)));
+                        float* yy = y + 16 * hf + c;
                         const float2 t0 = ffma2(fmul2(make_float2(v[c], v[c + 1]), make_float2(d4.x, d4.y)), s2,
-                                                make_float2(y[c], y[c + 1]));
+                                                make_float2(yy[0], yy[1]));
                         const float2 t1 = ffma2(fmul2(make_float2(v[c + 2], v[c + 3]), make_float2(d4.z, d4.w)), s2,
-                                                make_float2(y[c + 2], y[c + 3]));
-                        y[c] = t0.x;
-                        y[c + 1] = t0.y;
-                        y[c + 2] = t1.x;
-                        y[c + 3] = t1.y;
+                                                make_float2(yy[2], yy[3]));
+                        yy[0] = t0.x;
+                        yy[1] = t0.y;
+                        yy[2] = t1.x;
+                        yy[3] = t1.y;
                     }
                 }
                 QMM_TRACE(32, kb);
-                if (Q6 && ((kb & 7) == 7 || kb + 1 == nkb32)) {
-                    // end of the super-block: y += d * z in tensor memory, z = 0
-                    const uint32_t dk = kb >> 3;
-                    const uint32_t di = dk & (DR - 1);
-                    if (!wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (dk / DR) & 1, FLAG, a.st.err)) {
-                        ok = false;
-                        break;
-                    }
-                    float yv[kEpiCols];
-                    tc_ld32(ycol, yv);
-                    tc_wait_ld();
-                    const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
-#pragma unroll
-                    for (int c = 0; c < kEpiCols; c += 4) {
-                        float4 d4;
-                        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                     : "=f"(d4.x), "=f"(d4.y), "=f"(d4.z), "=f"(d4.w)
-                                     : "r"(dv + 4 * c));
-                        const float2 t0 = ffma2(make_float2(d4.x, d4.y), make_float2(y[c], y[c + 1]),
-                                                make_float2(yv[c], yv[c + 1]));
-                        const float2 t1 = ffma2(make_float2(d4.z, d4.w), make_float2(y[c + 2], y[c + 3]),
-                                                make_float2(yv[c + 2], yv[c + 3]));
-                        yv[c] = t0.x;
-                        yv[c + 1] = t0.y;
-                        yv[c + 2] = t1.x;
-                        yv[c + 3] = t1.y;
-                    }
-                    tc_st32(ycol, yv);
-                    tc_wait_st();
-#pragma unroll
-                    for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
-                }
             }
             if (!ok) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, static_cast<int>(q & 1)));
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) sxa[bi] = sxb[bi];
-        }
-        if (ok && Q6) {
-            // the running output, out of tensor memory (every lane: the load is warp-wide)
-            tc_ld32(ycol, y);
-            tc_wait_ld();
         }
         if (ok && m < a.M) {
             const int64_t nb0 = n0 + c0;
