@@ -312,6 +312,71 @@ def time_graph(torch, g, steps, device):
     return start.elapsed_time(end) / steps  # ms per replay
 
 
+def rotated(torch, W, target_bytes=384 << 20, lo=2, hi=64):
+    """Copies of W, enough that one pass over them streams more than the
+    129 MB L2 (between lo and hi copies): a call on copy i finds none of its
+    weights left in L2 by the calls before it."""
+    n = max(lo, min(hi, -(-target_bytes // W.numel())))
+    return W.reshape(1, -1).repeat(n, 1), n
+
+
+class MatvecRun:
+    """One public qmm_gemv call per rotated copy of one matrix, captured in one
+    CUDA graph; time_us() is the graph's time over the number of calls."""
+
+    def __init__(self, torch, qmm, fmt, W, x, N, K, device, copies=None):
+        self.torch, self.device = torch, device
+        if copies is None:
+            self.W, self.n = rotated(torch, W)
+        else:
+            self.W, self.n = W.reshape(1, -1).repeat(copies, 1), copies
+        self.y = torch.empty((x.shape[0], N), dtype=torch.float32, device=device)
+
+        def fn():
+            for i in range(self.n):
+                qmm.gemv(fmt, self.W[i], x, self.y, N, K)
+        self.g = capture(torch, fn, device)
+
+    def time_us(self, steps):
+        return 1e3 * time_graph(self.torch, self.g, steps, self.device) / self.n
+
+
+def per_matrix(torch, qmm, dec, device, steps):
+    """Per-matrix time of the decode set (single calls over rotated copies),
+    and the equivalent decode rate of a 32-layer 7B-shaped model built from
+    these matrices: a token streams 32 x (wq wk wo w1 w3 attn_v ffn_down)
+    plus output, so tok/s = B / (32 x layer time + output time); in the
+    bandwidth form, tok/s = eta x BW / bytes per token with eta x BW the
+    effective weight bandwidth those times give."""
+    rows, mats = [], {}
+    for (name, fmt, N, K, B, Wt, xt, yt) in dec.items:
+        if B != BATCHES[0]:
+            continue
+        mats[name] = (fmt, N, K, Wt)
+    us = {}
+    for B in BATCHES:
+        x_b = {it[0]: it[6] for it in dec.items if it[4] == B}
+        for name, (fmt, N, K, Wt) in mats.items():
+            run = MatvecRun(torch, qmm, FMT_CODE[fmt], Wt, x_b[name], N, K, device)
+            for _ in range(3):
+                run.g.replay()
+            t = run.time_us(max(5, steps // 2))
+            us[(name, B)] = t
+            wb = weight_bytes(fmt, N, K)
+            rows.append({"matrix": name, "format": fmt, "N": N, "K": K, "batch": B, "us": t,
+                         "gbps": wb / (t * 1e-6) / 1e9, "copies": run.n})
+            del run
+    layer = ("wq", "wk", "wo", "w1", "w3", "attn_v", "ffn_down")
+    tok = {}
+    for B in BATCHES:
+        t_tok = 32 * sum(us[(n, B)] for n in layer) + us[("output", B)]
+        b_tok = 32 * sum(weight_bytes(mats[n][0], mats[n][1], mats[n][2]) for n in layer) + weight_bytes(
+            *[mats["output"][i] for i in range(3)])
+        tok[str(B)] = {"tok_per_s": B / (t_tok * 1e-6), "us_per_token_step": t_tok,
+                       "weight_bytes_per_step": b_tok, "effective_gbps": b_tok / (t_tok * 1e-6) / 1e9}
+    return rows, tok
+
+
 # ------------------------------------------------------------------ CPU baseline
 
 def host_threads():
@@ -520,56 +585,147 @@ SWEEP_OUTPUT = ("output", "q6_K", 32000, 4096)
 
 def run_sweep(args):
     """The 32-layer prefill sweep: whole-sweep TOPS at M = 128, 512, 2048 with
-    the q6_K planes on and off, and the planes' device-memory delta."""
+    the q6_K planes on and off (each pass one CUDA graph of the 225 GEMM
+    calls, the two variants replayed alternately, L2 flushed before each
+    replay, SM clocks sampled throughout), the planes' device-memory delta, a
+    per-matrix plane on/off table with sampled outputs checked against the
+    oracle, and the oracle's own rate extrapolated to the whole sweep."""
     import torch
     import synth
     import __graft_entry__
     __graft_entry__.build()
     import block_quantized_weight_q6_gb300 as qmm
+    import oracle
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    mats = []  # (fmt code, N, K, W)
+    mats = []  # (name, fmt code, N, K, W)
     for layer in range(args.sweep_layers):
         for mid, (name, fmt, N, K) in enumerate(SWEEP_LAYER):
             W = synth.matrix_torch(FMT_CODE[fmt], synth.workload_seed(4, 16 * layer + mid), N, K, device)[0]
-            mats.append((FMT_CODE[fmt], N, K, W))
+            mats.append((name, FMT_CODE[fmt], N, K, W))
     name, fmt, N, K = SWEEP_OUTPUT
-    mats.append((FMT_CODE[fmt], N, K, synth.matrix_torch(FMT_CODE[fmt], synth.workload_seed(4, 15), N, K, device)[0]))
+    mats.append((name, FMT_CODE[fmt], N, K,
+                 synth.matrix_torch(FMT_CODE[fmt], synth.workload_seed(4, 15), N, K, device)[0]))
     torch.cuda.synchronize(device)
     # the planes, and the device memory they take
-    q6 = [(N, K, W) for f, N, K, W in mats if f == synth.Q6_K]
+    q6 = [(N, K, W) for _, f, N, K, W in mats if f == synth.Q6_K]
     free0, _ = torch.cuda.mem_get_info(device)
     planes = [qmm.plane_build(W, N, K) for N, K, W in q6]
     torch.cuda.synchronize(device)
     free1, _ = torch.cuda.mem_get_info(device)
+    plane_of = {id(W): p for (N, K, W), p in zip(q6, planes)}
     plane_bytes = sum(qmm.plane_bytes(N, K) for N, K, _ in q6)
-    ops_per_token = sum(2 * N * K for _, N, K, _ in mats)
+    ops_per_token = sum(2 * N * K for _, _, N, K, _ in mats)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=device)
+
+    def l2_flush():
+        flush.zero_()
+        flush_rd.sum()
+
+    def timed(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l2_flush()
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1)
+
     out = {"sweep": f"{args.sweep_layers} layers x (Q4_0 wq/wk/wo/w1/w3 + q6_K attn_v/ffn_down) + q6_K output",
            "data": "synthetic", "plane_bytes": plane_bytes,
-           "plane_mem_delta_bytes": int(free0 - free1), "results": {}}
-    for M in (128, 512, 2048):
-        xs = {K: torch.from_numpy(synth.normal_bf16(synth.workload_seed(4, 100 + K % 97 + M), (M, K)).view(np.int16)
-                                  ).to(device).view(torch.bfloat16) for K in (4096, 11008)}
-        Y = torch.empty((M, 32000), dtype=torch.float32, device=device)
-        res = {}
-        for variant in ("plane_on", "plane_off"):
-            pl = {id(W): p for (N, K, W), p in zip(q6, planes)} if variant == "plane_on" else {}
+           "plane_mem_delta_bytes": int(free0 - free1), "reps": args.sweep_reps,
+           "timing": "CUDA graph per (M, variant), variants replayed alternately, L2 flushed before "
+                     "each replay, median over reps", "results": {}, "per_matrix": []}
+    xs_host = {}
+    with ClockSampler(0) as clk:
+        for M in (128, 512, 2048):
+            xs = {}
+            for K in (4096, 11008):
+                xh = synth.normal_bf16(synth.workload_seed(4, 100 + K % 97 + M), (M, K))
+                xs_host[(M, K)] = xh
+                xs[K] = torch.from_numpy(xh.view(np.int16)).to(device).view(torch.bfloat16)
+            Y = torch.empty((M, 32000), dtype=torch.float32, device=device)
+            graphs = {}
+            for variant in ("plane_on", "plane_off"):
+                pl = plane_of if variant == "plane_on" else {}
 
-            def fn():
-                for f, N, K, W in mats:
-                    qmm.gemm(f, W, xs[K], Y.view(-1)[: M * N], M, N, K, pl.get(id(W)))
-            for _ in range(2):
-                fn()
-            torch.cuda.synchronize(device)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            fn()
-            e1.record()
-            torch.cuda.synchronize(device)
+                def fn(pl=pl):
+                    for _, f, N, K, W in mats:
+                        qmm.gemm(f, W, xs[K], Y.view(-1)[: M * N], M, N, K, pl.get(id(W)))
+                graphs[variant] = capture(torch, fn, device)
+            times = {v: [] for v in graphs}
+            for rep in range(args.sweep_reps + 1):
+                for v, g in graphs.items():
+                    t = timed(g)
+                    if rep > 0:
+                        times[v].append(t)
             qmm.sync_check()
-            ms = e0.elapsed_time(e1)
-            res[variant] = {"ms": ms, "tops": ops_per_token * M / (ms * 1e-3) / 1e12}
-        out["results"][str(M)] = res
+            res = {}
+            for v in graphs:
+                ms = statistics.median(times[v])
+                res[v] = {"ms": ms, "tops": ops_per_token * M / (ms * 1e-3) / 1e12}
+            out["results"][str(M)] = res
+            del graphs
+
+            # the q6_K matrices one at a time (layer 0's attn_v and ffn_down,
+            # and output), plane on and off, with sampled outputs checked
+            for name, f, N, K, W in [m for m in mats[:len(SWEEP_LAYER)] if m[1] == synth.Q6_K] + [mats[-1]]:
+                Ys = {v: torch.empty((M, N), dtype=torch.float32, device=device) for v in ("plane_on", "plane_off")}
+                gs = {v: capture(torch, lambda v=v: qmm.gemm(f, W, xs[K], Ys[v], M, N, K,
+                                                              plane_of[id(W)] if v == "plane_on" else None),
+                                 device) for v in Ys}
+                tt = {v: [] for v in gs}
+                for rep in range(args.sweep_reps + 1):
+                    for v, g in gs.items():
+                        t = timed(g)
+                        if rep > 0:
+                            tt[v].append(t)
+                row = {"matrix": name, "M": M, "N": N, "K": K}
+                for v in gs:
+                    ms = statistics.median(tt[v])
+                    row[v + "_ms"] = ms
+                    row[v + "_tops"] = 2 * M * N * K / (ms * 1e-3) / 1e12
+                row["bitwise_equal"] = bool(torch.equal(Ys["plane_on"].view(torch.int32),
+                                                        Ys["plane_off"].view(torch.int32)))
+                xq, sx = oracle.quantize_q8(xs_host[(M, K)])
+                rng = np.random.default_rng(M + N)
+                ms_, ns_ = rng.integers(0, M, 64), rng.integers(0, N, 64)
+                ref, absum = oracle.gemm_q8_pairs(f, W.cpu().numpy(), K, xq, sx, ms_, ns_)
+                row["max_err_over_bound"] = _worst(Ys["plane_on"].cpu().numpy()[ms_, ns_], ref, 1e-4 * absum + 1e-6)
+                out["per_matrix"].append(row)
+                del gs, Ys
+    out["clocks"] = clk.summary()
+
+    # the oracle's rate on sampled outputs of one layer's shapes (M = 128),
+    # extrapolated to the whole sweep at each M
+    threads = host_threads()
+    shapes = {}
+    for name, f, N, K, W in mats[:len(SWEEP_LAYER)] + [mats[-1]]:
+        shapes.setdefault((f, N, K), (name, W))
+    rates = {}
+    for (f, N, K), (name, W) in shapes.items():
+        Wh = W.cpu().numpy()
+        xq, sx = oracle.quantize_q8(xs_host[(128, K)])
+        rng = np.random.default_rng(N + K)
+
+        def one(i, Wh=Wh, xq=xq, sx=sx, f=f, K=K, N=N, rng_seed=N + K):
+            r = np.random.default_rng(rng_seed + i)
+            ms_, ns_ = r.integers(0, 128, 32), r.integers(0, N, 32)
+            oracle.gemm_q8_pairs(f, Wh, K, xq, sx, ms_, ns_)
+            return 32
+        done, t = _run_tasks(list(range(64 * threads)), one, 2.0, threads)
+        rates[(f, N, K)] = 2.0 * K * sum(done) / t
+    est = {}
+    for M in (128, 512, 2048):
+        sec = sum(2.0 * M * N * K / rates[(f, N, K)] for _, f, N, K, _ in mats)
+        est[str(M)] = {"seconds": sec, "tops": ops_per_token * M / sec / 1e12}
+    out["cpu_baseline"] = {"kind": "oracle", "cores": threads, "host_cores": os.cpu_count(),
+                           "extrapolated": True,
+                           "sample": "oracle q8 dot products of sampled outputs of each of one layer's "
+                                     "shapes and of output at M = 128 (2 s per shape), rate per shape "
+                                     "extrapolated to every matrix of the sweep",
+                           "per_M": est}
     for N, K, W in q6:
         qmm.plane_release(W)
     print(json.dumps(out))
@@ -623,6 +779,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="the 32-layer prefill sweep (plane on/off, M = 128, 512, 2048)")
     ap.add_argument("--sweep-layers", type=int, default=32)
+    ap.add_argument("--sweep-reps", type=int, default=5)
     args = ap.parse_args()
     if args.profile:
         run_profile(args)
@@ -749,6 +906,30 @@ def main():
     ms_e2e = max_over_ranks(world, t0.elapsed_time(t1) / e2e_steps, device)
     e2e_gbs = dec.weight_bytes / (ms_e2e * 1e-3) / 1e9 * world
 
+    # config 0: the single q6_K 1024 x 4096 batch-1 matvec, fp32 activations,
+    # over 64 rotated weight copies in one CUDA graph; all 1024 outputs
+    # against the oracle
+    import synth
+    c0_W = torch.from_numpy(synth.q6k_matrix(synth.workload_seed(0, 0), 1024, 4096)).to(device)
+    c0_x = torch.from_numpy(synth.normal_f32(synth.workload_seed(0, 1), (1, 4096))).to(device)
+    c0 = MatvecRun(torch, qmm, qmm.Q6_K, c0_W, c0_x, 1024, 4096, device, copies=64)
+    for _ in range(args.warmup):
+        c0.g.replay()
+    c0_us = max_over_ranks(world, c0.time_us(args.steps), device)
+    c0_parity = None
+    if rank == 0:
+        import oracle
+        ref, absum = oracle.gemv_float(qmm.Q6_K, c0_W.cpu().numpy(), c0_x.cpu().numpy(), 1024, 4096)
+        c0_parity = {"outputs": 1024, "max_err_over_bound": _worst(c0.y.cpu().numpy(), ref, 1e-4 * absum + 1e-6)}
+        c0_parity["ok"] = bool(c0_parity["max_err_over_bound"] <= 1.0)
+    c0_bytes = weight_bytes("q6_K", 1024, 4096)
+    config0 = {"workload": "q6_K 1024x4096, batch 1, fp32 x (64 rotated weight copies in one graph)",
+               "us": c0_us, "gbps": c0_bytes / (c0_us * 1e-6) / 1e9 * world, "parity": c0_parity}
+    del c0
+
+    # per-matrix times of the decode set and the equivalent tok/s
+    pm_rows, pm_tok = per_matrix(torch, qmm, dec, device, args.steps)
+
     # roofline of the part that takes the most time in the step
     hbm = pk["hbm_gbs"]
     tc_peak = pk["bf16_tflops"]  # fp16 operands run at the bf16 dense rate
@@ -809,6 +990,9 @@ def main():
                      "unit": "TOPS (2*M*N*K / time, incl. activation quantize)",
                      "plane_vs_in_kernel_bitwise_equal": gem_identical,
                      "plane_bytes": gem.N * gem.K, "plane_mem_delta_bytes": gem.plane_delta},
+            "config0": config0,
+            "per_matrix": pm_rows,
+            "equivalent_tok_s": pm_tok,
             "moe": {"t1_gbps": moe_gbs["moe_t1"], "t16_gbps": moe_gbs["moe_t16"],
                     "t16_distinct_experts": moe16.distinct, "t1_bytes": moe1.bytes,
                     "t16_bytes": moe16.bytes},
