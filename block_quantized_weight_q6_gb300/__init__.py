@@ -25,6 +25,7 @@ LIVE = {
     "gemm_exp_plane": 5, "gemm_in_kernel": 6, "gemm_exp_off": 7, "gemm_fallback": 8,
     "gemm_q4_0": 9, "route": 10, "moe_gate_up": 11, "moe_down": 12, "moe_combine": 13,
     "x_tile": 14, "moe_plan": 15, "moe_gather": 16, "gemv_mv1": 17, "gemv_mv8": 18, "moe_silu": 19,
+    "gemm_split_reduce": 20,
 }
 LIVE_COUNT = 24
 

@@ -829,7 +829,8 @@ int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, in
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
     const size_t a16b = round_up(gemm_a16_bytes(M, K), 256);
-    const size_t need = a16b + round_up(static_cast<size_t>(M) * (K / 32) * 4, 256);
+    const size_t xsb = round_up(static_cast<size_t>(M) * (K / 32) * 4, 256);
+    const size_t need = a16b + xsb + round_up(gemm_part_bytes(M, N, K), 256);
     if (need > t_ws_bytes || !t_ws)
         return fail(QMM_ENOWORKSPACE, "qmm_gemm needs %zu bytes of workspace, %zu set", need,
                     t_ws_bytes);
@@ -838,8 +839,9 @@ int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, in
     float* xs = reinterpret_cast<float*>(ws + a16b);
     cudaError_t e = quantize_q8_launch(X, bf16, M, K, nullptr, xs, a16, t_stream, d->st);
     if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+    float* part = gemm_part_bytes(M, N, K) ? reinterpret_cast<float*>(ws + a16b + xsb) : nullptr;
     e = gemm_launch(wf, exp_plane != nullptr, static_cast<const uint8_t*>(W), exp_plane, a16, xs, Y,
-                    M, N, K, t_stream, d->st, label);
+                    M, N, K, t_stream, d->st, label, part);
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
     return QMM_OK;
 }
@@ -917,7 +919,8 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
     size_t gemm = 0;
     if (wf != QMM_Q8_0)
         gemm = round_up(gemm_a16_bytes(M_or_B, K), 256) +
-               round_up(static_cast<size_t>(M_or_B) * (K / 32) * 4, 256);
+               round_up(static_cast<size_t>(M_or_B) * (K / 32) * 4, 256) +
+               round_up(gemm_part_bytes(M_or_B, N, K), 256);
     if (M_or_B > 16) return gemm;
     DevInfo* d;
     if (dev_info(&d)) return gemm;

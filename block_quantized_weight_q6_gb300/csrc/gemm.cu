@@ -42,7 +42,8 @@
 //   warps 12-27 epilogue: tcgen05.ld of the accumulators, scaling, output
 //   warp 3      idle
 // Registers are moved between warpgroups (setmaxnreg): the producers' and
-// the MMA's warpgroup gives up most of its share to the epilogue's.
+// the MMA's warpgroup and the converters give up part of their share to the
+// epilogue's.
 // Handing work between warps through an mbarrier costs a few hundred cycles
 // of a warp's time, so the epilogue and the MMA meet once per stage of KP
 // blocks rather than once per block.
@@ -75,10 +76,10 @@ constexpr int kConv0 = 4, kConvWarps = 8;   // converter warps (warpgroups 1, 2)
 constexpr int kConvRows = 8 / kConvWarps;   // rows 8 g + j a converter lane takes per pass (j = kConvRows cw + jj)
 constexpr int kEpi0 = 12, kEpiWarps = 16;   // epilogue warps (warpgroups 3 .. 6)
 constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
-// registers per thread after the reallocation: 4 warps x 40 + 8 x 72 + 16 x 80 = 2016 x 32, the
-// 28 x 72 x 32 the block is launched with (an increase beyond that pool would never complete)
-constexpr int kRegsLow = 40, kRegsEpi = 80;
-static_assert(4 * kRegsLow + kConvWarps * 72 + kEpiWarps * kRegsEpi <= kThreads / 32 * 72, "register pool");
+// registers per thread after the reallocation: 4 warps x 48 + 8 x 64 + 16 x 80 = 1984 x 32, within
+// the 28 x 72 x 32 the block is launched with (an increase beyond that pool would never complete)
+constexpr int kRegsLow = 48, kRegsConv = 64, kRegsEpi = 80;
+static_assert(4 * kRegsLow + kConvWarps * kRegsConv + kEpiWarps * kRegsEpi <= kThreads / 32 * 72, "register pool");
 static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
 constexpr int kTmemCols = 512;    // NACC * BN accumulators
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
@@ -363,6 +364,10 @@ struct GemmArgs {
     int64_t total_bytes;   // bytes of W
     int64_t rowbytes;      // bytes per row of W
     int64_t n8;            // rows of W reached through the tensor map: 8 * floor(N / 8)
+    int64_t kb_split;      // K blocks per split (a multiple of 8): CTA z takes blocks z * kb_split ..
+    float* part;           // split partial outputs, split z at part + z * pstride as [M][N]; or
+                           // null: the CTA writes Y
+    int64_t pstride;       // floats per split: M * N rounded up to 64 (keeps 16-byte alignment)
     DevState st;
     int live_slot;
 };
@@ -381,9 +386,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t BARS = S + L.bars;
     const uint32_t FLAG = S + L.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nkb = a.K / 32;
-    const uint32_t nkb32 = static_cast<uint32_t>(nkb);
-    const int64_t nsc = (a.K + 255) / 256;  // 256-column super-chunks
+    const int64_t nkb = a.K / 32;  // K blocks of a row (the operands' strides)
+    // this CTA's K range: blocks kbg .. kbg + nkb32 - 1 (local index kb = 0 ..)
+    const int64_t kbg = static_cast<int64_t>(blockIdx.z) * a.kb_split;
+    const uint32_t nkb32 = static_cast<uint32_t>(min(a.kb_split, nkb - kbg));
+    const int64_t nsc = (nkb32 + 7) / 8;      // 256-column super-chunks of the range
+    const int64_t sc0 = kbg / 8;              // the range's first super-chunk
     const int64_t mt = blockIdx.y, nt = blockIdx.x;
     const int64_t n0 = nt * BN;
 
@@ -428,8 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
         // raw stage of 256-column chunk sc into slot sc % NR
-        auto issue_raw = [&](uint32_t sc) {
-            const int r = static_cast<int>(sc % NR);
+        auto issue_raw = [&](uint32_t scl) {
+            const int r = static_cast<int>(scl % NR);
+            const int64_t sc = sc0 + scl;  // the chunk within the row
             const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
             const uint32_t bar = bar_raw_full(BARS, r);
             uint32_t bytes = 0;
@@ -506,11 +515,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t pk = kb0 + kPrefetch * KP;
                     if (q == 0)
                         for (uint32_t k = 0; k < pk && k < nkb32; k += KP)
-                            prefetch_l2(a.a16 + (mt * nkb + k) * (BM * 32), (nkb32 - k < KP ? nkb32 - k : KP) * kATile);
+                            prefetch_l2(a.a16 + (mt * nkb + kbg + k) * (BM * 32),
+                                        (nkb32 - k < KP ? nkb32 - k : KP) * kATile);
                     if (pk < nkb32)
-                        prefetch_l2(a.a16 + (mt * nkb + pk) * (BM * 32), (nkb32 - pk < KP ? nkb32 - pk : KP) * kATile);
+                        prefetch_l2(a.a16 + (mt * nkb + kbg + pk) * (BM * 32),
+                                    (nkb32 - pk < KP ? nkb32 - pk : KP) * kATile);
                     mbar_arrive_expect_tx(bar_full(BARS, static_cast<int>(st)), nbk * kATile);
-                    bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kb0) * (BM * 32), nbk * kATile,
+                    bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kbg + kb0) * (BM * 32), nbk * kATile,
                              bar_full(BARS, static_cast<int>(st)));
                 }
                 __syncwarp();
@@ -556,6 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     } else if (warp < kEpi0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConv));
         // ------------------------------------------------------------ converters
         // One stage (two K blocks) per pass: one wait, one proxy fence and one
         // arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
@@ -594,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
             const uint32_t j0 = kb0 & 7;
             const uint32_t raw0 = S + L.raw + r * L.rawslot;
-            const uint32_t ls = Q6 ? 2u * sc : 0u;
+            const uint32_t ls = Q6 ? 2u * static_cast<uint32_t>(sc0 + sc) : 0u;  // the global chunk's shift
             QMM_TRACE(20, kb0);
             if (j0 == 0 && !wait_or_abort(bar_raw_full(BARS, static_cast<int>(r)), rph, FLAG, a.st.err)) break;
             QMM_TRACE(21, kb0);
@@ -770,7 +782,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
         float sxa[KP], sxb[KP];
-        const float* xrow = a.xs + (m < a.M ? m : 0) * nkb;
+        const float* xrow = a.xs + (m < a.M ? m : 0) * nkb + kbg;
         auto load_sx = [&](uint32_t q, float (&o)[KP]) {
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) {
@@ -834,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok && m < a.M) {
             const int64_t nb0 = n0 + c0;
-            float* out = a.Y + m * a.N + nb0;
+            float* out = (a.part ? a.part + static_cast<int64_t>(blockIdx.z) * a.pstride : a.Y) + m * a.N + nb0;
             if (nb0 + kEpiCols <= a.N && (a.N & 3) == 0) {
 #pragma unroll
                 for (int c = 0; c < kEpiCols; c += 4)
@@ -870,9 +882,85 @@ size_t gemm_a16_bytes(int64_t M, int64_t K) {
     return static_cast<size_t>((M + BM - 1) / BM * BM) * static_cast<size_t>(K) * 2;
 }
 
+// Y = the sum of the split partials, in split order (bitwise reproducible).
+// Split z's partial starts at part + z * pstride, pstride a multiple of 4, so
+// that the 16-byte loads of every split stay aligned (Y is 16-byte aligned).
+__global__ void gemm_split_reduce_kernel(const float* __restrict__ part, float* __restrict__ Y, int64_t count,
+                                         int64_t pstride, int splits, DevState st) {
+    grid_dependency_wait();  // the GEMM's partials
+    grid_launch_dependents();
+    live_bump(st, 20);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 4;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4; i < count; i += stride) {
+        if (i + 4 <= count) {
+            float4 acc = *reinterpret_cast<const float4*>(part + i);
+            for (int z = 1; z < splits; ++z) {
+                const float4 v = *reinterpret_cast<const float4*>(part + z * pstride + i);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
+            *reinterpret_cast<float4*>(Y + i) = acc;
+        } else {
+            for (int64_t j = i; j < count; ++j) {
+                float acc = part[j];
+                for (int z = 1; z < splits; ++z) acc += part[z * pstride + j];
+                Y[j] = acc;
+            }
+        }
+    }
+}
+
+namespace {
+
+int sm_count() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cache[dev] = n;
+    return n;
+}
+
+// K blocks per split: a grid of fewer tiles than SMs splits K so that tiles
+// x splits fills the SMs, keeping at least 4 super-chunks (32 blocks) per
+// split; a multiple of 8 blocks, so that splits start on super-chunks.
+int64_t gemm_kb_split(int64_t M, int64_t N, int64_t K) {
+    const int64_t nkb = K / 32;
+    const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+    int64_t S = sm_count() / (tiles > 0 ? tiles : 1);
+    if (S > nkb / 32) S = nkb / 32;
+    if (S < 2) return nkb;
+    const int64_t per = (nkb + S - 1) / S;
+    return (per + 7) / 8 * 8;
+}
+
+}  // namespace
+
+int gemm_splits(int64_t M, int64_t N, int64_t K) {
+    const int64_t nkb = K / 32;
+    const int64_t kbs = gemm_kb_split(M, N, K);
+    return static_cast<int>((nkb + kbs - 1) / kbs);
+}
+
+namespace {
+int64_t part_stride(int64_t M, int64_t N) { return (M * N + 63) / 64 * 64; }
+}  // namespace
+
+size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K) {
+    const int S = gemm_splits(M, N, K);
+    return S > 1 ? static_cast<size_t>(S) * static_cast<size_t>(part_stride(M, N)) * 4 : 0;
+}
+
 cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, DevState st, int live_slot) {
+                        int64_t K, cudaStream_t s, DevState st, int live_slot, float* part) {
     GemmKernel k = pick_gemm(fmt, exp);
     if (!k) return cudaErrorInvalidValue;
     const SmemLayout L = smem_layout(fmt, exp);
@@ -905,7 +993,14 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
     a.n8 = N / 8 * 8;
     a.st = st;
     a.live_slot = live_slot;
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
+    a.kb_split = gemm_kb_split(M, N, K);
+    const int splits = gemm_splits(M, N, K);
+    if (splits > 1 && !part) return cudaErrorInvalidValue;
+    a.part = splits > 1 ? part : nullptr;
+    a.pstride = part_stride(M, N);
+    if (a.part && (reinterpret_cast<uintptr_t>(part) & 15u)) return cudaErrorMisalignedAddress;
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM),
+                    static_cast<unsigned>(splits));
     // q6_K / Q4_0 rows: W as [N / 8][8 * rowbytes] bytes of 16-bit elements
     // (the pitch of 8 rows is a multiple of 16 bytes for both formats); a box
     // is one row slot wide and 16 groups of 8 rows high
@@ -938,6 +1033,14 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
             return cudaErrorInvalidValue;
     }
     e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a, wmap, pmap);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess || splits == 1) return e;
+    const int64_t count = M * N;
+    int64_t blocks = (count / 4 + 255) / 256;
+    if (blocks > 4 * sm_count()) blocks = 4 * sm_count();
+    if (blocks < 1) blocks = 1;
+    e = launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                   static_cast<const float*>(part), Y, count, a.pstride, splits, st);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -241,10 +241,15 @@ cudaError_t quantize_q8_launch(const void* x, int x_bf16, int64_t rows, int64_t 
 // ---------------------------------------------------------------- GEMM
 // bytes of the fp16 A-operand tiles for M x K activations (M rounded up to 128)
 size_t gemm_a16_bytes(int64_t M, int64_t K);
-// fmt FMT_Q6_K (exp: plane variant) or FMT_Q4_0 (exp false)
+// K splits of an M x N x K GEMM (1 when its tiles fill the SMs), and the
+// bytes of the split partials gemm_launch then needs (0 for one split)
+int gemm_splits(int64_t M, int64_t N, int64_t K);
+size_t gemm_part_bytes(int64_t M, int64_t N, int64_t K);
+// fmt FMT_Q6_K (exp: plane variant) or FMT_Q4_0 (exp false); part: device
+// workspace of gemm_part_bytes(M, N, K) bytes (null when that is 0)
 cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane,
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
-                        int64_t K, cudaStream_t s, DevState st, int live_slot);
+                        int64_t K, cudaStream_t s, DevState st, int live_slot, float* part);
 
 // ---------------------------------------------------------------- MoE
 constexpr int kMoeMaxExperts = 1024;

@@ -103,6 +103,8 @@ enum {
                                          warp-level MMA (fp16 or bf16)       */
     QMM_LIVE_MOE_SILU = 19,           /* silu(g) * u laid out for the expert
                                          matvecs on the warp-level MMA       */
+    QMM_LIVE_GEMM_SPLIT_REDUCE = 20,  /* sum of a GEMM's K-split partials
+                                         (grids with fewer tiles than SMs)   */
     QMM_LIVE_COUNT = 24
 };
 

@@ -304,3 +304,41 @@ def test_sweep_shapes_vs_oracle(name, fmt_name, N, K, mid, M):
     xq, s = oracle.quantize_q8(X)
     ref, absum = oracle.gemm_q8_pairs(fmt, W, K, xq, s, ms, ns)
     assert_within(Y2[ms, ns], ref, absum, f"sweep {name} {N}x{K} M={M}")
+
+
+@pytest.mark.parametrize("fmt_name,M,N,K", [("q6_K", 128, 4096, 4096), ("Q4_0", 77, 130, 2048),
+                                            ("q6_K", 200, 520, 8192)])
+def test_split_k_grid_vs_oracle_deterministic(fmt_name, M, N, K):
+    """A grid of fewer tiles than SMs splits K over CTAs and sums the partials
+    in a fixed order: the sum-of-partials launch runs, a second call is
+    bitwise identical, the q6_K plane and in-kernel variants agree bitwise,
+    and sampled outputs (with the corners) are within the bound."""
+    fmt = {"Q4_0": qmm.Q4_0, "q6_K": qmm.Q6_K}[fmt_name]
+    Wt = synth.matrix_torch(fmt, synth.workload_seed(7, M % 13), N, K, "cuda")[0]
+    X = synth.normal_bf16(synth.workload_seed(7, 3 + K % 11), (M, K))
+    qmm.liveness_reset()
+    Y = run_gemm(fmt, None, X, N, K, Wt=Wt)
+    assert qmm.liveness()["gemm_split_reduce"] == 1
+    Y2 = run_gemm(fmt, None, X, N, K, Wt=Wt)
+    assert np.array_equal(Y.view(np.uint32), Y2.view(np.uint32))
+    if fmt == qmm.Q6_K:
+        plane = qmm.plane_build(Wt, N, K)
+        Y3 = run_gemm(fmt, None, X, N, K, plane=plane, Wt=Wt)
+        qmm.plane_release(Wt)
+        assert np.array_equal(Y.view(np.uint32), Y3.view(np.uint32))
+    rng = np.random.default_rng(M * N)
+    ms = np.concatenate([rng.integers(0, M, 252), [0, M - 1, 0, M - 1]])
+    ns = np.concatenate([rng.integers(0, N, 252), [0, N - 1, N - 1, 0]])
+    xq, s = oracle.quantize_q8(X)
+    ref, absum = oracle.gemm_q8_pairs(fmt, Wt.cpu().numpy(), K, xq, s, ms, ns)
+    assert_within(Y[ms, ns], ref, absum, f"split-K {fmt_name} {M}x{N}x{K}")
+
+
+def test_full_grid_does_not_split():
+    """M = 512 against N = 4096 makes 128 tiles: one pass over K, no partials."""
+    M, N, K = 512, 4096, 2048
+    Wt = synth.matrix_torch(qmm.Q6_K, synth.workload_seed(7, 9), N, K, "cuda")[0]
+    X = synth.normal_bf16(synth.workload_seed(7, 10), (M, K))
+    qmm.liveness_reset()
+    run_gemm(qmm.Q6_K, None, X, N, K, Wt=Wt)
+    assert qmm.liveness()["gemm_split_reduce"] == 0
