@@ -42,8 +42,7 @@
 //   warps 12-27 epilogue: tcgen05.ld of the accumulators, scaling, output
 //   warp 3      idle
 // Registers are moved between warpgroups (setmaxnreg): the producers' and
-// the MMA's warpgroup and the converters give up part of their share to the
-// epilogue's.
+// the MMA's warpgroup gives up most of its share to the epilogue's.
 // Handing work between warps through an mbarrier costs a few hundred cycles
 // of a warp's time, so the epilogue and the MMA meet once per stage of KP
 // blocks rather than once per block.
@@ -76,10 +75,25 @@ constexpr int kConv0 = 4, kConvWarps = 8;   // converter warps (warpgroups 1, 2)
 constexpr int kConvRows = 8 / kConvWarps;   // rows 8 g + j a converter lane takes per pass (j = kConvRows cw + jj)
 constexpr int kEpi0 = 12, kEpiWarps = 16;   // epilogue warps (warpgroups 3 .. 6)
 constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
-// registers per thread after the reallocation: 4 warps x 48 + 8 x 64 + 16 x 80 = 1984 x 32, within
-// the 28 x 72 x 32 the block is launched with (an increase beyond that pool would never complete)
-constexpr int kRegsLow = 48, kRegsConv = 64, kRegsEpi = 80;
-static_assert(4 * kRegsLow + kConvWarps * kRegsConv + kEpiWarps * kRegsEpi <= kThreads / 32 * 72, "register pool");
+// registers per thread after the reallocation: 4 warps x 40 + 8 x 72 + 16 x 80 = 2016 x 32, or 4 x 48 +
+// 8 x 64 + 16 x 80 = 1984 x 32, within the 28 x 72 x 32 the block is launched with (an increase
+// beyond that pool would never complete)
+// The split depends on the variant: the in-kernel q6_K expansion wants the
+// converters' 72, the others fit them in 64 and give the producers 48.
+struct RegSplit {
+    int low, conv, epi;
+};
+__host__ __device__ constexpr RegSplit reg_split(int fmt, bool exp) {
+    return (fmt == FMT_Q6_K && !exp) ? RegSplit{40, 72, 80} : RegSplit{48, 64, 80};
+}
+static_assert(4 * reg_split(FMT_Q6_K, false).low + kConvWarps * reg_split(FMT_Q6_K, false).conv +
+                      kEpiWarps * reg_split(FMT_Q6_K, false).epi <=
+                  kThreads / 32 * 72,
+              "register pool");
+static_assert(4 * reg_split(FMT_Q6_K, true).low + kConvWarps * reg_split(FMT_Q6_K, true).conv +
+                      kEpiWarps * reg_split(FMT_Q6_K, true).epi <=
+                  kThreads / 32 * 72,
+              "register pool");
 static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
 constexpr int kTmemCols = 512;    // NACC * BN accumulators
 constexpr int kATile = BM * 32 * 2;   // bytes of one A stage
@@ -372,6 +386,31 @@ struct GemmArgs {
     int live_slot;
 };
 
+// The up to 7 rows of W past its last whole group of 8 rows (rows n8 ..
+// N - 1) that fall in the tile at n0: lane j < 8 takes row n8 + j, the
+// segment of len bytes at koff, into dst + j * rs. Pass 0 stores the bytes
+// past the last 16-byte boundary of W with plain loads and returns the bytes
+// of the lane's 1-D bulk copy (from the 16-byte boundary at or below the
+// segment); pass 1 issues that copy on bar. Out of line: only the last tile
+// of a matrix with N % 8 != 0 runs it, and the producers' registers are few.
+__device__ __noinline__ uint32_t raw_tail_rows(const uint8_t* W, int64_t N, int64_t n8, int64_t rowbytes,
+                                               int64_t total_bytes, int lane, int64_t n0, int64_t koff, int64_t len,
+                                               uint32_t dst, uint32_t rs, uint32_t bar, int pass) {
+    const int64_t ng = n8 + lane;
+    if (lane >= 8 || ng >= N || ng < n0 || ng >= n0 + BN) return 0;
+    const int64_t tb16 = total_bytes & ~static_cast<int64_t>(15);
+    const int64_t st = ng * rowbytes + koff;
+    const int64_t s16 = st & ~static_cast<int64_t>(15);
+    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
+    const uint32_t d = dst + static_cast<uint32_t>(lane) * rs;
+    if (pass == 0) {
+        for (int64_t q = max(e16, s16); q < st + len; ++q) sts_u8(d + static_cast<uint32_t>(q - s16), W[q]);
+        return e16 > s16 ? static_cast<uint32_t>(e16 - s16) : 0u;
+    }
+    if (e16 > s16) bulk_g2s(d, W + s16, static_cast<uint32_t>(e16 - s16), bar);
+    return 0;
+}
+
 template <int FMT, bool EXP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap wmap,
@@ -431,10 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first warpgroup (producers, MMA issue, one idle warp) gives up most of
     // its share, the epilogue's two warpgroups take it.
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).low));
     if (warp == 0 || warp == kRawWarp) {
         // ------------------------------------------------------------ producers
-        const int64_t tb16 = a.total_bytes & ~static_cast<int64_t>(15);
         // raw stage of 256-column chunk sc into slot sc % NR
         auto issue_raw = [&](uint32_t scl) {
             const int r = static_cast<int>(scl % NR);
@@ -452,24 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t len = EXP ? 18 : (Q6 ? 210 : min(static_cast<int64_t>(8), a.nb - sc * 8) * 18);
             const uint32_t rw0 = dst0 + RW;
             const bool boxes = n0 < a.n8;
-            int64_t cs = 0, ce = 0;
-            int tr = -1;
-            {
-                const int64_t ng = a.n8 + lane;
-                if (lane < 8 && ng < a.N && ng >= n0 && ng < n0 + BN) {
-                    tr = lane;
-                    const int64_t st = ng * a.rowbytes + koff;
-                    const int64_t s16 = st & ~static_cast<int64_t>(15);
-                    const int64_t e16 = min((st + len + 15) & ~static_cast<int64_t>(15), tb16);
-                    if (e16 > s16) {
-                        cs = s16;
-                        ce = e16;
-                        bytes = static_cast<uint32_t>(e16 - s16);
-                    }
-                    for (int64_t q = max(e16, s16); q < st + len; ++q)
-                        sts_u8(rw0 + 8u * 16u * RS + tr * RS + static_cast<uint32_t>(q - s16), a.W[q]);
-                }
-            }
+            // the tile holds rows past W's last whole group of 8 (last tile only)
+            const bool tail = a.n8 < a.N && n0 + BN > a.n8;
+            if (tail)
+                bytes = raw_tail_rows(a.W, a.N, a.n8, a.rowbytes, a.total_bytes, lane, n0, koff, len,
+                                      rw0 + 8u * 16u * RS, RS, bar, 0);
             fence_proxy_async_smem();
             bytes = __reduce_add_sync(0xffffffffu, bytes);
             if (lane == 0)
@@ -483,8 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (EXP && lane < 16)
                 tma_load_2d(dst0 + lane * (BN * 16u), &pmap, static_cast<int>(sc * 256 + 16 * lane),
                             static_cast<int>(n0), bar);
-            if (ce > cs)
-                bulk_g2s(rw0 + 8u * 16u * RS + tr * RS, a.W + cs, static_cast<uint32_t>(ce - cs), bar);
+            if (tail)
+                (void)raw_tail_rows(a.W, a.N, a.n8, a.rowbytes, a.total_bytes, lane, n0, koff, len,
+                                    rw0 + 8u * 16u * RS, RS, bar, 1);
         };
         if (warp == kRawWarp) {
             uint32_t r = 0, eph = 1;  // raw slot; parity of its release ((sc / NR) - 1) & 1
@@ -502,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t sc = nsc > NR ? nsc - NR : 0; sc < nsc; ++sc)
                 (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(sc % NR)), (sc / NR) & 1, FLAG, a.st.err);
         } else {
+            const uint16_t* a16t = a.a16 + (mt * nkb + kbg) * (BM * 32);  // this CTA's first A tile
             uint32_t st = 0, eph = 1;  // stage; parity of its release ((q / NS) - 1) & 1
             for (uint32_t q = 0, kb0 = 0; kb0 < nkb32; ++q, kb0 += KP) {
                 // the A tiles of blocks KP q .. (consecutive in the pre-tiled operand)
@@ -515,13 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t pk = kb0 + kPrefetch * KP;
                     if (q == 0)
                         for (uint32_t k = 0; k < pk && k < nkb32; k += KP)
-                            prefetch_l2(a.a16 + (mt * nkb + kbg + k) * (BM * 32),
+                            prefetch_l2(a16t + static_cast<size_t>(k) * (BM * 32),
                                         (nkb32 - k < KP ? nkb32 - k : KP) * kATile);
                     if (pk < nkb32)
-                        prefetch_l2(a.a16 + (mt * nkb + kbg + pk) * (BM * 32),
+                        prefetch_l2(a16t + static_cast<size_t>(pk) * (BM * 32),
                                     (nkb32 - pk < KP ? nkb32 - pk : KP) * kATile);
                     mbar_arrive_expect_tx(bar_full(BARS, static_cast<int>(st)), nbk * kATile);
-                    bulk_g2s(S + L.a + st * kAStage, a.a16 + (mt * nkb + kbg + kb0) * (BM * 32), nbk * kATile,
+                    bulk_g2s(S + L.a + st * kAStage, a16t + static_cast<size_t>(kb0) * (BM * 32), nbk * kATile,
                              bar_full(BARS, static_cast<int>(st)));
                 }
                 __syncwarp();
@@ -567,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     } else if (warp < kEpi0) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsConv));
+        if constexpr (reg_split(FMT, EXP).conv != 72)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).conv));
         // ------------------------------------------------------------ converters
         // One stage (two K blocks) per pass: one wait, one proxy fence and one
         // arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
@@ -765,7 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).epi));
         // ------------------------------------------------------------ epilogue
         // One wait per stage of KP blocks (the MMA signals a stage once), then
         // per K block b: I_b from its accumulator buffer in two 16-column
