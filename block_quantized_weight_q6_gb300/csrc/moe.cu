@@ -91,16 +91,60 @@ __global__ void __launch_bounds__(1024) moe_plan_kernel(const MoeArgs a) {
         if (e >= 0) atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int so = 0, to = 0;
-        for (int e = 0; e < a.E; ++e) {
-            off[e] = so;
-            toff[e] = to;
-            so += cnt[e];
-            to += (cnt[e] + a.task_nb - 1) / a.task_nb;
+    // exclusive prefix sums over the experts of the slot counts (off) and of
+    // the task counts (toff), a block-wide scan per chunk of blockDim.x
+    // experts with the running totals carried between chunks
+    __shared__ int wsum[2][32];
+    __shared__ int carry[2];
+    if (threadIdx.x == 0) carry[0] = carry[1] = 0;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+    for (int e0 = 0; e0 < a.E; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        const int c = e < a.E ? cnt[e] : 0;
+        const int t = (c + a.task_nb - 1) / a.task_nb;
+        int ic = c, it = t;  // inclusive scans within the warp
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vc = __shfl_up_sync(0xffffffffu, ic, o), vt = __shfl_up_sync(0xffffffffu, it, o);
+            if (lane >= o) {
+                ic += vc;
+                it += vt;
+            }
         }
-        *a.n_tasks = to;
+        __syncthreads();  // carry[] of the previous chunk is final, wsum[] is free
+        if (lane == 31) {
+            wsum[0][wid] = ic;
+            wsum[1][wid] = it;
+        }
+        __syncthreads();
+        if (wid == 0) {
+            int sc = lane < nw ? wsum[0][lane] : 0, st = lane < nw ? wsum[1][lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int vc = __shfl_up_sync(0xffffffffu, sc, o), vt = __shfl_up_sync(0xffffffffu, st, o);
+                if (lane >= o) {
+                    sc += vc;
+                    st += vt;
+                }
+            }
+            if (lane < nw) {  // exclusive warp offsets
+                wsum[0][lane] = sc - wsum[0][lane];
+                wsum[1][lane] = st - wsum[1][lane];
+            }
+        }
+        __syncthreads();
+        if (e < a.E) {
+            off[e] = carry[0] + wsum[0][wid] + ic - c;
+            toff[e] = carry[1] + wsum[1][wid] + it - t;
+        }
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) {  // the chunk's totals
+            carry[0] += wsum[0][wid] + ic;
+            carry[1] += wsum[1][wid] + it;
+        }
     }
+    __syncthreads();
+    if (threadIdx.x == 0) *a.n_tasks = carry[1];
     __syncthreads();
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int e = eidx[s];
@@ -346,14 +390,20 @@ __global__ void route_topk_softmax_kernel(const float* __restrict__ logits, int 
     unsigned taken = 0;  // bit i: expert lane + 32 i already chosen
     float sel_v[32];
     int sel_i[32];
+    float lv[kPer];  // the lane's logits, read once
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        lv[i] = e < E ? l[e] : -INFINITY;
+    }
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bi = 0x7fffffff;
-#pragma unroll 4
+#pragma unroll
         for (int i = 0; i < kPer; ++i) {
             const int e = lane + 32 * i;
             if (e >= E || ((taken >> i) & 1u)) continue;
-            const float v = l[e];
+            const float v = lv[i];
             if (v > bv || (v == bv && e < bi)) {
                 bv = v;
                 bi = e;
