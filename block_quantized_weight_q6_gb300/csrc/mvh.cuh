@@ -40,7 +40,7 @@
 // super-block and its lead cover, and 2 more), so the 128-bit loads of one
 // load phase (rows 2k and 2k + 1, lanes c = 0..3 reading pieces c + s) hit 32
 // different banks; Q4_0 / Q8_0 one box 144 bytes wide (their stage, lead
-// included), read with 32-bit loads at a row base plus a constant. Box
+// included), read with 32- and 64-bit loads at a row base plus a constant. Box
 // destinations are 128-byte aligned.
 //
 // Each warp streams its own items through a private ring of NS stages (an
@@ -107,6 +107,9 @@ __device__ __forceinline__ uint32_t h_pair23(uint32_t w) { return __byte_perm(w,
 constexpr uint32_t kH2M1032 = 0xE408E408u;  // fp16 pair (-1032, -1032): (1024 + q) - 1032 = q - 8
 constexpr uint32_t kH2M1056 = 0xE420E420u;  // (-1056, -1056): (1024 + q) - 1056 = q - 32
 constexpr uint32_t kH2M1152 = 0xE480E480u;  // (-1152, -1152): (1024 + (v ^ 128)) - 1152 = v, signed byte v
+constexpr uint32_t kH2One = 0x3C003C00u;       // (1, 1)
+constexpr uint32_t kH2Sixteenth = 0x2C002C00u; // (1/16, 1/16)
+constexpr uint32_t kH2M72 = 0xD480D480u;       // (-72, -72): (1024 + 16 q) / 16 - 72 = q - 8
 
 __device__ __forceinline__ void mvh_lds_v4(uint32_t a, uint32_t* w) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -321,31 +324,91 @@ __device__ __forceinline__ void q6k_stage(uint32_t slot, int g, int c, const Q6O
 // ------------------------------------------------------------ Q4_0 / Q8_0 stages
 // Block BLK of the stage; lane c's weights 8c .. 8c + 7 (MMA u = 0: 8c .. + 3,
 // u = 1: 8c + 4 .. + 7). Rows are 144 bytes apart in the slot.
-// Q4_0 (18 B: d | qs[16]), lead 0: weight e is nibble e / 16 of qs[e % 16],
-// so the lane's codes are nibble c / 2 of qs[8 (c % 2) .. + 7]. ra, rb: the
-// rows' bases (slot + 144 r); la, lb: the same plus 8 (c % 2).
-template <int BLK>
-__device__ __forceinline__ void q4_0_block(uint32_t ra, uint32_t rb, uint32_t la, uint32_t lb, uint32_t sh, int c,
-                                           const uint16_t* xr, float (&acc)[4]) {
-    constexpr uint32_t O = 18 * BLK + 2;  // qs of block BLK: O % 4 is 0 for odd BLK, 2 for even
-    constexpr bool AL = (O % 4) == 0;
-    const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
-    const uint32_t a0 = (mvh_word<AL, O>(la) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t a1 = (mvh_word<AL, O + 4>(la) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t b0 = (mvh_word<AL, O>(lb) >> sh) & 0x0F0F0F0Fu;
-    const uint32_t b1 = (mvh_word<AL, O + 4>(lb) >> sh) & 0x0F0F0F0Fu;
-    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+// two consecutive 32-bit words at an 8-byte-aligned shared address
+__device__ __forceinline__ void mvh_lds_v2(uint32_t a, uint32_t& w0, uint32_t& w1) {
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(a));
+}
+
+// The lane's eight code bytes at base + O (base a multiple of 8, O even), each
+// masked with m (FLIP: with the top bit flipped instead), as four fp16 pairs
+// p[i] = (1024 + byte 2i, 1024 + byte 2i + 1). Both steps are bytewise, so
+// they work on the aligned words around the bytes: for O % 4 == 2 the pairs
+// are the upper half of one word and the lower half of the next, and no word
+// is put together first.
+template <bool FLIP>
+__device__ __forceinline__ uint32_t mvh_code_word(uint32_t w, uint32_t m) {
+    return FLIP ? (w ^ 0x80808080u) : (w & m);
+}
+
+template <uint32_t O, bool FLIP>
+__device__ __forceinline__ void mvh_code_pairs(uint32_t base, uint32_t m, uint32_t (&p)[4]) {
+    if constexpr (O % 4 == 0) {
+        uint32_t w0, w1;
+        if constexpr (O % 8 == 0) {
+            mvh_lds_v2(base + O, w0, w1);
+        } else {
+            w0 = lds_u32(base + O);
+            w1 = lds_u32(base + O + 4);
+        }
+        w0 = mvh_code_word<FLIP>(w0, m);
+        w1 = mvh_code_word<FLIP>(w1, m);
+        p[0] = h_pair01(w0);
+        p[1] = h_pair23(w0);
+        p[2] = h_pair01(w1);
+        p[3] = h_pair23(w1);
+    } else {
+        uint32_t lo, mid, hi;
+        if constexpr ((O - 2) % 8 == 0) {
+            mvh_lds_v2(base + O - 2, lo, mid);
+        } else {
+            lo = lds_u32(base + O - 2);
+            mid = lds_u32(base + O + 2);
+        }
+        hi = lds_u32(base + O + 6);
+        lo = mvh_code_word<FLIP>(lo, m);
+        mid = mvh_code_word<FLIP>(mid, m);
+        hi = mvh_code_word<FLIP>(hi, m);
+        p[0] = h_pair23(lo);
+        p[1] = h_pair01(mid);
+        p[2] = h_pair23(mid);
+        p[3] = h_pair01(hi);
+    }
+}
+
+// The two MMAs of a block from the code pairs of rows g (pa) and g + 8 (pb):
+// A = pair * hm + ha, the lane's signed codes, exact in fp16.
+__device__ __forceinline__ void mvh_block_mma(const uint32_t (&pa)[4], const uint32_t (&pb)[4], uint32_t hm,
+                                              uint32_t ha, uint4 xv, float (&D)[4]) {
     uint32_t A[4];
-    A[0] = h2_add(h_pair01(a0), kH2M1032);
-    A[1] = h2_add(h_pair01(b0), kH2M1032);
-    A[2] = h2_add(h_pair23(a0), kH2M1032);
-    A[3] = h2_add(h_pair23(b0), kH2M1032);
+    A[0] = h2_fma(pa[0], hm, ha);
+    A[1] = h2_fma(pb[0], hm, ha);
+    A[2] = h2_fma(pa[1], hm, ha);
+    A[3] = h2_fma(pb[1], hm, ha);
     mma_f16_16816(D, A, xv.x, xv.y);
-    A[0] = h2_add(h_pair01(a1), kH2M1032);
-    A[1] = h2_add(h_pair01(b1), kH2M1032);
-    A[2] = h2_add(h_pair23(a1), kH2M1032);
-    A[3] = h2_add(h_pair23(b1), kH2M1032);
+    A[0] = h2_fma(pa[2], hm, ha);
+    A[1] = h2_fma(pb[2], hm, ha);
+    A[2] = h2_fma(pa[3], hm, ha);
+    A[3] = h2_fma(pb[3], hm, ha);
     mma_f16_16816(D, A, xv.z, xv.w);
+}
+
+// Q4_0 (18 B: d | qs[16]), lead 0: weight e is nibble e / 16 of qs[e % 16],
+// so the lane's codes are nibble c / 2 of qs[8 (c % 2) .. + 7]. The nibble is
+// masked in place: a low nibble q gives the pair value 1024 + q, a high one
+// 1024 + 16 q, and A = (1024 + q) - 1032 or (1024 + 16 q) / 16 - 72, both
+// q - 8. ra, rb: the rows' bases (slot + 144 r); la, lb: the same plus
+// 8 (c % 2); nm, hm, ha: the lane's nibble mask, multiplier and addend.
+template <int BLK>
+__device__ __forceinline__ void q4_0_block(uint32_t ra, uint32_t rb, uint32_t la, uint32_t lb, uint32_t nm,
+                                           uint32_t hm, uint32_t ha, int c, const uint16_t* xr, float (&acc)[4]) {
+    constexpr uint32_t O = 18 * BLK + 2;  // qs of block BLK: O % 4 is 0 for odd BLK, 2 for even
+    const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
+    uint32_t pa[4], pb[4];
+    mvh_code_pairs<O, false>(la, nm, pa);
+    mvh_code_pairs<O, false>(lb, nm, pb);
+    float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mvh_block_mma(pa, pb, hm, ha, xv, D);
     const float da = half_bits_to_float(lds_u16(ra + 18 * BLK)), db = half_bits_to_float(lds_u16(rb + 18 * BLK));
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
@@ -354,29 +417,18 @@ __device__ __forceinline__ void q4_0_block(uint32_t ra, uint32_t rb, uint32_t la
 }
 
 // Q8_0 (34 B: d | qs[32] int8), blocks at lead L (0 or 8); the lane's codes
-// are qs[8c .. 8c + 7]. ra, rb: the rows' bases plus L; la, lb: plus 8c more.
+// are qs[8c .. 8c + 7], flipped to v ^ 128 = v + 128, so A = (1024 + (v ^
+// 128)) - 1152 = v. ra, rb: the rows' bases plus L; la, lb: plus 8c more.
 template <int BLK>
 __device__ __forceinline__ void q8_0_block(uint32_t ra, uint32_t rb, uint32_t la, uint32_t lb, int c,
                                            const uint16_t* xr, float (&acc)[4]) {
-    constexpr uint32_t O = 34 * BLK + 2;  // O % 4 is 0 for odd BLK, 2 for even (L % 4 == 0)
-    constexpr bool AL = (O % 4) == 0;
+    constexpr uint32_t O = 34 * BLK + 2;  // O % 4 is 0 for odd BLK, 2 for even (L % 8 == 0)
     const uint4 xv = mvh_x8(xr, 32 * BLK + 8 * c);
-    const uint32_t a0 = mvh_word<AL, O>(la) ^ 0x80808080u;
-    const uint32_t a1 = mvh_word<AL, O + 4>(la) ^ 0x80808080u;
-    const uint32_t b0 = mvh_word<AL, O>(lb) ^ 0x80808080u;
-    const uint32_t b1 = mvh_word<AL, O + 4>(lb) ^ 0x80808080u;
+    uint32_t pa[4], pb[4];
+    mvh_code_pairs<O, true>(la, 0u, pa);
+    mvh_code_pairs<O, true>(lb, 0u, pb);
     float D[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    uint32_t A[4];
-    A[0] = h2_add(h_pair01(a0), kH2M1152);
-    A[1] = h2_add(h_pair01(b0), kH2M1152);
-    A[2] = h2_add(h_pair23(a0), kH2M1152);
-    A[3] = h2_add(h_pair23(b0), kH2M1152);
-    mma_f16_16816(D, A, xv.x, xv.y);
-    A[0] = h2_add(h_pair01(a1), kH2M1152);
-    A[1] = h2_add(h_pair01(b1), kH2M1152);
-    A[2] = h2_add(h_pair23(a1), kH2M1152);
-    A[3] = h2_add(h_pair23(b1), kH2M1152);
-    mma_f16_16816(D, A, xv.z, xv.w);
+    mvh_block_mma(pa, pb, kH2One, kH2M1152, xv, D);
     const float da = half_bits_to_float(lds_u16(ra + 34 * BLK)), db = half_bits_to_float(lds_u16(rb + 34 * BLK));
     acc[0] = fmaf(da, D[0], acc[0]);
     acc[1] = fmaf(da, D[1], acc[1]);
@@ -385,17 +437,20 @@ __device__ __forceinline__ void q8_0_block(uint32_t ra, uint32_t rb, uint32_t la
 }
 
 __device__ __forceinline__ void q4_0_stage(uint32_t slot, int g, int c, const uint16_t* xr, float (&acc)[4]) {
-    const uint32_t sh = 4u * static_cast<uint32_t>(c >> 1), lo = 8u * static_cast<uint32_t>(c & 1);
+    const bool high = (c >> 1) != 0;
+    const uint32_t nm = high ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    const uint32_t hm = high ? kH2Sixteenth : kH2One, ha = high ? kH2M72 : kH2M1032;
+    const uint32_t lo = 8u * static_cast<uint32_t>(c & 1);
     const uint32_t ra = slot + kMvhRow32 * static_cast<uint32_t>(g), rb = ra + 8u * kMvhRow32;
     const uint32_t la = ra + lo, lb = rb + lo;
-    q4_0_block<0>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<1>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<2>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<3>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<4>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<5>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<6>(ra, rb, la, lb, sh, c, xr, acc);
-    q4_0_block<7>(ra, rb, la, lb, sh, c, xr, acc);
+    q4_0_block<0>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<1>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<2>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<3>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<4>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<5>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<6>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
+    q4_0_block<7>(ra, rb, la, lb, nm, hm, ha, c, xr, acc);
 }
 
 __device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t L, const uint16_t* xr,
