@@ -20,11 +20,13 @@ _SRC = os.path.join(_HERE, "qmm_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-Q4_0, Q8_0, Q6_K = 1, 2, 3
+Q4_0, Q8_0, Q6_K, Q4_K, Q2_K = 1, 2, 3, 4, 5
 X_F32, X_BF16 = 0, 1
 
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256, Q4_K: 256, Q2_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210, Q4_K: 144, Q2_K: 84}
+# formats whose quantized-activation (integer) path the oracle defines
+Q8_FORMATS = (Q4_0, Q8_0, Q6_K)
 
 _lib = None
 
@@ -54,6 +56,8 @@ def lib():
             "orc_block_elems": (I, [I]),
             "orc_block_bytes": (I, [I]),
             "orc_q6k_code": (I, [P, I]),
+            "orc_kq_code": (I, [I, P, I]),
+            "orc_kq_scale_min": (None, [I, P, I, P, P]),
             "orc_weight": (D, [I, P, I64]),
             "orc_dequant_row": (None, [I, P, I64, P]),
             "orc_gemv_float": (None, [I, P, I64, I64, P, I, I, P, P]),
@@ -112,6 +116,25 @@ def q6k_codes(block: np.ndarray) -> np.ndarray:
     return np.array([lib().orc_q6k_code(_p(b), i) for i in range(256)], np.int64)
 
 
+def kq_codes(fmt: int, block: np.ndarray) -> np.ndarray:
+    """The 256 unsigned codes of one Q4_K / Q2_K super-block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    return np.array([lib().orc_kq_code(fmt, _p(b), i) for i in range(256)], np.int64)
+
+
+def kq_scale_min(fmt: int, block: np.ndarray, j: int):
+    """(scale, min) of sub-block j of one Q4_K / Q2_K super-block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8)
+    sc, mn = C.c_int(), C.c_int()
+    lib().orc_kq_scale_min(fmt, _p(b), j, C.byref(sc), C.byref(mn))
+    return sc.value, mn.value
+
+
+def _q8_only(fmt):
+    if fmt not in Q8_FORMATS:
+        raise ValueError(f"the quantized-activation path is defined for q6_K, Q4_0, Q8_0 only")
+
+
 def gemv_float(fmt, W, x, N, K):
     """x: [B][K] float32 or bf16 bits -> (y [B][N] float64, sum|w x| [B][N])."""
     x = np.ascontiguousarray(x)
@@ -134,11 +157,13 @@ def quantize_q8(x):
 
 
 def group_int(fmt, row: np.ndarray, xq_row: np.ndarray, g: int) -> int:
+    _q8_only(fmt)
     return lib().orc_group_int(fmt, _p(np.ascontiguousarray(row)),
                                _p(np.ascontiguousarray(xq_row)), g)
 
 
 def gemv_q8(fmt, W, xq, s, N, K):
+    _q8_only(fmt)
     xq = np.ascontiguousarray(xq)
     s = np.ascontiguousarray(s, dtype=np.float32)
     B = xq.shape[0]
@@ -149,6 +174,7 @@ def gemv_q8(fmt, W, xq, s, N, K):
 
 
 def gemm_q8_pairs(fmt, W, K, xq, s, ms, ns):
+    _q8_only(fmt)
     ms = np.ascontiguousarray(ms, dtype=np.int64)
     ns = np.ascontiguousarray(ns, dtype=np.int64)
     y = np.empty(len(ms), np.float64)

@@ -1,6 +1,7 @@
 /*
  * qmm_oracle.c -- plain, slow CPU reference for matrix multiplication against
- * block-quantized weights (q6_K, Q4_0, Q8_0).
+ * block-quantized weights (q6_K, Q4_0, Q8_0, and the K-quant ladder formats
+ * Q4_K and Q2_K).
  *
  * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the benchmark's
  * CPU-baseline leg may load or call this file. The CUDA library never does:
@@ -26,6 +27,10 @@
  *   [X100]    "Chasing x100", "Where the wall actually fell: inversion"
  *             (routed experts kept resident and decoded in place; top-k
  *             routed expert FFN per token).
+ *   [L16]     quantprobe "LAWS.md", Law 4, the per-format eta paragraph and
+ *             amendment L-16 (metadata application density: Q2_K applies a
+ *             scale and a min every 16 weights = 4 bytes at 2 bits, Q4_K
+ *             every 32 weights = 16 bytes at 4 bits).
  *
  * Readings where the pages are silent (they print no byte order for the
  * nibbles): q6_K element i of a 256-weight super-block takes its low four
@@ -34,6 +39,21 @@
  * scales[i div 16]; every 16-element group therefore reads 16 consecutive ql
  * bytes and 16 consecutive qh bytes with one shift pair, as [MINFER] 2.1
  * describes the in-kernel expansion.
+ *
+ * The K-quant ladder formats ([L16]): the pages give their sub-block sizes
+ * and that each sub-block carries a scale and a min, but no byte layout. The
+ * reading here (the common K-quant super-block of 256 weights), weight =
+ * d * scale_j * q - dmin * min_j for sub-block j:
+ *   Q4_K, 144 bytes: d (fp16) | dmin (fp16) | 12 bytes holding eight 6-bit
+ *     scales and eight 6-bit mins | 128 bytes of 4-bit codes. Sub-block j
+ *     (32 weights) for j < 4: scale = b[j] & 63, min = b[j + 4] & 63; for
+ *     j >= 4: scale = (b[j + 4] & 15) | (b[j - 4] >> 6) << 4, min =
+ *     (b[j + 4] >> 4) | (b[j] >> 6) << 4, b the 12 bytes. Element i is nibble
+ *     (i / 32) % 2 (0 = low) of code byte 32 * (i / 64) + i % 32.
+ *   Q2_K, 84 bytes: 16 bytes (sub-block j = i / 16: low nibble scale, high
+ *     nibble min) | 64 bytes of 2-bit codes | d (fp16) | dmin (fp16).
+ *     Element i is the 2-bit field at bit 2 * ((i % 128) / 32) of code byte
+ *     32 * (i / 128) + i % 32.
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,6 +64,8 @@
 #define ORC_Q4_0 1
 #define ORC_Q8_0 2
 #define ORC_Q6_K 3
+#define ORC_Q4_K 4
+#define ORC_Q2_K 5
 
 /* activation element kinds */
 #define ORC_X_F32 0
@@ -92,6 +114,8 @@ int orc_block_elems(int fmt) {
     case ORC_Q4_0: return 32;
     case ORC_Q8_0: return 32;
     case ORC_Q6_K: return 256;
+    case ORC_Q4_K: return 256;
+    case ORC_Q2_K: return 256;
     }
     return 0;
 }
@@ -101,6 +125,8 @@ int orc_block_bytes(int fmt) {
     case ORC_Q4_0: return 2 + 16;              /* d fp16, 16 bytes of nibbles  */
     case ORC_Q8_0: return 2 + 32;              /* d fp16, 32 int8 values       */
     case ORC_Q6_K: return 128 + 64 + 16 + 2;   /* ql, qh, scales, d = 210 B    */
+    case ORC_Q4_K: return 2 + 2 + 12 + 128;    /* d, dmin, scales+mins, codes  */
+    case ORC_Q2_K: return 16 + 64 + 2 + 2;     /* scales+mins, codes, d, dmin  */
     }
     return 0;
 }
@@ -116,6 +142,57 @@ int orc_q6k_code(const uint8_t* blk, int i) {
     int lo = (ql[i % 128] >> (4 * (i / 128))) & 0xF;
     int hi = (qh[i % 64] >> (2 * (i / 64))) & 0x3;
     return lo | (hi << 4);
+}
+
+/* K-quant ladder formats (readings in the file header) */
+static int is_kquant(int fmt) { return fmt == ORC_Q4_K || fmt == ORC_Q2_K; }
+
+/* the unsigned code of element i (0..255): Q4_K 0..15, Q2_K 0..3 */
+int orc_kq_code(int fmt, const uint8_t* blk, int i) {
+    if (fmt == ORC_Q4_K) {
+        const uint8_t* qs = blk + 16;
+        return (qs[32 * (i / 64) + i % 32] >> (4 * ((i / 32) % 2))) & 0xF;
+    }
+    const uint8_t* qs = blk + 16;
+    return (qs[32 * (i / 128) + i % 32] >> (2 * ((i % 128) / 32))) & 0x3;
+}
+
+/* the scale and the min of sub-block j (Q4_K: j < 8, Q2_K: j < 16) */
+void orc_kq_scale_min(int fmt, const uint8_t* blk, int j, int* scale, int* min) {
+    if (fmt == ORC_Q4_K) {
+        const uint8_t* b = blk + 4;
+        if (j < 4) {
+            *scale = b[j] & 63;
+            *min = b[j + 4] & 63;
+        } else {
+            *scale = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4);
+            *min = (b[j + 4] >> 4) | ((b[j] >> 6) << 4);
+        }
+        return;
+    }
+    *scale = blk[j] & 15;
+    *min = blk[j] >> 4;
+}
+
+int orc_kq_sub_elems(int fmt) { return fmt == ORC_Q4_K ? 32 : 16; }
+
+/* d and dmin of a K-quant super-block */
+double orc_kq_d(int fmt, const uint8_t* blk) {
+    int off = fmt == ORC_Q4_K ? 0 : 80;
+    return orc_half_to_double((uint16_t)(blk[off] | (blk[off + 1] << 8)));
+}
+double orc_kq_dmin(int fmt, const uint8_t* blk) {
+    int off = fmt == ORC_Q4_K ? 2 : 82;
+    return orc_half_to_double((uint16_t)(blk[off] | (blk[off + 1] << 8)));
+}
+
+/* the two terms of a K-quant weight: d * scale * q and dmin * min, each an
+ * exact double (11-bit d times at most 10 bits, 11-bit dmin times 6 bits) */
+static void kq_terms(int fmt, const uint8_t* blk, int i, double* pos, double* neg) {
+    int sc, mn;
+    orc_kq_scale_min(fmt, blk, i / orc_kq_sub_elems(fmt), &sc, &mn);
+    *pos = orc_kq_d(fmt, blk) * (double)(sc * orc_kq_code(fmt, blk, i));
+    *neg = orc_kq_dmin(fmt, blk) * (double)mn;
 }
 
 /* integer value of element i before the weight-side scale: q6_K gives
@@ -160,6 +237,11 @@ int orc_group_scale(int fmt, const uint8_t* blk, int g) {
 double orc_weight(int fmt, const uint8_t* row, int64_t k) {
     int be = orc_block_elems(fmt);
     const uint8_t* blk = row + (k / be) * orc_block_bytes(fmt);
+    if (is_kquant(fmt)) {
+        double pos, neg;
+        kq_terms(fmt, blk, (int)(k % be), &pos, &neg);
+        return pos - neg;
+    }
     return orc_block_d(fmt, blk) * (double)int_value(fmt, blk, (int)(k % be));
 }
 
@@ -176,15 +258,24 @@ static const uint8_t* row_ptr(int fmt, const uint8_t* W, int64_t K, int64_t n) {
 /* float-activation matvec: y[b][n] = sum_k w[n][k] * x[b][k]          */
 /* ------------------------------------------------------------------ */
 
-/* one dot product in double; *absum receives sum_k |w*x| (the scale the
- * float tolerance is stated against) */
+/* one dot product in double; *absum receives the scale the float tolerance
+ * is stated against: sum_k |w*x|, and for the K-quant formats, whose weight
+ * is the difference of two terms, sum_k (|d*scale*q| + |dmin*min|) * |x| */
 double orc_dot_float(int fmt, const uint8_t* row, int64_t K, const void* x,
                      int xkind, int64_t xoff, double* absum) {
     double s = 0.0, a = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-        double p = orc_weight(fmt, row, k) * load_x(x, xkind, xoff + k);
+        double xv = load_x(x, xkind, xoff + k);
+        double p = orc_weight(fmt, row, k) * xv;
         s += p;
-        a += fabs(p);
+        if (is_kquant(fmt)) {
+            int be = orc_block_elems(fmt);
+            double pos, neg;
+            kq_terms(fmt, row + (k / be) * orc_block_bytes(fmt), (int)(k % be), &pos, &neg);
+            a += (fabs(pos) + fabs(neg)) * fabs(xv);
+        } else {
+            a += fabs(p);
+        }
     }
     if (absum) *absum = a;
     return s;

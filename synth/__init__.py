@@ -16,6 +16,10 @@ Value distributions (per block of each format):
   Q4_0 (18 B):  d as above, then 16 uniform bytes (every nibble q uniform on
       0..15).
   Q8_0 (34 B):  d as above, then 32 int8 uniform on -127..127.
+  Q4_K (144 B): d and dmin as d above, then 12 + 128 uniform bytes (every
+      6-bit scale and min uniform on 0..63, every code on 0..15).
+  Q2_K (84 B):  16 + 64 uniform bytes (every 4-bit scale and min uniform on
+      0..15, every code on 0..3), then d and dmin as d above.
   activations:  N(0,1) as float32, or rounded to bfloat16 (ties to even).
 """
 from __future__ import annotations
@@ -26,9 +30,11 @@ _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-Q4_0, Q8_0, Q6_K = 1, 2, 3
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210}
+Q4_0, Q8_0, Q6_K, Q4_K, Q2_K = 1, 2, 3, 4, 5
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256, Q4_K: 256, Q2_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210, Q4_K: 144, Q2_K: 84}
+# byte offsets of the fp16 d and dmin in a K-quant super-block
+KQ_D_OFF = {Q4_K: 0, Q2_K: 80}
 
 _CHUNK = 1 << 22  # draws per numpy pass (bounded temporaries)
 
@@ -135,7 +141,19 @@ def q8_0_matrix(seed: int, N: int, K: int) -> np.ndarray:
     return out.reshape(-1)
 
 
+def kq_matrix(fmt: int, seed: int, N: int, K: int) -> np.ndarray:
+    """N x K Q4_K or Q2_K weights, rows of K/256 consecutive super-blocks."""
+    assert K % 256 == 0
+    nb, bb, o = N * (K // 256), BLOCK_BYTES[fmt], KQ_D_OFF[fmt]
+    out = uniform_bytes(substream(seed, 1), nb * bb).reshape(nb, bb)
+    out[:, o:o + 2] = _scale_d(substream(seed, 3), nb)
+    out[:, o + 2:o + 4] = _scale_d(substream(seed, 4), nb)
+    return out.reshape(-1)
+
+
 def matrix(fmt: int, seed: int, N: int, K: int) -> np.ndarray:
+    if fmt in KQ_D_OFF:
+        return kq_matrix(fmt, seed, N, K)
     return {Q4_0: q4_0_matrix, Q8_0: q8_0_matrix, Q6_K: q6k_matrix}[fmt](seed, N, K)
 
 
@@ -176,6 +194,11 @@ def matrix_torch(fmt: int, seed: int, N: int, K: int, device, count: int = 1):
         out[:, :, 208:210] = d_bytes
     elif fmt == Q4_0:
         out[:, :, 0:2] = d_bytes
+    elif fmt in KQ_D_OFF:
+        o = KQ_D_OFF[fmt]
+        dm = (torch.randn((count, nb), generator=g, device=device).abs() * 2e-4).half()
+        out[:, :, o:o + 2] = d_bytes
+        out[:, :, o + 2:o + 4] = dm.view(torch.uint8).view(count, nb, 2)
     else:
         qs = torch.randint(-127, 128, (count, nb, 32), dtype=torch.int8, device=device, generator=g)
         out[:, :, 2:34] = qs.view(torch.uint8)

@@ -21,6 +21,14 @@ MUTANTS = {
     "q4_offset": ("return q - 8;", "return q - 7;"),
     "round_away": ("float rq = nearbyintf(t);", "float rq = roundf(t);"),
     "d_offset": ("int off = (fmt == ORC_Q6_K) ? 208 : 0;", "int off = (fmt == ORC_Q6_K) ? 206 : 0;"),
+    "q4k_scale_top_bits": ("*scale = (b[j + 4] & 15) | ((b[j - 4] >> 6) << 4);",
+                           "*scale = (b[j + 4] & 15) | ((b[j] >> 6) << 4);"),
+    "q4k_nibble": ("(qs[32 * (i / 64) + i % 32] >> (4 * ((i / 32) % 2)))",
+                   "(qs[32 * (i / 64) + i % 32] >> (4 * ((i / 64) % 2)))"),
+    "q2k_shift": ("(qs[32 * (i / 128) + i % 32] >> (2 * ((i % 128) / 32)))",
+                  "(qs[32 * (i / 128) + i % 32] >> (2 * ((i % 64) / 16)))"),
+    "q2k_min_nibble": ("*min = blk[j] >> 4;", "*min = blk[j] & 15;"),
+    "kq_min_sign": ("return pos - neg;", "return pos + neg;"),
 }
 
 
@@ -59,6 +67,15 @@ def _pins_pass(L) -> bool:
     if not np.array_equal(_dequant(L, oracle.Q4_0, pack.pack_q4_0_block(c4, pack.f16_bits(1.0)), 32),
                           c4 - 8.0):
         return False
+    for fmt, packer, qmax, sub, smax in [(oracle.Q4_K, pack.pack_q4k_block, 15, 32, 63),
+                                         (oracle.Q2_K, pack.pack_q2k_block, 3, 16, 15)]:
+        kc = rng.integers(0, qmax + 1, 256)
+        ks = rng.integers(0, smax + 1, 256 // sub)
+        km = rng.integers(0, smax + 1, 256 // sub)
+        blk = packer(kc, ks, km, pack.f16_bits(0.5), pack.f16_bits(0.25))
+        e = np.arange(256) // sub
+        if not np.array_equal(_dequant(L, fmt, blk, 256), 0.5 * ks[e] * kc - 0.25 * km[e]):
+            return False
     x = np.array([[127, 2.5, -2.5, 3.5] + [0.0] * 28], np.float32)
     xq = np.empty((1, 32), np.int8)
     s = np.empty((1, 1), np.float32)

@@ -140,6 +140,119 @@ def test_synth_fields_land_where_the_layout_says():
     assert codes.min() == 0 and codes.max() == 63
 
 
+# --------------------------------------------------------------- K-quant ladder formats
+
+def _f16(v):
+    return float(np.array([pack.f16_bits(v)], np.uint16).view(np.float16)[0])
+
+
+@pytest.mark.parametrize("fmt,name", [(oracle.Q4_K, "q4k_block_hand.txt"),
+                                      (oracle.Q2_K, "q2k_block_hand.txt")])
+def test_kq_hand_block(fmt, name):
+    blk, rows = _read_fixture(name)
+    assert blk.size == oracle.BLOCK_BYTES[fmt]
+    codes = oracle.kq_codes(fmt, blk)
+    w = oracle.dequant(fmt, blk, 1, 256)[0]
+    for i, q, j, wt in rows:
+        assert codes[int(i)] == int(q), i
+        assert w[int(i)] == float(wt), i
+
+
+def test_q4k_hand_block_scales_and_mins():
+    blk, _ = _read_fixture("q4k_block_hand.txt")
+    got = [oracle.kq_scale_min(oracle.Q4_K, blk, j) for j in range(8)]
+    assert got == list(zip([1, 2, 3, 4, 17, 33, 50, 63], [0, 5, 10, 63, 16, 31, 47, 2]))
+
+
+def test_q2k_hand_block_scales_and_mins():
+    blk, _ = _read_fixture("q2k_block_hand.txt")
+    assert [oracle.kq_scale_min(oracle.Q2_K, blk, j) for j in range(16)] == \
+        [(j, 15 - j) for j in range(16)]
+
+
+KQ = [(oracle.Q4_K, pack.pack_q4k_block, 15, 32, 63), (oracle.Q2_K, pack.pack_q2k_block, 3, 16, 15)]
+
+
+@pytest.mark.parametrize("fmt,packer,qmax,sub,smax", KQ)
+def test_kq_one_hot_positions(fmt, packer, qmax, sub, smax):
+    """a single nonzero code at position i decodes to a single nonzero weight
+    at i (unit scales, zero mins): the element order of the layout"""
+    ones, zeros = np.ones(256 // sub, int), np.zeros(256 // sub, int)
+    for i in range(256):
+        codes = np.zeros(256, int)
+        codes[i] = qmax
+        w = oracle.dequant(fmt, packer(codes, ones, zeros, pack.f16_bits(1.0), 0), 1, 256)[0]
+        assert w[i] == qmax and np.count_nonzero(w) == 1, i
+
+
+@pytest.mark.parametrize("fmt,packer,qmax,sub,smax", KQ)
+def test_kq_closed_form_every_scale_and_min(fmt, packer, qmax, sub, smax):
+    """w = d * scale_j * q - dmin * min_j for every scale and min value of
+    every sub-block (the others random), d and dmin exact fp16 values"""
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, qmax + 1, 256)
+    d, dmin = _f16(0.0078125), _f16(3.0517578125e-05)
+    for j in range(256 // sub):
+        for v in range(smax + 1):
+            for which in (0, 1):
+                sc = rng.integers(0, smax + 1, 256 // sub)
+                mn = rng.integers(0, smax + 1, 256 // sub)
+                (sc if which == 0 else mn)[j] = v
+                blk = packer(codes, sc, mn, pack.f16_bits(d), pack.f16_bits(dmin))
+                assert oracle.kq_scale_min(fmt, blk, j) == (sc[j], mn[j])
+                if v % 8 == 0:
+                    w = oracle.dequant(fmt, blk, 1, 256)[0]
+                    e = np.arange(256) // sub
+                    assert np.array_equal(w, d * sc[e] * codes - dmin * mn[e].astype(float))
+
+
+@pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q2_K])
+def test_kq_gemv_brute_force_4x512(fmt):
+    """float matvec = numpy matmul of the dequantized rows built by the
+    independent encoder; the bound's scale is the two-term magnitude sum"""
+    packer, qmax, sub, smax = {oracle.Q4_K: (pack.pack_q4k_block, 15, 32, 63),
+                               oracle.Q2_K: (pack.pack_q2k_block, 3, 16, 15)}[fmt]
+    N, K = 4, 512
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, qmax + 1, (N, K))
+    sc = rng.integers(0, smax + 1, (N, K // sub))
+    mn = rng.integers(0, smax + 1, (N, K // sub))
+    dv = np.array([[_f16(0.001 * (n + 1) + 0.0002 * b) for b in range(K // 256)] for n in range(N)])
+    mv = np.array([[_f16(0.0005 * (n + 2) + 0.0001 * b) for b in range(K // 256)] for n in range(N)])
+    W = pack.pack_kq_matrix(packer, codes, sc, mn,
+                            np.vectorize(pack.f16_bits)(dv), np.vectorize(pack.f16_bits)(mv))
+    e, blk = np.arange(K) // sub, np.arange(K) // 256
+    pos = dv[:, blk] * sc[:, e] * codes
+    neg = mv[:, blk] * mn[:, e]
+    dense = pos - neg
+    assert np.array_equal(oracle.dequant(fmt, W, N, K), dense)
+    x = synth.normal_f32(21, (3, K))
+    y, a = oracle.gemv_float(fmt, W, x, N, K)
+    ref = x.astype(np.float64) @ dense.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(x.astype(np.float64)) @ (np.abs(pos) + np.abs(neg)).T, rtol=1e-12)
+
+
+def test_kq_synth_fields_land_where_the_layout_says():
+    for fmt, qmax, smax, nsub in [(oracle.Q4_K, 15, 63, 8), (oracle.Q2_K, 3, 15, 16)]:
+        W = synth.matrix(fmt, 6, 32, 1024).reshape(-1, oracle.BLOCK_BYTES[fmt])
+        sm = np.array([oracle.kq_scale_min(fmt, b, j) for b in W[:64] for j in range(nsub)])
+        assert sm.min() == 0 and sm.max() == smax
+        codes = np.concatenate([oracle.kq_codes(fmt, b) for b in W[:8]])
+        assert codes.min() == 0 and codes.max() == qmax
+        o = synth.KQ_D_OFF[fmt]
+        for off in (o, o + 2):
+            v = W[:, off:off + 2].copy().view(np.float16).astype(np.float64)
+            assert (v >= 0).all() and v.max() < 2e-3 and v.max() > 0
+
+
+def test_kq_q8_path_is_refused():
+    W = synth.matrix(oracle.Q4_K, 1, 8, 256)
+    xq, s = oracle.quantize_q8(synth.normal_f32(1, (1, 256)))
+    with pytest.raises(ValueError):
+        oracle.gemv_q8(oracle.Q4_K, W, xq, s, 8, 256)
+
+
 # --------------------------------------------------------------- float matvec
 
 def _identity_q6k(n):
