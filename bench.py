@@ -56,8 +56,12 @@ DECODE_SET = [  # (name, fmt name, N, K)
     ("output", "q6_K", 32000, 4096), ("wq_q8_0", "Q8_0", 4096, 4096),
 ]
 BATCHES = (1, 8)
-FMT_CODE = {"Q4_0": 1, "Q8_0": 2, "q6_K": 3}
-BLOCK = {"Q4_0": (32, 18), "Q8_0": (32, 34), "q6_K": (256, 210)}
+FMT_CODE = {"Q4_0": 1, "Q8_0": 2, "q6_K": 3, "Q4_K": 4, "Q2_K": 5}
+BLOCK = {"Q4_0": (32, 18), "Q8_0": (32, 34), "q6_K": (256, 210), "Q4_K": (256, 144), "Q2_K": (256, 84)}
+# the format ladder (quantprobe "LAWS.md", Law 4, the per-format eta of
+# L-15 / L-16): the same two shapes in every format, highest bits first
+LADDER_FORMATS = ("Q8_0", "q6_K", "Q4_0", "Q4_K", "Q2_K")
+LADDER_SHAPES = (("attn 4096x4096", 4096, 4096), ("ffn_up 11008x4096", 11008, 4096))
 
 
 def weight_bytes(fmt, N, K):
@@ -375,6 +379,43 @@ def per_matrix(torch, qmm, dec, device, steps):
         tok[str(B)] = {"tok_per_s": B / (t_tok * 1e-6), "us_per_token_step": t_tok,
                        "weight_bytes_per_step": b_tok, "effective_gbps": b_tok / (t_tok * 1e-6) / 1e9}
     return rows, tok
+
+
+def format_ladder(torch, qmm, device, steps, hbm, check):
+    """Per-format matvec time of the same shapes at batch 1 and 8 (single
+    calls over rotated copies; bf16 activations, so every format runs on the
+    fp16-MMA matvec): GB/s, weights/s and eta = GB/s / HBM peak, the pages'
+    per-format utilisation. With check, 64 sampled outputs of each matrix
+    are compared with the oracle first."""
+    import synth
+    rows = []
+    for label, N, K in LADDER_SHAPES:
+        for fmt in LADDER_FORMATS:
+            code = FMT_CODE[fmt]
+            Wt = synth.matrix_torch(code, 0x1ADD + code * 16 + N, N, K, device)[0]
+            wb = weight_bytes(fmt, N, K)
+            for B in BATCHES:
+                xf = synth.normal_f32(0x1ADE + B + K, (B, K))
+                xt = torch.from_numpy(synth.to_bf16_bits(xf).view(np.int16)).to(device).view(torch.bfloat16)
+                run = MatvecRun(torch, qmm, code, Wt, xt, N, K, device)
+                for _ in range(3):
+                    run.g.replay()
+                parity = None
+                if check:
+                    import oracle
+                    rng = np.random.default_rng(N + B + code)
+                    ns, bs = rng.integers(0, N, 64), rng.integers(0, B, 64)
+                    ref, absum = oracle.gemv_float_pairs(code, Wt.cpu().numpy(), K, synth.to_bf16_bits(xf), bs, ns)
+                    worst = _worst(run.y.cpu().numpy()[bs, ns], ref, 1e-4 * absum + 1e-6)
+                    parity = {"outputs": 64, "max_err_over_bound": worst, "ok": bool(worst <= 1.0)}
+                t = run.time_us(max(5, steps // 2))
+                gbps = wb / (t * 1e-6) / 1e9
+                rows.append({"shape": label, "format": fmt, "bits_per_weight": 8.0 * wb / (N * K), "batch": B,
+                             "us": t, "gbps": gbps, "gweights_per_s": N * K / (t * 1e-6) / 1e9,
+                             "eta": gbps / hbm, "copies": run.n, "parity": parity})
+                del run
+            del Wt
+    return rows
 
 
 # ------------------------------------------------------------------ CPU baseline
@@ -929,6 +970,7 @@ def main():
 
     # per-matrix times of the decode set and the equivalent tok/s
     pm_rows, pm_tok = per_matrix(torch, qmm, dec, device, args.steps)
+    ladder = format_ladder(torch, qmm, device, args.steps, pk["hbm_gbs"], rank == 0)
 
     # roofline of the part that takes the most time in the step
     hbm = pk["hbm_gbs"]
@@ -993,6 +1035,7 @@ def main():
             "config0": config0,
             "per_matrix": pm_rows,
             "equivalent_tok_s": pm_tok,
+            "format_ladder": ladder,
             "moe": {"t1_gbps": moe_gbs["moe_t1"], "t16_gbps": moe_gbs["moe_t16"],
                     "t16_distinct_experts": moe16.distinct, "t1_bytes": moe1.bytes,
                     "t16_bytes": moe16.bytes},

@@ -13,7 +13,7 @@ import os
 
 from .build import LIB as _LIB_PATH
 
-Q4_0, Q8_0, Q6_K = 0x01, 0x02, 0x03
+Q4_0, Q8_0, Q6_K, Q4_K, Q2_K = 0x01, 0x02, 0x03, 0x04, 0x05
 X_F32, X_BF16 = 0x000, 0x100
 ACT_FLOAT, ACT_Q8 = 0x0000, 0x1000
 
@@ -29,8 +29,8 @@ LIVE = {
 }
 LIVE_COUNT = 24
 
-BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210}
+BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256, Q4_K: 256, Q2_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210, Q4_K: 144, Q2_K: 84}
 
 
 class QmmError(RuntimeError):

@@ -127,8 +127,17 @@ std::unordered_map<const void*, PlaneEntry> g_planes;
 std::mutex g_planes_mu;
 
 // ---------------------------------------------------------------- formats
-int block_elems(int f) { return f == FMT_Q6_K ? 256 : 32; }
-int block_bytes(int f) { return f == FMT_Q6_K ? 210 : (f == FMT_Q4_0 ? 18 : 34); }
+bool is_kquant(int f) { return f == FMT_Q4_K || f == FMT_Q2_K; }
+int block_elems(int f) { return (f == FMT_Q6_K || is_kquant(f)) ? 256 : 32; }
+int block_bytes(int f) {
+    switch (f) {
+        case FMT_Q6_K: return 210;
+        case FMT_Q4_0: return 18;
+        case FMT_Q4_K: return 144;
+        case FMT_Q2_K: return 84;
+        default: return 34;
+    }
+}
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -136,7 +145,7 @@ int check_fmt(uint32_t fmt, int* wf, bool* bf16, bool* q8) {
     if (fmt & ~static_cast<uint32_t>(QMM_FMT_MASK | QMM_X_MASK | QMM_ACT_MASK))
         return fail(QMM_EINVAL, "fmt 0x%x has unknown bits", fmt);
     *wf = static_cast<int>(fmt & QMM_FMT_MASK);
-    if (*wf != QMM_Q4_0 && *wf != QMM_Q8_0 && *wf != QMM_Q6_K)
+    if (*wf != QMM_Q4_0 && *wf != QMM_Q8_0 && *wf != QMM_Q6_K && *wf != QMM_Q4_K && *wf != QMM_Q2_K)
         return fail(QMM_EINVAL, "unknown weight format 0x%x", fmt & QMM_FMT_MASK);
     const uint32_t xk = fmt & QMM_X_MASK, am = fmt & QMM_ACT_MASK;
     if (xk != QMM_X_F32 && xk != QMM_X_BF16)
@@ -457,6 +466,11 @@ int fast_path(int wf, bool q8, bool bf16, int B, int64_t N, int64_t K) {
     return FAST_NONE;
 }
 
+// The K-quant ladder formats (Q4_K, Q2_K) run on the fp16-MMA matvec only.
+bool kquant_runs(int wf, bool q8, bool bf16, int B, int64_t N, int64_t K) {
+    return !is_kquant(wf) || fast_path(wf, q8, bf16, B, N, K) == FAST_MVH;
+}
+
 // Launches mv1 or mv8 over matrices sel[0 .. n-1] of the arrays.
 int run_fast(int path, int wf, bool bf16, int B, int n, const int* sel, const void* const* W,
              const void* const* x, float* const* y, const int64_t* N, const int64_t* K, const DevInfo* d) {
@@ -602,6 +616,9 @@ int check_gemv_args(uint32_t fmt, const void* W, const void* x, const float* y, 
                                           (long long)K, block_elems(*wf));
     if (!aligned16(W) || !aligned16(x)) return fail(QMM_EALIGN, "W and x must be 16-byte aligned");
     if (reinterpret_cast<uintptr_t>(y) & 3u) return fail(QMM_EALIGN, "y must be 4-byte aligned");
+    if (!kquant_runs(*wf, *q8, *bf16, B, N, K))
+        return fail(QMM_EUNSUPPORTED, "Q4_K / Q2_K matvecs need bf16 activations in float mode, B <= 8 "
+                                      "and N %% 8 == 0 (the fp16-MMA matvec)");
     return QMM_OK;
 }
 
@@ -700,6 +717,7 @@ static size_t set_workspace_bytes(int n, const uint32_t* fmts, uint32_t fmt1, co
         const uint32_t f = fmts ? fmts[m] : fmt1;
         if (check_fmt(f, &wf[m], &bf16, &q8)) return 0;
         if (N[m] <= 0 || K[m] <= 0 || K[m] % block_elems(wf[m])) return 0;
+        if (!kquant_runs(wf[m], q8, bf16, B, N[m], K[m])) return 0;
     }
     DevInfo* d;
     if (dev_info(&d)) return 0;
@@ -788,7 +806,7 @@ int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M, in
     bool bf16, q8;
     int rc = check_fmt(fmt, &wf, &bf16, &q8);
     if (rc) return rc;
-    if (wf == QMM_Q8_0) return fail(QMM_EUNSUPPORTED, "qmm_gemm supports q6_K and Q4_0 weights");
+    if (wf != QMM_Q6_K && wf != QMM_Q4_0) return fail(QMM_EUNSUPPORTED, "qmm_gemm supports q6_K and Q4_0 weights");
     if (!W || !X || !Y) return fail(QMM_EINVAL, "null pointer (W %p, X %p, Y %p)", W, X, (void*)Y);
     if (M <= 0 || N <= 0 || K <= 0) return fail(QMM_EINVAL, "M, N, K must be positive");
     if (K % block_elems(wf))
@@ -854,6 +872,7 @@ int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const f
     int rc = check_fmt(fmt, &wf, &bf16, &q8);
     if (rc) return rc;
     if (q8) return fail(QMM_EUNSUPPORTED, "moe_gemv runs in float activation mode");
+    if (is_kquant(wf)) return fail(QMM_EUNSUPPORTED, "moe_gemv supports q6_K, Q4_0 and Q8_0 experts");
     if (!experts || !experts->w_gate || !experts->w_up || !experts->w_down)
         return fail(QMM_EINVAL, "null expert table");
     const qmm_moe_t& m = *experts;
@@ -915,9 +934,12 @@ size_t qmm_workspace_bytes(uint32_t fmt, int64_t M_or_B, int64_t N, int64_t K) {
     bool bf16, q8;
     if (check_fmt(fmt, &wf, &bf16, &q8)) return 0;
     if (M_or_B < 1 || N <= 0 || K <= 0 || K % block_elems(wf)) return 0;
+    if (is_kquant(wf)) {
+        if (M_or_B > 8 || !kquant_runs(wf, q8, bf16, static_cast<int>(M_or_B), N, K)) return 0;
+    }
     // the GEMM's quantized activations (fp16 tiles + scales)
     size_t gemm = 0;
-    if (wf != QMM_Q8_0)
+    if (wf == QMM_Q6_K || wf == QMM_Q4_0)
         gemm = round_up(gemm_a16_bytes(M_or_B, K), 256) +
                round_up(static_cast<size_t>(M_or_B) * (K / 32) * 4, 256) +
                round_up(gemm_part_bytes(M_or_B, N, K), 256);
@@ -1008,6 +1030,7 @@ int qmm_gemv_noalloc(uint32_t fmt, const void* W, const void* x, float* y, int64
     bool bf16, q8;
     int rc = check_gemv_args(fmt, W, x, y, N, K, B, &wf, &bf16, &q8);
     if (rc) return rc;
+    if (is_kquant(wf)) return fail(QMM_EUNSUPPORTED, "qmm_gemv_noalloc supports q6_K, Q4_0 and Q8_0 weights");
     DevInfo* d;
     if ((rc = dev_info(&d))) return rc;
     GemvPlan p;

@@ -13,7 +13,7 @@
 namespace qmm {
 
 // Weight formats (same numbering as the C interface).
-enum : int { FMT_Q4_0 = 1, FMT_Q8_0 = 2, FMT_Q6_K = 3 };
+enum : int { FMT_Q4_0 = 1, FMT_Q8_0 = 2, FMT_Q6_K = 3, FMT_Q4_K = 4, FMT_Q2_K = 5 };
 
 // Bits of the device error word (sticky until qmm_sync_check clears it).
 enum : uint32_t {

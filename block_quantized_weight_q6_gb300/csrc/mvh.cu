@@ -73,15 +73,18 @@ __global__ void __launch_bounds__(256) mvh_prep_kernel(const __grid_constant__ M
 // ------------------------------------------------------------ host
 
 bool mvh_supported(int fmt, int64_t N, int64_t K) {
-    return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0 || fmt == FMT_Q6_K) && K > 0 && K % 256 == 0 && N >= 8 &&
+    return (fmt == FMT_Q4_0 || fmt == FMT_Q8_0 || fmt == FMT_Q6_K || fmt == FMT_Q4_K || fmt == FMT_Q2_K) && K > 0 &&
+           K % 256 == 0 && N >= 8 &&
            N % 8 == 0 && N / 8 <= (int64_t{1} << 31) - 1;
 }
 
 namespace {
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
-int block_elems(int f) { return f == FMT_Q6_K ? 256 : 32; }
-int block_bytes(int f) { return f == FMT_Q6_K ? 210 : (f == FMT_Q4_0 ? 18 : 34); }
+int block_elems(int f) { return (f == FMT_Q4_0 || f == FMT_Q8_0) ? 32 : 256; }
+int block_bytes(int f) {
+    return f == FMT_Q6_K ? 210 : f == FMT_Q4_0 ? 18 : f == FMT_Q8_0 ? 34 : f == FMT_Q4_K ? 144 : 84;
+}
 
 // distinct activation matrices among x[0 .. n-1] (same pointer and K): their
 // index for each matrix and their workspace offsets

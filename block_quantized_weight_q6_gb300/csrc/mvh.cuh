@@ -58,10 +58,14 @@ namespace qmm {
 
 constexpr int kMvhNS = 3;
 constexpr int kMvhRows = 16;                // rows per item: one 16-row MMA tile
-// box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 1 x 144
-__host__ __device__ constexpr uint32_t mvh_box_w(int fmt) { return fmt == FMT_Q6_K ? 64u : 144u; }
+// box width in bytes and boxes per stage: q6_K 4 x 64, Q4_0 / Q8_0 / Q4_K
+// 1 x 144, Q2_K 1 x 96 (its 84-byte super-block and a lead of up to 12)
+__host__ __device__ constexpr uint32_t mvh_box_w(int fmt) {
+    return fmt == FMT_Q6_K ? 64u : (fmt == FMT_Q2_K ? 96u : 144u);
+}
 __host__ __device__ constexpr int mvh_boxes(int fmt) { return fmt == FMT_Q6_K ? 4 : 1; }
-constexpr uint32_t kMvhRow32 = 144;  // Q4_0 / Q8_0 row stride in a stage slot
+constexpr uint32_t kMvhRow32 = 144;  // Q4_0 / Q8_0 / Q4_K row stride in a stage slot
+constexpr uint32_t kMvhRowQ2K = 96;  // Q2_K row stride in a stage slot
 constexpr uint32_t kMvhSlot = 4 * 64 * kMvhRows;   // the largest stage: 4 KB
 constexpr uint32_t kMvhPartOff = kMvhWarps * kMvhNS * kMvhSlot;  // team sums, after the rings
 constexpr uint32_t kMvhBarOff = kMvhPartOff + kMvhWarps * 4 * 32 * 4;
@@ -110,6 +114,12 @@ constexpr uint32_t kH2M1152 = 0xE480E480u;  // (-1152, -1152): (1024 + (v ^ 128)
 constexpr uint32_t kH2One = 0x3C003C00u;       // (1, 1)
 constexpr uint32_t kH2Sixteenth = 0x2C002C00u; // (1/16, 1/16)
 constexpr uint32_t kH2M72 = 0xD480D480u;       // (-72, -72): (1024 + 16 q) / 16 - 72 = q - 8
+constexpr uint32_t kH2M1024 = 0xE400E400u;     // (-1024, -1024)
+constexpr uint32_t kH2Quarter = 0x34003400u;   // (1/4, 1/4)
+constexpr uint32_t kH2Sixtyfourth = 0x24002400u;  // (1/64, 1/64)
+constexpr uint32_t kH2M256 = 0xDC00DC00u;      // -1024 / 4
+constexpr uint32_t kH2M64 = 0xD400D400u;       // -1024 / 16
+constexpr uint32_t kH2M16 = 0xCC00CC00u;       // -1024 / 64
 
 __device__ __forceinline__ void mvh_lds_v4(uint32_t a, uint32_t* w) {
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -463,11 +473,159 @@ __device__ __forceinline__ void q8_0_stage(uint32_t slot, int g, int c, uint32_t
     q8_0_block<3>(ra, rb, la, lb, c, xr, acc);
 }
 
+// ------------------------------------------------------------ Q4_K / Q2_K stages
+// The K-quant ladder formats (quantprobe "LAWS.md", Law 4 amendment L-16):
+// weight = d * sc_j * q - dmin * m_j per sub-block j. A = sc_j * q is exact
+// in fp16 (<= 63 * 15), made like Q4_0's from the code masked in place by
+// one fp16x2 FMA per pair, with the sub-block's scale folded into the FMA's
+// multiplier and addend. The min term is a second MMA on the same
+// activations with A = m_j (exact), so a stage keeps two sums per row, D1 =
+// sum sc q x and D2 = sum m x, and adds d D1 - dmin D2 once per super-block.
+// Lane c takes sub-blocks c + 4t of its two rows, so the scales and mins it
+// needs are its own: four consecutive weights of a sub-block per MMA.
+
+// (1024 + byte c of w) in both halves; selc = 0x4040 | c << 8 | c
+__device__ __forceinline__ uint32_t h_byte_pair(uint32_t w, uint32_t selc) {
+    return __byte_perm(w, 0x64646464u, selc);
+}
+
+// FMA operands of a sub-block: A = pair * hm + ha (hm = sc * f, ha = -1024 hm,
+// f undoing the code's place in its byte), and the min pair for D2
+struct KqSub {
+    uint32_t hm, ha, m;
+};
+
+// from the sub-block's scale and min bytes (byte c of sc4 / m4, each < 64)
+__device__ __forceinline__ KqSub kq_sub(uint32_t sc4, uint32_t m4, uint32_t selc, uint32_t f, uint32_t nf) {
+    KqSub o;
+    o.hm = h2_fma(h_byte_pair(sc4, selc), f, nf);  // (1024 + sc) f - 1024 f = sc f, exact
+    o.ha = h2_mul(o.hm, kH2M1024);
+    o.m = h2_add(h_byte_pair(m4, selc), kH2M1024);
+    return o;
+}
+
+// the four MMAs of one code word quad (words w[0..3] of both rows, masked
+// with nm): word u holds weights 4u .. 4u + 3, whose activations are x[4u ..]
+__device__ __forceinline__ void kq_mma4(const uint32_t (&wa)[4], const uint32_t (&wb)[4], uint32_t nm,
+                                        const KqSub& sa, const KqSub& sb, uint4 x0, uint4 x1, float (&D1)[4],
+                                        float (&D2)[4]) {
+    const uint32_t A2[4] = {sa.m, sb.m, sa.m, sb.m};
+    const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const uint32_t a = wa[u] & nm, b = wb[u] & nm;
+        uint32_t A[4];
+        A[0] = h2_fma(h_pair01(a), sa.hm, sa.ha);
+        A[1] = h2_fma(h_pair01(b), sb.hm, sb.ha);
+        A[2] = h2_fma(h_pair23(a), sa.hm, sa.ha);
+        A[3] = h2_fma(h_pair23(b), sb.hm, sb.ha);
+        mma_f16_16816(D1, A, xb[2 * u], xb[2 * u + 1]);
+        mma_f16_16816(D2, A2, xb[2 * u], xb[2 * u + 1]);
+    }
+}
+
+__device__ __forceinline__ void kq_finish(float da, float dma, float db, float dmb, const float (&D1)[4],
+                                          const float (&D2)[4], float (&acc)[4]) {
+    acc[0] = fmaf(da, D1[0], acc[0]);
+    acc[1] = fmaf(da, D1[1], acc[1]);
+    acc[2] = fmaf(db, D1[2], acc[2]);
+    acc[3] = fmaf(db, D1[3], acc[3]);
+    acc[0] = fmaf(-dma, D2[0], acc[0]);
+    acc[1] = fmaf(-dma, D2[1], acc[1]);
+    acc[2] = fmaf(-dmb, D2[2], acc[2]);
+    acc[3] = fmaf(-dmb, D2[3], acc[3]);
+}
+
+// Q4_K (144 B: d | dmin | 12 scale bytes | 128 code bytes), lead 0, rows 144
+// bytes apart. Lane c's sub-blocks c and c + 4: code bytes 16 + 32 (c / 2)
+// (+ 64), nibble c % 2; a high nibble is masked in place (1024 + 16 q) and
+// f = 1/16 takes the 16 out.
+__device__ __forceinline__ void q4k_row_subs(uint32_t r, uint32_t selc, uint32_t f, uint32_t nf, KqSub (&o)[2],
+                                             float& d, float& dmin) {
+    uint32_t w[4];
+    mvh_lds_v4(r, w);  // d | dmin, scale bytes 0..3, 4..7, 8..11
+    // sub-block c: scale = b[c] & 63, min = b[c + 4] & 63; sub-block c + 4:
+    // the low / high nibble of b[c + 8] and the top two bits of b[c] / b[c + 4]
+    const uint32_t sc0 = w[1] & 0x3F3F3F3Fu, m0 = w[2] & 0x3F3F3F3Fu;
+    const uint32_t sc1 = (w[3] & 0x0F0F0F0Fu) | ((w[1] & 0xC0C0C0C0u) >> 2);
+    const uint32_t m1 = ((w[3] >> 4) & 0x0F0F0F0Fu) | ((w[2] & 0xC0C0C0C0u) >> 2);
+    o[0] = kq_sub(sc0, m0, selc, f, nf);
+    o[1] = kq_sub(sc1, m1, selc, f, nf);
+    d = half_bits_to_float(w[0] & 0xFFFFu);
+    dmin = half_bits_to_float(w[0] >> 16);
+}
+
+__device__ __forceinline__ void q4k_stage(uint32_t slot, int g, int c, uint32_t selc, const uint16_t* xr,
+                                          float (&acc)[4]) {
+    const bool high = (c & 1) != 0;
+    const uint32_t nm = high ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    const uint32_t f = high ? kH2Sixteenth : kH2One, nf = high ? kH2M64 : kH2M1024;
+    const uint32_t pa = slot + kMvhRow32 * static_cast<uint32_t>(g), pb = pa + 8u * kMvhRow32;
+    KqSub sa[2], sb[2];
+    float da, dma, db, dmb;
+    q4k_row_subs(pa, selc, f, nf, sa, da, dma);
+    q4k_row_subs(pb, selc, f, nf, sb, db, dmb);
+    float D1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t co = 16u + 32u * static_cast<uint32_t>(c >> 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            uint32_t wa[4], wb[4];
+            mvh_lds_v4(pa + co + 64u * h + 16u * v, wa);
+            mvh_lds_v4(pb + co + 64u * h + 16u * v, wb);
+            const int x0 = 32 * (c + 4 * h) + 16 * v;
+            kq_mma4(wa, wb, nm, sa[h], sb[h], mvh_x8(xr, x0), mvh_x8(xr, x0 + 8), D1, D2);
+        }
+    }
+    kq_finish(da, dma, db, dmb, D1, D2, acc);
+}
+
+// Q2_K (84 B: 16 scale bytes | 64 code bytes | d | dmin) at lead L (0, 4, 8
+// or 12), rows 96 bytes apart. Lane c's sub-blocks c + 4t: scale byte c of
+// scale word t, codes 16 bytes at 16 + 32 (t / 2) + 16 (c % 2), the 2-bit
+// field s = c / 2 + 2 (t % 2) of each byte, masked in place (1024 + 4^s q)
+// with f = 4^-s. Kept out of line (inlined, it made the kernel spill) and
+// returns the stage's sums d D1 - dmin D2 of the lane's four outputs.
+__device__ __noinline__ float4 q2k_stage(uint32_t slot, int g, int c, uint32_t L, uint32_t selc,
+                                         const uint16_t* xr) {
+    const uint32_t s0 = static_cast<uint32_t>(c >> 1);  // field of the even t (0 or 1); odd t: s0 + 2
+    const uint32_t pa = slot + kMvhRowQ2K * static_cast<uint32_t>(g) + L, pb = pa + 8u * kMvhRowQ2K;
+    float D1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, D2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const uint32_t co = 16u + 16u * static_cast<uint32_t>(c & 1);
+#pragma unroll
+    for (int run = 0; run < 2; ++run) {
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            wa[u] = lds_u32(pa + co + 32u * run + 4u * u);
+            wb[u] = lds_u32(pb + co + 32u * run + 4u * u);
+        }
+#pragma unroll
+        for (int tt = 0; tt < 2; ++tt) {
+            const int t = 2 * run + tt;
+            const uint32_t f = tt ? (s0 ? kH2Sixtyfourth : kH2Sixteenth) : (s0 ? kH2Quarter : kH2One);
+            const uint32_t nf = tt ? (s0 ? kH2M16 : kH2M64) : (s0 ? kH2M256 : kH2M1024);
+            const uint32_t ka = lds_u32(pa + 4u * t), kb = lds_u32(pb + 4u * t);
+            const KqSub sa = kq_sub(ka & 0x0F0F0F0Fu, (ka >> 4) & 0x0F0F0F0Fu, selc, f, nf);
+            const KqSub sb = kq_sub(kb & 0x0F0F0F0Fu, (kb >> 4) & 0x0F0F0F0Fu, selc, f, nf);
+            const int x0 = 16 * (c + 4 * t);
+            kq_mma4(wa, wb, 0x03030303u << (2u * s0 + 4u * tt), sa, sb, mvh_x8(xr, x0), mvh_x8(xr, x0 + 8), D1,
+                    D2);
+        }
+    }
+    const uint32_t dda = lds_u32(pa + 80u), ddb = lds_u32(pb + 80u);
+    float r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    kq_finish(half_bits_to_float(dda & 0xFFFFu), half_bits_to_float(dda >> 16), half_bits_to_float(ddb & 0xFFFFu),
+              half_bits_to_float(ddb >> 16), D1, D2, r);
+    return make_float4(r[0], r[1], r[2], r[3]);
+}
+
 // ------------------------------------------------------------ the kernel
 
 __host__ __device__ constexpr int mvh_stage_k(int fmt) { return fmt == FMT_Q8_0 ? 128 : 256; }
 __host__ __device__ constexpr int mvh_stage_bytes(int fmt) {
-    return fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q4_0 ? 144 : 136);
+    return fmt == FMT_Q6_K ? 210 : (fmt == FMT_Q4_0 || fmt == FMT_Q4_K) ? 144 : (fmt == FMT_Q2_K ? 84 : 136);
 }
 
 // The walk of a warp's (or team's) stages. Teams (KS > 1) take items t,
@@ -632,7 +790,15 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
             const uint32_t L = static_cast<uint32_t>(mvh_stage_off(a, j, p) & 15);
             if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc);
             else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc);
-            else q8_0_stage(slot, gr, c, L, xr, acc);
+            else if (a.fmt == FMT_Q8_0) q8_0_stage(slot, gr, c, L, xr, acc);
+            else if (a.fmt == FMT_Q4_K) q4k_stage(slot, gr, c, selc, xr, acc);
+            else {
+                const float4 r = q2k_stage(slot, gr, c, L, selc, xr);
+                acc[0] += r.x;
+                acc[1] += r.y;
+                acc[2] += r.z;
+                acc[3] += r.w;
+            }
             __syncwarp();
         }
         // the team's sums of the item, added by member 0 in member order

@@ -44,6 +44,25 @@ enum {
     QMM_Q4_0 = 0x01,
     QMM_Q8_0 = 0x02,
     QMM_Q6_K = 0x03,
+    /* The K-quant ladder formats of quantprobe "LAWS.md", Law 4 amendment
+     * L-16 (a scale and a min per 32 weights for Q4_K, per 16 for Q2_K;
+     * weight = d * scale_j * q - dmin * min_j). The pages give no byte
+     * layout; the one read here, per 256-weight super-block:
+     *   Q4_K, 144 B: d (fp16) | dmin (fp16) | 12 bytes of eight 6-bit scales
+     *     and mins (sub-block j < 4: scale = b[j] & 63, min = b[j+4] & 63;
+     *     j >= 4: scale = (b[j+4] & 15) | (b[j-4] >> 6) << 4, min =
+     *     (b[j+4] >> 4) | (b[j] >> 6) << 4) | 128 code bytes; element i is
+     *     nibble (i/32) % 2 (0 = low) of code byte 32 (i/64) + i % 32.
+     *   Q2_K, 84 B: 16 bytes (sub-block i/16: low nibble scale, high nibble
+     *     min) | 64 code bytes | d (fp16) | dmin (fp16); element i is the
+     *     2-bit field at bit 2 ((i % 128) / 32) of code byte
+     *     32 (i/128) + i % 32.
+     * Rows are K/256 consecutive super-blocks. Only the matvecs take them
+     * (qmm_gemv, qmm_gemv_group, qmm_gemv_multi and their workspace queries),
+     * with bf16 activations in float mode, B <= 8, K % 256 == 0 and
+     * N % 8 == 0; every other call refuses them with QMM_EUNSUPPORTED. */
+    QMM_Q4_K = 0x04,
+    QMM_Q2_K = 0x05,
     QMM_FMT_MASK = 0xFF,
 
     QMM_X_F32 = 0x000,  /* activations are fp32                              */

@@ -66,7 +66,7 @@ def test_gemv_argument_errors(L, case, expect):
     if case == "zero_K": K = 0
     if case == "B0": B = 0
     if case == "B17": B = 17
-    if case == "bad_fmt": fmt = 0x04
+    if case == "bad_fmt": fmt = 0x06
     if case == "bad_x": fmt = L.Q6_K | 0x200
     if case == "bad_mode": fmt = L.Q6_K | 0x2000
     if case == "unknown_bits": fmt = L.Q6_K | 0x10000
@@ -77,6 +77,23 @@ def test_gemv_argument_errors(L, case, expect):
     rc, msg = _rc(L, "qmm_gemv", fmt, W, x, y, N, K, B)
     assert rc == expect, (case, rc, msg)
     assert msg
+
+
+def test_kquant_formats_only_on_the_fp16_mma_matvec(L):
+    """Q4_K / Q2_K: accepted by the matvecs for bf16 activations in float
+    mode, B <= 8, N % 8 == 0; refused with QMM_EUNSUPPORTED (-2) elsewhere,
+    on the host, before anything is launched"""
+    bf = L.X_BF16
+    for f in (L.Q4_K, L.Q2_K):
+        assert _rc(L, "qmm_gemv", f | L.X_F32, FAKE, FAKE, FAKE, 64, 256, 1)[0] == -2   # fp32 x
+        assert _rc(L, "qmm_gemv", f | bf | L.ACT_Q8, FAKE, FAKE, FAKE, 64, 256, 1)[0] == -2
+        assert _rc(L, "qmm_gemv", f | bf, FAKE, FAKE, FAKE, 64, 256, 9)[0] == -2      # B > 8
+        assert _rc(L, "qmm_gemv", f | bf, FAKE, FAKE, FAKE, 12, 256, 1)[0] == -2      # N % 8
+        assert _rc(L, "qmm_gemv", f | bf, FAKE, FAKE, FAKE, 64, 288, 1)[0] == -3      # K % 256
+        assert _rc(L, "qmm_gemm", f, FAKE, FAKE, FAKE, 128, 64, 256, None)[0] == -2
+        assert _rc(L, "qmm_gemv_noalloc", f | bf, FAKE, FAKE, FAKE, 64, 256, 1)[0] == -2
+        assert _rc(L, "moe_gemv", f | bf, None, None, None, None, None)[0] == -2
+        assert L.lib.qmm_workspace_bytes(f | L.X_F32, 1, 64, 256) == 0
 
 
 def test_quantize_and_plane_argument_errors(L):
