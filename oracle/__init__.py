@@ -69,6 +69,7 @@ def lib():
             "orc_plane_q6k": (None, [P, I64, I64, P]),
             "orc_route_topk_softmax": (None, [P, I, I, I, P, P]),
             "orc_moe_float": (None, [I, I, I, P, P, P, I, I, P, P, P, I, P, P, P]),
+            "orc_moe_q8": (None, [I, I, I, P, P, P, I, I, P, P, P, I, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -230,3 +231,25 @@ def moe_float(fmt, H, I, wg, wu, wd, idx, gate, x, want_h=False):
                         C.cast(pd, C.c_void_p), T, k, _p(idx), _p(gate), _p(x), _xkind(x),
                         _p(y), _p(bound), _p(h) if want_h else None)
     return (y, bound, h) if want_h else (y, bound)
+
+
+def moe_q8(fmt, H, I, wg, wu, wd, idx, gate, x):
+    """The expert FFN with quantized activations (the prefill GEMM's
+    arithmetic): returns (y [T][H], tight bound, loose bound)."""
+    _q8_only(fmt)
+    x = np.ascontiguousarray(x)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    gate = np.ascontiguousarray(gate, dtype=np.float64)
+    T, k = idx.shape
+    keep = [np.ascontiguousarray(m) for m in list(wg) + list(wu) + list(wd)]
+    E = len(wg)
+    arr = (C.c_void_p * E)
+    pg = arr(*[m.ctypes.data for m in keep[:E]])
+    pu = arr(*[m.ctypes.data for m in keep[E:2 * E]])
+    pd = arr(*[m.ctypes.data for m in keep[2 * E:]])
+    y = np.empty((T, H), np.float64)
+    tight = np.empty((T, H), np.float64)
+    loose = np.empty((T, H), np.float64)
+    lib().orc_moe_q8(fmt, H, I, C.cast(pg, C.c_void_p), C.cast(pu, C.c_void_p), C.cast(pd, C.c_void_p),
+                     T, k, _p(idx), _p(gate), _p(x), _xkind(x), _p(y), _p(tight), _p(loose))
+    return y, tight, loose

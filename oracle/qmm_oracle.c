@@ -487,3 +487,81 @@ void orc_moe_float(int fmt, int H, int I, const uint8_t* const* wg,
     free(h);
     free(dh);
 }
+
+/* ------------------------------------------------------------------ */
+/* expert-grouped MoE prefill ([LAWS] L-30: prefill divides parameters, */
+/* not bytes): the routed expert FFN of orc_moe_float with every matmul  */
+/* on quantized activations, as the prefill GEMM computes it:            */
+/*   g = W_g (q8 x), u = W_u (q8 x), h = silu(g) * u,                    */
+/*   o = W_d (q8 h), y_t = sum_j gate[t][j] * o_{idx[t][j]}.             */
+/* Reading: h is re-quantized per 32 like any GEMM input; its rounding   */
+/* decisions are taken in fp32 on h rounded to fp32.                     */
+/* ------------------------------------------------------------------ */
+
+/* tight (optional, [T][H]): the bound that holds when every code of the
+ * quantized h equals the oracle's: per expert output 1e-4 * sum|w_d h^| +
+ * 1e-6, gate-weighted. loose (optional, [T][H]): a bound that holds for any
+ * h within its propagated error of the oracle's (the GEMM bar 1e-4 *
+ * sum|w x^| + 1e-6 on g and u, carried through silu with |silu'| <= 1.1):
+ * every code may then be off by one step, so each h element adds
+ * |w_d| * (s + dh + max dh / 254) to it (s its block's scale). */
+void orc_moe_q8(int fmt, int H, int I, const uint8_t* const* wg, const uint8_t* const* wu,
+                const uint8_t* const* wd, int T, int k, const int32_t* idx, const double* gate,
+                const void* x, int xkind, double* y, double* tight, double* loose) {
+    int8_t* xq = (int8_t*)malloc((size_t)H);
+    float* sx = (float*)malloc(sizeof(float) * (size_t)(H / 32));
+    float* hf = (float*)malloc(sizeof(float) * (size_t)I);
+    int8_t* hq = (int8_t*)malloc((size_t)I);
+    float* sh = (float*)malloc(sizeof(float) * (size_t)(I / 32));
+    double* dh = (double*)malloc(sizeof(double) * (size_t)I);
+    double* stepw = (double*)malloc(sizeof(double) * (size_t)I);
+    for (int t = 0; t < T; ++t) {
+        orc_quantize_q8((const uint8_t*)x + (size_t)t * H * (xkind == ORC_X_BF16 ? 2 : 4), xkind, 1, H, xq,
+                        sx);
+        for (int n = 0; n < H; ++n) {
+            y[(int64_t)t * H + n] = 0.0;
+            if (tight) tight[(int64_t)t * H + n] = 0.0;
+            if (loose) loose[(int64_t)t * H + n] = 0.0;
+        }
+        for (int j = 0; j < k; ++j) {
+            int e = idx[t * k + j];
+            double gw = gate[t * k + j];
+            for (int i = 0; i < I; ++i) {
+                double ag, au;
+                double g = orc_dot_q8(fmt, row_ptr(fmt, wg[e], H, i), H, xq, sx, &ag);
+                double u = orc_dot_q8(fmt, row_ptr(fmt, wu[e], H, i), H, xq, sx, &au);
+                double sg = silu(g);
+                hf[i] = (float)(sg * u);
+                double eg = 1e-4 * ag + 1e-6, eu = 1e-4 * au + 1e-6;
+                dh[i] = fabs(u) * 1.1 * eg + (fabs(sg) + 1.1 * eg) * eu + 1e-6 * fabs(sg * u);
+            }
+            orc_quantize_q8(hf, ORC_X_F32, 1, I, hq, sh);
+            for (int b = 0; b < I / 32; ++b) {
+                double mx = 0.0;
+                for (int i = 32 * b; i < 32 * b + 32; ++i)
+                    if (dh[i] > mx) mx = dh[i];
+                for (int i = 32 * b; i < 32 * b + 32; ++i) stepw[i] = (double)sh[b] + dh[i] + mx / 254.0;
+            }
+            for (int n = 0; n < H; ++n) {
+                const uint8_t* row = row_ptr(fmt, wd[e], I, n);
+                double ad;
+                double o = orc_dot_q8(fmt, row, I, hq, sh, &ad);
+                y[(int64_t)t * H + n] += gw * o;
+                double tb = 1e-4 * ad + 1e-6;
+                if (tight) tight[(int64_t)t * H + n] += gw * tb;
+                if (loose) {
+                    double p = 0.0;
+                    for (int i = 0; i < I; ++i) p += fabs(orc_weight(fmt, row, i)) * stepw[i];
+                    loose[(int64_t)t * H + n] += gw * (tb + 1e-4 * p + p);
+                }
+            }
+        }
+    }
+    free(xq);
+    free(sx);
+    free(hf);
+    free(hq);
+    free(sh);
+    free(dh);
+    free(stepw);
+}

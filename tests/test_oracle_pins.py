@@ -515,3 +515,36 @@ def test_moe_identical_experts_sum_of_gates_is_one():
     for t in range(3):
         ref = _dense_ffn(fmt, g0, u0, d0, H, I, synth.bf16_bits_to_f32(x[t]).astype(np.float64))
         assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-15)
+
+
+# --------------------------------------------------------------- MoE prefill (quantized activations)
+
+def _moe_q8_single(fmt, Wg, Wu, Wd, H, I, x_row):
+    """one expert's FFN composed from the pinned primitives: quantize, q8
+    matvec, numpy silu, quantize of fp32 h, q8 matvec"""
+    xq, sx = oracle.quantize_q8(x_row[None, :])
+    g, _ = oracle.gemv_q8(fmt, Wg, xq, sx, I, H)
+    u, _ = oracle.gemv_q8(fmt, Wu, xq, sx, I, H)
+    with np.errstate(over="ignore"):
+        h = (g / (1.0 + np.exp(-g))) * u
+    hq, sh = oracle.quantize_q8(h.astype(np.float32))
+    o, _ = oracle.gemv_q8(fmt, Wd, hq, sh, H, I)
+    return o[0]
+
+
+@pytest.mark.parametrize("fmt", [oracle.Q4_0, oracle.Q6_K])
+def test_moe_q8_is_the_composition_of_pinned_steps(fmt):
+    E, H, I, T, k = 3, 512, 256, 4, 2
+    wg = [synth.matrix(fmt, 60 + e, I, H) for e in range(E)]
+    wu = [synth.matrix(fmt, 70 + e, I, H) for e in range(E)]
+    wd = [synth.matrix(fmt, 80 + e, H, I) for e in range(E)]
+    x = synth.to_bf16_bits(synth.normal_f32(90, (T, H)) * 1000)
+    idx = np.array([[0, 2], [1, 0], [2, 1], [1, 2]], np.int32)
+    gate = np.array([[0.25, 0.75], [0.5, 0.5], [1.0, 0.0], [0.125, 0.875]])
+    y, tight, loose = oracle.moe_q8(fmt, H, I, wg, wu, wd, idx, gate, x)
+    xf = synth.bf16_bits_to_f32(x)
+    for t in range(T):
+        ref = sum(gate[t, j] * _moe_q8_single(fmt, wg[idx[t, j]], wu[idx[t, j]], wd[idx[t, j]], H, I, xf[t])
+                  for j in range(k))
+        assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), t
+    assert (tight > 0).all() and (loose >= tight).all()
