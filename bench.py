@@ -291,6 +291,57 @@ class MoeCase:
         self.qmm.moe(self.qmm.Q4_0, self.experts, self.idx, self.gate, self.x, self.y)
 
 
+def moe_prefill_part(torch, qmm, wts, device, steps, warmup, check, T=4096):
+    """Expert-grouped MoE prefill over MoeWeights: T prompt tokens (bf16
+    N(0,1) x 1000, so that outputs are of order 1 with the synthetic scales),
+    top-8 of 256 N(0,1) router logits. Timed with CUDA events around each
+    call (the call reads the expert counts back to the host, so it is not a
+    graph); 2 sampled tokens checked against the oracle first."""
+    import synth
+    E, H, I, k = wts.E, wts.H, wts.I, wts.k
+    experts = qmm.moe_experts(list(wts.g), list(wts.u), list(wts.d), H, I, k, T)
+    logits = torch.from_numpy(synth.normal_f32(synth.workload_seed(3, 40), (T, E))).to(device)
+    xh = synth.to_bf16_bits(synth.normal_f32(synth.workload_seed(3, 41), (T, H)) * 1000.0)
+    x = torch.from_numpy(xh.view(np.int16)).to(device).view(torch.bfloat16)
+    idx = torch.empty((T, k), dtype=torch.int32, device=device)
+    gate = torch.empty((T, k), dtype=torch.float32, device=device)
+    y = torch.empty((T, H), dtype=torch.float32, device=device)
+    qmm.route_topk_softmax(logits, k, idx, gate)
+    for _ in range(max(1, warmup)):
+        qmm.moe_prefill(qmm.Q4_0, experts, idx, gate, x, y)
+    torch.cuda.synchronize(device)
+    qmm.sync_check()
+    parity = None
+    if check:
+        import oracle
+        ih, gh = idx.cpu().numpy(), gate.cpu().numpy().astype(np.float64)
+        ts = np.array([0, T - 1])
+        used = sorted(set(ih[ts].ravel().tolist()))
+        host = {e: (wts.g[e].cpu().numpy(), wts.u[e].cpu().numpy(), wts.d[e].cpu().numpy()) for e in used}
+        dummy = np.zeros(1, np.uint8)
+        pick = lambda j: [host[e][j] if e in host else dummy for e in range(E)]
+        ref, tight, loose = oracle.moe_q8(FMT_CODE["Q4_0"], H, I, pick(0), pick(1), pick(2), ih[ts], gh[ts], xh[ts])
+        yt = y.cpu().numpy()[ts].astype(np.float64)
+        err = np.abs(yt - ref)
+        parity = {"tokens": len(ts), "max_err_over_loose": float((err / loose).max()),
+                  "frac_within_tight": float((err <= tight).mean()), "ok": bool((err <= loose).all())}
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        qmm.moe_prefill(qmm.Q4_0, experts, idx, gate, x, y)
+        b.record()
+        torch.cuda.synchronize(device)
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    flops = 2.0 * T * k * 3 * H * I
+    distinct = len(set(idx.cpu().numpy().ravel().tolist()))
+    return {"workload": f"{T} tokens, top-{k} of {E} Q4_0 experts (gate/up {I}x{H}, down {H}x{I})",
+            "ms": ms, "tops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
+            "distinct_experts": distinct, "timing": "CUDA events around each call, median of the steps",
+            "parity": parity}
+
+
 def capture(torch, fn, device):
     s = torch.cuda.Stream(device)
     s.wait_stream(torch.cuda.current_stream(device))
@@ -971,6 +1022,7 @@ def main():
     # per-matrix times of the decode set and the equivalent tok/s
     pm_rows, pm_tok = per_matrix(torch, qmm, dec, device, args.steps)
     ladder = format_ladder(torch, qmm, device, args.steps, pk["hbm_gbs"], rank == 0)
+    prefill = moe_prefill_part(torch, qmm, moe_w, device, max(3, args.steps // 4), args.warmup, rank == 0)
 
     # roofline of the part that takes the most time in the step
     hbm = pk["hbm_gbs"]
@@ -1036,6 +1088,7 @@ def main():
             "per_matrix": pm_rows,
             "equivalent_tok_s": pm_tok,
             "format_ladder": ladder,
+            "moe_prefill": prefill,
             "moe": {"t1_gbps": moe_gbs["moe_t1"], "t16_gbps": moe_gbs["moe_t16"],
                     "t16_distinct_experts": moe16.distinct, "t1_bytes": moe1.bytes,
                     "t16_bytes": moe16.bytes},

@@ -25,7 +25,7 @@ LIVE = {
     "gemm_exp_plane": 5, "gemm_in_kernel": 6, "gemm_exp_off": 7, "gemm_fallback": 8,
     "gemm_q4_0": 9, "route": 10, "moe_gate_up": 11, "moe_down": 12, "moe_combine": 13,
     "x_tile": 14, "moe_plan": 15, "moe_gather": 16, "gemv_mv1": 17, "gemv_mv8": 18, "moe_silu": 19,
-    "gemm_split_reduce": 20,
+    "gemm_split_reduce": 20, "moe_prefill_plan": 21, "moe_prefill_rows": 22, "moe_prefill_silu": 23,
 }
 LIVE_COUNT = 24
 
@@ -73,6 +73,8 @@ def _load():
         "qmm_plane_release": (I, [P]),
         "moe_gemv": (I, [U32, C.POINTER(MoeExperts), P, P, P, P]),
         "qmm_moe_workspace_bytes": (SZ, [C.POINTER(MoeExperts)]),
+        "moe_prefill": (I, [U32, C.POINTER(MoeExperts), P, P, P, P]),
+        "qmm_moe_prefill_workspace_bytes": (SZ, [U32, C.POINTER(MoeExperts)]),
         "qmm_route_topk_softmax": (I, [P, I, I, I, P, P]),
         "qmm_liveness_read": (I, [C.POINTER(C.c_int64), I]),
         "qmm_liveness_reset": (I, []),
@@ -278,12 +280,14 @@ def route_topk_softmax(logits, k: int, idx, gate_w):
 
 
 def moe_experts(w_gate, w_up, w_down, hidden: int, inter: int, top_k: int, n_tokens: int):
-    """Host-side expert table (keeps the pointer arrays alive on the object)."""
+    """Host-side expert table (keeps the pointer arrays, and the tensors they
+    point into, alive on the object)."""
     E = len(w_gate)
     arr = C.c_void_p * E
     m = MoeExperts()
     m._keep = (arr(*[t.data_ptr() for t in w_gate]), arr(*[t.data_ptr() for t in w_up]),
                arr(*[t.data_ptr() for t in w_down]))
+    m._tensors = (list(w_gate), list(w_up), list(w_down))  # the device memory the pointers name
     m.n_experts, m.hidden, m.inter, m.top_k, m.n_tokens = E, hidden, inter, top_k, n_tokens
     m.w_gate = C.cast(m._keep[0], C.POINTER(C.c_void_p))
     m.w_up = C.cast(m._keep[1], C.POINTER(C.c_void_p))
@@ -323,3 +327,12 @@ def wait_probe(limit_us: int, device=None):
     _prepare(dev, 0)
     with torch.cuda.device(dev):
         _check(lib.qmm_wait_probe(limit_us))
+
+
+def moe_prefill(fmt: int, experts: MoeExperts, idx, gate_w, x, y):
+    """The routed expert FFN of `moe` for many tokens, grouped by expert
+    through the prefill GEMM (quantized activations); not graph-capturable."""
+    code = fmt | _act_bits(x)
+    _prepare(x.device, lib.qmm_moe_prefill_workspace_bytes(code, C.byref(experts)))
+    with _torch().cuda.device(x.device):
+        _check(lib.moe_prefill(code, C.byref(experts), _ptr(idx), _ptr(gate_w), _ptr(x), _ptr(y)))

@@ -906,6 +906,170 @@ int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const f
     return QMM_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+constexpr int64_t kPrefillMaxSlots = int64_t{1} << 22;
+
+// Workspace of moe_prefill, region by region (each rounded up to 256 B).
+struct PrefillWs {
+    size_t counts, order, pos, xg, g, u, o, a16, xs, part, total;
+};
+
+PrefillWs prefill_ws(int E, int64_t S, int H, int I, bool bf16) {
+    PrefillWs w{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = round_up(off + bytes, 256);
+        return at;
+    };
+    const int64_t Kmax = std::max(H, I);
+    size_t part = 0;
+    for (int64_t M = 128;; M += 128) {
+        const int64_t m = std::min<int64_t>(M, S);
+        part = std::max({part, gemm_part_bytes(m, I, H), gemm_part_bytes(m, H, I)});
+        if (m == S) break;
+    }
+    w.counts = take(static_cast<size_t>(E) * 4);
+    w.order = take(static_cast<size_t>(S) * 4);
+    w.pos = take(static_cast<size_t>(S) * 4);
+    w.xg = take(static_cast<size_t>(S) * H * (bf16 ? 2 : 4));
+    w.g = take(static_cast<size_t>(S) * I * 4);
+    w.u = take(static_cast<size_t>(S) * I * 4);
+    w.o = take(static_cast<size_t>(S) * H * 4);
+    w.a16 = take(gemm_a16_bytes(S, Kmax));
+    w.xs = take(static_cast<size_t>(S) * (Kmax / 32) * 4);
+    w.part = take(part);
+    w.total = off;
+    return w;
+}
+
+int check_prefill(uint32_t fmt, const qmm_moe_t* experts, int* wf, bool* bf16) {
+    bool q8;
+    int rc = check_fmt(fmt, wf, bf16, &q8);
+    if (rc) return rc;
+    if (*wf != QMM_Q4_0 && *wf != QMM_Q6_K)
+        return fail(QMM_EUNSUPPORTED, "moe_prefill supports q6_K and Q4_0 experts (the prefill GEMM's formats)");
+    if (!experts || !experts->w_gate || !experts->w_up || !experts->w_down)
+        return fail(QMM_EINVAL, "null expert table");
+    const qmm_moe_t& m = *experts;
+    if (m.n_experts < 1 || m.n_experts > kMoeMaxExperts)
+        return fail(QMM_EINVAL, "n_experts = %d outside 1..%d", m.n_experts, kMoeMaxExperts);
+    if (m.hidden <= 0 || m.inter <= 0 || m.n_tokens <= 0)
+        return fail(QMM_EINVAL, "hidden, inter and n_tokens must be positive");
+    if (m.top_k < 1 || m.top_k > 32 || m.top_k > m.n_experts)
+        return fail(QMM_EINVAL, "top_k = %d outside 1..min(32, n_experts)", m.top_k);
+    if (static_cast<int64_t>(m.n_tokens) * m.top_k > kPrefillMaxSlots)
+        return fail(QMM_EINVAL, "n_tokens * top_k = %lld exceeds %lld per call",
+                    static_cast<long long>(m.n_tokens) * m.top_k, static_cast<long long>(kPrefillMaxSlots));
+    const int be = std::max(block_elems(*wf), 32);
+    if (m.hidden % be || m.inter % be) return fail(QMM_EALIGN, "hidden and inter must be multiples of %d", be);
+    for (int e = 0; e < m.n_experts; ++e)
+        if (!aligned16(m.w_gate[e]) || !aligned16(m.w_up[e]) || !aligned16(m.w_down[e]) || !m.w_gate[e] ||
+            !m.w_up[e] || !m.w_down[e])
+            return fail(QMM_EALIGN, "expert %d: weights must be non-null and 16-byte aligned", e);
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmm_moe_prefill_workspace_bytes(uint32_t fmt, const qmm_moe_t* experts) {
+    qmm_init();
+    int wf;
+    bool bf16;
+    if (check_prefill(fmt, experts, &wf, &bf16)) return 0;
+    const qmm_moe_t& m = *experts;
+    return prefill_ws(m.n_experts, static_cast<int64_t>(m.n_tokens) * m.top_k, m.hidden, m.inter, bf16).total;
+}
+
+int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const float* gate_w, const void* x,
+                float* y) {
+    qmm_init();
+    int wf;
+    bool bf16;
+    int rc = check_prefill(fmt, experts, &wf, &bf16);
+    if (rc) return rc;
+    if (!idx || !gate_w || !x || !y) return fail(QMM_EINVAL, "null idx, gate_w, x or y");
+    if (!aligned16(x) || !aligned16(y)) return fail(QMM_EALIGN, "x and y must be 16-byte aligned");
+    const qmm_moe_t& m = *experts;
+    const int E = m.n_experts, H = m.hidden, I = m.inter, T = m.n_tokens, k = m.top_k;
+    const int64_t S = static_cast<int64_t>(T) * k;
+    const PrefillWs w = prefill_ws(E, S, H, I, bf16);
+    if (w.total > t_ws_bytes || !t_ws)
+        return fail(QMM_ENOWORKSPACE, "moe_prefill needs %zu bytes of workspace, %zu set", w.total, t_ws_bytes);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(t_stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+        return fail(QMM_EUNSUPPORTED, "moe_prefill reads the expert counts on the host: it cannot be captured");
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    uint8_t* ws = static_cast<uint8_t*>(t_ws);
+    int* counts = reinterpret_cast<int*>(ws + w.counts);
+    int* order = reinterpret_cast<int*>(ws + w.order);
+    int* pos = reinterpret_cast<int*>(ws + w.pos);
+    uint8_t* Xg = ws + w.xg;
+    float* G = reinterpret_cast<float*>(ws + w.g);
+    float* U = reinterpret_cast<float*>(ws + w.u);
+    float* O = reinterpret_cast<float*>(ws + w.o);
+    uint16_t* a16 = reinterpret_cast<uint16_t*>(ws + w.a16);
+    float* xs = reinterpret_cast<float*>(ws + w.xs);
+    float* part = reinterpret_cast<float*>(ws + w.part);
+    const int label = wf == QMM_Q4_0 ? QMM_LIVE_GEMM_Q4_0 : (g_env.exp_on ? QMM_LIVE_GEMM_IN_KERNEL : QMM_LIVE_GEMM_EXP_OFF);
+
+    // the slots by expert, and each expert's count on the host
+    cudaError_t e = moe_prefill_plan_launch(idx, static_cast<int>(S), E, counts, order, pos, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_prefill plan launch");
+    std::vector<int> cnt(static_cast<size_t>(E));
+    e = cudaMemcpyAsync(cnt.data(), counts, static_cast<size_t>(E) * 4, cudaMemcpyDeviceToHost, t_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(t_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_prefill counts");
+    int64_t total = 0;
+    for (int c : cnt) total += c;
+    if (total != S) return fail(QMM_EINVAL, "moe_prefill: %lld of %lld routing slots name an expert outside 0..%d",
+                                static_cast<long long>(S - total), static_cast<long long>(S), E - 1);
+
+    // gate and up: each expert's rows through the prefill GEMM
+    const int64_t xrow = static_cast<int64_t>(H) * (bf16 ? 2 : 4);
+    e = moe_prefill_gather_launch(x, xrow, order, k, static_cast<int>(S), Xg, d->sms, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_prefill gather launch");
+    auto gemm = [&](const void* W, const void* X, bool xb16, float* Y, int64_t M, int64_t N, int64_t K) {
+        cudaError_t r = quantize_q8_launch(X, xb16 ? 1 : 0, M, K, nullptr, xs, a16, t_stream, d->st);
+        if (r == cudaSuccess)
+            r = gemm_launch(wf, false, static_cast<const uint8_t*>(W), nullptr, a16, xs, Y, M, N, K, t_stream, d->st,
+                            label, gemm_part_bytes(M, N, K) ? part : nullptr);
+        return r;
+    };
+    int64_t off = 0;
+    for (int ex = 0; ex < E; ++ex) {
+        const int64_t n = cnt[static_cast<size_t>(ex)];
+        if (n == 0) continue;
+        const uint8_t* Xe = Xg + off * xrow;
+        e = gemm(m.w_gate[ex], Xe, bf16, G + off * I, n, I, H);
+        if (e == cudaSuccess)
+            e = gemm_launch(wf, false, static_cast<const uint8_t*>(m.w_up[ex]), nullptr, a16, xs, U + off * I, n, I,
+                            H, t_stream, d->st, label, gemm_part_bytes(n, I, H) ? part : nullptr);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_prefill gate/up launch");
+        off += n;
+    }
+    // h = silu(g) * u, then down: each expert's h rows through the GEMM
+    e = moe_prefill_silu_launch(G, U, S * I, d->sms, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_prefill silu launch");
+    off = 0;
+    for (int ex = 0; ex < E; ++ex) {
+        const int64_t n = cnt[static_cast<size_t>(ex)];
+        if (n == 0) continue;
+        e = gemm(m.w_down[ex], G + off * I, false, O + off * H, n, H, I);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_prefill down launch");
+        off += n;
+    }
+    e = moe_prefill_combine_launch(O, pos, gate_w, T, k, H, y, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "moe_prefill combine launch");
+    return QMM_OK;
+}
+
 size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts) {
     if (!experts || experts->n_tokens <= 0 || experts->top_k <= 0 || experts->hidden <= 0 ||
         experts->inter <= 0)
@@ -992,7 +1156,7 @@ int qmm_sync_check(void) {
         unsigned int zero = 0;
         cudaMemcpy(d->st.err, &zero, sizeof zero, cudaMemcpyHostToDevice);
         if (err & DERR_MOE_BAD_INDEX)
-            return fail(QMM_EINVAL, "moe_gemv: an expert index was outside 0..n_experts-1; "
+            return fail(QMM_EINVAL, "moe_gemv / moe_prefill: an expert index was outside 0..n_experts-1; "
                                     "its slot contributed nothing (flags 0x%x)", err);
         if (err & DERR_GEMM_SCALE)
             return fail(QMM_EUNSUPPORTED, "qmm_gemm: a q6_K sub-block scale is outside -56..56, "

@@ -251,6 +251,20 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t s, DevState st, int live_slot, float* part);
 
+// ---------------------------------------------------------------- MoE prefill
+// (moe_prefill.cu) the T*k routing slots ordered by expert, stable: counts
+// [E], order [S] (slots by expert), pos [S] (each slot's row in that order)
+cudaError_t moe_prefill_plan_launch(const int32_t* idx, int S, int E, int* counts, int* order, int* pos,
+                                    cudaStream_t s, DevState st);
+// Xg[r] = x row of token order[r] / k (rows of rowbytes, a multiple of 16)
+cudaError_t moe_prefill_gather_launch(const void* x, int64_t rowbytes, const int* order, int k, int S, void* Xg,
+                                      int sms, cudaStream_t s, DevState st);
+// g <- silu(g) * u over n values (n % 4 == 0)
+cudaError_t moe_prefill_silu_launch(float* g, const float* u, int64_t n, int sms, cudaStream_t s, DevState st);
+// y[t] = sum_j gate[t][j] * O[pos[t][j]], j in order (H % 4 == 0)
+cudaError_t moe_prefill_combine_launch(const float* O, const int* pos, const float* gate, int T, int k, int H,
+                                       float* y, cudaStream_t s, DevState st);
+
 // ---------------------------------------------------------------- MoE
 constexpr int kMoeMaxExperts = 1024;
 constexpr int kMoeMaxSlots = 1024;  // tokens x top_k per call

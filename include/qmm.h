@@ -124,6 +124,12 @@ enum {
                                          matvecs on the warp-level MMA       */
     QMM_LIVE_GEMM_SPLIT_REDUCE = 20,  /* sum of a GEMM's K-split partials
                                          (grids with fewer tiles than SMs)   */
+    QMM_LIVE_MOE_PREFILL_PLAN = 21,   /* moe_prefill: slots ordered by
+                                         expert                              */
+    QMM_LIVE_MOE_PREFILL_ROWS = 22,   /* moe_prefill: activation rows
+                                         gathered by expert, and the gated
+                                         sum scattered back (two launches)   */
+    QMM_LIVE_MOE_PREFILL_SILU = 23,   /* moe_prefill: silu(g) * u            */
     QMM_LIVE_COUNT = 24
 };
 
@@ -332,6 +338,32 @@ int moe_gemv(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
 
 /* Workspace moe_gemv needs. */
 size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts);
+
+/* Expert-grouped MoE prefill (quantprobe "LAWS.md", L-30: prefill divides
+ * parameters rather than bytes): the routed expert FFN of moe_gemv for a
+ * prompt's tokens, with each expert's weights read once for all the tokens
+ * that chose it. The T * top_k routing slots are ordered by expert (stable
+ * in slot order), each expert's activation rows gathered into one matrix,
+ * and g = Wg_e X_e, u = Wu_e X_e and o = Wd_e h_e computed by qmm_gemm's
+ * prefill GEMM (activations quantized per 32, exact integer group
+ * partials), with h = silu(g) * u in fp32 quantized per 32 again as the
+ * down projection's input; y[t] = sum_j gate_w[t][j] * o_j, in j order.
+ * Experts: q6_K or Q4_0 (the GEMM's formats), hidden and inter multiples of
+ * 32 (256 for q6_K), each matrix 16-byte aligned (any address, no stride
+ * needed). idx: [T][top_k] int32 device, gate_w: [T][top_k] fp32 device,
+ * x: [T][hidden] fp32 or bf16 (fmt's activation type), y: [T][hidden] fp32;
+ * x and y 16-byte aligned; T * top_k <= 2^22. Needs the workspace
+ * qmm_moe_prefill_workspace_bytes gives. The call reads the per-expert
+ * token counts back to the host (one stream synchronization) to size the
+ * GEMMs, so it cannot be captured in a CUDA graph (QMM_EUNSUPPORTED while
+ * the stream is capturing). An expert index outside 0..n_experts-1 returns
+ * QMM_EINVAL after that synchronization (and sets the device flag
+ * qmm_sync_check reports). Results are bitwise reproducible. */
+int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
+                const float* gate_w, const void* x, float* y);
+
+/* Workspace moe_prefill needs (0 if the arguments are invalid). */
+size_t qmm_moe_prefill_workspace_bytes(uint32_t fmt, const qmm_moe_t* experts);
 
 /* Router helper: per token, the k largest of E fp32 logits (ties go to the
  * lower expert index) and their softmax over those k, the routing of the

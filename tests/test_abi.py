@@ -96,6 +96,32 @@ def test_kquant_formats_only_on_the_fp16_mma_matvec(L):
         assert L.lib.qmm_workspace_bytes(f | L.X_F32, 1, 64, 256) == 0
 
 
+def test_moe_prefill_argument_errors(L):
+    """host-side checks of moe_prefill, before anything is launched"""
+    P = C.c_void_p * 2
+    ptrs = P(FAKE, FAKE)
+    m = L.MoeExperts()
+    m.n_experts, m.hidden, m.inter, m.top_k, m.n_tokens = 2, 256, 128, 1, 4
+    m.w_gate = m.w_up = m.w_down = C.cast(ptrs, C.POINTER(C.c_void_p))
+    ok = L.Q4_0 | L.X_BF16
+    assert _rc(L, "moe_prefill", L.Q8_0 | L.X_BF16, C.byref(m), FAKE, FAKE, FAKE, FAKE)[0] == -2
+    assert _rc(L, "moe_prefill", L.Q4_K | L.X_BF16, C.byref(m), FAKE, FAKE, FAKE, FAKE)[0] == -2
+    assert _rc(L, "moe_prefill", ok, None, FAKE, FAKE, FAKE, FAKE)[0] == -1
+    assert _rc(L, "moe_prefill", ok, C.byref(m), None, FAKE, FAKE, FAKE)[0] == -1
+    assert _rc(L, "moe_prefill", ok, C.byref(m), FAKE, FAKE, MIS, FAKE)[0] == -3
+    m.top_k = 3
+    assert _rc(L, "moe_prefill", ok, C.byref(m), FAKE, FAKE, FAKE, FAKE)[0] == -1   # top_k > n_experts
+    m.top_k, m.hidden = 1, 100
+    assert _rc(L, "moe_prefill", ok, C.byref(m), FAKE, FAKE, FAKE, FAKE)[0] == -3   # hidden % 32
+    assert L.lib.qmm_moe_prefill_workspace_bytes(ok, C.byref(m)) == 0
+    m.hidden = 256
+    misaligned = P(MIS, FAKE)
+    m.w_down = C.cast(misaligned, C.POINTER(C.c_void_p))
+    assert _rc(L, "moe_prefill", ok, C.byref(m), FAKE, FAKE, FAKE, FAKE)[0] == -3
+    m.w_down = C.cast(ptrs, C.POINTER(C.c_void_p))
+    assert L.lib.qmm_moe_prefill_workspace_bytes(ok, C.byref(m)) > 0
+
+
 def test_quantize_and_plane_argument_errors(L):
     assert _rc(L, "qmm_quantize_q8", 0x300, FAKE, 4, 64, FAKE, FAKE)[0] == -1
     assert _rc(L, "qmm_quantize_q8", 0x100, FAKE, 4, 48, FAKE, FAKE)[0] == -3
