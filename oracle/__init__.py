@@ -70,6 +70,8 @@ def lib():
             "orc_route_topk_softmax": (None, [P, I, I, I, P, P]),
             "orc_moe_float": (None, [I, I, I, P, P, P, I, I, P, P, P, I, P, P, P]),
             "orc_moe_q8": (None, [I, I, I, P, P, P, I, I, P, P, P, I, P, P, P]),
+            "orc_cbk_weight": (D, [I, P, P, P, I64, I64, I64]),
+            "orc_cbk_gemv": (None, [I, P, P, P, I64, I64, P, I, I, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -253,3 +255,23 @@ def moe_q8(fmt, H, I, wg, wu, wd, idx, gate, x):
     lib().orc_moe_q8(fmt, H, I, C.cast(pg, C.c_void_p), C.cast(pu, C.c_void_p), C.cast(pd, C.c_void_p),
                      T, k, _p(idx), _p(gate), _p(x), _xkind(x), _p(y), _p(tight), _p(loose))
     return y, tight, loose
+
+
+def cbk_dequant(M, codes, books, scales, N, K):
+    """Dense [N][K] weights of an additive-codebook matrix (codes [N][K/8][M]
+    uint8, books [M][256][8] fp16 bits, scales [N] fp16 bits)."""
+    c, bk, sc = (np.ascontiguousarray(codes, np.uint8), np.ascontiguousarray(books, np.uint16),
+                 np.ascontiguousarray(scales, np.uint16))
+    return np.array([[lib().orc_cbk_weight(M, _p(c), _p(bk), _p(sc), K, n, k) for k in range(K)]
+                     for n in range(N)])
+
+
+def cbk_gemv(M, codes, books, scales, x, N, K):
+    """x: [B][K] float32 or bf16 bits -> (y [B][N] float64, tolerance scale)."""
+    x = np.ascontiguousarray(x)
+    B = x.shape[0]
+    y = np.empty((B, N), np.float64)
+    a = np.empty((B, N), np.float64)
+    lib().orc_cbk_gemv(M, _p(np.ascontiguousarray(codes, np.uint8)), _p(np.ascontiguousarray(books, np.uint16)),
+                       _p(np.ascontiguousarray(scales, np.uint16)), N, K, _p(x), _xkind(x), B, _p(y), _p(a))
+    return y, a

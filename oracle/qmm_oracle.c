@@ -27,6 +27,9 @@
  *   [X100]    "Chasing x100", "Where the wall actually fell: inversion"
  *             (routed experts kept resident and decoded in place; top-k
  *             routed expert FFN per token).
+ *   [CBK]     "Chasing x100", "The kernel is ready" (a 2-bit and a 3-bit
+ *             additive codebook matvec, checked against a bit-faithful CPU
+ *             reference).
  *   [L16]     quantprobe "LAWS.md", Law 4, the per-format eta paragraph and
  *             amendment L-16 (metadata application density: Q2_K applies a
  *             scale and a min every 16 weights = 4 bytes at 2 bits, Q4_K
@@ -564,4 +567,55 @@ void orc_moe_q8(int fmt, int H, int I, const uint8_t* const* wg, const uint8_t* 
     free(sh);
     free(dh);
     free(stepw);
+}
+
+/* ------------------------------------------------------------------ */
+/* additive-codebook matrix ([CBK]). The pages give no layout; the one   */
+/* read here: M (2 or 3) codebooks of 256 entries of 8 fp16 values,      */
+/* books[m][c][j]; codes[n][g][m] one byte per codebook per group of 8   */
+/* consecutive weights; an fp16 scale per row. Weight 8g + j of row n:   */
+/*   w = scale[n] * sum_m books[m][codes[n][g][m]][j]                    */
+/* (2 bits per weight for M = 2, 3 for M = 3, plus the shared books).    */
+/* ------------------------------------------------------------------ */
+
+/* the M terms of weight k of row n (each an exact double) */
+static void cbk_terms(int M, const uint8_t* codes, const uint16_t* books, const uint16_t* scales,
+                      int64_t K, int64_t n, int64_t k, double* t) {
+    int64_t g = k / 8;
+    int j = (int)(k % 8);
+    double s = orc_half_to_double(scales[n]);
+    for (int m = 0; m < M; ++m) {
+        int c = codes[(n * (K / 8) + g) * M + m];
+        t[m] = s * orc_half_to_double(books[((int64_t)m * 256 + c) * 8 + j]);
+    }
+}
+
+double orc_cbk_weight(int M, const uint8_t* codes, const uint16_t* books, const uint16_t* scales, int64_t K,
+                      int64_t n, int64_t k) {
+    double t[3], w = 0.0;
+    cbk_terms(M, codes, books, scales, K, n, k, t);
+    for (int m = 0; m < M; ++m) w += t[m];
+    return w;
+}
+
+/* y[b][n] = sum_k w[n][k] x[b][k] in double; absum the tolerance scale:
+ * sum_k sum_m |term_m| |x| (the kernel sums the codebooks' terms apart) */
+void orc_cbk_gemv(int M, const uint8_t* codes, const uint16_t* books, const uint16_t* scales, int64_t N,
+                  int64_t K, const void* x, int xkind, int B, double* y, double* absum) {
+    for (int b = 0; b < B; ++b)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, a = 0.0, t[3];
+            for (int64_t k = 0; k < K; ++k) {
+                double xv = load_x(x, xkind, (int64_t)b * K + k);
+                cbk_terms(M, codes, books, scales, K, n, k, t);
+                double w = 0.0;
+                for (int m = 0; m < M; ++m) {
+                    w += t[m];
+                    a += fabs(t[m]) * fabs(xv);
+                }
+                acc += w * xv;
+            }
+            y[b * N + n] = acc;
+            if (absum) absum[b * N + n] = a;
+        }
 }

@@ -20,6 +20,8 @@ Value distributions (per block of each format):
       6-bit scale and min uniform on 0..63, every code on 0..15).
   Q2_K (84 B):  16 + 64 uniform bytes (every 4-bit scale and min uniform on
       0..15, every code on 0..3), then d and dmin as d above.
+  additive codebooks: codes uniform bytes; codebook entries fp16(N(0,1) *
+      0.05); row scales fp16(0.5 + U(0,1)).
   activations:  N(0,1) as float32, or rounded to bfloat16 (ties to even).
 """
 from __future__ import annotations
@@ -204,3 +206,14 @@ def matrix_torch(fmt: int, seed: int, N: int, K: int, device, count: int = 1):
         out[:, :, 2:34] = qs.view(torch.uint8)
         out[:, :, 0:2] = d_bytes
     return out.view(count, nb * bb)
+
+
+def cbk_matrix(seed: int, M: int, N: int, K: int):
+    """An N x K additive-codebook matrix with M codebooks: (codes [N][K/8][M]
+    uint8, books [M][256][8] fp16 bits, scales [N] fp16 bits)."""
+    assert K % 8 == 0 and M in (2, 3)
+    codes = uniform_bytes(substream(seed, 1), N * (K // 8) * M).reshape(N, K // 8, M)
+    books = (normals(substream(seed, 2), M * 256 * 8) * 0.05).astype(np.float16).view(np.uint16).reshape(M, 256, 8)
+    u = (splitmix64(substream(seed, 3), N) >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+    scales = (0.5 + u).astype(np.float16).view(np.uint16)
+    return codes, books, scales

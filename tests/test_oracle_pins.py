@@ -548,3 +548,68 @@ def test_moe_q8_is_the_composition_of_pinned_steps(fmt):
                   for j in range(k))
         assert np.allclose(y[t], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max()), t
     assert (tight > 0).all() and (loose >= tight).all()
+
+
+# --------------------------------------------------------------- additive codebooks
+
+def _f16bits(vals):
+    return np.asarray(vals, np.float64).astype(np.float16).view(np.uint16)
+
+
+def test_cbk_hand_matrix():
+    """M = 2, one row of two groups, scale 2, hand-derived weights"""
+    books = np.zeros((2, 256, 8))
+    books[0, 3] = [1, 2, 3, 4, 0.5, 0.25, -1, -2]
+    books[0, 200] = [0.125, 0, 0, 0, 0, 0, 0, 8]
+    books[1, 7] = [-1, -1, -1, -1, 1, 1, 1, 1]
+    books[1, 255] = [0, 0.5, 0, 0.5, 0, 0.5, 0, 0.5]
+    codes = np.array([[[3, 7], [200, 255]]], np.uint8)
+    w = oracle.cbk_dequant(2, codes, _f16bits(books), _f16bits([2.0]), 1, 16)[0]
+    assert list(w) == [0, 2, 4, 6, 3, 2.5, 0, -2, 0.25, 1, 0, 1, 0, 1, 0, 17]
+
+
+@pytest.mark.parametrize("M", [2, 3])
+def test_cbk_one_hot_books_reveal_the_codes(M):
+    """book 0 entry c = (c + 1) at position c % 8, the other books zero: each
+    weight shows which code of which group the layout picked"""
+    N, K = 3, 64
+    books = np.zeros((M, 256, 8))
+    for c in range(256):
+        books[0, c, c % 8] = c + 1
+    rng = np.random.default_rng(M)
+    codes = rng.integers(0, 256, (N, K // 8, M)).astype(np.uint8)
+    w = oracle.cbk_dequant(M, codes, _f16bits(books), _f16bits([1.0, 0.5, 4.0]), N, K)
+    sc = [1.0, 0.5, 4.0]
+    for n in range(N):
+        for g in range(K // 8):
+            c = int(codes[n, g, 0])
+            expect = np.zeros(8)
+            expect[c % 8] = sc[n] * (c + 1)
+            assert np.array_equal(w[n, 8 * g:8 * g + 8], expect), (n, g)
+
+
+def test_cbk_books_add_and_scales_multiply():
+    """three books = the sum of the one-book matrices; a row's scale
+    multiplies its weights"""
+    codes, books, scales = synth.cbk_matrix(9, 3, 4, 128)
+    w3 = oracle.cbk_dequant(3, codes, books, scales, 4, 128)
+    parts = []
+    for m in range(3):
+        bm = np.zeros_like(books)
+        bm[0] = books[m]
+        cm = np.zeros_like(codes[:, :, :2])
+        cm[:, :, 0] = codes[:, :, m]
+        parts.append(oracle.cbk_dequant(2, cm, bm[:2], scales, 4, 128))
+    assert np.allclose(w3, parts[0] + parts[1] + parts[2], rtol=0, atol=1e-15)
+    s2 = _f16bits(2.0 * scales.view(np.float16).astype(np.float64))
+    assert np.array_equal(oracle.cbk_dequant(3, codes, books, s2, 4, 128), 2.0 * w3)
+
+
+@pytest.mark.parametrize("M", [2, 3])
+def test_cbk_gemv_brute_force(M):
+    codes, books, scales = synth.cbk_matrix(11 + M, M, 5, 256)
+    w = oracle.cbk_dequant(M, codes, books, scales, 5, 256)
+    x = synth.normal_f32(12, (3, 256))
+    y, a = oracle.cbk_gemv(M, codes, books, scales, x, 5, 256)
+    assert np.allclose(y, x.astype(np.float64) @ w.T, rtol=1e-12, atol=1e-15)
+    assert (a >= np.abs(x.astype(np.float64)) @ np.abs(w).T * (1 - 1e-12)).all()
