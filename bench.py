@@ -291,6 +291,60 @@ class MoeCase:
         self.qmm.moe(self.qmm.Q4_0, self.experts, self.idx, self.gate, self.x, self.y)
 
 
+class CbkRun:
+    """qmm_cbk_gemv calls over rotated copies of one additive-codebook
+    matrix's codes (the books and scales shared), captured in one graph."""
+
+    def __init__(self, torch, qmm, M, codes, books, scales, x, N, K, device):
+        self.torch, self.device = torch, device
+        self.codes, self.n = rotated(torch, codes)
+        self.books, self.scales = books, scales
+        self.y = torch.empty((x.shape[0], N), dtype=torch.float32, device=device)
+
+        def fn():
+            for i in range(self.n):
+                qmm.cbk_gemv(M, self.codes[i], books, scales, x, self.y, N, K)
+        self.g = capture(torch, fn, device)
+
+    def time_us(self, steps):
+        return 1e3 * time_graph(self.torch, self.g, steps, self.device) / self.n
+
+
+def cbk_ladder(torch, qmm, device, steps, hbm, check):
+    """The additive-codebook matvec ("Chasing x100", "The kernel is ready")
+    at the ladder's shapes, 2 and 3 books (2 and 3 bits per weight)."""
+    import synth
+    rows = []
+    for label, N, K in LADDER_SHAPES:
+        for M in (2, 3):
+            codes, books, scales = synth.cbk_matrix(0xCB0 + M + N, M, N, K)
+            ct = torch.from_numpy(codes.reshape(-1)).to(device)
+            bt = torch.from_numpy(books.view(np.int16)).to(device)
+            st_ = torch.from_numpy(scales.view(np.int16)).to(device)
+            cb = codes.nbytes + books.nbytes + scales.nbytes
+            for B in BATCHES:
+                xf = synth.normal_f32(0xCB1 + B + K, (B, K))
+                xt = torch.from_numpy(synth.to_bf16_bits(xf).view(np.int16)).to(device).view(torch.bfloat16)
+                run = CbkRun(torch, qmm, M, ct, bt, st_, xt, N, K, device)
+                for _ in range(3):
+                    run.g.replay()
+                parity = None
+                if check:
+                    import oracle
+                    rng = np.random.default_rng(N + B + M)
+                    ns = np.sort(rng.integers(0, N, 32))
+                    ref, absum = oracle.cbk_gemv(M, codes[ns], books, scales[ns], synth.to_bf16_bits(xf), len(ns), K)
+                    worst = _worst(run.y.cpu().numpy()[:, ns], ref, 1e-4 * absum + 1e-6)
+                    parity = {"outputs": int(ref.size), "max_err_over_bound": worst, "ok": bool(worst <= 1.0)}
+                t = run.time_us(max(5, steps // 2))
+                gbps = cb / (t * 1e-6) / 1e9
+                rows.append({"shape": label, "format": f"additive codebook, {M} books", "bits_per_weight": 8.0 * cb / (N * K),
+                             "batch": B, "us": t, "gbps": gbps, "gweights_per_s": N * K / (t * 1e-6) / 1e9,
+                             "eta": gbps / hbm, "copies": run.n, "parity": parity})
+                del run
+    return rows
+
+
 def moe_prefill_part(torch, qmm, wts, device, steps, warmup, check, T=4096):
     """Expert-grouped MoE prefill over MoeWeights: T prompt tokens (bf16
     N(0,1) x 1000, so that outputs are of order 1 with the synthetic scales),
@@ -1022,6 +1076,7 @@ def main():
     # per-matrix times of the decode set and the equivalent tok/s
     pm_rows, pm_tok = per_matrix(torch, qmm, dec, device, args.steps)
     ladder = format_ladder(torch, qmm, device, args.steps, pk["hbm_gbs"], rank == 0)
+    ladder += cbk_ladder(torch, qmm, device, args.steps, pk["hbm_gbs"], rank == 0)
     prefill = moe_prefill_part(torch, qmm, moe_w, device, max(3, args.steps // 4), args.warmup, rank == 0)
 
     # roofline of the part that takes the most time in the step

@@ -26,8 +26,9 @@ LIVE = {
     "gemm_q4_0": 9, "route": 10, "moe_gate_up": 11, "moe_down": 12, "moe_combine": 13,
     "x_tile": 14, "moe_plan": 15, "moe_gather": 16, "gemv_mv1": 17, "gemv_mv8": 18, "moe_silu": 19,
     "gemm_split_reduce": 20, "moe_prefill_plan": 21, "moe_prefill_rows": 22, "moe_prefill_silu": 23,
+    "cbk_gemv": 24,
 }
-LIVE_COUNT = 24
+LIVE_COUNT = 32
 
 BLOCK_ELEMS = {Q4_0: 32, Q8_0: 32, Q6_K: 256, Q4_K: 256, Q2_K: 256}
 BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q6_K: 210, Q4_K: 144, Q2_K: 84}
@@ -74,6 +75,8 @@ def _load():
         "moe_gemv": (I, [U32, C.POINTER(MoeExperts), P, P, P, P]),
         "qmm_moe_workspace_bytes": (SZ, [C.POINTER(MoeExperts)]),
         "moe_prefill": (I, [U32, C.POINTER(MoeExperts), P, P, P, P]),
+        "qmm_cbk_gemv": (I, [I, P, P, P, U32, P, P, I64, I64, I]),
+        "qmm_cbk_workspace_bytes": (SZ, [I, I64, I64, I]),
         "qmm_moe_prefill_workspace_bytes": (SZ, [U32, C.POINTER(MoeExperts)]),
         "qmm_route_topk_softmax": (I, [P, I, I, I, P, P]),
         "qmm_liveness_read": (I, [C.POINTER(C.c_int64), I]),
@@ -336,3 +339,13 @@ def moe_prefill(fmt: int, experts: MoeExperts, idx, gate_w, x, y):
     _prepare(x.device, lib.qmm_moe_prefill_workspace_bytes(code, C.byref(experts)))
     with _torch().cuda.device(x.device):
         _check(lib.moe_prefill(code, C.byref(experts), _ptr(idx), _ptr(gate_w), _ptr(x), _ptr(y)))
+
+
+def cbk_gemv(n_books: int, codes, books, scales, x, y, N: int, K: int):
+    """y[B][N] = the additive-codebook matrix (codes uint8 [N][K/8][n_books],
+    books fp16 bits [n_books][256][8], scales fp16 bits [N]) times x[B][K]."""
+    B = x.shape[0]
+    xt = _act_bits(x)
+    _prepare(x.device, lib.qmm_cbk_workspace_bytes(n_books, N, K, B))
+    with _torch().cuda.device(x.device):
+        _check(lib.qmm_cbk_gemv(n_books, _ptr(codes), _ptr(books), _ptr(scales), xt, _ptr(x), _ptr(y), N, K, B))

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqmm.so")
 
 SOURCES = ["api.cu", "gemv.cu", "tcmv.cu", "tcmv_q6k.cu", "tcmv_q4_0.cu", "tcmv_q8_0.cu", "gemm.cu", "mv1.cu", "mv8.cu", "mvh.cu",
-           "moe.cu", "moe_prefill.cu"]
+           "moe.cu", "moe_prefill.cu", "cbk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]

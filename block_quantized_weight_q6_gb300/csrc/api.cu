@@ -1070,6 +1070,50 @@ int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, cons
     return QMM_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+int check_cbk(int M, int64_t N, int64_t K, int B) {
+    if (M != 2 && M != 3) return fail(QMM_EINVAL, "n_books = %d: 2 or 3 codebooks", M);
+    if (N <= 0 || K <= 0) return fail(QMM_EINVAL, "N %lld and K %lld must be positive", (long long)N, (long long)K);
+    if (B < 1 || B > 8) return fail(QMM_EINVAL, "B = %d outside 1..8", B);
+    if (K % 128) return fail(QMM_EALIGN, "K = %lld is not a multiple of 128", (long long)K);
+    if (N > (int64_t{1} << 31) / 8) return fail(QMM_EINVAL, "N = %lld too large", (long long)N);
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qmm_cbk_workspace_bytes(int n_books, int64_t N, int64_t K, int B) {
+    qmm_init();
+    if (check_cbk(n_books, N, K, B)) return 0;
+    return round_up(cbk_part_bytes(n_books, N, K, B), 256);
+}
+
+int qmm_cbk_gemv(int n_books, const uint8_t* codes, const uint16_t* books, const uint16_t* scales, uint32_t x_type,
+                 const void* x, float* y, int64_t N, int64_t K, int B) {
+    qmm_init();
+    int rc = check_cbk(n_books, N, K, B);
+    if (rc) return rc;
+    if (x_type != QMM_X_F32 && x_type != QMM_X_BF16) return fail(QMM_EINVAL, "x_type 0x%x", x_type);
+    if (!codes || !books || !scales || !x || !y) return fail(QMM_EINVAL, "null pointer");
+    if (!aligned16(codes) || !aligned16(books) || !aligned16(x) || (reinterpret_cast<uintptr_t>(y) & 3u) ||
+        (reinterpret_cast<uintptr_t>(scales) & 1u))
+        return fail(QMM_EALIGN, "codes, books and x must be 16-byte aligned, y 4-byte, scales 2-byte");
+    const size_t need = round_up(cbk_part_bytes(n_books, N, K, B), 256);
+    if (need > t_ws_bytes || !t_ws)
+        return fail(QMM_ENOWORKSPACE, "qmm_cbk_gemv needs %zu bytes of workspace, %zu set", need, t_ws_bytes);
+    DevInfo* d;
+    if ((rc = dev_info(&d))) return rc;
+    cudaError_t e = cbk_launch(n_books, codes, books, scales, x, x_type == QMM_X_BF16 ? 1 : 0, y, N, K, B,
+                               static_cast<float*>(t_ws), d->sms, t_stream, d->st);
+    if (e != cudaSuccess) return cuda_fail(e, "cbk launch");
+    return QMM_OK;
+}
+
 size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts) {
     if (!experts || experts->n_tokens <= 0 || experts->top_k <= 0 || experts->hidden <= 0 ||
         experts->inter <= 0)

@@ -265,6 +265,14 @@ cudaError_t moe_prefill_silu_launch(float* g, const float* u, int64_t n, int sms
 cudaError_t moe_prefill_combine_launch(const float* O, const int* pos, const float* gate, int T, int k, int H,
                                        float* y, cudaStream_t s, DevState st);
 
+// ---------------------------------------------------------------- additive codebooks
+// (cbk.cu) partial-sum bytes of the launch, and the launch itself
+size_t cbk_part_bytes(int M, int64_t N, int64_t K, int B);
+size_t cbk_smem_bytes(int M, int B);
+cudaError_t cbk_launch(int M, const uint8_t* codes, const uint16_t* books, const uint16_t* scales, const void* x,
+                       int x_bf16, float* y, int64_t N, int64_t K, int B, float* part, int sms, cudaStream_t s,
+                       DevState st);
+
 // ---------------------------------------------------------------- MoE
 constexpr int kMoeMaxExperts = 1024;
 constexpr int kMoeMaxSlots = 1024;  // tokens x top_k per call

@@ -130,7 +130,9 @@ enum {
                                          gathered by expert, and the gated
                                          sum scattered back (two launches)   */
     QMM_LIVE_MOE_PREFILL_SILU = 23,   /* moe_prefill: silu(g) * u            */
-    QMM_LIVE_COUNT = 24
+    QMM_LIVE_CBK_GEMV = 24,           /* qmm_cbk_gemv: the table-lookup
+                                         launch and its fixed-order sum      */
+    QMM_LIVE_COUNT = 32
 };
 
 /* Reads the environment once: QMM_Q6K_EXP ("0" opts out of building W_exp
@@ -364,6 +366,28 @@ int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
 
 /* Workspace moe_prefill needs (0 if the arguments are invalid). */
 size_t qmm_moe_prefill_workspace_bytes(uint32_t fmt, const qmm_moe_t* experts);
+
+/* Matvec against an additive-codebook matrix ("Chasing x100", "The kernel
+ * is ready": the 2-bit and 3-bit additive codebook matvec). The pages give
+ * no layout; the one read here: n_books (2 or 3) codebooks of 256 entries,
+ * each 8 fp16 values, books[m][c][j] ([n_books][256][8] fp16, device);
+ * codes[n][g][m], one byte per book for each group of 8 consecutive weights
+ * of row n ([N][K/8][n_books] uint8, device); scales[n] one fp16 per row
+ * (device). Weight 8g + j of row n is scale[n] * sum_m books[m][codes[n][g]
+ * [m]][j], so a weight costs 2 (n_books = 2) or 3 bits plus the shared
+ * books. y[b][n] = sum_k w[n][k] * x[b][k] for b < B <= 8; x: [B][K] of
+ * x_type (QMM_X_F32 or QMM_X_BF16), y: [B][N] fp32 (overwritten). K % 128
+ * == 0; codes, books, x 16-byte aligned. The kernel builds, per chunk of K,
+ * the table of every book entry's dot with each 8-wide activation slice
+ * (fp32) and sums table entries; chunk sums are added in a fixed order, so
+ * results are bitwise reproducible and within 1e-4 * sum_k sum_m |scale *
+ * book term * x| + 1e-6 of the exact product. Needs the workspace
+ * qmm_cbk_workspace_bytes gives. */
+int qmm_cbk_gemv(int n_books, const uint8_t* codes, const uint16_t* books, const uint16_t* scales,
+                 uint32_t x_type, const void* x, float* y, int64_t N, int64_t K, int B);
+
+/* Workspace qmm_cbk_gemv needs (0 if the arguments are invalid). */
+size_t qmm_cbk_workspace_bytes(int n_books, int64_t N, int64_t K, int B);
 
 /* Router helper: per token, the k largest of E fp32 logits (ties go to the
  * lower expert index) and their softmax over those k, the routing of the

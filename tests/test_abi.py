@@ -137,7 +137,7 @@ def test_quantize_and_plane_argument_errors(L):
 def test_liveness_read_argument_errors(L):
     buf = (C.c_int64 * 32)()
     assert _rc(L, "qmm_liveness_read", None, 4)[0] == -1
-    assert _rc(L, "qmm_liveness_read", buf, 25)[0] == -1
+    assert _rc(L, "qmm_liveness_read", buf, 33)[0] == -1
 
 
 def _gate_in_fresh_process(env_value):
