@@ -904,6 +904,38 @@ def run_profile(args):
         case = MoeCase(torch, device, MoeWeights(torch, device, ne), 1 if part[0] == "moe_t1" else 16)
         print(json.dumps({"moe_distinct_experts": case.distinct, "expert_bytes": case.expert_bytes}))
         fn = case.run
+    elif part[0] == "moe_prefill":
+        # E experts (default 16) and 16 E tokens top-8: about 128 tokens per
+        # expert, as in the bench's 4096-token case, in a capture-sized run
+        import synth
+        import block_quantized_weight_q6_gb300 as qmm
+        wts = MoeWeights(torch, device, int(part[1]) if len(part) > 1 else 16)
+        T = 16 * wts.E
+        experts = qmm.moe_experts(list(wts.g), list(wts.u), list(wts.d), wts.H, wts.I, wts.k, T)
+        logits = torch.from_numpy(synth.normal_f32(synth.workload_seed(3, 40), (T, wts.E))).to(device)
+        xh = synth.to_bf16_bits(synth.normal_f32(synth.workload_seed(3, 41), (T, wts.H)) * 1000.0)
+        x = torch.from_numpy(xh.view(np.int16)).to(device).view(torch.bfloat16)
+        idx = torch.empty((T, wts.k), dtype=torch.int32, device=device)
+        gate = torch.empty((T, wts.k), dtype=torch.float32, device=device)
+        y = torch.empty((T, wts.H), dtype=torch.float32, device=device)
+        qmm.route_topk_softmax(logits, wts.k, idx, gate)
+
+        def fn():
+            qmm.moe_prefill(qmm.Q4_0, experts, idx, gate, x, y)
+    elif part[0] == "cbk":
+        # the additive-codebook matvec: cbk:M:B on the 4096 x 4096 shape
+        import synth
+        import block_quantized_weight_q6_gb300 as qmm
+        M, B = (int(part[1]), int(part[2])) if len(part) > 2 else (2, 1)
+        codes, books, scales = synth.cbk_matrix(0xCB0 + M + 4096, M, 4096, 4096)
+        ct = torch.from_numpy(codes.reshape(-1)).to(device)
+        bt = torch.from_numpy(books.view(np.int16)).to(device)
+        st_ = torch.from_numpy(scales.view(np.int16)).to(device)
+        xt = torch.from_numpy(synth.normal_bf16(0xCB1 + B, (B, 4096)).view(np.int16)).to(device).view(torch.bfloat16)
+        y = torch.empty((B, 4096), dtype=torch.float32, device=device)
+
+        def fn():
+            qmm.cbk_gemv(M, ct, bt, st_, xt, y, 4096, 4096)
     else:
         raise SystemExit(f"unknown part {args.profile}")
     for _ in range(args.warmup + args.steps):

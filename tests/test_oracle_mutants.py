@@ -29,6 +29,9 @@ MUTANTS = {
                   "(qs[32 * (i / 128) + i % 32] >> (2 * ((i % 64) / 16)))"),
     "q2k_min_nibble": ("*min = blk[j] >> 4;", "*min = blk[j] & 15;"),
     "kq_min_sign": ("return pos - neg;", "return pos + neg;"),
+    "cbk_code_order": ("int c = codes[(n * (K / 8) + g) * M + m];", "int c = codes[(n * (K / 8) + m) * M + g % M];"),
+    "cbk_lane_flip": ("t[m] = s * orc_half_to_double(books[((int64_t)m * 256 + c) * 8 + j]);",
+                      "t[m] = s * orc_half_to_double(books[((int64_t)m * 256 + c) * 8 + (7 - j)]);"),
 }
 
 
@@ -75,6 +78,20 @@ def _pins_pass(L) -> bool:
         blk = packer(kc, ks, km, pack.f16_bits(0.5), pack.f16_bits(0.25))
         e = np.arange(256) // sub
         if not np.array_equal(_dequant(L, fmt, blk, 256), 0.5 * ks[e] * kc - 0.25 * km[e]):
+            return False
+    # additive codebooks: one-hot books reveal the code and lane order
+    cb = np.zeros((2, 256, 8))
+    for c in range(256):
+        cb[0, c, c % 8] = c + 1
+    cbits = cb.astype(np.float16).view(np.uint16)
+    codes = rng.integers(0, 256, (1, 4, 2)).astype(np.uint8)
+    sc = np.array([1.0], np.float16).view(np.uint16)
+    L.orc_cbk_weight.restype = C.c_double
+    L.orc_cbk_weight.argtypes = [C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int64]
+    for k in range(32):
+        c = int(codes[0, k // 8, 0])
+        want = (c + 1.0) if k % 8 == c % 8 else 0.0
+        if L.orc_cbk_weight(2, codes.ctypes.data, cbits.ctypes.data, sc.ctypes.data, 32, 0, k) != want:
             return False
     x = np.array([[127, 2.5, -2.5, 3.5] + [0.0] * 28], np.float32)
     xq = np.empty((1, 32), np.int8)
