@@ -80,6 +80,26 @@ def test_moe_small_vs_oracle(fmt, E, H, I, T, k):
     assert (err <= bound).all(), (err / bound).max()
 
 
+@pytest.mark.parametrize("fmt,E,H,I", SMALL)
+@pytest.mark.parametrize("T,k", [(1, 4), (16, 4)])
+def test_moe_small_vs_oracle_outputs_of_order_one(fmt, E, H, I, T, k):
+    """activations N(0,1) * 1000: with the synthetic scales the outputs are
+    then of order 1, so the relative part of the propagated bound (not its
+    1e-6 floor) is what the comparison tests"""
+    wg = [synth.matrix(fmt, 800 + e, I, H) for e in range(E)]
+    wu = [synth.matrix(fmt, 820 + e, I, H) for e in range(E)]
+    wd = [synth.matrix(fmt, 840 + e, H, I) for e in range(E)]
+    x = synth.to_bf16_bits(synth.normal_f32(860 + T, (T, H)) * 1000.0)
+    logits = synth.normal_f32(861 + T, (T, E))
+    idx, gate = oracle.route_topk_softmax(logits, k)
+    y = run_moe(fmt, [dev(w) for w in wg], [dev(w) for w in wu], [dev(w) for w in wd], H, I, idx,
+                gate.astype(np.float32), x)
+    ref, bound = oracle.moe_float(fmt, H, I, wg, wu, wd, idx, gate.astype(np.float32).astype(np.float64), x)
+    assert np.abs(ref).max() > 1.0 and bound.min() > 1e-4  # the 1e-6 floor is under 1% of every bound
+    err = np.abs(y.astype(np.float64) - ref)
+    assert (err <= bound).all(), (err / bound).max()
+
+
 def test_moe_all_tokens_on_one_expert():
     """one expert chosen by every token (tasks of 2 tokens, odd tail)"""
     fmt, E, H, I, T = synth.Q4_0, 4, 256, 128, 7
