@@ -104,6 +104,7 @@ struct MvhMat {
     float* y;             // [B][N]
     int64_t N, K, rowbytes;
     int fmt, stages, item0;
+    int stage_bytes, stage_k, box_w, boxes;  // the format's stage shape, set by the host
 };
 struct MvhGroup {
     CUtensorMap map[kMvhMaxMats];  // W as [N / 8][8 * rowbytes] 16-bit elements, boxes 32 rows high

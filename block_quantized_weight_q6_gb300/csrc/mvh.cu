@@ -120,11 +120,13 @@ cudaError_t prepare_kernel() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(mvh_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(kMvhSmem));
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(mvh_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       cudaSharedmemCarveoutMaxShared);
+        for (auto k : {mvh_kernel<false>, mvh_kernel<true>}) {
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMvhSmem));
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           cudaSharedmemCarveoutMaxShared);
+        }
     });
     return err;
 }
@@ -195,6 +197,10 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
         a.fmt = fmt[m];
         a.rowbytes = K[m] / block_elems(a.fmt) * block_bytes(a.fmt);
         a.stages = static_cast<int>(K[m] / (a.fmt == FMT_Q8_0 ? 128 : 256));
+        a.stage_bytes = mvh_stage_bytes(a.fmt);
+        a.stage_k = mvh_stage_k(a.fmt);
+        a.box_w = static_cast<int>(mvh_box_w(a.fmt));
+        a.boxes = mvh_boxes(a.fmt);
         a.item0 = static_cast<int>(items);
         items += (N[m] + 8 * kMvhRows - 1) / (8 * kMvhRows) * 8;
         min_stages = std::min(min_stages, a.stages);
@@ -221,7 +227,9 @@ cudaError_t mvh_run(int n, const int* sel, const int* fmt, const void* const* W,
     }
     const int64_t per_cta = kMvhWarps / g.ks;
     const int grid = static_cast<int>(std::min<int64_t>(sms, (items + per_cta - 1) / per_cta));
-    e = launch_pdl(mvh_kernel, dim3(grid), dim3(kMvhWarps * 32), kMvhSmem, s, g);
+    bool kq = false;
+    for (int i = 0; i < n; ++i) kq = kq || fmt[ord[i]] == FMT_Q4_K || fmt[ord[i]] == FMT_Q2_K;
+    e = launch_pdl(kq ? mvh_kernel<true> : mvh_kernel<false>, dim3(grid), dim3(kMvhWarps * 32), kMvhSmem, s, g);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -657,7 +657,7 @@ __device__ __forceinline__ void mvh_advance(const MvhGroup& g, int ks, int membe
 
 // byte offset of stage p of row j (of every group) in a view row of W
 __device__ __forceinline__ int64_t mvh_stage_off(const MvhMat& a, int j, int p) {
-    return static_cast<int64_t>(j) * a.rowbytes + static_cast<int64_t>(p) * mvh_stage_bytes(a.fmt);
+    return static_cast<int64_t>(j) * a.rowbytes + static_cast<int64_t>(p) * a.stage_bytes;
 }
 
 // Issues the TMA copies of the stage at cursor c into `slot` (completing on
@@ -668,8 +668,8 @@ __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c,
     const MvhMat& a = g.m[c.m];
     const int li = c.it - a.item0;
     const int j = li & 7, G0 = (li >> 3) * kMvhRows;
-    const int nb = mvh_boxes(a.fmt);
-    const uint32_t bw = mvh_box_w(a.fmt);
+    const int nb = a.boxes;
+    const uint32_t bw = static_cast<uint32_t>(a.box_w);
     const int64_t off = mvh_stage_off(a, j, c.p) & ~static_cast<int64_t>(15);
     if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb) * bw * kMvhRows);
     __syncwarp();
@@ -680,7 +680,7 @@ __device__ __forceinline__ void mvh_issue(const MvhGroup& g, const MvhCursor& c,
 
 // The lane's activation row (xb: its batch row) at the first K of stage p.
 __device__ __forceinline__ const uint16_t* mvh_xrow(const MvhMat& a, int xb, int p) {
-    return a.xh + static_cast<int64_t>(xb) * a.K + static_cast<int64_t>(p) * mvh_stage_k(a.fmt);
+    return a.xh + static_cast<int64_t>(xb) * a.K + static_cast<int64_t>(p) * a.stage_k;
 }
 
 // Bounded wait for the TMA copies of a slot; false (and the error word set)
@@ -705,6 +705,10 @@ __device__ __forceinline__ void mvh_team_sync(int team, int ks) {
     if (ks > 1) asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(32 * ks) : "memory");
 }
 
+// KQ: the launch has Q4_K / Q2_K matrices. Their stages are built only into
+// that instantiation, so the code of the other formats' launches is the same
+// as if they did not exist.
+template <bool KQ>
 __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_constant__ MvhGroup g) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -790,7 +794,7 @@ __global__ void __launch_bounds__(kMvhWarps * 32, 1) mvh_kernel(const __grid_con
             const uint32_t L = static_cast<uint32_t>(mvh_stage_off(a, j, p) & 15);
             if (a.fmt == FMT_Q6_K) q6k_stage(slot, gr, c, po, L, selc, xr, acc);
             else if (a.fmt == FMT_Q4_0) q4_0_stage(slot, gr, c, xr, acc);
-            else if (a.fmt == FMT_Q8_0) q8_0_stage(slot, gr, c, L, xr, acc);
+            else if (!KQ || a.fmt == FMT_Q8_0) q8_0_stage(slot, gr, c, L, xr, acc);
             else if (a.fmt == FMT_Q4_K) q4k_stage(slot, gr, c, selc, xr, acc);
             else {
                 const float4 r = q2k_stage(slot, gr, c, L, selc, xr);
