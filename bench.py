@@ -718,8 +718,8 @@ def run_reference(args, world, rank):
 # ------------------------------------------------------------------ main
 
 # read + write DRAM bytes of the MoE part per distinct expert (ncu, 24 experts, T=16)
-MOE_DRAM_BYTES_PER_EXPERT = (11264 + 237824 + 398583808 + 1786368 + 2106880 + 199277824 + 1957376
-                             + 3686656) / 24
+MOE_DRAM_BYTES_PER_EXPERT = (23552 + 12800 + 243968 + 398698240 + 1658368 + 2125312 + 199287808 + 2048256
+                             + 3685120) / 24
 
 SWEEP_LAYER = [  # (name, fmt name, N, K) of one layer
     ("wq", "Q4_0", 4096, 4096), ("wk", "Q4_0", 4096, 4096), ("wo", "Q4_0", 4096, 4096),
