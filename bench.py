@@ -379,6 +379,13 @@ def moe_prefill_part(torch, qmm, wts, device, steps, warmup, check, T=4096):
         err = np.abs(yt - ref)
         parity = {"tokens": len(ts), "max_err_over_loose": float((err / loose).max()),
                   "frac_within_tight": float((err <= tight).mean()), "ok": bool((err <= loose).all())}
+    # GEMM launches in one call, each counted once per K split: 3 for the
+    # grouped flow (the experts of each projection lie at one stride in one
+    # tensor, no split), 3 per used expert and split otherwise
+    qmm.liveness_reset()
+    qmm.moe_prefill(qmm.Q4_0, experts, idx, gate, x, y)
+    torch.cuda.synchronize(device)
+    gemm_launches = qmm.liveness()["gemm_q4_0"]
     times = []
     for _ in range(steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -392,7 +399,8 @@ def moe_prefill_part(torch, qmm, wts, device, steps, warmup, check, T=4096):
     distinct = len(set(idx.cpu().numpy().ravel().tolist()))
     return {"workload": f"{T} tokens, top-{k} of {E} Q4_0 experts (gate/up {I}x{H}, down {H}x{I})",
             "ms": ms, "tops": flops / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
-            "distinct_experts": distinct, "timing": "CUDA events around each call, median of the steps",
+            "distinct_experts": distinct, "gemm_launch_splits_per_call": gemm_launches,
+            "timing": "CUDA events around each call, median of the steps",
             "parity": parity}
 
 

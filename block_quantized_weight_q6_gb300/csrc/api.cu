@@ -59,6 +59,7 @@ struct Env {
     bool mv1_on = true;
     bool mv8_on = true;
     bool mvh_on = true;
+    bool moe_grouped = true;  // one grouped GEMM launch per projection in moe_prefill
 };
 Env g_env;
 std::once_flag g_env_once;
@@ -78,6 +79,8 @@ void read_env() {
     qmm::g_moe_mvh_enabled = !(mm && std::strcmp(mm, "0") == 0);
     const char* mh = std::getenv("QMM_MVH");
     g_env.mvh_on = !(mh && std::strcmp(mh, "0") == 0);
+    const char* mg = std::getenv("QMM_MOE_GROUPED");
+    g_env.moe_grouped = !(mg && std::strcmp(mg, "0") == 0);
     const char* pdl = std::getenv("QMM_PDL");
     qmm::g_pdl_enabled = !(pdl && std::strcmp(pdl, "0") == 0);
 }
@@ -913,11 +916,18 @@ namespace {
 constexpr int64_t kPrefillMaxSlots = int64_t{1} << 22;
 
 // Workspace of moe_prefill, region by region (each rounded up to 256 B).
+// The grouped flow pads every expert's rows to whole 128-row tiles, so its
+// row regions hold up to S + 127 * min(E, S) rows.
 struct PrefillWs {
-    size_t counts, order, pos, xg, g, u, o, a16, xs, part, total;
+    size_t counts, order, pos, xg, g, u, o, a16, xs, part, off, poff, tile, pos_pad, prow, total;
+    int64_t rows;  // rows of the row regions
 };
 
-PrefillWs prefill_ws(int E, int64_t S, int H, int I, bool bf16) {
+int64_t prefill_rows(int E, int64_t S, bool grouped) {
+    return grouped ? (S + 127 * std::min<int64_t>(E, S) + 127) / 128 * 128 : S;
+}
+
+PrefillWs prefill_ws(int E, int64_t S, int H, int I, bool bf16, bool grouped) {
     PrefillWs w{};
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -926,24 +936,59 @@ PrefillWs prefill_ws(int E, int64_t S, int H, int I, bool bf16) {
         return at;
     };
     const int64_t Kmax = std::max(H, I);
+    const int64_t R = prefill_rows(E, S, grouped);
     size_t part = 0;
-    for (int64_t M = 128;; M += 128) {
-        const int64_t m = std::min<int64_t>(M, S);
-        part = std::max({part, gemm_part_bytes(m, I, H), gemm_part_bytes(m, H, I)});
-        if (m == S) break;
+    if (!grouped) {
+        for (int64_t M = 128;; M += 128) {
+            const int64_t m = std::min<int64_t>(M, S);
+            part = std::max({part, gemm_part_bytes(m, I, H), gemm_part_bytes(m, H, I)});
+            if (m == S) break;
+        }
     }
+    w.rows = R;
     w.counts = take(static_cast<size_t>(E) * 4);
     w.order = take(static_cast<size_t>(S) * 4);
     w.pos = take(static_cast<size_t>(S) * 4);
-    w.xg = take(static_cast<size_t>(S) * H * (bf16 ? 2 : 4));
-    w.g = take(static_cast<size_t>(S) * I * 4);
-    w.u = take(static_cast<size_t>(S) * I * 4);
-    w.o = take(static_cast<size_t>(S) * H * 4);
-    w.a16 = take(gemm_a16_bytes(S, Kmax));
-    w.xs = take(static_cast<size_t>(S) * (Kmax / 32) * 4);
+    w.xg = take(static_cast<size_t>(R) * H * (bf16 ? 2 : 4));
+    w.g = take(static_cast<size_t>(R) * I * 4);
+    w.u = take(static_cast<size_t>(R) * I * 4);
+    w.o = take(static_cast<size_t>(R) * H * 4);
+    w.a16 = take(gemm_a16_bytes(R, Kmax));
+    w.xs = take(static_cast<size_t>(R) * (Kmax / 32) * 4);
     w.part = take(part);
+    if (grouped) {
+        w.off = take(static_cast<size_t>(E) * 4);
+        w.poff = take(static_cast<size_t>(E) * 4);
+        w.tile = take(static_cast<size_t>(R / 128) * 4);
+        w.pos_pad = take(static_cast<size_t>(S) * 4);
+        w.prow = take(static_cast<size_t>(R) * 4);
+    }
     w.total = off;
     return w;
+}
+
+// Whether the table's matrices lie at one fixed stride (a multiple of 16
+// bytes, at least a matrix apart): *stride is that stride.
+bool table_stride(const void* const* w, int E, int64_t bytes, int64_t* stride) {
+    if (E == 1) {
+        *stride = static_cast<int64_t>(round_up(static_cast<size_t>(bytes), 16));
+        return true;
+    }
+    const int64_t st = reinterpret_cast<intptr_t>(w[1]) - reinterpret_cast<intptr_t>(w[0]);
+    if (st < bytes || st % 16) return false;
+    for (int e = 2; e < E; ++e)
+        if (reinterpret_cast<intptr_t>(w[e]) - reinterpret_cast<intptr_t>(w[e - 1]) != st) return false;
+    *stride = st;
+    return true;
+}
+
+// The grouped flow applies: the environment gate, and all three tables strided.
+bool prefill_grouped(int wf, const qmm_moe_t& m, int64_t* sg, int64_t* su, int64_t* sd) {
+    if (!g_env.moe_grouped) return false;
+    const int64_t bg = static_cast<int64_t>(m.inter) * (m.hidden / block_elems(wf)) * block_bytes(wf);
+    const int64_t bd = static_cast<int64_t>(m.hidden) * (m.inter / block_elems(wf)) * block_bytes(wf);
+    return table_stride(m.w_gate, m.n_experts, bg, sg) && table_stride(m.w_up, m.n_experts, bg, su) &&
+           table_stride(m.w_down, m.n_experts, bd, sd);
 }
 
 int check_prefill(uint32_t fmt, const qmm_moe_t* experts, int* wf, bool* bf16) {
@@ -983,7 +1028,10 @@ size_t qmm_moe_prefill_workspace_bytes(uint32_t fmt, const qmm_moe_t* experts) {
     bool bf16;
     if (check_prefill(fmt, experts, &wf, &bf16)) return 0;
     const qmm_moe_t& m = *experts;
-    return prefill_ws(m.n_experts, static_cast<int64_t>(m.n_tokens) * m.top_k, m.hidden, m.inter, bf16).total;
+    int64_t sg, su, sd;
+    const bool grouped = prefill_grouped(wf, m, &sg, &su, &sd);
+    return prefill_ws(m.n_experts, static_cast<int64_t>(m.n_tokens) * m.top_k, m.hidden, m.inter, bf16, grouped)
+        .total;
 }
 
 int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, const float* gate_w, const void* x,
@@ -998,7 +1046,9 @@ int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, cons
     const qmm_moe_t& m = *experts;
     const int E = m.n_experts, H = m.hidden, I = m.inter, T = m.n_tokens, k = m.top_k;
     const int64_t S = static_cast<int64_t>(T) * k;
-    const PrefillWs w = prefill_ws(E, S, H, I, bf16);
+    int64_t sg = 0, su = 0, sd = 0;
+    const bool grouped = prefill_grouped(wf, m, &sg, &su, &sd);
+    const PrefillWs w = prefill_ws(E, S, H, I, bf16, grouped);
     if (w.total > t_ws_bytes || !t_ws)
         return fail(QMM_ENOWORKSPACE, "moe_prefill needs %zu bytes of workspace, %zu set", w.total, t_ws_bytes);
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -1031,8 +1081,58 @@ int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx, cons
     if (total != S) return fail(QMM_EINVAL, "moe_prefill: %lld of %lld routing slots name an expert outside 0..%d",
                                 static_cast<long long>(S - total), static_cast<long long>(S), E - 1);
 
-    // gate and up: each expert's rows through the prefill GEMM
     const int64_t xrow = static_cast<int64_t>(H) * (bf16 ? 2 : 4);
+    if (grouped) {
+        // every expert's rows padded to whole 128-row tiles: one GEMM launch
+        // per projection over all experts, the weights of tile mt those of
+        // expert tile[mt] (a tensor map over the strided table)
+        static thread_local std::vector<int> hoff, hpoff, htile;
+        hoff.assign(static_cast<size_t>(E), 0);
+        hpoff.assign(static_cast<size_t>(E), 0);
+        htile.clear();
+        int64_t o = 0, po = 0;
+        for (int ex = 0; ex < E; ++ex) {
+            hoff[static_cast<size_t>(ex)] = static_cast<int>(o);
+            hpoff[static_cast<size_t>(ex)] = static_cast<int>(po);
+            const int64_t n = cnt[static_cast<size_t>(ex)];
+            for (int64_t t = 0; t < (n + 127) / 128; ++t) htile.push_back(ex);
+            o += n;
+            po += (n + 127) / 128 * 128;
+        }
+        const int64_t R = po;  // padded rows
+        int* doff = reinterpret_cast<int*>(ws + w.off);
+        int* dpoff = reinterpret_cast<int*>(ws + w.poff);
+        int* dtile = reinterpret_cast<int*>(ws + w.tile);
+        int* pos_pad = reinterpret_cast<int*>(ws + w.pos_pad);
+        int* prow = reinterpret_cast<int*>(ws + w.prow);
+        e = cudaMemcpyAsync(doff, hoff.data(), static_cast<size_t>(E) * 4, cudaMemcpyHostToDevice, t_stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dpoff, hpoff.data(), static_cast<size_t>(E) * 4, cudaMemcpyHostToDevice, t_stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(dtile, htile.data(), htile.size() * 4, cudaMemcpyHostToDevice, t_stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(prow, 0xFF, static_cast<size_t>(R) * 4, t_stream);
+        if (e == cudaSuccess)
+            e = moe_prefill_padmap_launch(idx, pos, doff, dpoff, static_cast<int>(S), pos_pad, prow, d->sms, t_stream,
+                                          d->st);
+        if (e == cudaSuccess)
+            e = moe_prefill_gather_pad_launch(x, xrow, prow, k, static_cast<int>(R), Xg, d->sms, t_stream, d->st);
+        if (e == cudaSuccess) e = quantize_q8_launch(Xg, bf16 ? 1 : 0, R, H, nullptr, xs, a16, t_stream, d->st);
+        const uint8_t* g0 = static_cast<const uint8_t*>(m.w_gate[0]);
+        const uint8_t* u0 = static_cast<const uint8_t*>(m.w_up[0]);
+        const uint8_t* d0 = static_cast<const uint8_t*>(m.w_down[0]);
+        if (e == cudaSuccess)
+            e = gemm_grouped_launch(wf, g0, sg, E, dtile, a16, xs, G, R, I, H, t_stream, d->st, label);
+        if (e == cudaSuccess)
+            e = gemm_grouped_launch(wf, u0, su, E, dtile, a16, xs, U, R, I, H, t_stream, d->st, label);
+        if (e == cudaSuccess) e = moe_prefill_silu_launch(G, U, R * I, d->sms, t_stream, d->st);
+        if (e == cudaSuccess) e = quantize_q8_launch(G, 0, R, I, nullptr, xs, a16, t_stream, d->st);
+        if (e == cudaSuccess)
+            e = gemm_grouped_launch(wf, d0, sd, E, dtile, a16, xs, O, R, H, I, t_stream, d->st, label);
+        if (e == cudaSuccess) e = moe_prefill_combine_launch(O, pos_pad, gate_w, T, k, H, y, t_stream, d->st);
+        if (e != cudaSuccess) return cuda_fail(e, "moe_prefill grouped launch");
+        return QMM_OK;
+    }
+    // gate and up: each expert's rows through the prefill GEMM
     e = moe_prefill_gather_launch(x, xrow, order, k, static_cast<int>(S), Xg, d->sms, t_stream, d->st);
     if (e != cudaSuccess) return cuda_fail(e, "moe_prefill gather launch");
     auto gemm = [&](const void* W, const void* X, bool xb16, float* Y, int64_t M, int64_t N, int64_t K) {

@@ -83,8 +83,10 @@ constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogu
 struct RegSplit {
     int low, conv, epi;
 };
-__host__ __device__ constexpr RegSplit reg_split(int fmt, bool exp) {
-    return (fmt == FMT_Q6_K && !exp) ? RegSplit{40, 72, 80} : RegSplit{48, 64, 80};
+__host__ __device__ constexpr RegSplit reg_split(int fmt, bool exp, bool grouped = false) {
+    // (a grouped Q4_0 launch's producers hold the tile's expert and a 3-D
+    // copy coordinate: the first warpgroup takes the pool's remainder)
+    return (fmt == FMT_Q6_K && !exp) ? RegSplit{40, 72, 80} : grouped ? RegSplit{56, 64, 80} : RegSplit{48, 64, 80};
 }
 static_assert(4 * reg_split(FMT_Q6_K, false).low + kConvWarps * reg_split(FMT_Q6_K, false).conv +
                       kEpiWarps * reg_split(FMT_Q6_K, false).epi <=
@@ -92,6 +94,10 @@ static_assert(4 * reg_split(FMT_Q6_K, false).low + kConvWarps * reg_split(FMT_Q6
               "register pool");
 static_assert(4 * reg_split(FMT_Q6_K, true).low + kConvWarps * reg_split(FMT_Q6_K, true).conv +
                       kEpiWarps * reg_split(FMT_Q6_K, true).epi <=
+                  kThreads / 32 * 72,
+              "register pool");
+static_assert(4 * reg_split(FMT_Q4_0, false, true).low + kConvWarps * reg_split(FMT_Q4_0, false, true).conv +
+                      kEpiWarps * reg_split(FMT_Q4_0, false, true).epi <=
                   kThreads / 32 * 72,
               "register pool");
 static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
@@ -384,6 +390,11 @@ struct GemmArgs {
     int64_t pstride;       // floats per split: M * N rounded up to 64 (keeps 16-byte alignment)
     DevState st;
     int live_slot;
+    // grouped launch (GROUPED kernels): 128-row tile mt of A and Y belongs
+    // to expert tile_expert[mt], whose weights are W + expert * wstride (the
+    // tensor map's third coordinate)
+    const int* tile_expert;
+    int64_t wstride;
 };
 
 // The up to 7 rows of W past its last whole group of 8 rows (rows n8 ..
@@ -411,7 +422,7 @@ __device__ __noinline__ uint32_t raw_tail_rows(const uint8_t* W, int64_t N, int6
     return 0;
 }
 
-template <int FMT, bool EXP>
+template <int FMT, bool EXP, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const GemmArgs a, const __grid_constant__ CUtensorMap wmap,
                 const __grid_constant__ CUtensorMap pmap) {
@@ -470,9 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // first warpgroup (producers, MMA issue, one idle warp) gives up most of
     // its share, the epilogue's two warpgroups take it.
     if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).low));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP, GROUPED).low));
     if (warp == 0 || warp == kRawWarp) {
         // ------------------------------------------------------------ producers
+        // the tile's expert (grouped launches)
+        const int ex = GROUPED ? __ldg(a.tile_expert + mt) : 0;
         // raw stage of 256-column chunk sc into slot sc % NR
         auto issue_raw = [&](uint32_t scl) {
             const int r = static_cast<int>(scl % NR);
@@ -493,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tile holds rows past W's last whole group of 8 (last tile only)
             const bool tail = a.n8 < a.N && n0 + BN > a.n8;
             if (tail)
-                bytes = raw_tail_rows(a.W, a.N, a.n8, a.rowbytes, a.total_bytes, lane, n0, koff, len,
-                                      rw0 + 8u * 16u * RS, RS, bar, 0);
+                bytes = raw_tail_rows(GROUPED ? a.W + static_cast<int64_t>(ex) * a.wstride : a.W, a.N, a.n8,
+                                      a.rowbytes, a.total_bytes, lane, n0, koff, len, rw0 + 8u * 16u * RS, RS, bar, 0);
             fence_proxy_async_smem();
             bytes = __reduce_add_sync(0xffffffffu, bytes);
             if (lane == 0)
@@ -502,15 +515,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (boxes && lane < 8) {
                 const int64_t xb = (lane * a.rowbytes + koff) & ~static_cast<int64_t>(15);
-                tma_load_2d(rw0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2), static_cast<int>(n0 / 8),
-                            bar);
+                if constexpr (GROUPED)
+                    tma_load_3d(rw0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2), static_cast<int>(n0 / 8), ex,
+                                bar);
+                else
+                    tma_load_2d(rw0 + lane * 16u * RS, &wmap, static_cast<int>(xb / 2), static_cast<int>(n0 / 8),
+                                bar);
             }
             if (EXP && lane < 16)
                 tma_load_2d(dst0 + lane * (BN * 16u), &pmap, static_cast<int>(sc * 256 + 16 * lane),
                             static_cast<int>(n0), bar);
             if (tail)
-                (void)raw_tail_rows(a.W, a.N, a.n8, a.rowbytes, a.total_bytes, lane, n0, koff, len,
-                                    rw0 + 8u * 16u * RS, RS, bar, 1);
+                (void)raw_tail_rows(GROUPED ? a.W + static_cast<int64_t>(ex) * a.wstride : a.W, a.N, a.n8,
+                                    a.rowbytes, a.total_bytes, lane, n0, koff, len, rw0 + 8u * 16u * RS, RS, bar, 1);
         };
         if (warp == kRawWarp) {
             uint32_t r = 0, eph = 1;  // raw slot; parity of its release ((sc / NR) - 1) & 1
@@ -594,8 +611,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     } else if (warp < kEpi0) {
-        if constexpr (reg_split(FMT, EXP).conv != 72)
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).conv));
+        if constexpr (reg_split(FMT, EXP, GROUPED).conv != 72)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP, GROUPED).conv));
         // ------------------------------------------------------------ converters
         // One stage (two K blocks) per pass: one wait, one proxy fence and one
         // arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
@@ -793,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP).epi));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP, GROUPED).epi));
         // ------------------------------------------------------------ epilogue
         // One wait per stage of KP blocks (the MMA signals a stage once), then
         // per K block b: I_b from its accumulator buffer in two 16-column
@@ -900,9 +917,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 using GemmKernel = void (*)(const GemmArgs, const CUtensorMap, const CUtensorMap);
 
-static GemmKernel pick_gemm(int fmt, bool exp) {
-    if (fmt == FMT_Q6_K) return exp ? gemm_kernel<FMT_Q6_K, true> : gemm_kernel<FMT_Q6_K, false>;
-    if (fmt == FMT_Q4_0 && !exp) return gemm_kernel<FMT_Q4_0, false>;
+static GemmKernel pick_gemm(int fmt, bool exp, bool grouped = false) {
+    if (grouped) {
+        if (exp) return nullptr;
+        return fmt == FMT_Q6_K ? gemm_kernel<FMT_Q6_K, false, true> : gemm_kernel<FMT_Q4_0, false, true>;
+    }
+    if (fmt == FMT_Q6_K) return exp ? gemm_kernel<FMT_Q6_K, true, false> : gemm_kernel<FMT_Q6_K, false, false>;
+    if (fmt == FMT_Q4_0 && !exp) return gemm_kernel<FMT_Q4_0, false, false>;
     return nullptr;
 }
 
@@ -1070,6 +1091,69 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
     e = launch_pdl(gemm_split_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
                    static_cast<const float*>(part), Y, count, a.pstride, splits, st);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t gemm_grouped_launch(int fmt, const uint8_t* W, int64_t wstride, int n_experts, const int* tile_expert,
+                                const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t s, DevState st, int live_slot) {
+    GemmKernel k = pick_gemm(fmt, false, true);
+    if (!k) return cudaErrorInvalidValue;
+    if (M % BM || wstride % 16 || n_experts < 1) return cudaErrorInvalidValue;
+    const SmemLayout L = smem_layout(fmt, false);
+    static std::mutex mu;
+    static std::map<std::pair<int, GemmKernel>, bool> ready;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!ready[{dev, k}]) {
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(L.total));
+            if (e != cudaSuccess) return e;
+            ready[{dev, k}] = true;
+        }
+    }
+    GemmArgs a{};
+    a.W = W;
+    a.a16 = a16;
+    a.xs = xs;
+    a.Y = Y;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.nb = K / (fmt == FMT_Q6_K ? 256 : 32);
+    a.total_bytes = N * a.nb * (fmt == FMT_Q6_K ? 210 : 18);
+    a.rowbytes = a.nb * (fmt == FMT_Q6_K ? 210 : 18);
+    a.n8 = N / 8 * 8;
+    a.st = st;
+    a.live_slot = live_slot;
+    a.kb_split = K / 32;  // one split: the tiles of all experts fill the SMs
+    a.part = nullptr;
+    a.pstride = part_stride(M, N);
+    a.tile_expert = tile_expert;
+    a.wstride = wstride;
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>(M / BM), 1u);
+    // W of every expert as [E][N / 8][8 * rowbytes] 16-bit elements, experts
+    // wstride bytes apart; a box one row slot wide, 16 groups of 8 rows high
+    CUtensorMap wmap, pmap;
+    memset(&wmap, 0, sizeof wmap);
+    memset(&pmap, 0, sizeof pmap);
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    if (a.n8 > 0) {
+        const int rs = fmt == FMT_Q6_K ? kRawQ6K : kRawQ40;
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(4 * a.rowbytes), static_cast<cuuint64_t>(a.n8 / 8),
+                                    static_cast<cuuint64_t>(n_experts)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(8 * a.rowbytes), static_cast<cuuint64_t>(wstride)};
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(rs / 2), 16u, 1u};
+        const cuuint32_t es[3] = {1u, 1u, 1u};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint8_t*>(W), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    e = launch_pdl(k, grid, dim3(kThreads), L.total, s, a, wmap, pmap);
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace qmm

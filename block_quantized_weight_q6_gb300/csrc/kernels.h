@@ -252,6 +252,14 @@ cudaError_t gemm_launch(int fmt, bool exp, const uint8_t* W, const int8_t* plane
                         const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N,
                         int64_t K, cudaStream_t s, DevState st, int live_slot, float* part);
 
+// One GEMM over several experts' rows: 128-row tile mt of A (M % 128 == 0)
+// and Y belongs to expert tile_expert[mt] (device array), whose weights are
+// W + expert * wstride (wstride % 16 == 0); fmt FMT_Q6_K or FMT_Q4_0, the
+// in-kernel expansion, no K split.
+cudaError_t gemm_grouped_launch(int fmt, const uint8_t* W, int64_t wstride, int n_experts, const int* tile_expert,
+                                const uint16_t* a16, const float* xs, float* Y, int64_t M, int64_t N, int64_t K,
+                                cudaStream_t s, DevState st, int live_slot);
+
 // ---------------------------------------------------------------- MoE prefill
 // (moe_prefill.cu) the T*k routing slots ordered by expert, stable: counts
 // [E], order [S] (slots by expert), pos [S] (each slot's row in that order)
@@ -260,6 +268,14 @@ cudaError_t moe_prefill_plan_launch(const int32_t* idx, int S, int E, int* count
 // Xg[r] = x row of token order[r] / k (rows of rowbytes, a multiple of 16)
 cudaError_t moe_prefill_gather_launch(const void* x, int64_t rowbytes, const int* order, int k, int S, void* Xg,
                                       int sms, cudaStream_t s, DevState st);
+// the padded layout of a grouped launch (expert e's rows from poff[e], a
+// multiple of 128): pos_pad[slot], and prow[row] = slot (rows left at -1
+// are padding)
+cudaError_t moe_prefill_padmap_launch(const int32_t* idx, const int* pos, const int* off, const int* poff, int S,
+                                      int* pos_pad, int* prow, int sms, cudaStream_t s, DevState st);
+// padded row r of Xg = x row of slot prow[r] / k, or zeros
+cudaError_t moe_prefill_gather_pad_launch(const void* x, int64_t rowbytes, const int* prow, int k, int rows, void* Xg,
+                                          int sms, cudaStream_t s, DevState st);
 // g <- silu(g) * u over n values (n % 4 == 0)
 cudaError_t moe_prefill_silu_launch(float* g, const float* u, int64_t n, int sms, cudaStream_t s, DevState st);
 // y[t] = sum_j gate[t][j] * O[pos[t][j]], j in order (H % 4 == 0)

@@ -123,6 +123,44 @@ __global__ void __launch_bounds__(256) mp_gather_kernel(const uint8_t* __restric
     }
 }
 
+// The padded layout of the grouped launch: expert e's rows start at row
+// poff[e] (a multiple of 128). pos_pad[s] = the slot's padded row, prow[row]
+// = the slot of a padded row (left at -1 for padding rows).
+__global__ void __launch_bounds__(256) mp_padmap_kernel(const int32_t* __restrict__ idx, const int* __restrict__ pos,
+                                                       const int* __restrict__ off, const int* __restrict__ poff,
+                                                       int S, int* __restrict__ pos_pad, int* __restrict__ prow,
+                                                       DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, QMM_LIVE_MOE_PREFILL_PLAN);
+    for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < S; s += gridDim.x * blockDim.x) {
+        const int e = idx[s];
+        const int pp = poff[e] + (pos[s] - off[e]);
+        pos_pad[s] = pp;
+        prow[pp] = s;
+    }
+}
+
+// padded row r of Xg = the activation row of slot prow[r], or zeros
+__global__ void __launch_bounds__(256) mp_gather_pad_kernel(const uint8_t* __restrict__ x, int64_t rowbytes,
+                                                           const int* __restrict__ prow, int k, int rows,
+                                                           uint8_t* __restrict__ Xg, DevState st) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    live_bump(st, QMM_LIVE_MOE_PREFILL_ROWS);
+    const int64_t nv = rowbytes / 16;
+    for (int r = static_cast<int>(blockIdx.x); r < rows; r += static_cast<int>(gridDim.x)) {
+        const int s = prow[r];
+        uint4* dst = reinterpret_cast<uint4*>(Xg + static_cast<int64_t>(r) * rowbytes);
+        if (s < 0) {
+            for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(s / k) * rowbytes);
+            for (int64_t v = threadIdx.x; v < nv; v += blockDim.x) dst[v] = __ldg(src + v);
+        }
+    }
+}
+
 // g <- silu(g) * u, element-wise over n values (n a multiple of 4)
 __global__ void __launch_bounds__(256) mp_silu_kernel(float* __restrict__ g, const float* __restrict__ u,
                                                      int64_t n, DevState st) {
@@ -182,6 +220,20 @@ cudaError_t moe_prefill_gather_launch(const void* x, int64_t rowbytes, const int
     const int grid = static_cast<int>(std::min<int64_t>(S, static_cast<int64_t>(sms) * 8));
     return launch_pdl(mp_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s,
                       static_cast<const uint8_t*>(x), rowbytes, order, k, S, static_cast<uint8_t*>(Xg), st);
+}
+
+cudaError_t moe_prefill_padmap_launch(const int32_t* idx, const int* pos, const int* off, const int* poff, int S,
+                                      int* pos_pad, int* prow, int sms, cudaStream_t s, DevState st) {
+    const int blocks = std::max(1, std::min((S + 255) / 256, sms * 4));
+    return launch_pdl(mp_padmap_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, idx, pos, off, poff, S,
+                      pos_pad, prow, st);
+}
+
+cudaError_t moe_prefill_gather_pad_launch(const void* x, int64_t rowbytes, const int* prow, int k, int rows, void* Xg,
+                                          int sms, cudaStream_t s, DevState st) {
+    const int grid = static_cast<int>(std::min<int64_t>(rows, static_cast<int64_t>(sms) * 8));
+    return launch_pdl(mp_gather_pad_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s,
+                      static_cast<const uint8_t*>(x), rowbytes, prow, k, rows, static_cast<uint8_t*>(Xg), st);
 }
 
 cudaError_t moe_prefill_silu_launch(float* g, const float* u, int64_t n, int sms, cudaStream_t s, DevState st) {
