@@ -125,7 +125,8 @@ enum {
     QMM_LIVE_GEMM_SPLIT_REDUCE = 20,  /* sum of a GEMM's K-split partials
                                          (grids with fewer tiles than SMs)   */
     QMM_LIVE_MOE_PREFILL_PLAN = 21,   /* moe_prefill: slots ordered by
-                                         expert                              */
+                                         expert, and (grouped flow) the
+                                         padded row map                      */
     QMM_LIVE_MOE_PREFILL_ROWS = 22,   /* moe_prefill: activation rows
                                          gathered by expert, and the gated
                                          sum scattered back (two launches)   */
@@ -146,7 +147,9 @@ enum {
  * batch 2-8), QMM_MVH ("0" turns the fp16-MMA matvec for bf16 batches 1-8
  * off, so those batches take the paths above), QMM_PDL ("0" launches
  * without programmatic dependent launch), QMM_MOE_MMA ("0" keeps moe_gemv on
- * the CUDA-core expert matvec even where the warp-level MMA one applies).
+ * the CUDA-core expert matvec even where the warp-level MMA one applies),
+ * QMM_MOE_GROUPED ("0" keeps moe_prefill on one GEMM launch per expert even
+ * where the grouped launch applies).
  * Called implicitly by every entry point; calling it again is a no-op. */
 int qmm_init(void);
 
@@ -352,7 +355,13 @@ size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts);
  * down projection's input; y[t] = sum_j gate_w[t][j] * o_j, in j order.
  * Experts: q6_K or Q4_0 (the GEMM's formats), hidden and inter multiples of
  * 32 (256 for q6_K), each matrix 16-byte aligned (any address, no stride
- * needed). idx: [T][top_k] int32 device, gate_w: [T][top_k] fp32 device,
+ * needed). When each of w_gate, w_up and w_down lists its experts at one
+ * fixed stride (a multiple of 16 bytes, at least one matrix), every
+ * expert's rows are padded to whole 128-row tiles and each projection runs
+ * as one grouped GEMM launch over all tiles (the tile's expert selects the
+ * weights); any other table runs one GEMM per expert. The two flows meet
+ * the same bound; their sums are grouped differently (the per-expert GEMMs
+ * may split K), so their outputs can differ in the last bits. idx: [T][top_k] int32 device, gate_w: [T][top_k] fp32 device,
  * x: [T][hidden] fp32 or bf16 (fmt's activation type), y: [T][hidden] fp32;
  * x and y 16-byte aligned; T * top_k <= 2^22. Needs the workspace
  * qmm_moe_prefill_workspace_bytes gives. The call reads the per-expert
@@ -360,7 +369,8 @@ size_t qmm_moe_workspace_bytes(const qmm_moe_t* experts);
  * GEMMs, so it cannot be captured in a CUDA graph (QMM_EUNSUPPORTED while
  * the stream is capturing). An expert index outside 0..n_experts-1 returns
  * QMM_EINVAL after that synchronization (and sets the device flag
- * qmm_sync_check reports). Results are bitwise reproducible. */
+ * qmm_sync_check reports). Results are bitwise reproducible for a given
+ * table layout. */
 int moe_prefill(uint32_t fmt, const qmm_moe_t* experts, const int32_t* idx,
                 const float* gate_w, const void* x, float* y);
 
