@@ -1302,10 +1302,6 @@ int qmm_sync_check(void) {
         if (err & DERR_MOE_BAD_INDEX)
             return fail(QMM_EINVAL, "moe_gemv / moe_prefill: an expert index was outside 0..n_experts-1; "
                                     "its slot contributed nothing (flags 0x%x)", err);
-        if (err & DERR_GEMM_SCALE)
-            return fail(QMM_EUNSUPPORTED, "qmm_gemm: a q6_K sub-block scale is outside -56..56, "
-                                          "which the fp16 tensor-core B tile cannot hold exactly; "
-                                          "the output is not valid (flags 0x%x)", err);
         return fail(QMM_EDEVICE_TIMEOUT, "a kernel gave up a bounded wait (flags 0x%x)", err);
     }
     return QMM_OK;

@@ -21,7 +21,6 @@ enum : uint32_t {
     DERR_GEMM_TIMEOUT = 1u << 1,
     DERR_MOE_TIMEOUT = 1u << 2,
     DERR_MOE_BAD_INDEX = 1u << 3,
-    DERR_GEMM_SCALE = 1u << 4,   // a q6_K sub-block scale outside the GEMM's exact range
 };
 
 // Pointers to the library's device-resident state, passed to every kernel.

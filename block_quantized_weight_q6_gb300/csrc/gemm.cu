@@ -10,12 +10,17 @@
 // accumulator holds I exactly. The accumulator is drained once per K block
 // and the scales are applied on the CUDA cores.
 //
-// Exactness of the B values: sc * (q - 32) is formed as (off + c) * sc -
-// off * sc with one rounding (off = 1056 from the raw bits, 1152 from the
-// plane), so off * sc must be a finite fp16 and the result an exact one:
-// |sc| <= kScMax = 56 keeps both (|sc * (q - 32)| <= 1792). The synthetic
-// workloads draw sc on -32..31; a block with a larger scale sets
-// DERR_GEMM_SCALE, and the call reports an error instead of a wrong result.
+// Exactness of the B values: s * (q - 32) is formed as (off + c) * s -
+// off * s with one rounding (off = 1056 from the raw bits, 1152 from the
+// plane), so off * s must be a finite fp16 and the result an exact one:
+// |s| <= kScMax = 56 keeps both (|s * (q - 32)| <= 1792). A q6_K sub-block
+// scale sc (any int8) is split as sc = s0 + 2 s1 with s0 and s1 of sc's
+// sign, |s0| <= 56 and |s1| <= 36 (|s0| = |sc| up to 56; beyond, 56 or 55,
+// whichever leaves an even rest). The K loop runs with B = s0 * (q - 32);
+// a CTA whose tile held a scale beyond 56 runs it a second time with B =
+// s1 * (q - 32) and d doubled, summing both passes into the same outputs.
+// Each pass's block partials stay exact integers. (The synthetic workloads
+// draw sc on -32..31: one pass.)
 //
 // The two q6_K variants of "57 - r54 MINFER_MMQ_Q6K_EXP" section 2.1:
 //   EXP  : the B tile comes from the centered-int8 W_exp plane (one byte per
@@ -75,29 +80,18 @@ constexpr int kConv0 = 4, kConvWarps = 8;   // converter warps (warpgroups 1, 2)
 constexpr int kConvRows = 8 / kConvWarps;   // rows 8 g + j a converter lane takes per pass (j = kConvRows cw + jj)
 constexpr int kEpi0 = 12, kEpiWarps = 16;   // epilogue warps (warpgroups 3 .. 6)
 constexpr int kEpiCols = BN * 4 / kEpiWarps;  // accumulator columns per epilogue thread
-// registers per thread after the reallocation: 4 warps x 40 + 8 x 72 + 16 x 80 = 2016 x 32, or 4 x 48 +
-// 8 x 64 + 16 x 80 = 1984 x 32, within the 28 x 72 x 32 the block is launched with (an increase
-// beyond that pool would never complete)
-// The split depends on the variant: the in-kernel q6_K expansion wants the
-// converters' 72, the others fit them in 64 and give the producers 48.
+// registers per thread after the reallocation: 4 warps x 56 + 8 x 64 + 16 x 80 = 2016 x 32, the
+// whole 28 x 72 x 32 the block is launched with (an increase beyond that pool would never
+// complete). The producers' warpgroup needs its 56: with fewer it spills, and the slower
+// issue of the raw-weight copies cost up to 12% of the GEMM (measured).
 struct RegSplit {
     int low, conv, epi;
 };
-__host__ __device__ constexpr RegSplit reg_split(int fmt, bool exp, bool grouped = false) {
-    // (a grouped Q4_0 launch's producers hold the tile's expert and a 3-D
-    // copy coordinate: the first warpgroup takes the pool's remainder)
-    return (fmt == FMT_Q6_K && !exp) ? RegSplit{40, 72, 80} : grouped ? RegSplit{56, 64, 80} : RegSplit{48, 64, 80};
+__host__ __device__ constexpr RegSplit reg_split(int, bool, bool = false) {
+    return RegSplit{56, 64, 80};
 }
 static_assert(4 * reg_split(FMT_Q6_K, false).low + kConvWarps * reg_split(FMT_Q6_K, false).conv +
                       kEpiWarps * reg_split(FMT_Q6_K, false).epi <=
-                  kThreads / 32 * 72,
-              "register pool");
-static_assert(4 * reg_split(FMT_Q6_K, true).low + kConvWarps * reg_split(FMT_Q6_K, true).conv +
-                      kEpiWarps * reg_split(FMT_Q6_K, true).epi <=
-                  kThreads / 32 * 72,
-              "register pool");
-static_assert(4 * reg_split(FMT_Q4_0, false, true).low + kConvWarps * reg_split(FMT_Q4_0, false, true).conv +
-                      kEpiWarps * reg_split(FMT_Q4_0, false, true).epi <=
                   kThreads / 32 * 72,
               "register pool");
 static_assert(kEpiCols == 32, "one 32-column tensor-memory load per block and thread");
@@ -232,14 +226,15 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 
 // ---------------------------------------------------------------- trace
 // Diagnostic builds define QMM_GEMM_TRACE and point qmm_gemm_trace at mapped
-// host memory: each warp records where it is, so a stall can be located from
-// the host while the kernel is still running. Product builds compile it out.
+// host memory (128 words per CTA of a one-split grid): each warp records
+// where it is, so a stall can be located from the host while the kernel is
+// still running. Product builds compile it out.
 #ifdef QMM_GEMM_TRACE
 __device__ unsigned* qmm_gemm_trace;
 #define QMM_TRACE(code, kb)                                                                   \
     do {                                                                                      \
         if (qmm_gemm_trace && (threadIdx.x & 31) == 0) {                                       \
-            unsigned* t_ = qmm_gemm_trace + (blockIdx.y * gridDim.x + blockIdx.x) * 64 + 4 * (threadIdx.x >> 5); \
+            unsigned* t_ = qmm_gemm_trace + (blockIdx.y * gridDim.x + blockIdx.x) * 128 + 4 * (threadIdx.x >> 5); \
             asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(t_), "r"((unsigned)(code)) : "memory"); \
             asm volatile("st.volatile.global.u32 [%0], %1;" ::"l"(t_ + 1), "r"((unsigned)(kb)) : "memory"); \
         }                                                                                     \
@@ -476,6 +471,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = lds_u32(S + L.tslot);
     // the quantized activations come from the previous kernel on the stream
     grid_dependency_wait();
+    // End of a K pass, by all 896 threads (one barrier with an OR
+    // reduction): another pass follows if any thread asks for one. Only the
+    // converters do, at the end of the first pass of a tile that held a scale
+    // beyond kScMax, so every thread makes the same number of calls. The
+    // barrier is the non-aligned form, which counts threads one by one: a
+    // warp whose lanes arrive apart (after lane-dependent copies) still
+    // counts 32. (After an abort the second pass's waits give up at once.)
+    auto next_pass = [](bool want) -> bool {
+        QMM_TRACE(50, want);
+        __syncwarp();
+        uint32_t more;
+        asm volatile(
+            "{\n\t.reg .pred p, q;\n\t"
+            "setp.ne.u32 p, %1, 0;\n\t"
+            "barrier.red.or.pred q, 1, %2, p;\n\t"
+            "selp.u32 %0, 1, 0, q;\n\t}"
+            : "=r"(more)
+            : "r"(static_cast<uint32_t>(want)), "n"(kThreads)
+            : "memory");
+        QMM_TRACE(51, more);
+        return more != 0;
+    };
 
     // Registers move between warpgroups (warpgroup-wide instructions): the
     // first warpgroup (producers, MMA issue, one idle warp) gives up most of
@@ -486,9 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producers
         // the tile's expert (grouped launches)
         const int ex = GROUPED ? __ldg(a.tile_expert + mt) : 0;
-        // raw stage of 256-column chunk sc into slot sc % NR
-        auto issue_raw = [&](uint32_t scl) {
-            const int r = static_cast<int>(scl % NR);
+        // raw stage of 256-column chunk scl of the range into slot r (the
+        // slots cycle over the chunks of all passes)
+        auto issue_raw = [&](uint32_t scl, int r) {
             const int64_t sc = sc0 + scl;  // the chunk within the row
             const uint32_t dst0 = S + L.raw + static_cast<uint32_t>(r) * L.rawslot;
             const uint32_t bar = bar_raw_full(BARS, r);
@@ -530,25 +547,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     a.rowbytes, a.total_bytes, lane, n0, koff, len, rw0 + 8u * 16u * RS, RS, bar, 1);
         };
         if (warp == kRawWarp) {
-            uint32_t r = 0, eph = 1;  // raw slot; parity of its release ((sc / NR) - 1) & 1
+            uint32_t r = 0, eph = 1;  // raw slot; parity of its release ((g / NR) - 1) & 1
+            uint32_t g = 0;           // chunks issued, over the passes
             const uint32_t nsc32 = static_cast<uint32_t>(nsc);
-            for (uint32_t sc = 0; sc < nsc32; ++sc) {
-                QMM_TRACE(1, sc);
-                if (sc >= NR && !wait_or_abort(bar_raw_empty(BARS, static_cast<int>(r)), eph, FLAG, a.st.err)) break;
-                issue_raw(sc);
-                if (++r == NR) {
-                    r = 0;
-                    eph ^= 1;
+            // each pass (a wait that gives up ends it), then the pass barrier
+            do {
+                for (uint32_t sc = 0; sc < nsc32; ++sc) {
+                    QMM_TRACE(1, sc);
+                    if (g >= NR && !wait_or_abort(bar_raw_empty(BARS, static_cast<int>(r)), eph, FLAG, a.st.err))
+                        break;
+                    issue_raw(sc, static_cast<int>(r));
+                    ++g;
+                    if (++r == NR) {
+                        r = 0;
+                        eph ^= 1;
+                    }
                 }
-            }
+            } while (next_pass(false));
             // the copies still in flight land before the CTA ends
-            for (int64_t sc = nsc > NR ? nsc - NR : 0; sc < nsc; ++sc)
-                (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(sc % NR)), (sc / NR) & 1, FLAG, a.st.err);
+            for (uint32_t c = g > NR ? g - NR : 0; c < g; ++c)
+                (void)wait_or_abort(bar_raw_full(BARS, static_cast<int>(c % NR)), (c / NR) & 1, FLAG, a.st.err);
         } else {
             const uint16_t* a16t = a.a16 + (mt * nkb + kbg) * (BM * 32);  // this CTA's first A tile
             uint32_t st = 0, eph = 1;  // stage; parity of its release ((q / NS) - 1) & 1
-            for (uint32_t q = 0, kb0 = 0; kb0 < nkb32; ++q, kb0 += KP) {
-                // the A tiles of blocks KP q .. (consecutive in the pre-tiled operand)
+            uint32_t q = 0;            // stages, over the passes
+            do {  // each pass, then the pass barrier
+            for (uint32_t kb0 = 0; kb0 < nkb32; ++q, kb0 += KP) {
+                // the A tiles of blocks kb0 .. (consecutive in the pre-tiled operand)
                 const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
                 QMM_TRACE(2, kb0);
                 if (q >= NS && !wait_or_abort(bar_empty(BARS, static_cast<int>(st)), eph, FLAG, a.st.err)) break;
@@ -557,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // pull the tiles kPrefetch stages ahead into L2 first: the
                     // copy into shared memory then waits on L2, not on DRAM
                     const uint32_t pk = kb0 + kPrefetch * KP;
-                    if (q == 0)
+                    if (kb0 == 0)
                         for (uint32_t k = 0; k < pk && k < nkb32; k += KP)
                             prefetch_l2(a16t + static_cast<size_t>(k) * (BM * 32),
                                         (nkb32 - k < KP ? nkb32 - k : KP) * kATile);
@@ -574,13 +599,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     eph ^= 1;
                 }
             }
+            } while (next_pass(false));
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
         constexpr uint32_t idesc = idesc_f16(BM, BN);
-        bool ok = true;
         uint32_t st = 0, fph = 0;   // stage; parity of its fill (q / NS) & 1
-        for (uint32_t q = 0, kb0 = 0; ok && kb0 < nkb32; ++q, kb0 += KP) {
+        uint32_t q = 0;             // stages, over the passes
+        do {  // each pass, then the pass barrier
+        for (uint32_t kb0 = 0; kb0 < nkb32; ++q, kb0 += KP) {
             const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
             QMM_TRACE(10, kb0);
             if (!wait_or_abort(bar_full(BARS, static_cast<int>(st)), fph, FLAG, a.st.err)) break;
@@ -609,19 +636,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             QMM_TRACE(14, kb0);
         }
+        } while (next_pass(false));
+    } else {
+        // the idle warp keeps the pass barrier's count
+        while (next_pass(false)) {
+        }
     }
     } else if (warp < kEpi0) {
         if constexpr (reg_split(FMT, EXP, GROUPED).conv != 72)
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP, GROUPED).conv));
         // ------------------------------------------------------------ converters
-        // One stage (two K blocks) per pass: one wait, one proxy fence and one
-        // arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
+        // One stage (two K blocks) per iteration: one wait, one proxy fence and
+        // one arrival. Warp cw converts the rows 8 g + cw of the tile (the plane
         // variant: g + 16 cw): lane (g = lane % 16, hh = lane / 16) the 16
         // columns 16 hh .. 16 hh + 15 of each block. In the raw stage of q6_K
         // / Q4_0 rows, a row's offset inside its slot depends only on cw, so
         // the realignment of its bytes is the same for the whole warp; plane
         // bytes need none.
-        static_assert(kConvRows == 1 && KP == 2, "a converter pass is one row and one stage of two blocks");
+        static_assert(kConvRows == 1 && KP == 2, "a converter iteration is one row and one stage of two blocks");
         static_assert((DR & (DR - 1)) == 0, "the d ring is a power of two");
         const int cw = warp - kConv0;
         const int tid = threadIdx.x - 32 * kConv0;  // rows 0..127 store d
@@ -643,10 +675,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ro = row_off(n), l0 = live ? lead0(n0 + n) : 0u;
         const bool live_d = tid < BN && n0 + tid < a.N;  // row tid, whose d this lane stores
         const uint32_t ro_d = live_d ? row_off(tid) : 0u, l0_d = live_d ? lead0(n0 + tid) : 0u;
-        bool scale_bad = false;
         uint32_t r = 0, rph = 0;   // raw slot; parity of its fill (sc / NR) & 1
         uint32_t st = 0, eph = 1;  // B stage; parity of its release ((q / NS) - 1) & 1
-        for (uint32_t q = 0, kb0 = 0; kb0 < nkb32; ++q, kb0 += 2) {
+        uint32_t q = 0;            // stages, over the passes
+        // pass 0 takes s0 of each scale; pass 1, run when some scale of the
+        // tile lies beyond kScMax, takes s1 with d doubled. pf: bit 0 the
+        // pass, bit 1 a scale beyond kScMax seen (one register for both).
+        uint32_t pf = 0;
+        for (;;) {  // each pass, then the pass barrier
+        for (uint32_t kb0 = 0; kb0 < nkb32; ++q, kb0 += 2) {
             const uint32_t nbk = nkb32 - kb0 < 2 ? 1u : 2u;
             const uint32_t sc = kb0 >> 3;  // both blocks lie in this 256-column chunk
             const uint32_t j0 = kb0 & 7;
@@ -659,12 +696,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the first four converter warps (rows 0..127)
             if (tid < BN) {
                 for (uint32_t bi = 0; bi < (Q6 ? (j0 == 0 ? 1u : 0u) : nbk); ++bi) {
-                    const uint32_t di = (Q6 ? sc : kb0 + bi) & (DR - 1);
+                    // the d ring counts over the passes
+                    const uint32_t di = ((pf & 1u) * (Q6 ? static_cast<uint32_t>(nsc) : nkb32) +
+                                         (Q6 ? sc : kb0 + bi)) & (DR - 1);
                     float dval = 0.0f;
                     if (live_d) {
                         const uint32_t rowb = raw0 + ro_d + ((l0_d + ls) & 15u);
                         const uint32_t doff = EXP ? 16 : (Q6 ? 208 : 18 * (j0 + bi));
                         dval = half_bits_to_float(lds_u16(rowb + doff));
+                        if (pf & 1u) dval += dval;  // the second pass holds s1 = (sc - s0) / 2
                     }
                     asm volatile("st.shared.f32 [%0], %1;" ::"r"(S + L.dv + (di * BN + tid) * 4), "f"(dval)
                                  : "memory");
@@ -732,9 +772,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int bi = 0; bi < KP; ++bi) {
-                        // sc * (v - off) exactly: (off + v) * sc - off * sc, one rounding
-                        if (scv[bi] > kScMax || scv[bi] < -kScMax) scale_bad = true;
-                        const float scf = static_cast<float>(scv[bi]);
+                        // this pass's part s of sc; s * (v - off) exactly:
+                        // (off + v) * s - off * s, one rounding
+                        // (s0 = sc clamped to +-56, or to +-55 for odd sc,
+                        // so that sc - s0 is even; s1 = (sc - s0) / 2)
+                        const int lim = kScMax - (scv[bi] & 1);
+                        const int s0 = min(max(scv[bi], -lim), lim);
+                        pf |= static_cast<uint32_t>(s0 != scv[bi]) << 1;
+                        const float scf = static_cast<float>((pf & 1u) ? (scv[bi] - s0) >> 1 : s0);
                         const float off = EXP ? 1152.0f : 1056.0f;
                         const uint32_t sc2 = half2_bits(scf);
                         const uint32_t bias = half2_bits(-off * scf);
@@ -808,7 +853,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (__any_sync(0xffffffffu, scale_bad) && lane == 0) atomicOr(a.st.err, DERR_GEMM_SCALE);
+        if (!next_pass(pf == 2u)) break;  // first pass, a scale beyond kScMax
+        pf = 1u;
+        }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(reg_split(FMT, EXP, GROUPED).epi));
         // ------------------------------------------------------------ epilogue
@@ -828,26 +875,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kEpiCols; ++c) y[c] = 0.0f;
         float sxa[KP], sxb[KP];
         const float* xrow = a.xs + (m < a.M ? m : 0) * nkb + kbg;
-        auto load_sx = [&](uint32_t q, float (&o)[KP]) {
+        auto load_sx = [&](uint32_t k0, float (&o)[KP]) {
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) {
-                const uint32_t kb = q * KP + bi;
+                const uint32_t kb = k0 + bi;
                 o[bi] = 0.0f;
                 if (m < a.M && kb < nkb32) asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(o[bi]) : "l"(xrow + kb));
             }
         };
-        load_sx(0, sxa);
         bool ok = true;
-        for (uint32_t q = 0, kb0 = 0; ok && kb0 < nkb32; ++q, kb0 += KP) {
+        uint32_t qg = 0;     // stages, over the passes (accumulator buffers)
+        uint32_t dbase = 0;  // d ring entries of the earlier passes
+        for (;;) {  // each pass, then the pass barrier
+        load_sx(0, sxa);
+        for (uint32_t kb0 = 0; ok && kb0 < nkb32; ++qg, kb0 += KP) {
             const uint32_t nbk = nkb32 - kb0 < KP ? nkb32 - kb0 : KP;
-            load_sx(q + 1, sxb);
+            load_sx(kb0 + KP, sxb);
             QMM_TRACE(30, kb0);
-            if (!wait_or_abort(bar_acc_full(BARS, static_cast<int>(q & 1)), (q >> 1) & 1, FLAG, a.st.err)) break;
+            if (!wait_or_abort(bar_acc_full(BARS, static_cast<int>(qg & 1)), (qg >> 1) & 1, FLAG, a.st.err)) {
+                ok = false;
+                break;
+            }
             QMM_TRACE(31, kb0);
             tc_fence_after();
             for (uint32_t bi = 0; bi < nbk; ++bi) {
                 const uint32_t kb = kb0 + bi;
-                const uint32_t dk = Q6 ? kb >> 3 : kb;  // index of the d in use
+                // index of the d in use, counted over the passes
+                const uint32_t dk = dbase + (Q6 ? kb >> 3 : kb);
                 const uint32_t di = dk & (DR - 1);
                 if ((!Q6 || (kb & 7) == 0) &&
                     !wait_or_abort(bar_dv_full(BARS, static_cast<int>(di)), (dk / DR) & 1, FLAG, a.st.err)) {
@@ -856,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float sx = bi == 0 ? sxa[0] : sxa[1];
                 const float2 s2 = make_float2(sx, sx);
-                const uint32_t accb = tl + (2 * (q & 1) + bi) * BN + c0;
+                const uint32_t accb = tl + (2 * (qg & 1) + bi) * BN + c0;
                 const uint32_t dv = S + L.dv + (di * BN + c0) * 4;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
@@ -885,9 +939,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, static_cast<int>(q & 1)));
+            if (lane == 0) mbar_arrive(bar_acc_empty(BARS, static_cast<int>(qg & 1)));
 #pragma unroll
             for (int bi = 0; bi < KP; ++bi) sxa[bi] = sxb[bi];
+        }
+        if (!next_pass(false)) break;
+        dbase += Q6 ? static_cast<uint32_t>(nsc) : nkb32;
         }
         if (ok && m < a.M) {
             const int64_t nb0 = n0 + c0;

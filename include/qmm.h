@@ -283,11 +283,11 @@ int qmm_quantize_q8(uint32_t x_type, const void* x, int64_t rows, int64_t K, int
  *   plane must come from qmm_plane_build for this same W, N and K, else
  *   QMM_EPLANE.
  * Q4_0: in-kernel expansion only; exp_plane must be NULL.
- * Range: the fp16 B tile holds sc * (q - 32) exactly for q6_K sub-block
- *   scales in -56..56 (the synthetic workloads draw -32..31). A matrix with a
- *   larger scale makes the next qmm_sync_check return QMM_EUNSUPPORTED, and
- *   Y is then not valid. The matvec (qmm_gemv) has no such limit: it applies
- *   the scales in fp32.
+ * Scales: any int8 q6_K sub-block scale. The fp16 B tile holds
+ *   s * (q - 32) exactly for |s| <= 56, so a 128 x 128 output tile whose
+ *   weights hold a larger scale sc runs its K range twice, with
+ *   sc = s0 + 2 s1 (|s0| <= 56, |s1| <= 36, both of sc's sign), summing
+ *   both passes; every block partial stays an exact integer.
  * Needs workspace (quantized X). */
 int qmm_gemm(uint32_t fmt, const void* W, const void* X, float* Y, int64_t M,
              int64_t N, int64_t K, const int8_t* exp_plane);

@@ -229,18 +229,34 @@ print(int(wanted), l["gemm_exp_off"], l["gemm_fallback"], l["gemm_in_kernel"], l
     assert "fallback!" in r.stderr
 
 
-@pytest.mark.gpu
-def test_q6k_gemm_scale_range():
-    """Sub-block scales up to +-56 stay exact in the fp16 B tile (both
-    variants, against the oracle); a larger scale is reported by
-    qmm_sync_check instead of yielding a wrong Y. The matvec, which applies
-    the scales in fp32, takes the large scale exactly."""
-    M, N, K = 40, 136, 512
-    W = synth.q6k_matrix(71, N, K)
-    X = synth.normal_bf16(72, (M, K))
+def full_range_scales(W, N, K, rows, seed):
+    """W (N x K q6_K) with the sub-block scales of the given rows drawn on
+    the whole int8 range (-128..127), the rest as drawn"""
     W = W.copy()
-    W.reshape(-1, 210)[::7, 192 + 3] = np.uint8(56)               # +56 on some blocks
-    W.reshape(-1, 210)[1::7, 192 + 9] = np.uint8(256 - 56)        # -56 on others
+    blocks = W.reshape(N, K // 256, 210)
+    rng = np.random.default_rng(seed)
+    rows = np.asarray(rows)
+    blocks[rows, :, 192:208] = rng.integers(0, 256, (len(rows), K // 256, 16)).astype(np.uint8)
+    return W
+
+
+@pytest.mark.parametrize("M,N,K,rows", [
+    (40, 136, 512, "all"),           # every tile two passes
+    (200, 264, 1024, "tile1"),       # only the second 128-row weight tile holds large scales
+    (40, 136, 4096, "all"),          # K split over CTAs, each split two passes
+])
+def test_q6k_gemm_full_int8_scales(M, N, K, rows):
+    """Sub-block scales anywhere in -128..127 (a tile holding one beyond 56
+    runs its K range a second time for the rest of each scale): both
+    variants bitwise equal, within the bound against the oracle, and the
+    tiles without large scales unchanged from a matrix where the large ones
+    are absent."""
+    W0 = synth.q6k_matrix(71 + K, N, K)
+    sel = np.arange(N) if rows == "all" else np.arange(128, 256)
+    W = full_range_scales(W0, N, K, sel, 72 + N)
+    sc = W.reshape(-1, 210)[:, 192:208].view(np.int8)
+    assert np.abs(sc.astype(int)).max() > 120
+    X = synth.normal_bf16(73 + M, (M, K))
     Wt = dev(W)
     Y2 = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
     plane = qmm.plane_build(Wt, N, K)
@@ -249,25 +265,51 @@ def test_q6k_gemm_scale_range():
     assert np.array_equal(Y1.view(np.int32), Y2.view(np.int32))
     xq, s = oracle.quantize_q8(X)
     ref, absum = oracle.gemv_q8(qmm.Q6_K, W, xq, s, N, K)
-    assert_within(Y2, ref, absum, "q6_K GEMM, scales +-56")
+    assert_within(Y2, ref, absum, f"q6_K GEMM, int8 scales, {M}x{N}x{K}")
+    if rows != "all":
+        # weight tiles 0 and 2 hold the same rows as in W0 and run one pass
+        Y0 = run_gemm(qmm.Q6_K, W0, X, N, K)
+        keep = np.r_[0:128, 256:N]
+        assert np.array_equal(Y0[:, keep].view(np.int32), Y2[:, keep].view(np.int32))
 
-    Wbig = W.copy()
-    Wbig.reshape(-1, 210)[5, 192 + 2] = np.uint8(100)
-    Wb = dev(Wbig)
-    Y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    qmm.gemm(qmm.Q6_K, Wb, x_tensor(X), Y, M, N, K, None)
-    torch.cuda.synchronize()
-    with pytest.raises(qmm.QmmError) as ei:
-        qmm.sync_check()
-    assert ei.value.code == qmm.EUNSUPPORTED
-    qmm.sync_check()  # the error word was cleared by the report
 
-    x1 = synth.normal_bf16(73, (2, K))
-    y = torch.empty((2, N), dtype=torch.float32, device="cuda")
-    qmm.gemv(qmm.Q6_K, Wb, x_tensor(x1), y, N, K)
+@pytest.mark.parametrize("K", [256, 512])
+def test_q6k_gemm_full_int8_scales_integer_exact(K):
+    """d = 1, scales on -128..127, codes 30..34 (q - 32 in -2..2), integer
+    activations with amax 127 per block (activation scale 1): every pass's
+    block partials and the whole sum are integers below 2^24, so Y is the
+    exact integer product, bitwise, in both variants"""
+    M, N = 40, 136
+    rng = np.random.default_rng(K)
+    codes = rng.integers(30, 35, (N, K))
+    scales = rng.integers(-128, 128, (N, K // 16))
+    scales[:, 0] = -128
+    scales[:, 1] = 127
+    W = pack.pack_q6k_matrix(codes, scales, np.full((N, K // 256), pack.f16_bits(1.0)))
+    wint = np.repeat(scales, 16, axis=1) * (codes - 32)
+    xi, X = int_acts(M, K, rng)
+    exact = (xi @ wint.T).astype(np.float64)
+    assert np.abs(exact).max() < 2 ** 24
+    Wt = dev(W)
+    Y2 = run_gemm(qmm.Q6_K, W, X, N, K, Wt=Wt)
+    assert np.array_equal(Y2.astype(np.float64), exact)
+    plane = qmm.plane_build(Wt, N, K)
+    Y1 = run_gemm(qmm.Q6_K, W, X, N, K, plane=plane, Wt=Wt)
+    qmm.plane_release(Wt)
+    assert np.array_equal(Y1.astype(np.float64), exact)
+
+
+def test_q6k_matvec_large_scale():
+    """The matvec applies the scales in fp32: a scale of 100 is exact there."""
+    M, N, K = 2, 136, 512
+    W = synth.q6k_matrix(71, N, K).copy()
+    W.reshape(-1, 210)[5, 192 + 2] = np.uint8(100)
+    x1 = synth.normal_bf16(73, (M, K))
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    qmm.gemv(qmm.Q6_K, dev(W), x_tensor(x1), y, N, K)
     torch.cuda.synchronize()
     qmm.sync_check()
-    ref, absum = oracle.gemv_float(qmm.Q6_K, Wbig, x1, N, K)
+    ref, absum = oracle.gemv_float(qmm.Q6_K, W, x1, N, K)
     assert_within(y.cpu().numpy(), ref, absum, "q6_K matvec, scale 100")
 
 
