@@ -146,6 +146,32 @@ def test_moe_prefill_grouped_tiles_and_empty_experts(fmt):
     assert (np.abs(yg.astype(np.float64) - yr) <= 2 * tight).mean() >= 0.95
 
 
+@pytest.mark.parametrize("layout", ["strided", "ragged"])
+def test_moe_prefill_q6k_full_int8_scales(layout):
+    """q6_K experts whose sub-block scales span the whole int8 range: the
+    prefill GEMM's second K pass (scales beyond 56) in the grouped launch
+    and in the per-expert one, against the oracle"""
+    fmt, E, H, I, T, k = synth.Q6_K, 4, 512, 256, 64, 2
+    wg, wu, wd = experts(fmt, E, H, I, 3950)
+    rng = np.random.default_rng(3951)
+
+    def widen(w):
+        w = w.copy()
+        b = w.reshape(-1, 210)
+        b[:, 192:208] = rng.integers(0, 256, (b.shape[0], 16)).astype(np.uint8)
+        return w
+
+    wg, wu, wd = [widen(w) for w in wg], [widen(w) for w in wu], [widen(w) for w in wd]
+    x = synth.normal_bf16(3952, (T, H))
+    idx, gate = oracle.route_topk_softmax(synth.normal_f32(3953, (T, E)), k)
+    gate32 = gate.astype(np.float32)
+    live = {}
+    y = run(fmt, wg, wu, wd, H, I, idx, gate32, x, layout, live)
+    assert live["moe_prefill_plan"] == (2 if layout == "strided" else 1)
+    ref, tight, loose = oracle.moe_q8(fmt, H, I, wg, wu, wd, idx, gate32.astype(np.float64), x)
+    check(y, ref, tight, loose, f"q6_K int8 scales {layout}")
+
+
 def test_moe_prefill_one_expert_takes_every_token():
     """all tokens on one expert (its GEMMs span several 128-row tiles), the
     other experts unused"""
