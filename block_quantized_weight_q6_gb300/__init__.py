@@ -334,7 +334,10 @@ def wait_probe(limit_us: int, device=None):
 
 def moe_prefill(fmt: int, experts: MoeExperts, idx, gate_w, x, y):
     """The routed expert FFN of `moe` for many tokens, grouped by expert
-    through the prefill GEMM (quantized activations); not graph-capturable."""
+    through the prefill GEMM (quantized activations); not graph-capturable.
+    Experts whose matrices lie at one stride per projection (e.g. the rows
+    of one [E, bytes] tensor each) run one grouped GEMM launch per
+    projection; any other table runs one per expert."""
     code = fmt | _act_bits(x)
     _prepare(x.device, lib.qmm_moe_prefill_workspace_bytes(code, C.byref(experts)))
     with _torch().cuda.device(x.device):

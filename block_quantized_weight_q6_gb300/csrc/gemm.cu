@@ -45,7 +45,7 @@
 //               warp cw converts the rows 8 g + cw (the plane variant:
 //               g + 16 cw)
 //   warps 12-27 epilogue: tcgen05.ld of the accumulators, scaling, output
-//   warp 3      idle
+//   warp 3      idle (it only joins the barrier at the end of each K pass)
 // Registers are moved between warpgroups (setmaxnreg): the producers' and
 // the MMA's warpgroup gives up most of its share to the epilogue's.
 // Handing work between warps through an mbarrier costs a few hundred cycles
